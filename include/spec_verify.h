@@ -1,0 +1,236 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify.so, the batched verify step of
+ * speculative decoding on one GB300 (sm_103a).
+ *
+ * The operation (sources: page title, section):
+ *   "Speculative decoding" (mhtirogla.ai), How it works, steps 2-5: the target
+ *   returns p_1..p_{gamma+1} over the whole vocabulary; for i = 1..gamma accept
+ *   x_i if u < p_i(x_i)/q_i(x_i); at the first rejection draw one token from
+ *   norm(max(0, p_i - q_i)) and stop; if all gamma are accepted draw a bonus
+ *   token from p_{gamma+1}; roll back the KV entries of the rejected drafts.
+ *   Its "Code" section states the result: the accepted tokens plus exactly one
+ *   corrected or bonus token. Greedy decoding reduces to "accept while the
+ *   draft token equals the target's argmax" (same page, How it works; and
+ *   "Speculative Decoding" (tokentrails.org), One round).
+ *
+ * Conventions for every entry point:
+ *   - Pointers named *device* point to device memory owned by the caller; the
+ *     library never frees or retains them after the call returns.
+ *   - Every call is asynchronous on the given stream (NULL = legacy default
+ *     stream) and never synchronises the host with the device.
+ *   - The library allocates no device memory. Scratch space is the caller's
+ *     workspace (see spec_verify_workspace_size / spec_workspace_init).
+ *   - Host-detectable errors (NULL pointer, bad size, misaligned pointer, short
+ *     workspace) return a non-zero spec_status_t synchronously and launch
+ *     nothing. A failed launch returns SPEC_ERR_CUDA.
+ *   - Data-dependent errors are reported per sequence in seq_status (one of
+ *     SPEC_SEQ_*), never by a device trap or assert. An errored sequence gets
+ *     accepted = 0, all of its token slots = -1 (not written for
+ *     SPEC_SEQ_BAD_LAYOUT), and its KV length unchanged.
+ *   - Two calls that share a workspace must not overlap on the device.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define SPEC_API __attribute__((visibility("default")))
+#else
+#define SPEC_API
+#endif
+
+/* Same type as cudaStream_t; declared here so plain C callers need no CUDA header. */
+typedef struct CUstream_st* spec_stream_t;
+
+#define SPEC_ABI_VERSION 1
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1, /* NULL where required, size out of range, bad enum */
+    SPEC_ERR_ALIGNMENT = 2,   /* a pointer not aligned to its element type */
+    SPEC_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned (256 B) or too small */
+    SPEC_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+    SPEC_ERR_UNSUPPORTED = 5  /* a combination this build does not implement */
+} spec_status_t;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype_t;
+
+/* Per-sequence status words written to seq_status[b]. Checked in this order. */
+enum {
+    SPEC_SEQ_OK = 0,
+    SPEC_SEQ_BAD_TOKEN = 1,  /* a draft token outside [0, V) */
+    SPEC_SEQ_BAD_KV = 2,     /* kv_lens_in[b] < gamma_b */
+    SPEC_SEQ_BAD_ROW = 3,    /* a row the decision needed has a NaN, +inf, no finite
+                                logit, or (probs mode) a sum that is not > 0 */
+    SPEC_SEQ_BAD_LAYOUT = 4, /* offsets of sequence b inconsistent or out of range */
+    SPEC_SEQ_BAD_TEMP = 5    /* temperature of sequence b not finite and > 0 */
+};
+/* Precedence when several apply: LAYOUT, TEMP (sampling only), TOKEN, KV, then
+ * ROW for the first bad row met while scanning positions left to right. */
+
+/*
+ * Arguments of one batched verify call.
+ *
+ * Layout (row-major, V elements per row, rows packed contiguously):
+ *   target_logits [rows_target, V]: sequence b owns rows target_row_off[b] ..
+ *     target_row_off[b] + gamma_b, i.e. gamma_b + 1 rows, the last one being the
+ *     bonus position (the target's distribution after x_gamma).
+ *   draft [rows_draft, V]: sequence b owns rows draft_row_off[b] .. + gamma_b - 1,
+ *     the drafter's logits (draft_is_probs = 0) or probabilities (= 1) at the
+ *     positions where x_1..x_gamma were drawn.
+ *   draft_tokens [rows_draft]: x_i of sequence b at draft_row_off[b] + i.
+ *   out_tokens [rows_target]: slot target_row_off[b] + k, k = 0..gamma_b; slots
+ *     0..accepted-1 hold the accepted drafts, slot `accepted` the corrected or
+ *     bonus token, the rest -1.
+ * With both offset pointers NULL every gamma_b = gamma_max and the offsets are
+ * b*(gamma_max+1) and b*gamma_max. gamma_b is draft_row_off[b+1] -
+ * draft_row_off[b] and must satisfy target_row_off[b+1] - target_row_off[b] ==
+ * gamma_b + 1 and 0 <= gamma_b <= gamma_max (else SPEC_SEQ_BAD_LAYOUT). The
+ * offsets must be non-decreasing from 0 to rows_target / rows_draft: the work
+ * split relies on it, and a call that breaks it leaves undefined tokens
+ * (but stays inside the buffers) and needs spec_workspace_init again.
+ *
+ * Temperature: both p and q are softmax(logits / T_b) with the same T_b
+ * ("Speculative decoding" (mhtirogla.ai), Implementation notes: both models'
+ * logits go through the same processing). A probabilities draft is used after
+ * dividing each row by its own sum.
+ *
+ * Uniforms: with uniforms == NULL each draw comes from Philox4x32-10 (Salmon et
+ * al., SC'11) keyed by seed, counter (position i, seq_offset + b, round lo 32,
+ * round hi 32); word 0 gives u_acc, word 1 u_smp, each (w >> 8) * 2^-24, the
+ * 24-bit uniforms of the page's Code section. Position i = 0..gamma_b - 1 is
+ * draft x_{i+1}; i = gamma_b is the bonus position. With uniforms != NULL,
+ * uniforms[2 * (target_row_off[b] + i) + {0, 1}] = (u_acc, u_smp) in [0, 1).
+ * seq_offset lets a shard of a larger batch reproduce the whole batch's draws.
+ */
+typedef struct {
+    uint32_t struct_size; /* sizeof(spec_verify_args_t), for ABI checks */
+    int32_t batch;        /* B >= 1 */
+    int32_t vocab;        /* V >= 1 */
+    int32_t gamma_max;    /* >= 0 */
+    int64_t rows_target;  /* sum_b (gamma_b + 1) */
+    int64_t rows_draft;   /* sum_b gamma_b */
+
+    const int64_t* target_row_off; /* device [B+1] or NULL */
+    const int64_t* draft_row_off;  /* device [B+1] or NULL (both or neither) */
+
+    const void* target_logits; /* device [rows_target, V] */
+    int32_t target_dtype;      /* spec_dtype_t */
+    const void* draft;         /* device [rows_draft, V]; unused by greedy */
+    int32_t draft_dtype;       /* spec_dtype_t */
+    int32_t draft_is_probs;    /* 0: logits, 1: probabilities */
+    const int32_t* draft_tokens; /* device [rows_draft] */
+
+    const float* temperatures; /* device [B] or NULL; unused by greedy */
+    float temperature;         /* used when temperatures == NULL; > 0 */
+
+    uint64_t seed;       /* Philox key */
+    uint64_t round;      /* Philox counter words 2-3 */
+    uint32_t seq_offset; /* added to b in the Philox counter */
+    const float* uniforms; /* device [rows_target, 2] or NULL */
+
+    const int32_t* kv_lens_in; /* device [B] or NULL: target KV length incl. the gamma_b drafts */
+    int32_t* kv_lens_out;      /* device [B] or NULL: kv - (gamma_b - accepted); may alias kv_lens_in */
+    int32_t block_size;        /* > 0: also write ceil(kv_out / block_size) to out_num_blocks */
+    int32_t* out_num_blocks;   /* device [B] or NULL */
+
+    int32_t* out_tokens;   /* device [rows_target], required */
+    int32_t* out_accepted; /* device [B], required */
+    int32_t* seq_status;   /* device [B] or NULL */
+
+    void* workspace;        /* device, 256-byte aligned, caller-owned */
+    size_t workspace_bytes; /* >= spec_verify_workspace_size(this, mode) */
+} spec_verify_args_t;
+
+/* ABI version of the loaded library (SPEC_ABI_VERSION at build time). */
+SPEC_API int32_t spec_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+SPEC_API const char* spec_status_string(spec_status_t status);
+
+/* Workspace bytes a call with these arguments needs (greedy != 0 for
+ * spec_verify_greedy). Reads only the host fields batch, vocab, gamma_max,
+ * rows_target, rows_draft; pure host arithmetic, no CUDA call. Returns 0 if
+ * those fields are out of range. */
+SPEC_API size_t spec_verify_workspace_size(const spec_verify_args_t* args, int32_t greedy);
+
+/* Zero the workspace's arrival counters (a stream-ordered memset of its
+ * header). Call once after allocating a workspace, before its first use; the
+ * kernels reset the counters themselves afterwards. */
+SPEC_API spec_status_t spec_workspace_init(void* workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/* Sampling verify ("Speculative decoding" (mhtirogla.ai), How it works steps
+ * 2-5 and Code; "Speculative decoding" (inference.tusharamrit.in), modified
+ * rejection sampling). For each sequence: p_i = softmax(target row i / T_b),
+ * q_i likewise for the draft row (or its normalised probabilities); accept x_i
+ * while u_acc_i * q_i(x_i) < p_i(x_i); at the first rejection i emit the first
+ * j with sum_{k<=j} max(0, p_i - q_i)_k > u_smp_i * Z, Z = sum max(0, p_i - q_i)
+ * (if Z == 0, the same rule on p_i); if all gamma_b are accepted emit the bonus
+ * from p_{gamma_b+1} by the same rule with u_smp at position gamma_b. Writes
+ * out_tokens, out_accepted, kv_lens_out, out_num_blocks, seq_status. */
+SPEC_API spec_status_t spec_verify_sample(const spec_verify_args_t* args, spec_stream_t stream);
+
+/* Greedy verify ("Speculative decoding" (mhtirogla.ai), How it works;
+ * "Speculative Decoding" (tokentrails.org), One round and Code): g_i = first
+ * index of the largest raw target logit of row i (NaN read as -inf, -0 == +0);
+ * accepted = number of leading i with x_i == g_i; emits x_1..x_accepted then
+ * g_{accepted+1}. Ignores draft, draft_dtype, draft_is_probs, temperatures,
+ * temperature, seed, round, seq_offset and uniforms. */
+SPEC_API spec_status_t spec_verify_greedy(const spec_verify_args_t* args, spec_stream_t stream);
+
+/* KV-length rollback alone, e.g. for the draft model's cache ("Speculative
+ * decoding" (mhtirogla.ai), How it works step 5: truncate the length in both
+ * models; Implementation notes: paged KV makes this a length truncate).
+ * kv_out[b] = kv_in[b] - (gamma_b - accepted[b]) with gamma_b = gammas[b] (or
+ * gamma_max if gammas == NULL); out_num_blocks[b] = ceil(kv_out[b] / block_size)
+ * if block_size > 0 and out_num_blocks != NULL. A sequence with accepted outside
+ * [0, gamma_b] gets SPEC_SEQ_BAD_LAYOUT, one with kv_in < gamma_b SPEC_SEQ_BAD_KV;
+ * both keep kv_out = kv_in. All arrays are device [batch]; kv_out may alias
+ * kv_in; gammas, out_num_blocks, seq_status may be NULL. */
+SPEC_API spec_status_t spec_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,
+                                        const int32_t* gammas, int32_t gamma_max, int32_t batch,
+                                        int32_t block_size, int32_t* out_num_blocks, int32_t* seq_status,
+                                        spec_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Test hooks. Same conventions; they expose intermediate values of the last
+ * spec_verify_sample / spec_verify_greedy call made with the same arguments
+ * and workspace (stream-ordered after it).
+ * ------------------------------------------------------------------------- */
+
+/* The uniforms the sampling path draws: out[(b * npos + i) * 2 + {0,1}] =
+ * (u_acc, u_smp) of sequence seq_offset + b at position i, i < npos.
+ * out is device [batch * npos * 2]. */
+SPEC_API spec_status_t spec_debug_philox(uint64_t seed, uint64_t round, uint32_t seq_offset, int32_t batch,
+                                         int32_t npos, float* out, spec_stream_t stream);
+
+/* Merged statistics of every row of the last call, in its row order (target
+ * rows, then draft rows for sampling). Sampling: out_a[r] = m_r, out_b[r] =
+ * s_r with m_r = max_j(l_j) * log2(e) / T and s_r = sum_j 2^(l_j log2(e) / T -
+ * m_r) (probabilities rows: m_r = 0, s_r = sum_j q_j); greedy: out_a[r] = the
+ * largest logit, out_idx[r] = its first index. Device arrays of
+ * rows_target + rows_draft (greedy: rows_target) entries; any may be NULL. */
+SPEC_API spec_status_t spec_debug_row_stats(const spec_verify_args_t* args, int32_t greedy, float* out_a,
+                                            float* out_b, int32_t* out_idx, spec_stream_t stream);
+
+/* The distributions the last sampling call used at position pos of sequence
+ * seq: out_p[V] = p_pos, out_q[V] = q_pos (zeros at the bonus position),
+ * out_w[V] = the normalised sampling weights (max(0, p - q) / Z, or p_pos at
+ * the bonus position or when Z == 0), out_scalars[4] = (p(x), q(x), Z, 0) with
+ * x the draft token at pos (p(x), q(x) = 0 at the bonus position; Z is the
+ * normaliser the sampler used if it sampled at pos, else the one this hook
+ * computes). Device arrays; any may be NULL. */
+SPEC_API spec_status_t spec_debug_probs(const spec_verify_args_t* args, int32_t seq, int32_t pos, float* out_p,
+                                        float* out_q, float* out_w, float* out_scalars, spec_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

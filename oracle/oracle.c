@@ -1,0 +1,520 @@
+/*
+ * oracle.c -- plain float64 CPU oracle for the speculative-decoding verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference leg of bench.py may load this library. The product
+ * path (libspecverify.so and its Python binding) never calls it, and this
+ * file shares no code, header, table or constant with the CUDA path.
+ *
+ * Every function follows the pages' statement of the method step by step, in
+ * float64, with plain sequential loops in index order. No blocking, fusion or
+ * reordering beyond what the method states. Sources (page title, section):
+ *
+ *   [P1] "Speculative decoding" (mhtirogla.ai, ml-training encyclopaedia
+ *        entry): "How it works" steps 1-5, the "Code" section's verify and
+ *        sample routines (read for what they compute), "Implementation notes".
+ *   [P3] "Speculative decoding: the secretary who types ahead of the boss"
+ *        (blog.lo0.es): "The bare mechanism", step 3.
+ *   [P4] "Speculative decoding" (inference.tusharamrit.in module): modified
+ *        rejection sampling, the residual p'(z) and its normaliser identity.
+ *   [P5] "Speculative Decoding" (tokentrails.org): "One round" and the greedy
+ *        round in its "Code" section.
+ *   Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
+ *        Easy as 1, 2, 3", SC'11, section on the Philox S-box and key schedule.
+ *
+ * Readings where the pages are silent or ambiguous (all listed in the design doc):
+ *   - uniforms come from Philox4x32-10 keyed by the 64-bit seed with counter
+ *     (position, sequence, round lo, round hi); word 0 -> u_acc, word 1 ->
+ *     u_smp, each (w >> 8) * 2^-24, the pages' 24-bit resolution ([P1] Code);
+ *   - accept iff u * q(x) < p(x), strict ([P1] Code, division-free form);
+ *   - inverse CDF: first index whose running sum exceeds u * total, in index
+ *     order ([P1] Code, sample); if rounding leaves none, the last index with
+ *     positive mass (the page returns the last index even if it has no mass);
+ *   - residual normaliser Z == 0 at a rejection: sample from p_i instead;
+ *   - greedy argmax: first index of the maximum raw logit, NaN read as -inf.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_F32 0
+#define ORC_BF16 1
+
+/* per-sequence status words (values mirror the library's documented codes) */
+#define ORC_SEQ_OK 0
+#define ORC_SEQ_BAD_TOKEN 1
+#define ORC_SEQ_BAD_KV 2
+#define ORC_SEQ_BAD_ROW 3
+#define ORC_SEQ_BAD_LAYOUT 4
+#define ORC_SEQ_BAD_TEMP 5
+
+/* ------------------------------------------------------------------ */
+/* Element access: bf16 is the top half of an IEEE binary32, so widening */
+/* the 16 bits to 32 and reading them as float is exact.                 */
+/* ------------------------------------------------------------------ */
+double orc_value(const void* base, int32_t dtype, int64_t idx) {
+    float f;
+    if (dtype == ORC_F32) {
+        memcpy(&f, (const char*)base + 4 * idx, 4);
+    } else {
+        uint16_t h;
+        memcpy(&h, (const char*)base + 2 * idx, 2);
+        uint32_t w = ((uint32_t)h) << 16;
+        memcpy(&f, &w, 4);
+    }
+    return (double)f;
+}
+
+static const void* row_ptr(const void* base, int32_t dtype, int64_t row, int64_t V) {
+    int64_t esz = (dtype == ORC_F32) ? 4 : 2;
+    return (const char*)base + row * V * esz;
+}
+
+/* ------------------------------------------------------------------ */
+/* Philox4x32-10 (SC'11). One round: two 32x32->64 products of counter */
+/* words 0 and 2 with the round multipliers; the new counter is        */
+/* (hi1 ^ c1 ^ k0, lo1, hi0 ^ c3 ^ k1, lo0). The key is bumped by the   */
+/* Weyl constants between rounds.                                       */
+/* ------------------------------------------------------------------ */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int r = 0; r < 10; ++r) {
+        if (r > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        uint64_t prod0 = (uint64_t)0xD2511F53u * (uint64_t)c0;
+        uint64_t prod1 = (uint64_t)0xCD9E8D57u * (uint64_t)c2;
+        uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+        uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+        uint32_t n0 = hi1 ^ c1 ^ k0;
+        uint32_t n2 = hi0 ^ c3 ^ k1;
+        c0 = n0;
+        c1 = lo1;
+        c2 = n2;
+        c3 = lo0;
+    }
+    out[0] = c0;
+    out[1] = c1;
+    out[2] = c2;
+    out[3] = c3;
+}
+
+/* u in [0,1) on the 24-bit grid, from the top 24 bits of a 32-bit word. */
+double orc_u24(uint32_t w) { return (double)(w >> 8) * (1.0 / 16777216.0); }
+
+/* (u_acc, u_smp) for global sequence `seq`, position `pos` of round `round`. */
+void orc_uniform_pair(uint64_t seed, uint64_t round, uint32_t seq, uint32_t pos,
+                      double* u_acc, double* u_smp) {
+    uint32_t ctr[4] = {pos, seq, (uint32_t)(round & 0xffffffffu), (uint32_t)(round >> 32)};
+    uint32_t key[2] = {(uint32_t)(seed & 0xffffffffu), (uint32_t)(seed >> 32)};
+    uint32_t w[4];
+    orc_philox4x32_10(ctr, key, w);
+    *u_acc = orc_u24(w[0]);
+    *u_smp = orc_u24(w[1]);
+}
+
+/* ------------------------------------------------------------------ */
+/* Distributions.                                                      */
+/* ------------------------------------------------------------------ */
+
+/* p = softmax(l / T) over the whole row ([P1] How it works, step 2; the same
+ * temperature on both models, [P1] Implementation notes). Returns a status. */
+int32_t orc_softmax_row(const void* row, int32_t dtype, int64_t V, double T, double* p) {
+    if (!(T > 0.0) || !isfinite(T)) return ORC_SEQ_BAD_TEMP;
+    double m = -INFINITY;
+    int has_nan = 0;
+    for (int64_t j = 0; j < V; ++j) {
+        double x = orc_value(row, dtype, j) / T;
+        if (isnan(x))
+            has_nan = 1;
+        else if (x > m)
+            m = x;
+    }
+    if (has_nan || !isfinite(m)) return ORC_SEQ_BAD_ROW;
+    double s = 0.0;
+    for (int64_t j = 0; j < V; ++j) {
+        p[j] = exp(orc_value(row, dtype, j) / T - m);
+        s += p[j];
+    }
+    if (!(s > 0.0) || !isfinite(s)) return ORC_SEQ_BAD_ROW;
+    for (int64_t j = 0; j < V; ++j) p[j] /= s;
+    return ORC_SEQ_OK;
+}
+
+/* A probability row given directly is used after dividing by its own sum
+ * (the page's sampler tolerates unnormalised input, [P1] Code). */
+int32_t orc_normalize_row(const void* row, int32_t dtype, int64_t V, double* q) {
+    double s = 0.0;
+    int has_nan = 0;
+    for (int64_t j = 0; j < V; ++j) {
+        q[j] = orc_value(row, dtype, j);
+        if (isnan(q[j])) has_nan = 1;
+        s += q[j];
+    }
+    if (has_nan || !(s > 0.0) || !isfinite(s)) return ORC_SEQ_BAD_ROW;
+    for (int64_t j = 0; j < V; ++j) q[j] /= s;
+    return ORC_SEQ_OK;
+}
+
+/* r = max(0, p - q) elementwise; returns Z = sum r ([P1] How it works step 3;
+ * [P4] residual p'(z)). */
+double orc_residual(const double* p, const double* q, int64_t V, double* r) {
+    double Z = 0.0;
+    for (int64_t j = 0; j < V; ++j) {
+        double d = p[j] - q[j];
+        r[j] = d > 0.0 ? d : 0.0;
+        Z += r[j];
+    }
+    return Z;
+}
+
+/* First index whose running sum exceeds u * total, total = sum w in index
+ * order ([P1] Code, sample). Fallback: last index with positive mass. */
+int64_t orc_inverse_cdf(const double* w, int64_t V, double u) {
+    double total = 0.0;
+    for (int64_t j = 0; j < V; ++j) total += w[j];
+    double t = u * total;
+    double c = 0.0;
+    for (int64_t j = 0; j < V; ++j) {
+        c += w[j];
+        if (c > t) return j;
+    }
+    for (int64_t j = V - 1; j >= 0; --j)
+        if (w[j] > 0.0) return j;
+    return -1;
+}
+
+/* Normalised CDF edges (C_{j-1}, C_j) of index j under weights w. */
+void orc_cdf_edges(const double* w, int64_t V, int64_t j, double* lo, double* hi) {
+    double total = 0.0;
+    for (int64_t k = 0; k < V; ++k) total += w[k];
+    double c = 0.0;
+    for (int64_t k = 0; k < j; ++k) c += w[k];
+    *lo = c / total;
+    *hi = (c + w[j]) / total;
+}
+
+/* First index of the largest logit; NaN counts as -inf ([P5] Code, argmax). */
+int64_t orc_argmax_row(const void* row, int32_t dtype, int64_t V) {
+    double best = -INFINITY;
+    int64_t idx = 0;
+    for (int64_t j = 0; j < V; ++j) {
+        double v = orc_value(row, dtype, j);
+        if (isnan(v)) v = -INFINITY;
+        if (v > best) {
+            best = v;
+            idx = j;
+        }
+    }
+    return idx;
+}
+
+/* ------------------------------------------------------------------ */
+/* Batched verify.                                                     */
+/* ------------------------------------------------------------------ */
+typedef struct {
+    int32_t batch, vocab, gamma_max;
+    int64_t rows_target, rows_draft;
+    const int64_t* target_row_off; /* [B+1] or NULL: b*(gamma_max+1) */
+    const int64_t* draft_row_off;  /* [B+1] or NULL: b*gamma_max */
+    const void* target;            /* [rows_target, V] */
+    int32_t target_dtype;
+    const void* draft; /* [rows_draft, V] */
+    int32_t draft_dtype;
+    int32_t draft_is_probs;
+    const int32_t* draft_tokens; /* [rows_draft] */
+    const float* temperatures;   /* [B] or NULL */
+    float temperature;
+    uint64_t seed, round;
+    uint32_t seq_offset;
+    const float* uniforms; /* [rows_target, 2] or NULL */
+    const int32_t* kv_in;  /* [B] or NULL */
+    int32_t block_size;    /* 0: no block count */
+    int32_t* out_tokens;   /* [rows_target] */
+    int32_t* out_accepted; /* [B] */
+    int32_t* kv_out;       /* [B] or NULL */
+    int32_t* out_blocks;   /* [B] or NULL */
+    int32_t* seq_status;   /* [B] or NULL */
+    /* diagnostics, each [B] or NULL */
+    double* diag_acc_margin; /* min over accept tests done of |u_acc - p(x)/q(x)| */
+    double* diag_u_smp;      /* the u used for the final sample */
+    double* diag_cdf_lo;     /* normalised CDF edges of the emitted token */
+    double* diag_cdf_hi;
+    double* diag_z; /* residual normaliser at the rejection, -1 for a bonus */
+} orc_args_t;
+
+typedef struct {
+    const orc_args_t* a;
+    int greedy;
+    int tid, nthreads;
+} orc_job_t;
+
+static int64_t toff(const orc_args_t* a, int64_t b) {
+    return a->target_row_off ? a->target_row_off[b] : b * (int64_t)(a->gamma_max + 1);
+}
+static int64_t doff(const orc_args_t* a, int64_t b) {
+    return a->draft_row_off ? a->draft_row_off[b] : b * (int64_t)a->gamma_max;
+}
+
+/* Checks that do not depend on the logits, in a fixed order: layout,
+ * temperature (sampling only), draft tokens, KV length. */
+static int32_t precheck(const orc_args_t* a, int64_t b, int greedy, int64_t* g_out, double* T_out) {
+    int64_t t0 = toff(a, b), t1 = toff(a, b + 1), d0 = doff(a, b), d1 = doff(a, b + 1);
+    int64_t g = d1 - d0;
+    *g_out = g;
+    if (g < 0 || g > a->gamma_max || t1 - t0 != g + 1 || t0 < 0 || t1 > a->rows_target ||
+        d0 < 0 || d1 > a->rows_draft)
+        return ORC_SEQ_BAD_LAYOUT;
+    double T = a->temperatures ? (double)a->temperatures[b] : (double)a->temperature;
+    *T_out = T;
+    if (!greedy && (!(T > 0.0) || !isfinite(T))) return ORC_SEQ_BAD_TEMP;
+    for (int64_t i = 0; i < g; ++i) {
+        int32_t x = a->draft_tokens[d0 + i];
+        if (x < 0 || x >= a->vocab) return ORC_SEQ_BAD_TOKEN;
+    }
+    if (a->kv_in && a->kv_in[b] < g) return ORC_SEQ_BAD_KV;
+    return ORC_SEQ_OK;
+}
+
+static void write_error(const orc_args_t* a, int64_t b, int32_t st) {
+    a->out_accepted[b] = 0;
+    if (st != ORC_SEQ_BAD_LAYOUT) {
+        for (int64_t k = toff(a, b); k < toff(a, b + 1); ++k) a->out_tokens[k] = -1;
+    }
+    if (a->kv_out) a->kv_out[b] = a->kv_in ? a->kv_in[b] : 0;
+    if (a->out_blocks) {
+        int32_t kv = a->kv_in ? a->kv_in[b] : 0;
+        a->out_blocks[b] = a->block_size > 0 ? (kv + a->block_size - 1) / a->block_size : 0;
+    }
+    if (a->seq_status) a->seq_status[b] = st;
+}
+
+static void write_result(const orc_args_t* a, int64_t b, int64_t g, int64_t acc) {
+    a->out_accepted[b] = (int32_t)acc;
+    if (a->kv_out || a->out_blocks) {
+        /* drop the KV entries of the rejected drafts ([P1] How it works step 5) */
+        int32_t kv = a->kv_in ? a->kv_in[b] : 0;
+        int32_t kv2 = a->kv_in ? kv - (int32_t)(g - acc) : 0;
+        if (a->kv_out) a->kv_out[b] = kv2;
+        if (a->out_blocks)
+            a->out_blocks[b] = a->block_size > 0 ? (kv2 + a->block_size - 1) / a->block_size : 0;
+    }
+    if (a->seq_status) a->seq_status[b] = ORC_SEQ_OK;
+}
+
+static void uniforms_for(const orc_args_t* a, int64_t b, int64_t i, double* ua, double* us) {
+    if (a->uniforms) {
+        int64_t row = toff(a, b) + i;
+        *ua = (double)a->uniforms[2 * row];
+        *us = (double)a->uniforms[2 * row + 1];
+    } else {
+        orc_uniform_pair(a->seed, a->round, (uint32_t)(a->seq_offset + b), (uint32_t)i, ua, us);
+    }
+}
+
+static int32_t draft_dist(const orc_args_t* a, int64_t drow, double T, double* q) {
+    const void* rp = row_ptr(a->draft, a->draft_dtype, drow, a->vocab);
+    if (a->draft_is_probs) return orc_normalize_row(rp, a->draft_dtype, a->vocab, q);
+    return orc_softmax_row(rp, a->draft_dtype, a->vocab, T, q);
+}
+
+/* One sequence of the sampling verify ([P1] How it works steps 3-5;
+ * [P3] The bare mechanism step 3; [P4] accept/residual rule). */
+static void verify_sample_one(const orc_args_t* a, int64_t b, double* p, double* q, double* r) {
+    int64_t g;
+    double T;
+    int32_t st = precheck(a, b, 0, &g, &T);
+    if (st) {
+        write_error(a, b, st);
+        return;
+    }
+    const int64_t V = a->vocab, t0 = toff(a, b), d0 = doff(a, b);
+    double margin = INFINITY;
+    for (int64_t i = 0; i < g; ++i) {
+        st = orc_softmax_row(row_ptr(a->target, a->target_dtype, t0 + i, V), a->target_dtype, V, T, p);
+        if (st) { write_error(a, b, st); return; }
+        st = draft_dist(a, d0 + i, T, q);
+        if (st) { write_error(a, b, st); return; }
+        int32_t x = a->draft_tokens[d0 + i];
+        double ua, us;
+        uniforms_for(a, b, i, &ua, &us);
+        if (q[x] > 0.0) {
+            double dm = fabs(ua - p[x] / q[x]);
+            if (dm < margin) margin = dm;
+        }
+        if (ua * q[x] < p[x]) { /* accept x_i: u < p/q without dividing */
+            a->out_tokens[t0 + i] = x;
+            continue;
+        }
+        /* first rejection: draw from norm(max(0, p - q)) and stop */
+        double Z = orc_residual(p, q, V, r);
+        const double* w = (Z > 0.0) ? r : p;
+        int64_t tok = orc_inverse_cdf(w, V, us);
+        a->out_tokens[t0 + i] = (int32_t)tok;
+        for (int64_t k = i + 1; k <= g; ++k) a->out_tokens[t0 + k] = -1;
+        if (a->diag_acc_margin) a->diag_acc_margin[b] = margin;
+        if (a->diag_u_smp) a->diag_u_smp[b] = us;
+        if (a->diag_z) a->diag_z[b] = Z;
+        if (a->diag_cdf_lo && a->diag_cdf_hi) orc_cdf_edges(w, V, tok, &a->diag_cdf_lo[b], &a->diag_cdf_hi[b]);
+        write_result(a, b, g, i);
+        return;
+    }
+    /* all gamma accepted: bonus token from p_{gamma+1} ([P1] step 4) */
+    st = orc_softmax_row(row_ptr(a->target, a->target_dtype, t0 + g, V), a->target_dtype, V, T, p);
+    if (st) { write_error(a, b, st); return; }
+    double ua, us;
+    uniforms_for(a, b, g, &ua, &us);
+    int64_t tok = orc_inverse_cdf(p, V, us);
+    a->out_tokens[t0 + g] = (int32_t)tok;
+    if (a->diag_acc_margin) a->diag_acc_margin[b] = margin;
+    if (a->diag_u_smp) a->diag_u_smp[b] = us;
+    if (a->diag_z) a->diag_z[b] = -1.0;
+    if (a->diag_cdf_lo && a->diag_cdf_hi) orc_cdf_edges(p, V, tok, &a->diag_cdf_lo[b], &a->diag_cdf_hi[b]);
+    write_result(a, b, g, g);
+}
+
+/* One sequence of the greedy verify: accept while the draft token equals the
+ * target's argmax, then append the target's own pick ([P1] How it works,
+ * greedy remark; [P5] One round and its greedy Code). */
+static void verify_greedy_one(const orc_args_t* a, int64_t b) {
+    int64_t g;
+    double T;
+    int32_t st = precheck(a, b, 1, &g, &T);
+    if (st) {
+        write_error(a, b, st);
+        return;
+    }
+    const int64_t V = a->vocab, t0 = toff(a, b), d0 = doff(a, b);
+    int64_t n = 0;
+    for (;;) {
+        int64_t pick = orc_argmax_row(row_ptr(a->target, a->target_dtype, t0 + n, V), a->target_dtype, V);
+        a->out_tokens[t0 + n] = (int32_t)pick;
+        if (n < g && a->draft_tokens[d0 + n] == pick) {
+            ++n;
+            continue;
+        }
+        break;
+    }
+    for (int64_t k = n + 1; k <= g; ++k) a->out_tokens[t0 + k] = -1;
+    write_result(a, b, g, n);
+}
+
+static void* worker(void* arg) {
+    const orc_job_t* job = (const orc_job_t*)arg;
+    const orc_args_t* a = job->a;
+    double *p = NULL, *q = NULL, *r = NULL;
+    if (!job->greedy) {
+        p = (double*)malloc(sizeof(double) * (size_t)a->vocab);
+        q = (double*)malloc(sizeof(double) * (size_t)a->vocab);
+        r = (double*)malloc(sizeof(double) * (size_t)a->vocab);
+    }
+    for (int64_t b = job->tid; b < a->batch; b += job->nthreads) {
+        if (job->greedy)
+            verify_greedy_one(a, b);
+        else
+            verify_sample_one(a, b, p, q, r);
+    }
+    free(p);
+    free(q);
+    free(r);
+    return NULL;
+}
+
+static int run(const orc_args_t* a, int greedy, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > a->batch) nthreads = a->batch > 0 ? a->batch : 1;
+    pthread_t th[256];
+    orc_job_t jobs[256];
+    if (nthreads > 256) nthreads = 256;
+    for (int t = 0; t < nthreads; ++t) {
+        jobs[t].a = a;
+        jobs[t].greedy = greedy;
+        jobs[t].tid = t;
+        jobs[t].nthreads = nthreads;
+    }
+    if (nthreads == 1) {
+        worker(&jobs[0]);
+        return 0;
+    }
+    for (int t = 0; t < nthreads; ++t) pthread_create(&th[t], NULL, worker, &jobs[t]);
+    for (int t = 0; t < nthreads; ++t) pthread_join(th[t], NULL);
+    return 0;
+}
+
+int orc_verify_sample(const orc_args_t* a, int32_t nthreads) { return run(a, 0, nthreads); }
+int orc_verify_greedy(const orc_args_t* a, int32_t nthreads) { return run(a, 1, nthreads); }
+
+/* Length truncate by the rejected-draft count ([P1] How it works step 5,
+ * Implementation notes on paged KV). */
+void orc_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,
+                     const int32_t* gammas, int32_t gamma_max, int32_t batch, int32_t block_size,
+                     int32_t* out_blocks, int32_t* seq_status) {
+    for (int32_t b = 0; b < batch; ++b) {
+        int32_t g = gammas ? gammas[b] : gamma_max;
+        int32_t acc = accepted[b];
+        int32_t st = ORC_SEQ_OK;
+        int32_t kv = kv_in[b];
+        if (g < 0 || acc < 0 || acc > g)
+            st = ORC_SEQ_BAD_LAYOUT;
+        else if (kv < g)
+            st = ORC_SEQ_BAD_KV;
+        int32_t kv2 = st ? kv : kv - (g - acc);
+        kv_out[b] = kv2;
+        if (out_blocks) out_blocks[b] = block_size > 0 ? (kv2 + block_size - 1) / block_size : 0;
+        if (seq_status) seq_status[b] = st;
+    }
+}
+
+/* ------------------------------------------------------------------ */
+/* Per-sequence views used by the parity tests.                        */
+/* ------------------------------------------------------------------ */
+
+/* p_i(x_i) and q_i(x_i) of sequence b at draft position i. Status return. */
+int32_t orc_accept_terms(const orc_args_t* a, int64_t b, int64_t i, double* p_x, double* q_x) {
+    const int64_t V = a->vocab;
+    double T = a->temperatures ? (double)a->temperatures[b] : (double)a->temperature;
+    double* p = (double*)malloc(sizeof(double) * (size_t)V);
+    double* q = (double*)malloc(sizeof(double) * (size_t)V);
+    int32_t st = orc_softmax_row(row_ptr(a->target, a->target_dtype, toff(a, b) + i, V), a->target_dtype, V, T, p);
+    if (!st) st = draft_dist(a, doff(a, b) + i, T, q);
+    if (!st) {
+        int32_t x = a->draft_tokens[doff(a, b) + i];
+        *p_x = p[x];
+        *q_x = q[x];
+    }
+    free(p);
+    free(q);
+    return st;
+}
+
+/* The rows the method uses at position i of sequence b: p_i, q_i (zeros for
+ * the bonus position) and the sampling weights w (r = max(0, p - q) at a
+ * draft position, p at the bonus position, p again if Z == 0). Returns a
+ * status; *z_out receives Z (or -1 at the bonus position). */
+int32_t orc_position_rows(const orc_args_t* a, int64_t b, int64_t i, double* p, double* q, double* w,
+                          double* z_out) {
+    const int64_t V = a->vocab;
+    double T = a->temperatures ? (double)a->temperatures[b] : (double)a->temperature;
+    int64_t g = doff(a, b + 1) - doff(a, b);
+    int32_t st = orc_softmax_row(row_ptr(a->target, a->target_dtype, toff(a, b) + i, V), a->target_dtype, V, T, p);
+    if (st) return st;
+    if (i >= g) {
+        for (int64_t j = 0; j < V; ++j) {
+            q[j] = 0.0;
+            w[j] = p[j];
+        }
+        *z_out = -1.0;
+        return ORC_SEQ_OK;
+    }
+    st = draft_dist(a, doff(a, b) + i, T, q);
+    if (st) return st;
+    double Z = orc_residual(p, q, V, w);
+    *z_out = Z;
+    if (!(Z > 0.0))
+        for (int64_t j = 0; j < V; ++j) w[j] = p[j];
+    return ORC_SEQ_OK;
+}
