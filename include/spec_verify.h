@@ -111,9 +111,9 @@ enum {
  */
 typedef struct {
     uint32_t struct_size; /* sizeof(spec_verify_args_t), for ABI checks */
-    int32_t batch;        /* B >= 1 */
-    int32_t vocab;        /* V >= 1 */
-    int32_t gamma_max;    /* >= 0 */
+    int32_t batch;        /* 1 <= B <= 65536 */
+    int32_t vocab;        /* 1 <= V <= 8388608 (larger: SPEC_ERR_UNSUPPORTED) */
+    int32_t gamma_max;    /* 0 <= gamma_max <= 64 (larger: SPEC_ERR_UNSUPPORTED) */
     int64_t rows_target;  /* sum_b (gamma_b + 1) */
     int64_t rows_draft;   /* sum_b gamma_b */
 
@@ -228,6 +228,13 @@ SPEC_API spec_status_t spec_debug_row_stats(const spec_verify_args_t* args, int3
  * computes). Device arrays; any may be NULL. */
 SPEC_API spec_status_t spec_debug_probs(const spec_verify_args_t* args, int32_t seq, int32_t pos, float* out_p,
                                         float* out_q, float* out_w, float* out_scalars, spec_stream_t stream);
+
+/* Profiling hook for the calling thread: when both are non-NULL, the next
+ * spec_verify_sample / spec_verify_greedy call made by this thread records
+ * start_event (a cudaEvent_t) on its stream just before the streaming pass and
+ * stop_event just after it, then clears the hook. Lets a caller time the
+ * dominant kernel with its own CUDA events. NULL, NULL clears it. */
+SPEC_API spec_status_t spec_debug_time_next_stats(void* start_event, void* stop_event);
 
 #ifdef __cplusplus
 }

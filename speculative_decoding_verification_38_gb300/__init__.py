@@ -1,0 +1,311 @@
+"""Batched speculative-decoding verify on GB300: Python binding of libspecverify.so.
+
+The binding only marshals torch tensors into the C ABI declared in
+include/spec_verify.h; every step of the verify runs in the library's CUDA
+kernels. There is no CPU fallback: if the shared library is missing or fails
+to load, importing the binding's entry points raises.
+
+Low-level entry points (same names as the C ABI):
+    spec_verify_workspace_size, spec_workspace_init, spec_verify_sample,
+    spec_verify_greedy, spec_kv_rollback, spec_status_string, spec_abi_version,
+    spec_debug_philox, spec_debug_row_stats, spec_debug_probs
+Convenience: VerifyArgs (builds the argument struct from tensors), Workspace.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libspecverify.so")
+
+SPEC_OK = 0
+SPEC_ERR_INVALID_ARG = 1
+SPEC_ERR_ALIGNMENT = 2
+SPEC_ERR_WORKSPACE = 3
+SPEC_ERR_CUDA = 4
+SPEC_ERR_UNSUPPORTED = 5
+SPEC_F32, SPEC_BF16 = 0, 1
+SEQ_OK, SEQ_BAD_TOKEN, SEQ_BAD_KV, SEQ_BAD_ROW, SEQ_BAD_LAYOUT, SEQ_BAD_TEMP = 0, 1, 2, 3, 4, 5
+
+
+class SpecError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {spec_status_string(status)} ({status})")
+
+
+class SpecVerifyArgs(ctypes.Structure):
+    """Mirror of spec_verify_args_t (include/spec_verify.h)."""
+
+    _fields_ = [
+        ("struct_size", ctypes.c_uint32),
+        ("batch", ctypes.c_int32),
+        ("vocab", ctypes.c_int32),
+        ("gamma_max", ctypes.c_int32),
+        ("rows_target", ctypes.c_int64),
+        ("rows_draft", ctypes.c_int64),
+        ("target_row_off", ctypes.c_void_p),
+        ("draft_row_off", ctypes.c_void_p),
+        ("target_logits", ctypes.c_void_p),
+        ("target_dtype", ctypes.c_int32),
+        ("draft", ctypes.c_void_p),
+        ("draft_dtype", ctypes.c_int32),
+        ("draft_is_probs", ctypes.c_int32),
+        ("draft_tokens", ctypes.c_void_p),
+        ("temperatures", ctypes.c_void_p),
+        ("temperature", ctypes.c_float),
+        ("seed", ctypes.c_uint64),
+        ("round", ctypes.c_uint64),
+        ("seq_offset", ctypes.c_uint32),
+        ("uniforms", ctypes.c_void_p),
+        ("kv_lens_in", ctypes.c_void_p),
+        ("kv_lens_out", ctypes.c_void_p),
+        ("block_size", ctypes.c_int32),
+        ("out_num_blocks", ctypes.c_void_p),
+        ("out_tokens", ctypes.c_void_p),
+        ("out_accepted", ctypes.c_void_p),
+        ("seq_status", ctypes.c_void_p),
+        ("workspace", ctypes.c_void_p),
+        ("workspace_bytes", ctypes.c_size_t),
+    ]
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    from . import buildlib as _b
+
+    return _b.build(force=force)
+
+
+def lib():
+    """The loaded libspecverify.so. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: run "
+                                  "`python -c 'import __graft_entry__ as g; g.build()'` first")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, i32, i64, u32, u64, sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32,
+                                         ctypes.c_uint64, ctypes.c_size_t)
+            A = ctypes.POINTER(SpecVerifyArgs)
+            L.spec_abi_version.restype = i32
+            L.spec_abi_version.argtypes = []
+            L.spec_status_string.restype = ctypes.c_char_p
+            L.spec_status_string.argtypes = [ctypes.c_int]
+            L.spec_verify_workspace_size.restype = sz
+            L.spec_verify_workspace_size.argtypes = [A, i32]
+            L.spec_workspace_init.restype = ctypes.c_int
+            L.spec_workspace_init.argtypes = [vp, sz, vp]
+            L.spec_verify_sample.restype = ctypes.c_int
+            L.spec_verify_sample.argtypes = [A, vp]
+            L.spec_verify_greedy.restype = ctypes.c_int
+            L.spec_verify_greedy.argtypes = [A, vp]
+            L.spec_kv_rollback.restype = ctypes.c_int
+            L.spec_kv_rollback.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
+            L.spec_debug_philox.restype = ctypes.c_int
+            L.spec_debug_philox.argtypes = [u64, u64, u32, i32, i32, vp, vp]
+            L.spec_debug_row_stats.restype = ctypes.c_int
+            L.spec_debug_row_stats.argtypes = [A, i32, vp, vp, vp, vp]
+            L.spec_debug_probs.restype = ctypes.c_int
+            L.spec_debug_probs.argtypes = [A, i32, i32, vp, vp, vp, vp, vp]
+            L.spec_debug_time_next_stats.restype = ctypes.c_int
+            L.spec_debug_time_next_stats.argtypes = [vp, vp]
+            if L.spec_abi_version() != 1:
+                raise ImportError("libspecverify.so ABI version mismatch")
+            _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------------ marshalling
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.float32:
+        return SPEC_F32
+    if t.dtype == torch.bfloat16:
+        return SPEC_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t.dtype}")
+
+
+def _check_dev(t, name):
+    if t is not None:
+        if not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+
+
+class VerifyArgs:
+    """Builds spec_verify_args_t from CUDA tensors and keeps them alive.
+
+    target [rows_target, V] and draft [rows_draft, V] are float32 or bfloat16;
+    draft_tokens int32 [rows_draft]; offsets int64 [B+1] (both or neither);
+    temperatures float32 [B]; uniforms float32 [rows_target, 2]; kv int32 [B];
+    outputs int32. ``workspace`` is a Workspace (or a uint8 CUDA tensor).
+    """
+
+    def __init__(self, *, batch, gamma_max, target, draft=None, draft_tokens=None, target_row_off=None,
+                 draft_row_off=None, draft_is_probs=False, temperatures=None, temperature=1.0, seed=0, round=0,
+                 seq_offset=0, uniforms=None, kv_lens_in=None, kv_lens_out=None, block_size=0,
+                 out_num_blocks=None, out_tokens=None, out_accepted=None, seq_status=None, workspace=None):
+        for name, t in [("target", target), ("draft", draft), ("draft_tokens", draft_tokens),
+                        ("target_row_off", target_row_off), ("draft_row_off", draft_row_off),
+                        ("temperatures", temperatures), ("uniforms", uniforms), ("kv_lens_in", kv_lens_in),
+                        ("kv_lens_out", kv_lens_out), ("out_num_blocks", out_num_blocks),
+                        ("out_tokens", out_tokens), ("out_accepted", out_accepted), ("seq_status", seq_status)]:
+            _check_dev(t, name)
+        self.tensors = dict(target=target, draft=draft, draft_tokens=draft_tokens, target_row_off=target_row_off,
+                            draft_row_off=draft_row_off, temperatures=temperatures, uniforms=uniforms,
+                            kv_lens_in=kv_lens_in, kv_lens_out=kv_lens_out, out_num_blocks=out_num_blocks,
+                            out_tokens=out_tokens, out_accepted=out_accepted, seq_status=seq_status)
+        a = SpecVerifyArgs()
+        a.struct_size = ctypes.sizeof(SpecVerifyArgs)
+        a.batch = int(batch)
+        a.vocab = int(target.shape[1])
+        a.gamma_max = int(gamma_max)
+        a.rows_target = int(target.shape[0])
+        a.rows_draft = int(draft_tokens.shape[0]) if draft_tokens is not None else 0
+        a.target_row_off = _ptr(target_row_off)
+        a.draft_row_off = _ptr(draft_row_off)
+        a.target_logits = _ptr(target)
+        a.target_dtype = _dtype_code(target)
+        a.draft = _ptr(draft)
+        a.draft_dtype = _dtype_code(draft) if draft is not None else SPEC_F32
+        a.draft_is_probs = int(bool(draft_is_probs))
+        a.draft_tokens = _ptr(draft_tokens)
+        a.temperatures = _ptr(temperatures)
+        a.temperature = float(temperature)
+        a.seed = int(seed)
+        a.round = int(round)
+        a.seq_offset = int(seq_offset)
+        a.uniforms = _ptr(uniforms)
+        a.kv_lens_in = _ptr(kv_lens_in)
+        a.kv_lens_out = _ptr(kv_lens_out)
+        a.block_size = int(block_size)
+        a.out_num_blocks = _ptr(out_num_blocks)
+        a.out_tokens = _ptr(out_tokens)
+        a.out_accepted = _ptr(out_accepted)
+        a.seq_status = _ptr(seq_status)
+        self.struct = a
+        self.workspace = None
+        if workspace is not None:
+            self.set_workspace(workspace)
+
+    def set_workspace(self, ws):
+        buf = ws.buffer if isinstance(ws, Workspace) else ws
+        self.workspace = ws
+        self.struct.workspace = buf.data_ptr()
+        self.struct.workspace_bytes = buf.numel() * buf.element_size()
+
+    def set_round(self, rnd: int):
+        self.struct.round = int(rnd)
+
+    def set_tokens(self, draft_tokens):
+        _check_dev(draft_tokens, "draft_tokens")
+        self.tensors["draft_tokens"] = draft_tokens
+        self.struct.draft_tokens = _ptr(draft_tokens)
+
+
+class Workspace:
+    """A caller-owned device workspace (uint8 CUDA tensor), initialised once."""
+
+    def __init__(self, nbytes: int, device=None, stream=None):
+        import torch
+
+        nbytes = max(int(nbytes), 1)
+        self.buffer = torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+        check(spec_workspace_init(self.buffer.data_ptr(), nbytes, stream), "spec_workspace_init")
+
+    @classmethod
+    def for_args(cls, args: VerifyArgs, greedy: bool, device=None, stream=None, slack: float = 1.0):
+        n = spec_verify_workspace_size(args, greedy)
+        if n == 0:
+            raise SpecError(SPEC_ERR_INVALID_ARG, "spec_verify_workspace_size")
+        return cls(int(n * slack), device=device, stream=stream)
+
+
+def check(status: int, what: str = "spec call"):
+    if status != SPEC_OK:
+        raise SpecError(status, what)
+    return status
+
+
+# ------------------------------------------------------------- C ABI wrappers
+def spec_abi_version() -> int:
+    return lib().spec_abi_version()
+
+
+def spec_status_string(status: int) -> str:
+    try:
+        return lib().spec_status_string(int(status)).decode()
+    except ImportError:
+        return f"status {status}"
+
+
+def spec_verify_workspace_size(args: VerifyArgs, greedy: bool) -> int:
+    return int(lib().spec_verify_workspace_size(ctypes.byref(args.struct), int(bool(greedy))))
+
+
+def spec_workspace_init(ptr: int, nbytes: int, stream=None) -> int:
+    return lib().spec_workspace_init(ptr, nbytes, _stream(stream))
+
+
+def spec_verify_sample(args: VerifyArgs, stream=None) -> int:
+    return lib().spec_verify_sample(ctypes.byref(args.struct), _stream(stream))
+
+
+def spec_verify_greedy(args: VerifyArgs, stream=None) -> int:
+    return lib().spec_verify_greedy(ctypes.byref(args.struct), _stream(stream))
+
+
+def spec_kv_rollback(kv_in, kv_out, accepted, gammas, gamma_max, block_size=0, out_num_blocks=None,
+                     seq_status=None, stream=None) -> int:
+    for name, t in [("kv_in", kv_in), ("kv_out", kv_out), ("accepted", accepted), ("gammas", gammas),
+                    ("out_num_blocks", out_num_blocks), ("seq_status", seq_status)]:
+        _check_dev(t, name)
+    return lib().spec_kv_rollback(_ptr(kv_in), _ptr(kv_out), _ptr(accepted), _ptr(gammas), int(gamma_max),
+                                  int(kv_in.shape[0]), int(block_size), _ptr(out_num_blocks), _ptr(seq_status),
+                                  _stream(stream))
+
+
+def spec_debug_philox(seed, rnd, seq_offset, batch, npos, out, stream=None) -> int:
+    _check_dev(out, "out")
+    return lib().spec_debug_philox(int(seed), int(rnd), int(seq_offset), int(batch), int(npos), _ptr(out),
+                                   _stream(stream))
+
+
+def spec_debug_row_stats(args: VerifyArgs, greedy, out_a=None, out_b=None, out_idx=None, stream=None) -> int:
+    return lib().spec_debug_row_stats(ctypes.byref(args.struct), int(bool(greedy)), _ptr(out_a), _ptr(out_b),
+                                      _ptr(out_idx), _stream(stream))
+
+
+def spec_debug_probs(args: VerifyArgs, seq, pos, out_p=None, out_q=None, out_w=None, out_scalars=None,
+                     stream=None) -> int:
+    return lib().spec_debug_probs(ctypes.byref(args.struct), int(seq), int(pos), _ptr(out_p), _ptr(out_q),
+                                  _ptr(out_w), _ptr(out_scalars), _stream(stream))
+
+
+def spec_debug_time_next_stats(start_event=None, stop_event=None) -> int:
+    """Arm the hook: the next verify call on this thread records the two torch
+    CUDA events around its streaming pass."""
+    a = None if start_event is None else start_event.cuda_event
+    b = None if stop_event is None else stop_event.cuda_event
+    return lib().spec_debug_time_next_stats(a, b)

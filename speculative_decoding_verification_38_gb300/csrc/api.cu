@@ -1,0 +1,278 @@
+// api.cu -- the extern "C" entry points of libspecverify.so: argument
+// validation, the workspace layout, and the launches. Nothing here computes
+// part of the verify step on the host; every step runs in the kernels.
+#include <mutex>
+
+#include "internal.h"
+#include "spec_verify.h"
+
+using namespace specv;
+
+namespace {
+
+constexpr int kMaxGammaApi = 64;  // finalize keeps per-position state in shared memory
+
+struct DeviceInfo {
+    bool ready = false;
+    int resident_sample = 0;
+    int resident_greedy = 0;
+};
+std::mutex g_mu;
+DeviceInfo g_dev[64];
+
+bool device_info(int& dev, DeviceInfo& out) {
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (dev < 0 || dev >= 64) return false;
+    std::lock_guard<std::mutex> lk(g_mu);
+    DeviceInfo& d = g_dev[dev];
+    if (!d.ready) {
+        d.resident_sample = stats_resident_ctas(dev, 0);
+        d.resident_greedy = stats_resident_ctas(dev, 1);
+        if (d.resident_sample <= 0 || d.resident_greedy <= 0) return false;
+        d.ready = true;
+    }
+    out = d;
+    return true;
+}
+
+inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+thread_local cudaEvent_t t_ev_start = nullptr, t_ev_stop = nullptr;
+
+// Launch the streaming pass, bracketed by the caller's events if the
+// profiling hook is armed (the hook is consumed by this call).
+cudaError_t stats_with_hook(const StatsParams& p, cudaStream_t s) {
+    cudaEvent_t e0 = t_ev_start, e1 = t_ev_stop;
+    t_ev_start = t_ev_stop = nullptr;
+    if (e0 && e1 && cudaEventRecord(e0, s) != cudaSuccess) return cudaErrorUnknown;
+    cudaError_t e = launch_stats(p, s);
+    if (e != cudaSuccess) return e;
+    if (e0 && e1 && cudaEventRecord(e1, s) != cudaSuccess) return cudaErrorUnknown;
+    return cudaSuccess;
+}
+inline size_t esize(int32_t dt) { return dt == SPEC_F32 ? 4 : 2; }
+
+// Host fields only; no CUDA call.
+spec_status_t check_shape(const spec_verify_args_t* a) {
+    if (!a) return SPEC_ERR_INVALID_ARG;
+    if (a->struct_size != sizeof(spec_verify_args_t)) return SPEC_ERR_INVALID_ARG;
+    if (a->batch < 1 || a->batch > kMaxBatch) return SPEC_ERR_INVALID_ARG;
+    if (a->vocab < 1) return SPEC_ERR_INVALID_ARG;
+    if ((int64_t)a->vocab > kMaxVocab) return SPEC_ERR_UNSUPPORTED;
+    if (a->gamma_max < 0) return SPEC_ERR_INVALID_ARG;
+    if (a->gamma_max > kMaxGammaApi) return SPEC_ERR_UNSUPPORTED;
+    if (a->rows_target < a->batch || a->rows_draft < 0) return SPEC_ERR_INVALID_ARG;
+    if ((a->target_row_off == nullptr) != (a->draft_row_off == nullptr)) return SPEC_ERR_INVALID_ARG;
+    if (!a->target_row_off) {
+        if (a->rows_target != (int64_t)a->batch * (a->gamma_max + 1)) return SPEC_ERR_INVALID_ARG;
+        if (a->rows_draft != (int64_t)a->batch * a->gamma_max) return SPEC_ERR_INVALID_ARG;
+    }
+    if (a->rows_target > (int64_t)a->batch * (a->gamma_max + 1)) return SPEC_ERR_INVALID_ARG;
+    if (a->rows_draft > (int64_t)a->batch * a->gamma_max) return SPEC_ERR_INVALID_ARG;
+    return SPEC_OK;
+}
+
+spec_status_t check_call(const spec_verify_args_t* a, int greedy) {
+    spec_status_t st = check_shape(a);
+    if (st) return st;
+    if (a->target_dtype != SPEC_F32 && a->target_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+    if (!a->target_logits || !a->out_tokens || !a->out_accepted) return SPEC_ERR_INVALID_ARG;
+    if (a->rows_draft > 0 && !a->draft_tokens) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(a->target_logits, esize(a->target_dtype))) return SPEC_ERR_ALIGNMENT;
+    if (!greedy) {
+        if (a->draft_dtype != SPEC_F32 && a->draft_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+        if (a->draft_is_probs != 0 && a->draft_is_probs != 1) return SPEC_ERR_INVALID_ARG;
+        if (a->rows_draft > 0 && !a->draft) return SPEC_ERR_INVALID_ARG;
+        if (a->draft && !aligned(a->draft, esize(a->draft_dtype))) return SPEC_ERR_ALIGNMENT;
+        if (!a->temperatures && !(a->temperature > 0.f && a->temperature < 3.0e38f)) return SPEC_ERR_INVALID_ARG;
+        if (a->temperatures && !aligned(a->temperatures, 4)) return SPEC_ERR_ALIGNMENT;
+        if (a->uniforms && !aligned(a->uniforms, 8)) return SPEC_ERR_ALIGNMENT;
+    }
+    if (a->block_size < 0) return SPEC_ERR_INVALID_ARG;
+    if ((a->kv_lens_out || a->out_num_blocks) && !a->kv_lens_in) return SPEC_ERR_INVALID_ARG;
+    if (a->out_num_blocks && a->block_size == 0) return SPEC_ERR_INVALID_ARG;
+    const void* i32s[] = {a->draft_tokens, a->kv_lens_in, a->kv_lens_out, a->out_num_blocks,
+                          a->out_tokens, a->out_accepted, a->seq_status};
+    for (const void* p : i32s)
+        if (p && !aligned(p, 4)) return SPEC_ERR_ALIGNMENT;
+    if (a->target_row_off && (!aligned(a->target_row_off, 8) || !aligned(a->draft_row_off, 8)))
+        return SPEC_ERR_ALIGNMENT;
+    if (!a->workspace || !aligned(a->workspace, 256)) return SPEC_ERR_WORKSPACE;
+    return SPEC_OK;
+}
+
+bool build_params(const spec_verify_args_t* a, int greedy, int grid_cap, StatsParams& p, Layout& L) {
+    L = make_layout(a->batch, a->vocab, a->rows_target, a->rows_draft, greedy, grid_cap);
+    if (a->workspace_bytes < L.total) return false;
+    char* ws = (char*)a->workspace;
+    p.tgt = a->target_logits;
+    p.dft = greedy ? nullptr : a->draft;
+    p.tdt = a->target_dtype;
+    p.ddt = greedy ? SPEC_F32 : a->draft_dtype;
+    p.probs = greedy ? 0 : a->draft_is_probs;
+    p.greedy = greedy;
+    p.V = a->vocab;
+    p.rows_t = a->rows_target;
+    p.rows_d = a->rows_draft;
+    p.N = L.N;
+    p.chunk = L.chunk;
+    p.S = L.S;
+    p.B = a->batch;
+    p.gmax = a->gamma_max;
+    p.grid = L.grid;
+    p.tro = a->target_row_off;
+    p.dro = a->draft_row_off;
+    p.temps = greedy ? nullptr : a->temperatures;
+    p.temperature = greedy ? 1.f : a->temperature;
+    p.tokens = a->draft_tokens;
+    p.seed = a->seed;
+    p.round = a->round;
+    p.seq_offset = a->seq_offset;
+    p.uniforms = greedy ? nullptr : a->uniforms;
+    p.kv_in = a->kv_lens_in;
+    p.kv_out = a->kv_lens_out;
+    p.block_size = a->block_size;
+    p.out_blocks = a->out_num_blocks;
+    p.out_tokens = a->out_tokens;
+    p.out_accepted = a->out_accepted;
+    p.seq_status = a->seq_status;
+    p.counters = (uint32_t*)ws;
+    p.partials = (float2*)(ws + L.off_partials);
+    p.row_stats = (float2*)(ws + L.off_rowstats);
+    p.pq = (float2*)(ws + L.off_pq);
+    p.tasks = (SampleTask*)(ws + L.off_tasks);
+    return true;
+}
+
+spec_status_t prepare(const spec_verify_args_t* a, int greedy, StatsParams& p, Layout& L, int& dev) {
+    spec_status_t st = check_call(a, greedy);
+    if (st) return st;
+    DeviceInfo di;
+    if (!device_info(dev, di)) return SPEC_ERR_CUDA;
+    int cap = greedy ? di.resident_greedy : di.resident_sample;
+    if (cap > kGridCap) cap = kGridCap;
+    if (!build_params(a, greedy, cap, p, L)) return SPEC_ERR_WORKSPACE;
+    return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+SPEC_API int32_t spec_abi_version(void) { return SPEC_ABI_VERSION; }
+
+SPEC_API const char* spec_status_string(spec_status_t s) {
+    switch (s) {
+        case SPEC_OK: return "SPEC_OK";
+        case SPEC_ERR_INVALID_ARG: return "SPEC_ERR_INVALID_ARG";
+        case SPEC_ERR_ALIGNMENT: return "SPEC_ERR_ALIGNMENT";
+        case SPEC_ERR_WORKSPACE: return "SPEC_ERR_WORKSPACE";
+        case SPEC_ERR_CUDA: return "SPEC_ERR_CUDA";
+        case SPEC_ERR_UNSUPPORTED: return "SPEC_ERR_UNSUPPORTED";
+    }
+    return "SPEC_ERR_UNKNOWN";
+}
+
+SPEC_API size_t spec_verify_workspace_size(const spec_verify_args_t* a, int32_t greedy) {
+    if (check_shape(a) != SPEC_OK) return 0;
+    // the smallest slice any launch uses gives the most partial slots
+    Layout L = make_layout(a->batch, a->vocab, a->rows_target, a->rows_draft, greedy ? 1 : 0, kGridCap);
+    return L.total;
+}
+
+SPEC_API spec_status_t spec_workspace_init(void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+    if (!workspace || !aligned(workspace, 256) || workspace_bytes < kHeaderBytes) return SPEC_ERR_WORKSPACE;
+    if (cudaMemsetAsync(workspace, 0, kHeaderBytes, (cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+SPEC_API spec_status_t spec_verify_sample(const spec_verify_args_t* a, spec_stream_t stream) {
+    StatsParams p;
+    Layout L;
+    int dev = 0;
+    spec_status_t st = prepare(a, 0, p, L, dev);
+    if (st) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (stats_with_hook(p, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    SampleParams sp;
+    sp.tgt = p.tgt;
+    sp.dft = p.dft;
+    sp.tdt = p.tdt;
+    sp.ddt = p.ddt;
+    sp.V = p.V;
+    sp.nsplit = sampler_nsplit(dev, p.B, p.V);
+    const int64_t per = (p.V + sp.nsplit - 1) / sp.nsplit;
+    sp.vchunk = (per + kTile - 1) / kTile * kTile;
+    sp.tasks_in = p.tasks;
+    sp.tasks = p.tasks;
+    sp.out_tokens = p.out_tokens;
+    if (launch_sampler(sp, p.B, s, true) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+SPEC_API spec_status_t spec_verify_greedy(const spec_verify_args_t* a, spec_stream_t stream) {
+    StatsParams p;
+    Layout L;
+    int dev = 0;
+    spec_status_t st = prepare(a, 1, p, L, dev);
+    if (st) return st;
+    if (stats_with_hook(p, (cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+SPEC_API spec_status_t spec_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,
+                                        const int32_t* gammas, int32_t gamma_max, int32_t batch,
+                                        int32_t block_size, int32_t* out_num_blocks, int32_t* seq_status,
+                                        spec_stream_t stream) {
+    if (!kv_in || !kv_out || !accepted || batch < 1 || gamma_max < 0 || block_size < 0) return SPEC_ERR_INVALID_ARG;
+    if (out_num_blocks && block_size == 0) return SPEC_ERR_INVALID_ARG;
+    const void* ps[] = {kv_in, kv_out, accepted, gammas, out_num_blocks, seq_status};
+    for (const void* p : ps)
+        if (p && !aligned(p, 4)) return SPEC_ERR_ALIGNMENT;
+    if (launch_kv_rollback(kv_in, kv_out, accepted, gammas, gamma_max, batch, block_size, out_num_blocks,
+                           seq_status, (cudaStream_t)stream) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+SPEC_API spec_status_t spec_debug_philox(uint64_t seed, uint64_t round, uint32_t seq_offset, int32_t batch,
+                                         int32_t npos, float* out, spec_stream_t stream) {
+    if (!out || batch < 1 || npos < 1 || !aligned(out, 4)) return SPEC_ERR_INVALID_ARG;
+    if (launch_debug_philox(seed, round, seq_offset, batch, npos, out, (cudaStream_t)stream) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+SPEC_API spec_status_t spec_debug_row_stats(const spec_verify_args_t* a, int32_t greedy, float* out_a,
+                                            float* out_b, int32_t* out_idx, spec_stream_t stream) {
+    StatsParams p;
+    Layout L;
+    int dev = 0;
+    spec_status_t st = prepare(a, greedy ? 1 : 0, p, L, dev);
+    if (st) return st;
+    if (launch_debug_rowstats(p.row_stats, L.rows_total, greedy ? 1 : 0, out_a, out_b, out_idx,
+                              (cudaStream_t)stream) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+SPEC_API spec_status_t spec_debug_probs(const spec_verify_args_t* a, int32_t seq, int32_t pos, float* out_p,
+                                        float* out_q, float* out_w, float* out_scalars, spec_stream_t stream) {
+    StatsParams p;
+    Layout L;
+    int dev = 0;
+    spec_status_t st = prepare(a, 0, p, L, dev);
+    if (st) return st;
+    if (seq < 0 || seq >= a->batch || pos < 0 || pos > a->gamma_max) return SPEC_ERR_INVALID_ARG;
+    if (launch_debug_probs(p, seq, pos, out_p, out_q, out_w, out_scalars, (cudaStream_t)stream) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+SPEC_API spec_status_t spec_debug_time_next_stats(void* start_event, void* stop_event) {
+    t_ev_start = (cudaEvent_t)start_event;
+    t_ev_stop = (cudaEvent_t)stop_event;
+    return SPEC_OK;
+}
+
+}  // extern "C"

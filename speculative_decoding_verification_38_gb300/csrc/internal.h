@@ -1,0 +1,110 @@
+// internal.h -- kernel parameter blocks, workspace layout and launch entry
+// points shared by the translation units of libspecverify.so. Not installed.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#define SPECV_F32 0
+#define SPECV_BF16 1
+
+namespace specv {
+
+constexpr int kStatsThreads = 512;    // threads per CTA of the streaming pass
+constexpr int kSampThreads = 512;     // threads per CTA of the residual sampler
+constexpr int kTile = 256;            // sampler tile: 32 lanes x 8 contiguous elements
+constexpr int kMaxTilesPerCta = 4096; // sampler smem bound: V <= 8 * 4096 * 256
+constexpr int kMaxCluster = 8;        // portable cluster size
+constexpr int64_t kChunkAlign = 64;   // elements; keeps 16-byte alignment for both dtypes
+constexpr int64_t kMinChunk = 1024;   // smallest slice one CTA streams
+constexpr int kGridCap = 4096;        // most CTAs of one streaming pass
+constexpr int kMaxBatch = 65536;      // arrival counters in the workspace header
+constexpr size_t kHeaderBytes = (size_t)kMaxBatch * 4;
+constexpr int64_t kMaxVocab = (int64_t)kMaxCluster * kMaxTilesPerCta * kTile;
+
+enum TaskMode : int32_t { kTaskNone = 0, kTaskResidual = 1, kTaskBonus = 2 };
+
+// What the finalize step hands to the residual sampler, one per sequence.
+struct __align__(16) SampleTask {
+    int32_t mode;      // TaskMode
+    int32_t probs;     // draft row holds probabilities
+    int64_t trow;      // target row (index into target logits)
+    int64_t drow;      // draft row (residual only)
+    int64_t out_slot;  // index into out_tokens
+    float u;           // u_smp of the sampled position
+    float kt, mt, inv_st;  // target: k = log2e/T, m, 1/s
+    float kd, md, inv_sd;  // draft (logits: same T; probs: kd = md = 0)
+    float z;               // residual normaliser the sampler used (debug)
+    int32_t pad[2];
+};
+static_assert(sizeof(SampleTask) == 80, "task layout");
+
+// Everything one streaming pass (and its finalize tail) needs.
+struct StatsParams {
+    const void* tgt;
+    const void* dft;
+    int32_t tdt, ddt, probs, greedy;
+    int64_t V, rows_t, rows_d, N, chunk;
+    int32_t S;  // partial slots per row
+    int32_t B, gmax, grid;
+    const int64_t* tro;
+    const int64_t* dro;
+    const float* temps;
+    float temperature;
+    const int32_t* tokens;
+    uint64_t seed, round;
+    uint32_t seq_offset;
+    const float* uniforms;
+    const int32_t* kv_in;
+    int32_t* kv_out;
+    int32_t block_size;
+    int32_t* out_blocks;
+    int32_t* out_tokens;
+    int32_t* out_accepted;
+    int32_t* seq_status;
+    // workspace views
+    uint32_t* counters;  // [B] self-resetting arrival counters
+    float2* partials;    // [rows_total * S]
+    float2* row_stats;   // [rows_total] merged per-row statistics
+    float2* pq;          // [rows_d] (p(x), q(x))
+    SampleTask* tasks;   // [B]
+};
+
+struct SampleParams {
+    const void* tgt;
+    const void* dft;
+    int32_t tdt, ddt;
+    int64_t V;
+    int32_t nsplit;   // CTAs per sequence (cluster size)
+    int64_t vchunk;   // elements per CTA, multiple of kTile
+    const SampleTask* tasks_in;
+    SampleTask* tasks;
+    int32_t* out_tokens;
+};
+
+struct Layout {
+    int64_t rows_total, N, chunk;
+    int32_t S, grid;
+    size_t off_partials, off_rowstats, off_pq, off_tasks, total;
+};
+
+// Work split and workspace layout for a given problem. grid_cap bounds the
+// number of streaming CTAs (the launch uses the device's resident capacity).
+Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int greedy, int64_t grid_cap);
+
+cudaError_t launch_stats(const StatsParams& p, cudaStream_t s);
+int stats_resident_ctas(int device, int greedy);  // CTAs that fit at once on the device
+cudaError_t launch_sampler(const SampleParams& p, int32_t B, cudaStream_t s, bool pdl);
+int sampler_nsplit(int device, int64_t B, int64_t V);
+cudaError_t launch_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,
+                               const int32_t* gammas, int32_t gmax, int32_t B, int32_t block_size,
+                               int32_t* out_blocks, int32_t* seq_status, cudaStream_t s);
+cudaError_t launch_debug_philox(uint64_t seed, uint64_t round, uint32_t seq_offset, int32_t B, int32_t npos,
+                                float* out, cudaStream_t s);
+cudaError_t launch_debug_probs(const StatsParams& p, int32_t seq, int32_t pos, float* out_p, float* out_q,
+                               float* out_w, float* out_scalars, cudaStream_t s);
+cudaError_t launch_debug_rowstats(const float2* row_stats, int64_t rows, int greedy, float* out_a, float* out_b,
+                                  int32_t* out_idx, cudaStream_t s);
+
+}  // namespace specv

@@ -1,0 +1,113 @@
+"""Comparison of the CUDA path's outputs with the oracle's, draw by draw.
+
+Rule for the sampling path: tokens, accepted counts and KV lengths must be
+identical, except for a mismatching draw whose uniform lies within BAND of
+the oracle's decision boundary (|u_acc - p(x)/q(x)| at the first differing
+accept test) or of a CDF edge of the emitted token (the oracle's or the
+GPU's, under the oracle's weights). Excused mismatches must stay below
+1e-4 of all draws; unexcused ones must not occur. A draw is one uniform the
+decision consumed: every accept test performed plus the final sample.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+import oracle
+from speculative_decoding_verification_38_gb300 import workloads as wl
+
+BAND = 1e-5
+MAX_MISMATCH_FRACTION = 1e-4
+
+
+def offsets(w):
+    if w.target_row_off is not None:
+        return np.asarray(w.target_row_off), np.asarray(w.draft_row_off)
+    return wl.offsets_for(w.gammas)
+
+
+class Tally:
+    def __init__(self):
+        self.draws = 0
+        self.mismatches = 0
+        self.unexcused = []
+        self.in_band = 0
+        self.rounds = 0
+
+    def merge(self, o):
+        self.draws += o.draws
+        self.mismatches += o.mismatches
+        self.unexcused += o.unexcused
+        self.in_band += o.in_band
+        self.rounds += o.rounds
+
+    def check(self, label=""):
+        assert not self.unexcused, f"{label}: unexcused mismatches {self.unexcused[:10]}"
+        assert self.mismatches <= MAX_MISMATCH_FRACTION * self.draws, (
+            f"{label}: {self.mismatches} excused mismatches in {self.draws} draws")
+
+    def __repr__(self):
+        return (f"Tally(rounds={self.rounds}, draws={self.draws}, mismatches={self.mismatches}, "
+                f"in_band={self.in_band}, unexcused={len(self.unexcused)})")
+
+
+def compare_sample(w, gpu: dict, orc: dict, *, seed: int, rnd: int, tokens, seq_offset: int = 0,
+                   uniforms=None) -> Tally:
+    tro, dro = offsets(w)
+    T = Tally()
+    T.rounds = 1
+    diag = orc["diag"]
+    for b in range(w.batch):
+        so, sg = orc["status"][b], gpu["status"][b]
+        seg = slice(int(tro[b]), int(tro[b + 1]))
+        if so != 0 or sg != 0:
+            if so != sg or gpu["accepted"][b] != orc["accepted"][b] or \
+                    not np.array_equal(gpu["tokens"][seg], orc["tokens"][seg]):
+                T.unexcused.append((b, "status", int(so), int(sg)))
+            continue
+        g = int(dro[b + 1] - dro[b])
+        ao, ag = int(orc["accepted"][b]), int(gpu["accepted"][b])
+        T.draws += (ao + 1 if ao < g else g) + 1
+
+        def u_of(i):
+            if uniforms is not None:
+                r = int(tro[b]) + i
+                return float(uniforms[r, 0]), float(uniforms[r, 1])
+            return oracle.uniform_pair(seed, rnd, seq_offset + b, i)
+
+        band_hit = diag["acc_margin"][b] < BAND or min(abs(diag["u_smp"][b] - diag["cdf_lo"][b]),
+                                                         abs(diag["u_smp"][b] - diag["cdf_hi"][b])) < BAND
+        T.in_band += int(band_hit)
+        same = (ao == ag and np.array_equal(orc["tokens"][seg], gpu["tokens"][seg]))
+        if "kv" in orc and same:
+            same = orc["kv"][b] == gpu["kv"][b]
+            if "blocks" in orc:
+                same = same and orc["blocks"][b] == gpu["blocks"][b]
+        if same:
+            continue
+        T.mismatches += 1
+        ok = False
+        if ao != ag:
+            i = min(ao, ag)
+            st, px, qx = oracle.accept_terms(w, b, i, draft_tokens=tokens)
+            ua, _ = u_of(i)
+            ok = st == 0 and qx > 0 and abs(ua - px / qx) < BAND
+        else:
+            _, us = u_of(ao)
+            ok = min(abs(us - diag["cdf_lo"][b]), abs(us - diag["cdf_hi"][b])) < BAND
+            if not ok:
+                tok_g = int(gpu["tokens"][seg][ao])
+                if 0 <= tok_g < w.vocab:
+                    st, p, q, wts, Z = oracle.position_rows(w, b, ao, draft_tokens=tokens)
+                    lo, hi = oracle.cdf_edges(wts, tok_g)
+                    ok = min(abs(us - lo), abs(us - hi)) < BAND
+            ok = ok and np.array_equal(orc["tokens"][seg][:ao], gpu["tokens"][seg][:ao])
+        if not ok:
+            T.unexcused.append((b, ao, ag, orc["tokens"][seg].tolist(), gpu["tokens"][seg].tolist()))
+    return T
+
+
+def compare_exact(w, gpu: dict, orc: dict):
+    """Greedy / integer outputs: bit-exact."""
+    for k in ("tokens", "accepted", "status", "kv", "blocks"):
+        if k in orc:
+            assert np.array_equal(gpu[k], orc[k]), (k, np.nonzero(gpu[k] != orc[k])[0][:10])
