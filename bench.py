@@ -177,6 +177,9 @@ def run_ours(args):
     clk = ClockSampler(local_rank)
     clk.start()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ev:  # torch creates the CUDA events lazily, on first record
+        a.record()
+        b.record()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     wall0 = time.time()
@@ -223,7 +226,7 @@ def run_ours(args):
     traffic = ncu_traffic_per_launch()
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(copies[0], w, args, sv)
+    e2e = run_e2e(copies[0], w, args, sv) if args.e2e_steps > 0 else None
 
     out = {
         "metric": METRIC, "value": rounds_per_s, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
@@ -246,7 +249,7 @@ def run_ours(args):
         "e2e": e2e,
         "wall_s_timed": wall1 - wall0,
     }
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu_seconds > 0:
         out["cpu_baseline"] = run_cpu_baseline(w, args)
     if rank == 0:
         print(json.dumps(out), flush=True)

@@ -211,21 +211,22 @@ SPEC_API spec_status_t spec_debug_philox(uint64_t seed, uint64_t round, uint32_t
                                          int32_t npos, float* out, spec_stream_t stream);
 
 /* Merged statistics of every row of the last call, in its row order (target
- * rows, then draft rows for sampling). Sampling: out_a[r] = m_r, out_b[r] =
- * s_r with m_r = max_j(l_j) * log2(e) / T and s_r = sum_j 2^(l_j log2(e) / T -
- * m_r) (probabilities rows: m_r = 0, s_r = sum_j q_j); greedy: out_a[r] = the
+ * rows, then draft rows for sampling). Sampling: out_a[r] = m_r = max_j l_j
+ * (the raw logit), out_b[r] = s_r = sum_j 2^(l_j k - fl(m_r k)), k = log2(e)/T
+ * (probabilities rows: m_r = 0, s_r = sum_j q_j); greedy: out_a[r] = the
  * largest logit, out_idx[r] = its first index. Device arrays of
  * rows_target + rows_draft (greedy: rows_target) entries; any may be NULL. */
 SPEC_API spec_status_t spec_debug_row_stats(const spec_verify_args_t* args, int32_t greedy, float* out_a,
                                             float* out_b, int32_t* out_idx, spec_stream_t stream);
 
-/* The distributions the last sampling call used at position pos of sequence
- * seq: out_p[V] = p_pos, out_q[V] = q_pos (zeros at the bonus position),
- * out_w[V] = the normalised sampling weights (max(0, p - q) / Z, or p_pos at
- * the bonus position or when Z == 0), out_scalars[4] = (p(x), q(x), Z, 0) with
- * x the draft token at pos (p(x), q(x) = 0 at the bonus position; Z is the
- * normaliser the sampler used if it sampled at pos, else the one this hook
- * computes). Device arrays; any may be NULL. */
+/* The distributions the sampling path uses at position pos of sequence seq,
+ * recomputed with the sampler's own arithmetic from the row statistics of the
+ * last sampling call: out_p[V] = p_pos, out_q[V] = q_pos (zeros at the bonus
+ * position), out_w[V] = the normalised sampling weights (max(0, p - q) / Z, or
+ * p_pos at the bonus position or when Z == 0), out_scalars[4] = (p(x), q(x),
+ * Z, 0) with x the draft token at pos and p(x), q(x) the values the accept
+ * test used (0 at the bonus position; Z = -1 there). Device arrays; any may be
+ * NULL. */
 SPEC_API spec_status_t spec_debug_probs(const spec_verify_args_t* args, int32_t seq, int32_t pos, float* out_p,
                                         float* out_q, float* out_w, float* out_scalars, spec_stream_t stream);
 

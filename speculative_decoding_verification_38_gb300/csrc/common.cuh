@@ -124,13 +124,15 @@ __device__ __forceinline__ void pdl_wait_primary() { asm volatile("griddepcontro
 
 // ------------------------------------------------------------- softmax state
 // Online max/sum of one row slice in the base-2 domain with 1/T folded in:
-// m = max_j l_j * k, s = sum_j 2^(l_j * k - m), k = log2(e) / T. Merging two
-// states rescales each sum to the larger max. A zero sum contributes nothing
-// (so an all -inf slice never poisons the merge) while a NaN sum propagates.
-__device__ __forceinline__ float2 ms_merge(float2 a, float2 b) {
-    float M = fmaxf(a.x, b.x);
-    float sa = (a.y == 0.f) ? 0.f : a.y * ex2(a.x - M);
-    float sb = (b.y == 0.f) ? 0.f : b.y * ex2(b.x - M);
+// state (m, s) with m = the largest raw logit and s = sum_j 2^(l_j*k - fl(m*k)),
+// k = log2(e) / T. Merging two states rescales each sum to the larger max. A
+// zero sum contributes nothing (so an all -inf slice never poisons the merge)
+// while a NaN sum propagates.
+__device__ __forceinline__ float2 ms_merge(float2 a, float2 b, float k) {
+    const float M = fmaxf(a.x, b.x);
+    const float Ms = __fmul_rn(M, k);
+    const float sa = (a.y == 0.f) ? 0.f : a.y * ex2(__fmul_rn(a.x, k) - Ms);
+    const float sb = (b.y == 0.f) ? 0.f : b.y * ex2(__fmul_rn(b.x, k) - Ms);
     return make_float2(M, sa + sb);
 }
 

@@ -30,13 +30,14 @@ struct __align__(16) SampleTask {
     int32_t mode;      // TaskMode
     int32_t probs;     // draft row holds probabilities
     int64_t trow;      // target row (index into target logits)
-    int64_t drow;      // draft row (residual only)
+    int64_t drow;      // draft row (residual only), else -1
     int64_t out_slot;  // index into out_tokens
     float u;           // u_smp of the sampled position
-    float kt, mt, inv_st;  // target: k = log2e/T, m, 1/s
-    float kd, md, inv_sd;  // draft (logits: same T; probs: kd = md = 0)
-    float z;               // residual normaliser the sampler used (debug)
-    int32_t pad[2];
+    float k_hi, k_lo;  // log2(e) / T as a float pair
+    float mt, md;      // raw maxima of the target / draft row
+    float z_hi, z_lo;  // written by the sampler: the Z it used
+    float st_hi, st_lo, sd_hi, sd_lo;  // written by the sampler: row normalisers
+    int32_t pad;
 };
 static_assert(sizeof(SampleTask) == 80, "task layout");
 

@@ -1,7 +1,7 @@
 // misc.cu -- the standalone KV-length rollback and the test hooks.
 #include <math.h>
 
-#include "common.cuh"
+#include "precise.cuh"
 
 namespace specv {
 
@@ -54,28 +54,32 @@ __global__ void debug_rowstats_kernel(const float2* rs, int64_t rows, int greedy
 
 constexpr int kDbgThreads = 1024;
 
-__device__ float dbg_block_sum(float v, float* red) {
+__device__ df dbg_block_sum_df(df v, df* red) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    for (int o = 16; o > 0; o >>= 1) v = df_add(v, shfl_xor_df(v, o));
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
     __syncthreads();
-    float t = 0.f;
-    if (threadIdx.x == 0)
-        for (int w = 0; w < kDbgThreads / 32; ++w) t += red[w];
-    __syncthreads();
-    if (threadIdx.x == 0) red[0] = t;
-    __syncthreads();
-    t = red[0];
+    df t{0.f, 0.f};
+    for (int w = 0; w < kDbgThreads / 32; ++w) t = df_add(t, red[w]);  // same order in every thread
     __syncthreads();
     return t;
 }
 
-// p_pos, q_pos and the normalised sampling weights of one position, from the
-// row statistics the last sampling call stored (same formulas as the sampler).
+__device__ __forceinline__ df dbg_weight(const char* row, int dt, int64_t j, float lmax, df k, bool probs,
+                                         const Exp2Table& tab) {
+    const float l = ld_elem_rt(row, dt, j);
+    if (probs) return df{(l > -INFINITY) ? l : 0.f, 0.f};
+    return dt == SPECV_F32 ? logit_weight<true>(l, lmax, k, tab) : logit_weight<false>(l, lmax, k, tab);
+}
+
+// p_pos, q_pos and the normalised sampling weights of one position with the
+// sampler's own weight, normaliser and residual arithmetic.
 __global__ void __launch_bounds__(kDbgThreads) debug_probs_kernel(StatsParams p, int32_t seq, int32_t pos,
                                                                   float* out_p, float* out_q, float* out_w,
                                                                   float* out_sc) {
-    __shared__ float red[kDbgThreads / 32];
+    __shared__ df red[kDbgThreads / 32];
+    __shared__ Exp2Table tab;
+    exp2_table_init(tab);
     const int64_t t0 = p.tro ? p.tro[seq] : (int64_t)seq * (p.gmax + 1);
     const int64_t d0 = p.dro ? p.dro[seq] : (int64_t)seq * p.gmax;
     const int64_t d1 = p.dro ? p.dro[seq + 1] : (int64_t)(seq + 1) * p.gmax;
@@ -85,55 +89,53 @@ __global__ void __launch_bounds__(kDbgThreads) debug_probs_kernel(StatsParams p,
             for (int i = 0; i < 4; ++i) out_sc[i] = NAN;
         return;
     }
+    __syncthreads();
     const float T = p.temps ? p.temps[seq] : p.temperature;
-    const float k = kLog2e / T;
+    const df k = k_of_temperature(T);
     const bool draftpos = pos < g;
-    const float2 ts = p.row_stats[t0 + pos];
-    const float2 ds = draftpos ? p.row_stats[p.rows_t + d0 + pos] : make_float2(0.f, 1.f);
+    const float mt = p.row_stats[t0 + pos].x;
+    const float md = draftpos ? p.row_stats[p.rows_t + d0 + pos].x : 0.f;
     const int te = p.tdt == SPECV_F32 ? 4 : 2, de = p.ddt == SPECV_F32 ? 4 : 2;
     const char* trow = (const char*)p.tgt + (t0 + pos) * p.V * te;
     const char* drow = draftpos ? (const char*)p.dft + (d0 + pos) * p.V * de : trow;
-    const float inv_st = 1.0f / ts.y, inv_sd = 1.0f / ds.y;
-    float zpart = 0.f;
+    const bool probs = p.probs != 0;
+    df at{0.f, 0.f}, ad{0.f, 0.f};
     for (int64_t j = threadIdx.x; j < p.V; j += blockDim.x) {
-        const float pv = __fmul_rn(ex2(__fmaf_rn(ld_elem_rt(trow, p.tdt, j), k, -ts.x)), inv_st);
-        float qv = 0.f;
+        acc_add(at, dbg_weight(trow, p.tdt, j, mt, k, false, tab));
+        if (draftpos) acc_add(ad, dbg_weight(drow, p.ddt, j, md, k, probs, tab));
+    }
+    const df St = dbg_block_sum_df(df_norm(at), red);
+    const df Sd = draftpos ? dbg_block_sum_df(df_norm(ad), red) : df{1.f, 0.f};
+    const df It = df_recip(St), Id = df_recip(Sd);
+    df az{0.f, 0.f};
+    for (int64_t j = threadIdx.x; j < p.V; j += blockDim.x) {
+        const df wt = dbg_weight(trow, p.tdt, j, mt, k, false, tab);
+        const df pv = df_mul(wt, It);
+        df qv{0.f, 0.f};
         if (draftpos) {
-            const float l = ld_elem_rt(drow, p.ddt, j);
-            qv = p.probs ? __fmul_rn(l, inv_sd) : __fmul_rn(ex2(__fmaf_rn(l, k, -ds.x)), inv_sd);
+            const df wd = dbg_weight(drow, p.ddt, j, md, k, probs, tab);
+            qv = df_mul(wd, Id);
+            acc_add(az, resid_weight(wt, wd, It, Id));
         }
-        if (out_p) out_p[j] = pv;
-        if (out_q) out_q[j] = qv;
-        zpart += draftpos ? fmaxf(pv - qv, 0.f) : pv;
+        if (out_p) out_p[j] = pv.hi;
+        if (out_q) out_q[j] = qv.hi;
     }
-    const float Z = dbg_block_sum(zpart, red);
-    const bool use_r = draftpos && Z > 0.f;
-    float wsum = use_r ? Z : 1.f;
-    if (!use_r && draftpos) {
-        float s2 = 0.f;
-        for (int64_t j = threadIdx.x; j < p.V; j += blockDim.x)
-            s2 += __fmul_rn(ex2(__fmaf_rn(ld_elem_rt(trow, p.tdt, j), k, -ts.x)), inv_st);
-        wsum = dbg_block_sum(s2, red);
-    }
+    const df Z = draftpos ? dbg_block_sum_df(df_norm(az), red) : df{1.f, 0.f};
+    const bool use_r = draftpos && df_pos(Z);
+    const df Iz = use_r ? df_recip(Z) : df{1.f, 0.f};
     if (out_w) {
         for (int64_t j = threadIdx.x; j < p.V; j += blockDim.x) {
-            const float pv = __fmul_rn(ex2(__fmaf_rn(ld_elem_rt(trow, p.tdt, j), k, -ts.x)), inv_st);
-            float w = pv;
-            if (use_r) {
-                const float l = ld_elem_rt(drow, p.ddt, j);
-                const float qv = p.probs ? __fmul_rn(l, inv_sd) : __fmul_rn(ex2(__fmaf_rn(l, k, -ds.x)), inv_sd);
-                w = fmaxf(pv - qv, 0.f);
-            }
-            out_w[j] = w / wsum;
+            const df wt = dbg_weight(trow, p.tdt, j, mt, k, false, tab);
+            df w = df_mul(wt, It);
+            if (use_r) w = df_mul(resid_weight(wt, dbg_weight(drow, p.ddt, j, md, k, probs, tab), It, Id), Iz);
+            out_w[j] = w.hi;
         }
     }
     if (out_sc && threadIdx.x == 0) {
         const float2 pq = draftpos ? p.pq[d0 + pos] : make_float2(0.f, 0.f);
-        const SampleTask tk = p.tasks[seq];
-        const bool sampled_here = tk.mode != kTaskNone && tk.out_slot == t0 + pos;
         out_sc[0] = pq.x;
         out_sc[1] = pq.y;
-        out_sc[2] = (sampled_here && draftpos) ? tk.z : (draftpos ? Z : -1.f);
+        out_sc[2] = draftpos ? Z.hi : -1.f;
         out_sc[3] = 0.f;
     }
 }

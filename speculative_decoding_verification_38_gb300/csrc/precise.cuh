@@ -1,0 +1,181 @@
+// precise.cuh -- double-float arithmetic and the sampling weights of one row,
+// accurate enough that the GPU's inverse-CDF pick agrees with a float64
+// evaluation except within ~1e-10 of a CDF edge.
+//
+// Why: the sampled token is the first index j whose running weight sum
+// exceeds u * Z. A vocabulary of V tokens puts V CDF edges in [0, 1), so a
+// CDF error of e flips about 2 e V draws; fp32 weights and sums (e ~ 1e-8)
+// would flip ~1e-3 of the draws at V = 128k. Here every weight is
+// w_j = 2^((l_j - l_max) * k), k = log2(e) / T, with
+//   - the exponent (l_j - l_max) * k carried as an unevaluated pair hi + lo
+//     (Dekker's error-free product via FMA),
+//   - "heavy" weights (w_j > 2^-13 of the row maximum) evaluated in
+//     double-float: 2^x = 2^n * 2^(i/64) * e^(r ln 2), |r| <= 1/128, with the
+//     table 2^(i/64) held as float pairs and a degree-4 Taylor polynomial for
+//     e^a - 1 (Tang's table-driven method, ACM TOMS 15(2), 1989),
+//   - light weights from the SFU's 2^x of the high part, corrected to first
+//     order by the low part (their rounding errors average out in the sums),
+//   - all sums, normalisers and prefix sums in double-float (Knuth's TwoSum,
+//     Dekker's Fast2Sum and TwoProduct).
+#pragma once
+
+#include "common.cuh"
+
+namespace specv {
+
+struct df {
+    float hi, lo;
+};
+
+__device__ __forceinline__ df df_make(float h, float l = 0.f) { return df{h, l}; }
+
+// s + e == a + b exactly (Knuth).
+__device__ __forceinline__ df two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    return df{s, e};
+}
+// s + e == a + b exactly when |a| >= |b| (Dekker).
+__device__ __forceinline__ df fast_two_sum(float a, float b) {
+    const float s = __fadd_rn(a, b);
+    return df{s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+// p + e == a * b exactly (FMA).
+__device__ __forceinline__ df two_prod(float a, float b) {
+    const float p = __fmul_rn(a, b);
+    return df{p, __fmaf_rn(a, b, -p)};
+}
+__device__ __forceinline__ df df_add(df a, df b) {
+    df s = two_sum(a.hi, b.hi);
+    return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+__device__ __forceinline__ df df_mul(df a, df b) {
+    df p = two_prod(a.hi, b.hi);
+    return fast_two_sum(p.hi, __fadd_rn(p.lo, __fmaf_rn(a.hi, b.lo, __fmul_rn(a.lo, b.hi))));
+}
+__device__ __forceinline__ df df_mul_f(df a, float b) {
+    df p = two_prod(a.hi, b);
+    return fast_two_sum(p.hi, __fmaf_rn(a.lo, b, p.lo));
+}
+__device__ __forceinline__ df df_sub(df a, df b) { return df_add(a, df{-b.hi, -b.lo}); }
+// 1 / a with one Newton correction.
+__device__ __forceinline__ df df_recip(df a) {
+    const float y = 1.0f / a.hi;
+    // e = 1 - a * y, evaluated exactly enough in double-float
+    df ay = df_mul_f(a, y);
+    df e = df_sub(df{1.f, 0.f}, ay);
+    return fast_two_sum(y, __fmul_rn(y, e.hi));
+}
+// a > b for normalised pairs
+__device__ __forceinline__ bool df_gt(df a, df b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
+__device__ __forceinline__ bool df_pos(df a) { return a.hi > 0.f || (a.hi == 0.f && a.lo > 0.f); }
+
+// Running sum with the error term kept apart; normalise with df_norm.
+__device__ __forceinline__ void acc_add(df& acc, float v) {
+    df s = two_sum(acc.hi, v);
+    acc.hi = s.hi;
+    acc.lo = __fadd_rn(acc.lo, s.lo);
+}
+__device__ __forceinline__ void acc_add(df& acc, df v) {
+    df s = two_sum(acc.hi, v.hi);
+    acc.hi = s.hi;
+    acc.lo = __fadd_rn(acc.lo, __fadd_rn(s.lo, v.lo));
+}
+__device__ __forceinline__ df df_norm(df a) { return fast_two_sum(a.hi, a.lo); }
+
+__device__ __forceinline__ df shfl_xor_df(df v, int o) {
+    return df{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+}
+__device__ __forceinline__ df shfl_up_df(df v, int o) {
+    return df{__shfl_up_sync(0xffffffffu, v.hi, o), __shfl_up_sync(0xffffffffu, v.lo, o)};
+}
+__device__ __forceinline__ df shfl_df(df v, int src) {
+    return df{__shfl_sync(0xffffffffu, v.hi, src), __shfl_sync(0xffffffffu, v.lo, src)};
+}
+
+// ------------------------------------------------------------ constants
+// ln 2 and log2(e) as float pairs (hi = nearest float, lo = remainder).
+constexpr double kLn2D = 0.69314718055994530941723212145818;
+constexpr double kLog2eD = 1.4426950408889634073599246810019;
+constexpr float kLn2Hi = (float)kLn2D;
+constexpr float kLn2Lo = (float)(kLn2D - (double)(float)kLn2D);
+constexpr float kHeavyExp = -13.0f;  // weights above 2^-13 of the row maximum are evaluated in double-float
+
+// k = log2(e) / T as a float pair.
+__device__ __forceinline__ df k_of_temperature(float T) {
+    const double k = kLog2eD / (double)T;
+    const float hi = (float)k;
+    return df{hi, (float)(k - (double)hi)};
+}
+
+// Table 2^(i/64), i = 0..63, as float pairs; filled once per CTA.
+struct Exp2Table {
+    float hi[64], lo[64];
+};
+__device__ __forceinline__ void exp2_table_init(Exp2Table& t) {
+    for (int i = threadIdx.x; i < 64; i += blockDim.x) {
+        const double v = exp2((double)i / 64.0);
+        const float h = (float)v;
+        t.hi[i] = h;
+        t.lo[i] = (float)(v - (double)h);
+    }
+}
+
+// 2^(xh + xl) in double-float for |xh| < 2^16 (the heavy range is [-13, ~0]).
+__device__ __forceinline__ df exp2_df(float xh, float xl, const Exp2Table& tab) {
+    const float t = rintf(xh * 64.0f);                  // x = t/64 + r
+    const int ti = (int)t;
+    const int i = ti & 63;
+    const int n = ti >> 6;                              // floor(t / 64)
+    const float rh = __fmaf_rn(t, -0.015625f, xh);      // exact: |rh| <= 1/128
+    // a = (rh + xl) * ln2 as a pair
+    df a = two_prod(rh, kLn2Hi);
+    a.lo = __fadd_rn(a.lo, __fmaf_rn(rh, kLn2Lo, __fmul_rn(xl, kLn2Hi)));
+    // e^a - 1 = a + a^2 (1/2 + a (1/6 + a/24)), |a| < 0.0055
+    const float a2 = __fmul_rn(a.hi, a.hi);
+    const float poly = __fmul_rn(a2, __fmaf_rn(a.hi, __fmaf_rn(a.hi, 1.0f / 24.0f, 1.0f / 6.0f), 0.5f));
+    df e = fast_two_sum(1.0f, a.hi);
+    e.lo = __fadd_rn(e.lo, __fadd_rn(a.lo, poly));
+    df w = df_mul(df{tab.hi[i], tab.lo[i]}, e);
+    const float sc = __int_as_float((n + 127) << 23);   // 2^n, n in [-126, 127] here
+    return df{__fmul_rn(w.hi, sc), __fmul_rn(w.lo, sc)};
+}
+
+// Weight of one logit relative to the row maximum: 2^((l - lmax) * k).
+// FP32IN: the logits are fp32 (the difference l - lmax may then round and is
+// carried as a pair); bf16 logits differ exactly in fp32.
+template <bool FP32IN>
+__device__ __forceinline__ df logit_weight(float l, float lmax, df k, const Exp2Table& tab) {
+    float dh, dl = 0.f;
+    if constexpr (FP32IN) {
+        df d = two_sum(l, -lmax);
+        dh = d.hi;
+        dl = d.lo;
+    } else {
+        dh = __fsub_rn(l, lmax);
+    }
+    const float xh = __fmul_rn(dh, k.hi);
+    if (!(xh > -126.0f)) return df{0.f, 0.f};  // underflow, -inf logits
+    float xl = __fmaf_rn(dh, k.hi, -xh);
+    xl = __fmaf_rn(dh, k.lo, xl);
+    if constexpr (FP32IN) xl = __fmaf_rn(dl, k.hi, xl);
+    if (xh > kHeavyExp) return exp2_df(xh, xl, tab);
+    return df{__fmul_rn(ex2(xh), __fmaf_rn(xl, kLn2Hi, 1.0f)), 0.f};
+}
+
+// Residual weight of one column: max(0, Wt * It - Wd * Id).
+__device__ __forceinline__ df resid_weight(df a, df b, df It, df Id) {
+    if (a.lo == 0.f && b.lo == 0.f) {
+        // both weights light (single floats): the difference of two small
+        // products, each rounded once
+        const float p = __fmaf_rn(a.hi, It.hi, __fmul_rn(a.hi, It.lo));
+        const float q = __fmaf_rn(b.hi, Id.hi, __fmul_rn(b.hi, Id.lo));
+        const float r = __fsub_rn(p, q);
+        return df{r > 0.f ? r : 0.f, 0.f};
+    }
+    df d = df_sub(df_mul(a, It), df_mul(b, Id));
+    return df_pos(d) ? d : df{0.f, 0.f};
+}
+
+}  // namespace specv

@@ -8,18 +8,23 @@
 // weights exceeds u * Z, Z = the sum of all weights (the page's sampler in its
 // Code section, which tolerates unnormalised weights). If Z == 0 at a
 // rejection (p == q to rounding) the same rule runs on p_i; if rounding leaves
-// no index the last one with positive weight is taken.
+// no index, the last one with positive weight is taken.
 //
 // Only the selected row pair is re-read. Each sequence gets one thread-block
-// cluster of nsplit CTAs; CTA c owns a contiguous column chunk, computes the
-// weights tile by tile (a tile = 32 lanes x 8 consecutive columns), keeps each
-// tile's sum in shared memory, and publishes its chunk sum to every CTA of the
-// cluster through distributed shared memory. Every CTA then forms the same
-// prefix over chunk sums; the CTA whose interval holds u * Z walks its tile
-// sums and rescans one tile (L2-resident by then) to find the column.
+// cluster of nsplit CTAs, CTA c owning a contiguous column chunk:
+//   pass A (residual only): the exact normalisers S_p = sum_j 2^((l_j - l_max) k)
+//     of both rows, reduced over the cluster through distributed shared memory;
+//   pass B: the weights r_j (= max(0, p_j - q_j), or p_j's weight for a bonus)
+//     tile by tile (a tile = 32 lanes x 8 consecutive columns), each tile's sum
+//     kept in shared memory; chunk sums are exchanged across the cluster so
+//     every CTA knows Z and where its chunk starts in the CDF;
+//   the CTA whose interval holds u * Z finds the tile with one warp-wide
+//   prefix over its tile sums and rescans that tile to find the column.
+// Weights, sums and prefixes are double-float (precise.cuh), so the pick
+// matches a float64 evaluation except within ~1e-10 of a CDF edge.
 #include <math.h>
 
-#include "common.cuh"
+#include "precise.cuh"
 
 namespace specv {
 
@@ -28,17 +33,17 @@ namespace {
 constexpr int kWarps = kSampThreads / 32;
 
 struct SampSmem {
-    float tile_sum[kMaxTilesPerCta];
-    float zc[kMaxCluster];
-    float zc2[kMaxCluster];
-    float red[kWarps];
+    Exp2Table tab;
+    df tile_sum[kMaxTilesPerCta];
+    df norm_t[kMaxCluster], norm_d[kMaxCluster];
+    df zc[kMaxCluster], zc2[kMaxCluster];
+    df red_t[kWarps], red_d[kWarps];
     int32_t sel_tile;
-    float sel_base;
-    int32_t token;
+    df sel_base;
 };
 
 // Eight consecutive columns c..c+7 of a row as floats; columns at or past
-// `lim` read as -inf (their weight is masked to zero by the caller).
+// `lim` read as -inf (weight 0).
 template <int DT>
 __device__ __forceinline__ void load8(const char* row, int64_t c, int64_t lim, bool aligned, float (&v)[8]) {
     if (aligned && c + 8 <= lim) {
@@ -59,87 +64,127 @@ __device__ __forceinline__ void load8(const char* row, int64_t c, int64_t lim, b
     }
 }
 
-// Weight of one column. Explicit round-to-nearest intrinsics keep the value
-// bit-identical between the summing pass and the rescan.
-__device__ __forceinline__ float weight_p(float lt, const SampleTask& t) {
-    return __fmul_rn(ex2(__fmaf_rn(lt, t.kt, -t.mt)), t.inv_st);
-}
-__device__ __forceinline__ float weight_resid(float lt, float ld, const SampleTask& t) {
-    const float pt = weight_p(lt, t);
-    const float qd = t.probs ? __fmul_rn(ld, t.inv_sd) : __fmul_rn(ex2(__fmaf_rn(ld, t.kd, -t.md)), t.inv_sd);
-    return fmaxf(__fsub_rn(pt, qd), 0.f);
-}
-
 template <int TDT, int DDT>
 struct RowPair {
     const char* trow;
     const char* drow;
-    bool tal, dal;
-    int64_t lim;  // one past the last column of this CTA's chunk
-    // weights of the 8 columns c..c+7 owned by this lane of a tile
-    __device__ __forceinline__ void weights(int64_t c, bool resid, const SampleTask& t, float (&w)[8]) const {
-        float lt[8];
-        load8<TDT>(trow, c, lim, tal, lt);
-        if (resid) {
-            float ld[8];
-            load8<DDT>(drow, c, lim, dal, ld);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = (c + e < lim) ? weight_resid(lt[e], ld[e], t) : 0.f;
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) w[e] = (c + e < lim) ? weight_p(lt[e], t) : 0.f;
-        }
+    bool tal, dal, probs;
+    int64_t lim;
+    float mt, md;  // raw row maxima
+    df k;
+
+    __device__ __forceinline__ df wt(float l, const Exp2Table& tab) const {
+        return logit_weight<TDT == SPECV_F32>(l, mt, k, tab);
+    }
+    __device__ __forceinline__ df wd(float l, const Exp2Table& tab) const {
+        if (probs) return df{(l > -INFINITY) ? l : 0.f, 0.f};  // probabilities are their own weights
+        return logit_weight<DDT == SPECV_F32>(l, md, k, tab);
     }
 };
 
-// Inclusive warp scan of the lane sums (Hillis-Steele); also returns the
-// lane's exclusive prefix as the inclusive value of the lane below.
-__device__ __forceinline__ void warp_scan(float x, float& incl, float& excl) {
+// Weights of the 8 columns c..c+7 of this lane: residual, or p's weight only.
+template <int TDT, int DDT>
+__device__ __forceinline__ void lane_weights(const RowPair<TDT, DDT>& rp, int64_t c, int mode, df It, df Id,
+                                             const Exp2Table& tab, df (&w)[8]) {
+    float lt[8];
+    load8<TDT>(rp.trow, c, rp.lim, rp.tal, lt);
+    if (mode == kTaskResidual) {
+        float ld[8];
+        load8<DDT>(rp.drow, c, rp.lim, rp.dal, ld);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = resid_weight(rp.wt(lt[e], tab), rp.wd(ld[e], tab), It, Id);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = rp.wt(lt[e], tab);
+    }
+}
+
+// Inclusive warp scan of double-float values (Hillis-Steele).
+__device__ __forceinline__ df warp_scan_df(df x) {
     const int lane = threadIdx.x & 31;
-    incl = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        float y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl = __fadd_rn(incl, y);
+        df y = shfl_up_df(x, o);
+        if (lane >= o) x = df_add(y, x);
     }
-    excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) excl = 0.f;
+    return x;
 }
 
-// Sum of a tile as the rescan will see it at its last column: the exclusive
-// prefix of lane 31 plus lane 31's own sequential sum.
-__device__ __forceinline__ float tile_total(const float (&w)[8]) {
-    float ls = 0.f;
+__device__ __forceinline__ df warp_sum_df(df x) {
 #pragma unroll
-    for (int e = 0; e < 8; ++e) ls = __fadd_rn(ls, w[e]);
-    float incl, excl;
-    warp_scan(ls, incl, excl);
-    const float t = __fadd_rn(excl, ls);
-    return __shfl_sync(0xffffffffu, t, 31);
+    for (int o = 16; o > 0; o >>= 1) x = df_add(x, shfl_xor_df(x, o));
+    return x;
 }
 
-// Pass over this CTA's tiles: tile sums into smem; returns their in-order sum.
+// Total of a lane's 8 weights.
+__device__ __forceinline__ df lane_total(const df (&w)[8]) {
+    df acc{0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc_add(acc, w[e]);
+    return df_norm(acc);
+}
+
+// Pass A: exact normalisers of both rows over this CTA's chunk (block sums,
+// valid in warp 0).
 template <int TDT, int DDT>
-__device__ float chunk_pass(const RowPair<TDT, DDT>& rp, int64_t cs, int ntiles, bool resid, const SampleTask& t,
-                            SampSmem& sm) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int ti = warp; ti < ntiles; ti += 2 * kWarps) {
-        const int tj = ti + kWarps;
-        float w0[8], w1[8];
-        rp.weights(cs + (int64_t)ti * kTile + lane * 8, resid, t, w0);
-        if (tj < ntiles) rp.weights(cs + (int64_t)tj * kTile + lane * 8, resid, t, w1);
-        const float s0 = tile_total(w0);
-        if (lane == 0) sm.tile_sum[ti] = s0;
-        if (tj < ntiles) {
-            const float s1 = tile_total(w1);
-            if (lane == 0) sm.tile_sum[tj] = s1;
+__device__ void chunk_norms(const RowPair<TDT, DDT>& rp, int64_t cs, int64_t ce, SampSmem& sm, df& St, df& Sd) {
+    df at{0.f, 0.f}, ad{0.f, 0.f};
+    for (int64_t c = cs + (int64_t)threadIdx.x * 8; c < ce; c += (int64_t)blockDim.x * 8) {
+        float lt[8], ld[8];
+        load8<TDT>(rp.trow, c, rp.lim, rp.tal, lt);
+        load8<DDT>(rp.drow, c, rp.lim, rp.dal, ld);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            acc_add(at, rp.wt(lt[e], sm.tab));
+            acc_add(ad, rp.wd(ld[e], sm.tab));
         }
     }
+    at = warp_sum_df(df_norm(at));
+    ad = warp_sum_df(df_norm(ad));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) {
+        sm.red_t[warp] = at;
+        sm.red_d[warp] = ad;
+    }
     __syncthreads();
-    float z = 0.f;
+    if (warp == 0) {
+        at = lane < kWarps ? sm.red_t[lane] : df{0.f, 0.f};
+        ad = lane < kWarps ? sm.red_d[lane] : df{0.f, 0.f};
+        at = warp_sum_df(at);
+        ad = warp_sum_df(ad);
+    }
+    St = at;
+    Sd = ad;
+}
+
+// Pass B: tile sums in index order into smem; returns the chunk total (warp 0).
+template <int TDT, int DDT>
+__device__ df chunk_tiles(const RowPair<TDT, DDT>& rp, int64_t cs, int ntiles, int mode, df It, df Id,
+                          SampSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int ti = warp; ti < ntiles; ti += kWarps) {
+        df w[8];
+        lane_weights(rp, cs + (int64_t)ti * kTile + lane * 8, mode, It, Id, sm.tab, w);
+        const df incl = warp_scan_df(lane_total(w));
+        if (lane == 31) sm.tile_sum[ti] = incl;
+    }
+    __syncthreads();
+    df z{0.f, 0.f};
+    if (warp == 0) {
+        for (int ti = lane; ti < ntiles; ti += 32) z = df_add(z, sm.tile_sum[ti]);
+        z = warp_sum_df(z);
+    }
+    return z;
+}
+
+// Publish thread 0's value into slot c of every CTA in the cluster.
+__device__ __forceinline__ void cluster_publish(df* slots, uint32_t c, int ns, df v) {
     if (threadIdx.x == 0)
-        for (int ti = 0; ti < ntiles; ++ti) z = __fadd_rn(z, sm.tile_sum[ti]);
-    return z;  // thread 0
+        for (int r = 0; r < ns; ++r) {
+            st_cluster_f32(&slots[c].hi, r, v.hi);
+            st_cluster_f32(&slots[c].lo, r, v.lo);
+        }
+    cluster_sync_all();
 }
 
 template <int TDT, int DDT>
@@ -151,6 +196,7 @@ __global__ void __launch_bounds__(kSampThreads) sampler_kernel(SampleParams p) {
     const uint32_t c = cluster_ctarank();
     const SampleTask t = p.tasks_in[b];
     if (t.mode == kTaskNone) return;  // uniform across the cluster: nobody reaches a barrier
+    exp2_table_init(sm.tab);
 
     const int64_t cs = (int64_t)c * p.vchunk;
     const int64_t ce = min(p.V, cs + p.vchunk);
@@ -162,76 +208,107 @@ __global__ void __launch_bounds__(kSampThreads) sampler_kernel(SampleParams p) {
     rp.tal = ((uintptr_t)rp.trow & 15u) == 0;
     rp.dal = ((uintptr_t)rp.drow & 15u) == 0;
     rp.lim = ce;
-    bool resid = t.mode == kTaskResidual;
+    rp.probs = t.probs != 0;
+    rp.mt = t.mt;
+    rp.md = t.md;
+    rp.k = df{t.k_hi, t.k_lo};
+    __syncthreads();  // exp2 table ready
 
-    // chunk sums -> every CTA of the cluster
-    float zc = chunk_pass(rp, cs, ntiles, resid, t, sm);
-    if (threadIdx.x == 0)
-        for (int r = 0; r < p.nsplit; ++r) st_cluster_f32(&sm.zc[c], r, zc);
-    cluster_sync_all();
-    float pre = 0.f, Z = 0.f, lo = 0.f;
-    for (int r = 0; r < p.nsplit; ++r) {
-        if (r == (int)c) lo = pre;
-        pre = __fadd_rn(pre, sm.zc[r]);
-    }
-    Z = pre;
-    const float* zs = sm.zc;
-    if (resid && !(Z > 0.f)) {
-        // p_i == q_i to rounding: draw from p_i instead
-        resid = false;
-        __syncthreads();
-        zc = chunk_pass(rp, cs, ntiles, resid, t, sm);
-        if (threadIdx.x == 0)
-            for (int r = 0; r < p.nsplit; ++r) st_cluster_f32(&sm.zc2[c], r, zc);
-        cluster_sync_all();
-        pre = 0.f;
+    int mode = t.mode;
+    df It{1.f, 0.f}, Id{1.f, 0.f};
+    if (mode == kTaskResidual) {
+        df St, Sd;
+        chunk_norms(rp, cs, ce, sm, St, Sd);
+        cluster_publish(sm.norm_t, c, p.nsplit, St);
+        cluster_publish(sm.norm_d, c, p.nsplit, Sd);
+        df Tt{0.f, 0.f}, Td{0.f, 0.f};
         for (int r = 0; r < p.nsplit; ++r) {
-            if (r == (int)c) lo = pre;
-            pre = __fadd_rn(pre, sm.zc2[r]);
+            Tt = df_add(Tt, sm.norm_t[r]);
+            Td = df_add(Td, sm.norm_d[r]);
         }
-        Z = pre;
-        zs = sm.zc2;
+        It = df_recip(Tt);
+        Id = df_recip(Td);
+        if (c == 0 && threadIdx.x == 0) {
+            p.tasks[b].st_hi = Tt.hi;
+            p.tasks[b].st_lo = Tt.lo;
+            p.tasks[b].sd_hi = Td.hi;
+            p.tasks[b].sd_lo = Td.lo;
+        }
     }
-    const float thr = __fmul_rn(t.u, Z);
-    const float hi = __fadd_rn(lo, zs[c]);
-    bool owner = (lo <= thr) && (thr < hi);
+
+    df zc = chunk_tiles(rp, cs, ntiles, mode, It, Id, sm);
+    cluster_publish(sm.zc, c, p.nsplit, zc);
+    const df* zs = sm.zc;
+    df Z{0.f, 0.f}, lo{0.f, 0.f};
+    for (int r = 0; r < p.nsplit; ++r) {
+        if (r == (int)c) lo = Z;
+        Z = df_add(Z, zs[r]);
+    }
+    if (mode == kTaskResidual && !df_pos(Z)) {
+        // p_i == q_i to rounding: draw from p_i instead
+        mode = kTaskBonus;
+        __syncthreads();
+        zc = chunk_tiles(rp, cs, ntiles, mode, It, Id, sm);
+        cluster_publish(sm.zc2, c, p.nsplit, zc);
+        zs = sm.zc2;
+        Z = df{0.f, 0.f};
+        for (int r = 0; r < p.nsplit; ++r) {
+            if (r == (int)c) lo = Z;
+            Z = df_add(Z, zs[r]);
+        }
+    }
+    if (c == 0 && threadIdx.x == 0) {
+        p.tasks[b].z_hi = Z.hi;
+        p.tasks[b].z_lo = Z.lo;
+    }
+    // threshold u * Z; u has 24 significant bits
+    const df thr = df_add(two_prod(t.u, Z.hi), df{__fmul_rn(t.u, Z.lo), 0.f});
+    const df hi_edge = df_add(lo, zs[c]);
+    bool owner = !df_gt(lo, thr) && df_gt(hi_edge, thr) && df_pos(zs[c]);
     bool fallback = false;
-    if (!(thr < Z)) {
-        // rounding put u * Z at or past the total: last chunk with positive mass
+    if (!df_gt(Z, thr)) {
         int last = -1;
         for (int r = 0; r < p.nsplit; ++r)
-            if (zs[r] > 0.f) last = r;
+            if (df_pos(zs[r])) last = r;
         owner = (last == (int)c);
         fallback = true;
     }
-    if (c == 0 && threadIdx.x == 0) p.tasks[b].z = Z;
     if (!owner) return;
 
-    // locate the tile holding the crossing
-    if (threadIdx.x == 0) {
+    // locate the tile holding the crossing: one warp, 32 tiles per step
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
         int sel = -1;
-        float run = lo, base = lo;
+        df base = lo;
         if (!fallback) {
-            for (int ti = 0; ti < ntiles; ++ti) {
-                const float nxt = __fadd_rn(run, sm.tile_sum[ti]);
-                if (nxt > thr) {
-                    sel = ti;
-                    base = run;
-                    break;
+            df run = lo;
+            for (int t0 = 0; t0 < ntiles && sel < 0; t0 += 32) {
+                const int ti = t0 + lane;
+                const df v = ti < ntiles ? sm.tile_sum[ti] : df{0.f, 0.f};
+                const df end = df_add(run, warp_scan_df(v));
+                const unsigned hit = __ballot_sync(0xffffffffu, ti < ntiles && df_gt(end, thr));
+                if (hit) {
+                    const int src = __ffs(hit) - 1;
+                    sel = t0 + src;
+                    base = shfl_df(df_sub(end, v), src);  // run + exclusive prefix
+                } else {
+                    run = shfl_df(end, 31);
                 }
-                run = nxt;
             }
         }
-        if (sel < 0) {  // no crossing by this CTA's own running sum: last tile with mass
-            for (int ti = ntiles - 1; ti >= 0; --ti)
-                if (sm.tile_sum[ti] > 0.f) {
-                    sel = ti;
-                    break;
-                }
-            base = NAN;  // no comparison succeeds: the last-positive rule applies inside the tile
+        int mark = 0;
+        if (sel < 0) {  // rounding left no crossing here: the last tile with mass
+            for (int hi_t = ntiles - 1; hi_t >= 0 && sel < 0; hi_t -= 32) {
+                const int ti = hi_t - lane;
+                const unsigned pos = __ballot_sync(0xffffffffu, ti >= 0 && df_pos(sm.tile_sum[ti >= 0 ? ti : 0]));
+                if (pos) sel = hi_t - (__ffs(pos) - 1);
+            }
+            mark = 1;
         }
-        sm.sel_tile = sel;
-        sm.sel_base = base;
+        if (lane == 0) {
+            sm.sel_tile = sel;
+            sm.sel_base = mark ? df{NAN, 0.f} : base;  // NaN: no comparison succeeds
+        }
     }
     __syncthreads();
     if (threadIdx.x >= 32 || sm.sel_tile < 0) return;
@@ -239,22 +316,24 @@ __global__ void __launch_bounds__(kSampThreads) sampler_kernel(SampleParams p) {
     // one warp rescans the selected tile in index order
     const int lane = threadIdx.x;
     const int64_t col0 = cs + (int64_t)sm.sel_tile * kTile + lane * 8;
-    float w[8];
-    rp.weights(col0, resid, t, w);
-    float cum[8], ls = 0.f;
+    df w[8];
+    lane_weights(rp, col0, mode, It, Id, sm.tab, w);
+    df cum[8];
+    df acc{0.f, 0.f};
 #pragma unroll
     for (int e = 0; e < 8; ++e) {
-        ls = __fadd_rn(ls, w[e]);
-        cum[e] = ls;
+        acc_add(acc, w[e]);
+        cum[e] = df_norm(acc);
     }
-    float incl, excl;
-    warp_scan(ls, incl, excl);
-    const float base = sm.sel_base;
+    const df incl = warp_scan_df(cum[7]);
+    df excl = shfl_up_df(incl, 1);
+    if (lane == 0) excl = df{0.f, 0.f};
+    const df base = sm.sel_base;
     int hit = -1, lastpos = -1;
 #pragma unroll
     for (int e = 7; e >= 0; --e) {
-        if (__fadd_rn(base, __fadd_rn(excl, cum[e])) > thr) hit = e;
-        if (lastpos < 0 && w[e] > 0.f) lastpos = e;
+        if (df_gt(df_add(base, df_add(excl, cum[e])), thr)) hit = e;
+        if (lastpos < 0 && df_pos(w[e])) lastpos = e;
     }
     const unsigned hm = __ballot_sync(0xffffffffu, hit >= 0);
     int64_t tok = -1;

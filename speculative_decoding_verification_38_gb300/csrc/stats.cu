@@ -21,7 +21,7 @@
 // arriver resets the counter for the next call.
 #include <math.h>
 
-#include "common.cuh"
+#include "precise.cuh"
 
 namespace specv {
 
@@ -95,11 +95,11 @@ __device__ __forceinline__ float temp_of(const StatsParams& p, int32_t b) {
 }
 
 // ------------------------------------------------------------ block reductions
-__device__ float2 block_ms(float2 v, Smem& sm) {
+__device__ float2 block_ms(float2 v, float k, Smem& sm) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         float2 w = make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o));
-        v = ms_merge(v, w);
+        v = ms_merge(v, w, k);
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) sm.red[warp] = v;
@@ -109,7 +109,7 @@ __device__ float2 block_ms(float2 v, Smem& sm) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             float2 w = make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o));
-            v = ms_merge(v, w);
+            v = ms_merge(v, w, k);
         }
     }
     __syncthreads();
@@ -317,8 +317,7 @@ __device__ float2 seg_pass(const char* row, int64_t c0, int64_t c1, float k, Sme
     }
     // reduce across the CTA
     if constexpr (MODE == kLogits) {
-        float2 st = make_float2(a.m == -INFINITY ? -INFINITY : -a.neg, a.s);
-        return block_ms(st, sm);
+        return block_ms(make_float2(a.m, a.s), k, sm);  // (raw max, sum relative to it)
     } else if constexpr (MODE == kProbs) {
         return make_float2(0.f, block_sum(a.s, sm));
     } else {
@@ -409,20 +408,18 @@ __device__ void write_ok(const StatsParams& p, int32_t b, int32_t g, int32_t a) 
 }
 
 // Merge the partials of row r (flat index) with one warp; result in lane 0.
-__device__ float2 merge_row_ms(const StatsParams& p, int64_t r, bool probs_row) {
+__device__ float2 merge_row_ms(const StatsParams& p, int64_t r, bool probs_row, float k) {
     const int lane = threadIdx.x & 31;
-    const int64_t first = (r * p.V) / p.chunk;
     const uint32_t ns = nseg_of(r, p.V, p.chunk);
     float2 acc = make_float2(probs_row ? 0.f : -INFINITY, 0.f);
     for (uint32_t j = lane; j < ns; j += 32) {
         float2 v = ld_cg_f2(p.partials + r * p.S + j);
-        acc = probs_row ? make_float2(0.f, acc.y + v.y) : ms_merge(acc, v);
+        acc = probs_row ? make_float2(0.f, acc.y + v.y) : ms_merge(acc, v, k);
     }
-    (void)first;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         float2 w = make_float2(__shfl_xor_sync(0xffffffffu, acc.x, o), __shfl_xor_sync(0xffffffffu, acc.y, o));
-        acc = probs_row ? make_float2(0.f, acc.y + w.y) : ms_merge(acc, w);
+        acc = probs_row ? make_float2(0.f, acc.y + w.y) : ms_merge(acc, w, k);
     }
     return acc;
 }
@@ -459,7 +456,7 @@ __device__ void finalize_sample(const StatsParams& p, int32_t b, Smem& sm) {
         const bool is_t = j <= g;
         const int64_t r = is_t ? (t0 + j) : (p.rows_t + d0 + (j - g - 1));
         const bool probs_row = !is_t && p.probs;
-        float2 v = merge_row_ms(p, r, probs_row);
+        float2 v = merge_row_ms(p, r, probs_row, k);
         if (lane == 0) {
             sm.rs[j] = v;
             p.row_stats[r] = v;
@@ -473,8 +470,9 @@ __device__ void finalize_sample(const StatsParams& p, int32_t b, Smem& sm) {
             const float2 ts = sm.rs[i], ds = sm.rs[g + 1 + i];
             const float lt = ld_elem_rt((const char*)p.tgt + (t0 + i) * p.V * (p.tdt == SPECV_F32 ? 4 : 2), p.tdt, x);
             const float ld = ld_elem_rt((const char*)p.dft + (d0 + i) * p.V * (p.ddt == SPECV_F32 ? 4 : 2), p.ddt, x);
-            const float pxv = ex2(__fmaf_rn(lt, k, -ts.x)) * (1.0f / ts.y);
-            const float qxv = p.probs ? ld * (1.0f / ds.y) : ex2(__fmaf_rn(ld, k, -ds.x)) * (1.0f / ds.y);
+            const float pxv = ex2(__fmaf_rn(lt, k, -__fmul_rn(ts.x, k))) * (1.0f / ts.y);
+            const float qxv =
+                p.probs ? ld * (1.0f / ds.y) : ex2(__fmaf_rn(ld, k, -__fmul_rn(ds.x, k))) * (1.0f / ds.y);
             sm.px[i] = pxv;
             sm.qx[i] = qxv;
             sm.xt[i] = x;
@@ -514,19 +512,13 @@ __device__ void finalize_sample(const StatsParams& p, int32_t b, Smem& sm) {
             t.drow = a < g ? d0 + a : -1;
             t.out_slot = t0 + a;
             t.u = sm.us[a];
-            t.kt = k;
+            const df kk = k_of_temperature(temp_of(p, b));
+            t.k_hi = kk.hi;
+            t.k_lo = kk.lo;
             t.mt = sm.rs[a].x;
-            t.inv_st = 1.0f / sm.rs[a].y;
-            if (a < g) {
-                const float2 ds = sm.rs[g + 1 + a];
-                t.kd = p.probs ? 0.f : k;
-                t.md = p.probs ? 0.f : ds.x;
-                t.inv_sd = 1.0f / ds.y;
-            } else {
-                t.kd = t.md = t.inv_sd = 0.f;
-            }
-            t.z = 0.f;
-            t.pad[0] = t.pad[1] = 0;
+            t.md = a < g ? sm.rs[g + 1 + a].x : 0.f;
+            t.z_hi = t.z_lo = t.st_hi = t.st_lo = t.sd_hi = t.sd_lo = 0.f;
+            t.pad = 0;
             p.tasks[b] = t;
         }
     }

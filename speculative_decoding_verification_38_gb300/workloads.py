@@ -87,7 +87,8 @@ class Workload:
 
     @property
     def rows_draft(self) -> int:
-        return 0 if self.draft is None else int(self.draft.shape[0])
+        """Draft positions sum_b gamma_b (greedy keeps no draft logits, only tokens)."""
+        return int(np.asarray(self.gammas, dtype=np.int64).sum())
 
     @property
     def dtype_name(self) -> str:

@@ -32,6 +32,7 @@ class Tally:
         self.unexcused = []
         self.in_band = 0
         self.rounds = 0
+        self.excused = []  # (kind, distance of u to the boundary)
 
     def merge(self, o):
         self.draws += o.draws
@@ -39,6 +40,7 @@ class Tally:
         self.unexcused += o.unexcused
         self.in_band += o.in_band
         self.rounds += o.rounds
+        self.excused += o.excused
 
     def check(self, label=""):
         assert not self.unexcused, f"{label}: unexcused mismatches {self.unexcused[:10]}"
@@ -46,8 +48,12 @@ class Tally:
             f"{label}: {self.mismatches} excused mismatches in {self.draws} draws")
 
     def __repr__(self):
+        kinds = {}
+        for k, d in self.excused:
+            kinds.setdefault(k, []).append(d)
+        det = {k: (len(v), float(max(v))) for k, v in kinds.items()}
         return (f"Tally(rounds={self.rounds}, draws={self.draws}, mismatches={self.mismatches}, "
-                f"in_band={self.in_band}, unexcused={len(self.unexcused)})")
+                f"in_band={self.in_band}, unexcused={len(self.unexcused)}, excused(kind: n, max dist)={det})")
 
 
 def compare_sample(w, gpu: dict, orc: dict, *, seed: int, rnd: int, tokens, seq_offset: int = 0,
@@ -91,16 +97,22 @@ def compare_sample(w, gpu: dict, orc: dict, *, seed: int, rnd: int, tokens, seq_
             st, px, qx = oracle.accept_terms(w, b, i, draft_tokens=tokens)
             ua, _ = u_of(i)
             ok = st == 0 and qx > 0 and abs(ua - px / qx) < BAND
+            if ok:
+                T.excused.append(("accept", abs(ua - px / qx)))
         else:
             _, us = u_of(ao)
-            ok = min(abs(us - diag["cdf_lo"][b]), abs(us - diag["cdf_hi"][b])) < BAND
+            dist = min(abs(us - diag["cdf_lo"][b]), abs(us - diag["cdf_hi"][b]))
+            ok = dist < BAND
             if not ok:
                 tok_g = int(gpu["tokens"][seg][ao])
                 if 0 <= tok_g < w.vocab:
                     st, p, q, wts, Z = oracle.position_rows(w, b, ao, draft_tokens=tokens)
                     lo, hi = oracle.cdf_edges(wts, tok_g)
-                    ok = min(abs(us - lo), abs(us - hi)) < BAND
+                    dist = min(abs(us - lo), abs(us - hi))
+                    ok = dist < BAND
             ok = ok and np.array_equal(orc["tokens"][seg][:ao], gpu["tokens"][seg][:ao])
+            if ok:
+                T.excused.append(("resid" if ao < g else "bonus", dist))
         if not ok:
             T.unexcused.append((b, ao, ag, orc["tokens"][seg].tolist(), gpu["tokens"][seg].tolist()))
     return T

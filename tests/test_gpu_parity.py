@@ -241,10 +241,9 @@ def test_row_stats_match_oracle(sv):
         rows = [(w.target, r, r) for r in range(tro[b], tro[b + 1])] + \
                [(w.draft, r, w.rows_target + r) for r in range(dro[b], dro[b + 1])]
         for arr, r, flat in rows:
-            x = wl.stored_f32(arr[r]).astype(np.float64) / T * L2E
-            mm = x.max()
-            ss = np.exp2(x - mm).sum()
-            assert abs(m[flat] - mm) <= 1e-6 * max(1.0, abs(mm))
+            vals = wl.stored_f32(arr[r]).astype(np.float64)
+            assert m[flat] == vals.max()  # the raw maximum, exactly
+            ss = np.exp2((vals - vals.max()) / T * L2E).sum()
             assert abs(s[flat] - ss) <= 1e-5 * ss
 
 
@@ -338,7 +337,7 @@ def test_kv_rollback_matches_oracle(sv):
 
 
 # --------------------------------------------------------------- statistics
-def _iid_gpu_workload(p, q, gamma, B, rng):
+def _iid_gpu_workload(p, q, gamma, B, rng, pool=8):
     V = p.shape[0]
     with np.errstate(divide="ignore"):
         lp = np.log(p).astype(np.float32)
@@ -346,7 +345,7 @@ def _iid_gpu_workload(p, q, gamma, B, rng):
     dft = np.ascontiguousarray(np.broadcast_to(q.astype(np.float32), (B * gamma, V)))
     cq = np.cumsum(q)
     pool = [np.minimum(np.searchsorted(cq, rng.random(B * gamma) * cq[-1], side="right"), V - 1).astype(np.int32)
-            for _ in range(8)]
+            for _ in range(pool)]
     return wl.Workload(name="iid", batch=B, vocab=V, gamma_max=gamma, gammas=np.full(B, gamma, np.int32),
                        target=tgt, draft=dft, draft_tokens=pool[0], token_pool=pool, draft_is_probs=True)
 
@@ -355,13 +354,13 @@ def test_gpu_chi_square_1e6(sv):
     """1e6 GPU rounds: the emitted stream follows p (chi-square p > 1e-3)."""
     DeviceBatch = _harness()
     rng = np.random.default_rng(77)
-    V, gamma, B = 6, 3, 131072
+    V, gamma, B = 6, 3, 65536
     p = oracle.softmax_row(rng.standard_normal(V).astype(np.float32) * 1.5, 1.0)[1]
     q = oracle.softmax_row(rng.standard_normal(V).astype(np.float32) * 1.5, 1.0)[1]
-    w = _iid_gpu_workload(p, q, gamma, B, rng)
+    w = _iid_gpu_workload(p, q, gamma, B, rng, pool=16)
     db = DeviceBatch(w, seed=1234)
     firsts, streams = [], []
-    for r in range(8):
+    for r in range(16):
         db.run(rnd=r, pool_index=r)
         g = db.results()
         toks = g["tokens"].reshape(B, gamma + 1)
@@ -385,10 +384,13 @@ def test_gpu_mean_tokens_known_alpha(sv, alpha, gamma):
     bb = np.zeros(V)
     bb[4:] = rng.dirichlet(np.ones(4))
     p, q = alpha * s + (1 - alpha) * a, alpha * s + (1 - alpha) * bb
-    w = _iid_gpu_workload(p, q, gamma, 100_000, rng)
+    w = _iid_gpu_workload(p, q, gamma, 50_000, rng, pool=2)
     db = DeviceBatch(w, seed=5)
-    db.run(rnd=1)
-    emitted = db.results()["accepted"] + 1
+    em = []
+    for r in range(2):  # 1e5 rounds: two calls of 50,000 sequences
+        db.run(rnd=r, pool_index=r)
+        em.append(db.results()["accepted"] + 1)
+    emitted = np.concatenate(em)
     E = (1 - alpha ** (gamma + 1)) / (1 - alpha)
     assert abs(emitted.mean() - E) / E < 0.01
     assert emitted.min() >= 1 and emitted.max() <= gamma + 1
