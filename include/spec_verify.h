@@ -69,7 +69,9 @@ enum {
     SPEC_SEQ_BAD_ROW = 3,    /* a row the decision needed has a NaN, +inf, no finite
                                 logit, or (probs mode) a sum that is not > 0 */
     SPEC_SEQ_BAD_LAYOUT = 4, /* offsets of sequence b inconsistent or out of range */
-    SPEC_SEQ_BAD_TEMP = 5    /* temperature of sequence b not finite and > 0 */
+    SPEC_SEQ_BAD_TEMP = 5,   /* temperature of sequence b not finite and > 0 */
+    SPEC_SEQ_TIMEOUT = 6     /* a bounded on-device wait for a copy gave up (the draw
+                                is left at -1); never expected on a healthy GPU */
 };
 /* Precedence when several apply: LAYOUT, TEMP (sampling only), TOKEN, KV, then
  * ROW for the first bad row met while scanning positions left to right. */
@@ -229,6 +231,12 @@ SPEC_API spec_status_t spec_debug_row_stats(const spec_verify_args_t* args, int3
  * NULL. */
 SPEC_API spec_status_t spec_debug_probs(const spec_verify_args_t* args, int32_t seq, int32_t pos, float* out_p,
                                         float* out_q, float* out_w, float* out_scalars, spec_stream_t stream);
+
+/* The sampler's 2^x for light weights (exponents x <= -13) as its sums see
+ * them: (y[2i], y[2i+1]) = (the SFU's 2^x[i], the correction that removes the
+ * SFU's measured mean error when such weights are summed). x: device array of
+ * n floats; y: device array of 2n floats. */
+SPEC_API spec_status_t spec_debug_light_exp2(const float* x, float* y, int64_t n, spec_stream_t stream);
 
 /* Profiling hook for the calling thread: when both are non-NULL, the next
  * spec_verify_sample / spec_verify_greedy call made by this thread records

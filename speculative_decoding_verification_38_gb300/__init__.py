@@ -114,6 +114,8 @@ def lib():
             L.spec_debug_row_stats.argtypes = [A, i32, vp, vp, vp, vp]
             L.spec_debug_probs.restype = ctypes.c_int
             L.spec_debug_probs.argtypes = [A, i32, i32, vp, vp, vp, vp, vp]
+            L.spec_debug_light_exp2.restype = ctypes.c_int
+            L.spec_debug_light_exp2.argtypes = [vp, vp, i64, vp]
             L.spec_debug_time_next_stats.restype = ctypes.c_int
             L.spec_debug_time_next_stats.argtypes = [vp, vp]
             if L.spec_abi_version() != 1:
@@ -309,3 +311,11 @@ def spec_debug_time_next_stats(start_event=None, stop_event=None) -> int:
     a = None if start_event is None else start_event.cuda_event
     b = None if stop_event is None else stop_event.cuda_event
     return lib().spec_debug_time_next_stats(a, b)
+
+
+def spec_debug_light_exp2(x, y, stream=None) -> int:
+    """The sampler's light-weight 2^x for every element of x, as (value,
+    correction) pairs in y (float32 CUDA tensors, y has 2 * len(x) entries)."""
+    _check_dev(x, "x")
+    _check_dev(y, "y")
+    return lib().spec_debug_light_exp2(_ptr(x), _ptr(y), int(x.numel()), _stream(stream))

@@ -200,12 +200,17 @@ SPEC_API spec_status_t spec_verify_sample(const spec_verify_args_t* a, spec_stre
     sp.tdt = p.tdt;
     sp.ddt = p.ddt;
     sp.V = p.V;
-    sp.nsplit = sampler_nsplit(dev, p.B, p.V);
+    const int64_t et = esize(p.tdt), ed = esize(p.ddt);
+    sp.nsplit = sampler_nsplit(dev, p.B, p.V, et + ed);
     const int64_t per = (p.V + sp.nsplit - 1) / sp.nsplit;
     sp.vchunk = (per + kTile - 1) / kTile * kTile;
+    const int64_t row_bytes = (sp.vchunk * (et > ed ? et : ed) + 15) / 16 * 16;
+    sp.stage_bytes = (2 * row_bytes <= (int64_t)kSampStageMax) ? (uint32_t)row_bytes : 0u;
     sp.tasks_in = p.tasks;
     sp.tasks = p.tasks;
     sp.out_tokens = p.out_tokens;
+    sp.seq_status = p.seq_status;
+    sp.err = (uint32_t*)((char*)a->workspace + kErrWordOffset);
     if (launch_sampler(sp, p.B, s, true) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
@@ -266,6 +271,12 @@ SPEC_API spec_status_t spec_debug_probs(const spec_verify_args_t* a, int32_t seq
     if (seq < 0 || seq >= a->batch || pos < 0 || pos > a->gamma_max) return SPEC_ERR_INVALID_ARG;
     if (launch_debug_probs(p, seq, pos, out_p, out_q, out_w, out_scalars, (cudaStream_t)stream) != cudaSuccess)
         return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+SPEC_API spec_status_t spec_debug_light_exp2(const float* x, float* y, int64_t n, spec_stream_t stream) {
+    if (!x || !y || n < 1 || !aligned(x, 4) || !aligned(y, 4)) return SPEC_ERR_INVALID_ARG;
+    if (launch_debug_light_exp2(x, y, n, (cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
 

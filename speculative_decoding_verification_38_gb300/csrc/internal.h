@@ -12,15 +12,18 @@
 namespace specv {
 
 constexpr int kStatsThreads = 512;    // threads per CTA of the streaming pass
-constexpr int kSampThreads = 512;     // threads per CTA of the residual sampler
-constexpr int kTile = 256;            // sampler tile: 32 lanes x 8 contiguous elements
-constexpr int kMaxTilesPerCta = 4096; // sampler smem bound: V <= 8 * 4096 * 256
+constexpr int kSampThreads = 256;     // threads per CTA of the residual sampler
+constexpr int kTile = 1024;           // sampler tile: 32 lanes x 32 contiguous columns
+constexpr int kMaxTilesPerCta = 1024; // sampler smem bound: V <= 8 * 1024 * 1024
 constexpr int kMaxCluster = 8;        // portable cluster size
 constexpr int64_t kChunkAlign = 64;   // elements; keeps 16-byte alignment for both dtypes
 constexpr int64_t kMinChunk = 1024;   // smallest slice one CTA streams
 constexpr int kGridCap = 4096;        // most CTAs of one streaming pass
 constexpr int kMaxBatch = 65536;      // arrival counters in the workspace header
-constexpr size_t kHeaderBytes = (size_t)kMaxBatch * 4;
+constexpr size_t kHeaderBytes = (size_t)kMaxBatch * 4 + 256;  // arrival counters + error words
+constexpr size_t kErrWordOffset = (size_t)kMaxBatch * 4;        // device error flags (bit 0: a wait timed out)
+constexpr int kSeqTimeout = 6;                                   // per-sequence status after a timed-out wait
+constexpr size_t kSampStageMax = 112 * 1024;                     // staged row-pair chunk per sampler CTA
 constexpr int64_t kMaxVocab = (int64_t)kMaxCluster * kMaxTilesPerCta * kTile;
 
 enum TaskMode : int32_t { kTaskNone = 0, kTaskResidual = 1, kTaskBonus = 2 };
@@ -77,11 +80,14 @@ struct SampleParams {
     const void* dft;
     int32_t tdt, ddt;
     int64_t V;
-    int32_t nsplit;   // CTAs per sequence (cluster size)
-    int64_t vchunk;   // elements per CTA, multiple of kTile
+    int32_t nsplit;        // CTAs per sequence (cluster size)
+    int64_t vchunk;        // elements per CTA, multiple of kTile
+    uint32_t stage_bytes;  // shared memory per staged row chunk (0: read rows directly)
     const SampleTask* tasks_in;
     SampleTask* tasks;
     int32_t* out_tokens;
+    int32_t* seq_status;   // may be null
+    uint32_t* err;         // workspace error word
 };
 
 struct Layout {
@@ -97,7 +103,7 @@ Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int gre
 cudaError_t launch_stats(const StatsParams& p, cudaStream_t s);
 int stats_resident_ctas(int device, int greedy);  // CTAs that fit at once on the device
 cudaError_t launch_sampler(const SampleParams& p, int32_t B, cudaStream_t s, bool pdl);
-int sampler_nsplit(int device, int64_t B, int64_t V);
+int sampler_nsplit(int device, int64_t B, int64_t V, int64_t pair_bytes);
 cudaError_t launch_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,
                                const int32_t* gammas, int32_t gmax, int32_t B, int32_t block_size,
                                int32_t* out_blocks, int32_t* seq_status, cudaStream_t s);
@@ -105,6 +111,7 @@ cudaError_t launch_debug_philox(uint64_t seed, uint64_t round, uint32_t seq_offs
                                 float* out, cudaStream_t s);
 cudaError_t launch_debug_probs(const StatsParams& p, int32_t seq, int32_t pos, float* out_p, float* out_q,
                                float* out_w, float* out_scalars, cudaStream_t s);
+cudaError_t launch_debug_light_exp2(const float* x, float* y, int64_t n, cudaStream_t s);
 cudaError_t launch_debug_rowstats(const float2* row_stats, int64_t rows, int greedy, float* out_a, float* out_b,
                                   int32_t* out_idx, cudaStream_t s);
 

@@ -39,6 +39,15 @@ __global__ void debug_philox_kernel(uint64_t seed, uint64_t round, uint32_t seq_
     out[2 * i + 1] = u.y;
 }
 
+__global__ void debug_light_exp2_kernel(const float* x, float* y, int64_t n) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) {
+        const df w = light_sum_df(light_exp2(x[i]), kEx2LightBias);
+        y[2 * i] = w.hi;
+        y[2 * i + 1] = w.lo;
+    }
+}
+
 __global__ void debug_rowstats_kernel(const float2* rs, int64_t rows, int greedy, float* a, float* bb,
                                       int32_t* idx) {
     const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -156,6 +165,12 @@ cudaError_t launch_debug_philox(uint64_t seed, uint64_t round, uint32_t seq_offs
     const int64_t n = (int64_t)B * npos;
     const int th = 256;
     debug_philox_kernel<<<(unsigned)((n + th - 1) / th), th, 0, s>>>(seed, round, seq_offset, B, npos, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_debug_light_exp2(const float* x, float* y, int64_t n, cudaStream_t s) {
+    const int th = 256;
+    debug_light_exp2_kernel<<<(unsigned)((n + th - 1) / th), th, 0, s>>>(x, y, n);
     return cudaGetLastError();
 }
 

@@ -11,12 +11,14 @@
 // no index, the last one with positive weight is taken.
 //
 // Only the selected row pair is re-read. Each sequence gets one thread-block
-// cluster of nsplit CTAs, CTA c owning a contiguous column chunk:
-//   pass A (residual only): the exact normalisers S_p = sum_j 2^((l_j - l_max) k)
+// cluster of nsplit CTAs, CTA c owning a contiguous column chunk, which it
+// stages into shared memory with one TMA bulk copy per row (rows whose chunk
+// is not 16-byte aligned are read from global memory instead). Then:
+//   pass A (residual only): the exact normalisers S = sum_j 2^((l_j - l_max) k)
 //     of both rows, reduced over the cluster through distributed shared memory;
 //   pass B: the weights r_j (= max(0, p_j - q_j), or p_j's weight for a bonus)
-//     tile by tile (a tile = 32 lanes x 8 consecutive columns), each tile's sum
-//     kept in shared memory; chunk sums are exchanged across the cluster so
+//     tile by tile (a tile = 32 lanes x 32 consecutive columns), each tile's
+//     sum kept in shared memory; chunk sums are exchanged across the cluster so
 //     every CTA knows Z and where its chunk starts in the CDF;
 //   the CTA whose interval holds u * Z finds the tile with one warp-wide
 //   prefix over its tile sums and rescans that tile to find the column.
@@ -38,21 +40,61 @@ struct SampSmem {
     df norm_t[kMaxCluster], norm_d[kMaxCluster];
     df zc[kMaxCluster], zc2[kMaxCluster];
     df red_t[kWarps], red_d[kWarps];
+    float okflag[kMaxCluster];
+    uint64_t bar;
     int32_t sel_tile;
     df sel_base;
 };
 
-// Eight consecutive columns c..c+7 of a row as floats; columns at or past
-// `lim` read as -inf (weight 0).
+// One row's chunk: column j (0-based within the chunk) lives in shared memory
+// at s + j * esz when staged, else in global memory at g + j * esz.
+struct Src {
+    const char* g;
+    uint32_t s;
+    int64_t n;  // columns in the chunk
+    bool staged, al;
+};
+
 template <int DT>
-__device__ __forceinline__ void load8(const char* row, int64_t c, int64_t lim, bool aligned, float (&v)[8]) {
-    if (aligned && c + 8 <= lim) {
+__device__ __forceinline__ float src_elem(const Src& r, int64_t j) {
+    if (r.staged) {
         if constexpr (DT == SPECV_BF16) {
-            uint4 q = ld_stream_v4(row + c * 2);
+            unsigned short h;
+            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(r.s + (uint32_t)(j * 2)));
+            return __uint_as_float(((uint32_t)h) << 16);
+        } else {
+            float f;
+            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(f) : "r"(r.s + (uint32_t)(j * 4)));
+            return f;
+        }
+    }
+    return ld_elem<DT>(r.g, j);
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+// Columns j..j+7 of a chunk as floats; columns past the chunk read as -inf
+// (weight 0). j is a multiple of 8.
+template <int DT>
+__device__ __forceinline__ void src_load8(const Src& r, int64_t j, float (&v)[8]) {
+    if (j + 8 <= r.n && (r.staged || r.al)) {
+        if constexpr (DT == SPECV_BF16) {
+            const uint4 q = r.staged ? lds_v4(r.s + (uint32_t)(j * 2)) : ld_stream_v4(r.g + j * 2);
             v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
             v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
         } else {
-            uint4 q0 = ld_stream_v4(row + c * 4), q1 = ld_stream_v4(row + c * 4 + 16);
+            uint4 q0, q1;
+            if (r.staged) {
+                q0 = lds_v4(r.s + (uint32_t)(j * 4));
+                q1 = lds_v4(r.s + (uint32_t)(j * 4 + 16));
+            } else {
+                q0 = ld_stream_v4(r.g + j * 4);
+                q1 = ld_stream_v4(r.g + j * 4 + 16);
+            }
             v[0] = __uint_as_float(q0.x); v[1] = __uint_as_float(q0.y);
             v[2] = __uint_as_float(q0.z); v[3] = __uint_as_float(q0.w);
             v[4] = __uint_as_float(q1.x); v[5] = __uint_as_float(q1.y);
@@ -60,16 +102,14 @@ __device__ __forceinline__ void load8(const char* row, int64_t c, int64_t lim, b
         }
     } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = (c + e < lim) ? ld_elem<DT>(row, c + e) : -INFINITY;
+        for (int e = 0; e < 8; ++e) v[e] = (j + e < r.n) ? src_elem<DT>(r, j + e) : -INFINITY;
     }
 }
 
 template <int TDT, int DDT>
 struct RowPair {
-    const char* trow;
-    const char* drow;
-    bool tal, dal, probs;
-    int64_t lim;
+    Src t, d;
+    bool probs;
     float mt, md;  // raw row maxima
     df k;
 
@@ -82,21 +122,59 @@ struct RowPair {
     }
 };
 
-// Weights of the 8 columns c..c+7 of this lane: residual, or p's weight only.
+// A weight is "heavy" when it carries a low part (double-float path) or is
+// large enough that one rounding would matter; light ones are summed in fp32
+// over a short run before joining a double-float sum.
+__device__ __forceinline__ bool is_heavy(df w) { return w.lo != 0.f || w.hi > 1.220703125e-4f; }
+
+// Weights of the 8 chunk columns j..j+7: residual, or p's weight only.
 template <int TDT, int DDT>
-__device__ __forceinline__ void lane_weights(const RowPair<TDT, DDT>& rp, int64_t c, int mode, df It, df Id,
-                                             const Exp2Table& tab, df (&w)[8]) {
+__device__ __forceinline__ void weights8(const RowPair<TDT, DDT>& rp, int64_t j, int mode, df It, df Id,
+                                         const Exp2Table& tab, df (&w)[8]) {
     float lt[8];
-    load8<TDT>(rp.trow, c, rp.lim, rp.tal, lt);
+    src_load8<TDT>(rp.t, j, lt);
     if (mode == kTaskResidual) {
         float ld[8];
-        load8<DDT>(rp.drow, c, rp.lim, rp.dal, ld);
+        src_load8<DDT>(rp.d, j, ld);
 #pragma unroll
         for (int e = 0; e < 8; ++e) w[e] = resid_weight(rp.wt(lt[e], tab), rp.wd(ld[e], tab), It, Id);
     } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e) w[e] = rp.wt(lt[e], tab);
     }
+}
+
+// Tiles are kTile = kGroups x 256 columns; in group g, lane l owns the 8
+// consecutive columns g*256 + l*8 .. +7, so each warp-wide 16-byte load covers
+// 512 contiguous bytes (no shared-memory bank conflicts).
+constexpr int kGroups = kTile / 256;
+
+// Accumulate 8 weights: heavy ones into a double-float sum, light ones into
+// an fp32 sum (corrected by `cl` when the sum joins double-float arithmetic).
+__device__ __forceinline__ void acc8(const df (&w)[8], float& light, df& heavy) {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        if (is_heavy(w[e]))
+            acc_add(heavy, w[e]);
+        else
+            light = __fadd_rn(light, w[e].hi);
+    }
+}
+
+// This lane's share of a tile: the sum of its kGroups runs of 8 columns.
+template <int TDT, int DDT>
+__device__ __forceinline__ df lane_tile_sum(const RowPair<TDT, DDT>& rp, int64_t tile_j, int mode, df It, df Id,
+                                            float cl, const Exp2Table& tab) {
+    const int lane = threadIdx.x & 31;
+    float light = 0.f;
+    df heavy{0.f, 0.f};
+#pragma unroll 1
+    for (int g = 0; g < kGroups; ++g) {
+        df w[8];
+        weights8(rp, tile_j + g * 256 + lane * 8, mode, It, Id, tab, w);
+        acc8(w, light, heavy);
+    }
+    return df_add(df_norm(heavy), light_sum_df(light, cl));
 }
 
 // Inclusive warp scan of double-float values (Hillis-Steele).
@@ -116,28 +194,26 @@ __device__ __forceinline__ df warp_sum_df(df x) {
     return x;
 }
 
-// Total of a lane's 8 weights.
-__device__ __forceinline__ df lane_total(const df (&w)[8]) {
-    df acc{0.f, 0.f};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) acc_add(acc, w[e]);
-    return df_norm(acc);
-}
-
 // Pass A: exact normalisers of both rows over this CTA's chunk (block sums,
-// valid in warp 0).
+// valid in warp 0). Light weights are summed in fp32 per group of 8 columns.
 template <int TDT, int DDT>
-__device__ void chunk_norms(const RowPair<TDT, DDT>& rp, int64_t cs, int64_t ce, SampSmem& sm, df& St, df& Sd) {
+__device__ void chunk_norms(const RowPair<TDT, DDT>& rp, int64_t n, SampSmem& sm, df& St, df& Sd) {
     df at{0.f, 0.f}, ad{0.f, 0.f};
-    for (int64_t c = cs + (int64_t)threadIdx.x * 8; c < ce; c += (int64_t)blockDim.x * 8) {
+    const int64_t step = (int64_t)blockDim.x * 8;
+#pragma unroll 1
+    for (int64_t j = (int64_t)threadIdx.x * 8; j < n; j += step) {
         float lt[8], ld[8];
-        load8<TDT>(rp.trow, c, rp.lim, rp.tal, lt);
-        load8<DDT>(rp.drow, c, rp.lim, rp.dal, ld);
+        src_load8<TDT>(rp.t, j, lt);
+        src_load8<DDT>(rp.d, j, ld);
+        float gt = 0.f, gd = 0.f;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            acc_add(at, rp.wt(lt[e], sm.tab));
-            acc_add(ad, rp.wd(ld[e], sm.tab));
+            const df a = rp.wt(lt[e], sm.tab), b = rp.wd(ld[e], sm.tab);
+            if (is_heavy(a)) acc_add(at, a); else gt = __fadd_rn(gt, a.hi);
+            if (is_heavy(b)) acc_add(ad, b); else gd = __fadd_rn(gd, b.hi);
         }
+        acc_add(at, light_sum_df(gt, kEx2LightBias));
+        acc_add(ad, light_sum_df(gd, rp.probs ? 0.f : kEx2LightBias));
     }
     at = warp_sum_df(df_norm(at));
     ad = warp_sum_df(df_norm(ad));
@@ -159,14 +235,12 @@ __device__ void chunk_norms(const RowPair<TDT, DDT>& rp, int64_t cs, int64_t ce,
 
 // Pass B: tile sums in index order into smem; returns the chunk total (warp 0).
 template <int TDT, int DDT>
-__device__ df chunk_tiles(const RowPair<TDT, DDT>& rp, int64_t cs, int ntiles, int mode, df It, df Id,
+__device__ df chunk_tiles(const RowPair<TDT, DDT>& rp, int ntiles, int mode, df It, df Id, float cl,
                           SampSmem& sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int ti = warp; ti < ntiles; ti += kWarps) {
-        df w[8];
-        lane_weights(rp, cs + (int64_t)ti * kTile + lane * 8, mode, It, Id, sm.tab, w);
-        const df incl = warp_scan_df(lane_total(w));
-        if (lane == 31) sm.tile_sum[ti] = incl;
+        const df tot = warp_sum_df(lane_tile_sum(rp, (int64_t)ti * kTile, mode, It, Id, cl, sm.tab));
+        if (lane == 0) sm.tile_sum[ti] = tot;
     }
     __syncthreads();
     df z{0.f, 0.f};
@@ -175,6 +249,57 @@ __device__ df chunk_tiles(const RowPair<TDT, DDT>& rp, int64_t cs, int ntiles, i
         z = warp_sum_df(z);
     }
     return z;
+}
+
+// One warp walks the selected tile in index order from CDF position `base`
+// and returns the first chunk column whose running sum exceeds thr (or, if
+// rounding leaves none, the last column with weight; -1 if the tile has none).
+template <int TDT, int DDT>
+__device__ int64_t rescan_tile(const RowPair<TDT, DDT>& rp, int64_t tile_j, int mode, df It, df Id, float cl,
+                               df base, df thr, const Exp2Table& tab) {
+    const int lane = threadIdx.x & 31;
+    df run = base;
+    int64_t last = -1;
+#pragma unroll 1
+    for (int g = 0; g < kGroups; ++g) {
+        df w[8];
+        const int64_t j0 = tile_j + g * 256 + lane * 8;
+        weights8(rp, j0, mode, It, Id, tab, w);
+        // this lane's prefix at each of its 8 columns, then the warp-wide prefix
+        df pre[8];
+        float light = 0.f;
+        df heavy{0.f, 0.f};
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            if (is_heavy(w[e]))
+                acc_add(heavy, w[e]);
+            else
+                light = __fadd_rn(light, w[e].hi);
+            pre[e] = df_add(df_norm(heavy), light_sum_df(light, cl));
+        }
+        const df incl = warp_scan_df(pre[7]);
+        df excl = shfl_up_df(incl, 1);
+        if (lane == 0) excl = df{0.f, 0.f};
+        const df start = df_add(run, excl);
+        int hit = -1, lp = -1;
+#pragma unroll
+        for (int e = 7; e >= 0; --e) {
+            if (df_gt(df_add(start, pre[e]), thr)) hit = e;
+            if (lp < 0 && df_pos(w[e])) lp = e;
+        }
+        const unsigned hm = __ballot_sync(0xffffffffu, hit >= 0);
+        if (hm) {
+            const int src = __ffs(hm) - 1;
+            return tile_j + g * 256 + src * 8 + __shfl_sync(0xffffffffu, hit, src);
+        }
+        const unsigned pm = __ballot_sync(0xffffffffu, lp >= 0);
+        if (pm) {
+            const int src = 31 - __clz(pm);
+            last = tile_j + g * 256 + src * 8 + __shfl_sync(0xffffffffu, lp, src);
+        }
+        run = df_add(run, shfl_df(incl, 31));
+    }
+    return last;
 }
 
 // Publish thread 0's value into slot c of every CTA in the cluster.
@@ -187,9 +312,20 @@ __device__ __forceinline__ void cluster_publish(df* slots, uint32_t c, int ns, d
     cluster_sync_all();
 }
 
+// Stage one row chunk (n columns of esz bytes at g) into shared memory at s:
+// a bulk copy of the 16-byte aligned body (thread 0), plain loads for the
+// short tail.
+__device__ __forceinline__ void stage_row(const char* g, char* s, int64_t n, int esz, uint64_t* bar) {
+    const uint32_t bytes = (uint32_t)(n * esz);
+    const uint32_t body = bytes & ~15u;
+    if (threadIdx.x == 0 && body) bulk_g2s(s, g, body, bar);
+    for (uint32_t b = body + threadIdx.x; b < bytes; b += blockDim.x) s[b] = __ldg(g + b);
+}
+
 template <int TDT, int DDT>
 __global__ void __launch_bounds__(kSampThreads) sampler_kernel(SampleParams p) {
     __shared__ SampSmem sm;
+    extern __shared__ __align__(128) char dyn[];
     pdl_wait_primary();  // tasks are written by the streaming pass
 
     const int32_t b = blockIdx.x / p.nsplit;
@@ -200,25 +336,62 @@ __global__ void __launch_bounds__(kSampThreads) sampler_kernel(SampleParams p) {
 
     const int64_t cs = (int64_t)c * p.vchunk;
     const int64_t ce = min(p.V, cs + p.vchunk);
-    const int ntiles = ce > cs ? (int)((ce - cs + kTile - 1) / kTile) : 0;
+    const int64_t n = ce > cs ? ce - cs : 0;
+    const int ntiles = (int)((n + kTile - 1) / kTile);
     constexpr int te = TDT == SPECV_F32 ? 4 : 2, de = DDT == SPECV_F32 ? 4 : 2;
+    const bool resid0 = t.mode == kTaskResidual;
     RowPair<TDT, DDT> rp;
-    rp.trow = (const char*)p.tgt + t.trow * p.V * te;
-    rp.drow = t.drow >= 0 ? (const char*)p.dft + t.drow * p.V * de : rp.trow;
-    rp.tal = ((uintptr_t)rp.trow & 15u) == 0;
-    rp.dal = ((uintptr_t)rp.drow & 15u) == 0;
-    rp.lim = ce;
+    rp.t.g = (const char*)p.tgt + (t.trow * p.V + cs) * te;
+    rp.d.g = resid0 ? (const char*)p.dft + (t.drow * p.V + cs) * de : rp.t.g;
+    rp.t.n = rp.d.n = n;
+    rp.t.al = ((uintptr_t)rp.t.g & 15u) == 0;
+    rp.d.al = ((uintptr_t)rp.d.g & 15u) == 0;
+    rp.t.staged = p.stage_bytes > 0 && rp.t.al && n * te <= (int64_t)p.stage_bytes;
+    rp.d.staged = resid0 && p.stage_bytes > 0 && rp.d.al && n * de <= (int64_t)p.stage_bytes;
+    rp.t.s = smem_addr(dyn);
+    rp.d.s = smem_addr(dyn + p.stage_bytes);
     rp.probs = t.probs != 0;
     rp.mt = t.mt;
     rp.md = t.md;
     rp.k = df{t.k_hi, t.k_lo};
-    __syncthreads();  // exp2 table ready
+
+    // stage the chunk of both rows into shared memory
+    bool ok = true;
+    if (rp.t.staged || rp.d.staged) {
+        if (threadIdx.x == 0) {
+            mbar_init(&sm.bar, 1);
+            fence_barrier_init();
+        }
+        __syncthreads();
+        const uint32_t tb = rp.t.staged ? (uint32_t)(n * te) & ~15u : 0u;
+        const uint32_t db = rp.d.staged ? (uint32_t)(n * de) & ~15u : 0u;
+        if (threadIdx.x == 0) mbar_arrive_expect_tx(&sm.bar, tb + db);
+        if (rp.t.staged) stage_row(rp.t.g, dyn, n, te, &sm.bar);
+        if (rp.d.staged) stage_row(rp.d.g, dyn + p.stage_bytes, n, de, &sm.bar);
+        if (!mbar_wait_bounded(&sm.bar, 0, kWaitLimit)) {
+            ok = false;
+            mbar_wait_bounded(&sm.bar, 0, kWaitLimit);  // let copies in flight land before leaving
+        }
+    }
+    ok = __syncthreads_and(ok);  // also publishes the plain-load tails
+    if (threadIdx.x == 0)
+        for (int r = 0; r < p.nsplit; ++r) st_cluster_f32(&sm.okflag[c], r, ok ? 1.f : 0.f);
+    cluster_sync_all();
+    bool all_ok = true;
+    for (int r = 0; r < p.nsplit; ++r) all_ok = all_ok && sm.okflag[r] > 0.f;
+    if (!all_ok) {  // the whole cluster gives up together
+        if (c == 0 && threadIdx.x == 0) {
+            atomicOr(p.err, 1u);
+            if (p.seq_status) p.seq_status[b] = kSeqTimeout;
+        }
+        return;
+    }
 
     int mode = t.mode;
     df It{1.f, 0.f}, Id{1.f, 0.f};
     if (mode == kTaskResidual) {
         df St, Sd;
-        chunk_norms(rp, cs, ce, sm, St, Sd);
+        chunk_norms(rp, n, sm, St, Sd);
         cluster_publish(sm.norm_t, c, p.nsplit, St);
         cluster_publish(sm.norm_d, c, p.nsplit, Sd);
         df Tt{0.f, 0.f}, Td{0.f, 0.f};
@@ -236,7 +409,10 @@ __global__ void __launch_bounds__(kSampThreads) sampler_kernel(SampleParams p) {
         }
     }
 
-    df zc = chunk_tiles(rp, cs, ntiles, mode, It, Id, sm);
+    // light-sum correction of the sampling weights: both rows' light weights
+    // carry the same SFU bias unless the draft is given as probabilities
+    float cl = (mode == kTaskResidual && rp.probs) ? 0.f : kEx2LightBias;
+    df zc = chunk_tiles(rp, ntiles, mode, It, Id, cl, sm);
     cluster_publish(sm.zc, c, p.nsplit, zc);
     const df* zs = sm.zc;
     df Z{0.f, 0.f}, lo{0.f, 0.f};
@@ -247,8 +423,9 @@ __global__ void __launch_bounds__(kSampThreads) sampler_kernel(SampleParams p) {
     if (mode == kTaskResidual && !df_pos(Z)) {
         // p_i == q_i to rounding: draw from p_i instead
         mode = kTaskBonus;
+        cl = kEx2LightBias;
         __syncthreads();
-        zc = chunk_tiles(rp, cs, ntiles, mode, It, Id, sm);
+        zc = chunk_tiles(rp, ntiles, mode, It, Id, cl, sm);
         cluster_publish(sm.zc2, c, p.nsplit, zc);
         zs = sm.zc2;
         Z = df{0.f, 0.f};
@@ -315,49 +492,24 @@ __global__ void __launch_bounds__(kSampThreads) sampler_kernel(SampleParams p) {
 
     // one warp rescans the selected tile in index order
     const int lane = threadIdx.x;
-    const int64_t col0 = cs + (int64_t)sm.sel_tile * kTile + lane * 8;
-    df w[8];
-    lane_weights(rp, col0, mode, It, Id, sm.tab, w);
-    df cum[8];
-    df acc{0.f, 0.f};
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        acc_add(acc, w[e]);
-        cum[e] = df_norm(acc);
-    }
-    const df incl = warp_scan_df(cum[7]);
-    df excl = shfl_up_df(incl, 1);
-    if (lane == 0) excl = df{0.f, 0.f};
-    const df base = sm.sel_base;
-    int hit = -1, lastpos = -1;
-#pragma unroll
-    for (int e = 7; e >= 0; --e) {
-        if (df_gt(df_add(base, df_add(excl, cum[e])), thr)) hit = e;
-        if (lastpos < 0 && df_pos(w[e])) lastpos = e;
-    }
-    const unsigned hm = __ballot_sync(0xffffffffu, hit >= 0);
-    int64_t tok = -1;
-    if (hm) {
-        const int src = __ffs(hm) - 1;
-        const int e = __shfl_sync(0xffffffffu, hit, src);
-        tok = cs + (int64_t)sm.sel_tile * kTile + src * 8 + e;
-    } else {
-        const unsigned pm = __ballot_sync(0xffffffffu, lastpos >= 0);
-        if (pm) {
-            const int src = 31 - __clz(pm);
-            const int e = __shfl_sync(0xffffffffu, lastpos, src);
-            tok = cs + (int64_t)sm.sel_tile * kTile + src * 8 + e;
-        }
-    }
+    const int64_t jt = rescan_tile(rp, (int64_t)sm.sel_tile * kTile, mode, It, Id, cl, sm.sel_base, thr, sm.tab);
+    const int64_t tok = jt >= 0 ? cs + jt : -1;
     if (lane == 0 && tok >= 0) p.out_tokens[t.out_slot] = (int32_t)tok;
 }
 
 template <int TDT, int DDT>
 cudaError_t launch_typed(const SampleParams& p, int32_t B, cudaStream_t s, bool pdl) {
+    static bool attr_done = false;  // per instantiation
+    if (!attr_done) {
+        cudaError_t e = cudaFuncSetAttribute(sampler_kernel<TDT, DDT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kSampStageMax);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(B * p.nsplit));
     cfg.blockDim = dim3(kSampThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = 2 * (size_t)p.stage_bytes;
     cfg.stream = s;
     cudaLaunchAttribute attrs[2];
     int na = 0;
@@ -378,12 +530,17 @@ cudaError_t launch_typed(const SampleParams& p, int32_t B, cudaStream_t s, bool 
 
 }  // namespace
 
-int sampler_nsplit(int device, int64_t B, int64_t V) {
+// CTAs per sequence: enough CTAs to fill the GPU a few times over, chunks of
+// at least 4096 columns, and (when possible) a row-pair chunk that fits the
+// shared-memory staging budget.
+int sampler_nsplit(int device, int64_t B, int64_t V, int64_t pair_bytes) {
     int sms = 152;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
     int64_t n = (4 * (int64_t)sms + B - 1) / B;
-    const int64_t by_v = V / 4096;  // keep chunks of at least 4096 columns
+    const int64_t by_v = V / 4096;
     if (n > by_v) n = by_v;
+    const int64_t fit = (V * pair_bytes + (int64_t)kSampStageMax - 1) / (int64_t)kSampStageMax;
+    if (n < fit && fit <= kMaxCluster && V / fit >= 1024) n = fit;
     const int64_t need = (V + (int64_t)kMaxTilesPerCta * kTile - 1) / ((int64_t)kMaxTilesPerCta * kTile);
     if (n < need) n = need;
     if (n < 1) n = 1;

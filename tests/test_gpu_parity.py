@@ -394,3 +394,21 @@ def test_gpu_mean_tokens_known_alpha(sv, alpha, gamma):
     E = (1 - alpha ** (gamma + 1)) / (1 - alpha)
     assert abs(emitted.mean() - E) / E < 0.01
     assert emitted.min() >= 1 and emitted.max() <= gamma + 1
+
+
+def test_light_exp2_is_unbiased(sv):
+    """The sampler's light 2^x (exponents in [-45, -13]) as its sums see it
+    (SFU value plus the sum-level correction) against exact 2^x: mean relative
+    error below 3e-9; each SFU value within 3e-7."""
+    import torch
+
+    rng = np.random.default_rng(12)
+    x = rng.uniform(-45.0, -13.0, 1 << 22).astype(np.float32)
+    xt = torch.from_numpy(x).cuda()
+    yt = torch.empty(2 * x.shape[0], dtype=torch.float32, device="cuda")
+    sv.check(sv.spec_debug_light_exp2(xt, yt), "light_exp2")
+    y = yt.cpu().numpy().astype(np.float64).reshape(-1, 2)
+    ex = np.exp2(x.astype(np.float64))
+    assert np.abs((y[:, 0] - ex) / ex).max() < 3e-7
+    rel = (y[:, 0] + y[:, 1] - ex) / ex
+    assert abs(rel.mean()) < 3e-9, rel.mean()
