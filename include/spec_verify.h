@@ -114,7 +114,7 @@ enum {
 typedef struct {
     uint32_t struct_size; /* sizeof(spec_verify_args_t), for ABI checks */
     int32_t batch;        /* 1 <= B <= 65536 */
-    int32_t vocab;        /* 1 <= V <= 8388608 (larger: SPEC_ERR_UNSUPPORTED) */
+    int32_t vocab;        /* 1 <= V <= 2097152 (larger: SPEC_ERR_UNSUPPORTED) */
     int32_t gamma_max;    /* 0 <= gamma_max <= 64 (larger: SPEC_ERR_UNSUPPORTED) */
     int64_t rows_target;  /* sum_b (gamma_b + 1) */
     int64_t rows_draft;   /* sum_b gamma_b */

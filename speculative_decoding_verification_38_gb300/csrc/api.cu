@@ -16,6 +16,7 @@ struct DeviceInfo {
     bool ready = false;
     int resident_sample = 0;
     int resident_greedy = 0;
+    int sms = 0;
 };
 std::mutex g_mu;
 DeviceInfo g_dev[64];
@@ -28,6 +29,7 @@ bool device_info(int& dev, DeviceInfo& out) {
     if (!d.ready) {
         d.resident_sample = stats_resident_ctas(dev, 0);
         d.resident_greedy = stats_resident_ctas(dev, 1);
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
         if (d.resident_sample <= 0 || d.resident_greedy <= 0) return false;
         d.ready = true;
     }
@@ -101,8 +103,23 @@ spec_status_t check_call(const spec_verify_args_t* a, int greedy) {
     return SPEC_OK;
 }
 
-bool build_params(const spec_verify_args_t* a, int greedy, int grid_cap, StatsParams& p, Layout& L) {
-    L = make_layout(a->batch, a->vocab, a->rows_target, a->rows_draft, greedy, grid_cap);
+#ifndef SPECV_STREAM_TMA
+#define SPECV_STREAM_TMA 1  // build-time choice: 0 always runs the plain-load streaming pass
+#endif
+
+// The TMA-pipelined streaming pass needs every row to start on a 16-byte
+// boundary (bulk copies); otherwise the plain-load variant runs.
+bool tma_ok(const spec_verify_args_t* a, int greedy) {
+    const size_t V = (size_t)a->vocab;
+    if (!aligned(a->target_logits, 16) || (V * esize(a->target_dtype)) % 16 != 0) return false;
+    if (!greedy && a->rows_draft > 0 && (!aligned(a->draft, 16) || (V * esize(a->draft_dtype)) % 16 != 0))
+        return false;
+    return true;
+}
+
+bool build_params(const spec_verify_args_t* a, int greedy, int grid_cap, int tma, StatsParams& p, Layout& L) {
+    const int pw = tma ? kTmaConsumerWarps : 1;
+    L = make_layout(a->batch, a->vocab, a->rows_target, a->rows_draft, greedy, grid_cap, pw);
     if (a->workspace_bytes < L.total) return false;
     char* ws = (char*)a->workspace;
     p.tgt = a->target_logits;
@@ -117,6 +134,8 @@ bool build_params(const spec_verify_args_t* a, int greedy, int grid_cap, StatsPa
     p.N = L.N;
     p.chunk = L.chunk;
     p.S = L.S;
+    p.pw = pw;
+    p.tma = tma;
     p.B = a->batch;
     p.gmax = a->gamma_max;
     p.grid = L.grid;
@@ -137,6 +156,7 @@ bool build_params(const spec_verify_args_t* a, int greedy, int grid_cap, StatsPa
     p.out_accepted = a->out_accepted;
     p.seq_status = a->seq_status;
     p.counters = (uint32_t*)ws;
+    p.err = (uint32_t*)(ws + kErrWordOffset);
     p.partials = (float2*)(ws + L.off_partials);
     p.row_stats = (float2*)(ws + L.off_rowstats);
     p.pq = (float2*)(ws + L.off_pq);
@@ -149,9 +169,10 @@ spec_status_t prepare(const spec_verify_args_t* a, int greedy, StatsParams& p, L
     if (st) return st;
     DeviceInfo di;
     if (!device_info(dev, di)) return SPEC_ERR_CUDA;
-    int cap = greedy ? di.resident_greedy : di.resident_sample;
+    const int tma = (SPECV_STREAM_TMA && tma_ok(a, greedy)) ? 1 : 0;
+    int cap = tma ? di.sms : (greedy ? di.resident_greedy : di.resident_sample);
     if (cap > kGridCap) cap = kGridCap;
-    if (!build_params(a, greedy, cap, p, L)) return SPEC_ERR_WORKSPACE;
+    if (!build_params(a, greedy, cap, tma, p, L)) return SPEC_ERR_WORKSPACE;
     return SPEC_OK;
 }
 
@@ -176,7 +197,8 @@ SPEC_API const char* spec_status_string(spec_status_t s) {
 SPEC_API size_t spec_verify_workspace_size(const spec_verify_args_t* a, int32_t greedy) {
     if (check_shape(a) != SPEC_OK) return 0;
     // the smallest slice any launch uses gives the most partial slots
-    Layout L = make_layout(a->batch, a->vocab, a->rows_target, a->rows_draft, greedy ? 1 : 0, kGridCap);
+    Layout L = make_layout(a->batch, a->vocab, a->rows_target, a->rows_draft, greedy ? 1 : 0, kGridCap,
+                           kTmaConsumerWarps);
     return L.total;
 }
 

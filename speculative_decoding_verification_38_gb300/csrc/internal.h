@@ -11,10 +11,24 @@
 
 namespace specv {
 
-constexpr int kStatsThreads = 512;    // threads per CTA of the streaming pass
+constexpr int kStatsThreads = 512;    // threads per CTA of the streaming pass (plain-load variant)
+#ifndef SPECV_WS_WARPS
+#define SPECV_WS_WARPS 16
+#endif
+#ifndef SPECV_WS_STAGES
+#define SPECV_WS_STAGES 2
+#endif
+#ifndef SPECV_WS_STAGE_BYTES
+#define SPECV_WS_STAGE_BYTES 6144
+#endif
+constexpr int kTmaConsumerWarps = SPECV_WS_WARPS;  // streaming pass, TMA variant: warps per CTA
+constexpr int kTmaThreads = kTmaConsumerWarps * 32;
+constexpr int kTmaStages = SPECV_WS_STAGES;          // stages in each warp's shared-memory ring
+constexpr uint32_t kTmaStageBytes = SPECV_WS_STAGE_BYTES;  // bytes per stage (a multiple of 512)
+static_assert(kTmaConsumerWarps * kTmaStages * kTmaStageBytes <= 200 * 1024, "warp rings exceed shared memory");
 constexpr int kSampThreads = 256;     // threads per CTA of the residual sampler
 constexpr int kTile = 1024;           // sampler tile: 32 lanes x 32 contiguous columns
-constexpr int kMaxTilesPerCta = 1024; // sampler smem bound: V <= 8 * 1024 * 1024
+constexpr int kMaxTilesPerCta = 256;  // sampler smem bound: V <= 8 * 256 * 1024
 constexpr int kMaxCluster = 8;        // portable cluster size
 constexpr int64_t kChunkAlign = 64;   // elements; keeps 16-byte alignment for both dtypes
 constexpr int64_t kMinChunk = 1024;   // smallest slice one CTA streams
@@ -50,7 +64,9 @@ struct StatsParams {
     const void* dft;
     int32_t tdt, ddt, probs, greedy;
     int64_t V, rows_t, rows_d, N, chunk;
-    int32_t S;  // partial slots per row
+    int32_t S;   // partial slots (CTA pieces) per row
+    int32_t pw;  // partials per slot (1: one per CTA piece; kTmaConsumerWarps: one per consumer warp)
+    int32_t tma; // 1: TMA-pipelined variant
     int32_t B, gmax, grid;
     const int64_t* tro;
     const int64_t* dro;
@@ -69,7 +85,8 @@ struct StatsParams {
     int32_t* seq_status;
     // workspace views
     uint32_t* counters;  // [B] self-resetting arrival counters
-    float2* partials;    // [rows_total * S]
+    uint32_t* err;       // device error word (bit 0: a bounded wait gave up)
+    float2* partials;    // [rows_total * S * pw]
     float2* row_stats;   // [rows_total] merged per-row statistics
     float2* pq;          // [rows_d] (p(x), q(x))
     SampleTask* tasks;   // [B]
@@ -98,10 +115,10 @@ struct Layout {
 
 // Work split and workspace layout for a given problem. grid_cap bounds the
 // number of streaming CTAs (the launch uses the device's resident capacity).
-Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int greedy, int64_t grid_cap);
+Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int greedy, int64_t grid_cap, int pw);
 
 cudaError_t launch_stats(const StatsParams& p, cudaStream_t s);
-int stats_resident_ctas(int device, int greedy);  // CTAs that fit at once on the device
+int stats_resident_ctas(int device, int greedy);  // CTAs that fit at once on the device (plain-load variant)
 cudaError_t launch_sampler(const SampleParams& p, int32_t B, cudaStream_t s, bool pdl);
 int sampler_nsplit(int device, int64_t B, int64_t V, int64_t pair_bytes);
 cudaError_t launch_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,

@@ -185,6 +185,27 @@ static __device__ __noinline__ df resid_weight_df(df a, df b, df It, df Id) {
     return df_pos(d) ? d : df{0.f, 0.f};
 }
 
+// Light-path weight 2^((l - lmax) k) as one float, and whether the weight is
+// heavy (then the float is not used: the caller evaluates it with
+// heavy_logit_weight). Branch-free: -inf logits clamp to a huge negative
+// exponent, whose 2^x is 0.
+template <bool FP32IN>
+__device__ __forceinline__ float light_weight(float l, float lmax, df k, bool& heavy) {
+    const float dh = fmaxf(__fsub_rn(l, lmax), -1e30f);
+    float lo = __fmul_rn(dh, k.lo);
+    if constexpr (FP32IN) lo = __fmaf_rn((dh > -1e30f) ? two_sum(l, -lmax).lo : 0.f, k.hi, lo);
+    const float x = __fmaf_rn(dh, k.hi, lo);
+    heavy = x > kHeavyExp;
+    return light_exp2(x);
+}
+
+// The double-float weight of a heavy logit.
+template <bool FP32IN>
+__device__ __forceinline__ df heavy_logit_weight(float l, float lmax, df k, const Exp2Table& tab) {
+    const float dh = __fsub_rn(l, lmax);
+    return heavy_weight(dh, FP32IN ? two_sum(l, -lmax).lo : 0.f, k, tab);
+}
+
 // Residual weight of one column: max(0, Wt * It - Wd * Id).
 __device__ __forceinline__ df resid_weight(df a, df b, df It, df Id) {
     if (a.lo == 0.f && b.lo == 0.f) {

@@ -33,6 +33,7 @@ namespace specv {
 namespace {
 
 constexpr int kWarps = kSampThreads / 32;
+constexpr int kQCap = 128;  // entries per warp queue (power of two)
 
 struct SampSmem {
     Exp2Table tab;
@@ -41,6 +42,7 @@ struct SampSmem {
     df zc[kMaxCluster], zc2[kMaxCluster];
     df red_t[kWarps], red_d[kWarps];
     float okflag[kMaxCluster];
+    int32_t q[kWarps][kQCap];  // per-warp queue of heavy items awaiting dense evaluation
     uint64_t bar;
     int32_t sel_tile;
     df sel_base;
@@ -149,32 +151,74 @@ __device__ __forceinline__ void weights8(const RowPair<TDT, DDT>& rp, int64_t j,
 // 512 contiguous bytes (no shared-memory bank conflicts).
 constexpr int kGroups = kTile / 256;
 
-// Accumulate 8 weights: heavy ones into a double-float sum, light ones into
-// an fp32 sum (corrected by `cl` when the sum joins double-float arithmetic).
-__device__ __forceinline__ void acc8(const df (&w)[8], float& light, df& heavy) {
-#pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        if (is_heavy(w[e]))
-            acc_add(heavy, w[e]);
-        else
-            light = __fadd_rn(light, w[e].hi);
-    }
+// Pass B item: the double-float sampling weight of chunk column j.
+template <int TDT, int DDT>
+__device__ __forceinline__ df tile_item(const RowPair<TDT, DDT>& rp, int64_t j, int mode, df It, df Id,
+                                        const Exp2Table& tab) {
+    const df wt = rp.wt(src_elem<TDT>(rp.t, j), tab);
+    if (mode != kTaskResidual) return wt;
+    return resid_weight_df(wt, rp.wd(src_elem<DDT>(rp.d, j), tab), It, Id);
 }
 
-// This lane's share of a tile: the sum of its kGroups runs of 8 columns.
+// This lane's share of a tile (its kGroups runs of 8 columns): light columns
+// summed in fp32, columns with a heavy weight queued and evaluated densely.
 template <int TDT, int DDT>
 __device__ __forceinline__ df lane_tile_sum(const RowPair<TDT, DDT>& rp, int64_t tile_j, int mode, df It, df Id,
-                                            float cl, const Exp2Table& tab) {
-    const int lane = threadIdx.x & 31;
+                                            float cl, SampSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int32_t* q = sm.q[warp];
+    uint32_t head = 0, tail = 0;
     float light = 0.f;
-    df heavy{0.f, 0.f};
+    df acc{0.f, 0.f};
+    const bool resid = mode == kTaskResidual;
 #pragma unroll 1
     for (int g = 0; g < kGroups; ++g) {
-        df w[8];
-        weights8(rp, tile_j + g * 256 + lane * 8, mode, It, Id, tab, w);
-        acc8(w, light, heavy);
+        const int64_t j = tile_j + g * 256 + lane * 8;
+        float lt[8], ld[8];
+        src_load8<TDT>(rp.t, j, lt);
+        if (resid) src_load8<DDT>(rp.d, j, ld);
+        uint32_t m = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            bool ht, hd = false;
+            const float wt = light_weight<TDT == SPECV_F32>(lt[e], rp.mt, rp.k, ht);
+            if (!resid) {
+                if (ht) m |= 1u << e; else light = __fadd_rn(light, wt);
+                continue;
+            }
+            float qv;
+            if (rp.probs) {
+                const float v = ld[e] > -INFINITY ? ld[e] : 0.f;
+                hd = v > 1.220703125e-4f;
+                qv = __fmaf_rn(v, Id.hi, __fmul_rn(v, Id.lo));
+            } else {
+                const float wd = light_weight<DDT == SPECV_F32>(ld[e], rp.md, rp.k, hd);
+                qv = __fmaf_rn(wd, Id.hi, __fmul_rn(wd, Id.lo));
+            }
+            if (ht || hd) {
+                m |= 1u << e;
+            } else {
+                const float r = __fsub_rn(__fmaf_rn(wt, It.hi, __fmul_rn(wt, It.lo)), qv);
+                light = __fadd_rn(light, r > 0.f ? r : 0.f);
+            }
+        }
+        const auto code = [&](int b) { return (int32_t)(j + b); };
+        if (!wq_push(q, head, tail, m, code)) {
+            while (m) {
+                const int b = __ffs(m) - 1;
+                m &= m - 1;
+                acc_add(acc, tile_item(rp, j + b, mode, It, Id, sm.tab));
+            }
+        }
+        while (tail - head >= 32) {
+            acc_add(acc, tile_item(rp, q[(head + lane) & (kQCap - 1)], mode, It, Id, sm.tab));
+            head += 32;
+            __syncwarp();
+        }
     }
-    return df_add(df_norm(heavy), light_sum_df(light, cl));
+    if (lane < (int)(tail - head)) acc_add(acc, tile_item(rp, q[(head + lane) & (kQCap - 1)], mode, It, Id, sm.tab));
+    __syncwarp();
+    return df_add(df_norm(acc), light_sum_df(light, cl));
 }
 
 // Inclusive warp scan of double-float values (Hillis-Steele).
@@ -194,30 +238,104 @@ __device__ __forceinline__ df warp_sum_df(df x) {
     return x;
 }
 
+// ---------------------------------------------------------------- queues
+// Heavy weights are rare (about 1% of a row) but each takes the double-float
+// path. Evaluating them in place would make the whole warp wait for every
+// heavy lane; instead each warp queues them in shared memory and evaluates
+// them 32 at a time.
+
+// Warp-wide exclusive prefix of per-lane counts; returns the lane's offset and
+// sets `total`.
+__device__ __forceinline__ uint32_t warp_offsets(uint32_t n, uint32_t& total) {
+    const int lane = threadIdx.x & 31;
+    uint32_t incl = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    total = __shfl_sync(0xffffffffu, incl, 31);
+    return incl - n;
+}
+
+// Append this lane's items (bit b of m -> code(b)) to the warp's ring
+// buffer. Returns false (and appends nothing) if they do not fit.
+template <class Code>
+__device__ __forceinline__ bool wq_push(int32_t* q, uint32_t head, uint32_t& tail, uint32_t m, Code code) {
+    uint32_t total;
+    uint32_t off = warp_offsets(__popc(m), total);
+    if (tail + total - head > (uint32_t)kQCap) return false;  // warp-uniform
+    off += tail;
+    while (m) {
+        const int b = __ffs(m) - 1;
+        m &= m - 1;
+        q[(off++) & (kQCap - 1)] = code(b);
+    }
+    tail += total;
+    __syncwarp();
+    return true;
+}
+
+// Pass A item: bit 30 = draft row, low bits = chunk column.
+template <int TDT, int DDT>
+__device__ __forceinline__ void norm_item(const RowPair<TDT, DDT>& rp, int32_t it, const Exp2Table& tab, df& at,
+                                          df& ad) {
+    const int64_t j = it & 0x3fffffff;
+    if (it & (1 << 30)) {
+        const float l = src_elem<DDT>(rp.d, j);
+        acc_add(ad, rp.probs ? df{l, 0.f} : heavy_logit_weight<DDT == SPECV_F32>(l, rp.md, rp.k, tab));
+    } else {
+        acc_add(at, heavy_logit_weight<TDT == SPECV_F32>(src_elem<TDT>(rp.t, j), rp.mt, rp.k, tab));
+    }
+}
+
 // Pass A: exact normalisers of both rows over this CTA's chunk (block sums,
-// valid in warp 0). Light weights are summed in fp32 per group of 8 columns.
+// valid in warp 0). Each warp covers 256 contiguous columns per step.
 template <int TDT, int DDT>
 __device__ void chunk_norms(const RowPair<TDT, DDT>& rp, int64_t n, SampSmem& sm, df& St, df& Sd) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int32_t* q = sm.q[warp];
+    uint32_t head = 0, tail = 0;
     df at{0.f, 0.f}, ad{0.f, 0.f};
-    const int64_t step = (int64_t)blockDim.x * 8;
-#pragma unroll 1
-    for (int64_t j = (int64_t)threadIdx.x * 8; j < n; j += step) {
+    for (int64_t base = (int64_t)warp * 256; base < n; base += (int64_t)kWarps * 256) {
+        const int64_t j = base + lane * 8;
         float lt[8], ld[8];
         src_load8<TDT>(rp.t, j, lt);
         src_load8<DDT>(rp.d, j, ld);
         float gt = 0.f, gd = 0.f;
+        uint32_t m = 0;
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-            const df a = rp.wt(lt[e], sm.tab), b = rp.wd(ld[e], sm.tab);
-            if (is_heavy(a)) acc_add(at, a); else gt = __fadd_rn(gt, a.hi);
-            if (is_heavy(b)) acc_add(ad, b); else gd = __fadd_rn(gd, b.hi);
+            bool h;
+            const float w = light_weight<TDT == SPECV_F32>(lt[e], rp.mt, rp.k, h);
+            if (h) m |= 1u << e; else gt = __fadd_rn(gt, w);
+            if (rp.probs) {
+                const float v = ld[e] > -INFINITY ? ld[e] : 0.f;
+                if (v > 1.220703125e-4f) m |= 1u << (8 + e); else gd = __fadd_rn(gd, v);
+            } else {
+                const float wd = light_weight<DDT == SPECV_F32>(ld[e], rp.md, rp.k, h);
+                if (h) m |= 1u << (8 + e); else gd = __fadd_rn(gd, wd);
+            }
         }
         acc_add(at, light_sum_df(gt, kEx2LightBias));
         acc_add(ad, light_sum_df(gd, rp.probs ? 0.f : kEx2LightBias));
+        const auto code = [&](int b) { return (int32_t)((j + (b & 7)) | (b >= 8 ? (1 << 30) : 0)); };
+        if (!wq_push(q, head, tail, m, code)) {  // queue full: evaluate in place
+            while (m) {
+                const int b = __ffs(m) - 1;
+                m &= m - 1;
+                norm_item(rp, code(b), sm.tab, at, ad);
+            }
+        }
+        while (tail - head >= 32) {
+            norm_item(rp, q[(head + lane) & (kQCap - 1)], sm.tab, at, ad);
+            head += 32;
+            __syncwarp();
+        }
     }
+    if (lane < (int)(tail - head)) norm_item(rp, q[(head + lane) & (kQCap - 1)], sm.tab, at, ad);
     at = warp_sum_df(df_norm(at));
     ad = warp_sum_df(df_norm(ad));
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (lane == 0) {
         sm.red_t[warp] = at;
         sm.red_d[warp] = ad;
@@ -239,7 +357,7 @@ __device__ df chunk_tiles(const RowPair<TDT, DDT>& rp, int ntiles, int mode, df 
                           SampSmem& sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int ti = warp; ti < ntiles; ti += kWarps) {
-        const df tot = warp_sum_df(lane_tile_sum(rp, (int64_t)ti * kTile, mode, It, Id, cl, sm.tab));
+        const df tot = warp_sum_df(lane_tile_sum(rp, (int64_t)ti * kTile, mode, It, Id, cl, sm));
         if (lane == 0) sm.tile_sum[ti] = tot;
     }
     __syncthreads();

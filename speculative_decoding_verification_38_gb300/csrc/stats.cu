@@ -29,6 +29,7 @@ namespace {
 
 constexpr int kWarps = kStatsThreads / 32;
 constexpr int kMaxGamma = 64;
+constexpr int kMaxGroups = 64;  // arrival groups per batch (at most one thread each)
 constexpr int kUnroll = 4;
 
 enum Mode { kLogits = 0, kProbs = 1, kArgmax = 2 };
@@ -43,6 +44,12 @@ struct Smem {
     int32_t xt[kMaxGamma];
     int32_t pick[kMaxGamma + 1];
     int32_t status, accepted, flag_tok, is_last;
+    // batched arrivals of the TMA variant
+    int32_t grp_b[kMaxGroups];
+    uint32_t grp_n[kMaxGroups];
+    int32_t grp_last[kMaxGroups];
+    int32_t ngroups;
+    int64_t next_r;
 };
 
 __device__ __forceinline__ int64_t tro_at(const StatsParams& p, int64_t b) {
@@ -78,17 +85,19 @@ __device__ __forceinline__ uint32_t nseg_of(int64_t r, int64_t V, int64_t chunk)
     return (uint32_t)(((r + 1) * V - 1) / chunk - (r * V) / chunk + 1);
 }
 
-// Number of (row, slice) pieces the streaming pass produces for sequence b.
-__device__ uint32_t expected_arrivals(const StatsParams& p, int32_t b) {
-    int64_t t0 = max((int64_t)0, tro_at(p, b)), t1 = min(p.rows_t, tro_at(p, b + 1));
-    uint32_t n = 0;
-    for (int64_t r = t0; r < t1; ++r) n += nseg_of(r, p.V, p.chunk);
+// Elements (rows x V) the streaming pass folds for sequence b: every CTA
+// adds the elements of b it has folded to b's counter, and the one that
+// brings the counter to this total finalizes b.
+__device__ uint32_t expected_elements(const StatsParams& p, int32_t b) {
+    const int64_t t0 = max((int64_t)0, tro_at(p, b)), t1 = min(p.rows_t, tro_at(p, b + 1));
+    int64_t rows = max((int64_t)0, t1 - t0);
     if (!p.greedy) {
-        int64_t d0 = max((int64_t)0, dro_at(p, b)), d1 = min(p.rows_d, dro_at(p, b + 1));
-        for (int64_t r = d0; r < d1; ++r) n += nseg_of(p.rows_t + r, p.V, p.chunk);
+        const int64_t d0 = max((int64_t)0, dro_at(p, b)), d1 = min(p.rows_d, dro_at(p, b + 1));
+        rows += max((int64_t)0, d1 - d0);
     }
-    return n;
+    return (uint32_t)(rows * p.V);
 }
+static_assert((2 * 64 + 1) * kMaxVocab < (int64_t)1 << 32, "per-sequence element count fits 32 bits");
 
 __device__ __forceinline__ float temp_of(const StatsParams& p, int32_t b) {
     return p.temps ? __ldg(p.temps + b) : p.temperature;
@@ -208,9 +217,10 @@ __device__ __forceinline__ void acc_scalar(ThreadAcc& a, float v, float k, int32
     }
 }
 
-// n values v[0..n) in increasing column order; col_of(j) gives the column of v[j].
-template <int MODE, int NV>
-__device__ __forceinline__ void acc_block(ThreadAcc& a, const float (&v)[NV], float k, const int32_t (&cols)[NV]) {
+// NV values v[] in increasing column order; for argmax, value j sits at
+// column cb[j / VEC] + j % VEC (computed only when a new maximum appears).
+template <int MODE, int NV, int VEC>
+__device__ __forceinline__ void acc_block(ThreadAcc& a, const float (&v)[NV], float k, const int32_t (&cb)[NV / VEC]) {
     float bm = v[0];
 #pragma unroll
     for (int j = 1; j < NV; ++j) bm = fmaxf(bm, v[j]);
@@ -238,10 +248,10 @@ __device__ __forceinline__ void acc_block(ThreadAcc& a, const float (&v)[NV], fl
         a.s += s0 + s1;
     } else {
         if (bm > a.m) {
-            int32_t c = cols[NV - 1];
+            int32_t c = INT32_MAX;
 #pragma unroll
             for (int j = NV - 1; j >= 0; --j)
-                if (v[j] == bm) c = cols[j];
+                if (v[j] == bm) c = cb[j / VEC] + (j % VEC);
             a.m = bm;
             a.idx = c;
         }
@@ -277,14 +287,13 @@ __device__ float2 seg_pass(const char* row, int64_t c0, int64_t c1, float k, Sme
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) q[u] = ld_stream_v4(vp + i + u * kStatsThreads);
         float v[kUnroll * VEC];
-        int32_t cols[kUnroll * VEC];
+        int32_t cb[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             VT::unpack(q[u], v + u * VEC);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) cols[u * VEC + e] = (int32_t)(v0 + (i + u * kStatsThreads) * VEC + e);
+            cb[u] = (int32_t)(v0 + (i + u * kStatsThreads) * VEC);
         }
-        acc_block<MODE>(a, v, k, cols);
+        acc_block<MODE, kUnroll * VEC, VEC>(a, v, k, cb);
     }
     // last partial iteration
     if (i < nvec) {
@@ -300,14 +309,13 @@ __device__ float2 seg_pass(const char* row, int64_t c0, int64_t c1, float k, Sme
             }
         }
         float v[kUnroll * VEC];
-        int32_t cols[kUnroll * VEC];
+        int32_t cb[kUnroll];
 #pragma unroll
         for (int u = 0; u < kUnroll; ++u) {
             VT::unpack(q[u], v + u * VEC);
-#pragma unroll
-            for (int e = 0; e < VEC; ++e) cols[u * VEC + e] = (int32_t)(v0 + (i + u * kStatsThreads) * VEC + e);
+            cb[u] = (int32_t)(v0 + (i + u * kStatsThreads) * VEC);
         }
-        acc_block<MODE>(a, v, k, cols);
+        acc_block<MODE, kUnroll * VEC, VEC>(a, v, k, cb);
     }
     // tail scalars
     const int64_t t0 = v0 + nvec * VEC;
@@ -412,8 +420,8 @@ __device__ float2 merge_row_ms(const StatsParams& p, int64_t r, bool probs_row, 
     const int lane = threadIdx.x & 31;
     const uint32_t ns = nseg_of(r, p.V, p.chunk);
     float2 acc = make_float2(probs_row ? 0.f : -INFINITY, 0.f);
-    for (uint32_t j = lane; j < ns; j += 32) {
-        float2 v = ld_cg_f2(p.partials + r * p.S + j);
+    for (uint32_t j = lane; j < ns * (uint32_t)p.pw; j += 32) {
+        float2 v = ld_cg_f2(p.partials + r * p.S * p.pw + j);
         acc = probs_row ? make_float2(0.f, acc.y + v.y) : ms_merge(acc, v, k);
     }
 #pragma unroll
@@ -429,8 +437,8 @@ __device__ void merge_row_am(const StatsParams& p, int64_t r, float& v, int32_t&
     const uint32_t ns = nseg_of(r, p.V, p.chunk);
     v = -INFINITY;
     ix = INT32_MAX;
-    for (uint32_t j = lane; j < ns; j += 32) {
-        float2 w = ld_cg_f2(p.partials + r * p.S + j);
+    for (uint32_t j = lane; j < ns * (uint32_t)p.pw; j += 32) {
+        float2 w = ld_cg_f2(p.partials + r * p.S * p.pw + j);
         int32_t wi = __float_as_int(w.y);
         if (am_better(w.x, wi, v, ix)) {
             v = w.x;
@@ -452,7 +460,8 @@ __device__ void finalize_sample(const StatsParams& p, int32_t b, Smem& sm) {
     const float k = kLog2e / temp_of(p, b);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nrows = 2 * g + 1;  // rows 0..g target, g+1..2g draft
-    for (int j = warp; j < nrows; j += kWarps) {
+    const int nwarps = blockDim.x >> 5;
+    for (int j = warp; j < nrows; j += nwarps) {
         const bool is_t = j <= g;
         const int64_t r = is_t ? (t0 + j) : (p.rows_t + d0 + (j - g - 1));
         const bool probs_row = !is_t && p.probs;
@@ -540,10 +549,12 @@ __device__ void finalize_greedy(const StatsParams& p, int32_t b, Smem& sm) {
         return;
     }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int j = warp; j <= g; j += kWarps) {
+    const int nwarps = blockDim.x >> 5;
+    for (int j = warp; j <= g; j += nwarps) {
         float v;
         int32_t ix;
         merge_row_am(p, t0 + j, v, ix);
+        if (ix == INT32_MAX) ix = 0;  // every logit -inf or NaN: the first index
         if (lane == 0) {
             sm.pick[j] = ix;
             p.row_stats[t0 + j] = make_float2(v, __int_as_float(ix));
@@ -570,13 +581,13 @@ __device__ __forceinline__ void finalize(const StatsParams& p, int32_t b, Smem& 
         finalize_sample(p, b, sm);
 }
 
-// Count `cnt` pieces of sequence b as done; the CTA that completes the count
-// finalizes b. Block-uniform arguments.
+// Count `cnt` elements of sequence b as folded; the CTA that completes the
+// count finalizes b. Block-uniform arguments.
 __device__ void arrive(const StatsParams& p, int32_t b, uint32_t cnt, Smem& sm) {
     if (b < 0 || cnt == 0) return;
     if (threadIdx.x == 0) {
         __threadfence();  // this CTA's partials before its arrival
-        const uint32_t expected = expected_arrivals(p, b);
+        const uint32_t expected = expected_elements(p, b);
         const uint32_t old = atomicAdd(p.counters + b, cnt);
         sm.is_last = (old + cnt == expected);
         if (sm.is_last) {
@@ -599,7 +610,7 @@ __global__ void __launch_bounds__(kStatsThreads, 2) stats_kernel(StatsParams p) 
     // still get their outputs written.
     if (p.tro) {
         for (int32_t b = blockIdx.x; b < p.B; b += gridDim.x) {
-            if (expected_arrivals(p, b) == 0) {
+            if (expected_elements(p, b) == 0) {
                 finalize(p, b, sm);
                 __syncthreads();
             }
@@ -622,22 +633,430 @@ __global__ void __launch_bounds__(kStatsThreads, 2) stats_kernel(StatsParams p) 
         float k = 1.f;
         if (!p.greedy && b >= 0) k = kLog2e / temp_of(p, b);
         const float2 part = run_segment(p, is_t, lr, c0, c1, k, sm);
-        if (threadIdx.x == 0) p.partials[r * p.S + (blockIdx.x - (r * p.V) / p.chunk)] = part;
+        if (threadIdx.x == 0) p.partials[(r * p.S + (blockIdx.x - (r * p.V) / p.chunk)) * p.pw] = part;
         if (b != pend_b || (!is_t) != pend_draft) {
             arrive(p, pend_b, pend_n, sm);
             pend_b = b;
             pend_n = 0;
             pend_draft = !is_t;
         }
-        if (b >= 0) ++pend_n;
+        if (b >= 0) pend_n += (uint32_t)(seg_end - e);
         e = seg_end;
     }
     arrive(p, pend_b, pend_n, sm);
 }
 
+// ------------------------------------------------------------ TMA variant
+// One CTA per SM; its element range is cut into one contiguous piece per warp.
+// Every warp streams its own piece through a private ring of shared-memory
+// stages filled by 1-D bulk copies (cp.async.bulk, completion counted on a
+// per-stage mbarrier that lane 0 arms), folds each stage into per-lane
+// states with packed f32x2 arithmetic and, whenever a row ends, reduces its
+// lanes and stores one partial per (row, CTA slice, warp). Warps never wait
+// on one another while streaming. Every mbarrier wait is bounded; a warp that
+// gives up poisons its partials (NaN), so the affected sequences report
+// SPEC_SEQ_BAD_ROW, and sets the workspace error word.
+constexpr int kWarpRing = kTmaStages * (int)kTmaStageBytes;  // bytes of one warp's ring
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
+// Packed two-lane fp32 arithmetic (one instruction for two IEEE
+// round-to-nearest operations) and the three-input maximum.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Per-lane state of the warp-streaming pass: raw max m, neg = -fl(m*k) (0
+// while nothing finite was seen), a two-lane running sum, argmax index.
+struct LaneAcc {
+    float m, neg;
+    float2 s;
+    int32_t idx;
+};
+
+__device__ __forceinline__ void lane_reset(LaneAcc& a) {
+    a.m = -INFINITY;
+    a.neg = 0.f;
+    a.s = make_float2(0.f, 0.f);
+    a.idx = INT32_MAX;
+}
+
+// Fold NV values (NV a multiple of 8, increasing columns; value j at column
+// cb[j / VEC] + j % VEC) into a lane state. Maxima and sums run in four
+// independent chains so that consecutive instructions do not wait on one another.
+template <int MODE, int NV, int VEC>
+__device__ __forceinline__ void lane_block(LaneAcc& a, const float (&v)[NV], float k, const int32_t (&cb)[NV / VEC]) {
+    static_assert(NV % 8 == 0, "block of 8");
+    if constexpr (MODE == kProbs) {
+        float2 c[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) c[q] = make_float2(v[2 * q], v[2 * q + 1]);
+#pragma unroll
+        for (int j = 8; j < NV; j += 2) c[(j / 2) % 4] = add2(c[(j / 2) % 4], make_float2(v[j], v[j + 1]));
+        a.s = add2(a.s, add2(add2(c[0], c[1]), add2(c[2], c[3])));
+    } else {
+        float mx[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) mx[q] = fmaxf(v[2 * q], v[2 * q + 1]);
+#pragma unroll
+        for (int j = 8; j < NV; j += 2) mx[(j / 2) % 4] = max3(mx[(j / 2) % 4], v[j], v[j + 1]);
+        const float bm = max3(max3(a.m, mx[0], mx[1]), mx[2], mx[3]);
+        if constexpr (MODE == kLogits) {
+            if (bm > a.m) {
+                const float nneg = -(bm * k);
+                const float f = ex2(nneg - a.neg);
+                if (a.s.x != 0.f) a.s.x *= f;
+                if (a.s.y != 0.f) a.s.y *= f;
+                a.m = bm;
+                a.neg = nneg;
+            }
+            const float2 kk = make_float2(k, k), nn = make_float2(a.neg, a.neg);
+            float2 c[4];
+#pragma unroll
+            for (int j = 0; j < NV; j += 2) {
+                const float2 t = fma2(make_float2(v[j], v[j + 1]), kk, nn);
+                const float2 e = make_float2(ex2(t.x), ex2(t.y));
+                if (j < 8) c[j / 2] = e;
+                else c[(j / 2) % 4] = add2(c[(j / 2) % 4], e);
+            }
+            a.s = add2(a.s, add2(add2(c[0], c[1]), add2(c[2], c[3])));
+        } else {
+            if (bm > a.m) {
+                int32_t c = INT32_MAX;
+#pragma unroll
+                for (int j = NV - 1; j >= 0; --j)
+                    if (v[j] == bm) c = cb[j / VEC] + (j % VEC);
+                a.m = bm;
+                a.idx = c;
+            }
+        }
+    }
+}
+
+// Fold the nvec 16-byte vectors of one row segment held in shared memory at
+// sa (first column col0) into the lane states of one warp.
+template <int DT, int MODE>
+__device__ __forceinline__ void warp_segment(LaneAcc& a, uint32_t sa, int nvec, int64_t col0, float k, int lane) {
+    using VT = VecTraits<DT>;
+    constexpr int VEC = VT::kVec;
+    constexpr int U = 4;
+    int i = lane;
+    for (; i + 32 * (U - 1) < nvec; i += 32 * U) {
+        uint4 q[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) q[u] = lds_v4(sa + (uint32_t)(i + 32 * u) * 16u);
+        float v[U * VEC];
+        int32_t cb[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            VT::unpack(q[u], v + u * VEC);
+            cb[u] = (int32_t)(col0 + (int64_t)(i + 32 * u) * VEC);
+        }
+        lane_block<MODE, U * VEC, VEC>(a, v, k, cb);
+    }
+    for (; i < nvec; i += 32) {  // leftover vectors, one at a time (f32 pads with -inf / 0)
+        const uint4 q = lds_v4(sa + (uint32_t)i * 16u);
+        float v[8];
+        VT::unpack(q, v);
+        if constexpr (VEC == 4) {
+#pragma unroll
+            for (int j = 4; j < 8; ++j) v[j] = MODE == kProbs ? 0.f : -INFINITY;
+        }
+        const int32_t cb[8 / VEC] = {(int32_t)(col0 + (int64_t)i * VEC)};
+        lane_block<MODE, 8, VEC>(a, v, k, cb);
+    }
+}
+
+// Identity partial of a row nobody in this warp touched.
+__device__ __forceinline__ float2 ident_partial(const StatsParams& p, int64_t r) {
+    if (p.greedy) return make_float2(-INFINITY, __int_as_float(INT32_MAX));
+    if (r >= p.rows_t && p.probs) return make_float2(0.f, 0.f);
+    return make_float2(-INFINITY, 0.f);
+}
+
+__device__ __forceinline__ int64_t partial_index(const StatsParams& p, int64_t r, int warp) {
+    const int64_t slot = (int64_t)blockIdx.x - (r * p.V) / p.chunk;
+    return (r * p.S + slot) * p.pw + warp;
+}
+
+// Reduce the lane states of row r over the warp; lane 0 stores the partial
+// (NaN if the warp gave up on a copy).
+__device__ void lane_flush(const StatsParams& p, LaneAcc& a, int mode, float k, int64_t r, int warp, bool poison) {
+    const int lane = threadIdx.x & 31;
+    float2 out;
+    if (mode == kLogits) {
+        float2 v = make_float2(a.m, a.s.x + a.s.y);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float2 w = make_float2(__shfl_xor_sync(0xffffffffu, v.x, o), __shfl_xor_sync(0xffffffffu, v.y, o));
+            v = ms_merge(v, w, k);
+        }
+        out = v;
+    } else if (mode == kProbs) {
+        float v = a.s.x + a.s.y;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        out = make_float2(0.f, v);
+    } else {
+        float v = a.m;
+        int32_t ix = a.idx;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) am_merge_shfl(v, ix, o);
+        out = make_float2(v, __int_as_float(ix));
+    }
+    if (lane == 0) {
+        if (poison) out = make_float2(NAN, NAN);
+        p.partials[partial_index(p, r, warp)] = out;
+    }
+    lane_reset(a);
+}
+
+struct WarpRing {
+    uint64_t full[kTmaConsumerWarps][kTmaStages];
+    int64_t unit_of[kTmaConsumerWarps][kTmaStages];  // unit held by each stage of each warp's ring
+    int next_unit;                                     // next unit of this CTA's range to hand out
+    int failed;
+};
+
+__global__ void __launch_bounds__(kTmaThreads, 1) stats_tma_kernel(StatsParams p) {
+    __shared__ Smem sm;
+    __shared__ WarpRing wr;
+    extern __shared__ __align__(128) char ring[];
+    pdl_launch_dependents();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int w = 0; w < kTmaConsumerWarps; ++w)
+            for (int st = 0; st < kTmaStages; ++st) mbar_init(&wr.full[w][st], 1);
+        wr.next_unit = 0;
+        wr.failed = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (p.tro) {  // sequences that own no row (broken offsets) still get outputs
+        for (int32_t b = blockIdx.x; b < p.B; b += gridDim.x) {
+            if (expected_elements(p, b) == 0) {
+                finalize(p, b, sm);
+                __syncthreads();
+            }
+        }
+    }
+
+    const int64_t e0 = (int64_t)blockIdx.x * p.chunk;
+    const int64_t e1 = min(p.N, e0 + p.chunk);
+    // The range is handed out in units of one stage: units of the target part
+    // [e0, m) first, then of the draft part [m, e1); m = the first draft element.
+    const int64_t T = p.rows_t * p.V;
+    const int tesz = p.tdt == SPECV_F32 ? 4 : 2, desz = p.ddt == SPECV_F32 ? 4 : 2;
+    const int64_t m = max(e0, min(e1, T));
+    const int64_t ut = kTmaStageBytes / tesz, ud = kTmaStageBytes / desz;  // elements per unit
+    const int64_t nut = (m - e0 + ut - 1) / ut, nud = (e1 - m + ud - 1) / ud;
+    const int64_t nunits = nut + nud;
+    auto unit_start = [&](int64_t u) { return u < nut ? e0 + u * ut : m + (u - nut) * ud; };
+    auto unit_end = [&](int64_t u) { return u < nut ? min(m, e0 + (u + 1) * ut) : min(e1, m + (u - nut + 1) * ud); };
+
+    char* myring = ring + (size_t)warp * kWarpRing;
+    uint64_t* full = wr.full[warp];
+    // lane 0 takes the next unit and, unless the warp gave up, starts its copy
+    uint32_t issued = 0, copies = 0;  // stages handed to this warp / of those, stages with a copy
+    auto take = [&](bool copy) -> bool {
+        const int64_t u = atomicAdd(&wr.next_unit, 1);
+        if (u >= nunits) return false;
+        const int st = issued % kTmaStages;
+        wr.unit_of[warp][st] = u;
+        if (copy) {
+            const int64_t f = unit_start(u), s1 = unit_end(u);
+            const bool tgt = f < T;
+            const int esz = tgt ? tesz : desz;
+            const char* src = tgt ? (const char*)p.tgt + f * esz : (const char*)p.dft + (f - T) * esz;
+            mbar_arrive_expect_tx(&full[st], (uint32_t)((s1 - f) * esz));
+            bulk_g2s(myring + (size_t)st * kTmaStageBytes, src, (uint32_t)((s1 - f) * esz), &full[st]);
+            copies = issued + 1;
+        }
+        ++issued;
+        return true;
+    };
+    if (lane == 0)
+        for (int i = 0; i < kTmaStages; ++i)
+            if (!take(true)) break;
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+    __syncwarp();
+
+    LaneAcc a;
+    lane_reset(a);
+    bool dead = false;
+    uint32_t done = 0;  // stages whose copy completed
+    // row bookkeeping: the current row r of the CTA range, whether this warp
+    // has folded any of it, and its parameters
+    const int64_t R0 = e0 < e1 ? e0 / p.V : 0, R1 = e0 < e1 ? (e1 - 1) / p.V : -1;
+    int64_t r = R0, row_end = (R0 + 1) * p.V;
+    bool touched = false;
+    int mode = kLogits, dt = SPECV_BF16;
+    float k = 1.f;
+    int64_t param_row = -1;  // row the parameters above belong to
+    auto set_row = [&]() {
+        if (param_row == r) return;
+        param_row = r;
+        const bool is_t = r < p.rows_t;
+        dt = is_t ? p.tdt : p.ddt;
+        mode = p.greedy ? kArgmax : ((!is_t && p.probs) ? kProbs : kLogits);
+        k = 1.f;
+        if (!p.greedy) {
+            const int32_t b = seq_of_row(p, !is_t, is_t ? r : r - p.rows_t);
+            if (b >= 0) k = kLog2e / temp_of(p, b);
+        }
+    };
+    auto leave_row = [&]() {  // store this warp's partial of row r, then move to r + 1
+        if (touched) lane_flush(p, a, mode, k, r, warp, dead);
+        else if (lane == 0) p.partials[partial_index(p, r, warp)] = ident_partial(p, r);
+        touched = false;
+        ++r;
+        row_end += p.V;
+    };
+    if (R0 <= R1) set_row();
+
+    for (uint32_t kk = 0; kk < issued; ++kk) {
+        const int st = kk % kTmaStages;
+        if (!dead) {
+            const bool ok = mbar_wait_bounded(&full[st], (kk / kTmaStages) & 1, kWaitLimit);
+            dead = __any_sync(0xffffffffu, !ok);
+            if (dead && lane == 0) atomicExch(&wr.failed, 1);
+            if (!dead) done = kk + 1;
+        }
+        const int64_t u = wr.unit_of[warp][st];
+        const int64_t f = unit_start(u), s1 = unit_end(u);
+        while (f >= row_end) leave_row();
+        set_row();
+        const uint32_t base = smem_addr(myring + (size_t)st * kTmaStageBytes);
+        for (int64_t g0 = f; g0 < s1;) {
+            const int64_t se = min(s1, row_end);
+            touched = true;
+            if (!dead) {
+                const int esz = dt == SPECV_F32 ? 4 : 2;
+                const uint32_t sa = base + (uint32_t)((g0 - f) * esz);
+                const int nvec = (int)((se - g0) * esz / 16);
+                const int64_t col0 = g0 - (row_end - p.V);
+                if (mode == kLogits) {
+                    if (dt == SPECV_F32) warp_segment<SPECV_F32, kLogits>(a, sa, nvec, col0, k, lane);
+                    else warp_segment<SPECV_BF16, kLogits>(a, sa, nvec, col0, k, lane);
+                } else if (mode == kProbs) {
+                    if (dt == SPECV_F32) warp_segment<SPECV_F32, kProbs>(a, sa, nvec, col0, k, lane);
+                    else warp_segment<SPECV_BF16, kProbs>(a, sa, nvec, col0, k, lane);
+                } else {
+                    if (dt == SPECV_F32) warp_segment<SPECV_F32, kArgmax>(a, sa, nvec, col0, k, lane);
+                    else warp_segment<SPECV_BF16, kArgmax>(a, sa, nvec, col0, k, lane);
+                }
+            }
+            if (se == row_end) {  // the row ends inside this unit
+                leave_row();
+                if (se < s1) set_row();
+            }
+            g0 = se;
+        }
+        // refill the slot just consumed (the reads above are done once the warp converges)
+        __syncwarp();
+        if (lane == 0) {
+            if (!dead) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            take(!dead);
+        }
+        issued = __shfl_sync(0xffffffffu, issued, 0);
+        __syncwarp();  // lane 0's record of the unit is seen by the warp even without a wait
+    }
+    while (r <= R1) leave_row();  // the rest of the CTA range's rows
+    // never leave while a copy into this warp's ring may be in flight
+    if (lane == 0) {
+        for (uint32_t q = done; q < copies; ++q)
+            mbar_wait_bounded(&full[q % kTmaStages], (q / kTmaStages) & 1, kWaitLimit);
+        __threadfence();  // partials before the arrivals below
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && wr.failed) atomicOr(p.err, 1u);
+
+    // Arrivals for every (sequence, part) group of rows the CTA range touches,
+    // made in parallel by one thread per group, in batches of kMaxGroups;
+    // then the CTA finalizes the sequences it completed.
+    int64_t next_r = R0;  // same value in every thread
+    while (next_r <= R1) {
+        if (threadIdx.x == 0) {
+            int n = 0;
+            int32_t pb = -1;
+            uint32_t pn = 0;
+            bool pdraft = false;
+            int64_t rr = next_r;
+            for (; rr <= R1 && n < kMaxGroups - 1; ++rr) {
+                const bool is_t = rr < p.rows_t;
+                const int32_t b = seq_of_row(p, !is_t, is_t ? rr : rr - p.rows_t);
+                if (b != pb || (!is_t) != pdraft) {
+                    if (pb >= 0 && pn) {
+                        sm.grp_b[n] = pb;
+                        sm.grp_n[n++] = pn;
+                    }
+                    pb = b;
+                    pn = 0;
+                    pdraft = !is_t;
+                }
+                if (b >= 0) pn += (uint32_t)(min(e1, (rr + 1) * p.V) - max(e0, rr * p.V));
+            }
+            if (pb >= 0 && pn) {
+                sm.grp_b[n] = pb;
+                sm.grp_n[n++] = pn;
+            }
+            sm.ngroups = n;
+            sm.next_r = rr;
+        }
+        __syncthreads();
+        next_r = sm.next_r;
+        const int ng = sm.ngroups;
+        if (threadIdx.x < ng) {
+            const int32_t b = sm.grp_b[threadIdx.x];
+            const uint32_t cnt = sm.grp_n[threadIdx.x];
+            __threadfence();  // this CTA's partials before its arrival
+            const uint32_t old = atomicAdd(p.counters + b, cnt);
+            const bool last = old + cnt == expected_elements(p, b);
+            if (last) {
+                p.counters[b] = 0;  // every element of b has arrived: ready for the next call
+                __threadfence();
+            }
+            sm.grp_last[threadIdx.x] = last;
+        }
+        __syncthreads();
+        for (int gi = 0; gi < ng; ++gi) {
+            if (sm.grp_last[gi]) {
+                finalize(p, sm.grp_b[gi], sm);
+                __syncthreads();
+            }
+        }
+        __syncthreads();  // the group lists are rewritten by the next batch
+    }
+}
+
 }  // namespace
 
-Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int greedy, int64_t grid_cap) {
+Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int greedy, int64_t grid_cap, int pw) {
     Layout L;
     L.rows_total = rows_t + (greedy ? 0 : rows_d);
     L.N = L.rows_total * V;
@@ -651,7 +1070,7 @@ Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int gre
     auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
     size_t off = al(kHeaderBytes);
     L.off_partials = off;
-    off = al(off + (size_t)L.rows_total * L.S * sizeof(float2));
+    off = al(off + (size_t)L.rows_total * L.S * pw * sizeof(float2));
     L.off_rowstats = off;
     off = al(off + (size_t)L.rows_total * sizeof(float2));
     L.off_pq = off;
@@ -673,7 +1092,18 @@ int stats_resident_ctas(int device, int greedy) {
 }
 
 cudaError_t launch_stats(const StatsParams& p, cudaStream_t s) {
-    stats_kernel<<<p.grid, kStatsThreads, 0, s>>>(p);
+    if (p.tma) {
+        static bool attr_done = false;
+        if (!attr_done) {
+            cudaError_t e = cudaFuncSetAttribute(stats_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 kTmaConsumerWarps * kWarpRing);
+            if (e != cudaSuccess) return e;
+            attr_done = true;
+        }
+        stats_tma_kernel<<<p.grid, kTmaThreads, kTmaConsumerWarps * kWarpRing, s>>>(p);
+    } else {
+        stats_kernel<<<p.grid, kStatsThreads, 0, s>>>(p);
+    }
     return cudaGetLastError();
 }
 
