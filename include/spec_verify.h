@@ -186,6 +186,28 @@ SPEC_API spec_status_t spec_verify_sample(const spec_verify_args_t* args, spec_s
  * temperature, seed, round, seq_offset and uniforms. */
 SPEC_API spec_status_t spec_verify_greedy(const spec_verify_args_t* args, spec_stream_t stream);
 
+/* Largest scratch spec_verify_sample_static may use (bytes). */
+#define SPEC_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
+
+/* spec_verify_sample on scratch the library owns, for callers that cannot
+ * hand it device memory: a plain C caller with no device allocator of its
+ * own, or an engine whose memory pool has already reserved the free HBM (for
+ * its KV cache) and may not grow. Same arguments, results and errors as
+ * spec_verify_sample except that workspace and workspace_bytes are ignored.
+ * The source pages have no counterpart: this is a library convenience.
+ *   - Scratch: a fixed device array of SPEC_STATIC_SCRATCH_BYTES (8 MiB) per
+ *     device, part of the library's module; the call allocates nothing. A call
+ *     with spec_verify_workspace_size(args, 0) > SPEC_STATIC_SCRATCH_BYTES
+ *     returns SPEC_ERR_WORKSPACE before any CUDA call.
+ *   - Set-up: the first call on a device (that device current) looks up the
+ *     array's device address with cudaGetSymbolAddress; make that first call
+ *     before any stream capture.
+ *   - Every call clears the scratch's arrival counters and error word with a
+ *     stream-ordered memset before its kernels; no spec_workspace_init needed.
+ *   - There is one scratch per device: calls that overlap on the GPU (other
+ *     streams, other host threads) race on it. Serialise them. */
+SPEC_API spec_status_t spec_verify_sample_static(const spec_verify_args_t* args, spec_stream_t stream);
+
 /* KV-length rollback alone, e.g. for the draft model's cache ("Speculative
  * decoding" (mhtirogla.ai), How it works step 5: truncate the length in both
  * models; Implementation notes: paged KV makes this a length truncate).

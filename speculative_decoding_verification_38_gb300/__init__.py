@@ -27,6 +27,7 @@ SPEC_ERR_WORKSPACE = 3
 SPEC_ERR_CUDA = 4
 SPEC_ERR_UNSUPPORTED = 5
 SPEC_F32, SPEC_BF16 = 0, 1
+SPEC_STATIC_SCRATCH_BYTES = 8 << 20  # scratch of spec_verify_sample_static, per device
 SEQ_OK, SEQ_BAD_TOKEN, SEQ_BAD_KV, SEQ_BAD_ROW, SEQ_BAD_LAYOUT, SEQ_BAD_TEMP = 0, 1, 2, 3, 4, 5
 
 
@@ -106,6 +107,8 @@ def lib():
             L.spec_verify_sample.argtypes = [A, vp]
             L.spec_verify_greedy.restype = ctypes.c_int
             L.spec_verify_greedy.argtypes = [A, vp]
+            L.spec_verify_sample_static.restype = ctypes.c_int
+            L.spec_verify_sample_static.argtypes = [A, vp]
             L.spec_kv_rollback.restype = ctypes.c_int
             L.spec_kv_rollback.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
             L.spec_debug_philox.restype = ctypes.c_int
@@ -276,6 +279,13 @@ def spec_verify_sample(args: VerifyArgs, stream=None) -> int:
 
 def spec_verify_greedy(args: VerifyArgs, stream=None) -> int:
     return lib().spec_verify_greedy(ctypes.byref(args.struct), _stream(stream))
+
+
+def spec_verify_sample_static(args: VerifyArgs, stream=None) -> int:
+    """spec_verify_sample on the library's own fixed scratch (8 MiB per device)
+    for callers that cannot provide device memory; args' workspace is ignored.
+    Calls that overlap on the GPU race on that scratch."""
+    return lib().spec_verify_sample_static(ctypes.byref(args.struct), _stream(stream))
 
 
 def spec_kv_rollback(kv_in, kv_out, accepted, gammas, gamma_max, block_size=0, out_num_blocks=None,

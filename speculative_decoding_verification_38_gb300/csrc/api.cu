@@ -176,6 +176,30 @@ spec_status_t prepare(const spec_verify_args_t* a, int greedy, StatsParams& p, L
     return SPEC_OK;
 }
 
+// ------------------------------------------------ library-owned scratch
+// spec_verify_sample_static runs on this fixed device array instead of a
+// caller workspace. Its device address is looked up once per device, with
+// that device current, on the first call made there.
+constexpr size_t kStaticScratchBytes = SPEC_STATIC_SCRATCH_BYTES;
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+static_assert(kStaticScratchBytes >= kHeaderBytes, "static scratch holds at least the header");
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[64];
+
+spec_status_t static_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return SPEC_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_scratch_mu);
+    if (!g_scratch_ptr[dev]) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return SPEC_ERR_CUDA;
+        g_scratch_ptr[dev] = ptr;
+    }
+    *out = g_scratch_ptr[dev];
+    return SPEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -306,6 +330,27 @@ SPEC_API spec_status_t spec_debug_time_next_stats(void* start_event, void* stop_
     t_ev_start = (cudaEvent_t)start_event;
     t_ev_stop = (cudaEvent_t)stop_event;
     return SPEC_OK;
+}
+
+SPEC_API spec_status_t spec_verify_sample_static(const spec_verify_args_t* a, spec_stream_t stream) {
+    // host checks first: nothing is looked up or launched for a rejected call
+    spec_status_t st = check_shape(a);
+    if (st) return st;
+    if (spec_verify_workspace_size(a, 0) > kStaticScratchBytes) return SPEC_ERR_WORKSPACE;
+    void* ws = nullptr;
+    st = static_scratch(&ws);
+    if (st) return st;
+    spec_verify_args_t b = *a;
+    b.workspace = ws;
+    b.workspace_bytes = kStaticScratchBytes;
+    StatsParams p;
+    Layout L;
+    int dev = 0;
+    st = prepare(&b, 0, p, L, dev);
+    if (st) return st;
+    // arrival counters and error word start at zero on every call
+    if (cudaMemsetAsync(ws, 0, kHeaderBytes, (cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    return spec_verify_sample(&b, stream);
 }
 
 }  // extern "C"
