@@ -246,12 +246,10 @@ SPEC_API spec_status_t spec_verify_sample(const spec_verify_args_t* a, spec_stre
     sp.tdt = p.tdt;
     sp.ddt = p.ddt;
     sp.V = p.V;
-    const int64_t et = esize(p.tdt), ed = esize(p.ddt);
-    sp.nsplit = sampler_nsplit(dev, p.B, p.V, et + ed);
-    const int64_t per = (p.V + sp.nsplit - 1) / sp.nsplit;
-    sp.vchunk = (per + kTile - 1) / kTile * kTile;
-    const int64_t row_bytes = (sp.vchunk * (et > ed ? et : ed) + 15) / 16 * 16;
-    sp.stage_bytes = (2 * row_bytes <= (int64_t)kSampStageMax) ? (uint32_t)row_bytes : 0u;
+    const SampPlan plan = sampler_plan(dev, p.B, p.V, p.tdt, p.ddt);
+    sp.nsplit = plan.nsplit;
+    sp.vchunk = plan.vchunk;
+    sp.stage_bytes = plan.stage_bytes;
     sp.tasks_in = p.tasks;
     sp.tasks = p.tasks;
     sp.out_tokens = p.out_tokens;

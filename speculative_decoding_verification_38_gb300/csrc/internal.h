@@ -120,7 +120,12 @@ Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int gre
 cudaError_t launch_stats(const StatsParams& p, cudaStream_t s);
 int stats_resident_ctas(int device, int greedy);  // CTAs that fit at once on the device (plain-load variant)
 cudaError_t launch_sampler(const SampleParams& p, int32_t B, cudaStream_t s, bool pdl);
-int sampler_nsplit(int device, int64_t B, int64_t V, int64_t pair_bytes);
+struct SampPlan {
+    int nsplit;            // CTAs per sequence (cluster size)
+    int64_t vchunk;        // columns per CTA, multiple of kTile
+    uint32_t stage_bytes;  // shared memory per staged row chunk (0: read rows directly)
+};
+SampPlan sampler_plan(int device, int64_t B, int64_t V, int tdt, int ddt);
 cudaError_t launch_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,
                                const int32_t* gammas, int32_t gmax, int32_t B, int32_t block_size,
                                int32_t* out_blocks, int32_t* seq_status, cudaStream_t s);

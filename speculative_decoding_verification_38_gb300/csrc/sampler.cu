@@ -26,6 +26,8 @@
 // matches a float64 evaluation except within ~1e-10 of a CDF edge.
 #include <math.h>
 
+#include <mutex>
+
 #include "precise.cuh"
 
 namespace specv {
@@ -648,22 +650,104 @@ cudaError_t launch_typed(const SampleParams& p, int32_t B, cudaStream_t s, bool 
 
 }  // namespace
 
-// CTAs per sequence: enough CTAs to fill the GPU a few times over, chunks of
-// at least 4096 columns, and (when possible) a row-pair chunk that fits the
-// shared-memory staging budget.
-int sampler_nsplit(int device, int64_t B, int64_t V, int64_t pair_bytes) {
-    int sms = 152;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
-    int64_t n = (4 * (int64_t)sms + B - 1) / B;
-    const int64_t by_v = V / 4096;
-    if (n > by_v) n = by_v;
-    const int64_t fit = (V * pair_bytes + (int64_t)kSampStageMax - 1) / (int64_t)kSampStageMax;
-    if (n < fit && fit <= kMaxCluster && V / fit >= 1024) n = fit;
+namespace {
+
+template <int TDT, int DDT>
+int active_clusters(int nsplit, uint32_t stage_bytes) {
+    static bool attr_done = false;  // per instantiation
+    if (!attr_done) {
+        if (cudaFuncSetAttribute(sampler_kernel<TDT, DDT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kSampStageMax) != cudaSuccess)
+            return 0;
+        attr_done = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)nsplit);
+    cfg.blockDim = dim3(kSampThreads);
+    cfg.dynamicSmemBytes = 2 * (size_t)stage_bytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)nsplit;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)sampler_kernel<TDT, DDT>, &cfg) != cudaSuccess) return 0;
+    return n;
+}
+
+int active_clusters_rt(int tdt, int ddt, int nsplit, uint32_t stage_bytes) {
+    if (tdt == SPECV_BF16 && ddt == SPECV_BF16) return active_clusters<SPECV_BF16, SPECV_BF16>(nsplit, stage_bytes);
+    if (tdt == SPECV_BF16) return active_clusters<SPECV_BF16, SPECV_F32>(nsplit, stage_bytes);
+    if (ddt == SPECV_BF16) return active_clusters<SPECV_F32, SPECV_BF16>(nsplit, stage_bytes);
+    return active_clusters<SPECV_F32, SPECV_F32>(nsplit, stage_bytes);
+}
+
+struct PlanKey {
+    int device, tdt, ddt;
+    int64_t B, V;
+};
+std::mutex g_plan_mu;
+PlanKey g_plan_key[8];
+SampPlan g_plan_val[8];
+int g_plan_n = 0, g_plan_next = 0;
+
+}  // namespace
+
+// CTAs per sequence (cluster size) and shared-memory staging. Each candidate
+// split n keeps chunks of at least 4096 columns and at most kMaxTilesPerCta
+// tiles; its cost is the number of waves the B clusters need (from the
+// occupancy calculator, which knows how clusters pack into GPCs) times the
+// columns each CTA handles. Staging the row pair in shared memory is used
+// when it fits and does not cost a wave; the cheapest candidate wins, larger
+// splits first on ties. Plans are cached per (device, B, V, dtypes).
+SampPlan sampler_plan(int device, int64_t B, int64_t V, int tdt, int ddt) {
+    {
+        std::lock_guard<std::mutex> lk(g_plan_mu);
+        for (int i = 0; i < g_plan_n; ++i) {
+            const PlanKey& k = g_plan_key[i];
+            if (k.device == device && k.B == B && k.V == V && k.tdt == tdt && k.ddt == ddt) return g_plan_val[i];
+        }
+    }
+    const int64_t et = tdt == SPECV_F32 ? 4 : 2, ed = ddt == SPECV_F32 ? 4 : 2;
     const int64_t need = (V + (int64_t)kMaxTilesPerCta * kTile - 1) / ((int64_t)kMaxTilesPerCta * kTile);
-    if (n < need) n = need;
-    if (n < 1) n = 1;
-    if (n > kMaxCluster) n = kMaxCluster;
-    return (int)n;
+    int64_t hi = V / 4096;
+    if (hi > kMaxCluster) hi = kMaxCluster;
+    if (hi < need) hi = need;
+    if (hi < 1) hi = 1;
+    SampPlan best{};
+    double best_cost = -1.0;
+    for (int64_t n = hi; n >= (need < 1 ? 1 : need); --n) {
+        const int64_t per = (V + n - 1) / n;
+        const int64_t vchunk = (per + kTile - 1) / kTile * kTile;
+        const int64_t row_bytes = (vchunk * (et > ed ? et : ed) + 15) / 16 * 16;
+        for (int staged = 1; staged >= 0; --staged) {
+            if (staged && 2 * row_bytes > (int64_t)kSampStageMax) continue;
+            const uint32_t sb = staged ? (uint32_t)row_bytes : 0u;
+            const int act = active_clusters_rt(tdt, ddt, (int)n, sb);
+            if (act < 1) continue;
+            const int64_t waves = (B + act - 1) / act;
+            const double cost = (double)waves * (double)vchunk;
+            if (best_cost < 0.0 || cost < best_cost) {
+                best_cost = cost;
+                best.nsplit = (int)n;
+                best.vchunk = vchunk;
+                best.stage_bytes = sb;
+            }
+        }
+    }
+    if (best_cost < 0.0) {  // no occupancy answer: one CTA per sequence, direct reads
+        best.nsplit = (int)(need < 1 ? 1 : need);
+        const int64_t per = (V + best.nsplit - 1) / best.nsplit;
+        best.vchunk = (per + kTile - 1) / kTile * kTile;
+        best.stage_bytes = 0;
+    }
+    std::lock_guard<std::mutex> lk(g_plan_mu);
+    const int slot = g_plan_n < 8 ? g_plan_n++ : (g_plan_next++ & 7);
+    g_plan_key[slot] = PlanKey{device, tdt, ddt, B, V};
+    g_plan_val[slot] = best;
+    return best;
 }
 
 cudaError_t launch_sampler(const SampleParams& p, int32_t B, cudaStream_t s, bool pdl) {
