@@ -41,8 +41,9 @@ inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
 thread_local cudaEvent_t t_ev_start = nullptr, t_ev_stop = nullptr;
 
-// Launch the streaming pass, bracketed by the caller's events if the
-// profiling hook is armed (the hook is consumed by this call).
+// Launch the streaming pass (bracketed by the caller's events if the
+// profiling hook is armed; the hook is consumed by this call) and, for the
+// TMA variant, its finalize kernel.
 cudaError_t stats_with_hook(const StatsParams& p, cudaStream_t s) {
     cudaEvent_t e0 = t_ev_start, e1 = t_ev_stop;
     t_ev_start = t_ev_stop = nullptr;
@@ -50,6 +51,10 @@ cudaError_t stats_with_hook(const StatsParams& p, cudaStream_t s) {
     cudaError_t e = launch_stats(p, s);
     if (e != cudaSuccess) return e;
     if (e0 && e1 && cudaEventRecord(e1, s) != cudaSuccess) return cudaErrorUnknown;
+    if (p.tma) {
+        e = launch_finalize(p, s);
+        if (e != cudaSuccess) return e;
+    }
     return cudaSuccess;
 }
 inline size_t esize(int32_t dt) { return dt == SPEC_F32 ? 4 : 2; }

@@ -36,6 +36,7 @@ constexpr int kGridCap = 4096;        // most CTAs of one streaming pass
 constexpr int kMaxBatch = 65536;      // arrival counters in the workspace header
 constexpr size_t kHeaderBytes = (size_t)kMaxBatch * 4 + 256;  // arrival counters + error words
 constexpr size_t kErrWordOffset = (size_t)kMaxBatch * 4;        // device error flags (bit 0: a wait timed out)
+
 constexpr int kSeqTimeout = 6;                                   // per-sequence status after a timed-out wait
 constexpr size_t kSampStageMax = 112 * 1024;                     // staged row-pair chunk per sampler CTA
 constexpr int64_t kMaxVocab = (int64_t)kMaxCluster * kMaxTilesPerCta * kTile;
@@ -66,7 +67,7 @@ struct StatsParams {
     int64_t V, rows_t, rows_d, N, chunk;
     int32_t S;   // partial slots (CTA pieces) per row
     int32_t pw;  // partials per slot (1: one per CTA piece; kTmaConsumerWarps: one per consumer warp)
-    int32_t tma; // 1: TMA-pipelined variant
+    int32_t tma; // 1: TMA-pipelined variant (finalize runs as its own kernel)
     int32_t B, gmax, grid;
     const int64_t* tro;
     const int64_t* dro;
@@ -118,6 +119,9 @@ struct Layout {
 Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int greedy, int64_t grid_cap, int pw);
 
 cudaError_t launch_stats(const StatsParams& p, cudaStream_t s);
+// TMA variant only: the per-sequence finalize (one warp each), chained to the
+// streaming pass by programmatic launch.
+cudaError_t launch_finalize(const StatsParams& p, cudaStream_t s);
 int stats_resident_ctas(int device, int greedy);  // CTAs that fit at once on the device (plain-load variant)
 cudaError_t launch_sampler(const SampleParams& p, int32_t B, cudaStream_t s, bool pdl);
 struct SampPlan {

@@ -29,7 +29,6 @@ namespace {
 
 constexpr int kWarps = kStatsThreads / 32;
 constexpr int kMaxGamma = 64;
-constexpr int kMaxGroups = 64;  // arrival groups per batch (at most one thread each)
 constexpr int kUnroll = 4;
 
 enum Mode { kLogits = 0, kProbs = 1, kArgmax = 2 };
@@ -44,12 +43,6 @@ struct Smem {
     int32_t xt[kMaxGamma];
     int32_t pick[kMaxGamma + 1];
     int32_t status, accepted, flag_tok, is_last;
-    // batched arrivals of the TMA variant
-    int32_t grp_b[kMaxGroups];
-    uint32_t grp_n[kMaxGroups];
-    int32_t grp_last[kMaxGroups];
-    int32_t ngroups;
-    int64_t next_r;
 };
 
 __device__ __forceinline__ int64_t tro_at(const StatsParams& p, int64_t b) {
@@ -791,7 +784,28 @@ __device__ __forceinline__ void warp_segment(LaneAcc& a, uint32_t sa, int nvec, 
     }
 }
 
-// Identity partial of a row nobody in this warp touched.
+// ------------------------------------------------- finalize helpers (TMA variant)
+// Partials of row r: nseg_of(r) CTA slices of pw warp partials each, stored
+// contiguously from (r * S) * pw; a warp that folded nothing of the row
+// stored the identity.
+__device__ __forceinline__ int32_t pieces_of_row(const StatsParams& p, int64_t r) {
+    return (int32_t)nseg_of(r, p.V, p.chunk) * p.pw;
+}
+
+__device__ void warp_write_error(const StatsParams& p, int32_t b, int32_t st, int64_t t0, int32_t g) {
+    const int lane = threadIdx.x & 31;
+    if (st != 4)
+        for (int i = lane; i <= g; i += 32) p.out_tokens[t0 + i] = -1;
+    if (lane == 0) {
+        p.out_accepted[b] = 0;
+        const int32_t kv = p.kv_in ? p.kv_in[b] : 0;
+        if (p.kv_out) p.kv_out[b] = kv;
+        if (p.out_blocks) p.out_blocks[b] = p.block_size > 0 ? (kv + p.block_size - 1) / p.block_size : 0;
+        if (p.seq_status) p.seq_status[b] = st;
+        if (!p.greedy) p.tasks[b].mode = kTaskNone;
+    }
+}
+
 __device__ __forceinline__ float2 ident_partial(const StatsParams& p, int64_t r) {
     if (p.greedy) return make_float2(-INFINITY, __int_as_float(INT32_MAX));
     if (r >= p.rows_t && p.probs) return make_float2(0.f, 0.f);
@@ -843,7 +857,6 @@ struct WarpRing {
 };
 
 __global__ void __launch_bounds__(kTmaThreads, 1) stats_tma_kernel(StatsParams p) {
-    __shared__ Smem sm;
     __shared__ WarpRing wr;
     extern __shared__ __align__(128) char ring[];
     pdl_launch_dependents();
@@ -856,15 +869,6 @@ __global__ void __launch_bounds__(kTmaThreads, 1) stats_tma_kernel(StatsParams p
         fence_barrier_init();
     }
     __syncthreads();
-
-    if (p.tro) {  // sequences that own no row (broken offsets) still get outputs
-        for (int32_t b = blockIdx.x; b < p.B; b += gridDim.x) {
-            if (expected_elements(p, b) == 0) {
-                finalize(p, b, sm);
-                __syncthreads();
-            }
-        }
-    }
 
     const int64_t e0 = (int64_t)blockIdx.x * p.chunk;
     const int64_t e1 = min(p.N, e0 + p.chunk);
@@ -991,66 +995,225 @@ __global__ void __launch_bounds__(kTmaThreads, 1) stats_tma_kernel(StatsParams p
     if (lane == 0) {
         for (uint32_t q = done; q < copies; ++q)
             mbar_wait_bounded(&full[q % kTmaStages], (q / kTmaStages) & 1, kWaitLimit);
-        __threadfence();  // partials before the arrivals below
     }
     __syncthreads();
     if (threadIdx.x == 0 && wr.failed) atomicOr(p.err, 1u);
 
-    // Arrivals for every (sequence, part) group of rows the CTA range touches,
-    // made in parallel by one thread per group, in batches of kMaxGroups;
-    // then the CTA finalizes the sequences it completed.
-    int64_t next_r = R0;  // same value in every thread
-    while (next_r <= R1) {
-        if (threadIdx.x == 0) {
-            int n = 0;
-            int32_t pb = -1;
-            uint32_t pn = 0;
-            bool pdraft = false;
-            int64_t rr = next_r;
-            for (; rr <= R1 && n < kMaxGroups - 1; ++rr) {
-                const bool is_t = rr < p.rows_t;
-                const int32_t b = seq_of_row(p, !is_t, is_t ? rr : rr - p.rows_t);
-                if (b != pb || (!is_t) != pdraft) {
-                    if (pb >= 0 && pn) {
-                        sm.grp_b[n] = pb;
-                        sm.grp_n[n++] = pn;
-                    }
-                    pb = b;
-                    pn = 0;
-                    pdraft = !is_t;
+}
+
+// Finalize of the TMA variant: one CTA per sequence, after the streaming grid
+// has completed (programmatic launch; the wait returns once every partial of
+// that grid is visible). The same decisions as finalize_sample /
+// finalize_greedy, arranged for few dependent memory round trips: warp 0
+// issues every check's load at once, the CTA's warps merge one row each
+// (lane q loads partial q of the row, a coalesced read), and warp 0 takes the
+// accept decisions by ballot.
+constexpr int kFinThreads = 256;
+constexpr int kFinWarps = kFinThreads / 32;
+
+struct FinSmem {
+    float2 rs[2 * kMaxGamma + 1];
+    int64_t t0, d0;
+    int32_t g, status;
+};
+
+// Merge the n partials at src over the warp (all lanes get the result).
+__device__ float2 warp_merge_ms(const float2* src, int32_t n, bool probs_row, float k) {
+    const int lane = threadIdx.x & 31;
+    float2 acc = make_float2(probs_row ? 0.f : -INFINITY, 0.f);
+    for (int32_t q = lane; q < n; q += 32) {
+        const float2 v = ld_cg_f2(src + q);
+        acc = probs_row ? make_float2(0.f, acc.y + v.y) : ms_merge(acc, v, k);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float2 w = make_float2(__shfl_xor_sync(0xffffffffu, acc.x, o), __shfl_xor_sync(0xffffffffu, acc.y, o));
+        acc = probs_row ? make_float2(0.f, acc.y + w.y) : ms_merge(acc, w, k);
+    }
+    return acc;
+}
+
+__device__ void warp_merge_am(const float2* src, int32_t n, float& v, int32_t& ix) {
+    const int lane = threadIdx.x & 31;
+    v = -INFINITY;
+    ix = INT32_MAX;
+    for (int32_t q = lane; q < n; q += 32) {
+        const float2 w = ld_cg_f2(src + q);
+        const int32_t wi = __float_as_int(w.y);
+        if (am_better(w.x, wi, v, ix)) {
+            v = w.x;
+            ix = wi;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am_merge_shfl(v, ix, o);
+}
+
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
+    __shared__ FinSmem fs;
+    pdl_launch_dependents();
+    pdl_wait_primary();
+    const int32_t b = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // warp 0: the status checks (their loads issued together), then, for
+    // positions lane and lane + 32, the draft token, the two logits at it and
+    // u_acc, fetched while the other warps merge rows
+    int32_t x[2] = {0, 0};
+    float lt[2] = {0.f, 0.f}, ld[2] = {0.f, 0.f}, ua[2] = {0.f, 0.f};
+    int32_t kv = 0;
+    if (warp == 0) {
+        const int64_t t0 = tro_at(p, b), t1 = tro_at(p, b + 1);
+        const int64_t d0 = dro_at(p, b), d1 = dro_at(p, b + 1);
+        const float T = p.greedy ? 1.f : temp_of(p, b);
+        kv = p.kv_in ? __ldg(p.kv_in + b) : 0;
+        const int64_t gg = d1 - d0;
+        int32_t st = 0;
+        if (gg < 0 || gg > p.gmax || t1 - t0 != gg + 1 || t0 < 0 || t1 > p.rows_t || d0 < 0 || d1 > p.rows_d)
+            st = 4;  // SPEC_SEQ_BAD_LAYOUT
+        const int32_t g = (int32_t)gg;
+        if (!st && !p.greedy && (!(T > 0.f) || !isfinite(T))) st = 5;  // SPEC_SEQ_BAD_TEMP
+        if (!st) {
+            bool bad = false;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = lane + 32 * h;
+                if (i < g) {
+                    x[h] = __ldg(p.tokens + d0 + i);
+                    bad |= (x[h] < 0 || x[h] >= p.V);
                 }
-                if (b >= 0) pn += (uint32_t)(min(e1, (rr + 1) * p.V) - max(e0, rr * p.V));
             }
-            if (pb >= 0 && pn) {
-                sm.grp_b[n] = pb;
-                sm.grp_n[n++] = pn;
+            for (int i = lane + 64; i < g; i += 32) {  // gamma_max <= 64: at most one more
+                const int32_t xx = __ldg(p.tokens + d0 + i);
+                bad |= (xx < 0 || xx >= p.V);
             }
-            sm.ngroups = n;
-            sm.next_r = rr;
+            if (__any_sync(0xffffffffu, bad)) st = 1;  // SPEC_SEQ_BAD_TOKEN
         }
-        __syncthreads();
-        next_r = sm.next_r;
-        const int ng = sm.ngroups;
-        if (threadIdx.x < ng) {
-            const int32_t b = sm.grp_b[threadIdx.x];
-            const uint32_t cnt = sm.grp_n[threadIdx.x];
-            __threadfence();  // this CTA's partials before its arrival
-            const uint32_t old = atomicAdd(p.counters + b, cnt);
-            const bool last = old + cnt == expected_elements(p, b);
-            if (last) {
-                p.counters[b] = 0;  // every element of b has arrived: ready for the next call
-                __threadfence();
-            }
-            sm.grp_last[threadIdx.x] = last;
+        if (!st && p.kv_in && kv < g) st = 2;  // SPEC_SEQ_BAD_KV
+        if (lane == 0) {
+            fs.t0 = t0;
+            fs.d0 = d0;
+            fs.g = g;
+            fs.status = st;
         }
-        __syncthreads();
-        for (int gi = 0; gi < ng; ++gi) {
-            if (sm.grp_last[gi]) {
-                finalize(p, sm.grp_b[gi], sm);
-                __syncthreads();
+        if (!st && !p.greedy) {
+            const int tes = p.tdt == SPECV_F32 ? 4 : 2, des = p.ddt == SPECV_F32 ? 4 : 2;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = lane + 32 * h;
+                if (i < g) {
+                    lt[h] = ld_elem_rt((const char*)p.tgt + (t0 + i) * p.V * tes, p.tdt, x[h]);
+                    ld[h] = ld_elem_rt((const char*)p.dft + (d0 + i) * p.V * des, p.ddt, x[h]);
+                    ua[h] = p.uniforms ? __ldg(p.uniforms + 2 * (t0 + i))
+                                       : draw_uniforms(p.seed, p.round, p.seq_offset + (uint32_t)b, (uint32_t)i).x;
+                }
             }
         }
-        __syncthreads();  // the group lists are rewritten by the next batch
+    }
+    __syncthreads();
+    const int64_t t0 = fs.t0, d0 = fs.d0;
+    const int32_t g = fs.g;
+    if (fs.status) {
+        if (warp == 0) warp_write_error(p, b, fs.status, t0, g);
+        return;
+    }
+    const float k = p.greedy ? 1.f : kLog2e / temp_of(p, b);
+    const int nrows = p.greedy ? g + 1 : 2 * g + 1;  // rows 0..g target, g+1..2g draft
+    for (int j = warp; j < nrows; j += kFinWarps) {
+        const bool is_t = j <= g;
+        const int64_t r = is_t ? (t0 + j) : (p.rows_t + d0 + (j - g - 1));
+        const float2* src = p.partials + r * p.S * p.pw;
+        const int32_t n = pieces_of_row(p, r);
+        float2 v;
+        if (p.greedy) {
+            int32_t ix;
+            warp_merge_am(src, n, v.x, ix);
+            if (ix == INT32_MAX) ix = 0;  // every logit -inf or NaN: the first index
+            v.y = __int_as_float(ix);
+        } else {
+            v = warp_merge_ms(src, n, !is_t && p.probs, k);
+        }
+        if (lane == 0) {
+            fs.rs[j] = v;
+            p.row_stats[r] = v;
+        }
+    }
+    __syncthreads();
+    if (warp != 0) return;
+    if (p.greedy) {
+        int32_t a = g;
+        for (int base = 0; base < g; base += 32) {
+            const int i = base + lane;
+            const int32_t xi = base == 0 ? x[0] : (base == 32 ? x[1] : (i < g ? __ldg(p.tokens + d0 + i) : 0));
+            const bool miss = i < g && xi != __float_as_int(fs.rs[i].y);
+            const uint32_t m = __ballot_sync(0xffffffffu, miss);
+            if (m) {
+                a = base + __ffs(m) - 1;
+                break;
+            }
+        }
+        for (int i = lane; i <= g; i += 32)
+            p.out_tokens[t0 + i] = (i < a) ? __ldg(p.tokens + d0 + i) : (i == a ? __float_as_int(fs.rs[a].y) : -1);
+        if (lane == 0) write_ok(p, b, g, a);
+        return;
+    }
+    // accept scan: the first position that is rejected or needs a bad row
+    int32_t a = g, s2 = 0;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int base = 32 * h;
+        if (base >= g || a < g || s2) break;
+        const int i = base + lane;
+        bool stop = false, bad = false;
+        if (i < g) {
+            const float2 ts = fs.rs[i], ds = fs.rs[g + 1 + i];
+            bad = !row_ok(ts, false) || !row_ok(ds, p.probs != 0);
+            const float pxv = ex2(__fmaf_rn(lt[h], k, -__fmul_rn(ts.x, k))) * (1.0f / ts.y);
+            const float qxv =
+                p.probs ? ld[h] * (1.0f / ds.y) : ex2(__fmaf_rn(ld[h], k, -__fmul_rn(ds.x, k))) * (1.0f / ds.y);
+            p.pq[d0 + i] = make_float2(pxv, qxv);
+            stop = bad || !(__fmul_rn(ua[h], qxv) < pxv);
+        }
+        const uint32_t m = __ballot_sync(0xffffffffu, stop);
+        if (m) {
+            const int f = __ffs(m) - 1;
+            if (__shfl_sync(0xffffffffu, bad, f)) s2 = 3;  // SPEC_SEQ_BAD_ROW
+            else a = base + f;
+        }
+    }
+    if (!s2 && a == g && !row_ok(fs.rs[g], false)) s2 = 3;
+    if (s2) {
+        warp_write_error(p, b, s2, t0, g);
+        return;
+    }
+#pragma unroll
+    for (int h = 0; h < 3; ++h) {
+        const int i = lane + 32 * h;
+        if (i <= g) p.out_tokens[t0 + i] = (i < a) ? (h < 2 ? x[h] : __ldg(p.tokens + d0 + i)) : -1;
+    }
+    if (lane == 0) {
+        p.out_accepted[b] = a;
+        if (p.kv_out || p.out_blocks) {
+            const int32_t kvo = p.kv_in ? kv - (g - a) : 0;
+            if (p.kv_out) p.kv_out[b] = kvo;
+            if (p.out_blocks) p.out_blocks[b] = p.block_size > 0 ? (kvo + p.block_size - 1) / p.block_size : 0;
+        }
+        if (p.seq_status) p.seq_status[b] = 0;
+        SampleTask t;
+        t.mode = a < g ? kTaskResidual : kTaskBonus;
+        t.probs = p.probs;
+        t.trow = t0 + a;
+        t.drow = a < g ? d0 + a : -1;
+        t.out_slot = t0 + a;
+        t.u = p.uniforms ? __ldg(p.uniforms + 2 * (t0 + a) + 1)
+                         : draw_uniforms(p.seed, p.round, p.seq_offset + (uint32_t)b, (uint32_t)a).y;
+        const df kk = k_of_temperature(temp_of(p, b));
+        t.k_hi = kk.hi;
+        t.k_lo = kk.lo;
+        t.mt = fs.rs[a].x;
+        t.md = a < g ? fs.rs[g + 1 + a].x : 0.f;
+        t.z_hi = t.z_lo = t.st_hi = t.st_lo = t.sd_hi = t.sd_lo = 0.f;
+        t.pad = 0;
+        p.tasks[b] = t;
     }
 }
 
@@ -1089,6 +1252,20 @@ int stats_resident_ctas(int device, int greedy) {
         return 0;
     if (per < 1) per = 1;
     return sms * per;
+}
+
+cudaError_t launch_finalize(const StatsParams& p, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.B);
+    cfg.blockDim = dim3(kFinThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, finalize_kernel, p);
 }
 
 cudaError_t launch_stats(const StatsParams& p, cudaStream_t s) {
