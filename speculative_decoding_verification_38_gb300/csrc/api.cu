@@ -39,6 +39,16 @@ bool device_info(int& dev, DeviceInfo& out) {
 
 inline bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
 
+// 2^(i/64) as float pairs for the sampler's double-float exp2, computed once.
+const Exp2Pairs& exp2_table() {
+    static const Exp2Pairs t = [] {
+        Exp2Pairs x;
+        exp2_pairs(x);
+        return x;
+    }();
+    return t;
+}
+
 thread_local cudaEvent_t t_ev_start = nullptr, t_ev_stop = nullptr;
 
 // Launch the streaming pass (bracketed by the caller's events if the
@@ -251,16 +261,16 @@ SPEC_API spec_status_t spec_verify_sample(const spec_verify_args_t* a, spec_stre
     sp.tdt = p.tdt;
     sp.ddt = p.ddt;
     sp.V = p.V;
-    const SampPlan plan = sampler_plan(dev, p.B, p.V, p.tdt, p.ddt);
-    sp.nsplit = plan.nsplit;
-    sp.vchunk = plan.vchunk;
-    sp.stage_bytes = plan.stage_bytes;
+    sp.B = p.B;
+    sp.ntile = (int32_t)((p.V + kTile - 1) / kTile);
     sp.tasks_in = p.tasks;
     sp.tasks = p.tasks;
+    sp.recs = (TileRec*)((char*)a->workspace + L.off_recs);
     sp.out_tokens = p.out_tokens;
     sp.seq_status = p.seq_status;
     sp.err = (uint32_t*)((char*)a->workspace + kErrWordOffset);
-    if (launch_sampler(sp, p.B, s, true) != cudaSuccess) return SPEC_ERR_CUDA;
+    sp.tab = exp2_table();
+    if (launch_sampler(sp, s, true) != cudaSuccess) return SPEC_ERR_CUDA;
     return SPEC_OK;
 }
 

@@ -26,10 +26,8 @@ constexpr int kTmaThreads = kTmaConsumerWarps * 32;
 constexpr int kTmaStages = SPECV_WS_STAGES;          // stages in each warp's shared-memory ring
 constexpr uint32_t kTmaStageBytes = SPECV_WS_STAGE_BYTES;  // bytes per stage (a multiple of 512)
 static_assert(kTmaConsumerWarps * kTmaStages * kTmaStageBytes <= 200 * 1024, "warp rings exceed shared memory");
-constexpr int kSampThreads = 256;     // threads per CTA of the residual sampler
+constexpr int kSampThreads = 256;     // threads per CTA of the residual sampler (one tile item per warp)
 constexpr int kTile = 1024;           // sampler tile: 32 lanes x 32 contiguous columns
-constexpr int kMaxTilesPerCta = 256;  // sampler smem bound: V <= 8 * 256 * 1024
-constexpr int kMaxCluster = 8;        // portable cluster size
 constexpr int64_t kChunkAlign = 64;   // elements; keeps 16-byte alignment for both dtypes
 constexpr int64_t kMinChunk = 1024;   // smallest slice one CTA streams
 constexpr int kGridCap = 4096;        // most CTAs of one streaming pass
@@ -38,8 +36,7 @@ constexpr size_t kHeaderBytes = (size_t)kMaxBatch * 4 + 256;  // arrival counter
 constexpr size_t kErrWordOffset = (size_t)kMaxBatch * 4;        // device error flags (bit 0: a wait timed out)
 
 constexpr int kSeqTimeout = 6;                                   // per-sequence status after a timed-out wait
-constexpr size_t kSampStageMax = 112 * 1024;                     // staged row-pair chunk per sampler CTA
-constexpr int64_t kMaxVocab = (int64_t)kMaxCluster * kMaxTilesPerCta * kTile;
+constexpr int64_t kMaxVocab = 2097152;                            // largest vocabulary (2^21 columns)
 
 enum TaskMode : int32_t { kTaskNone = 0, kTaskResidual = 1, kTaskBonus = 2 };
 
@@ -53,9 +50,9 @@ struct __align__(16) SampleTask {
     float u;           // u_smp of the sampled position
     float k_hi, k_lo;  // log2(e) / T as a float pair
     float mt, md;      // raw maxima of the target / draft row
+    float it_apx, id_apx;  // 1 / row normaliser of the target / draft row from the streaming pass (~1e-6)
     float z_hi, z_lo;  // written by the sampler: the Z it used
-    float st_hi, st_lo, sd_hi, sd_lo;  // written by the sampler: row normalisers
-    int32_t pad;
+    int32_t pad[3];
 };
 static_assert(sizeof(SampleTask) == 80, "task layout");
 
@@ -93,25 +90,42 @@ struct StatsParams {
     SampleTask* tasks;   // [B]
 };
 
+// Table 2^(i/64), i = 0..63, as float pairs (value = hi + lo).
+struct Exp2Pairs {
+    float hi[64], lo[64];
+};
+
+// One 1024-column tile of a sequence's task rows, as the sampler's first
+// phase leaves it. Values are float pairs (double-float: value = [0] + [1]).
+struct __align__(16) TileRec {
+    float a[2], b[2];      // target / draft weight sums over the columns certainly in max(0, p - q)'s support
+    float st[2], sd[2];    // target / draft weight sums over every column of the tile
+    float uwt[2], uwd[2];  // the weights of the one column whose membership stayed open
+    int32_t nu;            // such columns (more than one: the tile is summed again exactly)
+    int32_t pad[3];
+};
+static_assert(sizeof(TileRec) == 64, "tile record layout");
+
 struct SampleParams {
     const void* tgt;
     const void* dft;
     int32_t tdt, ddt;
     int64_t V;
-    int32_t nsplit;        // CTAs per sequence (cluster size)
-    int64_t vchunk;        // elements per CTA, multiple of kTile
-    uint32_t stage_bytes;  // shared memory per staged row chunk (0: read rows directly)
+    int32_t B;
+    int32_t ntile;         // kTile-column tiles per row
     const SampleTask* tasks_in;
     SampleTask* tasks;
+    TileRec* recs;         // [B * ntile]
     int32_t* out_tokens;
     int32_t* seq_status;   // may be null
     uint32_t* err;         // workspace error word
+    Exp2Pairs tab;         // 2^(i/64), i = 0..63
 };
 
 struct Layout {
     int64_t rows_total, N, chunk;
     int32_t S, grid;
-    size_t off_partials, off_rowstats, off_pq, off_tasks, total;
+    size_t off_partials, off_rowstats, off_pq, off_tasks, off_recs, total;
 };
 
 // Work split and workspace layout for a given problem. grid_cap bounds the
@@ -123,13 +137,8 @@ cudaError_t launch_stats(const StatsParams& p, cudaStream_t s);
 // streaming pass by programmatic launch.
 cudaError_t launch_finalize(const StatsParams& p, cudaStream_t s);
 int stats_resident_ctas(int device, int greedy);  // CTAs that fit at once on the device (plain-load variant)
-cudaError_t launch_sampler(const SampleParams& p, int32_t B, cudaStream_t s, bool pdl);
-struct SampPlan {
-    int nsplit;            // CTAs per sequence (cluster size)
-    int64_t vchunk;        // columns per CTA, multiple of kTile
-    uint32_t stage_bytes;  // shared memory per staged row chunk (0: read rows directly)
-};
-SampPlan sampler_plan(int device, int64_t B, int64_t V, int tdt, int ddt);
+cudaError_t launch_sampler(const SampleParams& p, cudaStream_t s, bool pdl);
+void exp2_pairs(Exp2Pairs& t);  // host: fills the table
 cudaError_t launch_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,
                                const int32_t* gammas, int32_t gmax, int32_t B, int32_t block_size,
                                int32_t* out_blocks, int32_t* seq_status, cudaStream_t s);

@@ -109,10 +109,8 @@ __device__ __forceinline__ df k_of_temperature(float T) {
     return df{hi, (float)(k - (double)hi)};
 }
 
-// Table 2^(i/64), i = 0..63, as float pairs; filled once per CTA.
-struct Exp2Table {
-    float hi[64], lo[64];
-};
+// Table 2^(i/64), i = 0..63, as float pairs.
+using Exp2Table = Exp2Pairs;
 static __device__ __noinline__ void exp2_table_init(Exp2Table& t) {
     for (int i = threadIdx.x; i < 64; i += blockDim.x) {
         const double v = exp2((double)i / 64.0);

@@ -10,23 +10,23 @@
 // rejection (p == q to rounding) the same rule runs on p_i; if rounding leaves
 // no index, the last one with positive weight is taken.
 //
-// Only the selected row pair is re-read. Each sequence gets one thread-block
-// cluster of nsplit CTAs, CTA c owning a contiguous column chunk, which it
-// stages into shared memory with one TMA bulk copy per row (rows whose chunk
-// is not 16-byte aligned are read from global memory instead). Then:
-//   pass A (residual only): the exact normalisers S = sum_j 2^((l_j - l_max) k)
-//     of both rows, reduced over the cluster through distributed shared memory;
-//   pass B: the weights r_j (= max(0, p_j - q_j), or p_j's weight for a bonus)
-//     tile by tile (a tile = 32 lanes x 32 consecutive columns), each tile's
-//     sum kept in shared memory; chunk sums are exchanged across the cluster so
-//     every CTA knows Z and where its chunk starts in the CDF;
-//   the CTA whose interval holds u * Z finds the tile with one warp-wide
-//   prefix over its tile sums and rescans that tile to find the column.
-// Weights, sums and prefixes are double-float (precise.cuh), so the pick
-// matches a float64 evaluation except within ~1e-10 of a CDF edge.
+// Only the selected row pair is re-read, once. The work is split into tile
+// items (one sequence x one tile of kTile columns), one warp each:
+//   phase 1 (every item): the weights w_t = 2^((l - l_max) k) of both rows over
+//     the tile, summed over every column (the exact normalisers S_t, S_d are
+//     the sums over all tiles) and over the columns that are certainly in the
+//     residual's support. Support membership p > q is decided with the
+//     streaming pass's approximate normalisers and a relative margin of 1e-4;
+//     since the residual is linear in 1/S_t and 1/S_d on a fixed support, the
+//     tile's residual sum is then exactly  A / S_t - B / S_d  plus the columns
+//     the margin left open (kept apart, at most one per tile; a tile with more
+//     is summed again once the normalisers are known).
+//   phase 2 (the warp that finishes a sequence's last tile): S_t, S_d, the tile
+//     sums and Z in double precision, the tile holding u * Z by a prefix over
+//     the tile sums, and one exact rescan of that tile for the column.
+// Weights and their sums are double-float (precise.cuh), so the pick matches
+// a float64 evaluation except within ~1e-10 of a CDF edge.
 #include <math.h>
-
-#include <mutex>
 
 #include "precise.cuh"
 
@@ -35,19 +35,14 @@ namespace specv {
 namespace {
 
 constexpr int kWarps = kSampThreads / 32;
-constexpr int kQCap = 128;  // entries per warp queue (power of two)
+constexpr int kQCap = 128;      // entries per warp queue (power of two)
+constexpr float kMargin = 1e-4f;  // relative margin of the approximate support test
 
 struct SampSmem {
     Exp2Table tab;
-    df tile_sum[kMaxTilesPerCta];
-    df norm_t[kMaxCluster], norm_d[kMaxCluster];
-    df zc[kMaxCluster], zc2[kMaxCluster];
-    df red_t[kWarps], red_d[kWarps];
-    float okflag[kMaxCluster];
-    int32_t q[kWarps][kQCap];  // per-warp queue of heavy items awaiting dense evaluation
-    uint64_t bar;
-    int32_t sel_tile;
-    df sel_base;
+    int32_t q[kWarps][kQCap];  // per-warp queue of columns awaiting double-float evaluation
+    int32_t nu[kWarps];        // open columns found by each warp in its current tile
+    float uw[kWarps][4];       // the first one's weights (wt hi, lo, wd hi, lo)
 };
 
 // One row's chunk: column j (0-based within the chunk) lives in shared memory
@@ -278,99 +273,6 @@ __device__ __forceinline__ bool wq_push(int32_t* q, uint32_t head, uint32_t& tai
     return true;
 }
 
-// Pass A item: bit 30 = draft row, low bits = chunk column.
-template <int TDT, int DDT>
-__device__ __forceinline__ void norm_item(const RowPair<TDT, DDT>& rp, int32_t it, const Exp2Table& tab, df& at,
-                                          df& ad) {
-    const int64_t j = it & 0x3fffffff;
-    if (it & (1 << 30)) {
-        const float l = src_elem<DDT>(rp.d, j);
-        acc_add(ad, rp.probs ? df{l, 0.f} : heavy_logit_weight<DDT == SPECV_F32>(l, rp.md, rp.k, tab));
-    } else {
-        acc_add(at, heavy_logit_weight<TDT == SPECV_F32>(src_elem<TDT>(rp.t, j), rp.mt, rp.k, tab));
-    }
-}
-
-// Pass A: exact normalisers of both rows over this CTA's chunk (block sums,
-// valid in warp 0). Each warp covers 256 contiguous columns per step.
-template <int TDT, int DDT>
-__device__ void chunk_norms(const RowPair<TDT, DDT>& rp, int64_t n, SampSmem& sm, df& St, df& Sd) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    int32_t* q = sm.q[warp];
-    uint32_t head = 0, tail = 0;
-    df at{0.f, 0.f}, ad{0.f, 0.f};
-    for (int64_t base = (int64_t)warp * 256; base < n; base += (int64_t)kWarps * 256) {
-        const int64_t j = base + lane * 8;
-        float lt[8], ld[8];
-        src_load8<TDT>(rp.t, j, lt);
-        src_load8<DDT>(rp.d, j, ld);
-        float gt = 0.f, gd = 0.f;
-        uint32_t m = 0;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            bool h;
-            const float w = light_weight<TDT == SPECV_F32>(lt[e], rp.mt, rp.k, h);
-            if (h) m |= 1u << e; else gt = __fadd_rn(gt, w);
-            if (rp.probs) {
-                const float v = ld[e] > -INFINITY ? ld[e] : 0.f;
-                if (v > 1.220703125e-4f) m |= 1u << (8 + e); else gd = __fadd_rn(gd, v);
-            } else {
-                const float wd = light_weight<DDT == SPECV_F32>(ld[e], rp.md, rp.k, h);
-                if (h) m |= 1u << (8 + e); else gd = __fadd_rn(gd, wd);
-            }
-        }
-        acc_add(at, light_sum_df(gt, kEx2LightBias));
-        acc_add(ad, light_sum_df(gd, rp.probs ? 0.f : kEx2LightBias));
-        const auto code = [&](int b) { return (int32_t)((j + (b & 7)) | (b >= 8 ? (1 << 30) : 0)); };
-        if (!wq_push(q, head, tail, m, code)) {  // queue full: evaluate in place
-            while (m) {
-                const int b = __ffs(m) - 1;
-                m &= m - 1;
-                norm_item(rp, code(b), sm.tab, at, ad);
-            }
-        }
-        while (tail - head >= 32) {
-            norm_item(rp, q[(head + lane) & (kQCap - 1)], sm.tab, at, ad);
-            head += 32;
-            __syncwarp();
-        }
-    }
-    if (lane < (int)(tail - head)) norm_item(rp, q[(head + lane) & (kQCap - 1)], sm.tab, at, ad);
-    at = warp_sum_df(df_norm(at));
-    ad = warp_sum_df(df_norm(ad));
-    if (lane == 0) {
-        sm.red_t[warp] = at;
-        sm.red_d[warp] = ad;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        at = lane < kWarps ? sm.red_t[lane] : df{0.f, 0.f};
-        ad = lane < kWarps ? sm.red_d[lane] : df{0.f, 0.f};
-        at = warp_sum_df(at);
-        ad = warp_sum_df(ad);
-    }
-    St = at;
-    Sd = ad;
-}
-
-// Pass B: tile sums in index order into smem; returns the chunk total (warp 0).
-template <int TDT, int DDT>
-__device__ df chunk_tiles(const RowPair<TDT, DDT>& rp, int ntiles, int mode, df It, df Id, float cl,
-                          SampSmem& sm) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int ti = warp; ti < ntiles; ti += kWarps) {
-        const df tot = warp_sum_df(lane_tile_sum(rp, (int64_t)ti * kTile, mode, It, Id, cl, sm));
-        if (lane == 0) sm.tile_sum[ti] = tot;
-    }
-    __syncthreads();
-    df z{0.f, 0.f};
-    if (warp == 0) {
-        for (int ti = lane; ti < ntiles; ti += 32) z = df_add(z, sm.tile_sum[ti]);
-        z = warp_sum_df(z);
-    }
-    return z;
-}
-
 // One warp walks the selected tile in index order from CDF position `base`
 // and returns the first chunk column whose running sum exceeds thr (or, if
 // rounding leaves none, the last column with weight; -1 if the tile has none).
@@ -422,345 +324,465 @@ __device__ int64_t rescan_tile(const RowPair<TDT, DDT>& rp, int64_t tile_j, int 
     return last;
 }
 
-// Publish thread 0's value into slot c of every CTA in the cluster.
-__device__ __forceinline__ void cluster_publish(df* slots, uint32_t c, int ns, df v) {
-    if (threadIdx.x == 0)
-        for (int r = 0; r < ns; ++r) {
-            st_cluster_f32(&slots[c].hi, r, v.hi);
-            st_cluster_f32(&slots[c].lo, r, v.lo);
-        }
-    cluster_sync_all();
+
+// Tile records are read back through L2 (other SMs wrote them during this grid).
+__device__ __forceinline__ double dd(const float (&v)[2]) {
+    const float2 x = __ldcg(reinterpret_cast<const float2*>(v));
+    return (double)x.x + (double)x.y;
+}
+__device__ __forceinline__ df to_df(double x) {
+    const float h = (float)x;
+    return df{h, (float)(x - (double)h)};
+}
+__device__ __forceinline__ void put(float (&v)[2], df x) {
+    v[0] = x.hi;
+    v[1] = x.lo;
+}
+__device__ __forceinline__ double warp_sum_d(double x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+__device__ __forceinline__ double warp_scan_d(double x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    return x;
 }
 
-// Stage one row chunk (n columns of esz bytes at g) into shared memory at s:
-// a bulk copy of the 16-byte aligned body (thread 0), plain loads for the
-// short tail.
-__device__ __forceinline__ void stage_row(const char* g, char* s, int64_t n, int esz, uint64_t* bar) {
-    const uint32_t bytes = (uint32_t)(n * esz);
-    const uint32_t body = bytes & ~15u;
-    if (threadIdx.x == 0 && body) bulk_g2s(s, g, body, bar);
-    for (uint32_t b = body + threadIdx.x; b < bytes; b += blockDim.x) s[b] = __ldg(g + b);
+// The row pair of task t restricted to tile `tile` (columns read from global
+// memory; 16-byte loads where the tile start is aligned).
+template <int TDT, int DDT>
+__device__ __forceinline__ RowPair<TDT, DDT> tile_rows(const SampleParams& p, const SampleTask& t, int32_t tile) {
+    constexpr int te = TDT == SPECV_F32 ? 4 : 2, de = DDT == SPECV_F32 ? 4 : 2;
+    const int64_t c0 = (int64_t)tile * kTile;
+    const int64_t n = min((int64_t)kTile, p.V - c0);
+    const bool resid = t.mode == kTaskResidual;
+    RowPair<TDT, DDT> rp;
+    rp.t.g = (const char*)p.tgt + (t.trow * p.V + c0) * te;
+    rp.d.g = resid ? (const char*)p.dft + (t.drow * p.V + c0) * de : rp.t.g;
+    rp.t.n = rp.d.n = n;
+    rp.t.al = ((uintptr_t)rp.t.g & 15u) == 0;
+    rp.d.al = ((uintptr_t)rp.d.g & 15u) == 0;
+    rp.t.staged = rp.d.staged = false;
+    rp.t.s = rp.d.s = 0;
+    rp.probs = t.probs != 0;
+    rp.mt = t.mt;
+    rp.md = t.md;
+    rp.k = df{t.k_hi, t.k_lo};
+    return rp;
+}
+
+// Phase 1 for one tile: this lane's sums (double-float) over its columns.
+struct TileAcc {
+    df st, sd, a, b;
+};
+
+template <int TDT, int DDT>
+__device__ void tile_sums(const RowPair<TDT, DDT>& rp, bool resid, float r_hi, float r_lo, SampSmem& sm,
+                          TileAcc& out) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int32_t* q = sm.q[warp];
+    uint32_t head = 0, tail = 0;
+    float st_l = 0.f, sd_l = 0.f, a_l = 0.f, b_l = 0.f;
+    df st_h{0.f, 0.f}, sd_h{0.f, 0.f}, a_h{0.f, 0.f}, b_h{0.f, 0.f};
+    constexpr int32_t kOpen = 1 << 30;  // queued light column whose weights are already in st / sd
+    // one queued column: double-float weights, then the support decision
+    auto eval = [&](int32_t code) {
+        const int64_t j = code & (kOpen - 1);
+        const df wt = rp.wt(src_elem<TDT>(rp.t, j), sm.tab);
+        if (!resid) {
+            acc_add(st_h, wt);
+            return;
+        }
+        const df wd = rp.wd(src_elem<DDT>(rp.d, j), sm.tab);
+        if (!(code & kOpen)) {
+            acc_add(st_h, wt);
+            acc_add(sd_h, wd);
+        }
+        if (wt.hi == 0.f && wd.hi == 0.f) return;
+        if (wt.hi > wd.hi * r_hi) {
+            acc_add(a_h, wt);
+            acc_add(b_h, wd);
+        } else if (!(wt.hi < wd.hi * r_lo)) {  // still open: kept apart for phase 2
+            const int slot = atomicAdd(&sm.nu[warp], 1);
+            if (slot == 0) {
+                sm.uw[warp][0] = wt.hi;
+                sm.uw[warp][1] = wt.lo;
+                sm.uw[warp][2] = wd.hi;
+                sm.uw[warp][3] = wd.lo;
+            }
+        }
+    };
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+        const int64_t j = g * 256 + lane * 8;
+        float lt[8], ld[8];
+        src_load8<TDT>(rp.t, j, lt);
+        if (resid) src_load8<DDT>(rp.d, j, ld);
+        uint32_t m = 0, open = 0;
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            bool ht, hd = false;
+            const float wt = light_weight<TDT == SPECV_F32>(lt[e], rp.mt, rp.k, ht);
+            if (!resid) {
+                if (ht) m |= 1u << e; else st_l = __fadd_rn(st_l, wt);
+                continue;
+            }
+            float wd;
+            if (rp.probs) {
+                wd = ld[e] > -INFINITY ? ld[e] : 0.f;
+                hd = wd > 1.220703125e-4f;
+            } else {
+                wd = light_weight<DDT == SPECV_F32>(ld[e], rp.md, rp.k, hd);
+            }
+            if (ht || hd) {
+                m |= 1u << e;
+                continue;
+            }
+            st_l = __fadd_rn(st_l, wt);
+            sd_l = __fadd_rn(sd_l, wd);
+            if (wt > wd * r_hi) {  // certainly p > q
+                a_l = __fadd_rn(a_l, wt);
+                b_l = __fadd_rn(b_l, wd);
+            } else if (!(wt < wd * r_lo) && (wt != 0.f || wd != 0.f)) {
+                m |= 1u << e;
+                open |= 1u << e;
+            }
+        }
+        const auto code = [&](int bit) { return (int32_t)((j + bit) | ((open >> bit) & 1u ? kOpen : 0)); };
+        if (!wq_push(q, head, tail, m, code)) {  // queue full: evaluate in place
+            while (m) {
+                const int bit = __ffs(m) - 1;
+                m &= m - 1;
+                eval(code(bit));
+            }
+        }
+        while (tail - head >= 32) {
+            eval(q[(head + lane) & (kQCap - 1)]);
+            head += 32;
+            __syncwarp();
+        }
+    }
+    if (lane < (int)(tail - head)) eval(q[(head + lane) & (kQCap - 1)]);
+    __syncwarp();
+    const float cd = rp.probs ? 0.f : kEx2LightBias;
+    out.st = df_add(df_norm(st_h), light_sum_df(st_l, kEx2LightBias));
+    out.sd = df_add(df_norm(sd_h), light_sum_df(sd_l, cd));
+    out.a = df_add(df_norm(a_h), light_sum_df(a_l, kEx2LightBias));
+    out.b = df_add(df_norm(b_h), light_sum_df(b_l, cd));
+}
+
+// Double-float sums of four per-lane values over the warp, halving the
+// exchanged data at each step: afterwards lanes 8q .. 8q + 7 hold the total
+// of value q.
+__device__ __forceinline__ df warp_sum4_df(df v0, df v1, df v2, df v3) {
+    const int lane = threadIdx.x & 31;
+    // step 16: keep values 0,1 (lanes < 16) or 2,3; add the partner's copy
+    const bool up = lane & 16;
+    df s0 = up ? v2 : v0, s1 = up ? v3 : v1;
+    const df g0 = up ? v0 : v2, g1 = up ? v1 : v3;  // what the partner keeps
+    s0 = df_add(s0, shfl_xor_df(g0, 16));
+    s1 = df_add(s1, shfl_xor_df(g1, 16));
+    // step 8: keep one of the two
+    const bool up8 = lane & 8;
+    df s = up8 ? s1 : s0;
+    const df g = up8 ? s0 : s1;
+    s = df_add(s, shfl_xor_df(g, 8));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) s = df_add(s, shfl_xor_df(s, o));
+    return s;
 }
 
 template <int TDT, int DDT>
 __global__ void __launch_bounds__(kSampThreads) sampler_kernel(SampleParams p) {
     __shared__ SampSmem sm;
-    extern __shared__ __align__(128) char dyn[];
-    pdl_wait_primary();  // tasks are written by the streaming pass
-
-    const int32_t b = blockIdx.x / p.nsplit;
-    const uint32_t c = cluster_ctarank();
-    const SampleTask t = p.tasks_in[b];
-    if (t.mode == kTaskNone) return;  // uniform across the cluster: nobody reaches a barrier
-    exp2_table_init(sm.tab);
-
-    const int64_t cs = (int64_t)c * p.vchunk;
-    const int64_t ce = min(p.V, cs + p.vchunk);
-    const int64_t n = ce > cs ? ce - cs : 0;
-    const int ntiles = (int)((n + kTile - 1) / kTile);
-    constexpr int te = TDT == SPECV_F32 ? 4 : 2, de = DDT == SPECV_F32 ? 4 : 2;
-    const bool resid0 = t.mode == kTaskResidual;
-    RowPair<TDT, DDT> rp;
-    rp.t.g = (const char*)p.tgt + (t.trow * p.V + cs) * te;
-    rp.d.g = resid0 ? (const char*)p.dft + (t.drow * p.V + cs) * de : rp.t.g;
-    rp.t.n = rp.d.n = n;
-    rp.t.al = ((uintptr_t)rp.t.g & 15u) == 0;
-    rp.d.al = ((uintptr_t)rp.d.g & 15u) == 0;
-    rp.t.staged = p.stage_bytes > 0 && rp.t.al && n * te <= (int64_t)p.stage_bytes;
-    rp.d.staged = resid0 && p.stage_bytes > 0 && rp.d.al && n * de <= (int64_t)p.stage_bytes;
-    rp.t.s = smem_addr(dyn);
-    rp.d.s = smem_addr(dyn + p.stage_bytes);
-    rp.probs = t.probs != 0;
-    rp.mt = t.mt;
-    rp.md = t.md;
-    rp.k = df{t.k_hi, t.k_lo};
-
-    // stage the chunk of both rows into shared memory
-    bool ok = true;
-    if (rp.t.staged || rp.d.staged) {
-        if (threadIdx.x == 0) {
-            mbar_init(&sm.bar, 1);
-            fence_barrier_init();
-        }
-        __syncthreads();
-        const uint32_t tb = rp.t.staged ? (uint32_t)(n * te) & ~15u : 0u;
-        const uint32_t db = rp.d.staged ? (uint32_t)(n * de) & ~15u : 0u;
-        if (threadIdx.x == 0) mbar_arrive_expect_tx(&sm.bar, tb + db);
-        if (rp.t.staged) stage_row(rp.t.g, dyn, n, te, &sm.bar);
-        if (rp.d.staged) stage_row(rp.d.g, dyn + p.stage_bytes, n, de, &sm.bar);
-        if (!mbar_wait_bounded(&sm.bar, 0, kWaitLimit)) {
-            ok = false;
-            mbar_wait_bounded(&sm.bar, 0, kWaitLimit);  // let copies in flight land before leaving
-        }
-    }
-    ok = __syncthreads_and(ok);  // also publishes the plain-load tails
-    if (threadIdx.x == 0)
-        for (int r = 0; r < p.nsplit; ++r) st_cluster_f32(&sm.okflag[c], r, ok ? 1.f : 0.f);
-    cluster_sync_all();
-    bool all_ok = true;
-    for (int r = 0; r < p.nsplit; ++r) all_ok = all_ok && sm.okflag[r] > 0.f;
-    if (!all_ok) {  // the whole cluster gives up together
-        if (c == 0 && threadIdx.x == 0) {
-            atomicOr(p.err, 1u);
-            if (p.seq_status) p.seq_status[b] = kSeqTimeout;
-        }
-        return;
-    }
-
-    int mode = t.mode;
-    df It{1.f, 0.f}, Id{1.f, 0.f};
-    if (mode == kTaskResidual) {
-        df St, Sd;
-        chunk_norms(rp, n, sm, St, Sd);
-        cluster_publish(sm.norm_t, c, p.nsplit, St);
-        cluster_publish(sm.norm_d, c, p.nsplit, Sd);
-        df Tt{0.f, 0.f}, Td{0.f, 0.f};
-        for (int r = 0; r < p.nsplit; ++r) {
-            Tt = df_add(Tt, sm.norm_t[r]);
-            Td = df_add(Td, sm.norm_d[r]);
-        }
-        It = df_recip(Tt);
-        Id = df_recip(Td);
-        if (c == 0 && threadIdx.x == 0) {
-            p.tasks[b].st_hi = Tt.hi;
-            p.tasks[b].st_lo = Tt.lo;
-            p.tasks[b].sd_hi = Td.hi;
-            p.tasks[b].sd_lo = Td.lo;
-        }
-    }
-
-    // light-sum correction of the sampling weights: both rows' light weights
-    // carry the same SFU bias unless the draft is given as probabilities
-    float cl = (mode == kTaskResidual && rp.probs) ? 0.f : kEx2LightBias;
-    df zc = chunk_tiles(rp, ntiles, mode, It, Id, cl, sm);
-    cluster_publish(sm.zc, c, p.nsplit, zc);
-    const df* zs = sm.zc;
-    df Z{0.f, 0.f}, lo{0.f, 0.f};
-    for (int r = 0; r < p.nsplit; ++r) {
-        if (r == (int)c) lo = Z;
-        Z = df_add(Z, zs[r]);
-    }
-    if (mode == kTaskResidual && !df_pos(Z)) {
-        // p_i == q_i to rounding: draw from p_i instead
-        mode = kTaskBonus;
-        cl = kEx2LightBias;
-        __syncthreads();
-        zc = chunk_tiles(rp, ntiles, mode, It, Id, cl, sm);
-        cluster_publish(sm.zc2, c, p.nsplit, zc);
-        zs = sm.zc2;
-        Z = df{0.f, 0.f};
-        for (int r = 0; r < p.nsplit; ++r) {
-            if (r == (int)c) lo = Z;
-            Z = df_add(Z, zs[r]);
-        }
-    }
-    if (c == 0 && threadIdx.x == 0) {
-        p.tasks[b].z_hi = Z.hi;
-        p.tasks[b].z_lo = Z.lo;
-    }
-    // threshold u * Z; u has 24 significant bits
-    const df thr = df_add(two_prod(t.u, Z.hi), df{__fmul_rn(t.u, Z.lo), 0.f});
-    const df hi_edge = df_add(lo, zs[c]);
-    bool owner = !df_gt(lo, thr) && df_gt(hi_edge, thr) && df_pos(zs[c]);
-    bool fallback = false;
-    if (!df_gt(Z, thr)) {
-        int last = -1;
-        for (int r = 0; r < p.nsplit; ++r)
-            if (df_pos(zs[r])) last = r;
-        owner = (last == (int)c);
-        fallback = true;
-    }
-    if (!owner) return;
-
-    // locate the tile holding the crossing: one warp, 32 tiles per step
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        int sel = -1;
-        df base = lo;
-        if (!fallback) {
-            df run = lo;
-            for (int t0 = 0; t0 < ntiles && sel < 0; t0 += 32) {
-                const int ti = t0 + lane;
-                const df v = ti < ntiles ? sm.tile_sum[ti] : df{0.f, 0.f};
-                const df end = df_add(run, warp_scan_df(v));
-                const unsigned hit = __ballot_sync(0xffffffffu, ti < ntiles && df_gt(end, thr));
-                if (hit) {
-                    const int src = __ffs(hit) - 1;
-                    sel = t0 + src;
-                    base = shfl_df(df_sub(end, v), src);  // run + exclusive prefix
-                } else {
-                    run = shfl_df(end, 31);
-                }
-            }
-        }
-        int mark = 0;
-        if (sel < 0) {  // rounding left no crossing here: the last tile with mass
-            for (int hi_t = ntiles - 1; hi_t >= 0 && sel < 0; hi_t -= 32) {
-                const int ti = hi_t - lane;
-                const unsigned pos = __ballot_sync(0xffffffffu, ti >= 0 && df_pos(sm.tile_sum[ti >= 0 ? ti : 0]));
-                if (pos) sel = hi_t - (__ffs(pos) - 1);
-            }
-            mark = 1;
-        }
-        if (lane == 0) {
-            sm.sel_tile = sel;
-            sm.sel_base = mark ? df{NAN, 0.f} : base;  // NaN: no comparison succeeds
-        }
+    for (int i = threadIdx.x; i < 64; i += blockDim.x) {
+        sm.tab.hi[i] = p.tab.hi[i];
+        sm.tab.lo[i] = p.tab.lo[i];
     }
     __syncthreads();
-    if (threadIdx.x >= 32 || sm.sel_tile < 0) return;
-
-    // one warp rescans the selected tile in index order
-    const int lane = threadIdx.x;
-    const int64_t jt = rescan_tile(rp, (int64_t)sm.sel_tile * kTile, mode, It, Id, cl, sm.sel_base, thr, sm.tab);
-    const int64_t tok = jt >= 0 ? cs + jt : -1;
-    if (lane == 0 && tok >= 0) p.out_tokens[t.out_slot] = (int32_t)tok;
-}
-
-template <int TDT, int DDT>
-cudaError_t launch_typed(const SampleParams& p, int32_t B, cudaStream_t s, bool pdl) {
-    static bool attr_done = false;  // per instantiation
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(sampler_kernel<TDT, DDT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)kSampStageMax);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
+    pdl_launch_dependents();
+    pdl_wait_primary();  // tasks are written by the finalize step
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t item = (int64_t)blockIdx.x * kWarps + warp;
+    if (item >= (int64_t)p.B * p.ntile) return;
+    const int32_t b = (int32_t)(item / p.ntile), tile = (int32_t)(item - (int64_t)b * p.ntile);
+    const SampleTask t = p.tasks_in[b];
+    if (t.mode == kTaskNone) return;
+    const bool resid = t.mode == kTaskResidual;
+    // approximate support test p > q(1 + m) / p < q(1 - m), i.e. w_t > w_d * r
+    const float ratio = resid ? t.id_apx / t.it_apx : 0.f;
+    const float r_hi = ratio * (1.f + kMargin), r_lo = ratio * (1.f - kMargin);
+    if (lane == 0) sm.nu[warp] = 0;
+    __syncwarp();
+    const RowPair<TDT, DDT> rp = tile_rows<TDT, DDT>(p, t, tile);
+    TileAcc acc;
+    tile_sums(rp, resid, r_hi, r_lo, sm, acc);
+    const df tot = warp_sum4_df(acc.st, acc.sd, resid ? acc.a : acc.st, acc.b);
+    TileRec& r = p.recs[item];
+    if ((lane & 7) == 0) {
+        float* dst = lane == 0 ? r.st : (lane == 8 ? r.sd : (lane == 16 ? r.a : r.b));
+        dst[0] = tot.hi;
+        dst[1] = tot.lo;
     }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(B * p.nsplit));
-    cfg.blockDim = dim3(kSampThreads);
-    cfg.dynamicSmemBytes = 2 * (size_t)p.stage_bytes;
-    cfg.stream = s;
-    cudaLaunchAttribute attrs[2];
-    int na = 0;
-    attrs[na].id = cudaLaunchAttributeClusterDimension;
-    attrs[na].val.clusterDim.x = (unsigned)p.nsplit;
-    attrs[na].val.clusterDim.y = 1;
-    attrs[na].val.clusterDim.z = 1;
-    ++na;
-    if (pdl) {
-        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attrs[na].val.programmaticStreamSerializationAllowed = 1;
-        ++na;
+    if (lane == 1) {
+        r.nu = sm.nu[warp];
+        r.uwt[0] = sm.uw[warp][0];
+        r.uwt[1] = sm.uw[warp][1];
+        r.uwd[0] = sm.uw[warp][2];
+        r.uwd[1] = sm.uw[warp][3];
     }
-    cfg.attrs = attrs;
-    cfg.numAttrs = na;
-    return cudaLaunchKernelEx(&cfg, sampler_kernel<TDT, DDT>, p);
 }
 
-}  // namespace
+// ------------------------------------------------------------- phase 2
+// One CTA per sequence, after every tile record is in (programmatic launch).
+// Thread i owns tiles i*K .. i*K + K - 1 (K = ceil(ntile / 256) <= 8); the
+// tile sums of the sampling weights live in shared memory.
+constexpr int kMaxTiles = (int)(kMaxVocab / kTile);
+constexpr int kMaxPer = kMaxTiles / kSampThreads;
 
-namespace {
-
-template <int TDT, int DDT>
-int active_clusters(int nsplit, uint32_t stage_bytes) {
-    static bool attr_done = false;  // per instantiation
-    if (!attr_done) {
-        if (cudaFuncSetAttribute(sampler_kernel<TDT, DDT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kSampStageMax) != cudaSuccess)
-            return 0;
-        attr_done = true;
-    }
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)nsplit);
-    cfg.blockDim = dim3(kSampThreads);
-    cfg.dynamicSmemBytes = 2 * (size_t)stage_bytes;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeClusterDimension;
-    attr.val.clusterDim.x = (unsigned)nsplit;
-    attr.val.clusterDim.y = 1;
-    attr.val.clusterDim.z = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, (const void*)sampler_kernel<TDT, DDT>, &cfg) != cudaSuccess) return 0;
-    return n;
-}
-
-int active_clusters_rt(int tdt, int ddt, int nsplit, uint32_t stage_bytes) {
-    if (tdt == SPECV_BF16 && ddt == SPECV_BF16) return active_clusters<SPECV_BF16, SPECV_BF16>(nsplit, stage_bytes);
-    if (tdt == SPECV_BF16) return active_clusters<SPECV_BF16, SPECV_F32>(nsplit, stage_bytes);
-    if (ddt == SPECV_BF16) return active_clusters<SPECV_F32, SPECV_BF16>(nsplit, stage_bytes);
-    return active_clusters<SPECV_F32, SPECV_F32>(nsplit, stage_bytes);
-}
-
-struct PlanKey {
-    int device, tdt, ddt;
-    int64_t B, V;
+struct DrawSmem {
+    Exp2Table tab;
+    int32_t q[kWarps][kQCap];  // lane_tile_sum's queues (tiles summed again)
+    double w[kMaxTiles];       // tile sums
+    double red[kWarps];
+    double bc[4];              // broadcasts: St, Sd, Z, run
+    int32_t dirty[kMaxTiles];
+    int32_t ndirty, sel, col, last;
+    double start;
 };
-std::mutex g_plan_mu;
-PlanKey g_plan_key[8];
-SampPlan g_plan_val[8];
-int g_plan_n = 0, g_plan_next = 0;
+
+__device__ __forceinline__ double block_sum_d(double x, DrawSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    x = warp_sum_d(x);
+    __syncthreads();  // red[] is free
+    if (lane == 0) sm.red[warp] = x;
+    __syncthreads();
+    double t = 0.0;
+    for (int i = 0; i < kWarps; ++i) t += sm.red[i];
+    return t;
+}
+
+// Exclusive block-wide prefix of one value per thread (thread order).
+__device__ __forceinline__ double block_excl_scan_d(double x, DrawSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const double incl = warp_scan_d(x);
+    __syncthreads();
+    if (lane == 31) sm.red[warp] = incl;
+    __syncthreads();
+    double before = 0.0;
+    for (int i = 0; i < warp; ++i) before += sm.red[i];
+    return before + incl - x;
+}
+
+// Sampling weight of column j (0-based in the tile) as double-float, and
+// whether it is heavy (summed exactly) or light (summed in fp32 first).
+template <int TDT, int DDT>
+__device__ __forceinline__ df col_weight(const RowPair<TDT, DDT>& rp, int64_t j, int mode, df It, df Id,
+                                         const Exp2Table& tab) {
+    const df wt = rp.wt(src_elem<TDT>(rp.t, j), tab);
+    if (mode != kTaskResidual) return wt;
+    return resid_weight(wt, rp.wd(src_elem<DDT>(rp.d, j), tab), It, Id);
+}
+
+template <int TDT, int DDT>
+__global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
+    __shared__ DrawSmem sm;
+    for (int i = threadIdx.x; i < 64; i += blockDim.x) {
+        sm.tab.hi[i] = p.tab.hi[i];
+        sm.tab.lo[i] = p.tab.lo[i];
+    }
+    if (threadIdx.x == 0) sm.ndirty = 0;
+    pdl_wait_primary();
+    const int32_t b = blockIdx.x;
+    const SampleTask t = p.tasks_in[b];
+    if (t.mode == kTaskNone) return;  // block-uniform
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const TileRec* recs = p.recs + (int64_t)b * p.ntile;
+    const int nt = p.ntile;
+    const int K = (nt + kSampThreads - 1) / kSampThreads;
+    const int t0 = threadIdx.x * K, t1 = min(nt, t0 + K);
+    // the exact normalisers
+    double st = 0.0, sd = 0.0;
+#pragma unroll 1
+    for (int ti = t0; ti < t1; ++ti) {
+        const float4 ss = __ldcg(reinterpret_cast<const float4*>(recs + ti) + 1);
+        st += (double)ss.x + (double)ss.y;
+        sd += (double)ss.z + (double)ss.w;
+    }
+    const double St = block_sum_d(st, sm);
+    const double Sd = block_sum_d(sd, sm);
+    int mode = t.mode;
+    const bool resid = mode == kTaskResidual;
+    const double It = resid ? 1.0 / St : 1.0, Id = resid ? 1.0 / Sd : 1.0;
+    const df Itf = to_df(It), Idf = to_df(Id);
+    float cl = (resid && t.probs) ? 0.f : kEx2LightBias;
+    // tile sums of the sampling weights
+    double z = 0.0;
+#pragma unroll 1
+    for (int ti = t0; ti < t1; ++ti) {
+        const float4* r = reinterpret_cast<const float4*>(recs + ti);
+        double v;
+        if (!resid) {
+            const float4 ss = __ldcg(r + 1);
+            v = (double)ss.x + (double)ss.y;
+        } else {
+            const int32_t nu = __ldcg(reinterpret_cast<const int32_t*>(r + 3));
+            if (nu > 1) {  // more than one open column: summed again below
+                sm.dirty[atomicAdd(&sm.ndirty, 1)] = ti;
+                continue;
+            }
+            const float4 ab = __ldcg(r);
+            v = It * ((double)ab.x + (double)ab.y) - Id * ((double)ab.z + (double)ab.w);
+            if (nu == 1) {
+                const float4 uu = __ldcg(r + 2);
+                v += fmax(0.0, It * ((double)uu.x + (double)uu.y) - Id * ((double)uu.z + (double)uu.w));
+            }
+            v = fmax(v, 0.0);
+        }
+        sm.w[ti] = v;
+        z += v;
+    }
+    __syncthreads();
+    const int nd = sm.ndirty;
+#pragma unroll 1
+    for (int i = warp; i < nd; i += kWarps) {  // one warp per tile, exactly
+        const int ti = sm.dirty[i];
+        const RowPair<TDT, DDT> rp = tile_rows<TDT, DDT>(p, t, ti);
+        const df x = warp_sum_df(lane_tile_sum(rp, 0, mode, Itf, Idf, cl,
+                                               *reinterpret_cast<SampSmem*>(&sm)));
+        if (lane == 0) {
+            sm.w[ti] = (double)x.hi + (double)x.lo;
+            z += sm.w[ti];
+        }
+    }
+    double Z = block_sum_d(z, sm);
+    if (resid && !(Z > 0.0)) {  // p_i == q_i to rounding: draw from p_i instead
+        mode = kTaskBonus;
+        cl = kEx2LightBias;
+        for (int ti = t0; ti < t1; ++ti) {
+            const float4 ss = __ldcg(reinterpret_cast<const float4*>(recs + ti) + 1);
+            sm.w[ti] = (double)ss.x + (double)ss.y;
+        }
+        Z = St;
+    }
+    if (threadIdx.x == 0) {
+        const df zf = to_df(Z);
+        p.tasks[b].z_hi = zf.hi;
+        p.tasks[b].z_lo = zf.lo;
+        sm.sel = -1;
+        sm.last = -1;
+        sm.col = -1;
+    }
+    __syncthreads();
+    // the tile holding the crossing u * Z (u has 24 significant bits)
+    const double thr = (double)t.u * Z;
+    double mine = 0.0;
+    for (int ti = t0; ti < t1; ++ti) mine += sm.w[ti];
+    double run = block_excl_scan_d(mine, sm);
+    int last_here = -1;
+    for (int ti = t0; ti < t1; ++ti) {
+        const double v = sm.w[ti];
+        if (v > 0.0) last_here = ti;
+        if (run + v > thr && run <= thr) {
+            sm.sel = ti;  // the only thread with a crossing
+            sm.start = run;
+        }
+        run += v;
+    }
+    atomicMax(&sm.last, last_here);
+    __syncthreads();
+    int sel = sm.sel;
+    const bool last_mass = sel < 0;
+    if (last_mass) sel = sm.last;  // rounding left no crossing: the last tile with mass
+    if (sel < 0) return;
+    // rescan the selected tile: warp w covers columns w*128 .. +127, 4 per lane
+    const RowPair<TDT, DDT> rp = tile_rows<TDT, DDT>(p, t, sel);
+    const df basef = last_mass ? df{NAN, 0.f} : to_df(sm.start);  // NaN: no comparison succeeds
+    const df thrf = to_df(thr);
+    const int64_t j0 = (int64_t)warp * 128 + lane * 4;
+    df w4[4], pre[4];
+    float light = 0.f;
+    df heavy{0.f, 0.f};
+    int lp = -1;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        w4[e] = j0 + e < rp.t.n ? col_weight(rp, j0 + e, mode, Itf, Idf, sm.tab) : df{0.f, 0.f};
+        if (is_heavy(w4[e]))
+            acc_add(heavy, w4[e]);
+        else
+            light = __fadd_rn(light, w4[e].hi);
+        pre[e] = df_add(df_norm(heavy), light_sum_df(light, cl));
+        if (df_pos(w4[e])) lp = e;
+    }
+    // block prefix of the per-lane sums, in column order (warp-major)
+    const df incl = warp_scan_df(pre[3]);
+    __syncthreads();
+    if (lane == 31) {
+        sm.red[warp] = (double)incl.hi;  // hi and lo of each warp total, kept apart
+        sm.bc[0] = 0.0;
+    }
+    __shared__ float wlo[kWarps];
+    if (lane == 31) wlo[warp] = incl.lo;
+    __syncthreads();
+    df before = basef;
+    for (int i = 0; i < warp; ++i) before = df_add(before, df{(float)sm.red[i], wlo[i]});
+    df excl = shfl_up_df(incl, 1);
+    if (lane == 0) excl = df{0.f, 0.f};
+    const df start = df_add(before, excl);
+    int hit = -1;
+#pragma unroll
+    for (int e = 3; e >= 0; --e)
+        if (df_gt(df_add(start, pre[e]), thrf)) hit = e;
+    // the first column (in order) whose running sum exceeds thr
+    if (hit >= 0) atomicMin((unsigned*)&sm.col, (unsigned)(j0 + hit));
+    if (lp >= 0) atomicMax(&sm.last, (int)(0x40000000 | (j0 + lp)));
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int64_t jt = (sm.col >= 0) ? sm.col : ((sm.last & 0x40000000) ? (sm.last & 0x3fffffff) : -1);
+        if (jt >= 0) p.out_tokens[t.out_slot] = (int32_t)((int64_t)sel * kTile + jt);
+    }
+}
+
+template <int TDT, int DDT>
+cudaError_t launch_typed(const SampleParams& p, cudaStream_t s, bool pdl) {
+    const int64_t items = (int64_t)p.B * p.ntile;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((items + kWarps - 1) / kWarps));
+    cfg.blockDim = dim3(kSampThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, sampler_kernel<TDT, DDT>, p);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((unsigned)p.B);
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, draw_kernel<TDT, DDT>, p);
+}
 
 }  // namespace
 
-// CTAs per sequence (cluster size) and shared-memory staging. Each candidate
-// split n keeps chunks of at least 4096 columns and at most kMaxTilesPerCta
-// tiles; its cost is the number of waves the B clusters need (from the
-// occupancy calculator, which knows how clusters pack into GPCs) times the
-// columns each CTA handles. Staging the row pair in shared memory is used
-// when it fits and does not cost a wave; the cheapest candidate wins, larger
-// splits first on ties. Plans are cached per (device, B, V, dtypes).
-SampPlan sampler_plan(int device, int64_t B, int64_t V, int tdt, int ddt) {
-    {
-        std::lock_guard<std::mutex> lk(g_plan_mu);
-        for (int i = 0; i < g_plan_n; ++i) {
-            const PlanKey& k = g_plan_key[i];
-            if (k.device == device && k.B == B && k.V == V && k.tdt == tdt && k.ddt == ddt) return g_plan_val[i];
-        }
+void exp2_pairs(Exp2Pairs& t) {
+    for (int i = 0; i < 64; ++i) {
+        const double v = exp2((double)i / 64.0);
+        t.hi[i] = (float)v;
+        t.lo[i] = (float)(v - (double)t.hi[i]);
     }
-    const int64_t et = tdt == SPECV_F32 ? 4 : 2, ed = ddt == SPECV_F32 ? 4 : 2;
-    const int64_t need = (V + (int64_t)kMaxTilesPerCta * kTile - 1) / ((int64_t)kMaxTilesPerCta * kTile);
-    int64_t hi = V / 4096;
-    if (hi > kMaxCluster) hi = kMaxCluster;
-    if (hi < need) hi = need;
-    if (hi < 1) hi = 1;
-    SampPlan best{};
-    double best_cost = -1.0;
-    for (int64_t n = hi; n >= (need < 1 ? 1 : need); --n) {
-        const int64_t per = (V + n - 1) / n;
-        const int64_t vchunk = (per + kTile - 1) / kTile * kTile;
-        const int64_t row_bytes = (vchunk * (et > ed ? et : ed) + 15) / 16 * 16;
-        for (int staged = 1; staged >= 0; --staged) {
-            if (staged && 2 * row_bytes > (int64_t)kSampStageMax) continue;
-            const uint32_t sb = staged ? (uint32_t)row_bytes : 0u;
-            const int act = active_clusters_rt(tdt, ddt, (int)n, sb);
-            if (act < 1) continue;
-            const int64_t waves = (B + act - 1) / act;
-            const double cost = (double)waves * (double)vchunk;
-            if (best_cost < 0.0 || cost < best_cost) {
-                best_cost = cost;
-                best.nsplit = (int)n;
-                best.vchunk = vchunk;
-                best.stage_bytes = sb;
-            }
-        }
-    }
-    if (best_cost < 0.0) {  // no occupancy answer: one CTA per sequence, direct reads
-        best.nsplit = (int)(need < 1 ? 1 : need);
-        const int64_t per = (V + best.nsplit - 1) / best.nsplit;
-        best.vchunk = (per + kTile - 1) / kTile * kTile;
-        best.stage_bytes = 0;
-    }
-    std::lock_guard<std::mutex> lk(g_plan_mu);
-    const int slot = g_plan_n < 8 ? g_plan_n++ : (g_plan_next++ & 7);
-    g_plan_key[slot] = PlanKey{device, tdt, ddt, B, V};
-    g_plan_val[slot] = best;
-    return best;
 }
 
-cudaError_t launch_sampler(const SampleParams& p, int32_t B, cudaStream_t s, bool pdl) {
-    cudaError_t e;
-    if (p.tdt == SPECV_BF16 && p.ddt == SPECV_BF16)
-        e = launch_typed<SPECV_BF16, SPECV_BF16>(p, B, s, pdl);
-    else if (p.tdt == SPECV_BF16)
-        e = launch_typed<SPECV_BF16, SPECV_F32>(p, B, s, pdl);
-    else if (p.ddt == SPECV_BF16)
-        e = launch_typed<SPECV_F32, SPECV_BF16>(p, B, s, pdl);
-    else
-        e = launch_typed<SPECV_F32, SPECV_F32>(p, B, s, pdl);
-    return e;
+cudaError_t launch_sampler(const SampleParams& p, cudaStream_t s, bool pdl) {
+    if (p.tdt == SPECV_BF16 && p.ddt == SPECV_BF16) return launch_typed<SPECV_BF16, SPECV_BF16>(p, s, pdl);
+    if (p.tdt == SPECV_BF16) return launch_typed<SPECV_BF16, SPECV_F32>(p, s, pdl);
+    if (p.ddt == SPECV_BF16) return launch_typed<SPECV_F32, SPECV_BF16>(p, s, pdl);
+    return launch_typed<SPECV_F32, SPECV_F32>(p, s, pdl);
 }
 
 }  // namespace specv

@@ -442,6 +442,16 @@ __device__ void merge_row_am(const StatsParams& p, int64_t r, float& v, int32_t&
     for (int o = 16; o > 0; o >>= 1) am_merge_shfl(v, ix, o);
 }
 
+// 1 / (the sampler's normaliser of a logits row), from the streaming pass's
+// (raw max m, s = sum 2^(l k - fl(m k))): the sampler's weights 2^((l - m) k)
+// are s's terms times 2^(fl(m k) - m k). Good to ~1e-6, which is all the
+// sampler's support test asks of it.
+__device__ __forceinline__ float inv_norm_apx(float2 rsv, float k) {
+    const float mk = __fmul_rn(rsv.x, k);
+    const float e = __fmaf_rn(rsv.x, k, -mk);  // m k - fl(m k), exact
+    return 1.0f / (rsv.y * ex2(-e));
+}
+
 __device__ void finalize_sample(const StatsParams& p, int32_t b, Smem& sm) {
     int64_t t0, d0;
     int32_t g;
@@ -519,8 +529,10 @@ __device__ void finalize_sample(const StatsParams& p, int32_t b, Smem& sm) {
             t.k_lo = kk.lo;
             t.mt = sm.rs[a].x;
             t.md = a < g ? sm.rs[g + 1 + a].x : 0.f;
-            t.z_hi = t.z_lo = t.st_hi = t.st_lo = t.sd_hi = t.sd_lo = 0.f;
-            t.pad = 0;
+            t.it_apx = inv_norm_apx(sm.rs[a], k);
+            t.id_apx = a < g ? (p.probs ? 1.0f / sm.rs[g + 1 + a].y : inv_norm_apx(sm.rs[g + 1 + a], k)) : 0.f;
+            t.z_hi = t.z_lo = 0.f;
+            t.pad[0] = t.pad[1] = t.pad[2] = 0;
             p.tasks[b] = t;
         }
     }
@@ -1211,8 +1223,10 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
         t.k_lo = kk.lo;
         t.mt = fs.rs[a].x;
         t.md = a < g ? fs.rs[g + 1 + a].x : 0.f;
-        t.z_hi = t.z_lo = t.st_hi = t.st_lo = t.sd_hi = t.sd_lo = 0.f;
-        t.pad = 0;
+        t.it_apx = inv_norm_apx(fs.rs[a], k);
+        t.id_apx = a < g ? (p.probs ? 1.0f / fs.rs[g + 1 + a].y : inv_norm_apx(fs.rs[g + 1 + a], k)) : 0.f;
+        t.z_hi = t.z_lo = 0.f;
+        t.pad[0] = t.pad[1] = t.pad[2] = 0;
         p.tasks[b] = t;
     }
 }
@@ -1240,6 +1254,8 @@ Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int gre
     off = al(off + (greedy ? 0 : (size_t)rows_d * sizeof(float2)));
     L.off_tasks = off;
     off = al(off + (greedy ? 0 : (size_t)B * sizeof(SampleTask)));
+    L.off_recs = off;
+    off = al(off + (greedy ? 0 : (size_t)B * ((V + kTile - 1) / kTile) * sizeof(TileRec)));
     L.total = off;
     return L;
 }
