@@ -102,11 +102,15 @@ constexpr float kLn2Hi = (float)kLn2D;
 constexpr float kLn2Lo = (float)(kLn2D - (double)(float)kLn2D);
 constexpr float kHeavyExp = -13.0f;  // weights above 2^-13 of the row maximum are evaluated in double-float
 
-// k = log2(e) / T as a float pair.
+// k = log2(e) / T as a float pair, by float arithmetic only (the GPU's
+// float64 rate is low): q = fl(L_hi / T), then the remainder L - q T, exact
+// by FMA up to L_lo, divided by T gives the low part.
+constexpr float kLog2eHi = (float)kLog2eD;
+constexpr float kLog2eLo = (float)(kLog2eD - (double)(float)kLog2eD);
 __device__ __forceinline__ df k_of_temperature(float T) {
-    const double k = kLog2eD / (double)T;
-    const float hi = (float)k;
-    return df{hi, (float)(k - (double)hi)};
+    const float q = __fdiv_rn(kLog2eHi, T);
+    const float r = __fadd_rn(__fmaf_rn(-q, T, kLog2eHi), kLog2eLo);
+    return fast_two_sum(q, __fdiv_rn(r, T));
 }
 
 // Table 2^(i/64), i = 0..63, as float pairs.

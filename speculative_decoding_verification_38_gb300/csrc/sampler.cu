@@ -21,9 +21,9 @@
 //     tile's residual sum is then exactly  A / S_t - B / S_d  plus the columns
 //     the margin left open (kept apart, at most one per tile; a tile with more
 //     is summed again once the normalisers are known).
-//   phase 2 (the warp that finishes a sequence's last tile): S_t, S_d, the tile
-//     sums and Z in double precision, the tile holding u * Z by a prefix over
-//     the tile sums, and one exact rescan of that tile for the column.
+//   phase 2 (a second kernel, one CTA per sequence): S_t, S_d, the tile sums
+//     and Z, the tile holding u * Z by a prefix over the tile sums, and one
+//     exact rescan of that tile for the column.
 // Weights and their sums are double-float (precise.cuh), so the pick matches
 // a float64 evaluation except within ~1e-10 of a CDF edge.
 #include <math.h>
@@ -77,12 +77,13 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
 }
 
 // Columns j..j+7 of a chunk as floats; columns past the chunk read as -inf
-// (weight 0). j is a multiple of 8.
+// (weight 0). j is a multiple of 8. Loads keep the lines in L1: columns queued
+// for double-float evaluation are read again moments later.
 template <int DT>
 __device__ __forceinline__ void src_load8(const Src& r, int64_t j, float (&v)[8]) {
     if (j + 8 <= r.n && (r.staged || r.al)) {
         if constexpr (DT == SPECV_BF16) {
-            const uint4 q = r.staged ? lds_v4(r.s + (uint32_t)(j * 2)) : ld_stream_v4(r.g + j * 2);
+            const uint4 q = r.staged ? lds_v4(r.s + (uint32_t)(j * 2)) : __ldg(reinterpret_cast<const uint4*>(r.g + j * 2));
             v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
             v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
         } else {
@@ -91,8 +92,8 @@ __device__ __forceinline__ void src_load8(const Src& r, int64_t j, float (&v)[8]
                 q0 = lds_v4(r.s + (uint32_t)(j * 4));
                 q1 = lds_v4(r.s + (uint32_t)(j * 4 + 16));
             } else {
-                q0 = ld_stream_v4(r.g + j * 4);
-                q1 = ld_stream_v4(r.g + j * 4 + 16);
+                q0 = __ldg(reinterpret_cast<const uint4*>(r.g + j * 4));
+                q1 = __ldg(reinterpret_cast<const uint4*>(r.g + j * 4 + 16));
             }
             v[0] = __uint_as_float(q0.x); v[1] = __uint_as_float(q0.y);
             v[2] = __uint_as_float(q0.z); v[3] = __uint_as_float(q0.w);
@@ -125,23 +126,6 @@ struct RowPair {
 // large enough that one rounding would matter; light ones are summed in fp32
 // over a short run before joining a double-float sum.
 __device__ __forceinline__ bool is_heavy(df w) { return w.lo != 0.f || w.hi > 1.220703125e-4f; }
-
-// Weights of the 8 chunk columns j..j+7: residual, or p's weight only.
-template <int TDT, int DDT>
-__device__ __forceinline__ void weights8(const RowPair<TDT, DDT>& rp, int64_t j, int mode, df It, df Id,
-                                         const Exp2Table& tab, df (&w)[8]) {
-    float lt[8];
-    src_load8<TDT>(rp.t, j, lt);
-    if (mode == kTaskResidual) {
-        float ld[8];
-        src_load8<DDT>(rp.d, j, ld);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = resid_weight(rp.wt(lt[e], tab), rp.wd(ld[e], tab), It, Id);
-    } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) w[e] = rp.wt(lt[e], tab);
-    }
-}
 
 // Tiles are kTile = kGroups x 256 columns; in group g, lane l owns the 8
 // consecutive columns g*256 + l*8 .. +7, so each warp-wide 16-byte load covers
@@ -271,86 +255,6 @@ __device__ __forceinline__ bool wq_push(int32_t* q, uint32_t head, uint32_t& tai
     tail += total;
     __syncwarp();
     return true;
-}
-
-// One warp walks the selected tile in index order from CDF position `base`
-// and returns the first chunk column whose running sum exceeds thr (or, if
-// rounding leaves none, the last column with weight; -1 if the tile has none).
-template <int TDT, int DDT>
-__device__ int64_t rescan_tile(const RowPair<TDT, DDT>& rp, int64_t tile_j, int mode, df It, df Id, float cl,
-                               df base, df thr, const Exp2Table& tab) {
-    const int lane = threadIdx.x & 31;
-    df run = base;
-    int64_t last = -1;
-#pragma unroll 1
-    for (int g = 0; g < kGroups; ++g) {
-        df w[8];
-        const int64_t j0 = tile_j + g * 256 + lane * 8;
-        weights8(rp, j0, mode, It, Id, tab, w);
-        // this lane's prefix at each of its 8 columns, then the warp-wide prefix
-        df pre[8];
-        float light = 0.f;
-        df heavy{0.f, 0.f};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            if (is_heavy(w[e]))
-                acc_add(heavy, w[e]);
-            else
-                light = __fadd_rn(light, w[e].hi);
-            pre[e] = df_add(df_norm(heavy), light_sum_df(light, cl));
-        }
-        const df incl = warp_scan_df(pre[7]);
-        df excl = shfl_up_df(incl, 1);
-        if (lane == 0) excl = df{0.f, 0.f};
-        const df start = df_add(run, excl);
-        int hit = -1, lp = -1;
-#pragma unroll
-        for (int e = 7; e >= 0; --e) {
-            if (df_gt(df_add(start, pre[e]), thr)) hit = e;
-            if (lp < 0 && df_pos(w[e])) lp = e;
-        }
-        const unsigned hm = __ballot_sync(0xffffffffu, hit >= 0);
-        if (hm) {
-            const int src = __ffs(hm) - 1;
-            return tile_j + g * 256 + src * 8 + __shfl_sync(0xffffffffu, hit, src);
-        }
-        const unsigned pm = __ballot_sync(0xffffffffu, lp >= 0);
-        if (pm) {
-            const int src = 31 - __clz(pm);
-            last = tile_j + g * 256 + src * 8 + __shfl_sync(0xffffffffu, lp, src);
-        }
-        run = df_add(run, shfl_df(incl, 31));
-    }
-    return last;
-}
-
-
-// Tile records are read back through L2 (other SMs wrote them during this grid).
-__device__ __forceinline__ double dd(const float (&v)[2]) {
-    const float2 x = __ldcg(reinterpret_cast<const float2*>(v));
-    return (double)x.x + (double)x.y;
-}
-__device__ __forceinline__ df to_df(double x) {
-    const float h = (float)x;
-    return df{h, (float)(x - (double)h)};
-}
-__device__ __forceinline__ void put(float (&v)[2], df x) {
-    v[0] = x.hi;
-    v[1] = x.lo;
-}
-__device__ __forceinline__ double warp_sum_d(double x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-__device__ __forceinline__ double warp_scan_d(double x) {
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const double y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-    }
-    return x;
 }
 
 // The row pair of task t restricted to tile `tile` (columns read from global
@@ -498,7 +402,7 @@ __device__ __forceinline__ df warp_sum4_df(df v0, df v1, df v2, df v3) {
 }
 
 template <int TDT, int DDT>
-__global__ void __launch_bounds__(kSampThreads) sampler_kernel(SampleParams p) {
+__global__ void __launch_bounds__(kSampThreads, 4) sampler_kernel(SampleParams p) {
     __shared__ SampSmem sm;
     for (int i = threadIdx.x; i < 64; i += blockDim.x) {
         sm.tab.hi[i] = p.tab.hi[i];
@@ -541,52 +445,69 @@ __global__ void __launch_bounds__(kSampThreads) sampler_kernel(SampleParams p) {
 // ------------------------------------------------------------- phase 2
 // One CTA per sequence, after every tile record is in (programmatic launch).
 // Thread i owns tiles i*K .. i*K + K - 1 (K = ceil(ntile / 256) <= 8); the
-// tile sums of the sampling weights live in shared memory.
+// tile sums of the sampling weights live in shared memory. All arithmetic is
+// double-float (the GPU's float64 rate is far below its fp32 rate).
 constexpr int kMaxTiles = (int)(kMaxVocab / kTile);
-constexpr int kMaxPer = kMaxTiles / kSampThreads;
 
 struct DrawSmem {
     Exp2Table tab;
     int32_t q[kWarps][kQCap];  // lane_tile_sum's queues (tiles summed again)
-    double w[kMaxTiles];       // tile sums
-    double red[kWarps];
-    double bc[4];              // broadcasts: St, Sd, Z, run
+    float w_hi[kMaxTiles], w_lo[kMaxTiles];  // tile sums
+    float red_hi[kWarps], red_lo[kWarps];
     int32_t dirty[kMaxTiles];
     int32_t ndirty, sel, col, last;
-    double start;
+    float start_hi, start_lo;
 };
 
-__device__ __forceinline__ double block_sum_d(double x, DrawSmem& sm) {
+__device__ __forceinline__ df block_sum_df(df x, DrawSmem& sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    x = warp_sum_d(x);
+    x = warp_sum_df(x);
     __syncthreads();  // red[] is free
-    if (lane == 0) sm.red[warp] = x;
+    if (lane == 0) {
+        sm.red_hi[warp] = x.hi;
+        sm.red_lo[warp] = x.lo;
+    }
     __syncthreads();
-    double t = 0.0;
-    for (int i = 0; i < kWarps; ++i) t += sm.red[i];
+    df t{0.f, 0.f};
+    for (int i = 0; i < kWarps; ++i) t = df_add(t, df{sm.red_hi[i], sm.red_lo[i]});
     return t;
 }
 
 // Exclusive block-wide prefix of one value per thread (thread order).
-__device__ __forceinline__ double block_excl_scan_d(double x, DrawSmem& sm) {
+__device__ __forceinline__ df block_excl_scan_df(df x, DrawSmem& sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const double incl = warp_scan_d(x);
+    const df incl = warp_scan_df(x);
     __syncthreads();
-    if (lane == 31) sm.red[warp] = incl;
+    if (lane == 31) {
+        sm.red_hi[warp] = incl.hi;
+        sm.red_lo[warp] = incl.lo;
+    }
     __syncthreads();
-    double before = 0.0;
-    for (int i = 0; i < warp; ++i) before += sm.red[i];
-    return before + incl - x;
+    df before{0.f, 0.f};
+    for (int i = 0; i < warp; ++i) before = df_add(before, df{sm.red_hi[i], sm.red_lo[i]});
+    df excl = shfl_up_df(incl, 1);
+    if (lane == 0) excl = df{0.f, 0.f};
+    return df_add(before, excl);
 }
 
-// Sampling weight of column j (0-based in the tile) as double-float, and
-// whether it is heavy (summed exactly) or light (summed in fp32 first).
+__device__ __forceinline__ df ldcg_df(const float* v) {
+    const float2 x = __ldcg(reinterpret_cast<const float2*>(v));
+    return df{x.x, x.y};
+}
+
+// Sampling weight of column j (0-based in the tile) as double-float.
 template <int TDT, int DDT>
 __device__ __forceinline__ df col_weight(const RowPair<TDT, DDT>& rp, int64_t j, int mode, df It, df Id,
                                          const Exp2Table& tab) {
     const df wt = rp.wt(src_elem<TDT>(rp.t, j), tab);
     if (mode != kTaskResidual) return wt;
     return resid_weight(wt, rp.wd(src_elem<DDT>(rp.d, j), tab), It, Id);
+}
+
+// max(0, a * It - b * Id) for one tile record's pair of sums
+__device__ __forceinline__ df resid_of_sums(df a, df b, df It, df Id) {
+    const df v = df_sub(df_mul(It, a), df_mul(Id, b));
+    return df_pos(v) ? v : df{0.f, 0.f};
 }
 
 template <int TDT, int DDT>
@@ -607,29 +528,28 @@ __global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
     const int K = (nt + kSampThreads - 1) / kSampThreads;
     const int t0 = threadIdx.x * K, t1 = min(nt, t0 + K);
     // the exact normalisers
-    double st = 0.0, sd = 0.0;
+    df st{0.f, 0.f}, sd{0.f, 0.f};
 #pragma unroll 1
     for (int ti = t0; ti < t1; ++ti) {
         const float4 ss = __ldcg(reinterpret_cast<const float4*>(recs + ti) + 1);
-        st += (double)ss.x + (double)ss.y;
-        sd += (double)ss.z + (double)ss.w;
+        st = df_add(st, df{ss.x, ss.y});
+        sd = df_add(sd, df{ss.z, ss.w});
     }
-    const double St = block_sum_d(st, sm);
-    const double Sd = block_sum_d(sd, sm);
+    const df St = block_sum_df(st, sm);
+    const df Sd = block_sum_df(sd, sm);
     int mode = t.mode;
     const bool resid = mode == kTaskResidual;
-    const double It = resid ? 1.0 / St : 1.0, Id = resid ? 1.0 / Sd : 1.0;
-    const df Itf = to_df(It), Idf = to_df(Id);
+    const df It = resid ? df_recip(St) : df{1.f, 0.f}, Id = resid ? df_recip(Sd) : df{1.f, 0.f};
     float cl = (resid && t.probs) ? 0.f : kEx2LightBias;
     // tile sums of the sampling weights
-    double z = 0.0;
+    df z{0.f, 0.f};
 #pragma unroll 1
     for (int ti = t0; ti < t1; ++ti) {
         const float4* r = reinterpret_cast<const float4*>(recs + ti);
-        double v;
+        df v;
         if (!resid) {
             const float4 ss = __ldcg(r + 1);
-            v = (double)ss.x + (double)ss.y;
+            v = df{ss.x, ss.y};
         } else {
             const int32_t nu = __ldcg(reinterpret_cast<const int32_t*>(r + 3));
             if (nu > 1) {  // more than one open column: summed again below
@@ -637,15 +557,15 @@ __global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
                 continue;
             }
             const float4 ab = __ldcg(r);
-            v = It * ((double)ab.x + (double)ab.y) - Id * ((double)ab.z + (double)ab.w);
+            v = resid_of_sums(df{ab.x, ab.y}, df{ab.z, ab.w}, It, Id);
             if (nu == 1) {
                 const float4 uu = __ldcg(r + 2);
-                v += fmax(0.0, It * ((double)uu.x + (double)uu.y) - Id * ((double)uu.z + (double)uu.w));
+                v = df_add(v, resid_of_sums(df{uu.x, uu.y}, df{uu.z, uu.w}, It, Id));
             }
-            v = fmax(v, 0.0);
         }
-        sm.w[ti] = v;
-        z += v;
+        sm.w_hi[ti] = v.hi;
+        sm.w_lo[ti] = v.lo;
+        z = df_add(z, v);
     }
     __syncthreads();
     const int nd = sm.ndirty;
@@ -653,46 +573,48 @@ __global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
     for (int i = warp; i < nd; i += kWarps) {  // one warp per tile, exactly
         const int ti = sm.dirty[i];
         const RowPair<TDT, DDT> rp = tile_rows<TDT, DDT>(p, t, ti);
-        const df x = warp_sum_df(lane_tile_sum(rp, 0, mode, Itf, Idf, cl,
-                                               *reinterpret_cast<SampSmem*>(&sm)));
+        const df x = warp_sum_df(lane_tile_sum(rp, 0, mode, It, Id, cl, *reinterpret_cast<SampSmem*>(&sm)));
         if (lane == 0) {
-            sm.w[ti] = (double)x.hi + (double)x.lo;
-            z += sm.w[ti];
+            sm.w_hi[ti] = x.hi;
+            sm.w_lo[ti] = x.lo;
+            z = df_add(z, x);
         }
     }
-    double Z = block_sum_d(z, sm);
-    if (resid && !(Z > 0.0)) {  // p_i == q_i to rounding: draw from p_i instead
+    df Z = block_sum_df(z, sm);
+    if (resid && !df_pos(Z)) {  // p_i == q_i to rounding: draw from p_i instead
         mode = kTaskBonus;
         cl = kEx2LightBias;
         for (int ti = t0; ti < t1; ++ti) {
             const float4 ss = __ldcg(reinterpret_cast<const float4*>(recs + ti) + 1);
-            sm.w[ti] = (double)ss.x + (double)ss.y;
+            sm.w_hi[ti] = ss.x;
+            sm.w_lo[ti] = ss.y;
         }
         Z = St;
     }
     if (threadIdx.x == 0) {
-        const df zf = to_df(Z);
-        p.tasks[b].z_hi = zf.hi;
-        p.tasks[b].z_lo = zf.lo;
+        p.tasks[b].z_hi = Z.hi;
+        p.tasks[b].z_lo = Z.lo;
         sm.sel = -1;
         sm.last = -1;
         sm.col = -1;
     }
     __syncthreads();
     // the tile holding the crossing u * Z (u has 24 significant bits)
-    const double thr = (double)t.u * Z;
-    double mine = 0.0;
-    for (int ti = t0; ti < t1; ++ti) mine += sm.w[ti];
-    double run = block_excl_scan_d(mine, sm);
+    const df thr = df_add(two_prod(t.u, Z.hi), df{__fmul_rn(t.u, Z.lo), 0.f});
+    df mine{0.f, 0.f};
+    for (int ti = t0; ti < t1; ++ti) mine = df_add(mine, df{sm.w_hi[ti], sm.w_lo[ti]});
+    df run = block_excl_scan_df(mine, sm);
     int last_here = -1;
     for (int ti = t0; ti < t1; ++ti) {
-        const double v = sm.w[ti];
-        if (v > 0.0) last_here = ti;
-        if (run + v > thr && run <= thr) {
+        const df v{sm.w_hi[ti], sm.w_lo[ti]};
+        const df end = df_add(run, v);
+        if (df_pos(v)) last_here = ti;
+        if (df_gt(end, thr) && !df_gt(run, thr)) {
             sm.sel = ti;  // the only thread with a crossing
-            sm.start = run;
+            sm.start_hi = run.hi;
+            sm.start_lo = run.lo;
         }
-        run += v;
+        run = end;
     }
     atomicMax(&sm.last, last_here);
     __syncthreads();
@@ -702,8 +624,7 @@ __global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
     if (sel < 0) return;
     // rescan the selected tile: warp w covers columns w*128 .. +127, 4 per lane
     const RowPair<TDT, DDT> rp = tile_rows<TDT, DDT>(p, t, sel);
-    const df basef = last_mass ? df{NAN, 0.f} : to_df(sm.start);  // NaN: no comparison succeeds
-    const df thrf = to_df(thr);
+    const df basef = last_mass ? df{NAN, 0.f} : df{sm.start_hi, sm.start_lo};  // NaN: no comparison succeeds
     const int64_t j0 = (int64_t)warp * 128 + lane * 4;
     df w4[4], pre[4];
     float light = 0.f;
@@ -711,7 +632,7 @@ __global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
     int lp = -1;
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        w4[e] = j0 + e < rp.t.n ? col_weight(rp, j0 + e, mode, Itf, Idf, sm.tab) : df{0.f, 0.f};
+        w4[e] = j0 + e < rp.t.n ? col_weight(rp, j0 + e, mode, It, Id, sm.tab) : df{0.f, 0.f};
         if (is_heavy(w4[e]))
             acc_add(heavy, w4[e]);
         else
@@ -720,30 +641,17 @@ __global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
         if (df_pos(w4[e])) lp = e;
     }
     // block prefix of the per-lane sums, in column order (warp-major)
-    const df incl = warp_scan_df(pre[3]);
-    __syncthreads();
-    if (lane == 31) {
-        sm.red[warp] = (double)incl.hi;  // hi and lo of each warp total, kept apart
-        sm.bc[0] = 0.0;
-    }
-    __shared__ float wlo[kWarps];
-    if (lane == 31) wlo[warp] = incl.lo;
-    __syncthreads();
-    df before = basef;
-    for (int i = 0; i < warp; ++i) before = df_add(before, df{(float)sm.red[i], wlo[i]});
-    df excl = shfl_up_df(incl, 1);
-    if (lane == 0) excl = df{0.f, 0.f};
-    const df start = df_add(before, excl);
+    const df start = df_add(basef, block_excl_scan_df(pre[3], sm));
     int hit = -1;
 #pragma unroll
     for (int e = 3; e >= 0; --e)
-        if (df_gt(df_add(start, pre[e]), thrf)) hit = e;
+        if (df_gt(df_add(start, pre[e]), thr)) hit = e;
     // the first column (in order) whose running sum exceeds thr
     if (hit >= 0) atomicMin((unsigned*)&sm.col, (unsigned)(j0 + hit));
     if (lp >= 0) atomicMax(&sm.last, (int)(0x40000000 | (j0 + lp)));
     __syncthreads();
     if (threadIdx.x == 0) {
-        int64_t jt = (sm.col >= 0) ? sm.col : ((sm.last & 0x40000000) ? (sm.last & 0x3fffffff) : -1);
+        const int64_t jt = (sm.col >= 0) ? sm.col : ((sm.last & 0x40000000) ? (sm.last & 0x3fffffff) : -1);
         if (jt >= 0) p.out_tokens[t.out_slot] = (int32_t)((int64_t)sel * kTile + jt);
     }
 }

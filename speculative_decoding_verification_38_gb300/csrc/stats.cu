@@ -1067,23 +1067,28 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
     pdl_wait_primary();
     const int32_t b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // warp 0: the status checks (their loads issued together), then, for
-    // positions lane and lane + 32, the draft token, the two logits at it and
-    // u_acc, fetched while the other warps merge rows
+    // Layout first (every thread: the offsets are a broadcast load); with a
+    // valid layout warps 1.. merge rows at once while warp 0 runs the other
+    // status checks and, for positions lane and lane + 32, fetches the draft
+    // token, the two logits at it and u_acc.
+    const int64_t t0 = tro_at(p, b), t1 = tro_at(p, b + 1);
+    const int64_t d0 = dro_at(p, b), d1 = dro_at(p, b + 1);
+    const int64_t gg = d1 - d0;
+    const int32_t g = (int32_t)gg;
+    if (gg < 0 || gg > p.gmax || t1 - t0 != gg + 1 || t0 < 0 || t1 > p.rows_t || d0 < 0 || d1 > p.rows_d) {
+        if (warp == 0) warp_write_error(p, b, 4, t0, g);  // SPEC_SEQ_BAD_LAYOUT
+        return;
+    }
+    const float T = p.greedy ? 1.f : temp_of(p, b);
+    const float k = p.greedy ? 1.f : kLog2e / T;
+    const int nrows = p.greedy ? g + 1 : 2 * g + 1;  // rows 0..g target, g+1..2g draft
     int32_t x[2] = {0, 0};
     float lt[2] = {0.f, 0.f}, ld[2] = {0.f, 0.f}, ua[2] = {0.f, 0.f};
     int32_t kv = 0;
     if (warp == 0) {
-        const int64_t t0 = tro_at(p, b), t1 = tro_at(p, b + 1);
-        const int64_t d0 = dro_at(p, b), d1 = dro_at(p, b + 1);
-        const float T = p.greedy ? 1.f : temp_of(p, b);
         kv = p.kv_in ? __ldg(p.kv_in + b) : 0;
-        const int64_t gg = d1 - d0;
         int32_t st = 0;
-        if (gg < 0 || gg > p.gmax || t1 - t0 != gg + 1 || t0 < 0 || t1 > p.rows_t || d0 < 0 || d1 > p.rows_d)
-            st = 4;  // SPEC_SEQ_BAD_LAYOUT
-        const int32_t g = (int32_t)gg;
-        if (!st && !p.greedy && (!(T > 0.f) || !isfinite(T))) st = 5;  // SPEC_SEQ_BAD_TEMP
+        if (!p.greedy && (!(T > 0.f) || !isfinite(T))) st = 5;  // SPEC_SEQ_BAD_TEMP
         if (!st) {
             bool bad = false;
 #pragma unroll
@@ -1101,12 +1106,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
             if (__any_sync(0xffffffffu, bad)) st = 1;  // SPEC_SEQ_BAD_TOKEN
         }
         if (!st && p.kv_in && kv < g) st = 2;  // SPEC_SEQ_BAD_KV
-        if (lane == 0) {
-            fs.t0 = t0;
-            fs.d0 = d0;
-            fs.g = g;
-            fs.status = st;
-        }
+        if (lane == 0) fs.status = st;
         if (!st && !p.greedy) {
             const int tes = p.tdt == SPECV_F32 ? 4 : 2, des = p.ddt == SPECV_F32 ? 4 : 2;
 #pragma unroll
@@ -1120,36 +1120,31 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
                 }
             }
         }
+    } else {
+        for (int j = warp - 1; j < nrows; j += kFinWarps - 1) {
+            const bool is_t = j <= g;
+            const int64_t r = is_t ? (t0 + j) : (p.rows_t + d0 + (j - g - 1));
+            const float2* src = p.partials + r * p.S * p.pw;
+            const int32_t n = pieces_of_row(p, r);
+            float2 v;
+            if (p.greedy) {
+                int32_t ix;
+                warp_merge_am(src, n, v.x, ix);
+                if (ix == INT32_MAX) ix = 0;  // every logit -inf or NaN: the first index
+                v.y = __int_as_float(ix);
+            } else {
+                v = warp_merge_ms(src, n, !is_t && p.probs, k);
+            }
+            if (lane == 0) fs.rs[j] = v;
+        }
     }
     __syncthreads();
-    const int64_t t0 = fs.t0, d0 = fs.d0;
-    const int32_t g = fs.g;
     if (fs.status) {
         if (warp == 0) warp_write_error(p, b, fs.status, t0, g);
         return;
     }
-    const float k = p.greedy ? 1.f : kLog2e / temp_of(p, b);
-    const int nrows = p.greedy ? g + 1 : 2 * g + 1;  // rows 0..g target, g+1..2g draft
-    for (int j = warp; j < nrows; j += kFinWarps) {
-        const bool is_t = j <= g;
-        const int64_t r = is_t ? (t0 + j) : (p.rows_t + d0 + (j - g - 1));
-        const float2* src = p.partials + r * p.S * p.pw;
-        const int32_t n = pieces_of_row(p, r);
-        float2 v;
-        if (p.greedy) {
-            int32_t ix;
-            warp_merge_am(src, n, v.x, ix);
-            if (ix == INT32_MAX) ix = 0;  // every logit -inf or NaN: the first index
-            v.y = __int_as_float(ix);
-        } else {
-            v = warp_merge_ms(src, n, !is_t && p.probs, k);
-        }
-        if (lane == 0) {
-            fs.rs[j] = v;
-            p.row_stats[r] = v;
-        }
-    }
-    __syncthreads();
+    for (int j = threadIdx.x; j < nrows; j += kFinThreads)
+        p.row_stats[j <= g ? t0 + j : p.rows_t + d0 + (j - g - 1)] = fs.rs[j];
     if (warp != 0) return;
     if (p.greedy) {
         int32_t a = g;
