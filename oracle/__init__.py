@@ -68,6 +68,7 @@ class OrcArgs(ctypes.Structure):
         ("kv_out", ctypes.c_void_p), ("out_blocks", ctypes.c_void_p), ("seq_status", ctypes.c_void_p),
         ("diag_acc_margin", ctypes.c_void_p), ("diag_u_smp", ctypes.c_void_p),
         ("diag_cdf_lo", ctypes.c_void_p), ("diag_cdf_hi", ctypes.c_void_p), ("diag_z", ctypes.c_void_p),
+        ("top_k", ctypes.c_int32), ("top_ks", ctypes.c_void_p),
     ]
 
 
@@ -89,6 +90,12 @@ def lib():
             L.orc_softmax_row.argtypes = [vp, i32, i64, dbl, vp]
             L.orc_normalize_row.restype = i32
             L.orc_normalize_row.argtypes = [vp, i32, i64, vp]
+            L.orc_topk_threshold.restype = dbl
+            L.orc_topk_threshold.argtypes = [vp, i32, i64, i64]
+            L.orc_softmax_row_topk.restype = i32
+            L.orc_softmax_row_topk.argtypes = [vp, i32, i64, dbl, dbl, vp]
+            L.orc_normalize_row_topk.restype = i32
+            L.orc_normalize_row_topk.argtypes = [vp, i32, i64, dbl, vp]
             L.orc_residual.restype = dbl
             L.orc_residual.argtypes = [vp, vp, i64, vp]
             L.orc_inverse_cdf.restype = i64
@@ -157,6 +164,29 @@ def normalize_row(row: np.ndarray):
     return st, q
 
 
+def topk_threshold(row: np.ndarray, k: int) -> float:
+    """The k-th largest value of a row (NaN read as -inf); -inf when k <= 0 or k >= V."""
+    row = np.ascontiguousarray(row)
+    return float(lib().orc_topk_threshold(row.ctypes.data, _dtype_code(row), row.shape[0], int(k)))
+
+
+def softmax_row_topk(row: np.ndarray, T: float, tau: float):
+    """softmax(l / T) over the columns with l >= tau, 0 elsewhere. Returns (status, p)."""
+    row = np.ascontiguousarray(row)
+    p = np.zeros(row.shape[0], dtype=np.float64)
+    st = lib().orc_softmax_row_topk(row.ctypes.data, _dtype_code(row), row.shape[0], float(T), float(tau),
+                                    p.ctypes.data)
+    return st, p
+
+
+def normalize_row_topk(row: np.ndarray, tau: float):
+    """A probability row kept where value >= tau, divided by the kept sum. Returns (status, q)."""
+    row = np.ascontiguousarray(row)
+    q = np.zeros(row.shape[0], dtype=np.float64)
+    st = lib().orc_normalize_row_topk(row.ctypes.data, _dtype_code(row), row.shape[0], float(tau), q.ctypes.data)
+    return st, q
+
+
 def residual(p: np.ndarray, q: np.ndarray):
     """r = max(0, p - q) and its sum Z."""
     p = np.ascontiguousarray(p, dtype=np.float64)
@@ -212,6 +242,7 @@ class _Call:
         temps = keep(None if w.temperatures is None else np.asarray(w.temperatures, dtype=np.float32))
         kv = keep(None if w.kv_in is None else np.asarray(w.kv_in, dtype=np.int32))
         unif = keep(None if uniforms is None else np.asarray(uniforms, dtype=np.float32))
+        topks = keep(None if getattr(w, "top_ks", None) is None else np.asarray(w.top_ks, dtype=np.int32))
         self.out_tokens = np.full(w.rows_target, -7, dtype=np.int32)
         self.out_accepted = np.full(B, -7, dtype=np.int32)
         self.kv_out = np.full(B, -7, dtype=np.int32)
@@ -238,6 +269,8 @@ class _Call:
         a.kv_out = _ptr(self.kv_out) if kv is not None else None
         a.out_blocks = _ptr(self.out_blocks) if (kv is not None and w.block_size > 0) else None
         a.seq_status = _ptr(self.seq_status)
+        a.top_k = int(getattr(w, "top_k", 0))
+        a.top_ks = _ptr(topks)
         if self.diag is not None:
             a.diag_acc_margin = _ptr(self.diag["acc_margin"])
             a.diag_u_smp = _ptr(self.diag["u_smp"])

@@ -22,7 +22,7 @@
  *   Philox4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
  *        Easy as 1, 2, 3", SC'11, section on the Philox S-box and key schedule.
  *
- * Readings where the pages are silent or ambiguous (all listed in the design doc):
+ * Readings where the pages are silent or ambiguous:
  *   - uniforms come from Philox4x32-10 keyed by the 64-bit seed with counter
  *     (position, sequence, round lo, round hi); word 0 -> u_acc, word 1 ->
  *     u_smp, each (w >> 8) * 2^-24, the pages' 24-bit resolution ([P1] Code);
@@ -31,7 +31,11 @@
  *     order ([P1] Code, sample); if rounding leaves none, the last index with
  *     positive mass (the page returns the last index even if it has no mass);
  *   - residual normaliser Z == 0 at a rejection: sample from p_i instead;
- *   - greedy argmax: first index of the maximum raw logit, NaN read as -inf.
+ *   - greedy argmax: first index of the maximum raw logit, NaN read as -inf;
+ *   - top-k (an option of the library, applied to both models' rows alike as
+ *     [P1] Implementation notes asks of any logits processing): keep every
+ *     column whose value is at least the row's k-th largest (NaN ranks as
+ *     -inf; ties at the threshold all stay), renormalise over the kept ones.
  */
 #include <math.h>
 #include <pthread.h>
@@ -160,6 +164,72 @@ int32_t orc_normalize_row(const void* row, int32_t dtype, int64_t V, double* q) 
     return ORC_SEQ_OK;
 }
 
+/* Top-k truncation, applied the same way to the target's and the draft's row
+ * ([P1] Implementation notes: both models' logits go through the same
+ * processing). The threshold is the k-th largest value of the row, NaN read
+ * as -inf; every column whose value is at least that large is kept (ties at
+ * the threshold all stay). k <= 0 or k >= V keeps the whole row: the returned
+ * threshold is then -inf. Plain: copy, sort in decreasing order, index. */
+static int cmp_desc(const void* x, const void* y) {
+    const double a = *(const double*)x, b = *(const double*)y;
+    return (a < b) - (a > b);
+}
+
+double orc_topk_threshold(const void* row, int32_t dtype, int64_t V, int64_t k) {
+    if (k < 1 || k >= V) return -INFINITY;
+    double* v = (double*)malloc(sizeof(double) * (size_t)V);
+    for (int64_t j = 0; j < V; ++j) {
+        const double x = orc_value(row, dtype, j);
+        v[j] = isnan(x) ? -INFINITY : x;
+    }
+    qsort(v, (size_t)V, sizeof(double), cmp_desc);
+    const double t = v[k - 1];
+    free(v);
+    return t;
+}
+
+/* p = softmax(l / T) restricted to the columns with l >= tau (the others get
+ * probability 0); tau = -inf keeps every column. The same checks as
+ * orc_softmax_row over the whole row. */
+int32_t orc_softmax_row_topk(const void* row, int32_t dtype, int64_t V, double T, double tau, double* p) {
+    if (!(T > 0.0) || !isfinite(T)) return ORC_SEQ_BAD_TEMP;
+    double m = -INFINITY;
+    int has_nan = 0;
+    for (int64_t j = 0; j < V; ++j) {
+        double x = orc_value(row, dtype, j) / T;
+        if (isnan(x))
+            has_nan = 1;
+        else if (x > m)
+            m = x;
+    }
+    if (has_nan || !isfinite(m)) return ORC_SEQ_BAD_ROW;
+    double s = 0.0;
+    for (int64_t j = 0; j < V; ++j) {
+        const double l = orc_value(row, dtype, j);
+        p[j] = (l >= tau) ? exp(l / T - m) : 0.0;
+        s += p[j];
+    }
+    if (!(s > 0.0) || !isfinite(s)) return ORC_SEQ_BAD_ROW;
+    for (int64_t j = 0; j < V; ++j) p[j] /= s;
+    return ORC_SEQ_OK;
+}
+
+/* A probability row restricted to the columns with value >= tau, divided by
+ * the kept columns' sum. */
+int32_t orc_normalize_row_topk(const void* row, int32_t dtype, int64_t V, double tau, double* q) {
+    double s = 0.0;
+    int has_nan = 0;
+    for (int64_t j = 0; j < V; ++j) {
+        const double v = orc_value(row, dtype, j);
+        if (isnan(v)) has_nan = 1;
+        q[j] = (v >= tau) ? v : 0.0;
+        s += q[j];
+    }
+    if (has_nan || !(s > 0.0) || !isfinite(s)) return ORC_SEQ_BAD_ROW;
+    for (int64_t j = 0; j < V; ++j) q[j] /= s;
+    return ORC_SEQ_OK;
+}
+
 /* r = max(0, p - q) elementwise; returns Z = sum r ([P1] How it works step 3;
  * [P4] residual p'(z)). */
 double orc_residual(const double* p, const double* q, int64_t V, double* r) {
@@ -245,6 +315,10 @@ typedef struct {
     double* diag_cdf_lo;     /* normalised CDF edges of the emitted token */
     double* diag_cdf_hi;
     double* diag_z; /* residual normaliser at the rejection, -1 for a bonus */
+    /* top-k truncation of every row of a sequence (sampling only): k_b =
+     * top_ks[b] if top_ks, else top_k; k_b <= 0 or k_b >= V keeps every column */
+    int32_t top_k;
+    const int32_t* top_ks;
 } orc_args_t;
 
 typedef struct {
@@ -316,10 +390,22 @@ static void uniforms_for(const orc_args_t* a, int64_t b, int64_t i, double* ua, 
     }
 }
 
-static int32_t draft_dist(const orc_args_t* a, int64_t drow, double T, double* q) {
+static int64_t top_k_of(const orc_args_t* a, int64_t b) { return a->top_ks ? a->top_ks[b] : a->top_k; }
+
+/* p_i of sequence b from target row trow: softmax(l / T) over the row's
+ * top-k columns (every column when top-k is off). */
+static int32_t target_dist(const orc_args_t* a, int64_t b, int64_t trow, double T, double* p) {
+    const void* rp = row_ptr(a->target, a->target_dtype, trow, a->vocab);
+    const double tau = orc_topk_threshold(rp, a->target_dtype, a->vocab, top_k_of(a, b));
+    return orc_softmax_row_topk(rp, a->target_dtype, a->vocab, T, tau, p);
+}
+
+/* q_i of sequence b from draft row drow, truncated the same way. */
+static int32_t draft_dist(const orc_args_t* a, int64_t b, int64_t drow, double T, double* q) {
     const void* rp = row_ptr(a->draft, a->draft_dtype, drow, a->vocab);
-    if (a->draft_is_probs) return orc_normalize_row(rp, a->draft_dtype, a->vocab, q);
-    return orc_softmax_row(rp, a->draft_dtype, a->vocab, T, q);
+    const double tau = orc_topk_threshold(rp, a->draft_dtype, a->vocab, top_k_of(a, b));
+    if (a->draft_is_probs) return orc_normalize_row_topk(rp, a->draft_dtype, a->vocab, tau, q);
+    return orc_softmax_row_topk(rp, a->draft_dtype, a->vocab, T, tau, q);
 }
 
 /* One sequence of the sampling verify ([P1] How it works steps 3-5;
@@ -335,9 +421,9 @@ static void verify_sample_one(const orc_args_t* a, int64_t b, double* p, double*
     const int64_t V = a->vocab, t0 = toff(a, b), d0 = doff(a, b);
     double margin = INFINITY;
     for (int64_t i = 0; i < g; ++i) {
-        st = orc_softmax_row(row_ptr(a->target, a->target_dtype, t0 + i, V), a->target_dtype, V, T, p);
+        st = target_dist(a, b, t0 + i, T, p);
         if (st) { write_error(a, b, st); return; }
-        st = draft_dist(a, d0 + i, T, q);
+        st = draft_dist(a, b, d0 + i, T, q);
         if (st) { write_error(a, b, st); return; }
         int32_t x = a->draft_tokens[d0 + i];
         double ua, us;
@@ -364,7 +450,7 @@ static void verify_sample_one(const orc_args_t* a, int64_t b, double* p, double*
         return;
     }
     /* all gamma accepted: bonus token from p_{gamma+1} ([P1] step 4) */
-    st = orc_softmax_row(row_ptr(a->target, a->target_dtype, t0 + g, V), a->target_dtype, V, T, p);
+    st = target_dist(a, b, t0 + g, T, p);
     if (st) { write_error(a, b, st); return; }
     double ua, us;
     uniforms_for(a, b, g, &ua, &us);
@@ -479,8 +565,8 @@ int32_t orc_accept_terms(const orc_args_t* a, int64_t b, int64_t i, double* p_x,
     double T = a->temperatures ? (double)a->temperatures[b] : (double)a->temperature;
     double* p = (double*)malloc(sizeof(double) * (size_t)V);
     double* q = (double*)malloc(sizeof(double) * (size_t)V);
-    int32_t st = orc_softmax_row(row_ptr(a->target, a->target_dtype, toff(a, b) + i, V), a->target_dtype, V, T, p);
-    if (!st) st = draft_dist(a, doff(a, b) + i, T, q);
+    int32_t st = target_dist(a, b, toff(a, b) + i, T, p);
+    if (!st) st = draft_dist(a, b, doff(a, b) + i, T, q);
     if (!st) {
         int32_t x = a->draft_tokens[doff(a, b) + i];
         *p_x = p[x];
@@ -500,7 +586,7 @@ int32_t orc_position_rows(const orc_args_t* a, int64_t b, int64_t i, double* p, 
     const int64_t V = a->vocab;
     double T = a->temperatures ? (double)a->temperatures[b] : (double)a->temperature;
     int64_t g = doff(a, b + 1) - doff(a, b);
-    int32_t st = orc_softmax_row(row_ptr(a->target, a->target_dtype, toff(a, b) + i, V), a->target_dtype, V, T, p);
+    int32_t st = target_dist(a, b, toff(a, b) + i, T, p);
     if (st) return st;
     if (i >= g) {
         for (int64_t j = 0; j < V; ++j) {
@@ -510,7 +596,7 @@ int32_t orc_position_rows(const orc_args_t* a, int64_t b, int64_t i, double* p, 
         *z_out = -1.0;
         return ORC_SEQ_OK;
     }
-    st = draft_dist(a, doff(a, b) + i, T, q);
+    st = draft_dist(a, b, doff(a, b) + i, T, q);
     if (st) return st;
     double Z = orc_residual(p, q, V, w);
     *z_out = Z;

@@ -80,6 +80,8 @@ class Workload:
     draft_row_off: np.ndarray | None = None
     greedy: bool = False
     info: dict = field(default_factory=dict)
+    top_k: int = 0                    # top-k truncation of every row (0: off)
+    top_ks: np.ndarray | None = None  # per-sequence k (int32 [B]) instead of top_k
 
     @property
     def rows_target(self) -> int:
