@@ -48,7 +48,7 @@ extern "C" {
 /* Same type as cudaStream_t; declared here so plain C callers need no CUDA header. */
 typedef struct CUstream_st* spec_stream_t;
 
-#define SPEC_ABI_VERSION 1
+#define SPEC_ABI_VERSION 2
 
 typedef enum {
     SPEC_OK = 0,
@@ -148,6 +148,18 @@ typedef struct {
 
     void* workspace;        /* device, 256-byte aligned, caller-owned */
     size_t workspace_bytes; /* >= spec_verify_workspace_size(this, mode) */
+
+    /* Top-k truncation (sampling only; greedy ignores both): sequence b uses
+     * k_b = top_ks[b] if top_ks != NULL, else top_k. With 0 < k_b < V every
+     * target and draft row of b keeps the columns whose value is at least the
+     * row's k_b-th largest value (NaN ranks as -inf; all ties at that value
+     * stay) and p, q are renormalised over the kept columns; k_b <= 0 or
+     * k_b >= V keeps the whole row. Both models' rows are processed alike
+     * ("Speculative decoding" (mhtirogla.ai), Implementation notes). A draft
+     * token outside its draft row's kept set has q = 0 (accepted iff p > 0).
+     * Zero-initialise both for plain sampling. */
+    int32_t top_k;
+    const int32_t* top_ks; /* device [B] or NULL */
 } spec_verify_args_t;
 
 /* ABI version of the loaded library (SPEC_ABI_VERSION at build time). */

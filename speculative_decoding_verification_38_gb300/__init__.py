@@ -28,6 +28,7 @@ SPEC_ERR_CUDA = 4
 SPEC_ERR_UNSUPPORTED = 5
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_STATIC_SCRATCH_BYTES = 8 << 20  # scratch of spec_verify_sample_static, per device
+SPEC_ABI_VERSION = 2
 SEQ_OK, SEQ_BAD_TOKEN, SEQ_BAD_KV, SEQ_BAD_ROW, SEQ_BAD_LAYOUT, SEQ_BAD_TEMP = 0, 1, 2, 3, 4, 5
 
 
@@ -70,6 +71,8 @@ class SpecVerifyArgs(ctypes.Structure):
         ("seq_status", ctypes.c_void_p),
         ("workspace", ctypes.c_void_p),
         ("workspace_bytes", ctypes.c_size_t),
+        ("top_k", ctypes.c_int32),
+        ("top_ks", ctypes.c_void_p),
     ]
 
 
@@ -121,7 +124,7 @@ def lib():
             L.spec_debug_light_exp2.argtypes = [vp, vp, i64, vp]
             L.spec_debug_time_next_stats.restype = ctypes.c_int
             L.spec_debug_time_next_stats.argtypes = [vp, vp]
-            if L.spec_abi_version() != 1:
+            if L.spec_abi_version() != SPEC_ABI_VERSION:
                 raise ImportError("libspecverify.so ABI version mismatch")
             _lib = L
     return _lib
@@ -170,8 +173,9 @@ class VerifyArgs:
     def __init__(self, *, batch, gamma_max, target, draft=None, draft_tokens=None, target_row_off=None,
                  draft_row_off=None, draft_is_probs=False, temperatures=None, temperature=1.0, seed=0, round=0,
                  seq_offset=0, uniforms=None, kv_lens_in=None, kv_lens_out=None, block_size=0,
-                 out_num_blocks=None, out_tokens=None, out_accepted=None, seq_status=None, workspace=None):
-        for name, t in [("target", target), ("draft", draft), ("draft_tokens", draft_tokens),
+                 out_num_blocks=None, out_tokens=None, out_accepted=None, seq_status=None, workspace=None,
+                 top_k=0, top_ks=None):
+        for name, t in [("target", target), ("draft", draft), ("draft_tokens", draft_tokens), ("top_ks", top_ks),
                         ("target_row_off", target_row_off), ("draft_row_off", draft_row_off),
                         ("temperatures", temperatures), ("uniforms", uniforms), ("kv_lens_in", kv_lens_in),
                         ("kv_lens_out", kv_lens_out), ("out_num_blocks", out_num_blocks),
@@ -180,7 +184,8 @@ class VerifyArgs:
         self.tensors = dict(target=target, draft=draft, draft_tokens=draft_tokens, target_row_off=target_row_off,
                             draft_row_off=draft_row_off, temperatures=temperatures, uniforms=uniforms,
                             kv_lens_in=kv_lens_in, kv_lens_out=kv_lens_out, out_num_blocks=out_num_blocks,
-                            out_tokens=out_tokens, out_accepted=out_accepted, seq_status=seq_status)
+                            out_tokens=out_tokens, out_accepted=out_accepted, seq_status=seq_status,
+                            top_ks=top_ks)
         a = SpecVerifyArgs()
         a.struct_size = ctypes.sizeof(SpecVerifyArgs)
         a.batch = int(batch)
@@ -209,6 +214,8 @@ class VerifyArgs:
         a.out_tokens = _ptr(out_tokens)
         a.out_accepted = _ptr(out_accepted)
         a.seq_status = _ptr(seq_status)
+        a.top_k = int(top_k)
+        a.top_ks = _ptr(top_ks)
         self.struct = a
         self.workspace = None
         if workspace is not None:
@@ -222,6 +229,13 @@ class VerifyArgs:
 
     def set_round(self, rnd: int):
         self.struct.round = int(rnd)
+
+    def set_top_k(self, top_k=0, top_ks=None):
+        """Top-k truncation of every row (k <= 0 or k >= V: off); top_ks int32 [B] per sequence."""
+        _check_dev(top_ks, "top_ks")
+        self.tensors["top_ks"] = top_ks
+        self.struct.top_k = int(top_k)
+        self.struct.top_ks = _ptr(top_ks)
 
     def set_tokens(self, draft_tokens):
         _check_dev(draft_tokens, "draft_tokens")

@@ -67,6 +67,16 @@ cudaError_t stats_with_hook(const StatsParams& p, cudaStream_t s) {
     }
     return cudaSuccess;
 }
+// The top-k pass (hook as above) and the finalize kernel reading its rows.
+cudaError_t topk_with_hook(const StatsParams& p, cudaStream_t s) {
+    cudaEvent_t e0 = t_ev_start, e1 = t_ev_stop;
+    t_ev_start = t_ev_stop = nullptr;
+    if (e0 && e1 && cudaEventRecord(e0, s) != cudaSuccess) return cudaErrorUnknown;
+    cudaError_t e = launch_topk(p, s);
+    if (e != cudaSuccess) return e;
+    if (e0 && e1 && cudaEventRecord(e1, s) != cudaSuccess) return cudaErrorUnknown;
+    return launch_finalize(p, s);
+}
 inline size_t esize(int32_t dt) { return dt == SPEC_F32 ? 4 : 2; }
 
 // Host fields only; no CUDA call.
@@ -104,6 +114,7 @@ spec_status_t check_call(const spec_verify_args_t* a, int greedy) {
         if (!a->temperatures && !(a->temperature > 0.f && a->temperature < 3.0e38f)) return SPEC_ERR_INVALID_ARG;
         if (a->temperatures && !aligned(a->temperatures, 4)) return SPEC_ERR_ALIGNMENT;
         if (a->uniforms && !aligned(a->uniforms, 8)) return SPEC_ERR_ALIGNMENT;
+        if (a->top_ks && !aligned(a->top_ks, 4)) return SPEC_ERR_ALIGNMENT;
     }
     if (a->block_size < 0) return SPEC_ERR_INVALID_ARG;
     if ((a->kv_lens_out || a->out_num_blocks) && !a->kv_lens_in) return SPEC_ERR_INVALID_ARG;
@@ -130,6 +141,13 @@ bool tma_ok(const spec_verify_args_t* a, int greedy) {
     if (!greedy && a->rows_draft > 0 && (!aligned(a->draft, 16) || (V * esize(a->draft_dtype)) % 16 != 0))
         return false;
     return true;
+}
+
+// Whether any sequence of a sampling call truncates to its top k (host
+// fields only: a per-sequence array counts as truncating).
+bool topk_on(const spec_verify_args_t* a, int greedy) {
+    if (greedy) return false;
+    return a->top_ks != nullptr || (a->top_k > 0 && a->top_k < a->vocab);
 }
 
 bool build_params(const spec_verify_args_t* a, int greedy, int grid_cap, int tma, StatsParams& p, Layout& L) {
@@ -176,6 +194,11 @@ bool build_params(const spec_verify_args_t* a, int greedy, int grid_cap, int tma
     p.row_stats = (float2*)(ws + L.off_rowstats);
     p.pq = (float2*)(ws + L.off_pq);
     p.tasks = (SampleTask*)(ws + L.off_tasks);
+    const bool tk = topk_on(a, greedy);
+    p.top_ks = tk ? a->top_ks : nullptr;
+    p.top_k = tk ? a->top_k : 0;
+    p.direct = tk ? 1 : 0;
+    p.tau = tk ? (float*)(ws + L.off_tau) : nullptr;
     return true;
 }
 
@@ -254,7 +277,12 @@ SPEC_API spec_status_t spec_verify_sample(const spec_verify_args_t* a, spec_stre
     spec_status_t st = prepare(a, 0, p, L, dev);
     if (st) return st;
     cudaStream_t s = (cudaStream_t)stream;
-    if (stats_with_hook(p, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    if (p.direct) {
+        // top-k: thresholds and truncated row statistics in one pass, then finalize
+        if (topk_with_hook(p, s) != cudaSuccess) return SPEC_ERR_CUDA;
+    } else if (stats_with_hook(p, s) != cudaSuccess) {
+        return SPEC_ERR_CUDA;
+    }
     SampleParams sp;
     sp.tgt = p.tgt;
     sp.dft = p.dft;

@@ -52,7 +52,8 @@ struct __align__(16) SampleTask {
     float mt, md;      // raw maxima of the target / draft row
     float it_apx, id_apx;  // 1 / row normaliser of the target / draft row from the streaming pass (~1e-6)
     float z_hi, z_lo;  // written by the sampler: the Z it used
-    int32_t pad[3];
+    float tau_t, tau_d;  // top-k thresholds of the two rows: columns below weigh 0 (-inf: no truncation)
+    int32_t pad;
 };
 static_assert(sizeof(SampleTask) == 80, "task layout");
 
@@ -88,6 +89,13 @@ struct StatsParams {
     float2* row_stats;   // [rows_total] merged per-row statistics
     float2* pq;          // [rows_d] (p(x), q(x))
     SampleTask* tasks;   // [B]
+    // top-k truncation (sampling only): sequence b keeps the columns of each
+    // of its rows whose value is at least the row's k_b-th largest, k_b =
+    // top_ks[b] if top_ks, else top_k; k_b <= 0 or k_b >= V keeps every column
+    const int32_t* top_ks;
+    int32_t top_k;
+    int32_t direct;      // 1: row_stats were written whole by the top-k pass; finalize reads them
+    float* tau;          // [rows_total] threshold of every row (-inf: whole row), or null without top-k
 };
 
 // Table 2^(i/64), i = 0..63, as float pairs (value = hi + lo).
@@ -125,7 +133,7 @@ struct SampleParams {
 struct Layout {
     int64_t rows_total, N, chunk;
     int32_t S, grid;
-    size_t off_partials, off_rowstats, off_pq, off_tasks, off_recs, total;
+    size_t off_partials, off_rowstats, off_pq, off_tasks, off_recs, off_tau, total;
 };
 
 // Work split and workspace layout for a given problem. grid_cap bounds the
@@ -137,6 +145,10 @@ cudaError_t launch_stats(const StatsParams& p, cudaStream_t s);
 // streaming pass by programmatic launch.
 cudaError_t launch_finalize(const StatsParams& p, cudaStream_t s);
 int stats_resident_ctas(int device, int greedy);  // CTAs that fit at once on the device (plain-load variant)
+// Top-k pass: for every row (one CTA each) its threshold into p.tau and its
+// statistics over the kept columns into p.row_stats; replaces the streaming
+// pass when any sequence truncates (finalize then runs with p.direct = 1).
+cudaError_t launch_topk(const StatsParams& p, cudaStream_t s);
 cudaError_t launch_sampler(const SampleParams& p, cudaStream_t s, bool pdl);
 void exp2_pairs(Exp2Pairs& t);  // host: fills the table
 cudaError_t launch_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,

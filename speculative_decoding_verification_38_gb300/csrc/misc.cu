@@ -75,8 +75,9 @@ __device__ df dbg_block_sum_df(df v, df* red) {
 }
 
 __device__ __forceinline__ df dbg_weight(const char* row, int dt, int64_t j, float lmax, df k, bool probs,
-                                         const Exp2Table& tab) {
+                                         float tau, const Exp2Table& tab) {
     const float l = ld_elem_rt(row, dt, j);
+    if (!(l >= tau)) return df{0.f, 0.f};  // below the row's top-k threshold (or NaN)
     if (probs) return df{(l > -INFINITY) ? l : 0.f, 0.f};
     return dt == SPECV_F32 ? logit_weight<true>(l, lmax, k, tab) : logit_weight<false>(l, lmax, k, tab);
 }
@@ -108,21 +109,23 @@ __global__ void __launch_bounds__(kDbgThreads) debug_probs_kernel(StatsParams p,
     const char* trow = (const char*)p.tgt + (t0 + pos) * p.V * te;
     const char* drow = draftpos ? (const char*)p.dft + (d0 + pos) * p.V * de : trow;
     const bool probs = p.probs != 0;
+    const float tt = p.tau ? p.tau[t0 + pos] : -INFINITY;
+    const float td = (p.tau && draftpos) ? p.tau[p.rows_t + d0 + pos] : -INFINITY;
     df at{0.f, 0.f}, ad{0.f, 0.f};
     for (int64_t j = threadIdx.x; j < p.V; j += blockDim.x) {
-        acc_add(at, dbg_weight(trow, p.tdt, j, mt, k, false, tab));
-        if (draftpos) acc_add(ad, dbg_weight(drow, p.ddt, j, md, k, probs, tab));
+        acc_add(at, dbg_weight(trow, p.tdt, j, mt, k, false, tt, tab));
+        if (draftpos) acc_add(ad, dbg_weight(drow, p.ddt, j, md, k, probs, td, tab));
     }
     const df St = dbg_block_sum_df(df_norm(at), red);
     const df Sd = draftpos ? dbg_block_sum_df(df_norm(ad), red) : df{1.f, 0.f};
     const df It = df_recip(St), Id = df_recip(Sd);
     df az{0.f, 0.f};
     for (int64_t j = threadIdx.x; j < p.V; j += blockDim.x) {
-        const df wt = dbg_weight(trow, p.tdt, j, mt, k, false, tab);
+        const df wt = dbg_weight(trow, p.tdt, j, mt, k, false, tt, tab);
         const df pv = df_mul(wt, It);
         df qv{0.f, 0.f};
         if (draftpos) {
-            const df wd = dbg_weight(drow, p.ddt, j, md, k, probs, tab);
+            const df wd = dbg_weight(drow, p.ddt, j, md, k, probs, td, tab);
             qv = df_mul(wd, Id);
             acc_add(az, resid_weight(wt, wd, It, Id));
         }
@@ -134,9 +137,9 @@ __global__ void __launch_bounds__(kDbgThreads) debug_probs_kernel(StatsParams p,
     const df Iz = use_r ? df_recip(Z) : df{1.f, 0.f};
     if (out_w) {
         for (int64_t j = threadIdx.x; j < p.V; j += blockDim.x) {
-            const df wt = dbg_weight(trow, p.tdt, j, mt, k, false, tab);
+            const df wt = dbg_weight(trow, p.tdt, j, mt, k, false, tt, tab);
             df w = df_mul(wt, It);
-            if (use_r) w = df_mul(resid_weight(wt, dbg_weight(drow, p.ddt, j, md, k, probs, tab), It, Id), Iz);
+            if (use_r) w = df_mul(resid_weight(wt, dbg_weight(drow, p.ddt, j, md, k, probs, td, tab), It, Id), Iz);
             out_w[j] = w.hi;
         }
     }

@@ -45,35 +45,20 @@ struct SampSmem {
     float uw[kWarps][4];       // the first one's weights (wt hi, lo, wd hi, lo)
 };
 
-// One row's chunk: column j (0-based within the chunk) lives in shared memory
-// at s + j * esz when staged, else in global memory at g + j * esz.
+// One row's chunk: column j (0-based within the chunk) at g + j * esz. With
+// top-k truncation, columns whose value is below tau read as -inf (weight 0).
 struct Src {
     const char* g;
-    uint32_t s;
     int64_t n;  // columns in the chunk
-    bool staged, al;
+    float tau;  // the row's top-k threshold (-inf: no truncation)
+    bool al;    // g is 16-byte aligned
 };
+
+__device__ __forceinline__ float keep_top(float v, float tau) { return v >= tau ? v : -INFINITY; }
 
 template <int DT>
 __device__ __forceinline__ float src_elem(const Src& r, int64_t j) {
-    if (r.staged) {
-        if constexpr (DT == SPECV_BF16) {
-            unsigned short h;
-            asm volatile("ld.shared.u16 %0, [%1];" : "=h"(h) : "r"(r.s + (uint32_t)(j * 2)));
-            return __uint_as_float(((uint32_t)h) << 16);
-        } else {
-            float f;
-            asm volatile("ld.shared.f32 %0, [%1];" : "=f"(f) : "r"(r.s + (uint32_t)(j * 4)));
-            return f;
-        }
-    }
-    return ld_elem<DT>(r.g, j);
-}
-
-__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
+    return keep_top(ld_elem<DT>(r.g, j), r.tau);
 }
 
 // Columns j..j+7 of a chunk as floats; columns past the chunk read as -inf
@@ -81,24 +66,22 @@ __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
 // for double-float evaluation are read again moments later.
 template <int DT>
 __device__ __forceinline__ void src_load8(const Src& r, int64_t j, float (&v)[8]) {
-    if (j + 8 <= r.n && (r.staged || r.al)) {
+    if (j + 8 <= r.n && r.al) {
         if constexpr (DT == SPECV_BF16) {
-            const uint4 q = r.staged ? lds_v4(r.s + (uint32_t)(j * 2)) : __ldg(reinterpret_cast<const uint4*>(r.g + j * 2));
+            const uint4 q = __ldg(reinterpret_cast<const uint4*>(r.g + j * 2));
             v[0] = bf16_lo(q.x); v[1] = bf16_hi(q.x); v[2] = bf16_lo(q.y); v[3] = bf16_hi(q.y);
             v[4] = bf16_lo(q.z); v[5] = bf16_hi(q.z); v[6] = bf16_lo(q.w); v[7] = bf16_hi(q.w);
         } else {
-            uint4 q0, q1;
-            if (r.staged) {
-                q0 = lds_v4(r.s + (uint32_t)(j * 4));
-                q1 = lds_v4(r.s + (uint32_t)(j * 4 + 16));
-            } else {
-                q0 = __ldg(reinterpret_cast<const uint4*>(r.g + j * 4));
-                q1 = __ldg(reinterpret_cast<const uint4*>(r.g + j * 4 + 16));
-            }
+            const uint4 q0 = __ldg(reinterpret_cast<const uint4*>(r.g + j * 4));
+            const uint4 q1 = __ldg(reinterpret_cast<const uint4*>(r.g + j * 4 + 16));
             v[0] = __uint_as_float(q0.x); v[1] = __uint_as_float(q0.y);
             v[2] = __uint_as_float(q0.z); v[3] = __uint_as_float(q0.w);
             v[4] = __uint_as_float(q1.x); v[5] = __uint_as_float(q1.y);
             v[6] = __uint_as_float(q1.z); v[7] = __uint_as_float(q1.w);
+        }
+        if (r.tau > -INFINITY) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] = keep_top(v[e], r.tau);
         }
     } else {
 #pragma unroll
@@ -271,8 +254,8 @@ __device__ __forceinline__ RowPair<TDT, DDT> tile_rows(const SampleParams& p, co
     rp.t.n = rp.d.n = n;
     rp.t.al = ((uintptr_t)rp.t.g & 15u) == 0;
     rp.d.al = ((uintptr_t)rp.d.g & 15u) == 0;
-    rp.t.staged = rp.d.staged = false;
-    rp.t.s = rp.d.s = 0;
+    rp.t.tau = t.tau_t;
+    rp.d.tau = resid ? t.tau_d : t.tau_t;
     rp.probs = t.probs != 0;
     rp.mt = t.mt;
     rp.md = t.md;

@@ -532,7 +532,8 @@ __device__ void finalize_sample(const StatsParams& p, int32_t b, Smem& sm) {
             t.it_apx = inv_norm_apx(sm.rs[a], k);
             t.id_apx = a < g ? (p.probs ? 1.0f / sm.rs[g + 1 + a].y : inv_norm_apx(sm.rs[g + 1 + a], k)) : 0.f;
             t.z_hi = t.z_lo = 0.f;
-            t.pad[0] = t.pad[1] = t.pad[2] = 0;
+            t.tau_t = t.tau_d = -INFINITY;  // this path never truncates
+            t.pad = 0;
             p.tasks[b] = t;
         }
     }
@@ -1098,9 +1099,13 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
         for (int j = warp - 1; j < nrows; j += kFinWarps - 1) {
             const bool is_t = j <= g;
             const int64_t r = is_t ? (t0 + j) : (p.rows_t + d0 + (j - g - 1));
+            float2 v;
+            if (p.direct) {  // the top-k pass wrote the row's statistics whole
+                if (lane == 0) fs.rs[j] = __ldcg(p.row_stats + r);
+                continue;
+            }
             const float2* src = p.partials + r * p.S * p.pw;
             const int32_t n = pieces_of_row(p, r);
-            float2 v;
             if (p.greedy) {
                 int32_t ix;
                 warp_merge_am(src, n, v.x, ix);
@@ -1117,8 +1122,9 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
         if (warp == 0) warp_write_error(p, b, fs.status, t0, g);
         return;
     }
-    for (int j = threadIdx.x; j < nrows; j += kFinThreads)
-        p.row_stats[j <= g ? t0 + j : p.rows_t + d0 + (j - g - 1)] = fs.rs[j];
+    if (!p.direct)
+        for (int j = threadIdx.x; j < nrows; j += kFinThreads)
+            p.row_stats[j <= g ? t0 + j : p.rows_t + d0 + (j - g - 1)] = fs.rs[j];
     if (warp != 0) return;
     if (p.greedy) {
         int32_t a = g;
@@ -1148,9 +1154,13 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
         if (i < g) {
             const float2 ts = fs.rs[i], ds = fs.rs[g + 1 + i];
             bad = !row_ok(ts, false) || !row_ok(ds, p.probs != 0);
-            const float pxv = ex2(__fmaf_rn(lt[h], k, -__fmul_rn(ts.x, k))) * (1.0f / ts.y);
-            const float qxv =
+            float pxv = ex2(__fmaf_rn(lt[h], k, -__fmul_rn(ts.x, k))) * (1.0f / ts.y);
+            float qxv =
                 p.probs ? ld[h] * (1.0f / ds.y) : ex2(__fmaf_rn(ld[h], k, -__fmul_rn(ds.x, k))) * (1.0f / ds.y);
+            if (p.tau) {  // a token outside a row's top-k has probability 0 there
+                if (!(lt[h] >= __ldcg(p.tau + t0 + i))) pxv = 0.f;
+                if (!(ld[h] >= __ldcg(p.tau + p.rows_t + d0 + i))) qxv = 0.f;
+            }
             p.pq[d0 + i] = make_float2(pxv, qxv);
             stop = bad || !(__fmul_rn(ua[h], qxv) < pxv);
         }
@@ -1195,7 +1205,9 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
         t.it_apx = inv_norm_apx(fs.rs[a], k);
         t.id_apx = a < g ? (p.probs ? 1.0f / fs.rs[g + 1 + a].y : inv_norm_apx(fs.rs[g + 1 + a], k)) : 0.f;
         t.z_hi = t.z_lo = 0.f;
-        t.pad[0] = t.pad[1] = t.pad[2] = 0;
+        t.tau_t = p.tau ? __ldcg(p.tau + t0 + a) : -INFINITY;
+        t.tau_d = (p.tau && a < g) ? __ldcg(p.tau + p.rows_t + d0 + a) : -INFINITY;
+        t.pad = 0;
         p.tasks[b] = t;
     }
 }
@@ -1225,6 +1237,8 @@ Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int gre
     off = al(off + (greedy ? 0 : (size_t)B * sizeof(SampleTask)));
     L.off_recs = off;
     off = al(off + (greedy ? 0 : (size_t)B * ((V + kTile - 1) / kTile) * sizeof(TileRec)));
+    L.off_tau = off;
+    off = al(off + (greedy ? 0 : (size_t)L.rows_total * sizeof(float)));
     L.total = off;
     return L;
 }

@@ -1,0 +1,504 @@
+// topk.cu -- top-k truncation for the sampling verify.
+//
+// Both models' rows go through the same processing ("Speculative decoding"
+// (mhtirogla.ai), Implementation notes), so a sequence that samples from its
+// top k truncates its target rows and its draft rows alike: a row keeps every
+// column whose value is at least tau, the row's k-th largest value (NaN ranks
+// as -inf; ties at tau all stay), and its distribution is renormalised over
+// the kept columns. For every row this pass writes tau and the statistics the
+// rest of the step reads: logits rows (m, s), m the raw maximum and
+// s = sum over kept columns of 2^(l k - fl(m k)), k = log2(e) / T;
+// probabilities rows (0, sum of the kept values).
+//
+// One CTA per row and one read of the row from HBM. Each warp filters its
+// share of the row against a threshold that only rises: it keeps in a
+// shared-memory buffer every value at least as large as its threshold, and
+// when the buffer fills it selects the k-th largest of its entries (radix
+// select on order-preserving keys), makes that the threshold and drops what
+// lies below. A warp therefore always holds at least k of its own values at
+// or above its threshold, so its threshold never passes the row's tau and the
+// buffers together hold every kept column. The CTA then selects tau over the
+// union of the buffers and sums the kept entries' weights in a fixed order
+// (the result does not depend on timing). Rows where that cannot work (k past
+// half a buffer, more equal values than a buffer holds, k off) select over
+// the row itself in L2, one read per radix digit, and sum it in one more read.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace specv {
+
+namespace {
+
+constexpr int kTkThreads = 512;
+constexpr int kTkWarps = kTkThreads / 32;
+constexpr int kTkUnroll = 8;        // 16-byte loads in flight per lane
+constexpr int kBufBytes = 4096;     // candidate buffer per warp
+constexpr unsigned kFull = 0xffffffffu;
+
+struct TkSmem {
+    uint32_t buf[kTkWarps][kBufBytes / 4];  // candidate value bits (u16 for bf16, u32 for f32)
+    uint32_t hist[kTkWarps][256];           // per-warp radix histograms; [0] is the CTA's after the pass
+    int32_t cnt[kTkWarps];
+    int32_t ovf[kTkWarps];
+    float mx[kTkWarps];
+    int32_t nan[kTkWarps];
+    float red[kTkWarps];
+    uint32_t sel_bin, sel_above;
+};
+constexpr size_t kTkSmemBytes = sizeof(TkSmem);
+
+// --------------------------------------------------------- order-preserving keys
+// Storage bits of one value with -0 folded into +0, so that equal values have
+// equal bits. bf16: the 16-bit pattern; f32: the 32-bit pattern.
+template <int DT>
+struct KeyTraits;
+template <>
+struct KeyTraits<SPECV_BF16> {
+    using Bits = uint16_t;
+    static constexpr int kDigits = 2;  // 16-bit keys
+    static constexpr int kEsz = 2;
+    __device__ static uint32_t canon(uint32_t h) { return h == 0x8000u ? 0u : h; }
+    __device__ static float value(uint32_t h) { return __uint_as_float(h << 16); }
+    // unsigned key whose order is the order of the values (NaN excluded)
+    __device__ static uint32_t key(uint32_t h) { return h ^ ((h & 0x8000u) ? 0xFFFFu : 0x8000u); }
+    __device__ static uint32_t bits_of_key(uint32_t k) { return k ^ ((k & 0x8000u) ? 0x8000u : 0xFFFFu); }
+};
+template <>
+struct KeyTraits<SPECV_F32> {
+    using Bits = uint32_t;
+    static constexpr int kDigits = 4;  // 32-bit keys
+    static constexpr int kEsz = 4;
+    __device__ static uint32_t canon(uint32_t h) { return h == 0x80000000u ? 0u : h; }
+    __device__ static float value(uint32_t h) { return __uint_as_float(h); }
+    __device__ static uint32_t key(uint32_t h) { return h ^ ((h & 0x80000000u) ? 0xFFFFFFFFu : 0x80000000u); }
+    __device__ static uint32_t bits_of_key(uint32_t k) {
+        return k ^ ((k & 0x80000000u) ? 0x80000000u : 0xFFFFFFFFu);
+    }
+};
+
+// Key of a loaded value for the selects over the row: NaN ranks lowest
+// (as -inf would), -0 as +0.
+template <int DT>
+__device__ __forceinline__ uint32_t key_of_value(float v) {
+    using KT = KeyTraits<DT>;
+    if (v != v) return 0u;
+    const uint32_t b = DT == SPECV_BF16 ? (__float_as_uint(v) >> 16) : __float_as_uint(v);
+    return KT::key(KT::canon(b));
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// Find, in a 256-bin histogram, the digit b holding the `remaining`-th
+// largest key: sum_{b' > b} h[b'] < remaining <= sum_{b' >= b} h[b']. One
+// warp; lane L reads bins 8L..8L+7. Needs 1 <= remaining <= sum h. Returns b
+// and (in `above`) the count in the bins above it, in every lane.
+__device__ __forceinline__ uint32_t warp_find_bin(const uint32_t* h, uint32_t remaining, uint32_t& above) {
+    const int lane = threadIdx.x & 31;
+    uint32_t c[8], t = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        c[j] = h[lane * 8 + j];
+        t += c[j];
+    }
+    uint32_t s = t;  // inclusive suffix sum over lanes lane..31
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_down_sync(kFull, s, o);
+        if (lane + o < 32) s += v;
+    }
+    const uint32_t hi = s - t;  // keys in the bins of higher lanes
+    const bool mine = hi < remaining && remaining <= s;
+    uint32_t bin = 0, ab = 0;
+    if (mine) {
+        uint32_t acc = hi;
+#pragma unroll
+        for (int j = 7; j >= 0; --j) {
+            if (acc + c[j] >= remaining) {
+                bin = lane * 8 + j;
+                ab = acc;
+                break;
+            }
+            acc += c[j];
+        }
+    }
+    const uint32_t owner = __ballot_sync(kFull, mine);
+    const int src = owner ? __ffs(owner) - 1 : 0;
+    above = __shfl_sync(kFull, ab, src);
+    return __shfl_sync(kFull, bin, src);
+}
+
+// The kk-th largest key among a warp's buffer entries (1 <= kk <= cnt), by
+// most-significant-digit radix select with the warp's own histogram.
+template <int DT>
+__device__ uint32_t warp_select(const typename KeyTraits<DT>::Bits* wb, int cnt, uint32_t kk, uint32_t* hist) {
+    using KT = KeyTraits<DT>;
+    const int lane = threadIdx.x & 31;
+    uint32_t prefix = 0, remaining = kk;
+#pragma unroll 1
+    for (int d = KT::kDigits - 1; d >= 0; --d) {
+        const int sh = 8 * d;
+        for (int i = lane; i < 256; i += 32) hist[i] = 0;
+        __syncwarp();
+        for (int e = lane; e < cnt; e += 32) {
+            const uint32_t key = KT::key(wb[e]);
+            if (d == KT::kDigits - 1 || (key >> (sh + 8)) == (prefix >> (sh + 8)))
+                atomicAdd(&hist[(key >> sh) & 255u], 1u);
+        }
+        __syncwarp();
+        uint32_t above;
+        const uint32_t bin = warp_find_bin(hist, remaining, above);
+        __syncwarp();
+        prefix |= bin << sh;
+        remaining -= above;
+    }
+    return prefix;
+}
+
+// Keep the entries whose key is at least kmin, in order (in place).
+template <int DT>
+__device__ int warp_compact(typename KeyTraits<DT>::Bits* wb, int cnt, uint32_t kmin) {
+    using KT = KeyTraits<DT>;
+    const int lane = threadIdx.x & 31;
+    int out = 0;
+    for (int base = 0; base < cnt; base += 32) {
+        const int e = base + lane;
+        const uint32_t bits = e < cnt ? (uint32_t)wb[e] : 0u;
+        const bool keep = e < cnt && KT::key(bits) >= kmin;
+        const uint32_t bal = __ballot_sync(kFull, keep);
+        __syncwarp();  // every lane has read its entry before any write
+        if (keep) wb[out + __popc(bal & lanemask_lt())] = (typename KT::Bits)bits;
+        out += __popc(bal);
+        __syncwarp();
+    }
+    return out;
+}
+
+// ------------------------------------------------------- the filtering pass
+__device__ __forceinline__ uint32_t max_nan_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ float max_nan_f32(float a, float b) {
+    float d;
+    asm("max.NaN.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+    return d;
+}
+
+// Largest of the values in one 16-byte vector; NaN if any is NaN.
+template <int DT>
+__device__ __forceinline__ float vec_max(const uint4& q) {
+    if constexpr (DT == SPECV_BF16) {
+        const uint32_t m2 = max_nan_bf16x2(max_nan_bf16x2(q.x, q.y), max_nan_bf16x2(q.z, q.w));
+        return max_nan_f32(bf16_lo(m2), bf16_hi(m2));
+    } else {
+        return max_nan_f32(max_nan_f32(__uint_as_float(q.x), __uint_as_float(q.y)),
+                           max_nan_f32(__uint_as_float(q.z), __uint_as_float(q.w)));
+    }
+}
+
+// Append this lane's values of one vector that are >= thr (when `need`) to
+// the warp's buffer, slot by slot, lanes in order within a slot.
+template <int DT>
+__device__ __forceinline__ void warp_append(typename KeyTraits<DT>::Bits* wb, int& cnt, const uint4& q, bool need,
+                                            float thr) {
+    using KT = KeyTraits<DT>;
+    constexpr int EPV = 16 / KT::kEsz;
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    const uint32_t lt = lanemask_lt();
+#pragma unroll
+    for (int e = 0; e < EPV; ++e) {
+        const uint32_t bits = DT == SPECV_BF16 ? ((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu)) : w[e];
+        const bool c = need && KT::value(bits) >= thr;
+        const uint32_t bal = __ballot_sync(kFull, c);
+        if (c) wb[cnt + __popc(bal & lt)] = (typename KT::Bits)KT::canon(bits);
+        cnt += __popc(bal);
+    }
+}
+
+// Raise the warp's threshold to the kk-th largest of its buffer and drop the
+// entries below it. Returns false when the survivors (ties) leave less than
+// `room` free entries.
+template <int DT>
+__device__ __forceinline__ bool warp_make_room(typename KeyTraits<DT>::Bits* wb, int& cnt, uint32_t kk, float& thr,
+                                               uint32_t* hist, int room) {
+    using KT = KeyTraits<DT>;
+    constexpr int C = kBufBytes / KT::kEsz;
+    const uint32_t K = warp_select<DT>(wb, cnt, kk, hist);
+    cnt = warp_compact<DT>(wb, cnt, K);
+    thr = KT::value(KT::bits_of_key(K));
+    return cnt <= C - room;
+}
+
+// One warp's share of the row: vectors it + u * kTkThreads + warp * 32 + lane
+// (u < kTkUnroll) of every iteration, plus, for warp 0, the columns before
+// the first 16-byte boundary and after the last full vector. With `filt`,
+// the warp's buffer ends holding every value of its share that is at least
+// its final threshold (in the order met); the warp's maximum, NaN flag,
+// entry count and overflow flag go to shared memory.
+template <int DT>
+__device__ void filter_pass(const char* row, int64_t V, uint32_t kk, bool filt, TkSmem& sm) {
+    using KT = KeyTraits<DT>;
+    using Bits = typename KT::Bits;
+    constexpr int ESZ = KT::kEsz, EPV = 16 / ESZ, C = kBufBytes / ESZ, STEP = 32 * EPV;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Bits* wb = reinterpret_cast<Bits*>(sm.buf[warp]);
+    uint32_t* hist = sm.hist[warp];
+    int64_t head = (int64_t)(((16u - (uint32_t)((uintptr_t)row & 15u)) & 15u) / ESZ);
+    if (head > V) head = V;
+    const int64_t nvec = (V - head) / EPV;
+    const int64_t tail0 = head + nvec * EPV;
+    const uint4* vrow = reinterpret_cast<const uint4*>(row + head * ESZ);
+    float thr = -INFINITY, lmax = -INFINITY;
+    int cnt = 0;
+    bool nan = false, ovf = false;
+
+    for (int64_t it = 0; it < nvec; it += (int64_t)kTkUnroll * kTkThreads) {
+        const int64_t v0 = it + warp * 32 + lane;
+        uint4 q[kTkUnroll];
+#pragma unroll
+        for (int u = 0; u < kTkUnroll; ++u) {
+            const int64_t vi = v0 + (int64_t)u * kTkThreads;
+            q[u] = vi < nvec ? ld_stream_v4(vrow + vi) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        float mx[kTkUnroll];
+#pragma unroll
+        for (int u = 0; u < kTkUnroll; ++u) {
+            const bool valid = v0 + (int64_t)u * kTkThreads < nvec;
+            const float m = vec_max<DT>(q[u]);
+            nan |= valid && m != m;
+            mx[u] = valid ? m : -INFINITY;
+            lmax = fmaxf(lmax, mx[u]);
+        }
+        if (!filt) continue;
+#pragma unroll
+        for (int u = 0; u < kTkUnroll; ++u) {
+            const bool valid = v0 + (int64_t)u * kTkThreads < nvec;
+            bool need = valid && mx[u] >= thr;
+            if (!__any_sync(kFull, need)) continue;
+            if (cnt > C - STEP) {
+                if (!warp_make_room<DT>(wb, cnt, kk, thr, hist, STEP)) {
+                    filt = false;
+                    ovf = true;
+                    break;
+                }
+                need = valid && mx[u] >= thr;
+            }
+            warp_append<DT>(wb, cnt, q[u], need, thr);
+        }
+    }
+    if (warp == 0) {  // the ragged ends: at most EPV - 1 columns each
+        int64_t col = -1;
+        if (lane < head)
+            col = lane;
+        else if (lane >= 16 && (int64_t)(lane - 16) < V - tail0)
+            col = tail0 + (lane - 16);
+        const float v = col >= 0 ? ld_elem<DT>(row, col) : -INFINITY;
+        nan |= v != v;
+        lmax = fmaxf(lmax, v);
+        if (filt) {
+            bool need = col >= 0 && v >= thr;
+            if (__any_sync(kFull, need)) {
+                bool ok = true;
+                if (cnt > C - 32) {
+                    ok = warp_make_room<DT>(wb, cnt, kk, thr, hist, 32);
+                    need = col >= 0 && v >= thr;
+                }
+                if (ok) {
+                    const uint32_t bits = DT == SPECV_BF16 ? (__float_as_uint(v) >> 16) : __float_as_uint(v);
+                    const uint32_t bal = __ballot_sync(kFull, need);
+                    if (need) wb[cnt + __popc(bal & lanemask_lt())] = (Bits)KT::canon(bits);
+                    cnt += __popc(bal);
+                } else {
+                    ovf = true;
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lmax = fmaxf(lmax, __shfl_xor_sync(kFull, lmax, o));
+    nan = __any_sync(kFull, nan);
+    if (lane == 0) {
+        sm.cnt[warp] = cnt;
+        sm.ovf[warp] = ovf;
+        sm.mx[warp] = lmax;
+        sm.nan[warp] = nan;
+    }
+}
+
+// ------------------------------------------------------------ CTA level
+// The kk-th largest key over every key `each` visits (each thread visits its
+// own share; 1 <= kk <= their number), by MSD radix select with the CTA's
+// histogram hist[0].
+template <int DT, class Each>
+__device__ uint32_t block_select(uint32_t kk, TkSmem& sm, const Each& each) {
+    using KT = KeyTraits<DT>;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t* h = sm.hist[0];
+    uint32_t prefix = 0, remaining = kk;
+#pragma unroll 1
+    for (int d = KT::kDigits - 1; d >= 0; --d) {
+        const int sh = 8 * d;
+        __syncthreads();  // the last users of h and sel_* are done
+        for (int i = threadIdx.x; i < 256; i += kTkThreads) h[i] = 0;
+        __syncthreads();
+        each([&](uint32_t key) {
+            if (d == KT::kDigits - 1 || (key >> (sh + 8)) == (prefix >> (sh + 8)))
+                atomicAdd(&h[(key >> sh) & 255u], 1u);
+        });
+        __syncthreads();
+        if (warp == 0) {
+            uint32_t above;
+            const uint32_t bin = warp_find_bin(h, remaining, above);
+            if (lane == 0) {
+                sm.sel_bin = bin;
+                sm.sel_above = above;
+            }
+        }
+        __syncthreads();
+        prefix |= sm.sel_bin << sh;
+        remaining -= sm.sel_above;
+    }
+    return prefix;
+}
+
+// Sum over the CTA, the same association whatever the timing.
+__device__ float block_sum_fixed(float v, TkSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+    if (lane == 0) sm.red[warp] = v;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kTkWarps; ++w) t += sm.red[w];
+    return t;
+}
+
+// Weight of a kept value: 2^(l k - fl(m k)) for logits, the value itself for
+// probabilities.
+__device__ __forceinline__ float kept_weight(float v, bool probs_row, float k2, float nmk) {
+    return probs_row ? v : ex2(__fmaf_rn(v, k2, nmk));
+}
+
+template <int DT>
+__device__ void row_topk(const StatsParams& p, int64_t r, const char* row, int64_t kk, bool off, bool probs_row,
+                         float k2, TkSmem& sm) {
+    using KT = KeyTraits<DT>;
+    using Bits = typename KT::Bits;
+    constexpr int C = kBufBytes / KT::kEsz;
+    const int64_t V = p.V;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const bool filt = !off && kk <= C / 2;
+    filter_pass<DT>(row, V, (uint32_t)kk, filt, sm);
+    __syncthreads();
+    float m = -INFINITY;
+    bool nan = false, ovf = false;
+#pragma unroll
+    for (int w = 0; w < kTkWarps; ++w) {
+        m = fmaxf(m, sm.mx[w]);
+        nan |= sm.nan[w] != 0;
+        ovf |= sm.ovf[w] != 0;
+    }
+    const float nmk = -__fmul_rn(m, k2);
+    float tau = -INFINITY, acc = 0.f;
+    if (!off && filt && !ovf) {
+        // tau over the union of the buffers, then the kept entries' weights
+        const Bits* wb = reinterpret_cast<const Bits*>(sm.buf[warp]);
+        const int cnt = sm.cnt[warp];
+        const uint32_t K = block_select<DT>((uint32_t)kk, sm, [&](auto&& f) {
+            for (int e = lane; e < cnt; e += 32) f(KT::key(wb[e]));
+        });
+        tau = KT::value(KT::bits_of_key(K));
+        for (int e = lane; e < cnt; e += 32) {
+            const float v = KT::value(wb[e]);
+            if (v >= tau) acc += kept_weight(v, probs_row, k2, nmk);
+        }
+    } else {
+        // over the row itself (in L2 after the pass)
+        if (!off) {
+            const uint32_t K = block_select<DT>((uint32_t)kk, sm, [&](auto&& f) {
+                for (int64_t j = threadIdx.x; j < V; j += kTkThreads) f(key_of_value<DT>(ld_elem<DT>(row, j)));
+            });
+            tau = KT::value(KT::bits_of_key(K));
+        }
+        for (int64_t j = threadIdx.x; j < V; j += kTkThreads) {
+            const float v = ld_elem<DT>(row, j);
+            if (v >= tau) acc += kept_weight(v, probs_row, k2, nmk);
+        }
+    }
+    float s = block_sum_fixed(acc, sm);
+    if (threadIdx.x == 0) {
+        if (nan) s = NAN;  // a NaN anywhere makes the row invalid
+        p.row_stats[r] = make_float2(probs_row ? 0.f : m, s);
+        p.tau[r] = tau;
+    }
+}
+
+// Sequence owning local row lr of the target (draft = false) or draft
+// tensor, or -1 if none does.
+__device__ int32_t row_seq(const StatsParams& p, bool draft, int64_t lr) {
+    const int64_t* off = draft ? p.dro : p.tro;
+    if (!off) {
+        const int64_t per = draft ? p.gmax : p.gmax + 1;
+        const int64_t b = per > 0 ? lr / per : p.B;
+        return b < p.B ? (int32_t)b : -1;
+    }
+    int32_t lo = 0, hi = p.B - 1;  // largest b with off[b] <= lr
+    while (lo < hi) {
+        const int32_t mid = (lo + hi + 1) >> 1;
+        if (__ldg(off + mid) <= lr)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    if (lr < __ldg(off + lo) || lr >= __ldg(off + lo + 1)) return -1;
+    return lo;
+}
+
+__global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(StatsParams p) {
+    extern __shared__ __align__(16) unsigned char tk_raw[];
+    TkSmem& sm = *reinterpret_cast<TkSmem*>(tk_raw);
+    pdl_launch_dependents();
+    const int64_t r = blockIdx.x;
+    const bool is_t = r < p.rows_t;
+    const int64_t lr = is_t ? r : r - p.rows_t;
+    const int32_t b = row_seq(p, !is_t, lr);
+    const int dt = is_t ? p.tdt : p.ddt;
+    const bool probs_row = !is_t && p.probs != 0;
+    const int64_t kk = b < 0 ? 0 : (p.top_ks ? (int64_t)__ldg(p.top_ks + b) : (int64_t)p.top_k);
+    const bool off = kk <= 0 || kk >= p.V;
+    float T = b < 0 ? 1.f : (p.temps ? __ldg(p.temps + b) : p.temperature);
+    if (!(T > 0.f) || !isfinite(T)) T = 1.f;  // the finalize reports the sequence's bad temperature
+    const float k2 = kLog2e / T;
+    const int64_t esz = dt == SPECV_F32 ? 4 : 2;
+    const char* row = (const char*)(is_t ? p.tgt : p.dft) + lr * p.V * esz;
+    if (dt == SPECV_F32)
+        row_topk<SPECV_F32>(p, r, row, kk, off, probs_row, k2, sm);
+    else
+        row_topk<SPECV_BF16>(p, r, row, kk, off, probs_row, k2, sm);
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const StatsParams& p, cudaStream_t s) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kTkSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const int64_t rows = p.rows_t + p.rows_d;
+    if (rows < 1) return cudaSuccess;
+    topk_kernel<<<(unsigned)rows, kTkThreads, kTkSmemBytes, s>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace specv

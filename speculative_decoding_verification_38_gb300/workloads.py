@@ -137,16 +137,25 @@ def zipf_rows(rng: np.random.Generator, rows: int, V: int, block: int = 256) -> 
 
 
 def gumbel_argmax(rng: np.random.Generator, logits_f32: np.ndarray, temps_per_row: np.ndarray,
-                  block: int = 256) -> np.ndarray:
-    """Drafter simulation: one draw x ~ softmax(l / T) per row via Gumbel-max."""
-    rows = logits_f32.shape[0]
+                  block: int = 256, k_per_row: np.ndarray | None = None) -> np.ndarray:
+    """Drafter simulation: one draw x ~ softmax(l / T) per row via Gumbel-max.
+    With k_per_row, a drafter that samples from its own top k: row r draws
+    only among its columns at least as large as its k-th largest logit
+    (k <= 0 or k >= V: every column)."""
+    rows, V = logits_f32.shape
     out = np.empty(rows, dtype=np.int32)
     for r0 in range(0, rows, block):
         n = min(block, rows - r0)
-        u = rng.random((n, logits_f32.shape[1]), dtype=np.float32)
+        u = rng.random((n, V), dtype=np.float32)
         with np.errstate(divide="ignore"):
             g = -np.log(-np.log(u))
         z = logits_f32[r0:r0 + n] / temps_per_row[r0:r0 + n, None] + g
+        if k_per_row is not None:
+            for i in range(n):
+                k = int(k_per_row[r0 + i])
+                if 0 < k < V:
+                    row = logits_f32[r0 + i]
+                    z[i, row < np.partition(row, V - k)[V - k]] = -np.inf
         out[r0:r0 + n] = np.argmax(z, axis=1)
     return out
 
@@ -158,8 +167,9 @@ def _store(x: np.ndarray, dtype: str) -> np.ndarray:
 def sampling_workload(name: str, *, config: int, batch: int, vocab: int, gammas, profile: str,
                       dtype: str, sigma, temps, kv_range=None, block_size: int = 0,
                       ragged: bool = False, pool: int = 1, dataset: int = 0,
-                      gauss_std: float = 2.0) -> Workload:
-    """Generic sampling-verify workload; sigma and temps are scalars or [B] arrays."""
+                      gauss_std: float = 2.0, top_k=0) -> Workload:
+    """Generic sampling-verify workload; sigma, temps and top_k are scalars or
+    [B] arrays. With top-k on, the simulated drafter samples from its top k."""
     rng = _rng(config, dataset)
     gammas = np.asarray(gammas, dtype=np.int32)
     gmax = int(gammas.max()) if gammas.size else 0
@@ -191,7 +201,13 @@ def sampling_workload(name: str, *, config: int, batch: int, vocab: int, gammas,
         temperature = 1.0
         t_rows = temperatures[seq_of_d]
     dvals = stored_f32(draft)
-    token_pool = [gumbel_argmax(rng, dvals, t_rows) for _ in range(max(1, pool))]
+    ks = None if np.ndim(top_k) == 0 else np.asarray(top_k, dtype=np.int32)
+    k_rows = None
+    if ks is not None:
+        k_rows = ks[seq_of_d]
+    elif 0 < int(top_k) < V:
+        k_rows = np.full(rows_d, int(top_k), dtype=np.int32)
+    token_pool = [gumbel_argmax(rng, dvals, t_rows, k_per_row=k_rows) for _ in range(max(1, pool))]
     kv = None
     if kv_range is not None:
         kv = rng.integers(kv_range[0], kv_range[1] + 1, size=batch).astype(np.int32)
@@ -202,6 +218,7 @@ def sampling_workload(name: str, *, config: int, batch: int, vocab: int, gammas,
         temperature=temperature, kv_in=kv, block_size=block_size,
         target_row_off=None if uniform else tro, draft_row_off=None if uniform else dro,
         info={"sigma": sig, "config": config, "dataset": dataset, "profile": profile},
+        top_k=int(top_k) if ks is None else 0, top_ks=ks,
     )
 
 
@@ -220,14 +237,16 @@ def config2(batch=1, gamma=4, vocab=50257, pool=2000, dataset=0) -> Workload:
                              sigma=C2_SIGMA, temps=1.0, pool=pool, dataset=dataset)
 
 
-def config3(batch=64, gamma=8, vocab=128256, pool=4, dataset=0) -> Workload:
-    """Sampling, B=64, gamma=8, V=128256, bf16, Zipf, sigma_b ~ U[0.2,1.5], T=0.8."""
+def config3(batch=64, gamma=8, vocab=128256, pool=4, dataset=0, top_k=0) -> Workload:
+    """Sampling, B=64, gamma=8, V=128256, bf16, Zipf, sigma_b ~ U[0.2,1.5], T=0.8
+    (top_k > 0: the same rows, both models truncated to their top k)."""
     rng = _rng(30, dataset)
     sig = rng.uniform(0.2, 1.5, size=batch).astype(np.float32)
-    return sampling_workload("C3 sample B64 g8 V128256 bf16", config=3, batch=batch, vocab=vocab,
+    name = "C3 sample B64 g8 V128256 bf16" + (f" top-k {top_k}" if top_k else "")
+    return sampling_workload(name, config=3, batch=batch, vocab=vocab,
                              gammas=np.full(batch, gamma), profile="zipf", dtype="bf16",
                              sigma=sig, temps=0.8, kv_range=(512, 4096), block_size=16,
-                             pool=pool, dataset=dataset)
+                             pool=pool, dataset=dataset, top_k=top_k)
 
 
 def config5(batch=512, gamma_max=8, vocab=128256, pool=2, dataset=0) -> Workload:

@@ -62,7 +62,7 @@ def test_struct_layout_matches_header(sv):
 
 
 def test_abi_version_and_status_strings(sv):
-    assert sv.spec_abi_version() == 1
+    assert sv.spec_abi_version() == 2 == sv.SPEC_ABI_VERSION
     assert sv.spec_status_string(0) == "SPEC_OK"
     assert sv.spec_status_string(3) == "SPEC_ERR_WORKSPACE"
 
@@ -120,6 +120,13 @@ def test_host_validation_rejects_before_cuda(sv):
     assert call(_args(sv, workspace=0)) == sv.SPEC_ERR_WORKSPACE
     assert call(_args(sv, tdt=7)) == sv.SPEC_ERR_INVALID_ARG
     assert call(_args(sv, tdt=7), greedy=True) == sv.SPEC_ERR_INVALID_ARG
+    a = _args(sv)
+    a.top_ks = (1 << 20) + 2  # per-sequence k must be int32-aligned
+    assert call(a) == sv.SPEC_ERR_ALIGNMENT
+    # the struct grew with top_k / top_ks: the size of the previous layout is rejected
+    a = _args(sv)
+    a.struct_size = sv.SpecVerifyArgs.top_k.offset
+    assert call(a) == sv.SPEC_ERR_INVALID_ARG
     assert L.spec_kv_rollback(None, None, None, None, 3, 4, 0, None, None, None) == sv.SPEC_ERR_INVALID_ARG
     assert L.spec_debug_philox(0, 0, 0, 0, 1, None, None) == sv.SPEC_ERR_INVALID_ARG
 
