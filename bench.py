@@ -7,7 +7,10 @@ draw and the KV rollback). Inputs are resident in HBM; consecutive steps
 alternate between two resident copies of the 279 MB input (larger than the
 129 MB L2 on its own), so no step reads rows the previous step left in L2.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--top-k K]
+
+--top-k K truncates every target and draft row to its top K (the same rows;
+the step's first kernel is then the top-k threshold pass).
 
 Under torchrun each rank verifies its own batch of 64 sequences (weak
 scaling; no collective on the data path, a barrier and a max-reduce of the
@@ -44,7 +47,31 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=60)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--top-k", type=int, default=0,
+                    help="truncate every target and draft row to its top k (0: plain sampling, the headline)")
     return ap.parse_args()
+
+
+# The dominant kernel of each mode: its name, the sources whose hash keys the
+# committed ncu DRAM summary, and that summary's file.
+KERNELS = {
+    "stats": {"name": "stats_tma_kernel (streaming pass)", "sources": ("stats.cu", "common.cuh", "internal.h"),
+              "profile": "stats_kernel_c3_dram.txt"},
+    "topk": {"name": "topk_kernel (top-k threshold pass)", "sources": ("topk.cu", "common.cuh", "internal.h"),
+             "profile": "topk_kernel_c3_k{k}_dram.txt"},
+}
+
+
+def mode_of(args):
+    return "topk" if args.top_k > 0 else "stats"
+
+
+def metric_of(args):
+    return METRIC if args.top_k <= 0 else METRIC[:-1] + f", top-k {args.top_k})"
+
+
+def workload_of(args):
+    return WORKLOAD if args.top_k <= 0 else WORKLOAD + f", both models truncated to top-k {args.top_k}"
 
 
 def dist_env():
@@ -111,25 +138,25 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def stats_kernel_source_hash() -> str:
+def kernel_source_hash(mode: str = "stats") -> str:
     h = hashlib.sha256()
-    for f in ("stats.cu", "common.cuh", "internal.h"):
+    for f in KERNELS[mode]["sources"]:
         with open(os.path.join(ROOT, "speculative_decoding_verification_38_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def ncu_traffic_per_launch():
-    """DRAM bytes per launch of the streaming kernel from the committed ncu
-    summary, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", "stats_kernel_c3_dram.txt")
+def ncu_traffic_per_launch(mode: str = "stats", top_k: int = 0):
+    """DRAM bytes per launch of the mode's dominant kernel from the committed
+    ncu summary, if it was taken on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", KERNELS[mode]["profile"].format(k=top_k))
     try:
         kv = {}
         for line in open(path):
             if ":" in line and not line.startswith("#"):
                 k, v = line.split(":", 1)
                 kv[k.strip()] = v.strip()
-        if kv.get("source_hash") != stats_kernel_source_hash():
+        if kv.get("source_hash") != kernel_source_hash(mode):
             return None
         return int(kv["dram_bytes_per_launch"])
     except (OSError, KeyError, ValueError):
@@ -166,7 +193,8 @@ def run_ours(args):
 
     from speculative_decoding_verification_38_gb300.sharding import seq_offset
 
-    w = wl.config3()
+    mode = mode_of(args)
+    w = wl.config3(top_k=args.top_k)
     B = w.batch
     seq_off = seq_offset(rank, B)  # weak scaling: each rank verifies its own batch
     copies = [DeviceBatch(w, seed=0, seq_offset=seq_off) for _ in range(2)]
@@ -239,25 +267,26 @@ def run_ours(args):
     kern_ms = statistics.mean(stats_ms)
     peak, peak_kind = measured_hbm_peak()
     achieved = (algo_bytes + small_io) / (kern_ms / 1e3) / 1e9
-    traffic = ncu_traffic_per_launch()
+    traffic = ncu_traffic_per_launch(mode, args.top_k)
 
     # end to end through the public API with host buffers
     e2e = run_e2e(copies[0], w, args, sv) if args.e2e_steps > 0 else None
 
     out = {
-        "metric": METRIC, "value": rounds_per_s, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
+        "metric": metric_of(args), "value": rounds_per_s, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded Zipf logits; no dataset)",
-        "config": {"workload": WORKLOAD, "batch": B, "gamma": w.gamma_max, "vocab": w.vocab,
-                   "logits_dtype": "bf16", "parallelism": f"replicas x{world} (sequence shards)",
+        "config": {"workload": workload_of(args), "batch": B, "gamma": w.gamma_max, "vocab": w.vocab,
+                   "top_k": args.top_k, "logits_dtype": "bf16",
+                   "parallelism": f"replicas x{world} (sequence shards)",
                    "l2": "inputs larger than L2: 279 MB per step, alternating 2 resident copies"},
         "vocab_rows_per_s": rounds_per_s * w.vocab_rows(),
         "sequence_rounds_per_s": rounds_per_s * B,
         "step_hbm_gbs": rounds_per_s / world * algo_bytes / 1e9,
-        "gpu_launches": 2 * K,
+        "gpu_launches": 4 * K,  # per step: row pass, finalize, sampler tile pass, draw
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "stats_tma_kernel (streaming pass)", "kernel_ms": kern_ms,
+                     "kernel": KERNELS[mode]["name"], "kernel_ms": kern_ms,
                      "kernel_ms_samples": len(stats_ms),
                      "algorithmic_bytes_per_launch": algo_bytes + small_io,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -329,7 +358,8 @@ def _oracle_subset(w, nseq):
     sub = wl.Workload(name=w.name, batch=nseq, vocab=w.vocab, gamma_max=g, gammas=w.gammas[:nseq],
                       target=w.target[:nseq * (g + 1)], draft=w.draft[:nseq * g],
                       draft_tokens=w.draft_tokens[:nseq * g], temperature=w.temperature,
-                      kv_in=None if w.kv_in is None else w.kv_in[:nseq], block_size=w.block_size)
+                      kv_in=None if w.kv_in is None else w.kv_in[:nseq], block_size=w.block_size,
+                      top_k=w.top_k)
     return sub
 
 
@@ -357,7 +387,7 @@ def run_reference(args):
     from speculative_decoding_verification_38_gb300 import workloads as wl
 
     oracle.build()
-    w = wl.config3()
+    w = wl.config3(top_k=args.top_k)
     cores = os.cpu_count() or 1
     W, K = max(3, args.warmup), max(1, args.steps)
     # size each step so the whole run stays within ~3 minutes
@@ -373,11 +403,11 @@ def run_reference(args):
         oracle.verify_sample(sub, seed=0, rnd=W + i, nthreads=cores)
     el = time.time() - t0
     value = (K * per_step / w.batch) / el
-    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+    out = {"impl": "reference", "metric": metric_of(args), "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
            "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Zipf logits; no dataset)",
-           "config": {"workload": WORKLOAD, "batch": w.batch, "gamma": w.gamma_max, "vocab": w.vocab,
-                      "logits_dtype": "bf16", "parallelism": "host cores"},
+           "config": {"workload": workload_of(args), "batch": w.batch, "gamma": w.gamma_max, "vocab": w.vocab,
+                      "top_k": args.top_k, "logits_dtype": "bf16", "parallelism": "host cores"},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                             "sample": f"each step verifies {per_step} of the 64 sequences of one round "
                                       f"(counted as {per_step}/64 round), float64 C oracle"},

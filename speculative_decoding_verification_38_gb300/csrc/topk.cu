@@ -10,18 +10,21 @@
 // s = sum over kept columns of 2^(l k - fl(m k)), k = log2(e) / T;
 // probabilities rows (0, sum of the kept values).
 //
-// One CTA per row and one read of the row from HBM. Each warp filters its
-// share of the row against a threshold that only rises: it keeps in a
-// shared-memory buffer every value at least as large as its threshold, and
-// when the buffer fills it selects the k-th largest of its entries (radix
-// select on order-preserving keys), makes that the threshold and drops what
-// lies below. A warp therefore always holds at least k of its own values at
-// or above its threshold, so its threshold never passes the row's tau and the
-// buffers together hold every kept column. The CTA then selects tau over the
-// union of the buffers and sums the kept entries' weights in a fixed order
-// (the result does not depend on timing). Rows where that cannot work (k past
-// half a buffer, more equal values than a buffer holds, k off) select over
-// the row itself in L2, one read per radix digit, and sum it in one more read.
+// One CTA per row (four resident per SM) and one read of the row from HBM.
+// Each warp filters its share of the row against a threshold that only
+// rises and keeps, in a shared-memory buffer, every value at least that
+// large. The threshold starts, after the first batch of loads, at the k-th
+// largest of the maxima of every 16-byte vector the CTA loaded (k distinct
+// vectors each hold a value at least that large, so it cannot pass tau),
+// found by a CTA bisection on order-preserving keys. When a warp's buffer
+// fills, the warp raises its threshold to the k-th largest of its entries,
+// drops what lies below and shares the new bound with the other warps. Every
+// threshold is a proven lower bound of tau, so the buffers together hold
+// every kept column; the CTA then bisects for tau over the buffers and sums
+// the kept entries' weights in a fixed order (the result does not depend on
+// timing). Rows where that cannot work (k past half a buffer, more equal
+// values than a buffer holds, k off) select over the row itself in L2, one
+// read per radix digit, and sum it in one more read.
 #include <math.h>
 
 #include "common.cuh"
@@ -31,7 +34,7 @@ namespace specv {
 
 namespace {
 
-constexpr int kTkThreads = 512;
+constexpr int kTkThreads = 256;
 constexpr int kTkWarps = kTkThreads / 32;
 constexpr int kTkUnroll = 8;        // 16-byte loads in flight per lane
 constexpr int kBufBytes = 4096;     // candidate buffer per warp
@@ -39,13 +42,15 @@ constexpr unsigned kFull = 0xffffffffu;
 
 struct TkSmem {
     uint32_t buf[kTkWarps][kBufBytes / 4];  // candidate value bits (u16 for bf16, u32 for f32)
-    uint32_t hist[kTkWarps][256];           // per-warp radix histograms; [0] is the CTA's after the pass
+    uint32_t hist[256];                     // the CTA's radix histogram
+    uint32_t thr_key;                       // largest threshold key any warp has proven (a lower bound of tau's)
     int32_t cnt[kTkWarps];
     int32_t ovf[kTkWarps];
     float mx[kTkWarps];
     int32_t nan[kTkWarps];
     float red[kTkWarps];
     uint32_t sel_bin, sel_above;
+    uint32_t bis[2][3][kTkWarps];  // block bisection: per-warp counts, double-buffered
 };
 constexpr size_t kTkSmemBytes = sizeof(TkSmem);
 
@@ -133,29 +138,19 @@ __device__ __forceinline__ uint32_t warp_find_bin(const uint32_t* h, uint32_t re
     return __shfl_sync(kFull, bin, src);
 }
 
-// The kk-th largest key among a warp's buffer entries (1 <= kk <= cnt), by
-// most-significant-digit radix select with the warp's own histogram.
+// The kk-th largest key among a warp's buffer entries (1 <= kk <= cnt): the
+// largest K with #{key >= K} >= kk, found bit by bit from the top.
 template <int DT>
-__device__ uint32_t warp_select(const typename KeyTraits<DT>::Bits* wb, int cnt, uint32_t kk, uint32_t* hist) {
+__device__ uint32_t warp_kth_buf(const typename KeyTraits<DT>::Bits* wb, int cnt, uint32_t kk) {
     using KT = KeyTraits<DT>;
     const int lane = threadIdx.x & 31;
-    uint32_t prefix = 0, remaining = kk;
+    uint32_t prefix = 0;
 #pragma unroll 1
-    for (int d = KT::kDigits - 1; d >= 0; --d) {
-        const int sh = 8 * d;
-        for (int i = lane; i < 256; i += 32) hist[i] = 0;
-        __syncwarp();
-        for (int e = lane; e < cnt; e += 32) {
-            const uint32_t key = KT::key(wb[e]);
-            if (d == KT::kDigits - 1 || (key >> (sh + 8)) == (prefix >> (sh + 8)))
-                atomicAdd(&hist[(key >> sh) & 255u], 1u);
-        }
-        __syncwarp();
-        uint32_t above;
-        const uint32_t bin = warp_find_bin(hist, remaining, above);
-        __syncwarp();
-        prefix |= bin << sh;
-        remaining -= above;
+    for (int b = 8 * KT::kDigits - 1; b >= 0; --b) {
+        const uint32_t cand = prefix | (1u << b);
+        uint32_t c = 0;
+        for (int e = lane; e < cnt; e += 32) c += KT::key(wb[e]) >= cand ? 1u : 0u;
+        if (__reduce_add_sync(kFull, c) >= kk) prefix = cand;
     }
     return prefix;
 }
@@ -204,44 +199,115 @@ __device__ __forceinline__ float vec_max(const uint4& q) {
 }
 
 // Append this lane's values of one vector that are >= thr (when `need`) to
-// the warp's buffer, slot by slot, lanes in order within a slot.
+// the warp's buffer: lanes in order, each lane's values in column order.
 template <int DT>
 __device__ __forceinline__ void warp_append(typename KeyTraits<DT>::Bits* wb, int& cnt, const uint4& q, bool need,
                                             float thr) {
     using KT = KeyTraits<DT>;
     constexpr int EPV = 16 / KT::kEsz;
+    const int lane = threadIdx.x & 31;
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-    const uint32_t lt = lanemask_lt();
+    uint32_t bits[EPV];
+    bool c[EPV];
+    int n = 0;
 #pragma unroll
     for (int e = 0; e < EPV; ++e) {
-        const uint32_t bits = DT == SPECV_BF16 ? ((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu)) : w[e];
-        const bool c = need && KT::value(bits) >= thr;
-        const uint32_t bal = __ballot_sync(kFull, c);
-        if (c) wb[cnt + __popc(bal & lt)] = (typename KT::Bits)KT::canon(bits);
-        cnt += __popc(bal);
+        bits[e] = DT == SPECV_BF16 ? ((e & 1) ? (w[e >> 1] >> 16) : (w[e >> 1] & 0xFFFFu)) : w[e];
+        c[e] = need && KT::value(bits[e]) >= thr;
+        n += c[e] ? 1 : 0;
+    }
+    int incl = n;  // inclusive scan of the counts over the lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += t;
+    }
+    int pos = cnt + incl - n;
+#pragma unroll
+    for (int e = 0; e < EPV; ++e)
+        if (c[e]) wb[pos++] = (typename KT::Bits)KT::canon(bits[e]);
+    cnt += __shfl_sync(kFull, incl, 31);
+}
+
+// Threshold state of one warp: a key every value it must keep reaches, and
+// the value of that key (-inf while no key is known).
+struct WarpThr {
+    uint32_t key;
+    float val;
+};
+
+template <int DT>
+__device__ __forceinline__ void raise_thr(WarpThr& t, uint32_t k) {
+    using KT = KeyTraits<DT>;
+    if (k > t.key) {
+        t.key = k;
+        t.val = KT::value(KT::bits_of_key(k));
     }
 }
 
-// Raise the warp's threshold to the kk-th largest of its buffer and drop the
-// entries below it. Returns false when the survivors (ties) leave less than
-// `room` free entries.
+// Make room in a full buffer: drop the entries below the warp's threshold
+// (another warp may have raised it); if that is not enough, raise the
+// threshold to the kk-th largest entry and drop again. Returns false when
+// the survivors (ties) still leave fewer than `room` free entries.
 template <int DT>
-__device__ __forceinline__ bool warp_make_room(typename KeyTraits<DT>::Bits* wb, int& cnt, uint32_t kk, float& thr,
-                                               uint32_t* hist, int room) {
-    using KT = KeyTraits<DT>;
-    constexpr int C = kBufBytes / KT::kEsz;
-    const uint32_t K = warp_select<DT>(wb, cnt, kk, hist);
-    cnt = warp_compact<DT>(wb, cnt, K);
-    thr = KT::value(KT::bits_of_key(K));
+__device__ bool warp_make_room(typename KeyTraits<DT>::Bits* wb, int& cnt, uint32_t kk, WarpThr& thr,
+                               uint32_t* shared_key, int room) {
+    constexpr int C = kBufBytes / KeyTraits<DT>::kEsz;
+    cnt = warp_compact<DT>(wb, cnt, thr.key);
+    if (cnt <= C - room) return true;
+    const uint32_t K = warp_kth_buf<DT>(wb, cnt, kk);  // cnt > C - room >= kk
+    raise_thr<DT>(thr, K);
+    if ((threadIdx.x & 31) == 0) atomicMax(shared_key, K);
+    cnt = warp_compact<DT>(wb, cnt, thr.key);
     return cnt <= C - room;
+}
+
+// The kk-th largest key over the keys every thread counts (the largest K
+// with #{key >= K} >= kk; 0 if there are fewer than kk), two bits per
+// round: count(c1, c2, c3, n1, n2, n3) gives this thread's numbers of keys
+// at least c1 < c2 < c3. One barrier per round (the per-warp totals are
+// double-buffered). Every thread of the CTA calls it and gets the result.
+template <int BITS, class Count>
+__device__ uint32_t block_kth(uint32_t kk, TkSmem& sm, const Count& count) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint32_t prefix = 0;
+#pragma unroll 1
+    for (int b = BITS - 2; b >= 0; b -= 2) {
+        const uint32_t c1 = prefix | (1u << b), c2 = prefix | (2u << b), c3 = prefix | (3u << b);
+        uint32_t n1 = 0, n2 = 0, n3 = 0;
+        count(c1, c2, c3, n1, n2, n3);
+        n1 = __reduce_add_sync(kFull, n1);
+        n2 = __reduce_add_sync(kFull, n2);
+        n3 = __reduce_add_sync(kFull, n3);
+        const int par = (b >> 1) & 1;
+        if (lane == 0) {
+            sm.bis[par][0][warp] = n1;
+            sm.bis[par][1][warp] = n2;
+            sm.bis[par][2][warp] = n3;
+        }
+        __syncthreads();
+        uint32_t t1 = 0, t2 = 0, t3 = 0;
+#pragma unroll
+        for (int w = 0; w < kTkWarps; ++w) {
+            t1 += sm.bis[par][0][w];
+            t2 += sm.bis[par][1][w];
+            t3 += sm.bis[par][2][w];
+        }
+        prefix = t3 >= kk ? c3 : (t2 >= kk ? c2 : (t1 >= kk ? c1 : prefix));
+    }
+    return prefix;
 }
 
 // One warp's share of the row: vectors it + u * kTkThreads + warp * 32 + lane
 // (u < kTkUnroll) of every iteration, plus, for warp 0, the columns before
 // the first 16-byte boundary and after the last full vector. With `filt`,
-// the warp's buffer ends holding every value of its share that is at least
-// its final threshold (in the order met); the warp's maximum, NaN flag,
-// entry count and overflow flag go to shared memory.
+// the warp keeps in its buffer (in the order met) every value of its share
+// at least as large as its threshold. The threshold starts at the kk-th
+// largest of the maxima of every vector the CTA's first iteration loaded
+// (kk vectors each hold a value at least that large, so it cannot pass tau)
+// and rises with every select any warp makes (shared through sm.thr_key).
+// The warp's maximum, NaN flag, entry count and overflow flag go to shared
+// memory.
 template <int DT>
 __device__ void filter_pass(const char* row, int64_t V, uint32_t kk, bool filt, TkSmem& sm) {
     using KT = KeyTraits<DT>;
@@ -249,15 +315,37 @@ __device__ void filter_pass(const char* row, int64_t V, uint32_t kk, bool filt, 
     constexpr int ESZ = KT::kEsz, EPV = 16 / ESZ, C = kBufBytes / ESZ, STEP = 32 * EPV;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Bits* wb = reinterpret_cast<Bits*>(sm.buf[warp]);
-    uint32_t* hist = sm.hist[warp];
+    volatile uint32_t* shared_key = &sm.thr_key;
     int64_t head = (int64_t)(((16u - (uint32_t)((uintptr_t)row & 15u)) & 15u) / ESZ);
     if (head > V) head = V;
     const int64_t nvec = (V - head) / EPV;
     const int64_t tail0 = head + nvec * EPV;
     const uint4* vrow = reinterpret_cast<const uint4*>(row + head * ESZ);
-    float thr = -INFINITY, lmax = -INFINITY;
+    WarpThr thr{0u, -INFINITY};
+    float lmax = -INFINITY;
     int cnt = 0;
     bool nan = false, ovf = false;
+
+    if (filt && nvec > 0) {  // the first threshold (the whole CTA; its loads come back from L2 in the loop)
+        float mx[kTkUnroll];
+#pragma unroll
+        for (int u = 0; u < kTkUnroll; ++u) {
+            const int64_t vi = warp * 32 + lane + (int64_t)u * kTkThreads;
+            mx[u] = vi < nvec ? vec_max<DT>(ld_stream_v4(vrow + vi)) : -INFINITY;
+        }
+        const uint32_t K0 = block_kth<8 * KT::kDigits>(
+            kk, sm, [&](uint32_t c1, uint32_t c2, uint32_t c3, uint32_t& n1, uint32_t& n2, uint32_t& n3) {
+#pragma unroll
+                for (int u = 0; u < kTkUnroll; ++u) {
+                    const uint32_t key = key_of_value<DT>(mx[u]);
+                    n1 += key >= c1 ? 1u : 0u;
+                    n2 += key >= c2 ? 1u : 0u;
+                    n3 += key >= c3 ? 1u : 0u;
+                }
+            });
+        raise_thr<DT>(thr, K0);
+        if (threadIdx.x == 0 && K0) atomicMax(&sm.thr_key, K0);
+    }
 
     for (int64_t it = 0; it < nvec; it += (int64_t)kTkUnroll * kTkThreads) {
         const int64_t v0 = it + warp * 32 + lane;
@@ -277,20 +365,22 @@ __device__ void filter_pass(const char* row, int64_t V, uint32_t kk, bool filt, 
             lmax = fmaxf(lmax, mx[u]);
         }
         if (!filt) continue;
+        raise_thr<DT>(thr, *shared_key);
 #pragma unroll
         for (int u = 0; u < kTkUnroll; ++u) {
             const bool valid = v0 + (int64_t)u * kTkThreads < nvec;
-            bool need = valid && mx[u] >= thr;
+            bool need = valid && mx[u] >= thr.val;
             if (!__any_sync(kFull, need)) continue;
             if (cnt > C - STEP) {
-                if (!warp_make_room<DT>(wb, cnt, kk, thr, hist, STEP)) {
+                raise_thr<DT>(thr, *shared_key);
+                if (!warp_make_room<DT>(wb, cnt, kk, thr, &sm.thr_key, STEP)) {
                     filt = false;
                     ovf = true;
                     break;
                 }
-                need = valid && mx[u] >= thr;
+                need = valid && mx[u] >= thr.val;
             }
-            warp_append<DT>(wb, cnt, q[u], need, thr);
+            warp_append<DT>(wb, cnt, q[u], need, thr.val);
         }
     }
     if (warp == 0) {  // the ragged ends: at most EPV - 1 columns each
@@ -303,12 +393,12 @@ __device__ void filter_pass(const char* row, int64_t V, uint32_t kk, bool filt, 
         nan |= v != v;
         lmax = fmaxf(lmax, v);
         if (filt) {
-            bool need = col >= 0 && v >= thr;
+            bool need = col >= 0 && v >= thr.val;
             if (__any_sync(kFull, need)) {
                 bool ok = true;
                 if (cnt > C - 32) {
-                    ok = warp_make_room<DT>(wb, cnt, kk, thr, hist, 32);
-                    need = col >= 0 && v >= thr;
+                    ok = warp_make_room<DT>(wb, cnt, kk, thr, &sm.thr_key, 32);
+                    need = col >= 0 && v >= thr.val;
                 }
                 if (ok) {
                     const uint32_t bits = DT == SPECV_BF16 ? (__float_as_uint(v) >> 16) : __float_as_uint(v);
@@ -340,7 +430,7 @@ template <int DT, class Each>
 __device__ uint32_t block_select(uint32_t kk, TkSmem& sm, const Each& each) {
     using KT = KeyTraits<DT>;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint32_t* h = sm.hist[0];
+    uint32_t* h = sm.hist;
     uint32_t prefix = 0, remaining = kk;
 #pragma unroll 1
     for (int d = KT::kDigits - 1; d >= 0; --d) {
@@ -396,6 +486,8 @@ __device__ void row_topk(const StatsParams& p, int64_t r, const char* row, int64
     const int64_t V = p.V;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool filt = !off && kk <= C / 2;
+    if (threadIdx.x == 0) sm.thr_key = 0u;
+    __syncthreads();
     filter_pass<DT>(row, V, (uint32_t)kk, filt, sm);
     __syncthreads();
     float m = -INFINITY;
@@ -412,9 +504,15 @@ __device__ void row_topk(const StatsParams& p, int64_t r, const char* row, int64
         // tau over the union of the buffers, then the kept entries' weights
         const Bits* wb = reinterpret_cast<const Bits*>(sm.buf[warp]);
         const int cnt = sm.cnt[warp];
-        const uint32_t K = block_select<DT>((uint32_t)kk, sm, [&](auto&& f) {
-            for (int e = lane; e < cnt; e += 32) f(KT::key(wb[e]));
-        });
+        const uint32_t K = block_kth<8 * KT::kDigits>(
+            (uint32_t)kk, sm, [&](uint32_t c1, uint32_t c2, uint32_t c3, uint32_t& n1, uint32_t& n2, uint32_t& n3) {
+                for (int e = lane; e < cnt; e += 32) {
+                    const uint32_t key = KT::key(wb[e]);
+                    n1 += key >= c1 ? 1u : 0u;
+                    n2 += key >= c2 ? 1u : 0u;
+                    n3 += key >= c3 ? 1u : 0u;
+                }
+            });
         tau = KT::value(KT::bits_of_key(K));
         for (int e = lane; e < cnt; e += 32) {
             const float v = KT::value(wb[e]);
@@ -462,7 +560,7 @@ __device__ int32_t row_seq(const StatsParams& p, bool draft, int64_t lr) {
     return lo;
 }
 
-__global__ void __launch_bounds__(kTkThreads, 2) topk_kernel(StatsParams p) {
+__global__ void __launch_bounds__(kTkThreads, 4) topk_kernel(StatsParams p) {
     extern __shared__ __align__(16) unsigned char tk_raw[];
     TkSmem& sm = *reinterpret_cast<TkSmem*>(tk_raw);
     pdl_launch_dependents();
