@@ -45,7 +45,7 @@ def build(force: bool = False) -> str:
     if not force and os.path.exists(_LIB_PATH) and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-D_GNU_SOURCE", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm", "-lpthread"]
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-D_GNU_SOURCE", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm", "-lpthread"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, _LIB_PATH)
     return _LIB_PATH
@@ -96,6 +96,14 @@ def lib():
             L.orc_softmax_row_topk.argtypes = [vp, i32, i64, dbl, dbl, vp]
             L.orc_normalize_row_topk.restype = i32
             L.orc_normalize_row_topk.argtypes = [vp, i32, i64, dbl, vp]
+            L.orc_acceptance_ema.restype = None
+            L.orc_acceptance_ema.argtypes = [vp, vp, i32, i64, vp, ctypes.c_float, vp, vp]
+            L.orc_speedups.restype = None
+            L.orc_speedups.argtypes = [dbl, i32, dbl, vp]
+            L.orc_best_gamma.restype = i32
+            L.orc_best_gamma.argtypes = [ctypes.c_float, i32, ctypes.c_float]
+            L.orc_adapt_gamma.restype = i64
+            L.orc_adapt_gamma.argtypes = [vp, i64, i32, ctypes.c_float, i64, vp]
             L.orc_residual.restype = dbl
             L.orc_residual.argtypes = [vp, vp, i64, vp]
             L.orc_inverse_cdf.restype = i64
@@ -185,6 +193,38 @@ def normalize_row_topk(row: np.ndarray, tau: float):
     q = np.zeros(row.shape[0], dtype=np.float64)
     st = lib().orc_normalize_row_topk(row.ctypes.data, _dtype_code(row), row.shape[0], float(tau), q.ctypes.data)
     return st, q
+
+
+def acceptance_ema(accepted, gammas, gamma_max, ema, lam, status=None):
+    """One round's update of the running acceptance (float32 state)."""
+    acc = np.ascontiguousarray(accepted, dtype=np.int32)
+    g = None if gammas is None else np.ascontiguousarray(gammas, dtype=np.int32)
+    st = None if status is None else np.ascontiguousarray(status, dtype=np.int32)
+    e_in = np.ascontiguousarray(ema, dtype=np.float32)
+    e_out = np.empty_like(e_in)
+    lib().orc_acceptance_ema(acc.ctypes.data, _ptr(g), int(gamma_max), acc.shape[0], _ptr(st), float(lam),
+                             e_in.ctypes.data, e_out.ctypes.data)
+    return e_out
+
+
+def speedups(alpha: float, gamma_max: int, c: float) -> np.ndarray:
+    """E(alpha, g) / (1 + g c) for g = 0..gamma_max (float64)."""
+    sp = np.zeros(int(gamma_max) + 1, dtype=np.float64)
+    lib().orc_speedups(float(alpha), int(gamma_max), float(c), sp.ctypes.data)
+    return sp
+
+
+def best_gamma(ema: float, gamma_max: int, c: float) -> int:
+    return int(lib().orc_best_gamma(float(ema), int(gamma_max), float(c)))
+
+
+def adapt_gamma(ema, gamma_max: int, c: float, max_positions: int = 0):
+    """(gammas int32 [B], total verify positions) for the next round."""
+    e = np.ascontiguousarray(ema, dtype=np.float32)
+    out = np.zeros(e.shape[0], dtype=np.int32)
+    tot = lib().orc_adapt_gamma(e.ctypes.data, e.shape[0], int(gamma_max), float(c), int(max_positions),
+                                out.ctypes.data)
+    return out, int(tot)
 
 
 def residual(p: np.ndarray, q: np.ndarray):

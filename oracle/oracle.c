@@ -604,3 +604,80 @@ int32_t orc_position_rows(const orc_args_t* a, int64_t b, int64_t i, double* p, 
         for (int64_t j = 0; j < V; ++j) w[j] = p[j];
     return ORC_SEQ_OK;
 }
+
+/* ------------------------------------------------------------ adaptive gamma
+ * Under continuous batching gamma is chosen per request from its running
+ * acceptance, and speculation is switched off once the batch is large enough
+ * to be compute-bound ("Speculative decoding" (mhtirogla.ai), Implementation
+ * notes and Efficiency, adaptive gamma). The pages give the cost model
+ * (expected tokens per pass E = (1 - a^(g+1)) / (1 - a), wall-clock speedup
+ * E / (1 + g c); "Speculative decoding" (inference.tusharamrit.in), the
+ * actual speedup and its worked cases) but no estimator and no switch rule;
+ * the readings:
+ *   - a round of sequence b performed t_b accept tests (a_b + 1 when a draft
+ *     was rejected, else gamma_b) of which a_b passed; its running acceptance
+ *     is an exponential moving average of a_b / t_b over its rounds, state in
+ *     float32: ema += lambda * (a_b / t_b - ema), in that order, each
+ *     operation rounded to float32. Rounds with t_b = 0 (gamma_b = 0) or a
+ *     sequence status other than OK leave it unchanged;
+ *   - gamma_b for the next round is the smallest g in [0, gamma_max] with the
+ *     largest E(a, g) / (1 + g c), a = the running acceptance clamped to
+ *     [0, 1] (NaN read as 0), evaluated in float64 with the power taken by
+ *     repeated multiplication and E = g + 1 at a = 1 (the limit);
+ *   - if max_positions > 0 and the verify positions sum_b (gamma_b + 1)
+ *     exceed it, every gamma_b is 0 (speculation off for the batch). */
+void orc_acceptance_ema(const int32_t* accepted, const int32_t* gammas, int32_t gamma_max, int64_t B,
+                        const int32_t* status, float lambda, const float* ema_in, float* ema_out) {
+    for (int64_t b = 0; b < B; ++b) {
+        const int32_t g = gammas ? gammas[b] : gamma_max;
+        const int32_t a = accepted[b];
+        float e = ema_in[b];
+        if ((!status || status[b] == 0) && g > 0 && a >= 0 && a <= g) {
+            const int32_t t = a < g ? a + 1 : g;
+            const float x = (float)a / (float)t;
+            const float d = x - e;
+            const float s = lambda * d;
+            e = e + s;
+        }
+        ema_out[b] = e;
+    }
+}
+
+/* E(a, g) / (1 + g c) for g = 0..gamma_max into sp[]. */
+void orc_speedups(double a, int32_t gamma_max, double c, double* sp) {
+    if (!(a >= 0.0)) a = 0.0; /* NaN and negatives */
+    if (a > 1.0) a = 1.0;
+    double pw = a; /* a^(g+1) */
+    for (int32_t g = 0; g <= gamma_max; ++g) {
+        const double E = (a == 1.0) ? (double)(g + 1) : (1.0 - pw) / (1.0 - a);
+        const double den = 1.0 + (double)g * c;
+        sp[g] = E / den;
+        pw = pw * a;
+    }
+}
+
+int32_t orc_best_gamma(float ema, int32_t gamma_max, float c) {
+    double sp[65];
+    if (gamma_max > 64) gamma_max = 64;
+    if (gamma_max < 0) gamma_max = 0;
+    orc_speedups((double)ema, gamma_max, (double)c, sp);
+    int32_t best = 0;
+    for (int32_t g = 1; g <= gamma_max; ++g)
+        if (sp[g] > sp[best]) best = g;
+    return best;
+}
+
+/* Returns sum_b (gamma_b + 1) of the gammas written. */
+int64_t orc_adapt_gamma(const float* ema, int64_t B, int32_t gamma_max, float c, int64_t max_positions,
+                        int32_t* gammas_out) {
+    int64_t total = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        gammas_out[b] = orc_best_gamma(ema[b], gamma_max, c);
+        total += gammas_out[b] + 1;
+    }
+    if (max_positions > 0 && total > max_positions) {
+        for (int64_t b = 0; b < B; ++b) gammas_out[b] = 0;
+        total = B;
+    }
+    return total;
+}
