@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--top-k", type=int, default=0,
                     help="truncate every target and draft row to its top k (0: plain sampling, the headline)")
+    ap.add_argument("--adaptive", action="store_true",
+                    help="each step also updates the running acceptance and chooses the next gamma on the GPU")
     return ap.parse_args()
 
 
@@ -198,6 +200,11 @@ def run_ours(args):
     B = w.batch
     seq_off = seq_offset(rank, B)  # weak scaling: each rank verifies its own batch
     copies = [DeviceBatch(w, seed=0, seq_offset=seq_off) for _ in range(2)]
+    gammas_next = None
+    if args.adaptive:  # running acceptance per request, updated by every verify call
+        for db in copies:
+            db.args.set_accept_ema(torch.full((B,), 0.8, dtype=torch.float32, device="cuda"), 0.1)
+        gammas_next = torch.zeros(B, dtype=torch.int32, device="cuda")
     algo_bytes = w.input_bytes()  # every logits row read once
     small_io = (w.rows_draft * 4 + B * 4 * 3 + w.rows_target * 4)  # tokens, kv in/out, accepted, out tokens
     torch.cuda.synchronize()
@@ -207,6 +214,9 @@ def run_ours(args):
         st = db.call(rnd=rnd, pool_index=rnd)
         if st != 0:
             raise sv.SpecError(st, "spec_verify_sample")
+        if gammas_next is not None:  # the next round's gamma per request (the synthetic drafter keeps gamma = 8)
+            sv.check(sv.spec_adapt_gamma(db.args.tensors["accept_ema"], w.gamma_max, 0.05, gammas_next),
+                     "spec_adapt_gamma")
 
     W, K = max(3, args.warmup), max(1, args.steps)
     for i in range(W):
@@ -283,7 +293,7 @@ def run_ours(args):
         "vocab_rows_per_s": rounds_per_s * w.vocab_rows(),
         "sequence_rounds_per_s": rounds_per_s * B,
         "step_hbm_gbs": rounds_per_s / world * algo_bytes / 1e9,
-        "gpu_launches": 4 * K,  # per step: row pass, finalize, sampler tile pass, draw
+        "gpu_launches": (5 if args.adaptive else 4) * K,  # row pass, finalize, sampler tile pass, draw (+ gamma policy)
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": KERNELS[mode]["name"], "kernel_ms": kern_ms,
@@ -295,12 +305,37 @@ def run_ours(args):
         "e2e": e2e,
         "wall_s_timed": wall1 - wall0,
     }
+    if args.adaptive:
+        out["adaptive_gamma"] = time_policy(sv, w.gamma_max)
+        out["config"]["adaptive"] = "running acceptance (lambda 0.1) updated in finalize; gamma policy (c = 0.05) each step"
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         out["cpu_baseline"] = run_cpu_baseline(w, args)
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def time_policy(sv, gamma_max):
+    """spec_adapt_gamma alone, CUDA-event timed over 500 calls per batch size."""
+    import torch
+
+    res = {}
+    for B in (64, 4096, 65536):
+        ema = torch.rand(B, device="cuda", dtype=torch.float32)
+        g = torch.zeros(B, dtype=torch.int32, device="cuda")
+        for _ in range(10):
+            sv.check(sv.spec_adapt_gamma(ema, gamma_max, 0.05, g), "spec_adapt_gamma")
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        for _ in range(500):
+            sv.spec_adapt_gamma(ema, gamma_max, 0.05, g)
+        b.record()
+        torch.cuda.synchronize()
+        res[f"policy_us_B{B}"] = a.elapsed_time(b) * 1000 / 500
+    res["bound"] = "latency: up to 65 dependent float32 speedups per request (one CTA up to 1024 requests)"
+    return res
 
 
 def run_e2e(db, w, args, sv):

@@ -48,7 +48,7 @@ extern "C" {
 /* Same type as cudaStream_t; declared here so plain C callers need no CUDA header. */
 typedef struct CUstream_st* spec_stream_t;
 
-#define SPEC_ABI_VERSION 2
+#define SPEC_ABI_VERSION 3
 
 typedef enum {
     SPEC_OK = 0,
@@ -160,6 +160,18 @@ typedef struct {
      * Zero-initialise both for plain sampling. */
     int32_t top_k;
     const int32_t* top_ks; /* device [B] or NULL */
+
+    /* Running acceptance per request, for adaptive gamma ("Speculative
+     * decoding" (mhtirogla.ai), Implementation notes: gamma from running
+     * acceptance). When accept_ema != NULL, every sequence with status OK and
+     * gamma_b > 0 updates accept_ema[b] (float32, in place) by
+     *   x = a_b / t_b,  accept_ema[b] += ema_lambda * (x - accept_ema[b]),
+     * each operation rounded to float32 in that order, where a_b is the
+     * accepted count and t_b = a_b + 1 if a draft was rejected, else gamma_b
+     * (the accept tests the round performed). Other sequences keep their
+     * value. Both verify calls update it. Zero-initialise both to skip it. */
+    float* accept_ema; /* device [B] or NULL */
+    float ema_lambda;
 } spec_verify_args_t;
 
 /* ABI version of the loaded library (SPEC_ABI_VERSION at build time). */
@@ -219,6 +231,28 @@ SPEC_API spec_status_t spec_verify_greedy(const spec_verify_args_t* args, spec_s
  *   - There is one scratch per device: calls that overlap on the GPU (other
  *     streams, other host threads) race on it. Serialise them. */
 SPEC_API spec_status_t spec_verify_sample_static(const spec_verify_args_t* args, spec_stream_t stream);
+
+/* Adaptive gamma for the next round ("Speculative decoding" (mhtirogla.ai),
+ * Implementation notes and Efficiency: gamma adaptive per request from
+ * running acceptance, speculation off once the batch is compute-bound;
+ * "Speculative decoding" (inference.tusharamrit.in), actual speedup
+ * E / (1 + gamma c)). For each request b, with a = accept_ema[b] clamped to
+ * [0, 1] (NaN read as 0), gammas_out[b] = the smallest g in [0, gamma_max]
+ * with the largest E(a, g) / (1 + g c), E(a, g) = 1 + a + ... + a^g (the
+ * pages' (1 - a^(g+1)) / (1 - a), summed term by term), c = draft_cost,
+ * evaluated in float32 with correctly rounded operations in a fixed order
+ * (the powers by repeated multiplication), so the result does not depend on
+ * the device. If max_positions > 0 and the verify positions
+ * P = sum_b (gammas_out[b] + 1) exceed it, every gammas_out[b] is 0.
+ * total_positions_out (device int64, may be NULL) receives P, the positions
+ * of the chosen gammas before that switch. accept_ema and gammas_out are
+ * device [batch]; 1 <= batch <= 65536, 0 <= gamma_max <= 64, draft_cost >= 0
+ * and finite. A batch above 1024 with max_positions > 0 needs
+ * total_positions_out (the switch reads the sum from it); otherwise
+ * SPEC_ERR_INVALID_ARG. */
+SPEC_API spec_status_t spec_adapt_gamma(const float* accept_ema, int32_t batch, int32_t gamma_max, float draft_cost,
+                                        int64_t max_positions, int32_t* gammas_out, int64_t* total_positions_out,
+                                        spec_stream_t stream);
 
 /* KV-length rollback alone, e.g. for the draft model's cache ("Speculative
  * decoding" (mhtirogla.ai), How it works step 5: truncate the length in both

@@ -99,7 +99,7 @@ def lib():
             L.orc_acceptance_ema.restype = None
             L.orc_acceptance_ema.argtypes = [vp, vp, i32, i64, vp, ctypes.c_float, vp, vp]
             L.orc_speedups.restype = None
-            L.orc_speedups.argtypes = [dbl, i32, dbl, vp]
+            L.orc_speedups.argtypes = [ctypes.c_float, i32, ctypes.c_float, vp]
             L.orc_best_gamma.restype = i32
             L.orc_best_gamma.argtypes = [ctypes.c_float, i32, ctypes.c_float]
             L.orc_adapt_gamma.restype = i64
@@ -208,8 +208,8 @@ def acceptance_ema(accepted, gammas, gamma_max, ema, lam, status=None):
 
 
 def speedups(alpha: float, gamma_max: int, c: float) -> np.ndarray:
-    """E(alpha, g) / (1 + g c) for g = 0..gamma_max (float64)."""
-    sp = np.zeros(int(gamma_max) + 1, dtype=np.float64)
+    """E(alpha, g) / (1 + g c) for g = 0..gamma_max (float32 arithmetic)."""
+    sp = np.zeros(int(gamma_max) + 1, dtype=np.float32)
     lib().orc_speedups(float(alpha), int(gamma_max), float(c), sp.ctypes.data)
     return sp
 
@@ -219,7 +219,7 @@ def best_gamma(ema: float, gamma_max: int, c: float) -> int:
 
 
 def adapt_gamma(ema, gamma_max: int, c: float, max_positions: int = 0):
-    """(gammas int32 [B], total verify positions) for the next round."""
+    """(gammas int32 [B], verify positions of the chosen gammas before the switch)."""
     e = np.ascontiguousarray(ema, dtype=np.float32)
     out = np.zeros(e.shape[0], dtype=np.int32)
     tot = lib().orc_adapt_gamma(e.ctypes.data, e.shape[0], int(gamma_max), float(c), int(max_positions),

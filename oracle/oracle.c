@@ -622,8 +622,10 @@ int32_t orc_position_rows(const orc_args_t* a, int64_t b, int64_t i, double* p, 
  *     sequence status other than OK leave it unchanged;
  *   - gamma_b for the next round is the smallest g in [0, gamma_max] with the
  *     largest E(a, g) / (1 + g c), a = the running acceptance clamped to
- *     [0, 1] (NaN read as 0), evaluated in float64 with the power taken by
- *     repeated multiplication and E = g + 1 at a = 1 (the limit);
+ *     [0, 1] (NaN read as 0), in float32 with every operation rounded in a
+ *     fixed order: E(a, g) = 1 + a + ... + a^g (the same quantity as the
+ *     pages' closed form, summed term by term: no cancellation near a = 1),
+ *     the powers by repeated multiplication;
  *   - if max_positions > 0 and the verify positions sum_b (gamma_b + 1)
  *     exceed it, every gamma_b is 0 (speculation off for the batch). */
 void orc_acceptance_ema(const int32_t* accepted, const int32_t* gammas, int32_t gamma_max, int64_t B,
@@ -643,31 +645,34 @@ void orc_acceptance_ema(const int32_t* accepted, const int32_t* gammas, int32_t 
     }
 }
 
-/* E(a, g) / (1 + g c) for g = 0..gamma_max into sp[]. */
-void orc_speedups(double a, int32_t gamma_max, double c, double* sp) {
-    if (!(a >= 0.0)) a = 0.0; /* NaN and negatives */
-    if (a > 1.0) a = 1.0;
-    double pw = a; /* a^(g+1) */
+/* E(a, g) / (1 + g c) for g = 0..gamma_max into sp[] (float32 arithmetic). */
+void orc_speedups(float a, int32_t gamma_max, float c, float* sp) {
+    if (!(a >= 0.0f)) a = 0.0f; /* NaN and negatives */
+    if (a > 1.0f) a = 1.0f;
+    float pw = 1.0f, E = 1.0f; /* a^g and 1 + a + ... + a^g */
     for (int32_t g = 0; g <= gamma_max; ++g) {
-        const double E = (a == 1.0) ? (double)(g + 1) : (1.0 - pw) / (1.0 - a);
-        const double den = 1.0 + (double)g * c;
+        if (g > 0) {
+            pw = pw * a;
+            E = E + pw;
+        }
+        const float den = 1.0f + (float)g * c;
         sp[g] = E / den;
-        pw = pw * a;
     }
 }
 
 int32_t orc_best_gamma(float ema, int32_t gamma_max, float c) {
-    double sp[65];
+    float sp[65];
     if (gamma_max > 64) gamma_max = 64;
     if (gamma_max < 0) gamma_max = 0;
-    orc_speedups((double)ema, gamma_max, (double)c, sp);
+    orc_speedups(ema, gamma_max, c, sp);
     int32_t best = 0;
     for (int32_t g = 1; g <= gamma_max; ++g)
         if (sp[g] > sp[best]) best = g;
     return best;
 }
 
-/* Returns sum_b (gamma_b + 1) of the gammas written. */
+/* Returns the verify positions sum_b (gamma_b + 1) of the chosen gammas,
+ * before the switch (the quantity compared with max_positions). */
 int64_t orc_adapt_gamma(const float* ema, int64_t B, int32_t gamma_max, float c, int64_t max_positions,
                         int32_t* gammas_out) {
     int64_t total = 0;
@@ -675,9 +680,7 @@ int64_t orc_adapt_gamma(const float* ema, int64_t B, int32_t gamma_max, float c,
         gammas_out[b] = orc_best_gamma(ema[b], gamma_max, c);
         total += gammas_out[b] + 1;
     }
-    if (max_positions > 0 && total > max_positions) {
+    if (max_positions > 0 && total > max_positions)
         for (int64_t b = 0; b < B; ++b) gammas_out[b] = 0;
-        total = B;
-    }
     return total;
 }

@@ -28,7 +28,7 @@ SPEC_ERR_CUDA = 4
 SPEC_ERR_UNSUPPORTED = 5
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_STATIC_SCRATCH_BYTES = 8 << 20  # scratch of spec_verify_sample_static, per device
-SPEC_ABI_VERSION = 2
+SPEC_ABI_VERSION = 3
 SEQ_OK, SEQ_BAD_TOKEN, SEQ_BAD_KV, SEQ_BAD_ROW, SEQ_BAD_LAYOUT, SEQ_BAD_TEMP = 0, 1, 2, 3, 4, 5
 
 
@@ -73,6 +73,8 @@ class SpecVerifyArgs(ctypes.Structure):
         ("workspace_bytes", ctypes.c_size_t),
         ("top_k", ctypes.c_int32),
         ("top_ks", ctypes.c_void_p),
+        ("accept_ema", ctypes.c_void_p),
+        ("ema_lambda", ctypes.c_float),
     ]
 
 
@@ -112,6 +114,8 @@ def lib():
             L.spec_verify_greedy.argtypes = [A, vp]
             L.spec_verify_sample_static.restype = ctypes.c_int
             L.spec_verify_sample_static.argtypes = [A, vp]
+            L.spec_adapt_gamma.restype = ctypes.c_int
+            L.spec_adapt_gamma.argtypes = [vp, i32, i32, ctypes.c_float, i64, vp, vp, vp]
             L.spec_kv_rollback.restype = ctypes.c_int
             L.spec_kv_rollback.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
             L.spec_debug_philox.restype = ctypes.c_int
@@ -174,8 +178,9 @@ class VerifyArgs:
                  draft_row_off=None, draft_is_probs=False, temperatures=None, temperature=1.0, seed=0, round=0,
                  seq_offset=0, uniforms=None, kv_lens_in=None, kv_lens_out=None, block_size=0,
                  out_num_blocks=None, out_tokens=None, out_accepted=None, seq_status=None, workspace=None,
-                 top_k=0, top_ks=None):
+                 top_k=0, top_ks=None, accept_ema=None, ema_lambda=0.0):
         for name, t in [("target", target), ("draft", draft), ("draft_tokens", draft_tokens), ("top_ks", top_ks),
+                        ("accept_ema", accept_ema),
                         ("target_row_off", target_row_off), ("draft_row_off", draft_row_off),
                         ("temperatures", temperatures), ("uniforms", uniforms), ("kv_lens_in", kv_lens_in),
                         ("kv_lens_out", kv_lens_out), ("out_num_blocks", out_num_blocks),
@@ -185,7 +190,7 @@ class VerifyArgs:
                             draft_row_off=draft_row_off, temperatures=temperatures, uniforms=uniforms,
                             kv_lens_in=kv_lens_in, kv_lens_out=kv_lens_out, out_num_blocks=out_num_blocks,
                             out_tokens=out_tokens, out_accepted=out_accepted, seq_status=seq_status,
-                            top_ks=top_ks)
+                            top_ks=top_ks, accept_ema=accept_ema)
         a = SpecVerifyArgs()
         a.struct_size = ctypes.sizeof(SpecVerifyArgs)
         a.batch = int(batch)
@@ -216,6 +221,8 @@ class VerifyArgs:
         a.seq_status = _ptr(seq_status)
         a.top_k = int(top_k)
         a.top_ks = _ptr(top_ks)
+        a.accept_ema = _ptr(accept_ema)
+        a.ema_lambda = float(ema_lambda)
         self.struct = a
         self.workspace = None
         if workspace is not None:
@@ -236,6 +243,13 @@ class VerifyArgs:
         self.tensors["top_ks"] = top_ks
         self.struct.top_k = int(top_k)
         self.struct.top_ks = _ptr(top_ks)
+
+    def set_accept_ema(self, accept_ema=None, ema_lambda=0.0):
+        """Running acceptance (float32 [B], updated in place by each verify call) or None."""
+        _check_dev(accept_ema, "accept_ema")
+        self.tensors["accept_ema"] = accept_ema
+        self.struct.accept_ema = _ptr(accept_ema)
+        self.struct.ema_lambda = float(ema_lambda)
 
     def set_tokens(self, draft_tokens):
         _check_dev(draft_tokens, "draft_tokens")
@@ -289,6 +303,15 @@ def spec_workspace_init(ptr: int, nbytes: int, stream=None) -> int:
 
 def spec_verify_sample(args: VerifyArgs, stream=None) -> int:
     return lib().spec_verify_sample(ctypes.byref(args.struct), _stream(stream))
+
+
+def spec_adapt_gamma(accept_ema, gamma_max: int, draft_cost: float, gammas_out, max_positions: int = 0,
+                     total_positions_out=None, stream=None) -> int:
+    """Next-round gamma per request from the running acceptance (all device tensors)."""
+    for name, t in [("accept_ema", accept_ema), ("gammas_out", gammas_out), ("total_positions_out", total_positions_out)]:
+        _check_dev(t, name)
+    return lib().spec_adapt_gamma(accept_ema.data_ptr(), int(accept_ema.numel()), int(gamma_max), float(draft_cost),
+                                  int(max_positions), gammas_out.data_ptr(), _ptr(total_positions_out), _stream(stream))
 
 
 def spec_verify_greedy(args: VerifyArgs, stream=None) -> int:

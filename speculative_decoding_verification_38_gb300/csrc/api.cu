@@ -116,6 +116,8 @@ spec_status_t check_call(const spec_verify_args_t* a, int greedy) {
         if (a->uniforms && !aligned(a->uniforms, 8)) return SPEC_ERR_ALIGNMENT;
         if (a->top_ks && !aligned(a->top_ks, 4)) return SPEC_ERR_ALIGNMENT;
     }
+    if (a->accept_ema && !aligned(a->accept_ema, 4)) return SPEC_ERR_ALIGNMENT;
+    if (a->accept_ema && !(a->ema_lambda >= 0.f && a->ema_lambda <= 1.f)) return SPEC_ERR_INVALID_ARG;
     if (a->block_size < 0) return SPEC_ERR_INVALID_ARG;
     if ((a->kv_lens_out || a->out_num_blocks) && !a->kv_lens_in) return SPEC_ERR_INVALID_ARG;
     if (a->out_num_blocks && a->block_size == 0) return SPEC_ERR_INVALID_ARG;
@@ -199,6 +201,8 @@ bool build_params(const spec_verify_args_t* a, int greedy, int grid_cap, int tma
     p.top_k = tk ? a->top_k : 0;
     p.direct = tk ? 1 : 0;
     p.tau = tk ? (float*)(ws + L.off_tau) : nullptr;
+    p.ema = a->accept_ema;
+    p.ema_lambda = a->ema_lambda;
     return true;
 }
 
@@ -323,6 +327,21 @@ SPEC_API spec_status_t spec_kv_rollback(const int32_t* kv_in, int32_t* kv_out, c
         if (p && !aligned(p, 4)) return SPEC_ERR_ALIGNMENT;
     if (launch_kv_rollback(kv_in, kv_out, accepted, gammas, gamma_max, batch, block_size, out_num_blocks,
                            seq_status, (cudaStream_t)stream) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+SPEC_API spec_status_t spec_adapt_gamma(const float* accept_ema, int32_t batch, int32_t gamma_max, float draft_cost,
+                                        int64_t max_positions, int32_t* gammas_out, int64_t* total_positions_out,
+                                        spec_stream_t stream) {
+    if (!accept_ema || !gammas_out || batch < 1 || batch > kMaxBatch) return SPEC_ERR_INVALID_ARG;
+    if (gamma_max < 0 || gamma_max > kMaxGammaApi) return SPEC_ERR_INVALID_ARG;
+    if (!(draft_cost >= 0.f && draft_cost < 3.0e38f)) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(accept_ema, 4) || !aligned(gammas_out, 4)) return SPEC_ERR_ALIGNMENT;
+    if (total_positions_out && !aligned(total_positions_out, 8)) return SPEC_ERR_ALIGNMENT;
+    if (max_positions > 0 && batch > 1024 && !total_positions_out) return SPEC_ERR_INVALID_ARG;
+    if (launch_adapt_gamma(accept_ema, batch, gamma_max, draft_cost, max_positions, gammas_out, total_positions_out,
+                           (cudaStream_t)stream) != cudaSuccess)
         return SPEC_ERR_CUDA;
     return SPEC_OK;
 }

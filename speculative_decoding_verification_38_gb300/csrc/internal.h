@@ -96,6 +96,8 @@ struct StatsParams {
     int32_t top_k;
     int32_t direct;      // 1: row_stats were written whole by the top-k pass; finalize reads them
     float* tau;          // [rows_total] threshold of every row (-inf: whole row), or null without top-k
+    float* ema;          // [B] running acceptance (float32, updated in place), or null
+    float ema_lambda;
 };
 
 // Table 2^(i/64), i = 0..63, as float pairs (value = hi + lo).
@@ -154,6 +156,8 @@ void exp2_pairs(Exp2Pairs& t);  // host: fills the table
 cudaError_t launch_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,
                                const int32_t* gammas, int32_t gmax, int32_t B, int32_t block_size,
                                int32_t* out_blocks, int32_t* seq_status, cudaStream_t s);
+cudaError_t launch_adapt_gamma(const float* ema, int32_t B, int32_t gmax, float c, int64_t max_positions,
+                               int32_t* gammas, int64_t* total, cudaStream_t s);
 cudaError_t launch_debug_philox(uint64_t seed, uint64_t round, uint32_t seq_offset, int32_t B, int32_t npos,
                                 float* out, cudaStream_t s);
 cudaError_t launch_debug_probs(const StatsParams& p, int32_t seq, int32_t pos, float* out_p, float* out_q,

@@ -29,6 +29,81 @@ __global__ void kv_rollback_kernel(const int32_t* kv_in, int32_t* kv_out, const 
     if (seq_status) seq_status[b] = st;
 }
 
+// Adaptive gamma for the next round: per request, the smallest g in
+// [0, gmax] with the largest E(a, g) / (1 + g c) ("Speculative decoding"
+// (inference.tusharamrit.in), actual speedup), a the running acceptance
+// clamped to [0, 1], E(a, g) = 1 + a + ... + a^g summed term by term.
+// Float32, every operation an explicit correctly rounded one in a fixed
+// order (no contraction), so any IEEE machine gets the same gammas. Then
+// speculation is off for the whole batch if its verify positions sum
+// (g_b + 1) exceed max_positions (> 0) ("Speculative decoding"
+// (mhtirogla.ai), Implementation notes).
+constexpr int kAdaptThreads = 1024;  // one CTA: batches up to this size
+constexpr int kAdaptBlock = 256;     // larger batches: one request per thread
+
+__device__ int32_t best_gamma(float ema, int32_t gmax, float c) {
+    float a = ema;
+    if (!(a >= 0.f)) a = 0.f;
+    if (a > 1.f) a = 1.f;
+    float pw = 1.f, E = 1.f, best_sp = 0.f;
+    int32_t best = 0;
+#pragma unroll 4
+    for (int32_t g = 0; g <= gmax; ++g) {  // the divisions of successive g overlap
+        if (g > 0) {
+            pw = __fmul_rn(pw, a);
+            E = __fadd_rn(E, pw);
+        }
+        const float sp = __fdiv_rn(E, __fadd_rn(1.f, __fmul_rn((float)g, c)));
+        if (g == 0 || sp > best_sp) {
+            best_sp = sp;
+            best = g;
+        }
+    }
+    return best;
+}
+
+__device__ long long block_sum_ll(long long v, long long* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    long long t = 0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+    return t;
+}
+
+// The whole batch in one CTA (B <= kAdaptThreads): choice, sum and switch.
+__global__ void __launch_bounds__(kAdaptThreads) adapt_gamma_small(const float* ema, int32_t B, int32_t gmax, float c,
+                                                                    int64_t max_positions, int32_t* gammas,
+                                                                    int64_t* total) {
+    __shared__ long long red[kAdaptThreads / 32];
+    const int b = threadIdx.x;
+    const int32_t g = b < B ? best_gamma(ema[b], gmax, c) : 0;
+    const long long t = block_sum_ll(b < B ? g + 1 : 0, red);
+    if (b < B) gammas[b] = (max_positions > 0 && t > max_positions) ? 0 : g;
+    if (b == 0 && total) *total = t;
+}
+
+// Larger batches: each request's choice, and the positions summed into
+// *total (zeroed before; integer atomics, so the sum does not depend on order).
+__global__ void __launch_bounds__(kAdaptBlock) adapt_gamma_choose(const float* ema, int32_t B, int32_t gmax, float c,
+                                                                   int32_t* gammas, unsigned long long* total) {
+    __shared__ long long red[kAdaptBlock / 32];
+    const int32_t b = blockIdx.x * kAdaptBlock + threadIdx.x;
+    const int32_t g = b < B ? best_gamma(ema[b], gmax, c) : 0;
+    if (b < B) gammas[b] = g;
+    if (!total) return;
+    const long long t = block_sum_ll(b < B ? g + 1 : 0, red);
+    if (threadIdx.x == 0) atomicAdd(total, (unsigned long long)t);
+}
+
+// The switch for larger batches, after the sum is complete.
+__global__ void __launch_bounds__(kAdaptBlock) adapt_gamma_switch(int32_t B, int64_t max_positions, int32_t* gammas,
+                                                                   const int64_t* total) {
+    const int32_t b = blockIdx.x * kAdaptBlock + threadIdx.x;
+    if (b < B && *total > max_positions) gammas[b] = 0;
+}
+
 __global__ void debug_philox_kernel(uint64_t seed, uint64_t round, uint32_t seq_offset, int32_t B, int32_t npos,
                                     float* out) {
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
@@ -182,6 +257,19 @@ cudaError_t launch_debug_rowstats(const float2* row_stats, int64_t rows, int gre
     const int th = 256;
     debug_rowstats_kernel<<<(unsigned)((rows + th - 1) / th), th, 0, s>>>(row_stats, rows, greedy, out_a, out_b,
                                                                           out_idx);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_adapt_gamma(const float* ema, int32_t B, int32_t gmax, float c, int64_t max_positions,
+                               int32_t* gammas, int64_t* total, cudaStream_t s) {
+    if (B <= kAdaptThreads) {
+        adapt_gamma_small<<<1, kAdaptThreads, 0, s>>>(ema, B, gmax, c, max_positions, gammas, total);
+        return cudaGetLastError();
+    }
+    const unsigned grid = (unsigned)((B + kAdaptBlock - 1) / kAdaptBlock);
+    if (total && cudaMemsetAsync(total, 0, sizeof(int64_t), s) != cudaSuccess) return cudaErrorUnknown;
+    adapt_gamma_choose<<<grid, kAdaptBlock, 0, s>>>(ema, B, gmax, c, gammas, (unsigned long long*)total);
+    if (max_positions > 0) adapt_gamma_switch<<<grid, kAdaptBlock, 0, s>>>(B, max_positions, gammas, total);
     return cudaGetLastError();
 }
 

@@ -398,7 +398,20 @@ __device__ void write_error(const StatsParams& p, int32_t b, int32_t st, int64_t
     }
 }
 
+// The running acceptance of sequence b after a round with a of its g drafts
+// accepted: the round performed t = a + 1 accept tests if a draft was
+// rejected, else g; ema += lambda * (a / t - ema), each step rounded to
+// float32 in that order. Rounds with g = 0 leave it.
+__device__ __forceinline__ void update_ema(const StatsParams& p, int32_t b, int32_t g, int32_t a) {
+    if (!p.ema || g <= 0) return;
+    const int32_t t = a < g ? a + 1 : g;
+    const float x = __fdiv_rn((float)a, (float)t);
+    const float e = p.ema[b];
+    p.ema[b] = __fadd_rn(e, __fmul_rn(p.ema_lambda, __fsub_rn(x, e)));
+}
+
 __device__ void write_ok(const StatsParams& p, int32_t b, int32_t g, int32_t a) {
+    update_ema(p, b, g, a);
     p.out_accepted[b] = a;
     if (p.kv_out || p.out_blocks) {
         int32_t kv = p.kv_in ? p.kv_in[b] - (g - a) : 0;
@@ -1182,6 +1195,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
         if (i <= g) p.out_tokens[t0 + i] = (i < a) ? (h < 2 ? x[h] : __ldg(p.tokens + d0 + i)) : -1;
     }
     if (lane == 0) {
+        update_ema(p, b, g, a);
         p.out_accepted[b] = a;
         if (p.kv_out || p.out_blocks) {
             const int32_t kvo = p.kv_in ? kv - (g - a) : 0;

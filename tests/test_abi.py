@@ -62,7 +62,7 @@ def test_struct_layout_matches_header(sv):
 
 
 def test_abi_version_and_status_strings(sv):
-    assert sv.spec_abi_version() == 2 == sv.SPEC_ABI_VERSION
+    assert sv.spec_abi_version() == 3 == sv.SPEC_ABI_VERSION
     assert sv.spec_status_string(0) == "SPEC_OK"
     assert sv.spec_status_string(3) == "SPEC_ERR_WORKSPACE"
 
@@ -128,6 +128,16 @@ def test_host_validation_rejects_before_cuda(sv):
     a.struct_size = sv.SpecVerifyArgs.top_k.offset
     assert call(a) == sv.SPEC_ERR_INVALID_ARG
     assert L.spec_kv_rollback(None, None, None, None, 3, 4, 0, None, None, None) == sv.SPEC_ERR_INVALID_ARG
+    fake = 1 << 20
+    assert L.spec_adapt_gamma(None, 4, 8, 0.05, 0, fake, None, None) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_adapt_gamma(fake, 0, 8, 0.05, 0, fake, None, None) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_adapt_gamma(fake, 4, 65, 0.05, 0, fake, None, None) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_adapt_gamma(fake, 4, 8, float("nan"), 0, fake, None, None) == sv.SPEC_ERR_INVALID_ARG
+    assert L.spec_adapt_gamma(fake + 2, 4, 8, 0.05, 0, fake, None, None) == sv.SPEC_ERR_ALIGNMENT
+    a = _args(sv)
+    a.accept_ema = fake
+    a.ema_lambda = 1.5  # outside [0, 1]
+    assert call(a) == sv.SPEC_ERR_INVALID_ARG
     assert L.spec_debug_philox(0, 0, 0, 0, 1, None, None) == sv.SPEC_ERR_INVALID_ARG
 
 

@@ -39,9 +39,17 @@ def test_speedup_at_zero_cost_is_expected_tokens(orc):
         a, g, printed, dec = float(parts[0]), int(parts[1]), float(parts[2]), int(parts[3])
         assert round(orc.speedups(a, g, 0.0)[g], dec) == printed, parts
     sp = orc.speedups(0.0, 8, 0.1)  # alpha = 0: one token per pass, cost 1 + g c
-    np.testing.assert_allclose(sp, 1.0 / (1.0 + 0.1 * np.arange(9)), rtol=1e-15)
+    np.testing.assert_allclose(sp, 1.0 / (1.0 + 0.1 * np.arange(9)), rtol=2e-7)
     sp = orc.speedups(1.0, 8, 0.0)  # alpha = 1: the limit g + 1
-    assert np.array_equal(sp, np.arange(1, 10, dtype=np.float64))
+    assert np.array_equal(sp, np.arange(1, 10, dtype=np.float32))
+    # the closed form at alpha near 1 (where it cancels) against exact rationals
+    for a in (0.999, 0.9999, 0.5):
+        a32 = float(np.float32(a))
+        sp = orc.speedups(a32, 64, 0.0)
+        fa = Fraction(a32)
+        for g in (1, 8, 64):
+            exact = float((1 - fa ** (g + 1)) / (1 - fa))
+            assert abs(float(sp[g]) - exact) <= 1e-5 * exact, (a, g)
 
 
 def _exact_best(alpha: Fraction, gmax: int, c: Fraction):
@@ -64,8 +72,8 @@ def test_best_gamma_matches_exact_rationals(orc):
         c32 = np.float32(rng.choice([0.0, 0.01, 0.02, 0.05, 0.1, 0.2, 0.3, 0.5]))
         gmax = int(rng.integers(0, 17))
         best, gap = _exact_best(Fraction(float(a32)), gmax, Fraction(float(c32)))
-        if gap < Fraction(1, 10**9):
-            continue  # a near tie: float64 may order it either way
+        if gap < Fraction(1, 10**5):
+            continue  # a near tie: float32 may order it either way
         assert orc.best_gamma(float(a32), gmax, float(c32)) == best, (a32, c32, gmax)
         checked += 1
     assert checked > 350
@@ -94,7 +102,7 @@ def test_adapt_gamma_batch_switch(orc):
     g2, t2 = orc.adapt_gamma(ema, 8, 0.05, max_positions=total)  # exactly at the budget: kept
     assert np.array_equal(g2, g) and t2 == total
     g3, t3 = orc.adapt_gamma(ema, 8, 0.05, max_positions=total - 1)  # over it: speculation off
-    assert np.all(g3 == 0) and t3 == 4
+    assert np.all(g3 == 0) and t3 == total  # the positions reported are the ones compared
 
 
 def test_acceptance_ema_float32_steps(orc):
