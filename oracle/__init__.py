@@ -104,6 +104,8 @@ def lib():
             L.orc_best_gamma.argtypes = [ctypes.c_float, i32, ctypes.c_float]
             L.orc_adapt_gamma.restype = i64
             L.orc_adapt_gamma.argtypes = [vp, i64, i32, ctypes.c_float, i64, vp]
+            L.orc_ngram_draft.restype = None
+            L.orc_ngram_draft.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, vp, vp]
             L.orc_residual.restype = dbl
             L.orc_residual.argtypes = [vp, vp, i64, vp]
             L.orc_inverse_cdf.restype = i64
@@ -225,6 +227,20 @@ def adapt_gamma(ema, gamma_max: int, c: float, max_positions: int = 0):
     tot = lib().orc_adapt_gamma(e.ctypes.data, e.shape[0], int(gamma_max), float(c), int(max_positions),
                                 out.ctypes.data)
     return out, int(tot)
+
+
+def ngram_draft(ctx, ctx_off, n_max: int, n_min: int, gamma: int):
+    """Prompt-lookup drafts: dict of draft [B, gamma] (-1 padded), n_draft, match_pos, match_n."""
+    c = np.ascontiguousarray(ctx, dtype=np.int32)
+    off = np.ascontiguousarray(ctx_off, dtype=np.int64)
+    B = off.shape[0] - 1
+    draft = np.full(B * max(gamma, 1), -7, dtype=np.int32)
+    nd = np.zeros(B, np.int32)
+    pos = np.zeros(B, np.int64)
+    mn = np.zeros(B, np.int32)
+    lib().orc_ngram_draft(c.ctypes.data, off.ctypes.data, B, int(n_max), int(n_min), int(gamma), draft.ctypes.data,
+                          nd.ctypes.data, pos.ctypes.data, mn.ctypes.data)
+    return {"draft": draft[:B * gamma].reshape(B, gamma), "n_draft": nd, "match_pos": pos, "match_n": mn}
 
 
 def residual(p: np.ndarray, q: np.ndarray):

@@ -684,3 +684,52 @@ int64_t orc_adapt_gamma(const float* ema, int64_t B, int32_t gamma_max, float c,
         for (int64_t b = 0; b < B; ++b) gammas_out[b] = 0;
     return total;
 }
+
+/* ------------------------------------------------------------ n-gram drafter
+ * Prompt lookup / n-gram drafting ("Speculative decoding" (mhtirogla.ai),
+ * Implementation notes: copy the continuation of the last matching n-gram;
+ * "Speculative decoding" (inference.tusharamrit.in), n-gram / prompt lookup:
+ * search the existing context for the current suffix and propose what
+ * followed it last time). Readings where the pages stop short:
+ *   - the search covers the whole context of the sequence (prompt and the
+ *     tokens generated so far), ctx[0 .. L);
+ *   - the suffix is the last n tokens; a match is an earlier start j
+ *     (0 <= j <= L - n - 1, so at least one token follows it) with
+ *     ctx[j .. j+n) equal to the suffix; the match taken is the latest such
+ *     j (what followed "last time"); it may overlap the suffix;
+ *   - n runs from n_max down to n_min and the first n with a match is used;
+ *   - the draft is ctx[j+n .. min(j+n+gamma, L)), fewer than gamma tokens
+ *     when the context ends first; no match gives no draft.
+ * Outputs per sequence b: draft[b*gamma .. +gamma) (-1 after the drafted
+ * tokens), n_draft[b], match_pos[b] (j, or -1), match_n[b] (n, or 0). */
+void orc_ngram_draft(const int32_t* ctx, const int64_t* ctx_off, int64_t B, int32_t n_max, int32_t n_min,
+                     int32_t gamma, int32_t* draft, int32_t* n_draft, int64_t* match_pos, int32_t* match_n) {
+    for (int64_t b = 0; b < B; ++b) {
+        const int32_t* c = ctx + ctx_off[b];
+        const int64_t L = ctx_off[b + 1] - ctx_off[b];
+        int64_t jbest = -1;
+        int32_t nbest = 0;
+        for (int32_t n = n_max; n >= n_min && n >= 1 && jbest < 0; --n) {
+            if (L < (int64_t)n + 1) continue;
+            for (int64_t j = L - n - 1; j >= 0; --j) {
+                int32_t k = 0;
+                while (k < n && c[j + k] == c[L - n + k]) ++k;
+                if (k == n) {
+                    jbest = j;
+                    nbest = n;
+                    break;
+                }
+            }
+        }
+        int32_t cnt = 0;
+        for (int32_t i = 0; i < gamma; ++i) {
+            const int64_t src = jbest + nbest + i;
+            const int has = jbest >= 0 && src < L;
+            draft[b * gamma + i] = has ? c[src] : -1;
+            cnt += has;
+        }
+        n_draft[b] = cnt;
+        if (match_pos) match_pos[b] = jbest;
+        if (match_n) match_n[b] = nbest;
+    }
+}

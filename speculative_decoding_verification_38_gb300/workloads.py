@@ -296,4 +296,33 @@ def config4(batch=256, gamma=5, vocab=152064, dataset=0, tie_every=8) -> Workloa
     )
 
 
+def ngram_contexts(batch=64, doc_len=4096, gen_len=1024, vocab=128256, span=(8, 64), edit_prob=0.05,
+                   dataset=0):
+    """Contexts for the n-gram drafter: the edit / summarisation / RAG case
+    where the output copies the input. Sequence b holds a document of
+    doc_len tokens (Zipf-distributed ids, ranks permuted per sequence)
+    followed by gen_len generated tokens made of spans copied from random
+    places of the document, each token replaced by a fresh one with
+    probability edit_prob. Returns (ctx int32, ctx_off int64 [B+1])."""
+    rng = _rng(60, dataset)
+    ranks = np.arange(1, vocab + 1, dtype=np.float64)
+    w = 1.0 / ranks
+    cdf = np.cumsum(w / w.sum())
+    out = []
+    for _ in range(batch):
+        perm = rng.permutation(vocab).astype(np.int32)
+        doc = perm[np.minimum(np.searchsorted(cdf, rng.random(doc_len)), vocab - 1)]
+        gen = np.empty(0, np.int32)
+        while gen.size < gen_len:
+            n = int(rng.integers(span[0], span[1] + 1))
+            s0 = int(rng.integers(0, max(1, doc_len - n)))
+            piece = doc[s0:s0 + n].copy()
+            edit = rng.random(piece.size) < edit_prob
+            piece[edit] = perm[np.minimum(np.searchsorted(cdf, rng.random(int(edit.sum()))), vocab - 1)]
+            gen = np.concatenate([gen, piece])
+        out.append(np.concatenate([doc, gen[:gen_len]]))
+    off = np.concatenate([[0], np.cumsum([a.size for a in out])]).astype(np.int64)
+    return np.concatenate(out).astype(np.int32), off
+
+
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
