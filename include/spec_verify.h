@@ -254,6 +254,27 @@ SPEC_API spec_status_t spec_adapt_gamma(const float* accept_ema, int32_t batch, 
                                         int64_t max_positions, int32_t* gammas_out, int64_t* total_positions_out,
                                         spec_stream_t stream);
 
+/* N-gram (prompt lookup) drafter: draft tokens at no model cost ("Speculative
+ * decoding" (mhtirogla.ai), Implementation notes: copy the continuation of
+ * the last matching n-gram; "Speculative decoding" (inference.tusharamrit.in),
+ * n-gram / prompt lookup: search the context for the current suffix and
+ * propose what followed it last time). Sequence b's context is
+ * ctx[ctx_off[b] .. ctx_off[b+1]) (prompt and generated tokens, L_b of
+ * them). For n = n_max down to n_min, the first n for which the last n
+ * tokens occur earlier at a start j <= L_b - n - 1 (so a token follows; the
+ * occurrence may overlap the suffix) gives the match: the latest such j.
+ * Outputs: draft_out[b*gamma .. +gamma) = ctx[j+n ..] up to gamma tokens and
+ * the end of the context, -1 after them; n_draft_out[b] = their number (0
+ * without a match); match_pos_out[b] = j or -1 and match_n_out[b] = n or 0
+ * (both may be NULL). All arrays are device memory; ctx_off is int64
+ * [batch+1], non-decreasing. 1 <= batch <= 65536,
+ * 1 <= n_min <= n_max <= 16, 0 <= gamma <= 64. The drafts feed either
+ * verify: greedy as draft_tokens, sampling as draft_tokens with one-hot
+ * probability rows. */
+SPEC_API spec_status_t spec_ngram_draft(const int32_t* ctx, const int64_t* ctx_off, int32_t batch, int32_t n_max,
+                                        int32_t n_min, int32_t gamma, int32_t* draft_out, int32_t* n_draft_out,
+                                        int64_t* match_pos_out, int32_t* match_n_out, spec_stream_t stream);
+
 /* KV-length rollback alone, e.g. for the draft model's cache ("Speculative
  * decoding" (mhtirogla.ai), How it works step 5: truncate the length in both
  * models; Implementation notes: paged KV makes this a length truncate).

@@ -116,6 +116,8 @@ def lib():
             L.spec_verify_sample_static.argtypes = [A, vp]
             L.spec_adapt_gamma.restype = ctypes.c_int
             L.spec_adapt_gamma.argtypes = [vp, i32, i32, ctypes.c_float, i64, vp, vp, vp]
+            L.spec_ngram_draft.restype = ctypes.c_int
+            L.spec_ngram_draft.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
             L.spec_kv_rollback.restype = ctypes.c_int
             L.spec_kv_rollback.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
             L.spec_debug_philox.restype = ctypes.c_int
@@ -312,6 +314,17 @@ def spec_adapt_gamma(accept_ema, gamma_max: int, draft_cost: float, gammas_out, 
         _check_dev(t, name)
     return lib().spec_adapt_gamma(accept_ema.data_ptr(), int(accept_ema.numel()), int(gamma_max), float(draft_cost),
                                   int(max_positions), gammas_out.data_ptr(), _ptr(total_positions_out), _stream(stream))
+
+
+def spec_ngram_draft(ctx, ctx_off, n_max: int, n_min: int, gamma: int, draft_out, n_draft_out, match_pos_out=None,
+                     match_n_out=None, stream=None) -> int:
+    """Prompt-lookup drafts for every sequence (all device tensors; ctx int32, ctx_off int64 [B+1])."""
+    for name, t in [("ctx", ctx), ("ctx_off", ctx_off), ("draft_out", draft_out), ("n_draft_out", n_draft_out),
+                    ("match_pos_out", match_pos_out), ("match_n_out", match_n_out)]:
+        _check_dev(t, name)
+    return lib().spec_ngram_draft(_ptr(ctx) if ctx is not None and ctx.numel() else None, ctx_off.data_ptr(),
+                                  int(ctx_off.numel() - 1), int(n_max), int(n_min), int(gamma), draft_out.data_ptr(),
+                                  n_draft_out.data_ptr(), _ptr(match_pos_out), _ptr(match_n_out), _stream(stream))
 
 
 def spec_verify_greedy(args: VerifyArgs, stream=None) -> int:

@@ -346,6 +346,21 @@ SPEC_API spec_status_t spec_adapt_gamma(const float* accept_ema, int32_t batch, 
     return SPEC_OK;
 }
 
+SPEC_API spec_status_t spec_ngram_draft(const int32_t* ctx, const int64_t* ctx_off, int32_t batch, int32_t n_max,
+                                        int32_t n_min, int32_t gamma, int32_t* draft_out, int32_t* n_draft_out,
+                                        int64_t* match_pos_out, int32_t* match_n_out, spec_stream_t stream) {
+    if (!ctx_off || !draft_out || !n_draft_out || batch < 1 || batch > kMaxBatch) return SPEC_ERR_INVALID_ARG;
+    if (n_min < 1 || n_max < n_min || n_max > kNgMaxN || gamma < 0 || gamma > kMaxGammaApi) return SPEC_ERR_INVALID_ARG;
+    if ((ctx && !aligned(ctx, 4)) || !aligned(ctx_off, 8) || !aligned(draft_out, 4) || !aligned(n_draft_out, 4))
+        return SPEC_ERR_ALIGNMENT;
+    if ((match_pos_out && !aligned(match_pos_out, 8)) || (match_n_out && !aligned(match_n_out, 4)))
+        return SPEC_ERR_ALIGNMENT;
+    if (launch_ngram(ctx, ctx_off, batch, n_max, n_min, gamma, draft_out, n_draft_out, match_pos_out, match_n_out,
+                     (cudaStream_t)stream) != cudaSuccess)
+        return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
 SPEC_API spec_status_t spec_debug_philox(uint64_t seed, uint64_t round, uint32_t seq_offset, int32_t batch,
                                          int32_t npos, float* out, spec_stream_t stream) {
     if (!out || batch < 1 || npos < 1 || !aligned(out, 4)) return SPEC_ERR_INVALID_ARG;

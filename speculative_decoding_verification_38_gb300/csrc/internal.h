@@ -156,6 +156,9 @@ void exp2_pairs(Exp2Pairs& t);  // host: fills the table
 cudaError_t launch_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,
                                const int32_t* gammas, int32_t gmax, int32_t B, int32_t block_size,
                                int32_t* out_blocks, int32_t* seq_status, cudaStream_t s);
+constexpr int kNgMaxN = 16;  // longest n-gram the drafter matches
+cudaError_t launch_ngram(const int32_t* ctx, const int64_t* off, int32_t B, int32_t nmax, int32_t nmin, int32_t gamma,
+                         int32_t* draft, int32_t* n_draft, int64_t* match_pos, int32_t* match_n, cudaStream_t s);
 cudaError_t launch_adapt_gamma(const float* ema, int32_t B, int32_t gmax, float c, int64_t max_positions,
                                int32_t* gammas, int64_t* total, cudaStream_t s);
 cudaError_t launch_debug_philox(uint64_t seed, uint64_t round, uint32_t seq_offset, int32_t B, int32_t npos,

@@ -134,6 +134,13 @@ def test_host_validation_rejects_before_cuda(sv):
     assert L.spec_adapt_gamma(fake, 4, 65, 0.05, 0, fake, None, None) == sv.SPEC_ERR_INVALID_ARG
     assert L.spec_adapt_gamma(fake, 4, 8, float("nan"), 0, fake, None, None) == sv.SPEC_ERR_INVALID_ARG
     assert L.spec_adapt_gamma(fake + 2, 4, 8, 0.05, 0, fake, None, None) == sv.SPEC_ERR_ALIGNMENT
+    ng = L.spec_ngram_draft
+    assert ng(fake, None, 4, 3, 1, 8, fake, fake, None, None, None) == sv.SPEC_ERR_INVALID_ARG
+    assert ng(fake, fake, 4, 3, 0, 8, fake, fake, None, None, None) == sv.SPEC_ERR_INVALID_ARG  # n_min < 1
+    assert ng(fake, fake, 4, 2, 3, 8, fake, fake, None, None, None) == sv.SPEC_ERR_INVALID_ARG  # n_max < n_min
+    assert ng(fake, fake, 4, 17, 1, 8, fake, fake, None, None, None) == sv.SPEC_ERR_INVALID_ARG  # n_max > 16
+    assert ng(fake, fake, 4, 3, 1, 65, fake, fake, None, None, None) == sv.SPEC_ERR_INVALID_ARG  # gamma > 64
+    assert ng(fake, fake + 4, 4, 3, 1, 8, fake, fake, None, None, None) == sv.SPEC_ERR_ALIGNMENT  # ctx_off int64
     a = _args(sv)
     a.accept_ema = fake
     a.ema_lambda = 1.5  # outside [0, 1]
