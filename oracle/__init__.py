@@ -38,6 +38,7 @@ _lib = None
 
 F32, BF16 = 0, 1
 SEQ_OK, SEQ_BAD_TOKEN, SEQ_BAD_KV, SEQ_BAD_ROW, SEQ_BAD_LAYOUT, SEQ_BAD_TEMP = 0, 1, 2, 3, 4, 5
+SEQ_UNSUPPORTED = 7
 
 
 def build(force: bool = False) -> str:
@@ -69,6 +70,7 @@ class OrcArgs(ctypes.Structure):
         ("diag_acc_margin", ctypes.c_void_p), ("diag_u_smp", ctypes.c_void_p),
         ("diag_cdf_lo", ctypes.c_void_p), ("diag_cdf_hi", ctypes.c_void_p), ("diag_z", ctypes.c_void_p),
         ("top_k", ctypes.c_int32), ("top_ks", ctypes.c_void_p),
+        ("top_p", ctypes.c_float), ("top_ps", ctypes.c_void_p),
     ]
 
 
@@ -92,6 +94,8 @@ def lib():
             L.orc_normalize_row.argtypes = [vp, i32, i64, vp]
             L.orc_topk_threshold.restype = dbl
             L.orc_topk_threshold.argtypes = [vp, i32, i64, i64]
+            L.orc_topp_threshold.restype = dbl
+            L.orc_topp_threshold.argtypes = [vp, i32, i64, dbl, i32, dbl, dbl]
             L.orc_softmax_row_topk.restype = i32
             L.orc_softmax_row_topk.argtypes = [vp, i32, i64, dbl, dbl, vp]
             L.orc_normalize_row_topk.restype = i32
@@ -178,6 +182,13 @@ def topk_threshold(row: np.ndarray, k: int) -> float:
     """The k-th largest value of a row (NaN read as -inf); -inf when k <= 0 or k >= V."""
     row = np.ascontiguousarray(row)
     return float(lib().orc_topk_threshold(row.ctypes.data, _dtype_code(row), row.shape[0], int(k)))
+
+
+def topp_threshold(row: np.ndarray, T: float, tau_k: float, top_p: float, probs: bool = False) -> float:
+    """The top-p threshold over the columns >= tau_k (tau_k itself when top_p >= 1)."""
+    row = np.ascontiguousarray(row)
+    return float(lib().orc_topp_threshold(row.ctypes.data, _dtype_code(row), row.shape[0], float(T), int(probs),
+                                          float(tau_k), float(top_p)))
 
 
 def softmax_row_topk(row: np.ndarray, T: float, tau: float):
@@ -299,6 +310,7 @@ class _Call:
         kv = keep(None if w.kv_in is None else np.asarray(w.kv_in, dtype=np.int32))
         unif = keep(None if uniforms is None else np.asarray(uniforms, dtype=np.float32))
         topks = keep(None if getattr(w, "top_ks", None) is None else np.asarray(w.top_ks, dtype=np.int32))
+        topps = keep(None if getattr(w, "top_ps", None) is None else np.asarray(w.top_ps, dtype=np.float32))
         self.out_tokens = np.full(w.rows_target, -7, dtype=np.int32)
         self.out_accepted = np.full(B, -7, dtype=np.int32)
         self.kv_out = np.full(B, -7, dtype=np.int32)
@@ -327,6 +339,8 @@ class _Call:
         a.seq_status = _ptr(self.seq_status)
         a.top_k = int(getattr(w, "top_k", 0))
         a.top_ks = _ptr(topks)
+        a.top_p = float(getattr(w, "top_p", 1.0))
+        a.top_ps = _ptr(topps)
         if self.diag is not None:
             a.diag_acc_margin = _ptr(self.diag["acc_margin"])
             a.diag_u_smp = _ptr(self.diag["u_smp"])

@@ -35,7 +35,11 @@
  *   - top-k (an option of the library, applied to both models' rows alike as
  *     [P1] Implementation notes asks of any logits processing): keep every
  *     column whose value is at least the row's k-th largest (NaN ranks as
- *     -inf; ties at the threshold all stay), renormalise over the kept ones.
+ *     -inf; ties at the threshold all stay), renormalise over the kept ones;
+ *   - top-p after top-k (the same note): the nucleus of the top-k-renormalised
+ *     distribution (see orc_topp_threshold); asked for without top-k it is
+ *     reported as ORC_SEQ_UNSUPPORTED (this library computes the nucleus
+ *     only inside a top-k set).
  */
 #include <math.h>
 #include <pthread.h>
@@ -53,6 +57,7 @@
 #define ORC_SEQ_BAD_ROW 3
 #define ORC_SEQ_BAD_LAYOUT 4
 #define ORC_SEQ_BAD_TEMP 5
+#define ORC_SEQ_UNSUPPORTED 7 /* top-p asked for without top-k */
 
 /* ------------------------------------------------------------------ */
 /* Element access: bf16 is the top half of an IEEE binary32, so widening */
@@ -230,6 +235,63 @@ int32_t orc_normalize_row_topk(const void* row, int32_t dtype, int64_t V, double
     return ORC_SEQ_OK;
 }
 
+/* Top-p (nucleus) truncation after top-k, on both models' rows alike ([P1]
+ * Implementation notes: the same temperature, top-k and top-p processing).
+ * Reading: over the columns top-k kept (value >= tau_k) with weights
+ * w = exp(l/T - max(l/T)) (a probabilities row: its values), taken in
+ * decreasing value, the threshold is the value of the first group of equal
+ * values at which the cumulative weight reaches top_p times the kept total;
+ * every column at least that large stays (the whole group). top_p <= 0
+ * keeps the largest group; top_p >= 1 keeps all that top-k kept (this
+ * function then returns tau_k). Plain: copy, sort, walk. */
+typedef struct {
+    double v, w;
+} orc_vw_t;
+
+static int cmp_vw_desc(const void* x, const void* y) {
+    const double a = ((const orc_vw_t*)x)->v, b = ((const orc_vw_t*)y)->v;
+    return (a < b) - (a > b);
+}
+
+double orc_topp_threshold(const void* row, int32_t dtype, int64_t V, double T, int32_t probs, double tau_k,
+                          double top_p) {
+    if (!(top_p < 1.0)) return tau_k; /* off (and NaN) */
+    orc_vw_t* e = (orc_vw_t*)malloc(sizeof(orc_vw_t) * (size_t)(V > 0 ? V : 1));
+    int64_t n = 0;
+    double m = -INFINITY;
+    for (int64_t j = 0; j < V; ++j) {
+        const double l = orc_value(row, dtype, j);
+        if (l >= tau_k) {
+            e[n].v = l;
+            ++n;
+            if (!probs && l / T > m) m = l / T;
+        }
+    }
+    if (n == 0) {
+        free(e);
+        return tau_k;
+    }
+    qsort(e, (size_t)n, sizeof(orc_vw_t), cmp_vw_desc);
+    double S = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        e[i].w = probs ? e[i].v : exp(e[i].v / T - m);
+        S += e[i].w;
+    }
+    const double target = top_p * S;
+    double cum = 0.0, tau = e[n - 1].v;
+    for (int64_t i = 0; i < n;) {
+        int64_t k = i;
+        while (k < n && e[k].v == e[i].v) cum += e[k++].w;
+        if (cum >= target) {
+            tau = e[i].v;
+            break;
+        }
+        i = k;
+    }
+    free(e);
+    return tau;
+}
+
 /* r = max(0, p - q) elementwise; returns Z = sum r ([P1] How it works step 3;
  * [P4] residual p'(z)). */
 double orc_residual(const double* p, const double* q, int64_t V, double* r) {
@@ -319,6 +381,10 @@ typedef struct {
      * top_ks[b] if top_ks, else top_k; k_b <= 0 or k_b >= V keeps every column */
     int32_t top_k;
     const int32_t* top_ks;
+    /* top-p after top-k: p_b = top_ps[b] if top_ps, else top_p; active when
+     * p_b < 1 (NaN: off); needs top-k active for the sequence */
+    float top_p;
+    const float* top_ps;
 } orc_args_t;
 
 typedef struct {
@@ -336,6 +402,15 @@ static int64_t doff(const orc_args_t* a, int64_t b) {
 
 /* Checks that do not depend on the logits, in a fixed order: layout,
  * temperature (sampling only), draft tokens, KV length. */
+static int64_t top_k_of(const orc_args_t* a, int64_t b) { return a->top_ks ? a->top_ks[b] : a->top_k; }
+static double top_p_of(const orc_args_t* a, int64_t b) {
+    return a->top_ps ? (double)a->top_ps[b] : (double)a->top_p;
+}
+static int topk_on(const orc_args_t* a, int64_t b) {
+    const int64_t k = top_k_of(a, b);
+    return k >= 1 && k < a->vocab;
+}
+
 static int32_t precheck(const orc_args_t* a, int64_t b, int greedy, int64_t* g_out, double* T_out) {
     int64_t t0 = toff(a, b), t1 = toff(a, b + 1), d0 = doff(a, b), d1 = doff(a, b + 1);
     int64_t g = d1 - d0;
@@ -346,6 +421,7 @@ static int32_t precheck(const orc_args_t* a, int64_t b, int greedy, int64_t* g_o
     double T = a->temperatures ? (double)a->temperatures[b] : (double)a->temperature;
     *T_out = T;
     if (!greedy && (!(T > 0.0) || !isfinite(T))) return ORC_SEQ_BAD_TEMP;
+    if (!greedy && top_p_of(a, b) < 1.0 && !topk_on(a, b)) return ORC_SEQ_UNSUPPORTED;
     for (int64_t i = 0; i < g; ++i) {
         int32_t x = a->draft_tokens[d0 + i];
         if (x < 0 || x >= a->vocab) return ORC_SEQ_BAD_TOKEN;
@@ -390,20 +466,21 @@ static void uniforms_for(const orc_args_t* a, int64_t b, int64_t i, double* ua, 
     }
 }
 
-static int64_t top_k_of(const orc_args_t* a, int64_t b) { return a->top_ks ? a->top_ks[b] : a->top_k; }
 
 /* p_i of sequence b from target row trow: softmax(l / T) over the row's
  * top-k columns (every column when top-k is off). */
 static int32_t target_dist(const orc_args_t* a, int64_t b, int64_t trow, double T, double* p) {
     const void* rp = row_ptr(a->target, a->target_dtype, trow, a->vocab);
-    const double tau = orc_topk_threshold(rp, a->target_dtype, a->vocab, top_k_of(a, b));
+    double tau = orc_topk_threshold(rp, a->target_dtype, a->vocab, top_k_of(a, b));
+    tau = orc_topp_threshold(rp, a->target_dtype, a->vocab, T, 0, tau, top_p_of(a, b));
     return orc_softmax_row_topk(rp, a->target_dtype, a->vocab, T, tau, p);
 }
 
 /* q_i of sequence b from draft row drow, truncated the same way. */
 static int32_t draft_dist(const orc_args_t* a, int64_t b, int64_t drow, double T, double* q) {
     const void* rp = row_ptr(a->draft, a->draft_dtype, drow, a->vocab);
-    const double tau = orc_topk_threshold(rp, a->draft_dtype, a->vocab, top_k_of(a, b));
+    double tau = orc_topk_threshold(rp, a->draft_dtype, a->vocab, top_k_of(a, b));
+    tau = orc_topp_threshold(rp, a->draft_dtype, a->vocab, T, a->draft_is_probs, tau, top_p_of(a, b));
     if (a->draft_is_probs) return orc_normalize_row_topk(rp, a->draft_dtype, a->vocab, tau, q);
     return orc_softmax_row_topk(rp, a->draft_dtype, a->vocab, T, tau, q);
 }

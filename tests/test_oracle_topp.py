@@ -1,0 +1,142 @@
+"""Pins of the oracle's top-p (nucleus) truncation after top-k (no GPU).
+
+The threshold tau is fixed by two inequalities on the top-k-kept
+distribution: the columns at or above tau carry at least top_p of the mass,
+the columns strictly above tau carry less. The tests check those (with
+scipy's softmax for the masses), the limits, ties, the per-sequence status
+when top-k is off, and the acceptance-rate closed form on numpy-truncated
+pairs.
+"""
+import numpy as np
+import pytest
+import scipy.special
+
+from speculative_decoding_verification_38_gb300 import workloads as wl
+
+
+def _masses(vals, T, tau_k, probs):
+    kept = vals >= tau_k
+    if probs:
+        w = np.where(kept, vals, 0.0)
+    else:
+        w = scipy.special.softmax(np.where(kept, vals / T, -np.inf))
+    return w / w.sum()
+
+
+@pytest.mark.parametrize("probs", [False, True])
+def test_threshold_is_the_nucleus_boundary(orc, probs):
+    rng = np.random.default_rng(2 + probs)
+    for trial in range(60):
+        V = int(rng.integers(2, 600))
+        if probs:
+            x = rng.dirichlet(np.ones(V) * 0.3).astype(np.float32)
+        else:
+            x = (2.0 * rng.standard_normal(V)).astype(np.float32)
+        if trial % 3 == 0:
+            x = np.round(x * (4 if not probs else 400)) / (4 if not probs else 400)  # ties
+            x = x.astype(np.float32)
+        T = float(np.float32(rng.uniform(0.5, 1.5)))
+        k = int(rng.integers(1, V + 1))
+        tau_k = orc.topk_threshold(x, k)
+        for top_p in (0.0, 0.1, 0.5, 0.9, 0.99, float(np.float32(rng.random()))):
+            tau = orc.topp_threshold(x, T, tau_k, top_p, probs=probs)
+            v = x.astype(np.float64)
+            w = _masses(v, T, tau_k, probs)
+            assert tau >= tau_k
+            assert w[v >= tau].sum() >= top_p - 1e-12
+            assert w[v > tau].sum() < top_p + 1e-12 or top_p <= 0.0
+            assert np.any(v == tau)  # a value of the row
+
+
+def test_limits(orc):
+    x = np.array([3.0, 1.0, 2.0, 2.0, -1.0], np.float32)
+    assert orc.topp_threshold(x, 1.0, -np.inf, 1.0) == -np.inf  # off: top-k's threshold comes back
+    assert orc.topp_threshold(x, 1.0, 1.0, 1.5) == 1.0
+    assert orc.topp_threshold(x, 1.0, -np.inf, float("nan")) == -np.inf
+    assert orc.topp_threshold(x, 1.0, -np.inf, 0.0) == 3.0  # top_p <= 0: the largest group
+    assert orc.topp_threshold(x, 1.0, -np.inf, -2.0) == 3.0
+    # the tie group at 2.0 enters whole: 3 alone is below 0.9, 3 + both 2s reach it
+    w = scipy.special.softmax(x.astype(np.float64))
+    p = float(w[0] + w[2] + w[3] - 1e-9)
+    assert orc.topp_threshold(x, 1.0, -np.inf, p) == 2.0
+    st, q = orc.softmax_row_topk(x, 1.0, 2.0)
+    assert np.count_nonzero(q) == 3
+
+
+def _wl(tgt, dft, gammas, toks, **kw):
+    gammas = np.asarray(gammas, np.int32)
+    return wl.Workload(name="tiny-topp", batch=len(gammas), vocab=tgt.shape[1], gamma_max=int(gammas.max()),
+                       gammas=gammas, target=np.ascontiguousarray(tgt, np.float32),
+                       draft=np.ascontiguousarray(dft, np.float32), draft_tokens=np.asarray(toks, np.int32), **kw)
+
+
+def test_status_without_top_k(orc):
+    rng = np.random.default_rng(4)
+    V, g, B = 30, 3, 6
+    tgt = rng.standard_normal((B * (g + 1), V)).astype(np.float32)
+    dft = rng.standard_normal((B * g, V)).astype(np.float32)
+    toks = rng.integers(0, V, size=B * g)
+    ks = np.array([0, 5, V, 5, 0, 5], np.int32)
+    ps = np.array([0.9, 0.9, 0.5, 1.0, 1.0, np.nan], np.float32)
+    res = orc.verify_sample(_wl(tgt, dft, np.full(B, g), toks, top_ks=ks, top_ps=ps), seed=1)
+    assert res["status"].tolist() == [orc.SEQ_UNSUPPORTED, 0, orc.SEQ_UNSUPPORTED, 0, 0, 0]
+    assert np.all(res["tokens"].reshape(B, g + 1)[[0, 2]] == -1)
+    # the greedy verify ignores top-p
+    assert orc.verify_greedy(_wl(tgt, dft, np.full(B, g), toks, top_ks=ks, top_ps=ps, greedy=True))[
+        "status"].tolist() == [0] * B
+
+
+def test_position_rows_follow_the_nucleus(orc):
+    rng = np.random.default_rng(5)
+    V, g, B = 50, 2, 4
+    tgt = (2 * rng.standard_normal((B * (g + 1), V))).astype(np.float32)
+    dft = (2 * rng.standard_normal((B * g, V))).astype(np.float32)
+    toks = rng.integers(0, V, size=B * g)
+    ks = np.array([20, 49, 3, 10], np.int32)
+    ps = np.array([0.8, 0.5, 0.95, 0.3], np.float32)
+    w = _wl(tgt, dft, np.full(B, g), toks, top_ks=ks, top_ps=ps, temperature=0.7)
+    T = float(np.float32(0.7))
+    for b in range(B):
+        for i in range(g + 1):
+            st, p, q, wt, Z = orc.position_rows(w, b, i)
+            vals = tgt[b * (g + 1) + i].astype(np.float64)
+            tau_k = orc.topk_threshold(tgt[b * (g + 1) + i], int(ks[b]))
+            tau = orc.topp_threshold(tgt[b * (g + 1) + i], T, tau_k, float(ps[b]))
+            ref = scipy.special.softmax(np.where(vals >= tau, vals / T, -np.inf))
+            assert st == 0 and np.max(np.abs(p - ref)) < 1e-14
+            assert (ref[vals >= tau_k][ref[vals >= tau_k] > 0]).size <= int(ks[b]) + 5
+
+
+def test_acceptance_rate_of_nucleus_pair(orc):
+    """i.i.d. positions with top-k 8 and top-p 0.7 on both rows: the mean
+    emitted tokens follow the closed form at alpha' = sum min(p', q') of the
+    truncated pair (built here from the boundary inequalities)."""
+    rng = np.random.default_rng(6)
+    V, k, top_p, gamma, B = 12, 8, 0.7, 4, 100_000
+    p = rng.dirichlet(np.ones(V) * 0.6)
+    q = rng.dirichlet(np.ones(V) * 0.6)
+    lp = np.log(p).astype(np.float32)
+    q32 = q.astype(np.float32)
+
+    def nucleus(vals, probs):
+        tau_k = orc.topk_threshold(vals, k)
+        tau = orc.topp_threshold(vals, 1.0, tau_k, top_p, probs=probs)
+        v = vals.astype(np.float64)
+        w = _masses(v, 1.0, tau_k, probs)
+        keep = v >= tau
+        assert w[keep].sum() >= top_p and w[v > tau].sum() < top_p
+        out = np.where(keep, w, 0.0)
+        return out / out.sum()
+
+    pt, qt = nucleus(lp, False), nucleus(q32, True)
+    alpha = float(np.minimum(pt, qt).sum())
+    E = (1 - alpha ** (gamma + 1)) / (1 - alpha)
+    cq = np.cumsum(qt)
+    toks = np.minimum(np.searchsorted(cq, rng.random(B * gamma) * cq[-1], side="right"), V - 1)
+    w = _wl(np.broadcast_to(lp, (B * (gamma + 1), V)), np.broadcast_to(q32, (B * gamma, V)), np.full(B, gamma), toks,
+            draft_is_probs=True, top_k=k, top_p=top_p)
+    res = orc.verify_sample(w, seed=9, rnd=1, nthreads=8)
+    emitted = res["accepted"] + 1
+    assert abs(emitted.mean() - E) / E < 0.01, (emitted.mean(), E)
+    first = res["tokens"].reshape(B, gamma + 1)[:, 0]
+    assert np.all(np.bincount(first, minlength=V)[pt == 0] == 0)
