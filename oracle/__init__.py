@@ -185,7 +185,7 @@ def topk_threshold(row: np.ndarray, k: int) -> float:
 
 
 def topp_threshold(row: np.ndarray, T: float, tau_k: float, top_p: float, probs: bool = False) -> float:
-    """The top-p threshold over the columns >= tau_k (tau_k itself when top_p >= 1)."""
+    """The top-p threshold over the columns >= tau_k (tau_k itself unless 0 < top_p < 1)."""
     row = np.ascontiguousarray(row)
     return float(lib().orc_topp_threshold(row.ctypes.data, _dtype_code(row), row.shape[0], float(T), int(probs),
                                           float(tau_k), float(top_p)))
@@ -339,7 +339,7 @@ class _Call:
         a.seq_status = _ptr(self.seq_status)
         a.top_k = int(getattr(w, "top_k", 0))
         a.top_ks = _ptr(topks)
-        a.top_p = float(getattr(w, "top_p", 1.0))
+        a.top_p = float(getattr(w, "top_p", 0.0))
         a.top_ps = _ptr(topps)
         if self.diag is not None:
             a.diag_acc_margin = _ptr(self.diag["acc_margin"])

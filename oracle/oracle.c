@@ -241,9 +241,9 @@ int32_t orc_normalize_row_topk(const void* row, int32_t dtype, int64_t V, double
  * w = exp(l/T - max(l/T)) (a probabilities row: its values), taken in
  * decreasing value, the threshold is the value of the first group of equal
  * values at which the cumulative weight reaches top_p times the kept total;
- * every column at least that large stays (the whole group). top_p <= 0
- * keeps the largest group; top_p >= 1 keeps all that top-k kept (this
- * function then returns tau_k). Plain: copy, sort, walk. */
+ * every column at least that large stays (the whole group). Active for
+ * 0 < top_p < 1; otherwise (and for NaN) off, so that a zeroed parameter
+ * means no top-p: the function then returns tau_k. Plain: copy, sort, walk. */
 typedef struct {
     double v, w;
 } orc_vw_t;
@@ -255,7 +255,7 @@ static int cmp_vw_desc(const void* x, const void* y) {
 
 double orc_topp_threshold(const void* row, int32_t dtype, int64_t V, double T, int32_t probs, double tau_k,
                           double top_p) {
-    if (!(top_p < 1.0)) return tau_k; /* off (and NaN) */
+    if (!(top_p > 0.0 && top_p < 1.0)) return tau_k; /* off (and NaN) */
     orc_vw_t* e = (orc_vw_t*)malloc(sizeof(orc_vw_t) * (size_t)(V > 0 ? V : 1));
     int64_t n = 0;
     double m = -INFINITY;
@@ -382,7 +382,7 @@ typedef struct {
     int32_t top_k;
     const int32_t* top_ks;
     /* top-p after top-k: p_b = top_ps[b] if top_ps, else top_p; active when
-     * p_b < 1 (NaN: off); needs top-k active for the sequence */
+     * 0 < p_b < 1; needs top-k active for the sequence */
     float top_p;
     const float* top_ps;
 } orc_args_t;
@@ -421,7 +421,8 @@ static int32_t precheck(const orc_args_t* a, int64_t b, int greedy, int64_t* g_o
     double T = a->temperatures ? (double)a->temperatures[b] : (double)a->temperature;
     *T_out = T;
     if (!greedy && (!(T > 0.0) || !isfinite(T))) return ORC_SEQ_BAD_TEMP;
-    if (!greedy && top_p_of(a, b) < 1.0 && !topk_on(a, b)) return ORC_SEQ_UNSUPPORTED;
+    const double tp = top_p_of(a, b);
+    if (!greedy && tp > 0.0 && tp < 1.0 && !topk_on(a, b)) return ORC_SEQ_UNSUPPORTED;
     for (int64_t i = 0; i < g; ++i) {
         int32_t x = a->draft_tokens[d0 + i];
         if (x < 0 || x >= a->vocab) return ORC_SEQ_BAD_TOKEN;

@@ -38,13 +38,13 @@ def test_threshold_is_the_nucleus_boundary(orc, probs):
         T = float(np.float32(rng.uniform(0.5, 1.5)))
         k = int(rng.integers(1, V + 1))
         tau_k = orc.topk_threshold(x, k)
-        for top_p in (0.0, 0.1, 0.5, 0.9, 0.99, float(np.float32(rng.random()))):
+        for top_p in (1e-6, 0.1, 0.5, 0.9, 0.99, float(np.float32(rng.uniform(0.01, 0.99)))):
             tau = orc.topp_threshold(x, T, tau_k, top_p, probs=probs)
             v = x.astype(np.float64)
             w = _masses(v, T, tau_k, probs)
             assert tau >= tau_k
             assert w[v >= tau].sum() >= top_p - 1e-12
-            assert w[v > tau].sum() < top_p + 1e-12 or top_p <= 0.0
+            assert w[v > tau].sum() < top_p + 1e-12
             assert np.any(v == tau)  # a value of the row
 
 
@@ -53,8 +53,9 @@ def test_limits(orc):
     assert orc.topp_threshold(x, 1.0, -np.inf, 1.0) == -np.inf  # off: top-k's threshold comes back
     assert orc.topp_threshold(x, 1.0, 1.0, 1.5) == 1.0
     assert orc.topp_threshold(x, 1.0, -np.inf, float("nan")) == -np.inf
-    assert orc.topp_threshold(x, 1.0, -np.inf, 0.0) == 3.0  # top_p <= 0: the largest group
-    assert orc.topp_threshold(x, 1.0, -np.inf, -2.0) == 3.0
+    assert orc.topp_threshold(x, 1.0, -np.inf, 0.0) == -np.inf  # zero means off
+    assert orc.topp_threshold(x, 1.0, -np.inf, -2.0) == -np.inf
+    assert orc.topp_threshold(x, 1.0, -np.inf, 1e-9) == 3.0  # a tiny p keeps the largest group
     # the tie group at 2.0 enters whole: 3 alone is below 0.9, 3 + both 2s reach it
     w = scipy.special.softmax(x.astype(np.float64))
     p = float(w[0] + w[2] + w[3] - 1e-9)
@@ -77,7 +78,7 @@ def test_status_without_top_k(orc):
     dft = rng.standard_normal((B * g, V)).astype(np.float32)
     toks = rng.integers(0, V, size=B * g)
     ks = np.array([0, 5, V, 5, 0, 5], np.int32)
-    ps = np.array([0.9, 0.9, 0.5, 1.0, 1.0, np.nan], np.float32)
+    ps = np.array([0.9, 0.9, 0.5, 1.0, 0.0, np.nan], np.float32)
     res = orc.verify_sample(_wl(tgt, dft, np.full(B, g), toks, top_ks=ks, top_ps=ps), seed=1)
     assert res["status"].tolist() == [orc.SEQ_UNSUPPORTED, 0, orc.SEQ_UNSUPPORTED, 0, 0, 0]
     assert np.all(res["tokens"].reshape(B, g + 1)[[0, 2]] == -1)
