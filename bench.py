@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--top-k", type=int, default=0,
                     help="truncate every target and draft row to its top k (0: plain sampling, the headline)")
+    ap.add_argument("--top-p", type=float, default=0.0,
+                    help="with --top-k: also keep each row's top-p nucleus inside the top-k set (0: off)")
     ap.add_argument("--ngram", action="store_true",
                     help="time the n-gram (prompt lookup) drafter instead of the verify step")
     ap.add_argument("--adaptive", action="store_true",
@@ -63,19 +65,28 @@ KERNELS = {
               "profile": "stats_kernel_c3_dram.txt"},
     "topk": {"name": "topk_kernel (top-k threshold pass)", "sources": ("topk.cu", "common.cuh", "internal.h"),
              "profile": "topk_kernel_c3_k{k}_dram.txt"},
+    "topp": {"name": "topk_kernel (top-k threshold and top-p nucleus pass)",
+             "sources": ("topk.cu", "common.cuh", "internal.h", "precise.cuh"), "profile": "topk_kernel_c3_k{k}_p_dram.txt"},
 }
 
 
 def mode_of(args):
-    return "topk" if args.top_k > 0 else "stats"
+    if args.top_k > 0:
+        return "topp" if 0 < args.top_p < 1 else "topk"
+    return "stats"
 
 
 def metric_of(args):
-    return METRIC if args.top_k <= 0 else METRIC[:-1] + f", top-k {args.top_k})"
+    if args.top_k <= 0:
+        return METRIC
+    return METRIC[:-1] + f", top-k {args.top_k}" + (f", top-p {args.top_p}" if 0 < args.top_p < 1 else "") + ")"
 
 
 def workload_of(args):
-    return WORKLOAD if args.top_k <= 0 else WORKLOAD + f", both models truncated to top-k {args.top_k}"
+    if args.top_k <= 0:
+        return WORKLOAD
+    w = WORKLOAD + f", both models truncated to top-k {args.top_k}"
+    return w + (f" then top-p {args.top_p}" if 0 < args.top_p < 1 else "")
 
 
 def dist_env():
@@ -198,7 +209,7 @@ def run_ours(args):
     from speculative_decoding_verification_38_gb300.sharding import seq_offset
 
     mode = mode_of(args)
-    w = wl.config3(top_k=args.top_k)
+    w = wl.config3(top_k=args.top_k, top_p=args.top_p if args.top_k > 0 else 0.0)
     B = w.batch
     seq_off = seq_offset(rank, B)  # weak scaling: each rank verifies its own batch
     copies = [DeviceBatch(w, seed=0, seq_offset=seq_off) for _ in range(2)]
@@ -289,7 +300,7 @@ def run_ours(args):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded Zipf logits; no dataset)",
         "config": {"workload": workload_of(args), "batch": B, "gamma": w.gamma_max, "vocab": w.vocab,
-                   "top_k": args.top_k, "logits_dtype": "bf16",
+                   "top_k": args.top_k, "top_p": args.top_p, "logits_dtype": "bf16",
                    "parallelism": f"replicas x{world} (sequence shards)",
                    "l2": "inputs larger than L2: 279 MB per step, alternating 2 resident copies"},
         "vocab_rows_per_s": rounds_per_s * w.vocab_rows(),
@@ -503,7 +514,7 @@ def _oracle_subset(w, nseq):
                       target=w.target[:nseq * (g + 1)], draft=w.draft[:nseq * g],
                       draft_tokens=w.draft_tokens[:nseq * g], temperature=w.temperature,
                       kv_in=None if w.kv_in is None else w.kv_in[:nseq], block_size=w.block_size,
-                      top_k=w.top_k)
+                      top_k=w.top_k, top_p=w.top_p)
     return sub
 
 
@@ -531,7 +542,7 @@ def run_reference(args):
     from speculative_decoding_verification_38_gb300 import workloads as wl
 
     oracle.build()
-    w = wl.config3(top_k=args.top_k)
+    w = wl.config3(top_k=args.top_k, top_p=args.top_p if args.top_k > 0 else 0.0)
     cores = os.cpu_count() or 1
     W, K = max(3, args.warmup), max(1, args.steps)
     # size each step so the whole run stays within ~3 minutes

@@ -48,7 +48,7 @@ extern "C" {
 /* Same type as cudaStream_t; declared here so plain C callers need no CUDA header. */
 typedef struct CUstream_st* spec_stream_t;
 
-#define SPEC_ABI_VERSION 3
+#define SPEC_ABI_VERSION 4
 
 typedef enum {
     SPEC_OK = 0,
@@ -70,11 +70,13 @@ enum {
                                 logit, or (probs mode) a sum that is not > 0 */
     SPEC_SEQ_BAD_LAYOUT = 4, /* offsets of sequence b inconsistent or out of range */
     SPEC_SEQ_BAD_TEMP = 5,   /* temperature of sequence b not finite and > 0 */
-    SPEC_SEQ_TIMEOUT = 6     /* a bounded on-device wait for a copy gave up (the draw
+    SPEC_SEQ_TIMEOUT = 6,    /* a bounded on-device wait for a copy gave up (the draw
                                 is left at -1); never expected on a healthy GPU */
+    SPEC_SEQ_UNSUPPORTED = 7 /* top-p asked for without top-k (see top_p below) */
 };
-/* Precedence when several apply: LAYOUT, TEMP (sampling only), TOKEN, KV, then
- * ROW for the first bad row met while scanning positions left to right. */
+/* Precedence when several apply: LAYOUT, TEMP (sampling only), UNSUPPORTED
+ * (sampling only), TOKEN, KV, then ROW for the first bad row met while
+ * scanning positions left to right. */
 
 /*
  * Arguments of one batched verify call.
@@ -172,6 +174,21 @@ typedef struct {
      * value. Both verify calls update it. Zero-initialise both to skip it. */
     float* accept_ema; /* device [B] or NULL */
     float ema_lambda;
+
+    /* Top-p (nucleus) after top-k (sampling only; greedy ignores it):
+     * sequence b uses p_b = top_ps[b] if top_ps != NULL, else top_p; active
+     * for 0 < p_b < 1 (otherwise, and for NaN, off). Over the columns top-k
+     * kept, each row keeps the columns whose value is at least the value of
+     * the first group of equal values, in decreasing order, at which the
+     * cumulative probability reaches p_b (the whole group stays), on target
+     * and draft rows alike ("Speculative decoding" (mhtirogla.ai),
+     * Implementation notes: the same temperature, top-k and top-p
+     * processing). The masses are double-float. A sequence asking for top-p
+     * without top-k (k_b <= 0 or k_b >= V) gets SPEC_SEQ_UNSUPPORTED: the
+     * nucleus is computed only inside a top-k set. Zero-initialise both for
+     * no top-p. */
+    float top_p;
+    const float* top_ps; /* device [B] or NULL */
 } spec_verify_args_t;
 
 /* ABI version of the loaded library (SPEC_ABI_VERSION at build time). */
@@ -182,7 +199,8 @@ SPEC_API const char* spec_status_string(spec_status_t status);
 
 /* Workspace bytes a call with these arguments needs (greedy != 0 for
  * spec_verify_greedy). Reads only the host fields batch, vocab, gamma_max,
- * rows_target, rows_draft; pure host arithmetic, no CUDA call. Returns 0 if
+ * rows_target, rows_draft, top_p and top_ps (a call that may ask for top-p
+ * needs 4 KB more per row); pure host arithmetic, no CUDA call. Returns 0 if
  * those fields are out of range. */
 SPEC_API size_t spec_verify_workspace_size(const spec_verify_args_t* args, int32_t greedy);
 

@@ -28,8 +28,9 @@ SPEC_ERR_CUDA = 4
 SPEC_ERR_UNSUPPORTED = 5
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_STATIC_SCRATCH_BYTES = 8 << 20  # scratch of spec_verify_sample_static, per device
-SPEC_ABI_VERSION = 3
+SPEC_ABI_VERSION = 4
 SEQ_OK, SEQ_BAD_TOKEN, SEQ_BAD_KV, SEQ_BAD_ROW, SEQ_BAD_LAYOUT, SEQ_BAD_TEMP = 0, 1, 2, 3, 4, 5
+SEQ_TIMEOUT, SEQ_UNSUPPORTED = 6, 7
 
 
 class SpecError(RuntimeError):
@@ -75,6 +76,8 @@ class SpecVerifyArgs(ctypes.Structure):
         ("top_ks", ctypes.c_void_p),
         ("accept_ema", ctypes.c_void_p),
         ("ema_lambda", ctypes.c_float),
+        ("top_p", ctypes.c_float),
+        ("top_ps", ctypes.c_void_p),
     ]
 
 
@@ -180,9 +183,9 @@ class VerifyArgs:
                  draft_row_off=None, draft_is_probs=False, temperatures=None, temperature=1.0, seed=0, round=0,
                  seq_offset=0, uniforms=None, kv_lens_in=None, kv_lens_out=None, block_size=0,
                  out_num_blocks=None, out_tokens=None, out_accepted=None, seq_status=None, workspace=None,
-                 top_k=0, top_ks=None, accept_ema=None, ema_lambda=0.0):
+                 top_k=0, top_ks=None, accept_ema=None, ema_lambda=0.0, top_p=0.0, top_ps=None):
         for name, t in [("target", target), ("draft", draft), ("draft_tokens", draft_tokens), ("top_ks", top_ks),
-                        ("accept_ema", accept_ema),
+                        ("accept_ema", accept_ema), ("top_ps", top_ps),
                         ("target_row_off", target_row_off), ("draft_row_off", draft_row_off),
                         ("temperatures", temperatures), ("uniforms", uniforms), ("kv_lens_in", kv_lens_in),
                         ("kv_lens_out", kv_lens_out), ("out_num_blocks", out_num_blocks),
@@ -192,7 +195,7 @@ class VerifyArgs:
                             draft_row_off=draft_row_off, temperatures=temperatures, uniforms=uniforms,
                             kv_lens_in=kv_lens_in, kv_lens_out=kv_lens_out, out_num_blocks=out_num_blocks,
                             out_tokens=out_tokens, out_accepted=out_accepted, seq_status=seq_status,
-                            top_ks=top_ks, accept_ema=accept_ema)
+                            top_ks=top_ks, accept_ema=accept_ema, top_ps=top_ps)
         a = SpecVerifyArgs()
         a.struct_size = ctypes.sizeof(SpecVerifyArgs)
         a.batch = int(batch)
@@ -225,6 +228,8 @@ class VerifyArgs:
         a.top_ks = _ptr(top_ks)
         a.accept_ema = _ptr(accept_ema)
         a.ema_lambda = float(ema_lambda)
+        a.top_p = float(top_p)
+        a.top_ps = _ptr(top_ps)
         self.struct = a
         self.workspace = None
         if workspace is not None:

@@ -75,6 +75,7 @@ cudaError_t topk_with_hook(const StatsParams& p, cudaStream_t s) {
     cudaError_t e = launch_topk(p, s);
     if (e != cudaSuccess) return e;
     if (e0 && e1 && cudaEventRecord(e1, s) != cudaSuccess) return cudaErrorUnknown;
+    if (p.keep && (e = launch_nucleus(p, s)) != cudaSuccess) return e;
     return launch_finalize(p, s);
 }
 inline size_t esize(int32_t dt) { return dt == SPEC_F32 ? 4 : 2; }
@@ -115,6 +116,7 @@ spec_status_t check_call(const spec_verify_args_t* a, int greedy) {
         if (a->temperatures && !aligned(a->temperatures, 4)) return SPEC_ERR_ALIGNMENT;
         if (a->uniforms && !aligned(a->uniforms, 8)) return SPEC_ERR_ALIGNMENT;
         if (a->top_ks && !aligned(a->top_ks, 4)) return SPEC_ERR_ALIGNMENT;
+        if (a->top_ps && !aligned(a->top_ps, 4)) return SPEC_ERR_ALIGNMENT;
     }
     if (a->accept_ema && !aligned(a->accept_ema, 4)) return SPEC_ERR_ALIGNMENT;
     if (a->accept_ema && !(a->ema_lambda >= 0.f && a->ema_lambda <= 1.f)) return SPEC_ERR_INVALID_ARG;
@@ -145,16 +147,21 @@ bool tma_ok(const spec_verify_args_t* a, int greedy) {
     return true;
 }
 
-// Whether any sequence of a sampling call truncates to its top k (host
-// fields only: a per-sequence array counts as truncating).
-bool topk_on(const spec_verify_args_t* a, int greedy) {
+// Whether any sequence of a sampling call truncates its rows (top-k or
+// top-p; host fields only: a per-sequence array counts as truncating).
+bool topp_possible(const spec_verify_args_t* a, int greedy) {
+    return !greedy && (a->top_ps != nullptr || (a->top_p > 0.f && a->top_p < 1.f));
+}
+
+bool truncation_on(const spec_verify_args_t* a, int greedy) {
     if (greedy) return false;
-    return a->top_ks != nullptr || (a->top_k > 0 && a->top_k < a->vocab);
+    return a->top_ks != nullptr || (a->top_k > 0 && a->top_k < a->vocab) || a->top_ps != nullptr ||
+           (a->top_p > 0.f && a->top_p < 1.f);
 }
 
 bool build_params(const spec_verify_args_t* a, int greedy, int grid_cap, int tma, StatsParams& p, Layout& L) {
     const int pw = tma ? kTmaConsumerWarps : 1;
-    L = make_layout(a->batch, a->vocab, a->rows_target, a->rows_draft, greedy, grid_cap, pw);
+    L = make_layout(a->batch, a->vocab, a->rows_target, a->rows_draft, greedy, grid_cap, pw, topp_possible(a, greedy));
     if (a->workspace_bytes < L.total) return false;
     char* ws = (char*)a->workspace;
     p.tgt = a->target_logits;
@@ -196,9 +203,15 @@ bool build_params(const spec_verify_args_t* a, int greedy, int grid_cap, int tma
     p.row_stats = (float2*)(ws + L.off_rowstats);
     p.pq = (float2*)(ws + L.off_pq);
     p.tasks = (SampleTask*)(ws + L.off_tasks);
-    const bool tk = topk_on(a, greedy);
+    const bool tk = truncation_on(a, greedy);
     p.top_ks = tk ? a->top_ks : nullptr;
     p.top_k = tk ? a->top_k : 0;
+    p.top_ps = tk ? a->top_ps : nullptr;
+    p.top_p = tk ? a->top_p : 0.f;
+    const bool tp = tk && topp_possible(a, greedy);
+    if (tp) p.tab = exp2_table();
+    p.keep = tp ? (uint32_t*)(ws + L.off_keep) : nullptr;
+    p.keep_n = tp ? (int32_t*)(ws + L.off_keepn) : nullptr;
     p.direct = tk ? 1 : 0;
     p.tau = tk ? (float*)(ws + L.off_tau) : nullptr;
     p.ema = a->accept_ema;
@@ -264,7 +277,7 @@ SPEC_API size_t spec_verify_workspace_size(const spec_verify_args_t* a, int32_t 
     if (check_shape(a) != SPEC_OK) return 0;
     // the smallest slice any launch uses gives the most partial slots
     Layout L = make_layout(a->batch, a->vocab, a->rows_target, a->rows_draft, greedy ? 1 : 0, kGridCap,
-                           kTmaConsumerWarps);
+                           kTmaConsumerWarps, topp_possible(a, greedy ? 1 : 0));
     return L.total;
 }
 

@@ -36,6 +36,8 @@ constexpr size_t kHeaderBytes = (size_t)kMaxBatch * 4 + 256;  // arrival counter
 constexpr size_t kErrWordOffset = (size_t)kMaxBatch * 4;        // device error flags (bit 0: a wait timed out)
 
 constexpr int kSeqTimeout = 6;                                   // per-sequence status after a timed-out wait
+constexpr int kSeqUnsupported = 7;                               // per-sequence status: top-p without top-k
+constexpr int kKeepCap = 1024;  // top-k-kept values stored per row for the nucleus (top-p) kernel
 constexpr int64_t kMaxVocab = 2097152;                            // largest vocabulary (2^21 columns)
 
 enum TaskMode : int32_t { kTaskNone = 0, kTaskResidual = 1, kTaskBonus = 2 };
@@ -56,6 +58,11 @@ struct __align__(16) SampleTask {
     int32_t pad;
 };
 static_assert(sizeof(SampleTask) == 80, "task layout");
+
+// Table 2^(i/64), i = 0..63, as float pairs (value = hi + lo).
+struct Exp2Pairs {
+    float hi[64], lo[64];
+};
 
 // Everything one streaming pass (and its finalize tail) needs.
 struct StatsParams {
@@ -98,12 +105,15 @@ struct StatsParams {
     float* tau;          // [rows_total] threshold of every row (-inf: whole row), or null without top-k
     float* ema;          // [B] running acceptance (float32, updated in place), or null
     float ema_lambda;
+    // top-p after top-k (sampling only): sequence b's p_b = top_ps[b] if
+    // top_ps, else top_p; active for 0 < p_b < 1, and only with top-k active
+    const float* top_ps;
+    float top_p;
+    Exp2Pairs tab;       // 2^(i/64) for the double-float weights of the nucleus
+    uint32_t* keep;      // [rows_total * kKeepCap] keys of each top-p row's top-k-kept values, or null
+    int32_t* keep_n;     // [rows_total] their number (-1: more than kKeepCap; the row is read instead)
 };
 
-// Table 2^(i/64), i = 0..63, as float pairs (value = hi + lo).
-struct Exp2Pairs {
-    float hi[64], lo[64];
-};
 
 // One 1024-column tile of a sequence's task rows, as the sampler's first
 // phase leaves it. Values are float pairs (double-float: value = [0] + [1]).
@@ -135,12 +145,14 @@ struct SampleParams {
 struct Layout {
     int64_t rows_total, N, chunk;
     int32_t S, grid;
-    size_t off_partials, off_rowstats, off_pq, off_tasks, off_recs, off_tau, total;
+    size_t off_partials, off_rowstats, off_pq, off_tasks, off_recs, off_tau, off_keep, off_keepn, total;
 };
 
 // Work split and workspace layout for a given problem. grid_cap bounds the
 // number of streaming CTAs (the launch uses the device's resident capacity).
-Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int greedy, int64_t grid_cap, int pw);
+// topp: the call may ask for top-p (the kept-value arrays are laid out).
+Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int greedy, int64_t grid_cap, int pw,
+                   bool topp = false);
 
 cudaError_t launch_stats(const StatsParams& p, cudaStream_t s);
 // TMA variant only: the per-sequence finalize (one warp each), chained to the
@@ -151,6 +163,10 @@ int stats_resident_ctas(int device, int greedy);  // CTAs that fit at once on th
 // statistics over the kept columns into p.row_stats; replaces the streaming
 // pass when any sequence truncates (finalize then runs with p.direct = 1).
 cudaError_t launch_topk(const StatsParams& p, cudaStream_t s);
+// Top-p: each top-p row's nucleus inside its top-k set (one warp per row),
+// rewriting p.tau and the row sums; chained between launch_topk and
+// launch_finalize by programmatic launch.
+cudaError_t launch_nucleus(const StatsParams& p, cudaStream_t s);
 cudaError_t launch_sampler(const SampleParams& p, cudaStream_t s, bool pdl);
 void exp2_pairs(Exp2Pairs& t);  // host: fills the table
 cudaError_t launch_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,

@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(kDbgThreads) debug_probs_kernel(StatsParams p,
         if (out_q) out_q[j] = qv.hi;
     }
     const df Z = draftpos ? dbg_block_sum_df(df_norm(az), red) : df{1.f, 0.f};
-    const bool use_r = draftpos && df_pos(Z);
+    const bool use_r = draftpos && !residual_empty(Z);
     const df Iz = use_r ? df_recip(Z) : df{1.f, 0.f};
     if (out_w) {
         for (int64_t j = threadIdx.x; j < p.V; j += blockDim.x) {

@@ -71,6 +71,14 @@ __device__ __forceinline__ df df_recip(df a) {
 __device__ __forceinline__ bool df_gt(df a, df b) { return a.hi > b.hi || (a.hi == b.hi && a.lo > b.lo); }
 __device__ __forceinline__ bool df_pos(df a) { return a.hi > 0.f || (a.hi == 0.f && a.lo > 0.f); }
 
+// The residual's normaliser Z = sum max(0, p - q) lies in [0, 1]. When p and
+// q agree exactly (one-hot rows of the same column, say) the double-float
+// evaluation leaves a rounding residue of a few units of 2^-48 instead of 0;
+// a Z below 2^-40 is that residue, and the draw then takes p as the
+// float64 reading does for Z = 0.
+constexpr float kZeroResidual = 9.094947017729282e-13f;  // 2^-40
+__device__ __forceinline__ bool residual_empty(df Z) { return !(Z.hi > kZeroResidual); }
+
 // Running sum with the error term kept apart; normalise with df_norm.
 __device__ __forceinline__ void acc_add(df& acc, float v) {
     df s = two_sum(acc.hi, v);

@@ -564,7 +564,7 @@ __global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
         }
     }
     df Z = block_sum_df(z, sm);
-    if (resid && !df_pos(Z)) {  // p_i == q_i to rounding: draw from p_i instead
+    if (resid && residual_empty(Z)) {  // p_i == q_i to rounding: draw from p_i instead
         mode = kTaskBonus;
         cl = kEx2LightBias;
         for (int ti = t0; ti < t1; ++ti) {

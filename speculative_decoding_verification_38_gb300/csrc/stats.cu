@@ -1077,6 +1077,11 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
         kv = p.kv_in ? __ldg(p.kv_in + b) : 0;
         int32_t st = 0;
         if (!p.greedy && (!(T > 0.f) || !isfinite(T))) st = 5;  // SPEC_SEQ_BAD_TEMP
+        if (!st && !p.greedy) {  // top-p asked for without top-k
+            const float tp = p.top_ps ? __ldg(p.top_ps + b) : p.top_p;
+            const int64_t kb = p.top_ks ? (int64_t)__ldg(p.top_ks + b) : (int64_t)p.top_k;
+            if (tp > 0.f && tp < 1.f && !(kb >= 1 && kb < p.V)) st = kSeqUnsupported;
+        }
         if (!st) {
             bool bad = false;
 #pragma unroll
@@ -1228,7 +1233,8 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
 
 }  // namespace
 
-Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int greedy, int64_t grid_cap, int pw) {
+Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int greedy, int64_t grid_cap, int pw,
+                   bool topp) {
     Layout L;
     L.rows_total = rows_t + (greedy ? 0 : rows_d);
     L.N = L.rows_total * V;
@@ -1253,6 +1259,11 @@ Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int gre
     off = al(off + (greedy ? 0 : (size_t)B * ((V + kTile - 1) / kTile) * sizeof(TileRec)));
     L.off_tau = off;
     off = al(off + (greedy ? 0 : (size_t)L.rows_total * sizeof(float)));
+    const bool keep = topp && !greedy;
+    L.off_keep = off;
+    off = al(off + (keep ? (size_t)L.rows_total * kKeepCap * sizeof(uint32_t) : 0));
+    L.off_keepn = off;
+    off = al(off + (keep ? (size_t)L.rows_total * sizeof(int32_t) : 0));
     L.total = off;
     return L;
 }

@@ -25,10 +25,13 @@
 // timing). Rows where that cannot work (k past half a buffer, more equal
 // values than a buffer holds, k off) select over the row itself in L2, one
 // read per radix digit, and sum it in one more read.
+//
+// With top-p as well, a top-p row's kept values go to the workspace and a
+// second kernel (nucleus_kernel) takes the nucleus inside them, one warp per
+// row, with the loads done: the streaming pass keeps no serial tail.
 #include <math.h>
 
-#include "common.cuh"
-#include "internal.h"
+#include "precise.cuh"
 
 namespace specv {
 
@@ -51,6 +54,7 @@ struct TkSmem {
     float red[kTkWarps];
     uint32_t sel_bin, sel_above;
     uint32_t bis[2][3][kTkWarps];  // block bisection: per-warp counts, double-buffered
+    int32_t kc[kTkWarps];          // per-warp counts of kept values (top-p rows)
 };
 constexpr size_t kTkSmemBytes = sizeof(TkSmem);
 
@@ -479,13 +483,14 @@ __device__ __forceinline__ float kept_weight(float v, bool probs_row, float k2, 
 
 template <int DT>
 __device__ void row_topk(const StatsParams& p, int64_t r, const char* row, int64_t kk, bool off, bool probs_row,
-                         float k2, TkSmem& sm) {
+                         float k2, float tp, TkSmem& sm) {
     using KT = KeyTraits<DT>;
     using Bits = typename KT::Bits;
     constexpr int C = kBufBytes / KT::kEsz;
     const int64_t V = p.V;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const bool filt = !off && kk <= C / 2;
+    const bool topp = !off && tp > 0.f && tp < 1.f && p.keep;  // the nucleus kernel takes this row next
     if (threadIdx.x == 0) sm.thr_key = 0u;
     __syncthreads();
     filter_pass<DT>(row, V, (uint32_t)kk, filt, sm);
@@ -518,6 +523,31 @@ __device__ void row_topk(const StatsParams& p, int64_t r, const char* row, int64
             const float v = KT::value(wb[e]);
             if (v >= tau) acc += kept_weight(v, probs_row, k2, nmk);
         }
+        if (topp) {  // the kept values' keys for the nucleus kernel, warp by warp, in buffer order
+            int c = 0;
+            for (int e = lane; e < cnt; e += 32) c += KT::value(wb[e]) >= tau ? 1 : 0;
+            c = (int)__reduce_add_sync(kFull, (uint32_t)c);
+            if (lane == 0) sm.kc[warp] = c;
+            __syncthreads();
+            int off_w = 0, tot = 0;
+#pragma unroll
+            for (int w = 0; w < kTkWarps; ++w) {
+                off_w += w < warp ? sm.kc[w] : 0;
+                tot += sm.kc[w];
+            }
+            if (tot <= kKeepCap) {
+                uint32_t* dst = p.keep + r * kKeepCap + off_w;
+                int base = 0;
+                for (int e0 = 0; e0 < cnt; e0 += 32) {
+                    const int e = e0 + lane;
+                    const bool keep = e < cnt && KT::value(wb[e]) >= tau;
+                    const uint32_t bal = __ballot_sync(kFull, keep);
+                    if (keep) dst[base + __popc(bal & lanemask_lt())] = KT::key(wb[e]);
+                    base += __popc(bal);
+                }
+            }
+            if (threadIdx.x == 0) p.keep_n[r] = tot <= kKeepCap ? tot : -1;
+        }
     } else {
         // over the row itself (in L2 after the pass)
         if (!off) {
@@ -530,6 +560,7 @@ __device__ void row_topk(const StatsParams& p, int64_t r, const char* row, int64
             const float v = ld_elem<DT>(row, j);
             if (v >= tau) acc += kept_weight(v, probs_row, k2, nmk);
         }
+        if (topp && threadIdx.x == 0) p.keep_n[r] = -1;  // the nucleus kernel reads the row
     }
     float s = block_sum_fixed(acc, sm);
     if (threadIdx.x == 0) {
@@ -575,15 +606,142 @@ __global__ void __launch_bounds__(kTkThreads, 4) topk_kernel(StatsParams p) {
     float T = b < 0 ? 1.f : (p.temps ? __ldg(p.temps + b) : p.temperature);
     if (!(T > 0.f) || !isfinite(T)) T = 1.f;  // the finalize reports the sequence's bad temperature
     const float k2 = kLog2e / T;
+    const float tp = b < 0 ? 0.f : (p.top_ps ? __ldg(p.top_ps + b) : p.top_p);
     const int64_t esz = dt == SPECV_F32 ? 4 : 2;
     const char* row = (const char*)(is_t ? p.tgt : p.dft) + lr * p.V * esz;
     if (dt == SPECV_F32)
-        row_topk<SPECV_F32>(p, r, row, kk, off, probs_row, k2, sm);
+        row_topk<SPECV_F32>(p, r, row, kk, off, probs_row, k2, tp, sm);
     else
-        row_topk<SPECV_BF16>(p, r, row, kk, off, probs_row, k2, sm);
+        row_topk<SPECV_BF16>(p, r, row, kk, off, probs_row, k2, tp, sm);
+}
+
+// ---------------------------------------------------------------- top-p
+// The nucleus of each top-p row inside its top-k set: the largest key K
+// whose kept values at or above it carry at least top_p of the kept mass,
+// the masses double-float sums of the sampler's weights (so the boundary is
+// decided as the float64 reading decides it). One warp per row, after the
+// top-k pass: the row's kept values come from p.keep (or from the row
+// itself when they did not fit). The warp then rewrites the row's threshold
+// and its sum over the kept columns.
+constexpr int kNuThreads = 256;
+constexpr int kNuWarps = kNuThreads / 32;
+
+__device__ __forceinline__ df warp_sum_df(df v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = df_add(v, shfl_xor_df(v, o));
+    return v;
+}
+
+template <int DT>
+__device__ void row_nucleus(const StatsParams& p, int64_t r, const char* row, float T, float tp, bool probs_row,
+                            const Exp2Table& tab) {
+    using KT = KeyTraits<DT>;
+    const int lane = threadIdx.x & 31;
+    const float2 rs = __ldcg(p.row_stats + r);
+    if (!(rs.y == rs.y)) return;  // an invalid row stays invalid
+    const float m = rs.x, tk = __ldcg(p.tau + r);
+    const df kd = k_of_temperature(T);
+    const int32_t n = __ldcg(p.keep_n + r);
+    const uint32_t* kept = p.keep + r * kKeepCap;
+    auto weight = [&](float v) -> df {
+        if (probs_row) return df{v, 0.f};
+        return logit_weight<DT == SPECV_F32>(v, m, kd, tab);
+    };
+    auto visit = [&](auto&& f) {  // (key, value) of this lane's kept values
+        if (n >= 0) {
+            for (int e = lane; e < n; e += 32) {
+                const uint32_t key = __ldcg(kept + e);
+                f(key, KT::value(KT::bits_of_key(key)));
+            }
+        } else {
+            for (int64_t j = lane; j < p.V; j += 32) {
+                const float v = ld_elem<DT>(row, j);
+                if (v >= tk) f(key_of_value<DT>(v), v);
+            }
+        }
+    };
+    df S{0.f, 0.f};
+    visit([&](uint32_t, float v) { S = df_add(S, weight(v)); });
+    S = warp_sum_df(S);
+    const df target = df_mul_f(S, tp);
+    uint32_t prefix = 0;
+#pragma unroll 1
+    for (int b = 8 * KT::kDigits - 2; b >= 0; b -= 2) {
+        const uint32_t c1 = prefix | (1u << b), c2 = prefix | (2u << b), c3 = prefix | (3u << b);
+        df m1{0.f, 0.f}, m2{0.f, 0.f}, m3{0.f, 0.f};
+        visit([&](uint32_t key, float v) {
+            if (key < c1) return;
+            const df w = weight(v);
+            m1 = df_add(m1, w);
+            if (key >= c2) m2 = df_add(m2, w);
+            if (key >= c3) m3 = df_add(m3, w);
+        });
+        m1 = warp_sum_df(m1);
+        m2 = warp_sum_df(m2);
+        m3 = warp_sum_df(m3);
+        prefix = !df_gt(target, m3) ? c3 : (!df_gt(target, m2) ? c2 : (!df_gt(target, m1) ? c1 : prefix));
+    }
+    const float tau = KT::value(KT::bits_of_key(prefix));
+    // the row's sum over the nucleus, as the top-k pass sums its kept columns
+    const float k2 = kLog2e / T, nmk = -__fmul_rn(m, k2);
+    float acc = 0.f;
+    visit([&](uint32_t, float v) {
+        if (v >= tau) acc += kept_weight(v, probs_row, k2, nmk);
+    });
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(kFull, acc, o);
+    if (lane == 0) {
+        p.row_stats[r] = make_float2(rs.x, acc);
+        p.tau[r] = tau;
+    }
+}
+
+__global__ void __launch_bounds__(kNuThreads) nucleus_kernel(StatsParams p) {
+    __shared__ Exp2Table tab;
+    for (int i = threadIdx.x; i < 64; i += kNuThreads) {
+        tab.hi[i] = p.tab.hi[i];
+        tab.lo[i] = p.tab.lo[i];
+    }
+    __syncthreads();
+    pdl_launch_dependents();
+    pdl_wait_primary();
+    const int64_t r = (int64_t)blockIdx.x * kNuWarps + (threadIdx.x >> 5);
+    if (r >= p.rows_t + p.rows_d) return;
+    const bool is_t = r < p.rows_t;
+    const int64_t lr = is_t ? r : r - p.rows_t;
+    const int32_t b = row_seq(p, !is_t, lr);
+    if (b < 0) return;
+    const int64_t kk = p.top_ks ? (int64_t)__ldg(p.top_ks + b) : (int64_t)p.top_k;
+    const float tp = p.top_ps ? __ldg(p.top_ps + b) : p.top_p;
+    if (!(kk >= 1 && kk < p.V) || !(tp > 0.f && tp < 1.f)) return;  // no nucleus for this row
+    float T = p.temps ? __ldg(p.temps + b) : p.temperature;
+    if (!(T > 0.f) || !isfinite(T)) T = 1.f;  // the finalize reports the sequence's bad temperature
+    const int dt = is_t ? p.tdt : p.ddt;
+    const bool probs_row = !is_t && p.probs != 0;
+    const char* row = (const char*)(is_t ? p.tgt : p.dft) + lr * p.V * (dt == SPECV_F32 ? 4 : 2);
+    if (dt == SPECV_F32)
+        row_nucleus<SPECV_F32>(p, r, row, T, tp, probs_row, tab);
+    else
+        row_nucleus<SPECV_BF16>(p, r, row, T, tp, probs_row, tab);
 }
 
 }  // namespace
+
+cudaError_t launch_nucleus(const StatsParams& p, cudaStream_t s) {
+    const int64_t rows = p.rows_t + p.rows_d;
+    if (rows < 1) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((rows + kNuWarps - 1) / kNuWarps));
+    cfg.blockDim = dim3(kNuThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, nucleus_kernel, p);
+}
 
 cudaError_t launch_topk(const StatsParams& p, cudaStream_t s) {
     static bool attr_done = false;

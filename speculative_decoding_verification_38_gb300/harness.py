@@ -44,6 +44,8 @@ class DeviceBatch:
             np.ascontiguousarray(uniforms, dtype=np.float32)).to(dev)
         self.kv_in = None if w.kv_in is None else i32(w.kv_in)
         self.top_ks = None if w.top_ks is None else i32(w.top_ks)
+        self.top_ps = None if getattr(w, "top_ps", None) is None else torch.from_numpy(
+            np.asarray(w.top_ps, dtype=np.float32)).to(dev)
         B = w.batch
         self.kv_out = torch.full((B,), -7, dtype=torch.int32, device=dev) if self.kv_in is not None else None
         self.blocks = (torch.full((B,), -7, dtype=torch.int32, device=dev)
@@ -58,7 +60,7 @@ class DeviceBatch:
             uniforms=self.uniforms, kv_lens_in=self.kv_in, kv_lens_out=self.kv_out,
             block_size=w.block_size if self.blocks is not None else 0, out_num_blocks=self.blocks,
             out_tokens=self.out_tokens, out_accepted=self.out_accepted, seq_status=self.status,
-            top_k=w.top_k, top_ks=self.top_ks)
+            top_k=w.top_k, top_ks=self.top_ks, top_p=getattr(w, "top_p", 0.0), top_ps=self.top_ps)
         self.ws = Workspace.for_args(self.args, w.greedy, device=dev, slack=workspace_slack)
         self.args.set_workspace(self.ws)
 

@@ -169,9 +169,11 @@ def _store(x: np.ndarray, dtype: str) -> np.ndarray:
 def sampling_workload(name: str, *, config: int, batch: int, vocab: int, gammas, profile: str,
                       dtype: str, sigma, temps, kv_range=None, block_size: int = 0,
                       ragged: bool = False, pool: int = 1, dataset: int = 0,
-                      gauss_std: float = 2.0, top_k=0) -> Workload:
-    """Generic sampling-verify workload; sigma, temps and top_k are scalars or
-    [B] arrays. With top-k on, the simulated drafter samples from its top k."""
+                      gauss_std: float = 2.0, top_k=0, top_p=0.0) -> Workload:
+    """Generic sampling-verify workload; sigma, temps, top_k and top_p are
+    scalars or [B] arrays. With top-k on, the simulated drafter samples from
+    its top k (top-p is the verifier's: a draft token outside the nucleus has
+    q = 0 there)."""
     rng = _rng(config, dataset)
     gammas = np.asarray(gammas, dtype=np.int32)
     gmax = int(gammas.max()) if gammas.size else 0
@@ -221,6 +223,8 @@ def sampling_workload(name: str, *, config: int, batch: int, vocab: int, gammas,
         target_row_off=None if uniform else tro, draft_row_off=None if uniform else dro,
         info={"sigma": sig, "config": config, "dataset": dataset, "profile": profile},
         top_k=int(top_k) if ks is None else 0, top_ks=ks,
+        top_p=float(top_p) if np.ndim(top_p) == 0 else 0.0,
+        top_ps=None if np.ndim(top_p) == 0 else np.asarray(top_p, dtype=np.float32),
     )
 
 
@@ -239,16 +243,16 @@ def config2(batch=1, gamma=4, vocab=50257, pool=2000, dataset=0) -> Workload:
                              sigma=C2_SIGMA, temps=1.0, pool=pool, dataset=dataset)
 
 
-def config3(batch=64, gamma=8, vocab=128256, pool=4, dataset=0, top_k=0) -> Workload:
+def config3(batch=64, gamma=8, vocab=128256, pool=4, dataset=0, top_k=0, top_p=0.0) -> Workload:
     """Sampling, B=64, gamma=8, V=128256, bf16, Zipf, sigma_b ~ U[0.2,1.5], T=0.8
     (top_k > 0: the same rows, both models truncated to their top k)."""
     rng = _rng(30, dataset)
     sig = rng.uniform(0.2, 1.5, size=batch).astype(np.float32)
-    name = "C3 sample B64 g8 V128256 bf16" + (f" top-k {top_k}" if top_k else "")
+    name = "C3 sample B64 g8 V128256 bf16" + (f" top-k {top_k}" if top_k else "") + (f" top-p {top_p}" if top_p else "")
     return sampling_workload(name, config=3, batch=batch, vocab=vocab,
                              gammas=np.full(batch, gamma), profile="zipf", dtype="bf16",
                              sigma=sig, temps=0.8, kv_range=(512, 4096), block_size=16,
-                             pool=pool, dataset=dataset, top_k=top_k)
+                             pool=pool, dataset=dataset, top_k=top_k, top_p=top_p)
 
 
 def config5(batch=512, gamma_max=8, vocab=128256, pool=2, dataset=0) -> Workload:

@@ -62,7 +62,7 @@ def test_struct_layout_matches_header(sv):
 
 
 def test_abi_version_and_status_strings(sv):
-    assert sv.spec_abi_version() == 3 == sv.SPEC_ABI_VERSION
+    assert sv.spec_abi_version() == 4 == sv.SPEC_ABI_VERSION
     assert sv.spec_status_string(0) == "SPEC_OK"
     assert sv.spec_status_string(3) == "SPEC_ERR_WORKSPACE"
 

@@ -1,0 +1,117 @@
+"""GPU parity of top-p (nucleus) after top-k against the float64 oracle:
+per-sequence p with off values, both dtypes and odd vocabularies, the
+row path (large k, ties), probability drafts, the truncated distributions
+within 1e-5 with the same kept columns, the unsupported status, and the
+benchmarked workload at k = 50, p = 0.9."""
+import numpy as np
+import pytest
+
+import oracle
+from speculative_decoding_verification_38_gb300 import workloads as wl
+from tests.test_gpu_parity import _harness, run_rounds, sv  # noqa: F401  (fixture)
+from tests.test_gpu_topk import _tied_workload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V", [33, 3001, 16411])
+def test_topp_ragged_small(sv, dtype, V):
+    rng = np.random.default_rng(700 + V)
+    B = 21
+    gam = rng.integers(0, 9, size=B)
+    gam[0], gam[-1] = 0, 8
+    ks = rng.integers(1, max(2, min(V, 300)), size=B).astype(np.int32)
+    ps = rng.uniform(0.05, 0.99, size=B).astype(np.float32)
+    ps[:5] = [0.0, 1.0, np.nan, 1e-6, 0.999]
+    w = wl.sampling_workload(f"topp V{V}", config=390, batch=B, vocab=V, gammas=gam, profile="zipf",
+                             dtype=dtype, sigma=rng.uniform(0.2, 2.0, B), temps=rng.uniform(0.5, 1.5, B),
+                             kv_range=(8, 5000), block_size=16, ragged=True, pool=3, dataset=V, top_k=ks, top_p=ps)
+    run_rounds(w, range(8), seed=13, seq_offset=2, label=f"top-p ragged V={V} {dtype}")
+
+
+@pytest.mark.parametrize("k,p", [(50, 0.9), (1000, 0.5), (200, 0.99)])
+def test_topp_scalar(sv, k, p):
+    w = wl.sampling_workload(f"topp k{k} p{p}", config=391, batch=12, vocab=32000, gammas=np.full(12, 4),
+                             profile="zipf", dtype="bf16", sigma=0.6, temps=0.9, pool=4, top_k=k, top_p=p)
+    run_rounds(w, range(8), seed=5, label=f"top-k={k} top-p={p}")
+
+
+@pytest.mark.parametrize("dtype,k", [("bf16", 1500), ("f32", 700)])
+def test_topp_row_path(sv, dtype, k):
+    w = wl.sampling_workload(f"topp big k{k}", config=392, batch=6, vocab=40_009, gammas=[3, 1, 4, 0, 2, 5],
+                             profile="gaussian", dtype=dtype, sigma=0.5, temps=1.0, ragged=True, pool=3,
+                             top_k=k, top_p=0.8)
+    run_rounds(w, range(6), seed=6, label=f"top-p row path k={k} {dtype}")
+
+
+def test_topp_heavy_ties(sv):
+    w = _tied_workload("bf16", 300)
+    w.top_p = 0.6
+    run_rounds(w, range(4), seed=8, label="top-p ties")
+
+
+def test_topp_probs_draft(sv):
+    rng = np.random.default_rng(33)
+    B, g, V = 8, 4, 6007
+    base = wl.sampling_workload("probs", config=394, batch=B, vocab=V, gammas=np.full(B, g), profile="zipf",
+                                dtype="f32", sigma=0.7, temps=1.0, pool=2, top_k=40)
+    dvals = wl.stored_f32(base.draft)
+    probs = np.exp(dvals - dvals.max(axis=1, keepdims=True)).astype(np.float32)
+    probs *= rng.uniform(0.5, 3.0, size=(probs.shape[0], 1)).astype(np.float32)
+    w = wl.Workload(name="probs top-p", batch=B, vocab=V, gamma_max=g, gammas=base.gammas,
+                    target=wl.bf16_bits(wl.stored_f32(base.target)), draft=probs, draft_tokens=base.token_pool[0],
+                    token_pool=base.token_pool, draft_is_probs=True, temperature=1.0,
+                    top_ks=np.array([40, 1, 7, 40, 200, 3, 100, 60], np.int32),
+                    top_ps=np.array([0.9, 0.5, 0.0, 0.3, 0.95, 0.99, 0.7, 1e-4], np.float32))
+    run_rounds(w, range(10), seed=4, label="probs draft top-p")
+
+
+def test_topp_unsupported_status(sv):
+    rng = np.random.default_rng(3)
+    B = 8
+    w = wl.sampling_workload("topp status", config=395, batch=B, vocab=3001, gammas=np.full(B, 3), profile="zipf",
+                             dtype="bf16", sigma=0.5, temps=1.0, pool=2,
+                             top_k=np.array([0, 5, 3001, 5, 0, 5, -1, 10], np.int32),
+                             top_p=np.array([0.9, 0.9, 0.5, 1.0, 0.0, np.nan, 0.2, 0.5], np.float32))
+    run_rounds(w, range(2), seed=3, label="top-p status")
+    DeviceBatch = _harness()
+    db = DeviceBatch(w, seed=3)
+    db.run()
+    st = db.results()["status"]
+    assert st.tolist() == [7, 0, 7, 0, 0, 0, 7, 0]
+
+
+def test_topp_debug_probs_within_1e5(sv):
+    import torch
+
+    DeviceBatch = _harness()
+    rng = np.random.default_rng(23)
+    B = 5
+    gam = np.array([3, 0, 5, 1, 2])
+    w = wl.sampling_workload("dbg top-p", config=396, batch=B, vocab=5003, gammas=gam, profile="zipf", dtype="bf16",
+                             sigma=rng.uniform(0.2, 2.0, B), temps=rng.uniform(0.5, 1.5, B), ragged=True, pool=1,
+                             top_k=np.array([50, 1, 300, 20, 2], np.int32),
+                             top_p=np.array([0.9, 0.5, 0.3, 0.0, 0.99], np.float32))
+    db = DeviceBatch(w, seed=3)
+    db.run(rnd=1)
+    V = w.vocab
+    op, oq, ow = (torch.zeros(V, device="cuda") for _ in range(3))
+    sc = torch.zeros(4, device="cuda")
+    for b in range(B):
+        for pos in range(gam[b] + 1):
+            sv.check(sv.spec_debug_probs(db.args, b, pos, op, oq, ow, sc), "debug_probs")
+            st, p, q, wts, Z = oracle.position_rows(w, b, pos, draft_tokens=w.draft_tokens)
+            assert st == 0
+            gp, gq, gw, gs = (t.cpu().numpy().astype(np.float64) for t in (op, oq, ow, sc))
+            assert np.array_equal(gp > 0, p > 0) and np.array_equal(gq > 0, q > 0)  # the same nucleus
+            assert np.max(np.abs(gp - p)) < 1e-5 and np.max(np.abs(gq - q)) < 1e-5
+            assert np.max(np.abs(gw - wts / wts.sum())) < 1e-5
+            if pos < gam[b]:
+                _, px, qx = oracle.accept_terms(w, b, pos, draft_tokens=w.draft_tokens)
+                assert abs(gs[0] - px) < 1e-5 and abs(gs[1] - qx) < 1e-5
+
+
+def test_topp_config3_full_size(sv):
+    w = wl.config3(top_k=50, top_p=0.9)
+    run_rounds(w, range(8), seed=0, label="C3 top-k 50 top-p 0.9")
