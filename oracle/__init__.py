@@ -74,6 +74,21 @@ class OrcArgs(ctypes.Structure):
     ]
 
 
+class OrcTreeArgs(ctypes.Structure):
+    _fields_ = [
+        ("batch", ctypes.c_int32), ("vocab", ctypes.c_int32), ("greedy", ctypes.c_int32),
+        ("node_off", ctypes.c_void_p), ("parent", ctypes.c_void_p), ("tokens", ctypes.c_void_p),
+        ("target", ctypes.c_void_p), ("target_dtype", ctypes.c_int32),
+        ("draft", ctypes.c_void_p), ("draft_dtype", ctypes.c_int32), ("draft_is_probs", ctypes.c_int32),
+        ("temperatures", ctypes.c_void_p), ("temperature", ctypes.c_float),
+        ("seed", ctypes.c_uint64), ("round", ctypes.c_uint64), ("seq_offset", ctypes.c_uint32),
+        ("out_tokens", ctypes.c_void_p), ("out_accepted", ctypes.c_void_p), ("out_path", ctypes.c_void_p),
+        ("seq_status", ctypes.c_void_p),
+        ("diag_acc_margin", ctypes.c_void_p), ("diag_u_smp", ctypes.c_void_p),
+        ("diag_cdf_lo", ctypes.c_void_p), ("diag_cdf_hi", ctypes.c_void_p),
+    ]
+
+
 def lib():
     global _lib
     with _lock:
@@ -110,6 +125,8 @@ def lib():
             L.orc_adapt_gamma.argtypes = [vp, i64, i32, ctypes.c_float, i64, vp]
             L.orc_ngram_draft.restype = None
             L.orc_ngram_draft.argtypes = [vp, vp, i64, i32, i32, i32, vp, vp, vp, vp]
+            L.orc_tree_verify.restype = None
+            L.orc_tree_verify.argtypes = [ctypes.POINTER(OrcTreeArgs)]
             L.orc_residual.restype = dbl
             L.orc_residual.argtypes = [vp, vp, i64, vp]
             L.orc_inverse_cdf.restype = i64
@@ -252,6 +269,45 @@ def ngram_draft(ctx, ctx_off, n_max: int, n_min: int, gamma: int):
     lib().orc_ngram_draft(c.ctypes.data, off.ctypes.data, B, int(n_max), int(n_min), int(gamma), draft.ctypes.data,
                           nd.ctypes.data, pos.ctypes.data, mn.ctypes.data)
     return {"draft": draft[:B * gamma].reshape(B, gamma), "n_draft": nd, "match_pos": pos, "match_n": mn}
+
+
+def tree_verify(w, *, seed=0, rnd=0, seq_offset=0, greedy=None, parent=None, tokens=None, diagnostics=False):
+    """Tree verification of a workloads.TreeWorkload (float64; one thread)."""
+    N, B = w.nodes, w.batch
+    keep = []
+
+    def arr(a, dt):
+        a = np.ascontiguousarray(a, dtype=dt)
+        keep.append(a)
+        return a
+
+    off = arr(w.node_off, np.int64)
+    par = arr(w.parent if parent is None else parent, np.int32)
+    tok = arr(w.tokens if tokens is None else tokens, np.int32)
+    tgt = np.ascontiguousarray(w.target)
+    dft = np.ascontiguousarray(w.draft)
+    temps = None if w.temperatures is None else arr(w.temperatures, np.float32)
+    out = {"tokens": np.full(N, -7, np.int32), "accepted": np.full(B, -7, np.int32),
+           "path": np.full(N, -7, np.int32), "status": np.full(B, -7, np.int32)}
+    diag = {k: np.full(B, np.nan) for k in ("acc_margin", "u_smp", "cdf_lo", "cdf_hi")} if diagnostics else None
+    a = OrcTreeArgs()
+    a.batch, a.vocab = B, w.vocab
+    a.greedy = int(w.greedy if greedy is None else greedy)
+    a.node_off, a.parent, a.tokens = off.ctypes.data, par.ctypes.data, tok.ctypes.data
+    a.target, a.target_dtype = tgt.ctypes.data, _dtype_code(tgt)
+    a.draft, a.draft_dtype = dft.ctypes.data, _dtype_code(dft)
+    a.draft_is_probs = int(w.draft_is_probs)
+    a.temperatures = _ptr(temps)
+    a.temperature = float(w.temperature)
+    a.seed, a.round, a.seq_offset = int(seed) & (2**64 - 1), int(rnd) & (2**64 - 1), int(seq_offset)
+    a.out_tokens, a.out_accepted = out["tokens"].ctypes.data, out["accepted"].ctypes.data
+    a.out_path, a.seq_status = out["path"].ctypes.data, out["status"].ctypes.data
+    if diag is not None:
+        a.diag_acc_margin, a.diag_u_smp = diag["acc_margin"].ctypes.data, diag["u_smp"].ctypes.data
+        a.diag_cdf_lo, a.diag_cdf_hi = diag["cdf_lo"].ctypes.data, diag["cdf_hi"].ctypes.data
+        out["diag"] = diag
+    lib().orc_tree_verify(ctypes.byref(a))
+    return out
 
 
 def residual(p: np.ndarray, q: np.ndarray):

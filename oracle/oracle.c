@@ -811,3 +811,168 @@ void orc_ngram_draft(const int32_t* ctx, const int64_t* ctx_off, int64_t B, int3
         if (match_n) match_n[b] = nbest;
     }
 }
+
+/* ------------------------------------------------------------ tree verify
+ * Verification of a token tree in one pass: several candidate continuations
+ * per node ("Speculative decoding" (mhtirogla.ai), Levers and Implementation
+ * notes: tree speculation, verify several candidates with a tree attention
+ * mask; "Speculative decoding" (inference.tusharamrit.in), tree attention).
+ * The pages give no multi-candidate acceptance rule; the reading (the
+ * residual taken per node, the pages' single-draft rule applied to each
+ * candidate in turn):
+ *   - sequence b's tree has nodes 0..N_b-1, node 0 the root (the last
+ *     context token), every other node a drafted token whose parent has a
+ *     smaller index; the children of a node, in index order, are its
+ *     candidates, drawn from q_u, the draft distribution at that node; p_u is
+ *     the target's distribution after the path to node u (one target row and
+ *     one draft row per node);
+ *   - at node u with candidates c_1..c_m: r = p_u; candidate j with token x
+ *     passes if u_acc(u, j) * q_u(x) < r(x), and the walk moves to c_j; else
+ *     r becomes max(0, r - q_u) / Z (kept as it is if Z = 0) and the next
+ *     candidate is tried. If all fail, the token is drawn from r with
+ *     u_smp(u) (inverse CDF in index order, as the chain); at a node without
+ *     children, from p_u (the bonus);
+ *   - uniforms: u_acc(u, j) = word 0 of Philox4x32-10 at counter
+ *     (u + j * 65536, seq_offset + b, round lo, round hi), u_smp(u) = word 1
+ *     at counter (u, ...): a chain (one child per node) draws exactly what
+ *     the chain verify draws;
+ *   - greedy: the walk moves to the first child whose token is the target's
+ *     argmax at the node (first index, NaN read as -inf), else emits that
+ *     argmax and stops.
+ * Outputs per sequence: out_tokens[off .. off + a] the a accepted tokens
+ * then the emitted one, -1 after (up to N_b slots); out_path[off .. off+a)
+ * the accepted nodes, -1 after; out_accepted[b] = a. Statuses as the chain:
+ * layout (node offsets, N_b >= 1, parents), temperature, tokens, rows. */
+typedef struct {
+    int32_t batch, vocab, greedy;
+    const int64_t* node_off;
+    const int32_t* parent;
+    const int32_t* tokens;
+    const void* target;
+    int32_t target_dtype;
+    const void* draft;
+    int32_t draft_dtype, draft_is_probs;
+    const float* temperatures;
+    float temperature;
+    uint64_t seed, round;
+    uint32_t seq_offset;
+    int32_t* out_tokens;
+    int32_t* out_accepted;
+    int32_t* out_path;
+    int32_t* seq_status;
+    double* diag_acc_margin; /* per sequence: min |u_acc - r(x)/q(x)| over the tests made */
+    double* diag_u_smp;      /* u of the final draw */
+    double* diag_cdf_lo;     /* normalised CDF edges of the emitted token */
+    double* diag_cdf_hi;
+} orc_tree_args_t;
+
+static void tree_uniforms(const orc_tree_args_t* a, int64_t b, int64_t u, int64_t j, double* ua, double* us) {
+    double x, y;
+    orc_uniform_pair(a->seed, a->round, (uint32_t)(a->seq_offset + b), (uint32_t)(u + j * 65536), &x, &y);
+    *ua = x;
+    if (us) *us = y;
+}
+
+static void tree_write_error(const orc_tree_args_t* a, int64_t b, int32_t st) {
+    const int64_t o = a->node_off[b], n = a->node_off[b + 1] - o;
+    if (st != ORC_SEQ_BAD_LAYOUT)
+        for (int64_t k = 0; k < n; ++k) {
+            a->out_tokens[o + k] = -1;
+            if (a->out_path) a->out_path[o + k] = -1;
+        }
+    a->out_accepted[b] = 0;
+    if (a->seq_status) a->seq_status[b] = st;
+}
+
+static void tree_one(const orc_tree_args_t* a, int64_t b, double* p, double* q, double* r, double* t) {
+    const int64_t V = a->vocab, o = a->node_off[b], N = a->node_off[b + 1] - o;
+    if (N < 1 || o < 0 || a->parent[o] != -1) { tree_write_error(a, b, ORC_SEQ_BAD_LAYOUT); return; }
+    for (int64_t v = 1; v < N; ++v)
+        if (a->parent[o + v] < 0 || a->parent[o + v] >= v) { tree_write_error(a, b, ORC_SEQ_BAD_LAYOUT); return; }
+    const double T = a->temperatures ? (double)a->temperatures[b] : (double)a->temperature;
+    if (!a->greedy && (!(T > 0.0) || !isfinite(T))) { tree_write_error(a, b, ORC_SEQ_BAD_TEMP); return; }
+    for (int64_t v = 1; v < N; ++v)
+        if (a->tokens[o + v] < 0 || a->tokens[o + v] >= V) { tree_write_error(a, b, ORC_SEQ_BAD_TOKEN); return; }
+    int64_t u = 0, acc = 0;
+    double margin = INFINITY;
+    for (;;) {
+        const void* trow = row_ptr(a->target, a->target_dtype, o + u, V);
+        if (a->greedy) {
+            const int64_t g = orc_argmax_row(trow, a->target_dtype, V);
+            int64_t next = -1;
+            for (int64_t v = u + 1; v < N && next < 0; ++v)
+                if (a->parent[o + v] == u && a->tokens[o + v] == g) next = v;
+            if (next < 0) { a->out_tokens[o + acc] = (int32_t)g; break; }
+            a->out_tokens[o + acc] = (int32_t)g;
+            if (a->out_path) a->out_path[o + acc] = (int32_t)next;
+            ++acc;
+            u = next;
+            continue;
+        }
+        int32_t st = orc_softmax_row(trow, a->target_dtype, V, T, p);
+        if (st) { tree_write_error(a, b, st); return; }
+        int has_child = 0;
+        for (int64_t v = u + 1; v < N; ++v) has_child |= a->parent[o + v] == u;
+        double us;
+        if (!has_child) { /* the bonus token from p_u */
+            double ua;
+            tree_uniforms(a, b, u, 0, &ua, &us);
+            const int64_t tok = orc_inverse_cdf(p, V, us);
+            a->out_tokens[o + acc] = (int32_t)tok;
+            if (a->diag_u_smp) a->diag_u_smp[b] = us;
+            if (a->diag_cdf_lo && a->diag_cdf_hi) orc_cdf_edges(p, V, tok, &a->diag_cdf_lo[b], &a->diag_cdf_hi[b]);
+            break;
+        }
+        const void* drow = row_ptr(a->draft, a->draft_dtype, o + u, V);
+        st = a->draft_is_probs ? orc_normalize_row(drow, a->draft_dtype, V, q)
+                               : orc_softmax_row(drow, a->draft_dtype, V, T, q);
+        if (st) { tree_write_error(a, b, st); return; }
+        for (int64_t k = 0; k < V; ++k) r[k] = p[k];
+        int64_t next = -1, j = 0;
+        for (int64_t v = u + 1; v < N && next < 0; ++v) {
+            if (a->parent[o + v] != u) continue;
+            const int32_t x = a->tokens[o + v];
+            double ua;
+            tree_uniforms(a, b, u, j, &ua, NULL);
+            if (q[x] > 0.0) {
+                const double dm = fabs(ua - r[x] / q[x]);
+                if (dm < margin) margin = dm;
+            }
+            if (ua * q[x] < r[x]) {
+                next = v;
+                break;
+            }
+            const double Z = orc_residual(r, q, V, t);
+            if (Z > 0.0)
+                for (int64_t k = 0; k < V; ++k) r[k] = t[k] / Z;
+            ++j;
+        }
+        if (next >= 0) {
+            a->out_tokens[o + acc] = a->tokens[o + next];
+            if (a->out_path) a->out_path[o + acc] = (int32_t)next;
+            ++acc;
+            u = next;
+            continue;
+        }
+        double ua0;
+        tree_uniforms(a, b, u, 0, &ua0, &us);
+        const int64_t tok = orc_inverse_cdf(r, V, us);
+        a->out_tokens[o + acc] = (int32_t)tok;
+        if (a->diag_u_smp) a->diag_u_smp[b] = us;
+        if (a->diag_cdf_lo && a->diag_cdf_hi) orc_cdf_edges(r, V, tok, &a->diag_cdf_lo[b], &a->diag_cdf_hi[b]);
+        break;
+    }
+    for (int64_t k = acc + 1; k < N; ++k) a->out_tokens[o + k] = -1;
+    if (a->out_path)
+        for (int64_t k = acc; k < N; ++k) a->out_path[o + k] = -1;
+    a->out_accepted[b] = (int32_t)acc;
+    if (a->diag_acc_margin) a->diag_acc_margin[b] = margin;
+    if (a->seq_status) a->seq_status[b] = ORC_SEQ_OK;
+}
+
+void orc_tree_verify(const orc_tree_args_t* a) {
+    const int64_t V = a->vocab;
+    double* p = (double*)malloc(sizeof(double) * (size_t)V * 4);
+    for (int64_t b = 0; b < a->batch; ++b) tree_one(a, b, p, p + V, p + 2 * V, p + 3 * V);
+    free(p);
+}

@@ -331,4 +331,80 @@ def ngram_contexts(batch=64, doc_len=4096, gen_len=1024, vocab=128256, span=(8, 
     return np.concatenate(out).astype(np.int32), off
 
 
+@dataclass
+class TreeWorkload:
+    """Token trees to verify: sequence b owns nodes node_off[b] .. node_off[b+1]
+    (node 0 of each the root, the last context token); parent[n] is the
+    parent's local index (-1 for a root), tokens[n] the drafted token; one
+    target row and one draft row per node (p and q after that node's path)."""
+    name: str
+    batch: int
+    vocab: int
+    node_off: np.ndarray
+    parent: np.ndarray
+    tokens: np.ndarray
+    target: np.ndarray
+    draft: np.ndarray
+    draft_is_probs: bool = False
+    temperatures: np.ndarray | None = None
+    temperature: float = 1.0
+    greedy: bool = False
+    info: dict = field(default_factory=dict)
+
+    @property
+    def nodes(self) -> int:
+        return int(self.node_off[-1])
+
+
+def tree_shape(rng, branching, depth):
+    """Parents (local indices, node 0 the root) of a tree whose nodes at depth
+    d < depth have branching[d] children, the children of a node listed
+    together, nodes in breadth-first order."""
+    parent = [-1]
+    level = [0]
+    for d in range(depth):
+        nxt = []
+        for u in level:
+            for _ in range(int(branching[d])):
+                parent.append(u)
+                nxt.append(len(parent) - 1)
+        level = nxt
+    return np.asarray(parent, np.int32)
+
+
+def tree_workload(name, *, config, batch, vocab, branching, dtype="bf16", sigma=0.6, temps=1.0, profile="zipf",
+                  dataset=0, greedy_agree=None) -> TreeWorkload:
+    """Trees of the given per-depth branching for every sequence; target rows
+    Zipf (or Gaussian) logits per node, draft rows = target + N(0, sigma^2).
+    Each node's children are drafted i.i.d. (with replacement) from the
+    draft's softmax(q / T) at their parent by the Gumbel-max trick, the
+    drafter simulation of the chain workloads. With greedy_agree, a child
+    copies the target's argmax at its parent with that probability instead."""
+    rng = _rng(70 + config, dataset)
+    shape = tree_shape(rng, branching, len(branching))
+    n = shape.shape[0]
+    N = batch * n
+    tgt = zipf_rows(rng, N, vocab) if profile == "zipf" else (2.0 * rng.standard_normal((N, vocab))).astype(np.float32)
+    dft = (tgt + np.float32(sigma) * rng.standard_normal((N, vocab), dtype=np.float32)).astype(np.float32)
+    target, draft = _store(tgt, dtype), _store(dft, dtype)
+    tv, dv = stored_f32(target), stored_f32(draft)
+    T = np.broadcast_to(np.asarray(temps, np.float32), (batch,)).astype(np.float32)
+    parent = np.tile(shape, batch)
+    node_off = np.arange(batch + 1, dtype=np.int64) * n
+    tokens = np.full(N, -1, np.int32)
+    for b in range(batch):
+        o = b * n
+        for v in range(1, n):
+            u = o + shape[v]
+            if greedy_agree is not None and rng.random() < greedy_agree:
+                tokens[o + v] = int(np.argmax(tv[u]))
+            else:
+                g = rng.gumbel(size=vocab).astype(np.float32)
+                tokens[o + v] = int(np.argmax(dv[u] / T[b] + g))
+    return TreeWorkload(name=name, batch=batch, vocab=vocab, node_off=node_off, parent=parent, tokens=tokens,
+                        target=target, draft=draft, temperatures=None if np.ndim(temps) == 0 else T,
+                        temperature=float(temps) if np.ndim(temps) == 0 else 1.0,
+                        info={"branching": list(branching), "config": config})
+
+
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}
