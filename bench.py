@@ -53,6 +53,8 @@ def parse():
                     help="with --top-k: also keep each row's top-p nucleus inside the top-k set (0: off)")
     ap.add_argument("--ngram", action="store_true",
                     help="time the n-gram (prompt lookup) drafter instead of the verify step")
+    ap.add_argument("--tree", action="store_true",
+                    help="time tree verification (64 trees of branching 4, 2, 2) instead of the chain verify")
     ap.add_argument("--adaptive", action="store_true",
                     help="each step also updates the running acceptance and chooses the next gamma on the GPU")
     return ap.parse_args()
@@ -458,6 +460,140 @@ def run_ngram(args):
     print(json.dumps(out), flush=True)
 
 
+TREE_SHAPE = dict(batch=64, vocab=128256, branching=[4, 2, 2], dtype="bf16", sigma=0.6, temps=0.8)
+TREE_METRIC = "tree verify rounds/s (B=64 trees of 29 nodes, branching 4-2-2, V=128256, bf16 logits)"
+TREE_WORKLOAD = ("token trees: B=64, branching (4, 2, 2) = 29 nodes per tree, V=128256 bf16, T=0.8; Zipf target "
+                 "logits per node, draft = target + N(0, 0.6^2), children drafted i.i.d. from the draft at the parent")
+
+
+def tree_read_bytes(w, res, row_bytes):
+    """Rows the walk must read once: the target row of every visited node
+    (the root and the accepted path) and the draft row of each visited node
+    that has children."""
+    total = 0
+    off = w.node_off
+    for b in range(w.batch):
+        o, n = int(off[b]), int(off[b + 1] - off[b])
+        par = w.parent[o:o + n]
+        visited = [0] + [int(v) for v in res["path"][o:o + n] if v >= 0]
+        has_kids = set(int(x) for x in par[1:])
+        total += sum(row_bytes * (2 if u in has_kids else 1) for u in visited)
+    return total
+
+
+def run_tree(args):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import speculative_decoding_verification_38_gb300 as sv
+    from speculative_decoding_verification_38_gb300 import workloads as wl
+    from speculative_decoding_verification_38_gb300.harness import DeviceTree
+
+    w = wl.tree_workload("bench tree", config=20, **TREE_SHAPE)
+    dt = DeviceTree(w, seed=0)
+    copies = 4  # 4 x 952 MB resident: consecutive steps read different copies, none left in L2
+    tgts = [dt.target] + [dt.target.clone() for _ in range(copies - 1)]
+    dfts = [dt.draft] + [dt.draft.clone() for _ in range(copies - 1)]
+    arg_sets = []
+    for c in range(copies):
+        dt.target, dt.draft = tgts[c], dfts[c]
+        arg_sets.append([dt.args(rnd) for rnd in range(1)][0])
+    dt.target, dt.draft = tgts[0], dfts[0]
+
+    def step(i):
+        a = arg_sets[i % copies]
+        a.round = i
+        sv.check(sv.spec_tree_verify(a, False), "tree verify")
+
+    W, K = max(3, args.warmup), max(1, min(args.steps, 4000))
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+    clk = ClockSampler(0)
+    clk.start()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(K):
+        step(W + i)
+    e1.record()
+    torch.cuda.synchronize()
+    rows = clk.stop()
+    ms = e0.elapsed_time(e1)
+    # the rows each timed round's walk read, from the same rounds replayed
+    row_bytes = w.vocab * 2
+    read = 0
+    for i in range(K):
+        step(W + i)
+        read += tree_read_bytes(w, dt.results(), row_bytes)
+    per_launch = read / K
+    peak, peak_kind = measured_hbm_peak()
+    achieved = per_launch / (ms / K / 1e3) / 1e9
+    # end to end: every step copies the trees in from pinned host memory and reads the outputs back
+    host_t, host_d = tgts[0].cpu().pin_memory(), dfts[0].cpu().pin_memory()
+    host_meta = [x.cpu().pin_memory() for x in (dt.node_off, dt.parent, dt.tokens)]
+    out_h = [torch.empty_like(x, device="cpu").pin_memory() for x in
+             (dt.out_tokens, dt.out_path, dt.out_accepted, dt.status)]
+    h2d = host_t.numel() * 2 + host_d.numel() * 2 + sum(x.numel() * x.element_size() for x in host_meta)
+    d2h = sum(x.numel() * 4 for x in out_h)
+    n_e2e = max(3, min(args.e2e_steps, 30))
+
+    def one(i):
+        tgts[0].copy_(host_t, non_blocking=True)
+        dfts[0].copy_(host_d, non_blocking=True)
+        for d, h in zip((dt.node_off, dt.parent, dt.tokens), host_meta):
+            d.copy_(h, non_blocking=True)
+        a = arg_sets[0]
+        a.round = i
+        sv.check(sv.spec_tree_verify(a, False), "tree verify")
+        for h, d in zip(out_h, (dt.out_tokens, dt.out_path, dt.out_accepted, dt.status)):
+            h.copy_(d, non_blocking=True)
+
+    for i in range(3):
+        one(i)
+    torch.cuda.synchronize()
+    e0.record()
+    for i in range(n_e2e):
+        one(i)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    acc = dt.results()["accepted"]
+    out = {
+        "metric": TREE_METRIC, "value": K / (ms / 1e3), "unit": "rounds/s", "n_gpus": 1, "steps": K, "warmup": W,
+        "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32x2",
+        "data": "synthetic (seeded Zipf logits and drafted trees; no dataset)",
+        "config": {"workload": TREE_WORKLOAD, "batch": w.batch, "nodes_per_tree": int(w.node_off[1]),
+                   "vocab": w.vocab, "logits_dtype": "bf16",
+                   "l2": "4 resident copies of the 952 MB rows, rotated (inputs larger than L2)",
+                   "mean_accepted": float(np.mean(acc))},
+        "gpu_launches": K,
+        "roofline": {"bound": "latency", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None, "kernel": "tree_kernel", "kernel_ms": ms / K,
+                     "algorithmic_bytes_per_launch": per_launch,
+                     "note": "bytes = rows the walks must read once (visited nodes' target rows, draft rows of "
+                             "visited nodes with children); one CTA per tree walks node by node",
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        "clocks": ClockSampler.summarize(rows),
+        "e2e": {"value": n_e2e / (e2e_ms / 1e3), "unit": "rounds/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+    }
+    if args.cpu_seconds > 0:
+        import oracle
+
+        oracle.build()
+        t0, n = time.time(), 0
+        while time.time() - t0 < args.cpu_seconds and n < 50:
+            oracle.tree_verify(w, seed=0, rnd=n)
+            n += 1
+        el = time.time() - t0
+        out["cpu_baseline"] = {"value": n / el, "unit": "rounds/s", "cores": 1, "kind": "oracle",
+                               "sample": f"{n} full rounds of the same 64 trees, float64 C oracle, one thread"}
+    print(json.dumps(out), flush=True)
+
+
 def run_e2e(db, w, args, sv):
     """Same metric through the C ABI with inputs in pinned host memory: every
     step copies that step's inputs host -> device, verifies, and reads the
@@ -576,6 +712,8 @@ def main():
         run_reference(args)
     elif args.ngram:
         run_ngram(args)
+    elif args.tree:
+        run_tree(args)
     else:
         run_ours(args)
 

@@ -48,7 +48,7 @@ extern "C" {
 /* Same type as cudaStream_t; declared here so plain C callers need no CUDA header. */
 typedef struct CUstream_st* spec_stream_t;
 
-#define SPEC_ABI_VERSION 4
+#define SPEC_ABI_VERSION 5
 
 typedef enum {
     SPEC_OK = 0,
@@ -72,7 +72,9 @@ enum {
     SPEC_SEQ_BAD_TEMP = 5,   /* temperature of sequence b not finite and > 0 */
     SPEC_SEQ_TIMEOUT = 6,    /* a bounded on-device wait for a copy gave up (the draw
                                 is left at -1); never expected on a healthy GPU */
-    SPEC_SEQ_UNSUPPORTED = 7 /* top-p asked for without top-k (see top_p below) */
+    SPEC_SEQ_UNSUPPORTED = 7 /* top-p asked for without top-k (see top_p below); for
+                                spec_tree_verify, a visited node with more than
+                                SPEC_TREE_MAX_CANDIDATES children */
 };
 /* Precedence when several apply: LAYOUT, TEMP (sampling only), UNSUPPORTED
  * (sampling only), TOKEN, KV, then ROW for the first bad row met while
@@ -292,6 +294,68 @@ SPEC_API spec_status_t spec_adapt_gamma(const float* accept_ema, int32_t batch, 
 SPEC_API spec_status_t spec_ngram_draft(const int32_t* ctx, const int64_t* ctx_off, int32_t batch, int32_t n_max,
                                         int32_t n_min, int32_t gamma, int32_t* draft_out, int32_t* n_draft_out,
                                         int64_t* match_pos_out, int32_t* match_n_out, spec_stream_t stream);
+
+/* Tree verification: several candidate continuations per position checked
+ * in one target pass ("Speculative decoding" (mhtirogla.ai), Levers and
+ * Implementation notes: tree speculation with a tree attention mask;
+ * "Speculative decoding" (inference.tusharamrit.in), tree attention). The
+ * pages give no rule for several candidates; this library takes the pages'
+ * single-draft rule at every candidate in turn, with the residual carried
+ * over:
+ *   - sequence b owns nodes node_off[b] .. node_off[b+1) (N_b of them);
+ *     local node 0 is the root (the last context token, parent -1), every
+ *     other node v holds a drafted token tokens[v] and a parent in [0, v)
+ *     (local indices); a node's children, in index order, are its
+ *     candidates, drawn from the draft distribution q_u at that node;
+ *   - target row o+u holds the target's logits after the path to node u
+ *     (p_u), draft row o+u the draft's (q_u; probabilities if draft_is_probs);
+ *   - sampling, at node u: r = p_u; candidate j (token x) passes if
+ *     u_acc(u, j) * q_u(x) < r(x) and the walk moves to it; else r becomes
+ *     max(0, r - q_u) / Z (left as it is if Z = 0) and the next candidate
+ *     is tried; if none passes, the emitted token is drawn from r with
+ *     u_smp(u) by inverse CDF in index order; a node without children emits
+ *     the bonus token drawn from p_u. u_acc(u, j) = word 0 of Philox4x32-10
+ *     at counter (u + 65536 j, seq_offset + b, round lo, round hi), u_smp(u) =
+ *     word 1 at counter (u, ...), each (w >> 8) 2^-24: a chain-shaped tree
+ *     draws what spec_verify_sample draws for the same chain;
+ *   - greedy: the walk moves to the first child whose token is the target's
+ *     argmax at the node (first index, NaN read as -inf), else emits it.
+ * Outputs (device): out_tokens[node_off[b] + i] = the accepted tokens, then
+ * the emitted one, -1 after (N_b slots); out_path (may be NULL) the accepted
+ * nodes' local indices, -1 after; out_accepted[b] = their number;
+ * seq_status[b] (may be NULL). Statuses, in this order: LAYOUT (N_b < 1,
+ * offsets outside [0, nodes], a bad parent; the sequence's slots are not
+ * written), TEMP (sampling), TOKEN (a node token outside [0, V)), then,
+ * walking (sampling): UNSUPPORTED (a visited node with more than
+ * SPEC_TREE_MAX_CANDIDATES children), ROW (the visited node's target row,
+ * then its draft row if it has children). */
+#define SPEC_TREE_MAX_CANDIDATES 64
+typedef struct {
+    uint32_t struct_size;        /* sizeof(spec_tree_args_t), for ABI checks */
+    int32_t batch;               /* 1 <= batch <= 65536 */
+    int32_t vocab;               /* 1 <= V <= 2097152 */
+    int64_t nodes;               /* rows of parent, tokens, target, draft; <= 2^31 - 1 */
+    const int64_t* node_off;     /* device [batch + 1] */
+    const int32_t* parent;       /* device [nodes] */
+    const int32_t* tokens;       /* device [nodes] (the root's entry is not read) */
+    const void* target;          /* device [nodes, V], target_dtype */
+    int32_t target_dtype;        /* spec_dtype_t */
+    const void* draft;           /* device [nodes, V], draft_dtype (sampling; may be NULL for greedy) */
+    int32_t draft_dtype;
+    int32_t draft_is_probs;      /* 1: draft rows are probabilities, used divided by their sum */
+    const float* temperatures;   /* device [batch] or NULL: then temperature */
+    float temperature;
+    uint64_t seed, round;
+    uint32_t seq_offset;
+    int32_t* out_tokens;         /* device [nodes] */
+    int32_t* out_accepted;       /* device [batch] */
+    int32_t* out_path;           /* device [nodes] or NULL */
+    int32_t* seq_status;         /* device [batch] or NULL */
+} spec_tree_args_t;
+
+/* One launch, no workspace; greedy != 0 selects the greedy walk. Pointers
+ * must be aligned to their element types (target/draft rows to their dtype). */
+SPEC_API spec_status_t spec_tree_verify(const spec_tree_args_t* args, int32_t greedy, spec_stream_t stream);
 
 /* KV-length rollback alone, e.g. for the draft model's cache ("Speculative
  * decoding" (mhtirogla.ai), How it works step 5: truncate the length in both

@@ -77,6 +77,7 @@ class OrcArgs(ctypes.Structure):
 class OrcTreeArgs(ctypes.Structure):
     _fields_ = [
         ("batch", ctypes.c_int32), ("vocab", ctypes.c_int32), ("greedy", ctypes.c_int32),
+        ("nodes", ctypes.c_int64),
         ("node_off", ctypes.c_void_p), ("parent", ctypes.c_void_p), ("tokens", ctypes.c_void_p),
         ("target", ctypes.c_void_p), ("target_dtype", ctypes.c_int32),
         ("draft", ctypes.c_void_p), ("draft_dtype", ctypes.c_int32), ("draft_is_probs", ctypes.c_int32),
@@ -291,7 +292,7 @@ def tree_verify(w, *, seed=0, rnd=0, seq_offset=0, greedy=None, parent=None, tok
            "path": np.full(N, -7, np.int32), "status": np.full(B, -7, np.int32)}
     diag = {k: np.full(B, np.nan) for k in ("acc_margin", "u_smp", "cdf_lo", "cdf_hi")} if diagnostics else None
     a = OrcTreeArgs()
-    a.batch, a.vocab = B, w.vocab
+    a.batch, a.vocab, a.nodes = B, w.vocab, min(par.shape[0], tok.shape[0], tgt.shape[0], dft.shape[0])
     a.greedy = int(w.greedy if greedy is None else greedy)
     a.node_off, a.parent, a.tokens = off.ctypes.data, par.ctypes.data, tok.ctypes.data
     a.target, a.target_dtype = tgt.ctypes.data, _dtype_code(tgt)

@@ -842,9 +842,14 @@ void orc_ngram_draft(const int32_t* ctx, const int64_t* ctx_off, int64_t B, int3
  * Outputs per sequence: out_tokens[off .. off + a] the a accepted tokens
  * then the emitted one, -1 after (up to N_b slots); out_path[off .. off+a)
  * the accepted nodes, -1 after; out_accepted[b] = a. Statuses as the chain:
- * layout (node offsets, N_b >= 1, parents), temperature, tokens, rows. */
+ * layout (node offsets within [0, nodes], N_b >= 1, parents), temperature,
+ * tokens, rows. The boundary keeps at most ORC_TREE_MAX_CAND candidates per
+ * node for the sampling walk: a visited node with more gives the sequence
+ * ORC_SEQ_UNSUPPORTED (checked on arrival, before the node's rows). */
+#define ORC_TREE_MAX_CAND 64
 typedef struct {
     int32_t batch, vocab, greedy;
+    int64_t nodes; /* rows of parent / tokens / target / draft */
     const int64_t* node_off;
     const int32_t* parent;
     const int32_t* tokens;
@@ -886,7 +891,7 @@ static void tree_write_error(const orc_tree_args_t* a, int64_t b, int32_t st) {
 
 static void tree_one(const orc_tree_args_t* a, int64_t b, double* p, double* q, double* r, double* t) {
     const int64_t V = a->vocab, o = a->node_off[b], N = a->node_off[b + 1] - o;
-    if (N < 1 || o < 0 || a->parent[o] != -1) { tree_write_error(a, b, ORC_SEQ_BAD_LAYOUT); return; }
+    if (N < 1 || o < 0 || o + N > a->nodes || a->parent[o] != -1) { tree_write_error(a, b, ORC_SEQ_BAD_LAYOUT); return; }
     for (int64_t v = 1; v < N; ++v)
         if (a->parent[o + v] < 0 || a->parent[o + v] >= v) { tree_write_error(a, b, ORC_SEQ_BAD_LAYOUT); return; }
     const double T = a->temperatures ? (double)a->temperatures[b] : (double)a->temperature;
@@ -909,10 +914,12 @@ static void tree_one(const orc_tree_args_t* a, int64_t b, double* p, double* q, 
             u = next;
             continue;
         }
+        int64_t n_child = 0;
+        for (int64_t v = u + 1; v < N; ++v) n_child += a->parent[o + v] == u;
+        if (n_child > ORC_TREE_MAX_CAND) { tree_write_error(a, b, ORC_SEQ_UNSUPPORTED); return; }
         int32_t st = orc_softmax_row(trow, a->target_dtype, V, T, p);
         if (st) { tree_write_error(a, b, st); return; }
-        int has_child = 0;
-        for (int64_t v = u + 1; v < N; ++v) has_child |= a->parent[o + v] == u;
+        const int has_child = n_child > 0;
         double us;
         if (!has_child) { /* the bonus token from p_u */
             double ua;

@@ -28,9 +28,10 @@ SPEC_ERR_CUDA = 4
 SPEC_ERR_UNSUPPORTED = 5
 SPEC_F32, SPEC_BF16 = 0, 1
 SPEC_STATIC_SCRATCH_BYTES = 8 << 20  # scratch of spec_verify_sample_static, per device
-SPEC_ABI_VERSION = 4
+SPEC_ABI_VERSION = 5
 SEQ_OK, SEQ_BAD_TOKEN, SEQ_BAD_KV, SEQ_BAD_ROW, SEQ_BAD_LAYOUT, SEQ_BAD_TEMP = 0, 1, 2, 3, 4, 5
 SEQ_TIMEOUT, SEQ_UNSUPPORTED = 6, 7
+SPEC_TREE_MAX_CANDIDATES = 64
 
 
 class SpecError(RuntimeError):
@@ -81,6 +82,34 @@ class SpecVerifyArgs(ctypes.Structure):
     ]
 
 
+class SpecTreeArgs(ctypes.Structure):
+    """Mirror of spec_tree_args_t (include/spec_verify.h)."""
+
+    _fields_ = [
+        ("struct_size", ctypes.c_uint32),
+        ("batch", ctypes.c_int32),
+        ("vocab", ctypes.c_int32),
+        ("nodes", ctypes.c_int64),
+        ("node_off", ctypes.c_void_p),
+        ("parent", ctypes.c_void_p),
+        ("tokens", ctypes.c_void_p),
+        ("target", ctypes.c_void_p),
+        ("target_dtype", ctypes.c_int32),
+        ("draft", ctypes.c_void_p),
+        ("draft_dtype", ctypes.c_int32),
+        ("draft_is_probs", ctypes.c_int32),
+        ("temperatures", ctypes.c_void_p),
+        ("temperature", ctypes.c_float),
+        ("seed", ctypes.c_uint64),
+        ("round", ctypes.c_uint64),
+        ("seq_offset", ctypes.c_uint32),
+        ("out_tokens", ctypes.c_void_p),
+        ("out_accepted", ctypes.c_void_p),
+        ("out_path", ctypes.c_void_p),
+        ("seq_status", ctypes.c_void_p),
+    ]
+
+
 _lib = None
 _lock = threading.Lock()
 
@@ -121,6 +150,8 @@ def lib():
             L.spec_adapt_gamma.argtypes = [vp, i32, i32, ctypes.c_float, i64, vp, vp, vp]
             L.spec_ngram_draft.restype = ctypes.c_int
             L.spec_ngram_draft.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp, vp]
+            L.spec_tree_verify.restype = ctypes.c_int
+            L.spec_tree_verify.argtypes = [ctypes.POINTER(SpecTreeArgs), i32, vp]
             L.spec_kv_rollback.restype = ctypes.c_int
             L.spec_kv_rollback.argtypes = [vp, vp, vp, vp, i32, i32, i32, vp, vp, vp]
             L.spec_debug_philox.restype = ctypes.c_int
@@ -330,6 +361,38 @@ def spec_ngram_draft(ctx, ctx_off, n_max: int, n_min: int, gamma: int, draft_out
     return lib().spec_ngram_draft(_ptr(ctx) if ctx is not None and ctx.numel() else None, ctx_off.data_ptr(),
                                   int(ctx_off.numel() - 1), int(n_max), int(n_min), int(gamma), draft_out.data_ptr(),
                                   n_draft_out.data_ptr(), _ptr(match_pos_out), _ptr(match_n_out), _stream(stream))
+
+
+def tree_args(*, node_off, parent, tokens, target, draft=None, draft_is_probs=False, temperatures=None,
+              temperature=1.0, seed=0, rnd=0, seq_offset=0, out_tokens, out_accepted, out_path=None,
+              seq_status=None) -> SpecTreeArgs:
+    """spec_tree_args_t over device tensors: node_off int64 [B+1]; parent,
+    tokens int32 [nodes]; target (and draft) [nodes, V] float32 or bfloat16."""
+    for name, t in [("node_off", node_off), ("parent", parent), ("tokens", tokens), ("target", target),
+                    ("draft", draft), ("temperatures", temperatures), ("out_tokens", out_tokens),
+                    ("out_accepted", out_accepted), ("out_path", out_path), ("seq_status", seq_status)]:
+        _check_dev(t, name)
+    a = SpecTreeArgs()
+    a.struct_size = ctypes.sizeof(SpecTreeArgs)
+    a.batch = int(node_off.numel() - 1)
+    a.vocab = int(target.shape[1])
+    a.nodes = int(target.shape[0])
+    a.node_off, a.parent, a.tokens = node_off.data_ptr(), parent.data_ptr(), tokens.data_ptr()
+    a.target, a.target_dtype = target.data_ptr(), _dtype_code(target)
+    if draft is not None:
+        a.draft, a.draft_dtype = draft.data_ptr(), _dtype_code(draft)
+    a.draft_is_probs = int(bool(draft_is_probs))
+    a.temperatures = _ptr(temperatures)
+    a.temperature = float(temperature)
+    a.seed, a.round, a.seq_offset = int(seed) & (2**64 - 1), int(rnd) & (2**64 - 1), int(seq_offset)
+    a.out_tokens, a.out_accepted = out_tokens.data_ptr(), out_accepted.data_ptr()
+    a.out_path, a.seq_status = _ptr(out_path), _ptr(seq_status)
+    return a
+
+
+def spec_tree_verify(args: SpecTreeArgs, greedy: bool = False, stream=None) -> int:
+    """Verify every sequence's token tree in one launch (see tree_args)."""
+    return lib().spec_tree_verify(ctypes.byref(args), int(bool(greedy)), _stream(stream))
 
 
 def spec_verify_greedy(args: VerifyArgs, stream=None) -> int:

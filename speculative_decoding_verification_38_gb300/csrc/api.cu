@@ -374,6 +374,52 @@ SPEC_API spec_status_t spec_ngram_draft(const int32_t* ctx, const int64_t* ctx_o
     return SPEC_OK;
 }
 
+SPEC_API spec_status_t spec_tree_verify(const spec_tree_args_t* a, int32_t greedy, spec_stream_t stream) {
+    if (!a || a->struct_size != sizeof(spec_tree_args_t)) return SPEC_ERR_INVALID_ARG;
+    if (a->batch < 1 || a->batch > kMaxBatch || a->vocab < 1) return SPEC_ERR_INVALID_ARG;
+    if ((int64_t)a->vocab > kMaxVocab) return SPEC_ERR_UNSUPPORTED;
+    if (a->nodes < a->batch || a->nodes > INT32_MAX) return SPEC_ERR_INVALID_ARG;
+    if (!a->node_off || !a->parent || !a->tokens || !a->target || !a->out_tokens || !a->out_accepted)
+        return SPEC_ERR_INVALID_ARG;
+    if (a->target_dtype != SPEC_F32 && a->target_dtype != SPEC_BF16) return SPEC_ERR_INVALID_ARG;
+    if (!aligned(a->node_off, 8) || !aligned(a->parent, 4) || !aligned(a->tokens, 4) ||
+        !aligned(a->target, esize(a->target_dtype)) || !aligned(a->out_tokens, 4) || !aligned(a->out_accepted, 4))
+        return SPEC_ERR_ALIGNMENT;
+    if ((a->out_path && !aligned(a->out_path, 4)) || (a->seq_status && !aligned(a->seq_status, 4)))
+        return SPEC_ERR_ALIGNMENT;
+    if (!greedy) {
+        if (!a->draft || (a->draft_dtype != SPEC_F32 && a->draft_dtype != SPEC_BF16)) return SPEC_ERR_INVALID_ARG;
+        if (a->draft_is_probs != 0 && a->draft_is_probs != 1) return SPEC_ERR_INVALID_ARG;
+        if (!aligned(a->draft, esize(a->draft_dtype))) return SPEC_ERR_ALIGNMENT;
+        if (a->temperatures && !aligned(a->temperatures, 4)) return SPEC_ERR_ALIGNMENT;
+    }
+    TreeParams p{};
+    p.B = a->batch;
+    p.greedy = greedy ? 1 : 0;
+    p.V = a->vocab;
+    p.nodes = a->nodes;
+    p.node_off = a->node_off;
+    p.parent = a->parent;
+    p.tokens = a->tokens;
+    p.tgt = a->target;
+    p.dft = greedy ? nullptr : a->draft;
+    p.tdt = a->target_dtype;
+    p.ddt = a->draft_dtype;
+    p.probs = a->draft_is_probs;
+    p.temps = a->temperatures;
+    p.temperature = a->temperature;
+    p.seed = a->seed;
+    p.round = a->round;
+    p.seq_offset = a->seq_offset;
+    p.out_tokens = a->out_tokens;
+    p.out_accepted = a->out_accepted;
+    p.out_path = a->out_path;
+    p.seq_status = a->seq_status;
+    p.tab = exp2_table();
+    if (launch_tree(p, (cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
 SPEC_API spec_status_t spec_debug_philox(uint64_t seed, uint64_t round, uint32_t seq_offset, int32_t batch,
                                          int32_t npos, float* out, spec_stream_t stream) {
     if (!out || batch < 1 || npos < 1 || !aligned(out, 4)) return SPEC_ERR_INVALID_ARG;

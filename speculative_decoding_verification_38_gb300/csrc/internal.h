@@ -175,6 +175,27 @@ cudaError_t launch_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int3
 constexpr int kNgMaxN = 16;  // longest n-gram the drafter matches
 cudaError_t launch_ngram(const int32_t* ctx, const int64_t* off, int32_t B, int32_t nmax, int32_t nmin, int32_t gamma,
                          int32_t* draft, int32_t* n_draft, int64_t* match_pos, int32_t* match_n, cudaStream_t s);
+// Tree verification: one CTA per sequence walks its token tree.
+struct TreeParams {
+    int32_t B, greedy;
+    int64_t V, nodes;
+    const int64_t* node_off;  // [B+1]
+    const int32_t* parent;    // [nodes] local parent index, -1 for a root
+    const int32_t* tokens;    // [nodes]
+    const void* tgt;          // [nodes, V]
+    const void* dft;          // [nodes, V] (sampling)
+    int32_t tdt, ddt, probs;
+    const float* temps;
+    float temperature;
+    uint64_t seed, round;
+    uint32_t seq_offset;
+    int32_t* out_tokens;      // [nodes]
+    int32_t* out_accepted;    // [B]
+    int32_t* out_path;        // [nodes] or null
+    int32_t* seq_status;      // [B] or null
+    Exp2Pairs tab;
+};
+cudaError_t launch_tree(const TreeParams& p, cudaStream_t s);
 cudaError_t launch_adapt_gamma(const float* ema, int32_t B, int32_t gmax, float c, int64_t max_positions,
                                int32_t* gammas, int64_t* total, cudaStream_t s);
 cudaError_t launch_debug_philox(uint64_t seed, uint64_t round, uint32_t seq_offset, int32_t B, int32_t npos,

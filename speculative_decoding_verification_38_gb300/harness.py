@@ -2,7 +2,8 @@
 
 DeviceBatch uploads one workloads.Workload to the GPU once, allocates the
 outputs and the caller-owned workspace, and issues verify calls through the C
-ABI (spec_verify_sample / spec_verify_greedy). Nothing here computes any part
+ABI (spec_verify_sample / spec_verify_greedy); DeviceTree does the same for a
+workloads.TreeWorkload and spec_tree_verify. Nothing here computes any part
 of the verify.
 """
 from __future__ import annotations
@@ -10,8 +11,9 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import (SpecError, VerifyArgs, Workspace, check, spec_verify_greedy, spec_verify_sample)
-from .workloads import Workload
+from . import (SpecError, VerifyArgs, Workspace, check, spec_tree_verify, spec_verify_greedy, spec_verify_sample,
+               tree_args)
+from .workloads import TreeWorkload, Workload
 
 
 def to_device_rows(a: np.ndarray, device) -> torch.Tensor:
@@ -86,4 +88,45 @@ class DeviceBatch:
         return out
 
 
-__all__ = ["DeviceBatch", "to_device_rows", "SpecError"]
+class DeviceTree:
+    """A TreeWorkload on the device with its outputs; run() is one
+    spec_tree_verify launch over every sequence's tree."""
+
+    def __init__(self, w: TreeWorkload, device="cuda", seed: int = 0, seq_offset: int = 0):
+        self.w = w
+        self.device = dev = torch.device(device)
+        i32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)  # noqa: E731
+        self.node_off = torch.from_numpy(np.ascontiguousarray(w.node_off, dtype=np.int64)).to(dev)
+        self.parent = i32(w.parent)
+        self.tokens = i32(w.tokens)
+        self.target = to_device_rows(w.target, dev)
+        self.draft = None if (w.greedy or w.draft is None) else to_device_rows(w.draft, dev)
+        self.temps = None if w.temperatures is None else torch.from_numpy(
+            np.asarray(w.temperatures, dtype=np.float32)).to(dev)
+        n = self.target.shape[0]
+        self.out_tokens = torch.full((n,), -7, dtype=torch.int32, device=dev)
+        self.out_path = torch.full((n,), -7, dtype=torch.int32, device=dev)
+        self.out_accepted = torch.full((w.batch,), -7, dtype=torch.int32, device=dev)
+        self.status = torch.full((w.batch,), -7, dtype=torch.int32, device=dev)
+        self.seed, self.seq_offset = seed, seq_offset
+
+    def args(self, rnd: int = 0):
+        return tree_args(node_off=self.node_off, parent=self.parent, tokens=self.tokens, target=self.target,
+                         draft=self.draft, draft_is_probs=self.w.draft_is_probs, temperatures=self.temps,
+                         temperature=self.w.temperature, seed=self.seed, rnd=rnd, seq_offset=self.seq_offset,
+                         out_tokens=self.out_tokens, out_accepted=self.out_accepted, out_path=self.out_path,
+                         seq_status=self.status)
+
+    def call(self, rnd: int = 0, stream=None, args=None) -> int:
+        return spec_tree_verify(args if args is not None else self.args(rnd), self.w.greedy, stream)
+
+    def run(self, rnd: int = 0, stream=None):
+        check(self.call(rnd, stream), "tree verify")
+
+    def results(self) -> dict:
+        torch.cuda.synchronize(self.device)
+        return {"tokens": self.out_tokens.cpu().numpy(), "accepted": self.out_accepted.cpu().numpy(),
+                "path": self.out_path.cpu().numpy(), "status": self.status.cpu().numpy()}
+
+
+__all__ = ["DeviceBatch", "DeviceTree", "to_device_rows", "SpecError"]

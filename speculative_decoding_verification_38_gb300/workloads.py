@@ -34,8 +34,13 @@ C2_SIGMA = 0.4853515625
 def bf16_bits(x) -> np.ndarray:
     """float32 -> bfloat16 bit patterns, round to nearest even (NaN kept quiet)."""
     x = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
-    u = x.view(np.uint32).astype(np.uint64)
-    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    # uint32 arithmetic: u + 0x8000 overflows only for NaN patterns, set below
+    u = x.view(np.uint32)
+    t = (u >> 16) & 1
+    t += 0x7FFF
+    t += u
+    t >>= 16
+    r = t.astype(np.uint16)
     nan = np.isnan(x)
     if nan.any():
         r[nan] = 0x7FC0
@@ -372,39 +377,60 @@ def tree_shape(rng, branching, depth):
     return np.asarray(parent, np.int32)
 
 
-def tree_workload(name, *, config, batch, vocab, branching, dtype="bf16", sigma=0.6, temps=1.0, profile="zipf",
-                  dataset=0, greedy_agree=None) -> TreeWorkload:
-    """Trees of the given per-depth branching for every sequence; target rows
-    Zipf (or Gaussian) logits per node, draft rows = target + N(0, sigma^2).
-    Each node's children are drafted i.i.d. (with replacement) from the
-    draft's softmax(q / T) at their parent by the Gumbel-max trick, the
-    drafter simulation of the chain workloads. With greedy_agree, a child
-    copies the target's argmax at its parent with that probability instead."""
-    rng = _rng(70 + config, dataset)
-    shape = tree_shape(rng, branching, len(branching))
-    n = shape.shape[0]
-    N = batch * n
+def _tree_batch(name, rng, shapes, *, vocab, dtype, sigma, temps, profile, greedy_agree, info):
+    """Rows and drafted tokens for trees of the given parent arrays (one per
+    sequence): target rows Zipf (or Gaussian) logits per node, draft rows =
+    target + N(0, sigma^2); each node's children drafted i.i.d. (with
+    replacement) from the draft's softmax(q / T) at their parent by the
+    Gumbel-max trick, or, with greedy_agree, a copy of the target's argmax
+    at the parent with that probability."""
+    batch = len(shapes)
+    sizes = np.array([s.shape[0] for s in shapes], np.int64)
+    node_off = np.concatenate([[0], np.cumsum(sizes)]).astype(np.int64)
+    N = int(node_off[-1])
     tgt = zipf_rows(rng, N, vocab) if profile == "zipf" else (2.0 * rng.standard_normal((N, vocab))).astype(np.float32)
     dft = (tgt + np.float32(sigma) * rng.standard_normal((N, vocab), dtype=np.float32)).astype(np.float32)
     target, draft = _store(tgt, dtype), _store(dft, dtype)
     tv, dv = stored_f32(target), stored_f32(draft)
     T = np.broadcast_to(np.asarray(temps, np.float32), (batch,)).astype(np.float32)
-    parent = np.tile(shape, batch)
-    node_off = np.arange(batch + 1, dtype=np.int64) * n
+    parent = np.concatenate(shapes).astype(np.int32)
     tokens = np.full(N, -1, np.int32)
-    for b in range(batch):
-        o = b * n
-        for v in range(1, n):
-            u = o + shape[v]
-            if greedy_agree is not None and rng.random() < greedy_agree:
-                tokens[o + v] = int(np.argmax(tv[u]))
-            else:
-                g = rng.gumbel(size=vocab).astype(np.float32)
-                tokens[o + v] = int(np.argmax(dv[u] / T[b] + g))
+    seq = np.repeat(np.arange(batch), sizes)
+    kids = np.nonzero(parent >= 0)[0]
+    at = node_off[seq[kids]] + parent[kids]  # each drafted node's parent row
+    agree = (rng.random(kids.size) < greedy_agree) if greedy_agree is not None else np.zeros(kids.size, bool)
+    tokens[kids[agree]] = np.argmax(tv[at[agree]], axis=1) if agree.any() else []
+    rest = np.nonzero(~agree)[0]
+    for c0 in range(0, rest.size, 256):
+        c = rest[c0:c0 + 256]
+        tokens[kids[c]] = gumbel_argmax(rng, dv[at[c]], T[seq[kids[c]]])
     return TreeWorkload(name=name, batch=batch, vocab=vocab, node_off=node_off, parent=parent, tokens=tokens,
                         target=target, draft=draft, temperatures=None if np.ndim(temps) == 0 else T,
-                        temperature=float(temps) if np.ndim(temps) == 0 else 1.0,
-                        info={"branching": list(branching), "config": config})
+                        temperature=float(temps) if np.ndim(temps) == 0 else 1.0, info=info)
+
+
+def tree_workload(name, *, config, batch, vocab, branching, dtype="bf16", sigma=0.6, temps=1.0, profile="zipf",
+                  dataset=0, greedy_agree=None) -> TreeWorkload:
+    """The same tree, of the given per-depth branching, for every sequence
+    (rows and tokens as _tree_batch)."""
+    rng = _rng(70 + config, dataset)
+    shape = tree_shape(rng, branching, len(branching))
+    return _tree_batch(name, rng, [shape] * batch, vocab=vocab, dtype=dtype, sigma=sigma, temps=temps,
+                       profile=profile, greedy_agree=greedy_agree,
+                       info={"branching": list(branching), "config": config})
+
+
+def ragged_tree_workload(name, *, config, batch, vocab, max_nodes, dtype="bf16", sigma=0.6, temps=1.0,
+                         profile="zipf", greedy_agree=None) -> TreeWorkload:
+    """Trees of different sizes: sequence b has 1..max_nodes nodes (the first
+    a lone root, the last max_nodes), the parent of node v uniform over
+    0..v-1 (rows and tokens as _tree_batch)."""
+    rng = _rng(90 + config, 0)
+    sizes = rng.integers(1, max_nodes + 1, size=batch)
+    sizes[0], sizes[-1] = 1, max_nodes
+    shapes = [np.array([-1] + [int(rng.integers(0, v)) for v in range(1, int(n))], np.int32) for n in sizes]
+    return _tree_batch(name, rng, shapes, vocab=vocab, dtype=dtype, sigma=sigma, temps=temps, profile=profile,
+                       greedy_agree=greedy_agree, info={"max_nodes": max_nodes, "config": config})
 
 
 CONFIGS = {1: config1, 2: config2, 3: config3, 4: config4, 5: config5}

@@ -123,3 +123,39 @@ def compare_exact(w, gpu: dict, orc: dict):
     for k in ("tokens", "accepted", "status", "kv", "blocks"):
         if k in orc:
             assert np.array_equal(gpu[k], orc[k]), (k, np.nonzero(gpu[k] != orc[k])[0][:10])
+
+
+def compare_tree(w, gpu: dict, orc: dict) -> Tally:
+    """Tree verification, sequence by sequence: statuses identical; an OK
+    sequence's accepted count, node path and tokens identical, except when
+    the oracle's walk met an accept test within BAND of its boundary
+    (|u_acc - r(x)/q(x)|, the smallest over the walk) or drew its final
+    uniform within BAND of a CDF edge of the emitted token. Draws counted:
+    the accepted nodes' tests plus the final draw."""
+    T = Tally()
+    T.rounds = 1
+    diag = orc["diag"]
+    off = np.asarray(w.node_off)
+    for b in range(w.batch):
+        seg = slice(int(off[b]), int(off[b + 1]))
+        so, sg = int(orc["status"][b]), int(gpu["status"][b])
+        same = (gpu["accepted"][b] == orc["accepted"][b] and np.array_equal(gpu["tokens"][seg], orc["tokens"][seg])
+                and np.array_equal(gpu["path"][seg], orc["path"][seg]))
+        if so != 0 or sg != 0:
+            if so != sg or not same:
+                T.unexcused.append((b, "status", so, sg))
+            continue
+        T.draws += int(orc["accepted"][b]) + 1
+        band = diag["acc_margin"][b] < BAND or min(abs(diag["u_smp"][b] - diag["cdf_lo"][b]),
+                                                   abs(diag["u_smp"][b] - diag["cdf_hi"][b])) < BAND
+        T.in_band += int(band)
+        if same:
+            continue
+        T.mismatches += 1
+        if band:
+            T.excused.append(("tree", float(min(diag["acc_margin"][b], abs(diag["u_smp"][b] - diag["cdf_lo"][b]),
+                                                abs(diag["u_smp"][b] - diag["cdf_hi"][b])))))
+        else:
+            T.unexcused.append((b, int(orc["accepted"][b]), int(gpu["accepted"][b]), orc["tokens"][seg][:8].tolist(),
+                                gpu["tokens"][seg][:8].tolist()))
+    return T

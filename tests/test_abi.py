@@ -43,12 +43,15 @@ def test_library_exports_every_declared_symbol(sv):
     assert spec_exports == set(declared_symbols())
 
 
-def test_struct_layout_matches_header(sv):
-    fields = [f for f, _ in sv.SpecVerifyArgs._fields_]
+@pytest.mark.parametrize("cname,pyname", [("spec_verify_args_t", "SpecVerifyArgs"),
+                                           ("spec_tree_args_t", "SpecTreeArgs")])
+def test_struct_layout_matches_header(sv, cname, pyname):
+    S = getattr(sv, pyname)
+    fields = [f for f, _ in S._fields_]
     prog = "#include <stdio.h>\n#include <stddef.h>\n#include \"spec_verify.h\"\nint main(void){\n"
-    prog += 'printf("%zu\\n", sizeof(spec_verify_args_t));\n'
+    prog += f'printf("%zu\\n", sizeof({cname}));\n'
     for f in fields:
-        prog += f'printf("%zu\\n", offsetof(spec_verify_args_t, {f}));\n'
+        prog += f'printf("%zu\\n", offsetof({cname}, {f}));\n'
     prog += "return 0;}\n"
     with tempfile.TemporaryDirectory() as d:
         c = os.path.join(d, "t.c")
@@ -56,13 +59,14 @@ def test_struct_layout_matches_header(sv):
         open(c, "w").write(prog)
         subprocess.run(["gcc", "-std=c99", "-I", os.path.join(ROOT, "include"), c, "-o", exe], check=True)
         out = [int(x) for x in subprocess.run([exe], capture_output=True, text=True, check=True).stdout.split()]
-    assert out[0] == ctypes.sizeof(sv.SpecVerifyArgs)
+    assert out[0] == ctypes.sizeof(S)
+    assert len(out) == len(fields) + 1
     for f, off in zip(fields, out[1:]):
-        assert getattr(sv.SpecVerifyArgs, f).offset == off, f
+        assert getattr(S, f).offset == off, f
 
 
 def test_abi_version_and_status_strings(sv):
-    assert sv.spec_abi_version() == 4 == sv.SPEC_ABI_VERSION
+    assert sv.spec_abi_version() == 5 == sv.SPEC_ABI_VERSION
     assert sv.spec_status_string(0) == "SPEC_OK"
     assert sv.spec_status_string(3) == "SPEC_ERR_WORKSPACE"
 
@@ -146,6 +150,44 @@ def test_host_validation_rejects_before_cuda(sv):
     a.ema_lambda = 1.5  # outside [0, 1]
     assert call(a) == sv.SPEC_ERR_INVALID_ARG
     assert L.spec_debug_philox(0, 0, 0, 0, 1, None, None) == sv.SPEC_ERR_INVALID_ARG
+
+
+def _tree_args(sv, **kw):
+    fake = 1 << 20  # never dereferenced: validation fails before any launch
+    a = sv.SpecTreeArgs()
+    a.struct_size = ctypes.sizeof(sv.SpecTreeArgs)
+    a.batch, a.vocab, a.nodes = kw.get("batch", 4), kw.get("vocab", 1000), kw.get("nodes", 28)
+    a.node_off, a.parent, a.tokens = kw.get("node_off", fake), fake, fake
+    a.target, a.target_dtype = kw.get("target", fake), kw.get("tdt", 1)
+    a.draft, a.draft_dtype, a.draft_is_probs = kw.get("draft", fake), 1, kw.get("probs", 0)
+    a.temperature = 1.0
+    a.out_tokens, a.out_accepted = fake, fake
+    a.out_path = kw.get("out_path", None)
+    return a
+
+
+def test_tree_host_validation(sv):
+    L = sv.lib()
+
+    def call(a, greedy=0):
+        return L.spec_tree_verify(ctypes.byref(a), greedy, None)
+
+    assert L.spec_tree_verify(None, 0, None) == sv.SPEC_ERR_INVALID_ARG
+    a = _tree_args(sv)
+    a.struct_size = 8
+    assert call(a) == sv.SPEC_ERR_INVALID_ARG
+    assert call(_tree_args(sv, batch=0)) == sv.SPEC_ERR_INVALID_ARG
+    assert call(_tree_args(sv, vocab=0)) == sv.SPEC_ERR_INVALID_ARG
+    assert call(_tree_args(sv, vocab=(1 << 21) + 1)) == sv.SPEC_ERR_UNSUPPORTED
+    assert call(_tree_args(sv, nodes=3)) == sv.SPEC_ERR_INVALID_ARG  # fewer nodes than sequences
+    assert call(_tree_args(sv, nodes=1 << 31)) == sv.SPEC_ERR_INVALID_ARG
+    assert call(_tree_args(sv, target=0)) == sv.SPEC_ERR_INVALID_ARG
+    assert call(_tree_args(sv, tdt=3)) == sv.SPEC_ERR_INVALID_ARG
+    assert call(_tree_args(sv, draft=0)) == sv.SPEC_ERR_INVALID_ARG  # sampling reads draft rows
+    assert call(_tree_args(sv, probs=2)) == sv.SPEC_ERR_INVALID_ARG
+    assert call(_tree_args(sv, node_off=(1 << 20) + 4)) == sv.SPEC_ERR_ALIGNMENT
+    assert call(_tree_args(sv, target=(1 << 20) + 1)) == sv.SPEC_ERR_ALIGNMENT
+    assert call(_tree_args(sv, out_path=(1 << 20) + 2)) == sv.SPEC_ERR_ALIGNMENT
 
 
 def test_binding_fails_loudly_without_library(sv, tmp_path, monkeypatch):

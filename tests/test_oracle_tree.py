@@ -149,3 +149,59 @@ def test_statuses(orc):
     assert r["status"].tolist() == [0, orc.SEQ_BAD_LAYOUT, orc.SEQ_BAD_TOKEN, orc.SEQ_BAD_ROW, orc.SEQ_BAD_LAYOUT,
                                     orc.SEQ_BAD_TEMP]
     assert np.all(r["tokens"][2 * n:3 * n] == -1) and r["accepted"][2] == 0
+
+
+def test_offsets_past_the_rows_are_a_layout_error(orc):
+    w = wl.tree_workload("short rows", config=7, batch=3, vocab=20, branching=[2], dtype="f32")
+    off = w.node_off.copy()
+    off[3] = off[3] + 1  # the last sequence claims a node past the 9 rows given
+    w.node_off = off
+    r = orc.tree_verify(w, seed=1)
+    assert r["status"].tolist() == [0, 0, orc.SEQ_BAD_LAYOUT]
+    assert np.all(r["tokens"][6:9] == -7)  # a layout error writes none of the sequence's slots
+
+
+def _fan(B, m, V, rng):
+    """B trees, each a root with m leaf children (tokens drawn at random)."""
+    n = m + 1
+    parent = np.tile(np.array([-1] + [0] * m, np.int32), B)
+    toks = np.full(B * n, -1, np.int32)
+    toks.reshape(B, n)[:, 1:] = rng.integers(0, V, size=(B, m))
+    tgt = rng.standard_normal((B * n, V)).astype(np.float32)
+    dft = rng.standard_normal((B * n, V)).astype(np.float32)
+    return wl.TreeWorkload(name="fan", batch=B, vocab=V, node_off=np.arange(B + 1, dtype=np.int64) * n,
+                           parent=parent, tokens=toks, target=tgt, draft=dft)
+
+
+def test_candidate_limit(orc):
+    rng = np.random.default_rng(12)
+    ok = orc.tree_verify(_fan(3, 64, 50, rng), seed=2)
+    assert ok["status"].tolist() == [0, 0, 0]
+    over = orc.tree_verify(_fan(3, 65, 50, rng), seed=2)
+    assert over["status"].tolist() == [orc.SEQ_UNSUPPORTED] * 3
+    assert np.all(over["tokens"] == -1) and np.all(over["accepted"] == 0)
+    # greedy keeps no residual: no limit
+    assert orc.tree_verify(_fan(3, 65, 50, rng), greedy=True)["status"].tolist() == [0, 0, 0]
+
+
+def test_candidate_limit_applies_to_visited_nodes_only(orc):
+    """Node 1 has 70 children but the walk never reaches it: the root's
+    target is sure of node 2's token and its draft of node 1's, so node 1
+    fails (q > 0 = p there) and node 2 passes."""
+    V = 30
+    parent = np.array([-1, 0, 0] + [1] * 70, np.int32)
+    toks = np.concatenate([[-1, 4, 9], np.arange(70) % V]).astype(np.int32)
+    tgt = np.zeros((73, V), np.float32)
+    tgt[0] = -60.0
+    tgt[0, 9] = 60.0
+    dft = np.zeros((73, V), np.float32)
+    dft[0] = -60.0
+    dft[0, 4] = 60.0
+    t = wl.TreeWorkload(name="deep fan", batch=1, vocab=V, node_off=np.array([0, 73], np.int64), parent=parent,
+                        tokens=toks, target=tgt, draft=dft)
+    r = orc.tree_verify(t, seed=5)
+    assert r["status"].tolist() == [0] and r["path"][0] == 2 and r["accepted"][0] == 1
+    assert r["tokens"][0] == 9
+    t.parent = parent.copy()
+    t.parent[3:] = 2  # now the visited node 2 has the 70 children
+    assert orc.tree_verify(t, seed=5)["status"].tolist() == [orc.SEQ_UNSUPPORTED]
