@@ -16,11 +16,23 @@
 // at (u, ...), so a chain-shaped tree draws exactly what the chain verify
 // draws.
 //
-// One CTA per sequence walks its tree. A visited node costs full-row passes
-// (the maximum and the double-float normaliser of p and of q, one pass per
-// failed candidate for the next residual normaliser, and the draw), read
-// from global memory; the residual at a column is re-evaluated from p, q
-// and the normalisers met so far (r_1 = p, r_{i+1} = max(0, r_i - q) / Z_{i+1}).
+// One CTA per sequence walks its tree. At a visited node:
+//   - pass 1 reads the target row (and, with candidates, the draft row) for
+//     the maxima and the NaN checks (a probability row: its sum);
+//   - pass 2 takes the double-float normalisers and keeps the target's sums
+//     over 256-column segments in shared memory;
+//   - a rejected candidate costs one residual pass, which takes the next
+//     normaliser and keeps the residual's segment sums;
+//   - the final draw scans the kept segment sums of the distribution it
+//     draws from and rescans the one segment that holds u * total (one
+//     warp, 8 columns per lane), so it reads no row again.
+// The residual at a column is re-evaluated from p, q and the normalisers met
+// so far (r_1 = p, r_{i+1} = max(0, r_i - q) / Z_{i+1}). As in the chain's
+// sampler, weights below 2^-13 of the row maximum ("light") are single
+// floats whose sums carry the SFU's mean bias correction; the others, and
+// all sums, are double-float. Segment s covers columns 256 s .. 256 s + 255:
+// warp w reads segments w, w + 16, ..., lane l the 8 columns 256 s + 8 l ...,
+// with one or two 16-byte loads when the rows start on 16-byte boundaries.
 #include <math.h>
 
 #include "internal.h"
@@ -33,17 +45,22 @@ namespace {
 constexpr int kTrThreads = 512;
 constexpr int kTrWarps = kTrThreads / 32;
 constexpr int kTrMaxCand = 64;  // candidates per node whose residual normalisers are kept
+constexpr int kSeg = 256;       // columns per segment
+constexpr int kTrU = 2;         // segments in flight per warp
+constexpr float kLightMax = 1.220703125e-4f;  // 2^-13: a probability above it is heavy
 
 struct TreeSmem {
     Exp2Table tab;
     float fred[kTrWarps];
     int32_t ired[kTrWarps];
     df dred[kTrWarps];
-    df z[kTrMaxCand + 1];   // residual normalisers Z_2 .. of the current node (index i: r_{i+1})
+    df z[kTrMaxCand + 1];           // 1 / Z of each residual level (index i: r_i -> r_{i+1})
+    float zf[kTrMaxCand + 1];       // its high part, for light columns
     int32_t zlive[kTrMaxCand + 1];  // 1: that level changed r (Z > 0)
     int32_t kids[kTrMaxCand];       // the current node's children, in index order
     int32_t nkids;                  // how many it has (may exceed kTrMaxCand)
-    int32_t flag;
+    int32_t sel, col, last;         // the draw's segment, its column, the last column of positive weight
+    df start;                       // running sum before the selected segment
 };
 
 // ------------------------------------------------------------ reductions
@@ -73,11 +90,17 @@ __device__ int32_t block_min_i(int32_t v, TreeSmem& sm) {
     return t;
 }
 
+// Double-float sum over a warp in a fixed order (every lane gets it).
+__device__ __forceinline__ df warp_sum_dfx(df v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = df_add(v, shfl_xor_df(v, o));
+    return v;
+}
+
 // Double-float sum over the CTA in a fixed order (the same bits whatever the timing).
 __device__ df block_sum_dfx(df v, TreeSmem& sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = df_add(v, shfl_xor_df(v, o));
+    v = warp_sum_dfx(v);
     __syncthreads();
     if (lane == 0) sm.dred[warp] = v;
     __syncthreads();
@@ -87,18 +110,24 @@ __device__ df block_sum_dfx(df v, TreeSmem& sm) {
     return t;
 }
 
+// Inclusive prefix over a warp's lanes (double-float, Hillis-Steele).
+__device__ __forceinline__ df warp_incl_scan_dfx(df x) {
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const df y = shfl_up_df(x, o);
+        if (lane >= o) x = df_add(y, x);
+    }
+    return x;
+}
+
 // Prefix sums over the CTA's threads in thread order (double-float): incl
 // is the sum up to and including this thread, excl the previous thread's
 // incl (the same bits), total the last thread's incl. The intervals
 // [excl, incl) of the threads tile [0, total) without gaps or overlaps.
 __device__ void block_scan_dfx(df v, TreeSmem& sm, df& excl, df& incl, df& total) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    df x = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const df y = shfl_up_df(x, o);
-        if (lane >= o) x = df_add(y, x);
-    }
+    const df x = warp_incl_scan_dfx(v);
     __syncthreads();
     if (lane == 31) sm.dred[warp] = x;
     __syncthreads();
@@ -111,51 +140,25 @@ __device__ void block_scan_dfx(df v, TreeSmem& sm, df& excl, df& incl, df& total
     for (int w = 0; w < kTrWarps; ++w) total = df_add(total, sm.dred[w]);
 }
 
-// ------------------------------------------------------------ row passes
-// The node's two rows and what the walk has learnt about them.
-struct NodeRows {
+// ------------------------------------------------------------ the node's rows
+template <int TDT, int DDT>
+struct Rows {
     const char* t;  // target row
-    const char* d;  // draft row
-    int tdt, ddt;
-    bool probs;
-    bool vec;       // the rows read start on 16-byte boundaries: 16-byte loads
+    const char* d;  // draft row (nodes with candidates)
+    bool probs;     // the draft row holds probabilities
+    bool vec;       // the rows read start on 16-byte boundaries
     float mt, md;   // raw maxima
     df k;           // log2(e) / T
     df It, Id;      // 1 / the rows' normalisers
 };
 
-__device__ __forceinline__ df tgt_weight(const NodeRows& n, float l, const Exp2Table& tab) {
-    return n.tdt == SPECV_F32 ? logit_weight<true>(l, n.mt, n.k, tab) : logit_weight<false>(l, n.mt, n.k, tab);
-}
-__device__ __forceinline__ df dft_weight(const NodeRows& n, float l, const Exp2Table& tab) {
-    if (n.probs) return df{l, 0.f};  // a probability row is used as given, divided by its sum
-    return n.ddt == SPECV_F32 ? logit_weight<true>(l, n.md, n.k, tab) : logit_weight<false>(l, n.md, n.k, tab);
-}
-
-__device__ __forceinline__ df p_of(const NodeRows& n, float xt, const TreeSmem& sm) {
-    return df_mul(tgt_weight(n, xt, sm.tab), n.It);
-}
-
-// r_level at a column with values xt (target) and xd (draft), and q there:
-// r_1 = p, r_{i+1} = max(0, r_i - q) / Z_{i+1} for the levels that changed r
-// (the others left it as it was).
-__device__ df r_of(const NodeRows& n, float xt, float xd, int level, const TreeSmem& sm, df& q) {
-    const df p = p_of(n, xt, sm);
-    q = df_mul(dft_weight(n, xd, sm.tab), n.Id);
-    df t = p;
-    for (int i = 1; i < level; ++i) {
-        if (!sm.zlive[i]) continue;
-        const df dlt = df_sub(t, q);
-        t = df_pos(dlt) ? df_mul(dlt, sm.z[i]) : df{0.f, 0.f};  // sm.z holds 1 / Z
-    }
-    return t;
-}
-
-// Columns j .. j+7 of a row (j % 8 == 0): one or two 16-byte loads when the
-// row starts on a 16-byte boundary, else eight element loads.
-__device__ __forceinline__ void ld8(const char* row, int dt, bool vec, int64_t j, float (&x)[8]) {
-    if (vec) {
-        if (dt == SPECV_F32) {
+// Columns j .. j+7 (j % 8 == 0) as floats, fill past V: one or two 16-byte
+// loads when the row allows them, else element loads.
+template <int DT>
+__device__ __forceinline__ void load_unit(const char* row, bool vec, int64_t j, int64_t V, float fill,
+                                          float (&x)[8]) {
+    if (vec && j + 8 <= V) {
+        if constexpr (DT == SPECV_F32) {
             const float4* q = reinterpret_cast<const float4*>(row) + (j >> 2);
             const float4 a = __ldg(q), c = __ldg(q + 1);
             x[0] = a.x, x[1] = a.y, x[2] = a.z, x[3] = a.w, x[4] = c.x, x[5] = c.y, x[6] = c.z, x[7] = c.w;
@@ -166,112 +169,308 @@ __device__ __forceinline__ void ld8(const char* row, int dt, bool vec, int64_t j
         }
     } else {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) x[e] = ld_elem_rt(row, dt, j + e);
+        for (int e = 0; e < 8; ++e) x[e] = j + e < V ? ld_elem<DT>(row, j + e) : fill;
     }
 }
 
-constexpr int kTrU = 2;  // 8-column units in flight per thread
+// Target weight 2^((l - mt) k) of one column: a light one as a float
+// (returns false), a heavy one in double-float (returns true).
+template <int TDT, int DDT>
+__device__ __forceinline__ bool tgt_col(const Rows<TDT, DDT>& n, float l, const TreeSmem& sm, float& lw, df& hw) {
+    bool h;
+    lw = light_weight<TDT == SPECV_F32>(l, n.mt, n.k, h);
+    if (h) hw = heavy_logit_weight<TDT == SPECV_F32>(l, n.mt, n.k, sm.tab);
+    return h;
+}
 
-// f(j, xt, xd) for every column of the node's rows (xd = 0 unless D), each
-// thread taking 8-column units kTrThreads apart, kTrU loaded at a time, then
-// the columns past the last whole unit. Per thread, j increases.
-template <bool D, class F>
-__device__ __forceinline__ void node_pass(const NodeRows& n, int64_t V, F&& f) {
-    const int64_t units = V >> 3;
-    for (int64_t k0 = threadIdx.x; k0 < units; k0 += (int64_t)kTrThreads * kTrU) {
-        float t[kTrU][8], d[kTrU][8];
+// Draft weight of one column, the same way (a probability is its own weight).
+template <int TDT, int DDT>
+__device__ __forceinline__ bool dft_col(const Rows<TDT, DDT>& n, float l, const TreeSmem& sm, float& lw, df& hw) {
+    if (n.probs) {
+        lw = l;
+        hw = df{l, 0.f};
+        return l > kLightMax;
+    }
+    bool h;
+    lw = light_weight<DDT == SPECV_F32>(l, n.md, n.k, h);
+    if (h) hw = heavy_logit_weight<DDT == SPECV_F32>(l, n.md, n.k, sm.tab);
+    return h;
+}
+
+// max(0, r_L - q) at one column, L >= 1. Both weights light: in float
+// (returns false, value in lw); else in double-float (returns true).
+template <int TDT, int DDT>
+__device__ __forceinline__ bool resid_col(const Rows<TDT, DDT>& n, float xt, float xd, int L, const TreeSmem& sm,
+                                          float& lw, df& hw) {
+    float wt, wd;
+    df Wt, Wd;
+    const bool ht = tgt_col(n, xt, sm, wt, Wt);
+    const bool hd = dft_col(n, xd, sm, wd, Wd);
+    if (!ht && !hd) {
+        const float p = __fmaf_rn(wt, n.It.hi, __fmul_rn(wt, n.It.lo));
+        const float q = __fmaf_rn(wd, n.Id.hi, __fmul_rn(wd, n.Id.lo));
+        float r = p;
+        for (int i = 1; i < L; ++i) {
+            if (!sm.zlive[i]) continue;
+            const float dl = __fsub_rn(r, q);
+            r = dl > 0.f ? __fmul_rn(dl, sm.zf[i]) : 0.f;
+        }
+        const float dl = __fsub_rn(r, q);
+        lw = dl > 0.f ? dl : 0.f;
+        return false;
+    }
+    if (!ht) Wt = df{wt, 0.f};
+    if (!hd) Wd = df{wd, 0.f};
+    const df q = df_mul(Wd, n.Id);
+    df r = df_mul(Wt, n.It);
+    for (int i = 1; i < L; ++i) {
+        if (!sm.zlive[i]) continue;
+        const df dl = df_sub(r, q);
+        r = df_pos(dl) ? df_mul(dl, sm.z[i]) : df{0.f, 0.f};
+    }
+    const df dl = df_sub(r, q);
+    hw = df_pos(dl) ? dl : df{0.f, 0.f};
+    return true;
+}
+
+// r_L(x) and q(x) in double-float: the accept test at one column.
+template <int TDT, int DDT>
+__device__ df r_at(const Rows<TDT, DDT>& n, float xt, float xd, int L, const TreeSmem& sm, df& q) {
+    const df Wt = logit_weight<TDT == SPECV_F32>(xt, n.mt, n.k, sm.tab);
+    const df Wd = n.probs ? df{xd, 0.f} : logit_weight<DDT == SPECV_F32>(xd, n.md, n.k, sm.tab);
+    q = df_mul(Wd, n.Id);
+    df r = df_mul(Wt, n.It);
+    for (int i = 1; i < L; ++i) {
+        if (!sm.zlive[i]) continue;
+        const df dl = df_sub(r, q);
+        r = df_pos(dl) ? df_mul(dl, sm.z[i]) : df{0.f, 0.f};
+    }
+    return r;
+}
+
+// Weight of one column of the distribution a draw reads: kind 0, the target
+// weight; kind L >= 1, max(0, r_L - q).
+template <int TDT, int DDT>
+__device__ __forceinline__ bool draw_col(const Rows<TDT, DDT>& n, int kind, float xt, float xd, const TreeSmem& sm,
+                                         float& lw, df& hw) {
+    return kind == 0 ? tgt_col(n, xt, sm, lw, hw) : resid_col(n, xt, xd, kind, sm, lw, hw);
+}
+
+// ------------------------------------------------------------ passes
+template <bool D, int TDT, int DDT>
+__device__ __forceinline__ void load_seg(const Rows<TDT, DDT>& n, int64_t V, int64_t j, float (&t)[8],
+                                         float (&d)[8]) {
+    load_unit<TDT>(n.t, n.vec, j, V, -INFINITY, t);
+    if (D) load_unit<DDT>(n.d, n.vec, j, V, n.probs ? 0.f : -INFINITY, d);
+}
+
+// f(s, j, t, d) for every segment this warp owns (segments warp, warp + 16,
+// ...; s is warp-uniform), j = the lane's first column, t and d its 8
+// target and draft values (d only if D; columns past V read as -inf, or 0
+// in a probability row). The next segment's loads are in flight while f
+// runs. Per lane, columns increase.
+template <bool D, int TDT, int DDT, class F>
+__device__ __forceinline__ void seg_pass(const Rows<TDT, DDT>& n, int64_t V, F&& f) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t segs = (V + kSeg - 1) / kSeg;
+    int64_t s = warp;
+    if (s >= segs) return;
+    float tn[8], dn[8];
+    load_seg<D>(n, V, s * kSeg + lane * 8, tn, dn);
+#pragma unroll 1
+    for (; s < segs; s += kTrWarps) {
+        float t[8], d[8];
 #pragma unroll
-        for (int u = 0; u < kTrU; ++u) {
-            const int64_t k = k0 + (int64_t)u * kTrThreads;
-            if (k < units) {
-                ld8(n.t, n.tdt, n.vec, k << 3, t[u]);
-                if (D) ld8(n.d, n.ddt, n.vec, k << 3, d[u]);
+        for (int e = 0; e < 8; ++e) {
+            t[e] = tn[e];
+            if (D) d[e] = dn[e];
+        }
+        if (s + kTrWarps < segs) load_seg<D>(n, V, (s + kTrWarps) * kSeg + lane * 8, tn, dn);
+        f(s, s * kSeg + lane * 8, t, d);
+    }
+}
+
+// A lane's 8 column weights summed: light(e, l) gives a light weight in l
+// (returning false) or flags a heavy column (true); heavy columns are then
+// evaluated one by one, in column order, by heavy(j) in double-float, so the
+// double-float code exists once per pass and runs only for them. Light
+// weights are summed in float and joined with the correction cl.
+template <class L, class H>
+__device__ __forceinline__ df unit_sum(int64_t j, L&& light, H&& heavy, float cl) {
+    float lt = 0.f;
+    uint32_t hm = 0;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        float l;
+        if (light(e, l)) hm |= 1u << e;
+        else lt = __fadd_rn(lt, l);
+    }
+    df ht{0.f, 0.f};
+#pragma unroll 1
+    while (hm) {
+        const int e = __ffs(hm) - 1;
+        hm &= hm - 1;
+        acc_add(ht, heavy(j + e));
+    }
+    return df_add(df_norm(ht), light_sum_df(lt, cl));
+}
+
+// Light parts of the column weights (true: the column is heavy).
+template <int TDT, int DDT>
+__device__ __forceinline__ bool tgt_light(const Rows<TDT, DDT>& n, float l, float& w) {
+    bool h;
+    w = light_weight<TDT == SPECV_F32>(l, n.mt, n.k, h);
+    return h;
+}
+template <int TDT, int DDT>
+__device__ __forceinline__ bool dft_light(const Rows<TDT, DDT>& n, float l, float& w) {
+    if (n.probs) {
+        w = l;
+        return l > kLightMax;
+    }
+    bool h;
+    w = light_weight<DDT == SPECV_F32>(l, n.md, n.k, h);
+    return h;
+}
+template <int TDT, int DDT>
+__device__ __forceinline__ bool resid_light(const Rows<TDT, DDT>& n, float xt, float xd, int L, const TreeSmem& sm,
+                                            float& w) {
+    float wt, wd;
+    if (tgt_light(n, xt, wt) | dft_light(n, xd, wd)) return true;
+    const float p = __fmaf_rn(wt, n.It.hi, __fmul_rn(wt, n.It.lo));
+    const float q = __fmaf_rn(wd, n.Id.hi, __fmul_rn(wd, n.Id.lo));
+    float r = p;
+    for (int i = 1; i < L; ++i) {
+        if (!sm.zlive[i]) continue;
+        const float dl = __fsub_rn(r, q);
+        r = dl > 0.f ? __fmul_rn(dl, sm.zf[i]) : 0.f;
+    }
+    const float dl = __fsub_rn(r, q);
+    w = dl > 0.f ? dl : 0.f;
+    return false;
+}
+
+// The sum of the kept segment sums in a fixed order (every thread gets it).
+__device__ df seg_total(const float2* buf, int64_t segs, TreeSmem& sm) {
+    df s{0.f, 0.f};
+    for (int64_t i = threadIdx.x; i < segs; i += kTrThreads) s = df_add(s, df{buf[i].x, buf[i].y});
+    return block_sum_dfx(s, sm);
+}
+
+// Inverse CDF in index order over the distribution whose segment sums are
+// buf (kind as draw_col): the first column whose running sum exceeds
+// u * total; if rounding leaves none, the last column of positive weight;
+// -1 if no column has weight. Thread t scans segments [t K, t K + K); the
+// thread whose prefix interval holds u * total finds the segment, and warp 0
+// rescans it (lane l: columns 8 l .. 8 l + 7, running sums per lane as the
+// pass formed them).
+template <int TDT, int DDT>
+__device__ int32_t draw_from(const Rows<TDT, DDT>& n, int64_t V, int kind, const float2* buf, float us,
+                             TreeSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t segs = (V + kSeg - 1) / kSeg;
+    const int64_t K = (segs + kTrThreads - 1) / kTrThreads;
+    const int64_t s0 = min(segs, (int64_t)threadIdx.x * K), s1 = min(segs, s0 + K);
+    if (threadIdx.x == 0) {
+        sm.sel = -1;
+        sm.last = -1;
+        sm.col = INT32_MAX;
+    }
+    df mine{0.f, 0.f};
+    int32_t lastseg = -1;
+    for (int64_t s = s0; s < s1; ++s) {
+        const df v{buf[s].x, buf[s].y};
+        if (df_pos(v)) lastseg = (int32_t)s;
+        mine = df_add(mine, v);
+    }
+    df excl, incl, total;
+    block_scan_dfx(mine, sm, excl, incl, total);  // its barriers order the resets above
+    const df thr = df_mul_f(total, us);
+    if (!df_gt(excl, thr) && df_gt(incl, thr)) {  // exactly one thread
+        df run = excl;
+        int32_t found = -1;
+        for (int64_t s = s0; s < s1; ++s) {
+            const df end = df_add(run, df{buf[s].x, buf[s].y});
+            if (df_gt(end, thr)) {
+                found = (int32_t)s;
+                break;
             }
+            run = end;
         }
+        sm.sel = found >= 0 ? found : lastseg;
+        sm.start = found >= 0 ? run : df{NAN, 0.f};  // NaN: no comparison succeeds, the last column wins
+    }
+    if (lastseg >= 0) atomicMax(&sm.last, lastseg);
+    __syncthreads();
+    int32_t sel = sm.sel;
+    df start = sm.start;
+    if (sel < 0) {
+        sel = sm.last;
+        start = df{NAN, 0.f};
+    }
+    if (sel < 0) return -1;
+    if (warp == 0) {
+        const bool D = kind > 0;
+        const int64_t j = (int64_t)sel * kSeg + lane * 8;
+        float t[8], d[8];
+        load_unit<TDT>(n.t, n.vec, j, V, -INFINITY, t);
+        if (D) load_unit<DDT>(n.d, n.vec, j, V, n.probs ? 0.f : -INFINITY, d);
+        const float cl = (kind > 0 && n.probs) ? 0.f : kEx2LightBias;
+        df pre[8];
+        float lt = 0.f;
+        df ht{0.f, 0.f};
+        int lp = -1;
+#pragma unroll 1
+        for (int e = 0; e < 8; ++e) {
+            float l;
+            df h;
+            const bool heavy = draw_col(n, kind, t[e], D ? d[e] : 0.f, sm, l, h);
+            if (heavy) acc_add(ht, h);
+            else lt = __fadd_rn(lt, l);
+            if (heavy ? df_pos(h) : l > 0.f) lp = e;
+            pre[e] = df_add(df_norm(ht), light_sum_df(lt, cl));
+        }
+        const df incl_l = warp_incl_scan_dfx(pre[7]);
+        const df up = shfl_up_df(incl_l, 1);
+        const df base = df_add(start, lane == 0 ? df{0.f, 0.f} : up);
+        int hit = -1;
 #pragma unroll
-        for (int u = 0; u < kTrU; ++u) {
-            const int64_t k = k0 + (int64_t)u * kTrThreads;
-            if (k < units)
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f((k << 3) + e, t[u][e], D ? d[u][e] : 0.f);
+        for (int e = 7; e >= 0; --e)
+            if (df_gt(df_add(base, pre[e]), thr)) hit = e;
+        const uint32_t hm = __ballot_sync(0xffffffffu, hit >= 0);
+        const uint32_t pm = __ballot_sync(0xffffffffu, lp >= 0);
+        if (hm) {
+            const int hl = __ffs(hm) - 1;
+            if (lane == hl) sm.col = (int32_t)(j + hit);
+        } else if (pm) {
+            const int pl = 31 - __clz(pm);
+            if (lane == pl) sm.col = (int32_t)(j + lp);
+        } else if (lane == 0) {
+            sm.col = -1;
         }
     }
-    for (int64_t j = (units << 3) + threadIdx.x; j < V; j += kTrThreads)
-        f(j, ld_elem_rt(n.t, n.tdt, j), D ? ld_elem_rt(n.d, n.ddt, j) : 0.f);
-}
-
-// f(j, xt, xd) for the columns [j0, j1) of one thread's contiguous chunk
-// (j0 % 8 == 0), in increasing j.
-template <class F>
-__device__ __forceinline__ void chunk_pass(const NodeRows& n, bool D, int64_t j0, int64_t j1, F&& f) {
-    int64_t j = j0;
-    for (; j + 8 * kTrU <= j1; j += 8 * kTrU) {
-        float t[kTrU][8], d[kTrU][8];
-#pragma unroll
-        for (int u = 0; u < kTrU; ++u) {
-            ld8(n.t, n.tdt, n.vec, j + 8 * u, t[u]);
-            if (D) ld8(n.d, n.ddt, n.vec, j + 8 * u, d[u]);
-        }
-#pragma unroll
-        for (int u = 0; u < kTrU; ++u)
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f(j + 8 * u + e, t[u][e], D ? d[u][e] : 0.f);
-    }
-    for (; j < j1; ++j) f(j, ld_elem_rt(n.t, n.tdt, j), D ? ld_elem_rt(n.d, n.ddt, j) : 0.f);
+    __syncthreads();
+    return sm.col;
 }
 
 // First index of the largest target value (NaN read as -inf; a row of -inf
 // or NaN gives 0).
-__device__ int64_t row_argmax(const NodeRows& n, int64_t V, TreeSmem& sm) {
+template <int TDT, int DDT>
+__device__ int32_t row_argmax(const Rows<TDT, DDT>& n, int64_t V, TreeSmem& sm) {
+    const int lane = threadIdx.x & 31;
     float best = -INFINITY;
     int32_t bi = INT32_MAX;
-    node_pass<false>(n, V, [&](int64_t j, float x, float) {
-        if (x > best) {  // NaN never passes; per thread j increases: the first of equals stays
-            best = x;
-            bi = (int32_t)j;
-        }
+    seg_pass<false>(n, V, [&](int64_t, int64_t j, const float (&t)[8], const float (&)[8]) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            if (t[e] > best) {  // NaN never passes; per lane j increases: the first of equals stays
+                best = t[e];
+                bi = (int32_t)(j + e);
+            }
     });
     const float m = block_max_f(best, sm);
     const int32_t i = block_min_i(best == m ? bi : INT32_MAX, sm);
     return i == INT32_MAX ? 0 : i;
-}
-
-// Inverse CDF in index order over w(j) = r_level(j) (level 0: p, the target
-// row alone): the first index whose running sum exceeds u * total; if
-// rounding leaves none, the last index of positive weight. Each thread owns
-// a contiguous chunk of whole 8-column units; the thread whose prefix
-// interval holds u * total rescans its chunk.
-__device__ int64_t draw_index(const NodeRows& n, int level, float us, int64_t V, TreeSmem& sm) {
-    const int64_t C = (((V + 7) >> 3) + kTrThreads - 1) / kTrThreads * 8;
-    const int64_t j0 = min(V, (int64_t)threadIdx.x * C), j1 = min(V, j0 + C);
-    const bool D = level > 0;
-    auto w = [&](float xt, float xd) {
-        df q;
-        return D ? r_of(n, xt, xd, level, sm, q) : p_of(n, xt, sm);
-    };
-    df s{0.f, 0.f};
-    int32_t last = -1;
-    chunk_pass(n, D, j0, j1, [&](int64_t j, float xt, float xd) {
-        const df x = w(xt, xd);
-        if (df_pos(x)) last = (int32_t)j;
-        acc_add(s, x);
-    });
-    df excl, incl, total;
-    block_scan_dfx(df_norm(s), sm, excl, incl, total);
-    const df t = df_mul_f(total, us);
-    int32_t pick = INT32_MAX;
-    if (!df_gt(excl, t) && df_gt(incl, t)) {
-        df c = excl;
-        chunk_pass(n, D, j0, j1, [&](int64_t j, float xt, float xd) {
-            if (pick != INT32_MAX) return;
-            c = df_add(c, w(xt, xd));
-            if (df_gt(c, t)) pick = (int32_t)j;
-        });
-        if (pick == INT32_MAX) pick = last;
-    }
-    pick = block_min_i(pick, sm);
-    if (pick != INT32_MAX && pick >= 0) return pick;
-    return -block_min_i(-last, sm);  // the last index of positive weight
 }
 
 __device__ void write_error(const TreeParams& p, int32_t b, int32_t st, int64_t o, int64_t n) {
@@ -286,11 +485,14 @@ __device__ void write_error(const TreeParams& p, int32_t b, int32_t st, int64_t 
     }
 }
 
+// Dynamic shared memory: two buffers of segment sums, (hi, lo) per segment.
+template <int TDT, int DDT>
 __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
     __shared__ TreeSmem sm;
+    extern __shared__ float2 segbuf[];
     const int32_t b = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t V = p.V;
+    const int64_t V = p.V, segs = (V + kSeg - 1) / kSeg;
     // statuses that need no row, in the documented order
     const int64_t o = __ldg(p.node_off + b), N = __ldg(p.node_off + b + 1) - o;
     if (N < 1 || o < 0 || o + N > p.nodes) {
@@ -326,13 +528,12 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
     }
     __syncthreads();
 
-    const int64_t tes = p.tdt == SPECV_F32 ? 4 : 2, des = p.ddt == SPECV_F32 ? 4 : 2;
-    NodeRows n;
-    n.tdt = p.tdt;
-    n.ddt = p.ddt;
+    constexpr int64_t tes = TDT == SPECV_F32 ? 4 : 2, des = DDT == SPECV_F32 ? 4 : 2;
+    Rows<TDT, DDT> n;
     n.probs = p.probs != 0;
     n.k = p.greedy ? df{0.f, 0.f} : k_of_temperature(T);
     n.d = nullptr;
+    n.md = 0.f;
     int64_t u = 0;
     int32_t acc = 0, emit = -1;
     const uint32_t seq = p.seq_offset + (uint32_t)b;
@@ -340,7 +541,7 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
         n.t = (const char*)p.tgt + (o + u) * V * tes;
         if (p.greedy) {
             n.vec = ((uintptr_t)n.t & 15) == 0;
-            const int32_t g = (int32_t)row_argmax(n, V, sm);
+            const int32_t g = row_argmax(n, V, sm);
             int32_t c = INT32_MAX;
             for (int64_t v = u + 1 + threadIdx.x; v < N; v += kTrThreads)
                 if (__ldg(p.parent + o + v) == u && __ldg(p.tokens + o + v) == g) {
@@ -384,28 +585,34 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
         const bool D = m > 0;  // the draft row is read at nodes with candidates
         n.d = D ? (const char*)p.dft + (o + u) * V * des : nullptr;
         n.vec = ((uintptr_t)n.t & 15) == 0 && (!D || ((uintptr_t)n.d & 15) == 0);
-        // pass 1: maxima (a probability row: its sum) and NaN checks of both rows
+        // pass 1: maxima (a probability row: its sum) and NaN checks
         float mt = -INFINITY, md = -INFINITY;
         bool hnt = false, hnd = false;
         df sd{0.f, 0.f};
         if (D) {
-            node_pass<true>(n, V, [&](int64_t, float xt, float xd) {
-                mt = fmaxf(mt, xt);
-                hnt |= xt != xt;
-                hnd |= xd != xd;
-                if (n.probs) acc_add(sd, xd);
-                else md = fmaxf(md, xd);
+            seg_pass<true>(n, V, [&](int64_t, int64_t, const float (&t)[8], const float (&d)[8]) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    mt = fmaxf(mt, t[e]);
+                    hnt |= t[e] != t[e];
+                    hnd |= d[e] != d[e];
+                    if (n.probs) acc_add(sd, d[e]);
+                    else md = fmaxf(md, d[e]);
+                }
             });
         } else {
-            node_pass<false>(n, V, [&](int64_t, float xt, float) {
-                mt = fmaxf(mt, xt);
-                hnt |= xt != xt;
+            seg_pass<false>(n, V, [&](int64_t, int64_t, const float (&t)[8], const float (&)[8]) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    mt = fmaxf(mt, t[e]);
+                    hnt |= t[e] != t[e];
+                }
             });
         }
         hnt = __syncthreads_or(hnt);
         hnd = __syncthreads_or(hnd);
         n.mt = block_max_f(mt, sm);
-        bool bad = hnt || !isfinite(n.mt);
+        bad = hnt || !isfinite(n.mt);
         if (D) {
             if (n.probs) {
                 sd = block_sum_dfx(df_norm(sd), sm);
@@ -419,26 +626,44 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
             write_error(p, b, 3, o, N);  // SPEC_SEQ_BAD_ROW
             return;
         }
-        // pass 2: the normalisers
-        df st{0.f, 0.f};
-        if (D && !n.probs) {
-            df s2{0.f, 0.f};
-            node_pass<true>(n, V, [&](int64_t, float xt, float xd) {
-                acc_add(st, tgt_weight(n, xt, sm.tab));
-                acc_add(s2, dft_weight(n, xd, sm.tab));
+        // pass 2: the normalisers, and the target's segment sums into buffer 0
+        float2* cur = segbuf;         // segment sums of the distribution a draw would read
+        float2* spare = segbuf + segs;
+        int kind = 0;                 // what cur holds (draw_col)
+        const bool DL = D && !n.probs;
+        df sdl{0.f, 0.f};
+        auto tgt_heavy = [&](int64_t c) {
+            return heavy_logit_weight<TDT == SPECV_F32>(ld_elem<TDT>(n.t, c), n.mt, n.k, sm.tab);
+        };
+        auto tgt_seg = [&](int64_t s, int64_t j, const float (&t)[8]) {
+            const df v = warp_sum_dfx(
+                unit_sum(j, [&](int e, float& l) { return tgt_light(n, t[e], l); }, tgt_heavy, kEx2LightBias));
+            if (lane == 0) cur[s] = make_float2(v.hi, v.lo);
+        };
+        if (DL) {  // the draft row is read only when its logits need a normaliser
+            auto dft_heavy = [&](int64_t c) {
+                return heavy_logit_weight<DDT == SPECV_F32>(ld_elem<DDT>(n.d, c), n.md, n.k, sm.tab);
+            };
+            seg_pass<true>(n, V, [&](int64_t s, int64_t j, const float (&t)[8], const float (&d)[8]) {
+                tgt_seg(s, j, t);
+                sdl = df_add(sdl, unit_sum(j, [&](int e, float& l) { return dft_light(n, d[e], l); }, dft_heavy,
+                                           kEx2LightBias));
             });
-            sd = block_sum_dfx(df_norm(s2), sm);
         } else {
-            node_pass<false>(n, V, [&](int64_t, float xt, float) { acc_add(st, tgt_weight(n, xt, sm.tab)); });
+            seg_pass<false>(n, V,
+                            [&](int64_t s, int64_t j, const float (&t)[8], const float (&)[8]) { tgt_seg(s, j, t); });
         }
-        st = block_sum_dfx(df_norm(st), sm);
+        __syncthreads();
+        const df st = seg_total(cur, segs, sm);
+        if (DL) sd = block_sum_dfx(sdl, sm);
         n.It = df_recip(st);
         const float us = draw_uniforms(p.seed, p.round, seq, (uint32_t)u).y;
         if (!D) {  // a leaf: the bonus token from p
-            emit = (int32_t)draw_index(n, 0, us, V, sm);
+            emit = draw_from(n, V, 0, cur, us, sm);
             break;
         }
         n.Id = df_recip(sd);
+        const float cl = n.probs ? 0.f : kEx2LightBias;
         int level = 1;
         int32_t next = -1;
         for (int32_t j = 0; j < m; ++j) {
@@ -446,22 +671,36 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
             const int32_t x = __ldg(p.tokens + o + c);
             const float ua = draw_uniforms(p.seed, p.round, seq, (uint32_t)(u + (int64_t)j * 65536)).x;
             df qx;  // every thread: the same bits, no broadcast
-            const df rx = r_of(n, ld_elem_rt(n.t, p.tdt, x), ld_elem_rt(n.d, p.ddt, x), level, sm, qx);
+            const df rx = r_at(n, ld_elem<TDT>(n.t, x), ld_elem<DDT>(n.d, x), level, sm, qx);
             if (df_gt(rx, df_mul_f(qx, ua))) {
                 next = c;
                 break;
             }
-            // the next residual's normaliser
-            df z{0.f, 0.f};
-            node_pass<true>(n, V, [&](int64_t, float xt, float xd) {
-                df qv;
-                const df dl = df_sub(r_of(n, xt, xd, level, sm, qv), qv);
-                if (df_pos(dl)) acc_add(z, dl);
+            // the next residual: its normaliser and segment sums
+            auto res_heavy = [&](int64_t c) {
+                float l;
+                df h;
+                resid_col(n, ld_elem<TDT>(n.t, c), ld_elem<DDT>(n.d, c), level, sm, l, h);
+                return h;
+            };
+            seg_pass<true>(n, V, [&](int64_t s, int64_t j, const float (&t)[8], const float (&d)[8]) {
+                const df v = warp_sum_dfx(unit_sum(
+                    j, [&](int e, float& l) { return resid_light(n, t[e], d[e], level, sm, l); }, res_heavy, cl));
+                if (lane == 0) spare[s] = make_float2(v.hi, v.lo);
             });
-            z = block_sum_dfx(df_norm(z), sm);
+            __syncthreads();
+            const df z = seg_total(spare, segs, sm);
+            const bool live = !residual_empty(z);
             if (threadIdx.x == 0) {
-                sm.zlive[level] = !residual_empty(z);
+                sm.zlive[level] = live;
                 sm.z[level] = df_recip(z);
+                sm.zf[level] = sm.z[level].hi;
+            }
+            if (live) {  // r changed: the draw would read these sums
+                float2* t2 = cur;
+                cur = spare;
+                spare = t2;
+                kind = level;
             }
             __syncthreads();
             ++level;
@@ -475,7 +714,7 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
             u = next;
             continue;
         }
-        emit = (int32_t)draw_index(n, level, us, V, sm);
+        emit = draw_from(n, V, kind, cur, us, sm);
         break;
     }
     // the emitted token, then -1 over the sequence's remaining slots
@@ -489,12 +728,26 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
     }
 }
 
+template <int TDT, int DDT>
+cudaError_t launch_tree_t(const TreeParams& p, cudaStream_t s) {
+    const size_t dyn = sizeof(float2) * 2 * (size_t)((p.V + kSeg - 1) / kSeg);
+    if (dyn > 48 * 1024) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(tree_kernel<TDT, DDT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
+        if (e != cudaSuccess) return e;
+    }
+    tree_kernel<TDT, DDT><<<(unsigned)p.B, kTrThreads, dyn, s>>>(p);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_tree(const TreeParams& p, cudaStream_t s) {
     if (p.B == 0) return cudaSuccess;
-    tree_kernel<<<(unsigned)p.B, kTrThreads, 0, s>>>(p);
-    return cudaGetLastError();
+    const int ddt = p.greedy ? p.tdt : p.ddt;  // greedy reads no draft row
+    if (p.tdt == SPECV_F32)
+        return ddt == SPECV_F32 ? launch_tree_t<SPECV_F32, SPECV_F32>(p, s) : launch_tree_t<SPECV_F32, SPECV_BF16>(p, s);
+    return ddt == SPECV_F32 ? launch_tree_t<SPECV_BF16, SPECV_F32>(p, s) : launch_tree_t<SPECV_BF16, SPECV_BF16>(p, s);
 }
 
 }  // namespace specv
