@@ -48,6 +48,7 @@ constexpr int kTrMaxCand = 64;  // candidates per node whose residual normaliser
 constexpr int kSeg = 256;       // columns per segment
 constexpr int kTrU = 2;         // segments in flight per warp
 constexpr float kLightMax = 1.220703125e-4f;  // 2^-13: a probability above it is heavy
+constexpr int kCS = 2;          // CTAs per tree (one cluster), each taking half of the segments
 
 struct TreeSmem {
     Exp2Table tab;
@@ -59,8 +60,9 @@ struct TreeSmem {
     int32_t zlive[kTrMaxCand + 1];  // 1: that level changed r (Z > 0)
     int32_t kids[kTrMaxCand];       // the current node's children, in index order
     int32_t nkids;                  // how many it has (may exceed kTrMaxCand)
-    int32_t sel, col, last;         // the draw's segment, its column, the last column of positive weight
+    int32_t sel, col, last;         // the draw's segment, its column, the last segment of positive weight
     df start;                       // running sum before the selected segment
+    float xin[2][8];                // values the peer CTA stored here (two slots, used in turn)
 };
 
 // ------------------------------------------------------------ reductions
@@ -138,6 +140,41 @@ __device__ void block_scan_dfx(df v, TreeSmem& sm, df& excl, df& incl, df& total
     excl = lane == 0 ? before : up;
     total = df{0.f, 0.f};
     for (int w = 0; w < kTrWarps; ++w) total = df_add(total, sm.dred[w]);
+}
+
+// ------------------------------------------------------------ the pair of CTAs
+// This CTA's share of a tree: segments [s_lo, s_hi), its rank in the
+// cluster and the exchange slot to use next.
+struct Part {
+    int64_t s_lo, s_hi;
+    uint32_t rank;
+    int ph;
+};
+
+struct X8 {
+    float v[8];
+};
+
+// Every thread of both CTAs calls this with its CTA's values (block-uniform):
+// thread 0 stores them into the peer's slot, one cluster barrier, and each
+// thread reads the peer's values from its own slot. The slots alternate, so
+// a slot is written again only after a barrier its reader has passed.
+__device__ X8 xchg(TreeSmem& sm, Part& pt, const X8& mine) {
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) st_cluster_f32(&sm.xin[pt.ph][i], pt.rank ^ 1u, mine.v[i]);
+    }
+    cluster_sync_all();
+    X8 o;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) o.v[i] = sm.xin[pt.ph][i];
+    pt.ph ^= 1;
+    return o;
+}
+
+// Sum of the two CTAs' partial sums in rank order: the same bits in both.
+__device__ __forceinline__ df pair_sum(const Part& pt, df mine, df peer) {
+    return pt.rank == 0 ? df_add(mine, peer) : df_add(peer, mine);
 }
 
 // ------------------------------------------------------------ the node's rows
@@ -264,29 +301,29 @@ __device__ __forceinline__ void load_seg(const Rows<TDT, DDT>& n, int64_t V, int
     if (D) load_unit<DDT>(n.d, n.vec, j, V, n.probs ? 0.f : -INFINITY, d);
 }
 
-// f(s, j, t, d) for every segment this warp owns (segments warp, warp + 16,
-// ...; s is warp-uniform), j = the lane's first column, t and d its 8
+// f(i, j, t, d) for every segment of this CTA's share that this warp owns
+// (segments s_lo + warp, s_lo + warp + 16, ...; i = s - s_lo is
+// warp-uniform), j = the lane's first column, t and d its 8
 // target and draft values (d only if D; columns past V read as -inf, or 0
 // in a probability row). The next segment's loads are in flight while f
 // runs. Per lane, columns increase.
 template <bool D, int TDT, int DDT, class F>
-__device__ __forceinline__ void seg_pass(const Rows<TDT, DDT>& n, int64_t V, F&& f) {
+__device__ __forceinline__ void seg_pass(const Rows<TDT, DDT>& n, int64_t V, const Part& pt, F&& f) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t segs = (V + kSeg - 1) / kSeg;
-    int64_t s = warp;
-    if (s >= segs) return;
+    int64_t s = pt.s_lo + warp;
+    if (s >= pt.s_hi) return;
     float tn[8], dn[8];
     load_seg<D>(n, V, s * kSeg + lane * 8, tn, dn);
 #pragma unroll 1
-    for (; s < segs; s += kTrWarps) {
+    for (; s < pt.s_hi; s += kTrWarps) {
         float t[8], d[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
             t[e] = tn[e];
             if (D) d[e] = dn[e];
         }
-        if (s + kTrWarps < segs) load_seg<D>(n, V, (s + kTrWarps) * kSeg + lane * 8, tn, dn);
-        f(s, s * kSeg + lane * 8, t, d);
+        if (s + kTrWarps < pt.s_hi) load_seg<D>(n, V, (s + kTrWarps) * kSeg + lane * 8, tn, dn);
+        f(s - pt.s_lo, s * kSeg + lane * 8, t, d);
     }
 }
 
@@ -350,68 +387,25 @@ __device__ __forceinline__ bool resid_light(const Rows<TDT, DDT>& n, float xt, f
     return false;
 }
 
-// The sum of the kept segment sums in a fixed order (every thread gets it).
-__device__ df seg_total(const float2* buf, int64_t segs, TreeSmem& sm) {
+// The sum of this CTA's kept segment sums in a fixed order (every thread gets it).
+__device__ df seg_total(const float2* buf, const Part& pt, TreeSmem& sm) {
     df s{0.f, 0.f};
-    for (int64_t i = threadIdx.x; i < segs; i += kTrThreads) s = df_add(s, df{buf[i].x, buf[i].y});
+    for (int64_t i = threadIdx.x; i < pt.s_hi - pt.s_lo; i += kTrThreads) s = df_add(s, df{buf[i].x, buf[i].y});
     return block_sum_dfx(s, sm);
 }
 
-// Inverse CDF in index order over the distribution whose segment sums are
-// buf (kind as draw_col): the first column whose running sum exceeds
-// u * total; if rounding leaves none, the last column of positive weight;
-// -1 if no column has weight. Thread t scans segments [t K, t K + K); the
-// thread whose prefix interval holds u * total finds the segment, and warp 0
-// rescans it (lane l: columns 8 l .. 8 l + 7, running sums per lane as the
-// pass formed them).
+// Rescan of segment sel (global index) with warp 0: lane l takes columns
+// 8 l .. 8 l + 7 with running sums formed as the pass formed the segment's
+// sum; returns the first column whose running sum from start exceeds thr,
+// else (rounding, or a NaN start) the segment's last column of positive
+// weight, else -1. Every thread gets the result.
 template <int TDT, int DDT>
-__device__ int32_t draw_from(const Rows<TDT, DDT>& n, int64_t V, int kind, const float2* buf, float us,
-                             TreeSmem& sm) {
+__device__ int32_t rescan(const Rows<TDT, DDT>& n, int64_t V, int kind, int64_t sel, df start, df thr,
+                          TreeSmem& sm) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t segs = (V + kSeg - 1) / kSeg;
-    const int64_t K = (segs + kTrThreads - 1) / kTrThreads;
-    const int64_t s0 = min(segs, (int64_t)threadIdx.x * K), s1 = min(segs, s0 + K);
-    if (threadIdx.x == 0) {
-        sm.sel = -1;
-        sm.last = -1;
-        sm.col = INT32_MAX;
-    }
-    df mine{0.f, 0.f};
-    int32_t lastseg = -1;
-    for (int64_t s = s0; s < s1; ++s) {
-        const df v{buf[s].x, buf[s].y};
-        if (df_pos(v)) lastseg = (int32_t)s;
-        mine = df_add(mine, v);
-    }
-    df excl, incl, total;
-    block_scan_dfx(mine, sm, excl, incl, total);  // its barriers order the resets above
-    const df thr = df_mul_f(total, us);
-    if (!df_gt(excl, thr) && df_gt(incl, thr)) {  // exactly one thread
-        df run = excl;
-        int32_t found = -1;
-        for (int64_t s = s0; s < s1; ++s) {
-            const df end = df_add(run, df{buf[s].x, buf[s].y});
-            if (df_gt(end, thr)) {
-                found = (int32_t)s;
-                break;
-            }
-            run = end;
-        }
-        sm.sel = found >= 0 ? found : lastseg;
-        sm.start = found >= 0 ? run : df{NAN, 0.f};  // NaN: no comparison succeeds, the last column wins
-    }
-    if (lastseg >= 0) atomicMax(&sm.last, lastseg);
-    __syncthreads();
-    int32_t sel = sm.sel;
-    df start = sm.start;
-    if (sel < 0) {
-        sel = sm.last;
-        start = df{NAN, 0.f};
-    }
-    if (sel < 0) return -1;
     if (warp == 0) {
         const bool D = kind > 0;
-        const int64_t j = (int64_t)sel * kSeg + lane * 8;
+        const int64_t j = sel * kSeg + lane * 8;
         float t[8], d[8];
         load_unit<TDT>(n.t, n.vec, j, V, -INFINITY, t);
         if (D) load_unit<DDT>(n.d, n.vec, j, V, n.probs ? 0.f : -INFINITY, d);
@@ -440,27 +434,102 @@ __device__ int32_t draw_from(const Rows<TDT, DDT>& n, int64_t V, int kind, const
         const uint32_t hm = __ballot_sync(0xffffffffu, hit >= 0);
         const uint32_t pm = __ballot_sync(0xffffffffu, lp >= 0);
         if (hm) {
-            const int hl = __ffs(hm) - 1;
-            if (lane == hl) sm.col = (int32_t)(j + hit);
+            if (lane == __ffs(hm) - 1) sm.col = (int32_t)(j + hit);
         } else if (pm) {
-            const int pl = 31 - __clz(pm);
-            if (lane == pl) sm.col = (int32_t)(j + lp);
+            if (lane == 31 - __clz(pm)) sm.col = (int32_t)(j + lp);
         } else if (lane == 0) {
             sm.col = -1;
         }
     }
     __syncthreads();
-    return sm.col;
+    const int32_t c = sm.col;
+    __syncthreads();  // sm.col is written again only after every thread has read it
+    return c;
+}
+
+// Inverse CDF in index order over the distribution whose segment sums are
+// buf (this CTA's share; kind as draw_col): the first column whose running
+// sum exceeds u * total; if rounding leaves none, the last column of
+// positive weight; -1 if no column has weight. Rank 0's prefix sums start at
+// 0, rank 1's at rank 0's total, so the two CTAs' intervals tile [0, total).
+// Thread t scans this CTA's segments [t K, t K + K); the thread whose
+// interval holds u * total finds the segment, which warp 0 rescans. All
+// threads of both CTAs get the same column.
+template <int TDT, int DDT>
+__device__ int32_t draw_from(const Rows<TDT, DDT>& n, int64_t V, int kind, const float2* buf, float us, Part& pt,
+                             TreeSmem& sm) {
+    const int64_t ns = pt.s_hi - pt.s_lo;
+    const int64_t K = (ns + kTrThreads - 1) / kTrThreads;
+    const int64_t s0 = min(ns, (int64_t)threadIdx.x * K), s1 = min(ns, s0 + K);
+    if (threadIdx.x == 0) {
+        sm.sel = -1;
+        sm.last = -1;
+    }
+    df mine{0.f, 0.f};
+    int32_t lastseg = -1;
+    for (int64_t i = s0; i < s1; ++i) {
+        const df v{buf[i].x, buf[i].y};
+        if (df_pos(v)) lastseg = (int32_t)(pt.s_lo + i);
+        mine = df_add(mine, v);
+    }
+    df excl, incl, tl;
+    block_scan_dfx(mine, sm, excl, incl, tl);  // its barriers order the resets above
+    if (lastseg >= 0) atomicMax(&sm.last, lastseg);
+    __syncthreads();
+    X8 x{};
+    x.v[0] = tl.hi, x.v[1] = tl.lo, x.v[2] = __int_as_float(sm.last);
+    const X8 y = xchg(sm, pt, x);
+    const df tp{y.v[0], y.v[1]};
+    const int32_t last_all = max(sm.last, __float_as_int(y.v[2]));
+    const df t0 = pt.rank == 0 ? tl : tp;
+    const df total = pair_sum(pt, tl, tp);
+    const df thr = df_mul_f(total, us);
+    if (pt.rank != 0) {
+        excl = df_add(t0, excl);
+        incl = df_add(t0, incl);
+    }
+    if (!df_gt(excl, thr) && df_gt(incl, thr)) {  // at most one thread of the two CTAs
+        df run = excl;
+        int64_t found = -1;
+        for (int64_t i = s0; i < s1; ++i) {
+            const df end = df_add(run, df{buf[i].x, buf[i].y});
+            if (df_gt(end, thr)) {
+                found = i;
+                break;
+            }
+            run = end;
+        }
+        sm.sel = (int32_t)(found >= 0 ? pt.s_lo + found : lastseg);
+        sm.start = found >= 0 ? run : df{NAN, 0.f};  // NaN: no comparison succeeds, the last column wins
+    }
+    __syncthreads();
+    const int32_t sel = sm.sel;
+    const df start = sm.start;
+    int32_t c = INT32_MAX;
+    if (sel >= 0) {  // block-uniform
+        c = rescan(n, V, kind, sel, start, thr, sm);
+        if (c < 0) c = INT32_MAX;
+    }
+    x.v[0] = __int_as_float(c);
+    const int32_t cp = __float_as_int(xchg(sm, pt, x).v[0]);
+    c = min(c, cp);
+    if (c != INT32_MAX) return c;
+    // rounding left no crossing in either CTA: the last column of positive weight
+    if (last_all < 0) return -1;
+    int32_t lc = -1;
+    if (last_all >= pt.s_lo && last_all < pt.s_hi) lc = rescan(n, V, kind, last_all, df{NAN, 0.f}, thr, sm);
+    x.v[0] = __int_as_float(lc);
+    const int32_t lp = __float_as_int(xchg(sm, pt, x).v[0]);
+    return max(lc, lp);
 }
 
 // First index of the largest target value (NaN read as -inf; a row of -inf
 // or NaN gives 0).
 template <int TDT, int DDT>
-__device__ int32_t row_argmax(const Rows<TDT, DDT>& n, int64_t V, TreeSmem& sm) {
-    const int lane = threadIdx.x & 31;
+__device__ int32_t row_argmax(const Rows<TDT, DDT>& n, int64_t V, Part& pt, TreeSmem& sm) {
     float best = -INFINITY;
     int32_t bi = INT32_MAX;
-    seg_pass<false>(n, V, [&](int64_t, int64_t j, const float (&t)[8], const float (&)[8]) {
+    seg_pass<false>(n, V, pt, [&](int64_t, int64_t j, const float (&t)[8], const float (&)[8]) {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
             if (t[e] > best) {  // NaN never passes; per lane j increases: the first of equals stays
@@ -470,7 +539,12 @@ __device__ int32_t row_argmax(const Rows<TDT, DDT>& n, int64_t V, TreeSmem& sm) 
     });
     const float m = block_max_f(best, sm);
     const int32_t i = block_min_i(best == m ? bi : INT32_MAX, sm);
-    return i == INT32_MAX ? 0 : i;
+    X8 x{};
+    x.v[0] = m, x.v[1] = __int_as_float(i);
+    const X8 y = xchg(sm, pt, x);
+    const float M = fmaxf(m, y.v[0]);
+    const int32_t k = min(m == M ? i : INT32_MAX, y.v[0] == M ? __float_as_int(y.v[1]) : INT32_MAX);
+    return k == INT32_MAX ? 0 : k;
 }
 
 __device__ void write_error(const TreeParams& p, int32_t b, int32_t st, int64_t o, int64_t n) {
@@ -485,18 +559,24 @@ __device__ void write_error(const TreeParams& p, int32_t b, int32_t st, int64_t 
     }
 }
 
-// Dynamic shared memory: two buffers of segment sums, (hi, lo) per segment.
+// A cluster of kCS CTAs per tree; both CTAs run the same walk on the same
+// exchanged values, so they take the same branches and pass the same
+// cluster barriers; rank 0 writes the outputs. Dynamic shared memory: two
+// buffers of this CTA's segment sums, (hi, lo) per segment.
 template <int TDT, int DDT>
-__global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
+__global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
     __shared__ TreeSmem sm;
     extern __shared__ float2 segbuf[];
-    const int32_t b = blockIdx.x;
+    const uint32_t rank = cluster_ctarank();
+    const int32_t b = (int32_t)(blockIdx.x / kCS);
+    const bool writer = rank == 0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t V = p.V, segs = (V + kSeg - 1) / kSeg;
-    // statuses that need no row, in the documented order
+    const int64_t V = p.V, segs = (V + kSeg - 1) / kSeg, half = (segs + kCS - 1) / kCS;
+    Part pt{min(segs, (int64_t)rank * half), min(segs, (int64_t)rank * half + half), rank, 0};
+    // statuses that need no row, in the documented order (both CTAs alike)
     const int64_t o = __ldg(p.node_off + b), N = __ldg(p.node_off + b + 1) - o;
     if (N < 1 || o < 0 || o + N > p.nodes) {
-        write_error(p, b, 4, o, N);  // SPEC_SEQ_BAD_LAYOUT
+        if (writer) write_error(p, b, 4, o, N);  // SPEC_SEQ_BAD_LAYOUT
         return;
     }
     bool bad = threadIdx.x == 0 && __ldg(p.parent + o) != -1;
@@ -505,12 +585,12 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
         bad |= q < 0 || q >= v;
     }
     if (__syncthreads_or(bad)) {
-        write_error(p, b, 4, o, N);
+        if (writer) write_error(p, b, 4, o, N);
         return;
     }
     const float T = p.temps ? __ldg(p.temps + b) : p.temperature;
     if (!p.greedy && (!(T > 0.f) || !isfinite(T))) {
-        write_error(p, b, 5, o, N);  // SPEC_SEQ_BAD_TEMP
+        if (writer) write_error(p, b, 5, o, N);  // SPEC_SEQ_BAD_TEMP
         return;
     }
     bad = false;
@@ -519,7 +599,7 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
         bad |= x < 0 || x >= V;
     }
     if (__syncthreads_or(bad)) {
-        write_error(p, b, 1, o, N);  // SPEC_SEQ_BAD_TOKEN
+        if (writer) write_error(p, b, 1, o, N);  // SPEC_SEQ_BAD_TOKEN
         return;
     }
     for (int i = threadIdx.x; i < 64; i += kTrThreads) {
@@ -527,6 +607,7 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
         sm.tab.lo[i] = p.tab.lo[i];
     }
     __syncthreads();
+    cluster_sync_all();  // both CTAs are running before either stores into the other
 
     constexpr int64_t tes = TDT == SPECV_F32 ? 4 : 2, des = DDT == SPECV_F32 ? 4 : 2;
     Rows<TDT, DDT> n;
@@ -541,7 +622,7 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
         n.t = (const char*)p.tgt + (o + u) * V * tes;
         if (p.greedy) {
             n.vec = ((uintptr_t)n.t & 15) == 0;
-            const int32_t g = row_argmax(n, V, sm);
+            const int32_t g = row_argmax(n, V, pt, sm);
             int32_t c = INT32_MAX;
             for (int64_t v = u + 1 + threadIdx.x; v < N; v += kTrThreads)
                 if (__ldg(p.parent + o + v) == u && __ldg(p.tokens + o + v) == g) {
@@ -553,7 +634,7 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
                 emit = g;
                 break;
             }
-            if (threadIdx.x == 0) {
+            if (writer && threadIdx.x == 0) {
                 p.out_tokens[o + acc] = g;
                 if (p.out_path) p.out_path[o + acc] = c;
             }
@@ -579,7 +660,7 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
         __syncthreads();
         const int32_t m = sm.nkids;
         if (m > kTrMaxCand) {
-            write_error(p, b, kSeqUnsupported, o, N);
+            if (writer) write_error(p, b, kSeqUnsupported, o, N);
             return;
         }
         const bool D = m > 0;  // the draft row is read at nodes with candidates
@@ -590,7 +671,7 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
         bool hnt = false, hnd = false;
         df sd{0.f, 0.f};
         if (D) {
-            seg_pass<true>(n, V, [&](int64_t, int64_t, const float (&t)[8], const float (&d)[8]) {
+            seg_pass<true>(n, V, pt, [&](int64_t, int64_t, const float (&t)[8], const float (&d)[8]) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     mt = fmaxf(mt, t[e]);
@@ -601,7 +682,7 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
                 }
             });
         } else {
-            seg_pass<false>(n, V, [&](int64_t, int64_t, const float (&t)[8], const float (&)[8]) {
+            seg_pass<false>(n, V, pt, [&](int64_t, int64_t, const float (&t)[8], const float (&)[8]) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     mt = fmaxf(mt, t[e]);
@@ -611,55 +692,67 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
         }
         hnt = __syncthreads_or(hnt);
         hnd = __syncthreads_or(hnd);
-        n.mt = block_max_f(mt, sm);
-        bad = hnt || !isfinite(n.mt);
-        if (D) {
-            if (n.probs) {
-                sd = block_sum_dfx(df_norm(sd), sm);
-                bad |= hnd || !(sd.hi > 0.f) || !isfinite(sd.hi);
-            } else {
-                n.md = block_max_f(md, sm);
-                bad |= hnd || !isfinite(n.md);
-            }
+        mt = block_max_f(mt, sm);
+        md = block_max_f(md, sm);
+        sd = block_sum_dfx(df_norm(sd), sm);
+        {
+            X8 x{};
+            x.v[0] = mt, x.v[1] = md, x.v[2] = sd.hi, x.v[3] = sd.lo, x.v[4] = (float)(hnt ? 1 : 0) + (hnd ? 2 : 0);
+            const X8 y = xchg(sm, pt, x);
+            n.mt = fmaxf(mt, y.v[0]);
+            n.md = fmaxf(md, y.v[1]);
+            sd = pair_sum(pt, sd, df{y.v[2], y.v[3]});
+            const int fl = (int)x.v[4] | (int)y.v[4];
+            hnt = fl & 1;
+            hnd = fl & 2;
         }
+        bad = hnt || !isfinite(n.mt);
+        if (D) bad |= n.probs ? (hnd || !(sd.hi > 0.f) || !isfinite(sd.hi)) : (hnd || !isfinite(n.md));
         if (bad) {
-            write_error(p, b, 3, o, N);  // SPEC_SEQ_BAD_ROW
+            if (writer) write_error(p, b, 3, o, N);  // SPEC_SEQ_BAD_ROW
             return;
         }
         // pass 2: the normalisers, and the target's segment sums into buffer 0
         float2* cur = segbuf;         // segment sums of the distribution a draw would read
-        float2* spare = segbuf + segs;
+        float2* spare = segbuf + half;
         int kind = 0;                 // what cur holds (draw_col)
         const bool DL = D && !n.probs;
         df sdl{0.f, 0.f};
         auto tgt_heavy = [&](int64_t c) {
             return heavy_logit_weight<TDT == SPECV_F32>(ld_elem<TDT>(n.t, c), n.mt, n.k, sm.tab);
         };
-        auto tgt_seg = [&](int64_t s, int64_t j, const float (&t)[8]) {
+        auto tgt_seg = [&](int64_t i, int64_t j, const float (&t)[8]) {
             const df v = warp_sum_dfx(
                 unit_sum(j, [&](int e, float& l) { return tgt_light(n, t[e], l); }, tgt_heavy, kEx2LightBias));
-            if (lane == 0) cur[s] = make_float2(v.hi, v.lo);
+            if (lane == 0) cur[i] = make_float2(v.hi, v.lo);
         };
         if (DL) {  // the draft row is read only when its logits need a normaliser
             auto dft_heavy = [&](int64_t c) {
                 return heavy_logit_weight<DDT == SPECV_F32>(ld_elem<DDT>(n.d, c), n.md, n.k, sm.tab);
             };
-            seg_pass<true>(n, V, [&](int64_t s, int64_t j, const float (&t)[8], const float (&d)[8]) {
-                tgt_seg(s, j, t);
+            seg_pass<true>(n, V, pt, [&](int64_t i, int64_t j, const float (&t)[8], const float (&d)[8]) {
+                tgt_seg(i, j, t);
                 sdl = df_add(sdl, unit_sum(j, [&](int e, float& l) { return dft_light(n, d[e], l); }, dft_heavy,
                                            kEx2LightBias));
             });
         } else {
-            seg_pass<false>(n, V,
-                            [&](int64_t s, int64_t j, const float (&t)[8], const float (&)[8]) { tgt_seg(s, j, t); });
+            seg_pass<false>(n, V, pt,
+                            [&](int64_t i, int64_t j, const float (&t)[8], const float (&)[8]) { tgt_seg(i, j, t); });
         }
         __syncthreads();
-        const df st = seg_total(cur, segs, sm);
+        df st = seg_total(cur, pt, sm);
         if (DL) sd = block_sum_dfx(sdl, sm);
+        {
+            X8 x{};
+            x.v[0] = st.hi, x.v[1] = st.lo, x.v[2] = sd.hi, x.v[3] = sd.lo;
+            const X8 y = xchg(sm, pt, x);
+            st = pair_sum(pt, st, df{y.v[0], y.v[1]});
+            if (DL) sd = pair_sum(pt, sd, df{y.v[2], y.v[3]});
+        }
         n.It = df_recip(st);
         const float us = draw_uniforms(p.seed, p.round, seq, (uint32_t)u).y;
         if (!D) {  // a leaf: the bonus token from p
-            emit = draw_from(n, V, 0, cur, us, sm);
+            emit = draw_from(n, V, 0, cur, us, pt, sm);
             break;
         }
         n.Id = df_recip(sd);
@@ -670,26 +763,32 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
             const int32_t c = sm.kids[j];
             const int32_t x = __ldg(p.tokens + o + c);
             const float ua = draw_uniforms(p.seed, p.round, seq, (uint32_t)(u + (int64_t)j * 65536)).x;
-            df qx;  // every thread: the same bits, no broadcast
+            df qx;  // every thread of both CTAs: the same bits, no broadcast
             const df rx = r_at(n, ld_elem<TDT>(n.t, x), ld_elem<DDT>(n.d, x), level, sm, qx);
             if (df_gt(rx, df_mul_f(qx, ua))) {
                 next = c;
                 break;
             }
             // the next residual: its normaliser and segment sums
-            auto res_heavy = [&](int64_t c) {
+            auto res_heavy = [&](int64_t cc) {
                 float l;
                 df h;
-                resid_col(n, ld_elem<TDT>(n.t, c), ld_elem<DDT>(n.d, c), level, sm, l, h);
+                resid_col(n, ld_elem<TDT>(n.t, cc), ld_elem<DDT>(n.d, cc), level, sm, l, h);
                 return h;
             };
-            seg_pass<true>(n, V, [&](int64_t s, int64_t j, const float (&t)[8], const float (&d)[8]) {
+            seg_pass<true>(n, V, pt, [&](int64_t i, int64_t jj, const float (&t)[8], const float (&d)[8]) {
                 const df v = warp_sum_dfx(unit_sum(
-                    j, [&](int e, float& l) { return resid_light(n, t[e], d[e], level, sm, l); }, res_heavy, cl));
-                if (lane == 0) spare[s] = make_float2(v.hi, v.lo);
+                    jj, [&](int e, float& l) { return resid_light(n, t[e], d[e], level, sm, l); }, res_heavy, cl));
+                if (lane == 0) spare[i] = make_float2(v.hi, v.lo);
             });
             __syncthreads();
-            const df z = seg_total(spare, segs, sm);
+            df z = seg_total(spare, pt, sm);
+            {
+                X8 xx{};
+                xx.v[0] = z.hi, xx.v[1] = z.lo;
+                const X8 y = xchg(sm, pt, xx);
+                z = pair_sum(pt, z, df{y.v[0], y.v[1]});
+            }
             const bool live = !residual_empty(z);
             if (threadIdx.x == 0) {
                 sm.zlive[level] = live;
@@ -706,7 +805,7 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
             ++level;
         }
         if (next >= 0) {
-            if (threadIdx.x == 0) {
+            if (writer && threadIdx.x == 0) {
                 p.out_tokens[o + acc] = __ldg(p.tokens + o + next);
                 if (p.out_path) p.out_path[o + acc] = next;
             }
@@ -714,29 +813,32 @@ __global__ void __launch_bounds__(kTrThreads) tree_kernel(const TreeParams p) {
             u = next;
             continue;
         }
-        emit = draw_from(n, V, kind, cur, us, sm);
+        emit = draw_from(n, V, kind, cur, us, pt, sm);
         break;
     }
     // the emitted token, then -1 over the sequence's remaining slots
-    for (int64_t k = acc + threadIdx.x; k < N; k += kTrThreads) {
-        p.out_tokens[o + k] = k == acc ? emit : -1;
-        if (p.out_path) p.out_path[o + k] = -1;
-    }
-    if (threadIdx.x == 0) {
-        p.out_accepted[b] = acc;
-        if (p.seq_status) p.seq_status[b] = 0;
+    if (writer) {
+        for (int64_t k = acc + threadIdx.x; k < N; k += kTrThreads) {
+            p.out_tokens[o + k] = k == acc ? emit : -1;
+            if (p.out_path) p.out_path[o + k] = -1;
+        }
+        if (threadIdx.x == 0) {
+            p.out_accepted[b] = acc;
+            if (p.seq_status) p.seq_status[b] = 0;
+        }
     }
 }
 
 template <int TDT, int DDT>
 cudaError_t launch_tree_t(const TreeParams& p, cudaStream_t s) {
-    const size_t dyn = sizeof(float2) * 2 * (size_t)((p.V + kSeg - 1) / kSeg);
+    const int64_t segs = (p.V + kSeg - 1) / kSeg;
+    const size_t dyn = sizeof(float2) * 2 * (size_t)((segs + kCS - 1) / kCS);
     if (dyn > 48 * 1024) {
         const cudaError_t e =
             cudaFuncSetAttribute(tree_kernel<TDT, DDT>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn);
         if (e != cudaSuccess) return e;
     }
-    tree_kernel<TDT, DDT><<<(unsigned)p.B, kTrThreads, dyn, s>>>(p);
+    tree_kernel<TDT, DDT><<<(unsigned)p.B * kCS, kTrThreads, dyn, s>>>(p);
     return cudaGetLastError();
 }
 
