@@ -67,6 +67,8 @@ KERNELS = {
               "profile": "stats_kernel_c3_dram.txt"},
     "topk": {"name": "topk_kernel (top-k threshold pass)", "sources": ("topk.cu", "common.cuh", "internal.h"),
              "profile": "topk_kernel_c3_k{k}_dram.txt"},
+    "tree": {"name": "tree_kernel (tree verification)", "sources": ("tree.cu", "common.cuh", "internal.h", "precise.cuh"),
+             "profile": "tree_kernel_bench_trees_dram.txt"},
     "topp": {"name": "topk_kernel (top-k threshold and top-p nucleus pass)",
              "sources": ("topk.cu", "common.cuh", "internal.h", "precise.cuh"), "profile": "topk_kernel_c3_k{k}_p_dram.txt"},
 }
@@ -571,10 +573,10 @@ def run_tree(args):
                    "mean_accepted": float(np.mean(acc))},
         "gpu_launches": K,
         "roofline": {"bound": "latency", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "tree_kernel", "kernel_ms": ms / K,
+                     "traffic": ncu_traffic_per_launch("tree"), "kernel": "tree_kernel", "kernel_ms": ms / K,
                      "algorithmic_bytes_per_launch": per_launch,
                      "note": "bytes = rows the walks must read once (visited nodes' target rows, draft rows of "
-                             "visited nodes with children); one CTA per tree walks node by node",
+                             "visited nodes with children); a cluster of two CTAs per tree walks node by node",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
         "clocks": ClockSampler.summarize(rows),
         "e2e": {"value": n_e2e / (e2e_ms / 1e3), "unit": "rounds/s", "h2d_bytes_per_step": int(h2d),

@@ -33,6 +33,7 @@
 // all sums, are double-float. Segment s covers columns 256 s .. 256 s + 255:
 // warp w reads segments w, w + 16, ..., lane l the 8 columns 256 s + 8 l ...,
 // with one or two 16-byte loads when the rows start on 16-byte boundaries.
+#include <float.h>
 #include <math.h>
 
 #include "internal.h"
@@ -46,7 +47,6 @@ constexpr int kTrThreads = 512;
 constexpr int kTrWarps = kTrThreads / 32;
 constexpr int kTrMaxCand = 64;  // candidates per node whose residual normalisers are kept
 constexpr int kSeg = 256;       // columns per segment
-constexpr int kTrU = 2;         // segments in flight per warp
 constexpr float kLightMax = 1.220703125e-4f;  // 2^-13: a probability above it is heavy
 constexpr int kCS = 2;          // CTAs per tree (one cluster), each taking half of the segments
 
@@ -294,35 +294,90 @@ __device__ __forceinline__ bool draw_col(const Rows<TDT, DDT>& n, int kind, floa
 }
 
 // ------------------------------------------------------------ passes
-template <bool D, int TDT, int DDT>
-__device__ __forceinline__ void load_seg(const Rows<TDT, DDT>& n, int64_t V, int64_t j, float (&t)[8],
-                                         float (&d)[8]) {
-    load_unit<TDT>(n.t, n.vec, j, V, -INFINITY, t);
-    if (D) load_unit<DDT>(n.d, n.vec, j, V, n.probs ? 0.f : -INFINITY, d);
+// A lane's 8 columns as stored (bf16: four words; f32: eight), so that the
+// segments in flight cost half the registers in bf16.
+template <int DT>
+struct Raw {
+    uint32_t w[DT == SPECV_F32 ? 8 : 4];
+};
+
+template <int DT>
+__device__ __forceinline__ Raw<DT> fetch_unit(const char* row, bool vec, int64_t j, int64_t V, float fill) {
+    Raw<DT> r;
+    if (vec && j + 8 <= V) {
+        if constexpr (DT == SPECV_F32) {
+            const uint4* q = reinterpret_cast<const uint4*>(row) + (j >> 2);
+            const uint4 a = __ldg(q), c = __ldg(q + 1);
+            r.w[0] = a.x, r.w[1] = a.y, r.w[2] = a.z, r.w[3] = a.w, r.w[4] = c.x, r.w[5] = c.y, r.w[6] = c.z,
+            r.w[7] = c.w;
+        } else {
+            const uint4 a = __ldg(reinterpret_cast<const uint4*>(row) + (j >> 3));
+            r.w[0] = a.x, r.w[1] = a.y, r.w[2] = a.z, r.w[3] = a.w;
+        }
+    } else {
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = j + e < V ? ld_elem<DT>(row, j + e) : fill;
+        if constexpr (DT == SPECV_F32) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) r.w[e] = __float_as_uint(x[e]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)  // the values are bf16: their high halves hold them exactly
+                r.w[e] = (__float_as_uint(x[2 * e]) >> 16) | (__float_as_uint(x[2 * e + 1]) & 0xFFFF0000u);
+        }
+    }
+    return r;
+}
+
+template <int DT>
+__device__ __forceinline__ void decode_unit(const Raw<DT>& r, float (&x)[8]) {
+    if constexpr (DT == SPECV_F32) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = __uint_as_float(r.w[e]);
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[2 * e] = bf16_lo(r.w[e]);
+            x[2 * e + 1] = bf16_hi(r.w[e]);
+        }
+    }
 }
 
 // f(i, j, t, d) for every segment of this CTA's share that this warp owns
 // (segments s_lo + warp, s_lo + warp + 16, ...; i = s - s_lo is
 // warp-uniform), j = the lane's first column, t and d its 8
 // target and draft values (d only if D; columns past V read as -inf, or 0
-// in a probability row). The next segment's loads are in flight while f
+// in a probability row). The next two segments' loads are in flight while f
 // runs. Per lane, columns increase.
 template <bool D, int TDT, int DDT, class F>
 __device__ __forceinline__ void seg_pass(const Rows<TDT, DDT>& n, int64_t V, const Part& pt, F&& f) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int64_t s = pt.s_lo + warp;
     if (s >= pt.s_hi) return;
-    float tn[8], dn[8];
-    load_seg<D>(n, V, s * kSeg + lane * 8, tn, dn);
+    const float fd = n.probs ? 0.f : -INFINITY;
+    Raw<TDT> ta, tb;  // the next two segments, in flight
+    Raw<DDT> da, db;
+    ta = fetch_unit<TDT>(n.t, n.vec, s * kSeg + lane * 8, V, -INFINITY);
+    if (D) da = fetch_unit<DDT>(n.d, n.vec, s * kSeg + lane * 8, V, fd);
+    if (s + kTrWarps < pt.s_hi) {
+        tb = fetch_unit<TDT>(n.t, n.vec, (s + kTrWarps) * kSeg + lane * 8, V, -INFINITY);
+        if (D) db = fetch_unit<DDT>(n.d, n.vec, (s + kTrWarps) * kSeg + lane * 8, V, fd);
+    }
 #pragma unroll 1
     for (; s < pt.s_hi; s += kTrWarps) {
         float t[8], d[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            t[e] = tn[e];
-            if (D) d[e] = dn[e];
+        decode_unit<TDT>(ta, t);
+        ta = tb;
+        if (D) {
+            decode_unit<DDT>(da, d);
+            da = db;
         }
-        if (s + kTrWarps < pt.s_hi) load_seg<D>(n, V, (s + kTrWarps) * kSeg + lane * 8, tn, dn);
+        const int64_t s2 = s + 2 * kTrWarps;
+        if (s2 < pt.s_hi) {
+            tb = fetch_unit<TDT>(n.t, n.vec, s2 * kSeg + lane * 8, V, -INFINITY);
+            if (D) db = fetch_unit<DDT>(n.d, n.vec, s2 * kSeg + lane * 8, V, fd);
+        }
         f(s - pt.s_lo, s * kSeg + lane * 8, t, d);
     }
 }
@@ -666,10 +721,22 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTrThreads) tree_k
         const bool D = m > 0;  // the draft row is read at nodes with candidates
         n.d = D ? (const char*)p.dft + (o + u) * V * des : nullptr;
         n.vec = ((uintptr_t)n.t & 15) == 0 && (!D || ((uintptr_t)n.d & 15) == 0);
-        // pass 1: maxima (a probability row: its sum) and NaN checks
+        // pass 1: maxima and NaN checks; with candidates also float softmax
+        // sums of both rows (online, per lane; a probability row: its
+        // double-float sum) for the float test of the first candidate
+        const float kf = n.k.hi;
         float mt = -INFINITY, md = -INFINITY;
+        float om_t = -FLT_MAX, os_t = 0.f, om_d = -FLT_MAX, os_d = 0.f;  // online maxima and sums
         bool hnt = false, hnd = false;
         df sd{0.f, 0.f};
+        auto fold = [&](float x, float& om, float& os) {
+            if (x > om) {
+                os = __fmaf_rn(os, ex2(__fmul_rn(__fsub_rn(om, x), kf)), 1.f);
+                om = x;
+            } else {
+                os = __fadd_rn(os, ex2(__fmul_rn(__fsub_rn(x, om), kf)));
+            }
+        };
         if (D) {
             seg_pass<true>(n, V, pt, [&](int64_t, int64_t, const float (&t)[8], const float (&d)[8]) {
 #pragma unroll
@@ -677,8 +744,13 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTrThreads) tree_k
                     mt = fmaxf(mt, t[e]);
                     hnt |= t[e] != t[e];
                     hnd |= d[e] != d[e];
-                    if (n.probs) acc_add(sd, d[e]);
-                    else md = fmaxf(md, d[e]);
+                    fold(t[e], om_t, os_t);
+                    if (n.probs) {
+                        acc_add(sd, d[e]);
+                    } else {
+                        md = fmaxf(md, d[e]);
+                        fold(d[e], om_d, os_d);
+                    }
                 }
             });
         } else {
@@ -695,9 +767,18 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTrThreads) tree_k
         mt = block_max_f(mt, sm);
         md = block_max_f(md, sm);
         sd = block_sum_dfx(df_norm(sd), sm);
+        // the lanes' float sums relative to this CTA's maxima (NaN-free: an
+        // empty lane has os = 0; a bad row's sums are never used)
+        auto rel = [&](float os, float om, float M) {
+            return (os > 0.f && M > -INFINITY) ? __fmul_rn(os, ex2(__fmul_rn(__fsub_rn(om, M), kf))) : 0.f;
+        };
+        const float fs_t = D ? block_sum_dfx(df{rel(os_t, om_t, mt), 0.f}, sm).hi : 0.f;
+        const float fs_d = (D && !n.probs) ? block_sum_dfx(df{rel(os_d, om_d, md), 0.f}, sm).hi : 0.f;
+        float St_f, Sd_f;
         {
             X8 x{};
             x.v[0] = mt, x.v[1] = md, x.v[2] = sd.hi, x.v[3] = sd.lo, x.v[4] = (float)(hnt ? 1 : 0) + (hnd ? 2 : 0);
+            x.v[5] = fs_t, x.v[6] = fs_d;
             const X8 y = xchg(sm, pt, x);
             n.mt = fmaxf(mt, y.v[0]);
             n.md = fmaxf(md, y.v[1]);
@@ -705,6 +786,13 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTrThreads) tree_k
             const int fl = (int)x.v[4] | (int)y.v[4];
             hnt = fl & 1;
             hnd = fl & 2;
+            // rank order: rank 0's part first
+            const float a_t = pt.rank == 0 ? fs_t : y.v[5], b_t = pt.rank == 0 ? y.v[5] : fs_t;
+            const float ma_t = pt.rank == 0 ? mt : y.v[0], mb_t = pt.rank == 0 ? y.v[0] : mt;
+            const float a_d = pt.rank == 0 ? fs_d : y.v[6], b_d = pt.rank == 0 ? y.v[6] : fs_d;
+            const float ma_d = pt.rank == 0 ? md : y.v[1], mb_d = pt.rank == 0 ? y.v[1] : md;
+            St_f = __fadd_rn(rel(a_t, ma_t, n.mt), rel(b_t, mb_t, n.mt));
+            Sd_f = __fadd_rn(rel(a_d, ma_d, n.md), rel(b_d, mb_d, n.md));
         }
         bad = hnt || !isfinite(n.mt);
         if (D) bad |= n.probs ? (hnd || !(sd.hi > 0.f) || !isfinite(sd.hi)) : (hnd || !isfinite(n.md));
@@ -712,7 +800,27 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTrThreads) tree_k
             if (writer) write_error(p, b, 3, o, N);  // SPEC_SEQ_BAD_ROW
             return;
         }
-        // pass 2: the normalisers, and the target's segment sums into buffer 0
+        const float us = draw_uniforms(p.seed, p.round, seq, (uint32_t)u).y;
+        int32_t next = -1;
+        if (D) {  // the first candidate's test, in float (every thread of both CTAs: the same bits)
+            const int32_t c = sm.kids[0];
+            const int32_t x = __ldg(p.tokens + o + c);
+            const float ua = draw_uniforms(p.seed, p.round, seq, (uint32_t)u).x;
+            const float px = __fdiv_rn(ex2(__fmul_rn(__fsub_rn(ld_elem<TDT>(n.t, x), n.mt), kf)), St_f);
+            const float qv = ld_elem<DDT>(n.d, x);
+            const float qx = n.probs ? __fdiv_rn(qv, sd.hi) : __fdiv_rn(ex2(__fmul_rn(__fsub_rn(qv, n.md), kf)), Sd_f);
+            if (__fmul_rn(ua, qx) < px) next = c;
+        }
+        if (next >= 0) {
+            if (writer && threadIdx.x == 0) {
+                p.out_tokens[o + acc] = __ldg(p.tokens + o + next);
+                if (p.out_path) p.out_path[o + acc] = next;
+            }
+            ++acc;
+            u = next;
+            continue;
+        }
+        // pass 2: the double-float normalisers, and the target's segment sums into buffer 0
         float2* cur = segbuf;         // segment sums of the distribution a draw would read
         float2* spare = segbuf + half;
         int kind = 0;                 // what cur holds (draw_col)
@@ -750,24 +858,25 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTrThreads) tree_k
             if (DL) sd = pair_sum(pt, sd, df{y.v[2], y.v[3]});
         }
         n.It = df_recip(st);
-        const float us = draw_uniforms(p.seed, p.round, seq, (uint32_t)u).y;
         if (!D) {  // a leaf: the bonus token from p
             emit = draw_from(n, V, 0, cur, us, pt, sm);
             break;
         }
         n.Id = df_recip(sd);
         const float cl = n.probs ? 0.f : kEx2LightBias;
+        // candidate 0 failed above; from here each rejection costs a residual pass
         int level = 1;
-        int32_t next = -1;
         for (int32_t j = 0; j < m; ++j) {
             const int32_t c = sm.kids[j];
-            const int32_t x = __ldg(p.tokens + o + c);
-            const float ua = draw_uniforms(p.seed, p.round, seq, (uint32_t)(u + (int64_t)j * 65536)).x;
-            df qx;  // every thread of both CTAs: the same bits, no broadcast
-            const df rx = r_at(n, ld_elem<TDT>(n.t, x), ld_elem<DDT>(n.d, x), level, sm, qx);
-            if (df_gt(rx, df_mul_f(qx, ua))) {
-                next = c;
-                break;
+            if (j > 0) {
+                const int32_t x = __ldg(p.tokens + o + c);
+                const float ua = draw_uniforms(p.seed, p.round, seq, (uint32_t)(u + (int64_t)j * 65536)).x;
+                df qx;  // every thread of both CTAs: the same bits, no broadcast
+                const df rx = r_at(n, ld_elem<TDT>(n.t, x), ld_elem<DDT>(n.d, x), level, sm, qx);
+                if (df_gt(rx, df_mul_f(qx, ua))) {
+                    next = c;
+                    break;
+                }
             }
             // the next residual: its normaliser and segment sums
             auto res_heavy = [&](int64_t cc) {
