@@ -53,6 +53,8 @@ def parse():
                     help="with --top-k: also keep each row's top-p nucleus inside the top-k set (0: off)")
     ap.add_argument("--ngram", action="store_true",
                     help="time the n-gram (prompt lookup) drafter instead of the verify step")
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5],
+                    help="the workload: 3 (default) the B=64 headline; 1, 2 small sampling; 4 greedy; 5 ragged")
     ap.add_argument("--tree", action="store_true",
                     help="time tree verification (64 trees of branching 4, 2, 2) instead of the chain verify")
     ap.add_argument("--adaptive", action="store_true",
@@ -64,7 +66,7 @@ def parse():
 # committed ncu DRAM summary, and that summary's file.
 KERNELS = {
     "stats": {"name": "stats_tma_kernel (streaming pass)", "sources": ("stats.cu", "common.cuh", "internal.h"),
-              "profile": "stats_kernel_c3_dram.txt"},
+              "profile": "stats_kernel_c{c}_dram.txt"},
     "topk": {"name": "topk_kernel (top-k threshold pass)", "sources": ("topk.cu", "common.cuh", "internal.h"),
              "profile": "topk_kernel_c3_k{k}_dram.txt"},
     "tree": {"name": "tree_kernel (tree verification)", "sources": ("tree.cu", "common.cuh", "internal.h", "precise.cuh"),
@@ -80,13 +82,31 @@ def mode_of(args):
     return "stats"
 
 
+# The other workloads of the scope table (C1, C2, C4, C5): descriptions and metrics.
+CONFIGS = {
+    1: ("C1 sampling verify B=1 gamma=4 V=1000 f32 T=1 (Gaussian logits, draft = target + N(0, 0.5^2))",
+        "verify rounds/s (C1: B=1, gamma=4, V=1000, f32 logits)"),
+    2: ("C2 sampling verify B=1 gamma=4 V=50257 f32 T=1 (Zipf logits, draft noise tuned to alpha ~ 0.8)",
+        "verify rounds/s (C2: B=1, gamma=4, V=50257, f32 logits)"),
+    4: ("C4 greedy verify B=256 gamma=5 V=152064 bf16 (Zipf target; draft token = the target's argmax w.p. 0.75)",
+        "verify rounds/s (C4 greedy: B=256, gamma=5, V=152064, bf16 logits)"),
+    5: ("C5 ragged sampling verify B=512 gamma_b ~ U{1..8} V=128256 bf16, T_b ~ U[0.5, 1.5], sigma_b ~ U[0.2, 2.0]",
+        "verify rounds/s (C5 ragged: B=512, gamma_b in 1..8, V=128256, bf16 logits)"),
+}
+L2_BYTES = 129 << 20
+
+
 def metric_of(args):
+    if args.config != 3:
+        return CONFIGS[args.config][1]
     if args.top_k <= 0:
         return METRIC
     return METRIC[:-1] + f", top-k {args.top_k}" + (f", top-p {args.top_p}" if 0 < args.top_p < 1 else "") + ")"
 
 
 def workload_of(args):
+    if args.config != 3:
+        return CONFIGS[args.config][0]
     if args.top_k <= 0:
         return WORKLOAD
     w = WORKLOAD + f", both models truncated to top-k {args.top_k}"
@@ -165,10 +185,10 @@ def kernel_source_hash(mode: str = "stats") -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic_per_launch(mode: str = "stats", top_k: int = 0):
+def ncu_traffic_per_launch(mode: str = "stats", top_k: int = 0, config: int = 3):
     """DRAM bytes per launch of the mode's dominant kernel from the committed
     ncu summary, if it was taken on the current kernel source; else None."""
-    path = os.path.join(ROOT, "profiles", KERNELS[mode]["profile"].format(k=top_k))
+    path = os.path.join(ROOT, "profiles", KERNELS[mode]["profile"].format(k=top_k, c=config))
     try:
         kv = {}
         for line in open(path):
@@ -213,7 +233,14 @@ def run_ours(args):
     from speculative_decoding_verification_38_gb300.sharding import seq_offset
 
     mode = mode_of(args)
-    w = wl.config3(top_k=args.top_k, top_p=args.top_p if args.top_k > 0 else 0.0)
+    if args.config == 3:
+        w = wl.config3(top_k=args.top_k, top_p=args.top_p if args.top_k > 0 else 0.0)
+    else:
+        if args.top_k > 0 or args.adaptive:
+            raise SystemExit("--top-k, --top-p and --adaptive apply to the C3 workload only")
+        w = wl.CONFIGS[args.config]()
+    greedy = w.greedy
+    small = 2 * w.input_bytes() < L2_BYTES  # C1, C2: both copies would stay in L2
     B = w.batch
     seq_off = seq_offset(rank, B)  # weak scaling: each rank verifies its own batch
     copies = [DeviceBatch(w, seed=0, seq_offset=seq_off) for _ in range(2)]
@@ -230,12 +257,15 @@ def run_ours(args):
         db = copies[i % 2]
         st = db.call(rnd=rnd, pool_index=rnd)
         if st != 0:
-            raise sv.SpecError(st, "spec_verify_sample")
+            raise sv.SpecError(st, "spec_verify_greedy" if greedy else "spec_verify_sample")
         if gammas_next is not None:  # the next round's gamma per request (the synthetic drafter keeps gamma = 8)
             sv.check(sv.spec_adapt_gamma(db.args.tensors["accept_ema"], w.gamma_max, 0.05, gammas_next),
                      "spec_adapt_gamma")
 
     W, K = max(3, args.warmup), max(1, args.steps)
+    if small:
+        K = min(K, 5000)  # each step is timed alone, between L2 flushes
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") if small else None
     for i in range(W):
         step(i, i)
     torch.cuda.synchronize()
@@ -252,14 +282,21 @@ def run_ours(args):
         a.record()
         b.record()
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)] \
+        if small else []
     torch.cuda.synchronize()
     wall0 = time.time()
     t_start.record()
     for i in range(K):
+        if small:  # inputs smaller than L2: evict them, then time this step alone
+            flush.fill_(i & 255)
+            step_ev[i][0].record()
         if i % HOOK_EVERY == 0:
             e0, e1 = ev[i // HOOK_EVERY]
             sv.spec_debug_time_next_stats(e0, e1)  # brackets this step's streaming kernel
         step(i, W + i)
+        if small:
+            step_ev[i][1].record()
     t_end.record()
     torch.cuda.synchronize()
     wall1 = time.time()
@@ -286,6 +323,8 @@ def run_ours(args):
     clocks["window"] = clock_window
 
     elapsed_ms = t_start.elapsed_time(t_end)
+    if small:
+        elapsed_ms = sum(a.elapsed_time(b) for a, b in step_ev)
     stats_ms = [a.elapsed_time(b) for a, b in ev]
     if dist:
         elapsed_ms = max_over_ranks(elapsed_ms, dist, "cuda")
@@ -294,7 +333,8 @@ def run_ours(args):
     kern_ms = statistics.mean(stats_ms)
     peak, peak_kind = measured_hbm_peak()
     achieved = (algo_bytes + small_io) / (kern_ms / 1e3) / 1e9
-    traffic = ncu_traffic_per_launch(mode, args.top_k)
+    traffic = ncu_traffic_per_launch(mode, args.top_k, args.config)
+    graph = time_graph(copies[0], W, flush, K) if small else None
 
     # end to end through the public API with host buffers
     e2e = run_e2e(copies[0], w, args, sv) if args.e2e_steps > 0 else None
@@ -304,13 +344,18 @@ def run_ours(args):
         "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded Zipf logits; no dataset)",
         "config": {"workload": workload_of(args), "batch": B, "gamma": w.gamma_max, "vocab": w.vocab,
-                   "top_k": args.top_k, "top_p": args.top_p, "logits_dtype": "bf16",
+                   "top_k": args.top_k, "top_p": args.top_p, "logits_dtype": w.dtype_name,
                    "parallelism": f"replicas x{world} (sequence shards)",
-                   "l2": "inputs larger than L2: 279 MB per step, alternating 2 resident copies"},
+                   "l2": (f"inputs smaller than L2 ({w.input_bytes()} B): each step timed alone after a "
+                          f"{2 * L2_BYTES >> 20} MB write that evicts them") if small else
+                         (f"inputs larger than L2: {w.input_bytes() / 1e6:.0f} MB per step, "
+                          "alternating 2 resident copies")},
         "vocab_rows_per_s": rounds_per_s * w.vocab_rows(),
         "sequence_rounds_per_s": rounds_per_s * B,
         "step_hbm_gbs": rounds_per_s / world * algo_bytes / 1e9,
-        "gpu_launches": (5 if args.adaptive else 4) * K,  # row pass, finalize, sampler tile pass, draw (+ gamma policy)
+        # row pass and finalize; sampling adds the sampler tile pass and the draw
+        # (+ the nucleus kernel with top-p, + the gamma policy with --adaptive)
+        "gpu_launches": ((2 if greedy else 4) + (1 if mode == "topp" else 0) + (1 if args.adaptive else 0)) * K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": KERNELS[mode]["name"], "kernel_ms": kern_ms,
@@ -322,6 +367,8 @@ def run_ours(args):
         "e2e": e2e,
         "wall_s_timed": wall1 - wall0,
     }
+    if graph is not None:
+        out["cuda_graph"] = graph
     if args.adaptive:
         out["adaptive_gamma"] = time_policy(sv, w.gamma_max)
         out["config"]["adaptive"] = "running acceptance (lambda 0.1) updated in finalize; gamma policy (c = 0.05) each step"
@@ -331,6 +378,35 @@ def run_ours(args):
         print(json.dumps(out), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def time_graph(db, rnd, flush, K):
+    """One verify call captured in a CUDA graph and replayed, each replay timed
+    alone after an L2-evicting write (the launch-bound small workloads)."""
+    import torch
+
+    K = min(K, 2000)
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            st = db.call(rnd=rnd, pool_index=rnd)
+        if st != 0:
+            return {"unavailable": f"capture: verify returned status {st}"}
+        for _ in range(3):
+            g.replay()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+        for i in range(K):
+            flush.fill_(i & 255)
+            ev[i][0].record()
+            g.replay()
+            ev[i][1].record()
+        torch.cuda.synchronize()
+        ms = sum(a.elapsed_time(b) for a, b in ev)
+        return {"value": K / (ms / 1e3), "unit": UNIT, "ms_per_step": ms / K, "steps": K,
+                "note": "one captured call (fixed round) replayed"}
+    except Exception as e:  # a capture the runtime refuses is reported, not fatal
+        torch.cuda.synchronize()
+        return {"unavailable": f"capture failed: {type(e).__name__}: {str(e)[:160]}"}
 
 
 def time_policy(sv, gamma_max):
@@ -602,31 +678,24 @@ def run_e2e(db, w, args, sv):
     outputs back device -> host, all inside the timed region."""
     import torch
 
-    host_t = db.target.cpu().pin_memory()
-    host_d = db.draft.cpu().pin_memory()
+    ins = [(d, d.cpu().pin_memory()) for d in (db.target, db.draft, db.kv_in) if d is not None]
     host_tok = [t.cpu().pin_memory() for t in db.token_pool]
-    host_kv = db.kv_in.cpu().pin_memory()
-    out_tok = torch.empty_like(db.out_tokens, device="cpu").pin_memory()
-    out_acc = torch.empty_like(db.out_accepted, device="cpu").pin_memory()
-    out_kv = torch.empty_like(db.kv_out, device="cpu").pin_memory()
-    out_st = torch.empty_like(db.status, device="cpu").pin_memory()
-    h2d = host_t.numel() * 2 + host_d.numel() * 2 + host_tok[0].numel() * 4 + host_kv.numel() * 4
-    d2h = (out_tok.numel() + out_acc.numel() + out_kv.numel() + out_st.numel()) * 4
+    outs = [(d, torch.empty_like(d, device="cpu").pin_memory())
+            for d in (db.out_tokens, db.out_accepted, db.kv_out, db.status) if d is not None]
+    h2d = sum(h.numel() * h.element_size() for _, h in ins) + host_tok[0].numel() * 4
+    d2h = sum(h.numel() * h.element_size() for _, h in outs)
     n = max(3, args.e2e_steps)
 
     def one(i):
-        db.target.copy_(host_t, non_blocking=True)
-        db.draft.copy_(host_d, non_blocking=True)
+        for d, h in ins:
+            d.copy_(h, non_blocking=True)
         tok = db.token_pool[i % len(db.token_pool)]
         tok.copy_(host_tok[i % len(host_tok)], non_blocking=True)
-        db.kv_in.copy_(host_kv, non_blocking=True)
         st = db.call(rnd=i, pool_index=i)
         if st != 0:
-            raise sv.SpecError(st, "spec_verify_sample")
-        out_tok.copy_(db.out_tokens, non_blocking=True)
-        out_acc.copy_(db.out_accepted, non_blocking=True)
-        out_kv.copy_(db.kv_out, non_blocking=True)
-        out_st.copy_(db.status, non_blocking=True)
+            raise sv.SpecError(st, "verify")
+        for d, h in outs:
+            h.copy_(d, non_blocking=True)
 
     for i in range(3):
         one(i)
@@ -644,16 +713,22 @@ def run_e2e(db, w, args, sv):
 
 # ---------------------------------------------------------------- CPU / oracle
 def _oracle_subset(w, nseq):
-    """The first nseq sequences of a uniform-gamma workload (views, no copies)."""
+    """The first nseq sequences of a workload (views, no copies): rows up to
+    the (nseq)-th offset, per-sequence arrays cut to nseq."""
     from speculative_decoding_verification_38_gb300 import workloads as wl
 
     g = w.gamma_max
-    sub = wl.Workload(name=w.name, batch=nseq, vocab=w.vocab, gamma_max=g, gammas=w.gammas[:nseq],
-                      target=w.target[:nseq * (g + 1)], draft=w.draft[:nseq * g],
-                      draft_tokens=w.draft_tokens[:nseq * g], temperature=w.temperature,
-                      kv_in=None if w.kv_in is None else w.kv_in[:nseq], block_size=w.block_size,
-                      top_k=w.top_k, top_p=w.top_p)
-    return sub
+    if w.target_row_off is None:
+        rt, rd, tro, dro = nseq * (g + 1), nseq * g, None, None
+    else:
+        tro, dro = w.target_row_off[:nseq + 1], w.draft_row_off[:nseq + 1]
+        rt, rd = int(tro[-1]), int(dro[-1])
+    cut = (lambda a: None if a is None else a[:nseq])
+    return wl.Workload(name=w.name, batch=nseq, vocab=w.vocab, gamma_max=g, gammas=w.gammas[:nseq],
+                       target=w.target[:rt], draft=None if w.draft is None else w.draft[:rd],
+                       draft_tokens=w.draft_tokens[:rd], temperatures=cut(w.temperatures),
+                       temperature=w.temperature, kv_in=cut(w.kv_in), block_size=w.block_size,
+                       target_row_off=tro, draft_row_off=dro, greedy=w.greedy, top_k=w.top_k, top_p=w.top_p)
 
 
 def run_cpu_baseline(w, args):
@@ -664,12 +739,15 @@ def run_cpu_baseline(w, args):
     rounds, t = 0, 0.0
     t0 = time.time()
     while t < args.cpu_seconds and rounds < 200:
-        oracle.verify_sample(w, seed=0, rnd=rounds, draft_tokens=w.tokens_for_round(rounds), nthreads=cores)
+        if w.greedy:
+            oracle.verify_greedy(w, nthreads=cores)
+        else:
+            oracle.verify_sample(w, seed=0, rnd=rounds, draft_tokens=w.tokens_for_round(rounds), nthreads=cores)
         rounds += 1
         t = time.time() - t0
     return {"value": rounds / t, "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{rounds} full rounds of the same workload (all 64 sequences each), float64 C oracle, "
-                      f"one thread per sequence slice, {t:.1f} s"}
+            "sample": f"{rounds} full rounds of the same workload (all {w.batch} sequences each), float64 C "
+                      f"oracle, one thread per sequence slice, {t:.1f} s"}
 
 
 def run_reference(args):
@@ -680,30 +758,40 @@ def run_reference(args):
     from speculative_decoding_verification_38_gb300 import workloads as wl
 
     oracle.build()
-    w = wl.config3(top_k=args.top_k, top_p=args.top_p if args.top_k > 0 else 0.0)
+    if args.config == 3:
+        w = wl.config3(top_k=args.top_k, top_p=args.top_p if args.top_k > 0 else 0.0)
+    else:
+        w = wl.CONFIGS[args.config]()
     cores = os.cpu_count() or 1
     W, K = max(3, args.warmup), max(1, args.steps)
+
+    def run(x, rnd):
+        if x.greedy:
+            oracle.verify_greedy(x, nthreads=cores)
+        else:
+            oracle.verify_sample(x, seed=0, rnd=rnd, draft_tokens=x.draft_tokens, nthreads=cores)
+
     # size each step so the whole run stays within ~3 minutes
     t0 = time.time()
-    oracle.verify_sample(w, seed=0, rnd=0, draft_tokens=w.tokens_for_round(0), nthreads=cores)
+    run(w, 0)
     t_round = time.time() - t0
     per_step = max(1, min(w.batch, int(w.batch * 150.0 / ((K + W) * max(t_round, 1e-3)))))
     sub = _oracle_subset(w, per_step)
     for i in range(W):
-        oracle.verify_sample(sub, seed=0, rnd=i, nthreads=cores)
+        run(sub, i)
     t0 = time.time()
     for i in range(K):
-        oracle.verify_sample(sub, seed=0, rnd=W + i, nthreads=cores)
+        run(sub, W + i)
     el = time.time() - t0
     value = (K * per_step / w.batch) / el
     out = {"impl": "reference", "metric": metric_of(args), "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
            "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Zipf logits; no dataset)",
            "config": {"workload": workload_of(args), "batch": w.batch, "gamma": w.gamma_max, "vocab": w.vocab,
-                      "top_k": args.top_k, "logits_dtype": "bf16", "parallelism": "host cores"},
+                      "top_k": args.top_k, "logits_dtype": w.dtype_name, "parallelism": "host cores"},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
-                            "sample": f"each step verifies {per_step} of the 64 sequences of one round "
-                                      f"(counted as {per_step}/64 round), float64 C oracle"},
+                            "sample": f"each step verifies {per_step} of the {w.batch} sequences of one round "
+                                      f"(counted as {per_step}/{w.batch} round), float64 C oracle"},
            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(out), flush=True)
 

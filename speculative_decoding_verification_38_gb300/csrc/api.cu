@@ -311,6 +311,7 @@ SPEC_API spec_status_t spec_verify_sample(const spec_verify_args_t* a, spec_stre
     sp.tasks_in = p.tasks;
     sp.tasks = p.tasks;
     sp.recs = (TileRec*)((char*)a->workspace + L.off_recs);
+    sp.open = (uint16_t*)((char*)a->workspace + L.off_open);
     sp.out_tokens = p.out_tokens;
     sp.seq_status = p.seq_status;
     sp.err = (uint32_t*)((char*)a->workspace + kErrWordOffset);

@@ -28,6 +28,7 @@ constexpr uint32_t kTmaStageBytes = SPECV_WS_STAGE_BYTES;  // bytes per stage (a
 static_assert(kTmaConsumerWarps * kTmaStages * kTmaStageBytes <= 200 * 1024, "warp rings exceed shared memory");
 constexpr int kSampThreads = 256;     // threads per CTA of the residual sampler (one tile item per warp)
 constexpr int kTile = 1024;           // sampler tile: 32 lanes x 32 contiguous columns
+constexpr int kOpenCap = 32;           // open columns a sampler tile lists for the draw (more: the tile is summed again)
 constexpr int64_t kChunkAlign = 64;   // elements; keeps 16-byte alignment for both dtypes
 constexpr int64_t kMinChunk = 1024;   // smallest slice one CTA streams
 constexpr int kGridCap = 4096;        // most CTAs of one streaming pass
@@ -121,7 +122,7 @@ struct __align__(16) TileRec {
     float a[2], b[2];      // target / draft weight sums over the columns certainly in max(0, p - q)'s support
     float st[2], sd[2];    // target / draft weight sums over every column of the tile
     float uwt[2], uwd[2];  // the weights of the one column whose membership stayed open
-    int32_t nu;            // such columns (more than one: the tile is summed again exactly)
+    int32_t nu;            // such columns (more than one: see SampleParams::open)
     int32_t pad[3];
 };
 static_assert(sizeof(TileRec) == 64, "tile record layout");
@@ -136,6 +137,7 @@ struct SampleParams {
     const SampleTask* tasks_in;
     SampleTask* tasks;
     TileRec* recs;         // [B * ntile]
+    uint16_t* open;        // [B * ntile * kOpenCap]: a tile's open columns (first kOpenCap; more: summed again)
     int32_t* out_tokens;
     int32_t* seq_status;   // may be null
     uint32_t* err;         // workspace error word
@@ -145,7 +147,7 @@ struct SampleParams {
 struct Layout {
     int64_t rows_total, N, chunk;
     int32_t S, grid;
-    size_t off_partials, off_rowstats, off_pq, off_tasks, off_recs, off_tau, off_keep, off_keepn, total;
+    size_t off_partials, off_rowstats, off_pq, off_tasks, off_recs, off_open, off_tau, off_keep, off_keepn, total;
 };
 
 // Work split and workspace layout for a given problem. grid_cap bounds the

@@ -270,7 +270,7 @@ struct TileAcc {
 
 template <int TDT, int DDT>
 __device__ void tile_sums(const RowPair<TDT, DDT>& rp, bool resid, float r_hi, float r_lo, SampSmem& sm,
-                          TileAcc& out) {
+                          uint16_t* open_list, TileAcc& out) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t* q = sm.q[warp];
     uint32_t head = 0, tail = 0;
@@ -296,6 +296,7 @@ __device__ void tile_sums(const RowPair<TDT, DDT>& rp, bool resid, float r_hi, f
             acc_add(b_h, wd);
         } else if (!(wt.hi < wd.hi * r_lo)) {  // still open: kept apart for phase 2
             const int slot = atomicAdd(&sm.nu[warp], 1);
+            if (slot < kOpenCap) open_list[slot] = (uint16_t)j;  // the draw evaluates listed columns alone
             if (slot == 0) {
                 sm.uw[warp][0] = wt.hi;
                 sm.uw[warp][1] = wt.lo;
@@ -408,7 +409,7 @@ __global__ void __launch_bounds__(kSampThreads, 4) sampler_kernel(SampleParams p
     __syncwarp();
     const RowPair<TDT, DDT> rp = tile_rows<TDT, DDT>(p, t, tile);
     TileAcc acc;
-    tile_sums(rp, resid, r_hi, r_lo, sm, acc);
+    tile_sums(rp, resid, r_hi, r_lo, sm, p.open + item * kOpenCap, acc);
     const df tot = warp_sum4_df(acc.st, acc.sd, resid ? acc.a : acc.st, acc.b);
     TileRec& r = p.recs[item];
     if ((lane & 7) == 0) {
@@ -556,7 +557,17 @@ __global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
     for (int i = warp; i < nd; i += kWarps) {  // one warp per tile, exactly
         const int ti = sm.dirty[i];
         const RowPair<TDT, DDT> rp = tile_rows<TDT, DDT>(p, t, ti);
-        const df x = warp_sum_df(lane_tile_sum(rp, 0, mode, It, Id, cl, *reinterpret_cast<SampSmem*>(&sm)));
+        const int32_t nu = __ldcg(&recs[ti].nu);
+        df x;
+        if (nu <= kOpenCap) {  // the tile's open columns are listed: the certain part plus each of them
+            const uint16_t* lst = p.open + ((int64_t)b * nt + ti) * kOpenCap;
+            const df c = lane < nu ? col_weight(rp, (int64_t)__ldcg(lst + lane), kTaskResidual, It, Id, sm.tab)
+                                   : df{0.f, 0.f};
+            const float4 ab = __ldcg(reinterpret_cast<const float4*>(recs + ti));
+            x = df_add(resid_of_sums(df{ab.x, ab.y}, df{ab.z, ab.w}, It, Id), warp_sum_df(c));
+        } else {
+            x = warp_sum_df(lane_tile_sum(rp, 0, mode, It, Id, cl, *reinterpret_cast<SampSmem*>(&sm)));
+        }
         if (lane == 0) {
             sm.w_hi[ti] = x.hi;
             sm.w_lo[ti] = x.lo;

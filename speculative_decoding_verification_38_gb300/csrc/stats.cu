@@ -1257,6 +1257,8 @@ Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int gre
     off = al(off + (greedy ? 0 : (size_t)B * sizeof(SampleTask)));
     L.off_recs = off;
     off = al(off + (greedy ? 0 : (size_t)B * ((V + kTile - 1) / kTile) * sizeof(TileRec)));
+    L.off_open = off;
+    off = al(off + (greedy ? 0 : (size_t)B * ((V + kTile - 1) / kTile) * kOpenCap * sizeof(uint16_t)));
     L.off_tau = off;
     off = al(off + (greedy ? 0 : (size_t)L.rows_total * sizeof(float)));
     const bool keep = topp && !greedy;
