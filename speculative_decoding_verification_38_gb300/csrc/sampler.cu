@@ -37,12 +37,14 @@ namespace {
 constexpr int kWarps = kSampThreads / 32;
 constexpr int kQCap = 128;      // entries per warp queue (power of two)
 constexpr float kMargin = 1e-4f;  // relative margin of the approximate support test
+constexpr int64_t kWideItems = 608;  // at most this many tile items: one CTA per item (4 CTAs x 152 SMs)
 
 struct SampSmem {
     Exp2Table tab;
     int32_t q[kWarps][kQCap];  // per-warp queue of columns awaiting double-float evaluation
     int32_t nu[kWarps];        // open columns found by each warp in its current tile
     float uw[kWarps][4];       // the first one's weights (wt hi, lo, wd hi, lo)
+    float part[kWarps][4][2];  // wide tiles: each warp's four sums, combined in warp order
 };
 
 // One row's chunk: column j (0-based within the chunk) at g + j * esz. With
@@ -268,9 +270,11 @@ struct TileAcc {
     df st, sd, a, b;
 };
 
-template <int TDT, int DDT>
+// Every group of the tile, or (WIDE) group gw alone; sw: the shared-memory
+// slot counting the tile's open columns (the warp's own, or one for the CTA).
+template <int TDT, int DDT, bool WIDE>
 __device__ void tile_sums(const RowPair<TDT, DDT>& rp, bool resid, float r_hi, float r_lo, SampSmem& sm,
-                          uint16_t* open_list, TileAcc& out) {
+                          uint16_t* open_list, int sw, int gw, TileAcc& out) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int32_t* q = sm.q[warp];
     uint32_t head = 0, tail = 0;
@@ -295,18 +299,19 @@ __device__ void tile_sums(const RowPair<TDT, DDT>& rp, bool resid, float r_hi, f
             acc_add(a_h, wt);
             acc_add(b_h, wd);
         } else if (!(wt.hi < wd.hi * r_lo)) {  // still open: kept apart for phase 2
-            const int slot = atomicAdd(&sm.nu[warp], 1);
+            const int slot = atomicAdd(&sm.nu[sw], 1);
             if (slot < kOpenCap) open_list[slot] = (uint16_t)j;  // the draw evaluates listed columns alone
             if (slot == 0) {
-                sm.uw[warp][0] = wt.hi;
-                sm.uw[warp][1] = wt.lo;
-                sm.uw[warp][2] = wd.hi;
-                sm.uw[warp][3] = wd.lo;
+                sm.uw[sw][0] = wt.hi;
+                sm.uw[sw][1] = wt.lo;
+                sm.uw[sw][2] = wd.hi;
+                sm.uw[sw][3] = wd.lo;
             }
         }
     };
 #pragma unroll
     for (int g = 0; g < kGroups; ++g) {
+        if (WIDE && g != gw) continue;  // uniform per warp
         const int64_t j = g * 256 + lane * 8;
         float lt[8], ld[8];
         src_load8<TDT>(rp.t, j, lt);
@@ -385,19 +390,24 @@ __device__ __forceinline__ df warp_sum4_df(df v0, df v1, df v2, df v3) {
     return s;
 }
 
-template <int TDT, int DDT>
+// WIDE: one CTA per tile item, warp w summing group w (for problems with few
+// items, so that one tile's double-float columns are spread over kGroups
+// warps); otherwise one warp per item.
+template <int TDT, int DDT, bool WIDE>
 __global__ void __launch_bounds__(kSampThreads, 4) sampler_kernel(SampleParams p) {
     __shared__ SampSmem sm;
     for (int i = threadIdx.x; i < 64; i += blockDim.x) {
         sm.tab.hi[i] = p.tab.hi[i];
         sm.tab.lo[i] = p.tab.lo[i];
     }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int sw = WIDE ? 0 : warp;  // the open-column counter of this tile
+    if (WIDE && threadIdx.x == 0) sm.nu[0] = 0;
     __syncthreads();
     pdl_launch_dependents();
     pdl_wait_primary();  // tasks are written by the finalize step
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t item = (int64_t)blockIdx.x * kWarps + warp;
-    if (item >= (int64_t)p.B * p.ntile) return;
+    const int64_t item = WIDE ? (int64_t)blockIdx.x : (int64_t)blockIdx.x * kWarps + warp;
+    if (item >= (int64_t)p.B * p.ntile) return;  // block-uniform when WIDE
     const int32_t b = (int32_t)(item / p.ntile), tile = (int32_t)(item - (int64_t)b * p.ntile);
     const SampleTask t = p.tasks_in[b];
     if (t.mode == kTaskNone) return;
@@ -405,12 +415,26 @@ __global__ void __launch_bounds__(kSampThreads, 4) sampler_kernel(SampleParams p
     // approximate support test p > q(1 + m) / p < q(1 - m), i.e. w_t > w_d * r
     const float ratio = resid ? t.id_apx / t.it_apx : 0.f;
     const float r_hi = ratio * (1.f + kMargin), r_lo = ratio * (1.f - kMargin);
-    if (lane == 0) sm.nu[warp] = 0;
-    __syncwarp();
+    if (!WIDE) {
+        if (lane == 0) sm.nu[warp] = 0;
+        __syncwarp();
+    }
     const RowPair<TDT, DDT> rp = tile_rows<TDT, DDT>(p, t, tile);
     TileAcc acc;
-    tile_sums(rp, resid, r_hi, r_lo, sm, p.open + item * kOpenCap, acc);
-    const df tot = warp_sum4_df(acc.st, acc.sd, resid ? acc.a : acc.st, acc.b);
+    if (WIDE && warp >= kGroups) acc = TileAcc{};
+    else tile_sums<TDT, DDT, WIDE>(rp, resid, r_hi, r_lo, sm, p.open + item * kOpenCap, sw, warp, acc);
+    df tot = warp_sum4_df(acc.st, acc.sd, resid ? acc.a : acc.st, acc.b);
+    if (WIDE) {  // the groups' sums in warp order
+        if (warp < kGroups && (lane & 7) == 0) {
+            sm.part[warp][lane >> 3][0] = tot.hi;
+            sm.part[warp][lane >> 3][1] = tot.lo;
+        }
+        __syncthreads();
+        if (warp != 0) return;
+        tot = df{0.f, 0.f};
+        if ((lane & 7) == 0)
+            for (int w = 0; w < kGroups; ++w) tot = df_add(tot, df{sm.part[w][lane >> 3][0], sm.part[w][lane >> 3][1]});
+    }
     TileRec& r = p.recs[item];
     if ((lane & 7) == 0) {
         float* dst = lane == 0 ? r.st : (lane == 8 ? r.sd : (lane == 16 ? r.a : r.b));
@@ -418,11 +442,11 @@ __global__ void __launch_bounds__(kSampThreads, 4) sampler_kernel(SampleParams p
         dst[1] = tot.lo;
     }
     if (lane == 1) {
-        r.nu = sm.nu[warp];
-        r.uwt[0] = sm.uw[warp][0];
-        r.uwt[1] = sm.uw[warp][1];
-        r.uwd[0] = sm.uw[warp][2];
-        r.uwd[1] = sm.uw[warp][3];
+        r.nu = sm.nu[sw];
+        r.uwt[0] = sm.uw[sw][0];
+        r.uwt[1] = sm.uw[sw][1];
+        r.uwd[0] = sm.uw[sw][2];
+        r.uwd[1] = sm.uw[sw][3];
     }
 }
 
@@ -653,8 +677,9 @@ __global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
 template <int TDT, int DDT>
 cudaError_t launch_typed(const SampleParams& p, cudaStream_t s, bool pdl) {
     const int64_t items = (int64_t)p.B * p.ntile;
+    const bool wide = items <= kWideItems;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((items + kWarps - 1) / kWarps));
+    cfg.gridDim = dim3((unsigned)(wide ? items : (items + kWarps - 1) / kWarps));
     cfg.blockDim = dim3(kSampThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
@@ -663,7 +688,8 @@ cudaError_t launch_typed(const SampleParams& p, cudaStream_t s, bool pdl) {
     attr.val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = &attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, sampler_kernel<TDT, DDT>, p);
+    cudaError_t e = wide ? cudaLaunchKernelEx(&cfg, sampler_kernel<TDT, DDT, true>, p)
+                         : cudaLaunchKernelEx(&cfg, sampler_kernel<TDT, DDT, false>, p);
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3((unsigned)p.B);
     cfg.numAttrs = 1;
