@@ -69,6 +69,8 @@ KERNELS = {
               "profile": "stats_kernel_c{c}_dram.txt"},
     "topk": {"name": "topk_kernel (top-k threshold pass)", "sources": ("topk.cu", "common.cuh", "internal.h"),
              "profile": "topk_kernel_c3_k{k}_dram.txt"},
+    "ngram": {"name": "ngram_kernel (n-gram drafter)", "sources": ("ngram.cu", "common.cuh", "internal.h"),
+              "profile": "ngram_kernel_edit_contexts_dram.txt"},
     "tree": {"name": "tree_kernel (tree verification)", "sources": ("tree.cu", "common.cuh", "internal.h", "precise.cuh"),
              "profile": "tree_kernel_bench_trees_dram.txt"},
     "topp": {"name": "topk_kernel (top-k threshold and top-p nucleus pass)",
@@ -514,7 +516,7 @@ def run_ngram(args):
                    "l2": "128 resident copies of the 1.3 MB contexts (168 MB), rotated"},
         "gpu_launches": K,
         "roofline": {"bound": "latency", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None, "kernel": "ngram_kernel", "kernel_ms": ms / K,
+                     "traffic": ncu_traffic_per_launch("ngram"), "kernel": "ngram_kernel", "kernel_ms": ms / K,
                      "algorithmic_bytes_per_launch": scanned,
                      "note": "bytes = context tokens the backward search must read at least once (latest match first)",
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
