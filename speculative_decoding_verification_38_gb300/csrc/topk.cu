@@ -624,6 +624,7 @@ __global__ void __launch_bounds__(kTkThreads, 4) topk_kernel(StatsParams p) {
 // itself when they did not fit). The warp then rewrites the row's threshold
 // and its sum over the kept columns.
 constexpr int kNuThreads = 256;
+constexpr int kNuReg = 4;  // kept values per lane whose weights stay in registers
 constexpr int kNuWarps = kNuThreads / 32;
 
 __device__ __forceinline__ df warp_sum_df(df v) {
@@ -660,8 +661,28 @@ __device__ void row_nucleus(const StatsParams& p, int64_t r, const char* row, fl
             }
         }
     };
+    // Rows keeping at most 32 * kNuReg values keep each lane's keys and
+    // weights in registers: the rounds below then only compare and add, in
+    // the same per-lane order as the uncached walk (the same sums).
+    const bool cached = n >= 0 && n <= 32 * kNuReg;
+    uint32_t ck[kNuReg];
+    df cw[kNuReg];
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < kNuReg; ++i) {
+            const int e = lane + 32 * i;
+            ck[i] = e < n ? __ldcg(kept + e) : 0u;  // key 0 is below every round's bounds
+            cw[i] = e < n ? weight(KT::value(KT::bits_of_key(ck[i]))) : df{0.f, 0.f};
+        }
+    }
     df S{0.f, 0.f};
-    visit([&](uint32_t, float v) { S = df_add(S, weight(v)); });
+    if (cached) {
+#pragma unroll
+        for (int i = 0; i < kNuReg; ++i)
+            if (lane + 32 * i < n) S = df_add(S, cw[i]);
+    } else {
+        visit([&](uint32_t, float v) { S = df_add(S, weight(v)); });
+    }
     S = warp_sum_df(S);
     const df target = df_mul_f(S, tp);
     uint32_t prefix = 0;
@@ -669,13 +690,20 @@ __device__ void row_nucleus(const StatsParams& p, int64_t r, const char* row, fl
     for (int b = 8 * KT::kDigits - 2; b >= 0; b -= 2) {
         const uint32_t c1 = prefix | (1u << b), c2 = prefix | (2u << b), c3 = prefix | (3u << b);
         df m1{0.f, 0.f}, m2{0.f, 0.f}, m3{0.f, 0.f};
-        visit([&](uint32_t key, float v) {
+        auto take = [&](uint32_t key, const df& w) {
             if (key < c1) return;
-            const df w = weight(v);
             m1 = df_add(m1, w);
             if (key >= c2) m2 = df_add(m2, w);
             if (key >= c3) m3 = df_add(m3, w);
-        });
+        };
+        if (cached) {
+#pragma unroll
+            for (int i = 0; i < kNuReg; ++i) take(ck[i], cw[i]);
+        } else {
+            visit([&](uint32_t key, float v) {
+                if (key >= c1) take(key, weight(v));
+            });
+        }
         m1 = warp_sum_df(m1);
         m2 = warp_sum_df(m2);
         m3 = warp_sum_df(m3);
