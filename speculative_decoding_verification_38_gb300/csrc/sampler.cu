@@ -317,33 +317,37 @@ __device__ void tile_sums(const RowPair<TDT, DDT>& rp, bool resid, float r_hi, f
         src_load8<TDT>(rp.t, j, lt);
         if (resid) src_load8<DDT>(rp.d, j, ld);
         uint32_t m = 0, open = 0;
+        // branch-free per column: selects for the sums, predicated bits for
+        // the heavy and open masks (the same sums as the branching form)
+        if (!resid) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            bool ht, hd = false;
-            const float wt = light_weight<TDT == SPECV_F32>(lt[e], rp.mt, rp.k, ht);
-            if (!resid) {
-                if (ht) m |= 1u << e; else st_l = __fadd_rn(st_l, wt);
-                continue;
+            for (int e = 0; e < 8; ++e) {
+                bool ht;
+                const float wt = light_weight<TDT == SPECV_F32>(lt[e], rp.mt, rp.k, ht);
+                st_l = __fadd_rn(st_l, ht ? 0.f : wt);
+                m |= ht ? (1u << e) : 0u;
             }
-            float wd;
-            if (rp.probs) {
-                wd = ld[e] > -INFINITY ? ld[e] : 0.f;
-                hd = wd > 1.220703125e-4f;
-            } else {
-                wd = light_weight<DDT == SPECV_F32>(ld[e], rp.md, rp.k, hd);
-            }
-            if (ht || hd) {
-                m |= 1u << e;
-                continue;
-            }
-            st_l = __fadd_rn(st_l, wt);
-            sd_l = __fadd_rn(sd_l, wd);
-            if (wt > wd * r_hi) {  // certainly p > q
-                a_l = __fadd_rn(a_l, wt);
-                b_l = __fadd_rn(b_l, wd);
-            } else if (!(wt < wd * r_lo) && (wt != 0.f || wd != 0.f)) {
-                m |= 1u << e;
-                open |= 1u << e;
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                bool ht, hd = false;
+                const float wt = light_weight<TDT == SPECV_F32>(lt[e], rp.mt, rp.k, ht);
+                float wd;
+                if (rp.probs) {
+                    wd = ld[e] > -INFINITY ? ld[e] : 0.f;
+                    hd = wd > 1.220703125e-4f;
+                } else {
+                    wd = light_weight<DDT == SPECV_F32>(ld[e], rp.md, rp.k, hd);
+                }
+                const bool heavy = ht || hd;
+                const bool in = !heavy && wt > wd * r_hi;  // certainly p > q
+                const bool opn = !heavy && !in && !(wt < wd * r_lo) && (wt != 0.f || wd != 0.f);
+                st_l = __fadd_rn(st_l, heavy ? 0.f : wt);
+                sd_l = __fadd_rn(sd_l, heavy ? 0.f : wd);
+                a_l = __fadd_rn(a_l, in ? wt : 0.f);
+                b_l = __fadd_rn(b_l, in ? wd : 0.f);
+                m |= (heavy || opn) ? (1u << e) : 0u;
+                open |= opn ? (1u << e) : 0u;
             }
         }
         const auto code = [&](int bit) { return (int32_t)((j + bit) | ((open >> bit) & 1u ? kOpen : 0)); };
