@@ -17,7 +17,7 @@ from dataclasses import replace
 
 import numpy as np
 
-from .workloads import Workload
+from .workloads import TreeWorkload, Workload
 
 
 def seq_offset(rank: int, batch_per_rank: int) -> int:
@@ -59,5 +59,24 @@ def shard(w: Workload, rank: int, world: int) -> tuple[Workload, int]:
         kv_in=None if w.kv_in is None else w.kv_in[b0:b1],
         target_row_off=tro,
         draft_row_off=dro,
+    )
+    return part, b0
+
+
+def shard_tree(w: TreeWorkload, rank: int, world: int) -> tuple[TreeWorkload, int]:
+    """This rank's part of a host tree workload (its trees, node offsets
+    rebased to its first node) and its seq_offset."""
+    b0, b1 = shard_bounds(w.batch, rank, world)
+    off = np.asarray(w.node_off, dtype=np.int64)
+    n0, n1 = int(off[b0]), int(off[b1])
+    part = replace(
+        w,
+        batch=b1 - b0,
+        node_off=off[b0:b1 + 1] - n0,
+        parent=w.parent[n0:n1],
+        tokens=w.tokens[n0:n1],
+        target=w.target[n0:n1],
+        draft=None if w.draft is None else w.draft[n0:n1],
+        temperatures=None if w.temperatures is None else w.temperatures[b0:b1],
     )
     return part, b0

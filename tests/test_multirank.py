@@ -55,6 +55,45 @@ def _worker(rank, world, port, out_path):
         dist.destroy_process_group()
 
 
+def _tree_worker(rank, world, port, out_path):
+    sys.path.insert(0, ROOT)
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    import torch.distributed as dist
+
+    import oracle
+    from speculative_decoding_verification_38_gb300 import sharding
+    from speculative_decoding_verification_38_gb300 import workloads as wl
+
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        w = wl.ragged_tree_workload("sharded trees", config=11, batch=9, vocab=997, max_nodes=20, dtype="bf16",
+                                    sigma=0.7, temps=np.linspace(0.6, 1.4, 9).astype(np.float32))
+        part, off = sharding.shard_tree(w, rank, world)
+        res = oracle.tree_verify(part, seed=4, rnd=2, seq_offset=off)
+        got = [None] * world
+        dist.all_gather_object(got, {k: v.tolist() for k, v in res.items()})
+        if rank == 0:
+            whole = oracle.tree_verify(w, seed=4, rnd=2, seq_offset=0)
+            ok = True
+            for k in ("tokens", "path", "accepted", "status"):
+                ok = ok and np.array_equal(np.concatenate([np.asarray(g[k]) for g in got]), whole[k])
+            ok = ok and int(whole["accepted"].max()) >= 1
+            with open(out_path, "w") as f:
+                f.write("ok" if ok else "mismatch")
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_reproduce_the_unsplit_trees(tmp_path, orc):
+    """Tree verification sharded by tree with seq_offset draws what the
+    unsplit batch draws (the uniforms are keyed by the global tree index)."""
+    mp = pytest.importorskip("torch.multiprocessing")
+    out = tmp_path / "result.txt"
+    mp.spawn(_tree_worker, args=(2, _free_port(), str(out)), nprocs=2, join=True)
+    assert out.read_text() == "ok"
+
+
 def test_shard_bounds_cover_the_batch():
     from speculative_decoding_verification_38_gb300 import sharding
 
