@@ -133,9 +133,11 @@ static __device__ __noinline__ void exp2_table_init(Exp2Table& t) {
 }
 
 // 2^(xh + xl) in double-float for |xh| < 2^16 (the heavy range is [-13, ~0]).
-// Out of line: heavy weights are rare, and inlining this at every call site
-// would overflow the instruction cache.
-static __device__ __noinline__ df exp2_df(float xh, float xl, const Exp2Table& tab) {
+// The out-of-line exp2_df below is the one most call sites use: heavy
+// weights are rare, and inlining this at every call site would overflow the
+// instruction cache. A site that evaluates heavy columns in one place of its
+// own (already out of line) uses the inline body directly.
+__device__ __forceinline__ df exp2_df_inline(float xh, float xl, const Exp2Table& tab) {
     const float t = rintf(xh * 64.0f);                  // x = t/64 + r
     const int ti = (int)t;
     const int i = ti & 63;
@@ -153,6 +155,9 @@ static __device__ __noinline__ df exp2_df(float xh, float xl, const Exp2Table& t
     const float sc = __int_as_float((n + 127) << 23);   // 2^n, n in [-126, 127] here
     return df{__fmul_rn(w.hi, sc), __fmul_rn(w.lo, sc)};
 }
+static __device__ __noinline__ df exp2_df(float xh, float xl, const Exp2Table& tab) {
+    return exp2_df_inline(xh, xl, tab);
+}
 
 // Mean relative error of the SFU's 2^x over the light range x <= -13,
 // measured on GB300 (-5.1e-8, std 3.0e-8). A single fp32 weight cannot carry
@@ -165,12 +170,16 @@ __device__ __forceinline__ float light_exp2(float x) { return ex2(x); }
 __device__ __forceinline__ df light_sum_df(float s, float bias) { return df{s, __fmul_rn(s, bias)}; }
 
 // 2^((dh + dl) * k) in double-float, the exponent carried as a pair.
-static __device__ __noinline__ df heavy_weight(float dh, float dl, df k, const Exp2Table& tab) {
+template <bool INL>
+__device__ __forceinline__ df heavy_weight_t(float dh, float dl, df k, const Exp2Table& tab) {
     const float xh = __fmul_rn(dh, k.hi);
     float xl = __fmaf_rn(dh, k.hi, -xh);
     xl = __fmaf_rn(dh, k.lo, xl);
     xl = __fmaf_rn(dl, k.hi, xl);
-    return exp2_df(xh, xl, tab);
+    return INL ? exp2_df_inline(xh, xl, tab) : exp2_df(xh, xl, tab);
+}
+static __device__ __noinline__ df heavy_weight(float dh, float dl, df k, const Exp2Table& tab) {
+    return heavy_weight_t<false>(dh, dl, k, tab);
 }
 
 // Weight of one logit relative to the row maximum: 2^((l - lmax) * k).
@@ -179,7 +188,8 @@ static __device__ __noinline__ df heavy_weight(float dh, float dl, df k, const E
 // relative and average out in the sums. Heavy weights carry the exponent as a
 // pair (for fp32 logits, l - lmax itself is carried as a pair) and go through
 // the double-float exp2.
-template <bool FP32IN>
+// INL: the heavy path inline (for sites that are themselves out of line).
+template <bool FP32IN, bool INL = false>
 __device__ __forceinline__ df logit_weight(float l, float lmax, df k, const Exp2Table& tab) {
     const float dh = __fsub_rn(l, lmax);
     if (!(dh > -INFINITY)) return df{0.f, 0.f};  // -inf logits (and masked columns) weigh nothing
@@ -187,6 +197,7 @@ __device__ __forceinline__ df logit_weight(float l, float lmax, df k, const Exp2
     if constexpr (FP32IN) dl = two_sum(l, -lmax).lo;  // fp32 logits: l - lmax exactly, as a pair
     const float x = __fmaf_rn(dh, k.hi, __fmaf_rn(dl, k.hi, __fmul_rn(dh, k.lo)));
     if (!(x > kHeavyExp)) return df{light_exp2(x), 0.f};
+    if constexpr (INL) return heavy_weight_t<true>(dh, dl, k, tab);
     return heavy_weight(dh, dl, k, tab);
 }
 

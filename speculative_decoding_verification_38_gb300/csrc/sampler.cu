@@ -265,6 +265,22 @@ __device__ __forceinline__ RowPair<TDT, DDT> tile_rows(const SampleParams& p, co
     return rp;
 }
 
+// The double-float weights (target, and draft for a residual) of one queued
+// column, out of line with the heavy path inline inside it: the queue's three
+// evaluation sites share this one copy and pay one call per column. The same
+// arithmetic as RowPair::wt / wd.
+template <int TDT, int DDT>
+__device__ __noinline__ float4 col_weights(const char* tg, const char* dg, float tau_t, float tau_d, float mt, float md,
+                                           df k, bool probs, bool resid, int64_t j, const Exp2Table& tab) {
+    const df wt = logit_weight<TDT == SPECV_F32, true>(keep_top(ld_elem<TDT>(tg, j), tau_t), mt, k, tab);
+    df wd{0.f, 0.f};
+    if (resid) {
+        const float l = keep_top(ld_elem<DDT>(dg, j), tau_d);
+        wd = probs ? df{(l > -INFINITY) ? l : 0.f, 0.f} : logit_weight<DDT == SPECV_F32, true>(l, md, k, tab);
+    }
+    return make_float4(wt.hi, wt.lo, wd.hi, wd.lo);
+}
+
 // Phase 1 for one tile: this lane's sums (double-float) over its columns.
 struct TileAcc {
     df st, sd, a, b;
@@ -284,12 +300,14 @@ __device__ void tile_sums(const RowPair<TDT, DDT>& rp, bool resid, float r_hi, f
     // one queued column: double-float weights, then the support decision
     auto eval = [&](int32_t code) {
         const int64_t j = code & (kOpen - 1);
-        const df wt = rp.wt(src_elem<TDT>(rp.t, j), sm.tab);
+        const float4 w4 = col_weights<TDT, DDT>(rp.t.g, rp.d.g, rp.t.tau, rp.d.tau, rp.mt, rp.md, rp.k, rp.probs, resid,
+                                                j, sm.tab);
+        const df wt{w4.x, w4.y};
         if (!resid) {
             acc_add(st_h, wt);
             return;
         }
-        const df wd = rp.wd(src_elem<DDT>(rp.d, j), sm.tab);
+        const df wd{w4.z, w4.w};
         if (!(code & kOpen)) {
             acc_add(st_h, wt);
             acc_add(sd_h, wd);
