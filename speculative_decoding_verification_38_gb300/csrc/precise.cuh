@@ -220,11 +220,13 @@ __device__ __forceinline__ float light_weight(float l, float lmax, df k, bool& h
     return light_exp2(x);
 }
 
-// The double-float weight of a heavy logit.
-template <bool FP32IN>
+// The double-float weight of a heavy logit (INL: the exp2 inline).
+template <bool FP32IN, bool INL = false>
 __device__ __forceinline__ df heavy_logit_weight(float l, float lmax, df k, const Exp2Table& tab) {
     const float dh = __fsub_rn(l, lmax);
-    return heavy_weight(dh, FP32IN ? two_sum(l, -lmax).lo : 0.f, k, tab);
+    const float dl = FP32IN ? two_sum(l, -lmax).lo : 0.f;
+    if constexpr (INL) return heavy_weight_t<true>(dh, dl, k, tab);
+    return heavy_weight(dh, dl, k, tab);
 }
 
 // Residual weight of one column: max(0, Wt * It - Wd * Id).

@@ -216,7 +216,7 @@ template <int TDT, int DDT>
 __device__ __forceinline__ bool tgt_col(const Rows<TDT, DDT>& n, float l, const TreeSmem& sm, float& lw, df& hw) {
     bool h;
     lw = light_weight<TDT == SPECV_F32>(l, n.mt, n.k, h);
-    if (h) hw = heavy_logit_weight<TDT == SPECV_F32>(l, n.mt, n.k, sm.tab);
+    if (h) hw = heavy_logit_weight<TDT == SPECV_F32, true>(l, n.mt, n.k, sm.tab);
     return h;
 }
 
@@ -230,7 +230,7 @@ __device__ __forceinline__ bool dft_col(const Rows<TDT, DDT>& n, float l, const 
     }
     bool h;
     lw = light_weight<DDT == SPECV_F32>(l, n.md, n.k, h);
-    if (h) hw = heavy_logit_weight<DDT == SPECV_F32>(l, n.md, n.k, sm.tab);
+    if (h) hw = heavy_logit_weight<DDT == SPECV_F32, true>(l, n.md, n.k, sm.tab);
     return h;
 }
 
@@ -827,7 +827,7 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTrThreads) tree_k
         const bool DL = D && !n.probs;
         df sdl{0.f, 0.f};
         auto tgt_heavy = [&](int64_t c) {
-            return heavy_logit_weight<TDT == SPECV_F32>(ld_elem<TDT>(n.t, c), n.mt, n.k, sm.tab);
+            return heavy_logit_weight<TDT == SPECV_F32, true>(ld_elem<TDT>(n.t, c), n.mt, n.k, sm.tab);
         };
         auto tgt_seg = [&](int64_t i, int64_t j, const float (&t)[8]) {
             const df v = warp_sum_dfx(
@@ -836,7 +836,7 @@ __global__ void __cluster_dims__(kCS, 1, 1) __launch_bounds__(kTrThreads) tree_k
         };
         if (DL) {  // the draft row is read only when its logits need a normaliser
             auto dft_heavy = [&](int64_t c) {
-                return heavy_logit_weight<DDT == SPECV_F32>(ld_elem<DDT>(n.d, c), n.md, n.k, sm.tab);
+                return heavy_logit_weight<DDT == SPECV_F32, true>(ld_elem<DDT>(n.d, c), n.md, n.k, sm.tab);
             };
             seg_pass<true>(n, V, pt, [&](int64_t i, int64_t j, const float (&t)[8], const float (&d)[8]) {
                 tgt_seg(i, j, t);
