@@ -16,11 +16,16 @@
 // at (u, ...), so a chain-shaped tree draws exactly what the chain verify
 // draws.
 //
-// One CTA per sequence walks its tree. At a visited node:
+// A cluster of two CTAs per sequence walks its tree, each CTA taking half of
+// the columns; their partial sums meet through distributed shared memory.
+// At a visited node:
 //   - pass 1 reads the target row (and, with candidates, the draft row) for
-//     the maxima and the NaN checks (a probability row: its sum);
-//   - pass 2 takes the double-float normalisers and keeps the target's sums
-//     over 256-column segments in shared memory;
+//     the maxima and the NaN checks (a probability row: its sum), and, with
+//     candidates, float softmax sums for the first candidate's test, which
+//     runs in float as the chain's accept test does;
+//   - if that candidate fails (and at a leaf), pass 2 takes the double-float
+//     normalisers and keeps the target's sums over 256-column segments in
+//     shared memory;
 //   - a rejected candidate costs one residual pass, which takes the next
 //     normaliser and keeps the residual's segment sums;
 //   - the final draw scans the kept segment sums of the distribution it
