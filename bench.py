@@ -50,7 +50,7 @@ def parse():
     ap.add_argument("--top-k", type=int, default=0,
                     help="truncate every target and draft row to its top k (0: plain sampling, the headline)")
     ap.add_argument("--top-p", type=float, default=0.0,
-                    help="with --top-k: also keep each row's top-p nucleus inside the top-k set (0: off)")
+                    help="keep each row's top-p nucleus (inside the top-k set with --top-k, else of the whole row; 0: off)")
     ap.add_argument("--ngram", action="store_true",
                     help="time the n-gram (prompt lookup) drafter instead of the verify step")
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5],
@@ -78,9 +78,13 @@ KERNELS = {
 }
 
 
+def topp_on(args):
+    return 0 < args.top_p < 1
+
+
 def mode_of(args):
-    if args.top_k > 0:
-        return "topp" if 0 < args.top_p < 1 else "topk"
+    if args.top_k > 0 or topp_on(args):
+        return "topp" if topp_on(args) else "topk"
     return "stats"
 
 
@@ -101,18 +105,21 @@ L2_BYTES = 129 << 20
 def metric_of(args):
     if args.config != 3:
         return CONFIGS[args.config][1]
-    if args.top_k <= 0:
+    if args.top_k <= 0 and not topp_on(args):
         return METRIC
-    return METRIC[:-1] + f", top-k {args.top_k}" + (f", top-p {args.top_p}" if 0 < args.top_p < 1 else "") + ")"
+    tk = f", top-k {args.top_k}" if args.top_k > 0 else ""
+    return METRIC[:-1] + tk + (f", top-p {args.top_p}" if topp_on(args) else "") + ")"
 
 
 def workload_of(args):
     if args.config != 3:
         return CONFIGS[args.config][0]
-    if args.top_k <= 0:
+    if args.top_k <= 0 and not topp_on(args):
         return WORKLOAD
+    if args.top_k <= 0:
+        return WORKLOAD + f", both models truncated to their top-p {args.top_p} nucleus (no top-k)"
     w = WORKLOAD + f", both models truncated to top-k {args.top_k}"
-    return w + (f" then top-p {args.top_p}" if 0 < args.top_p < 1 else "")
+    return w + (f" then top-p {args.top_p}" if topp_on(args) else "")
 
 
 def dist_env():
@@ -236,9 +243,9 @@ def run_ours(args):
 
     mode = mode_of(args)
     if args.config == 3:
-        w = wl.config3(top_k=args.top_k, top_p=args.top_p if args.top_k > 0 else 0.0)
+        w = wl.config3(top_k=args.top_k, top_p=args.top_p)
     else:
-        if args.top_k > 0 or args.adaptive:
+        if args.top_k > 0 or topp_on(args) or args.adaptive:
             raise SystemExit("--top-k, --top-p and --adaptive apply to the C3 workload only")
         w = wl.CONFIGS[args.config]()
     greedy = w.greedy
@@ -356,8 +363,10 @@ def run_ours(args):
         "sequence_rounds_per_s": rounds_per_s * B,
         "step_hbm_gbs": rounds_per_s / world * algo_bytes / 1e9,
         # row pass and finalize; sampling adds the sampler tile pass and the draw
-        # (+ the nucleus kernel with top-p, + the gamma policy with --adaptive)
-        "gpu_launches": ((2 if greedy else 4) + (1 if mode == "topp" else 0) + (1 if args.adaptive else 0)) * K,
+        # (+ the nucleus kernel with top-p, + the whole-row kernel for top-p
+        # without top-k, + the gamma policy with --adaptive)
+        "gpu_launches": ((2 if greedy else 4) + (1 if mode == "topp" else 0) + (1 if mode == "topp" and args.top_k <= 0 else 0)
+                         + (1 if args.adaptive else 0)) * K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": KERNELS[mode]["name"], "kernel_ms": kern_ms,
@@ -761,7 +770,7 @@ def run_reference(args):
 
     oracle.build()
     if args.config == 3:
-        w = wl.config3(top_k=args.top_k, top_p=args.top_p if args.top_k > 0 else 0.0)
+        w = wl.config3(top_k=args.top_k, top_p=args.top_p)
     else:
         w = wl.CONFIGS[args.config]()
     cores = os.cpu_count() or 1

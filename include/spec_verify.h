@@ -72,13 +72,12 @@ enum {
     SPEC_SEQ_BAD_TEMP = 5,   /* temperature of sequence b not finite and > 0 */
     SPEC_SEQ_TIMEOUT = 6,    /* a bounded on-device wait for a copy gave up (the draw
                                 is left at -1); never expected on a healthy GPU */
-    SPEC_SEQ_UNSUPPORTED = 7 /* top-p asked for without top-k (see top_p below); for
-                                spec_tree_verify, a visited node with more than
+    SPEC_SEQ_UNSUPPORTED = 7 /* spec_tree_verify: a visited node with more than
                                 SPEC_TREE_MAX_CANDIDATES children */
 };
-/* Precedence when several apply: LAYOUT, TEMP (sampling only), UNSUPPORTED
- * (sampling only), TOKEN, KV, then ROW for the first bad row met while
- * scanning positions left to right. */
+/* Precedence when several apply (the verify calls): LAYOUT, TEMP (sampling
+ * only), TOKEN, KV, then ROW for the first bad row met while scanning
+ * positions left to right. */
 
 /*
  * Arguments of one batched verify call.
@@ -177,18 +176,19 @@ typedef struct {
     float* accept_ema; /* device [B] or NULL */
     float ema_lambda;
 
-    /* Top-p (nucleus) after top-k (sampling only; greedy ignores it):
-     * sequence b uses p_b = top_ps[b] if top_ps != NULL, else top_p; active
-     * for 0 < p_b < 1 (otherwise, and for NaN, off). Over the columns top-k
-     * kept, each row keeps the columns whose value is at least the value of
-     * the first group of equal values, in decreasing order, at which the
-     * cumulative probability reaches p_b (the whole group stays), on target
-     * and draft rows alike ("Speculative decoding" (mhtirogla.ai),
-     * Implementation notes: the same temperature, top-k and top-p
-     * processing). The masses are double-float. A sequence asking for top-p
-     * without top-k (k_b <= 0 or k_b >= V) gets SPEC_SEQ_UNSUPPORTED: the
-     * nucleus is computed only inside a top-k set. Zero-initialise both for
-     * no top-p. */
+    /* Top-p (nucleus), after top-k or alone (sampling only; greedy ignores
+     * it): sequence b uses p_b = top_ps[b] if top_ps != NULL, else top_p;
+     * active for 0 < p_b < 1 (otherwise, and for NaN, off). Over the columns
+     * top-k kept (every column when top-k is off for the sequence), each row
+     * keeps the columns whose value is at least the value of the first group
+     * of equal values, in decreasing order, at which the cumulative
+     * probability reaches p_b (the whole group stays), on target and draft
+     * rows alike ("Speculative decoding" (mhtirogla.ai), Implementation
+     * notes: the same temperature, top-k and top-p processing). The masses
+     * are double-float. Without top-k, one CTA per row takes the nucleus of
+     * the whole row by two-bit bisection on the value's bits, reading the row
+     * once per round (8 rounds for bf16 rows, 16 for f32). Zero-initialise
+     * both for no top-p. */
     float top_p;
     const float* top_ps; /* device [B] or NULL */
 } spec_verify_args_t;

@@ -36,10 +36,9 @@
  *     [P1] Implementation notes asks of any logits processing): keep every
  *     column whose value is at least the row's k-th largest (NaN ranks as
  *     -inf; ties at the threshold all stay), renormalise over the kept ones;
- *   - top-p after top-k (the same note): the nucleus of the top-k-renormalised
- *     distribution (see orc_topp_threshold); asked for without top-k it is
- *     reported as ORC_SEQ_UNSUPPORTED (this library computes the nucleus
- *     only inside a top-k set).
+ *   - top-p (the same note): the nucleus of the top-k-renormalised
+ *     distribution (see orc_topp_threshold), or of the whole row when top-k
+ *     is off.
  */
 #include <math.h>
 #include <pthread.h>
@@ -57,7 +56,7 @@
 #define ORC_SEQ_BAD_ROW 3
 #define ORC_SEQ_BAD_LAYOUT 4
 #define ORC_SEQ_BAD_TEMP 5
-#define ORC_SEQ_UNSUPPORTED 7 /* top-p asked for without top-k */
+#define ORC_SEQ_UNSUPPORTED 7 /* tree verification: a visited node with too many candidates */
 
 /* ------------------------------------------------------------------ */
 /* Element access: bf16 is the top half of an IEEE binary32, so widening */
@@ -381,8 +380,8 @@ typedef struct {
      * top_ks[b] if top_ks, else top_k; k_b <= 0 or k_b >= V keeps every column */
     int32_t top_k;
     const int32_t* top_ks;
-    /* top-p after top-k: p_b = top_ps[b] if top_ps, else top_p; active when
-     * 0 < p_b < 1; needs top-k active for the sequence */
+    /* top-p (inside the top-k set when top-k is on, else over the whole
+     * row): p_b = top_ps[b] if top_ps, else top_p; active when 0 < p_b < 1 */
     float top_p;
     const float* top_ps;
 } orc_args_t;
@@ -406,10 +405,6 @@ static int64_t top_k_of(const orc_args_t* a, int64_t b) { return a->top_ks ? a->
 static double top_p_of(const orc_args_t* a, int64_t b) {
     return a->top_ps ? (double)a->top_ps[b] : (double)a->top_p;
 }
-static int topk_on(const orc_args_t* a, int64_t b) {
-    const int64_t k = top_k_of(a, b);
-    return k >= 1 && k < a->vocab;
-}
 
 static int32_t precheck(const orc_args_t* a, int64_t b, int greedy, int64_t* g_out, double* T_out) {
     int64_t t0 = toff(a, b), t1 = toff(a, b + 1), d0 = doff(a, b), d1 = doff(a, b + 1);
@@ -421,8 +416,6 @@ static int32_t precheck(const orc_args_t* a, int64_t b, int greedy, int64_t* g_o
     double T = a->temperatures ? (double)a->temperatures[b] : (double)a->temperature;
     *T_out = T;
     if (!greedy && (!(T > 0.0) || !isfinite(T))) return ORC_SEQ_BAD_TEMP;
-    const double tp = top_p_of(a, b);
-    if (!greedy && tp > 0.0 && tp < 1.0 && !topk_on(a, b)) return ORC_SEQ_UNSUPPORTED;
     for (int64_t i = 0; i < g; ++i) {
         int32_t x = a->draft_tokens[d0 + i];
         if (x < 0 || x >= a->vocab) return ORC_SEQ_BAD_TOKEN;

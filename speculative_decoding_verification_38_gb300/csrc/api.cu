@@ -75,6 +75,7 @@ cudaError_t topk_with_hook(const StatsParams& p, cudaStream_t s) {
     cudaError_t e = launch_topk(p, s);
     if (e != cudaSuccess) return e;
     if (e0 && e1 && cudaEventRecord(e1, s) != cudaSuccess) return cudaErrorUnknown;
+    if (p.keep && (e = launch_alone(p, s)) != cudaSuccess) return e;
     if (p.keep && (e = launch_nucleus(p, s)) != cudaSuccess) return e;
     return launch_finalize(p, s);
 }

@@ -37,7 +37,7 @@ constexpr size_t kHeaderBytes = (size_t)kMaxBatch * 4 + 256;  // arrival counter
 constexpr size_t kErrWordOffset = (size_t)kMaxBatch * 4;        // device error flags (bit 0: a wait timed out)
 
 constexpr int kSeqTimeout = 6;                                   // per-sequence status after a timed-out wait
-constexpr int kSeqUnsupported = 7;                               // per-sequence status: top-p without top-k
+constexpr int kSeqUnsupported = 7;                               // per-sequence status: a tree node with too many candidates
 constexpr int kKeepCap = 1024;  // top-k-kept values stored per row for the nucleus (top-p) kernel
 constexpr int64_t kMaxVocab = 2097152;                            // largest vocabulary (2^21 columns)
 
@@ -107,7 +107,7 @@ struct StatsParams {
     float* ema;          // [B] running acceptance (float32, updated in place), or null
     float ema_lambda;
     // top-p after top-k (sampling only): sequence b's p_b = top_ps[b] if
-    // top_ps, else top_p; active for 0 < p_b < 1, and only with top-k active
+    // top_ps, else top_p; active for 0 < p_b < 1 (inside the top-k set, or over the whole row without top-k)
     const float* top_ps;
     float top_p;
     Exp2Pairs tab;       // 2^(i/64) for the double-float weights of the nucleus
@@ -169,6 +169,9 @@ cudaError_t launch_topk(const StatsParams& p, cudaStream_t s);
 // rewriting p.tau and the row sums; chained between launch_topk and
 // launch_finalize by programmatic launch.
 cudaError_t launch_nucleus(const StatsParams& p, cudaStream_t s);
+// Rows with top-p and no top-k: the nucleus of the whole row, one CTA per
+// row; chained after launch_topk (programmatic launch).
+cudaError_t launch_alone(const StatsParams& p, cudaStream_t s);
 cudaError_t launch_sampler(const SampleParams& p, cudaStream_t s, bool pdl);
 void exp2_pairs(Exp2Pairs& t);  // host: fills the table
 cudaError_t launch_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,

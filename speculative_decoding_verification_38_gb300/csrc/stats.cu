@@ -1077,11 +1077,6 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
         kv = p.kv_in ? __ldg(p.kv_in + b) : 0;
         int32_t st = 0;
         if (!p.greedy && (!(T > 0.f) || !isfinite(T))) st = 5;  // SPEC_SEQ_BAD_TEMP
-        if (!st && !p.greedy) {  // top-p asked for without top-k
-            const float tp = p.top_ps ? __ldg(p.top_ps + b) : p.top_p;
-            const int64_t kb = p.top_ks ? (int64_t)__ldg(p.top_ks + b) : (int64_t)p.top_k;
-            if (tp > 0.f && tp < 1.f && !(kb >= 1 && kb < p.V)) st = kSeqUnsupported;
-        }
         if (!st) {
             bool bad = false;
 #pragma unroll

@@ -28,7 +28,10 @@
 //
 // With top-p as well, a top-p row's kept values go to the workspace and a
 // second kernel (nucleus_kernel) takes the nucleus inside them, one warp per
-// row, with the loads done: the streaming pass keeps no serial tail.
+// row, with the loads done: the streaming pass keeps no serial tail. A row
+// with top-p but no top-k passes through this pass whole (its maximum and
+// sum) and a third kernel (alone_kernel) takes the nucleus of the whole row,
+// one CTA per row.
 #include <math.h>
 
 #include "precise.cuh"
@@ -615,6 +618,332 @@ __global__ void __launch_bounds__(kTkThreads, 4) topk_kernel(StatsParams p) {
         row_topk<SPECV_BF16>(p, r, row, kk, off, probs_row, k2, tp, sm);
 }
 
+// ------------------------------------------------- top-p without top-k
+// One CTA of 1024 threads per SM: about 152 rows are in flight at a time
+// (39 MB of bf16 rows at V = 128256), so the passes after the first read
+// their row from L2.
+constexpr int kAlThreads = 1024, kAlWarps = kAlThreads / 32;
+constexpr int kAlBinBits = 14, kAlBins = 1 << kAlBinBits;  // one narrowing pass's float histogram
+constexpr int kAlBinsPerThread = kAlBins / kAlThreads;
+constexpr size_t kAlSmemBytes = kAlBins * sizeof(float);   // dynamic: the histogram
+
+// Shared memory of alone_kernel (besides the histogram).
+struct AloneSmem {
+    Exp2Table tab;
+    df dsum[2][5][kAlWarps];  // block sums, double-buffered
+    float fsum[2][5][kAlWarps];
+    float wtot[kAlWarps];     // histogram choice: each warp's bins
+    int bin;                  // histogram choice: the bin
+    float bin_above;          // histogram choice: the float mass above the bin
+};
+
+// f(v) for each value of one 16-byte vector, in column order.
+template <int DT, typename F>
+__device__ __forceinline__ void vec_each(const uint4& q, F&& f) {
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        if constexpr (DT == SPECV_BF16) {
+            f(bf16_lo(w[e]));
+            f(bf16_hi(w[e]));
+        } else {
+            f(__uint_as_float(w[e]));
+        }
+    }
+}
+
+// N double-float and N float sums over the CTA in a fixed order; par
+// alternates between calls, so one barrier per call suffices.
+template <int N>
+__device__ void block_sum(df (&d)[N], float (&f)[N], int par, AloneSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            d[i] = df_add(d[i], shfl_xor_df(d[i], o));
+            f[i] += __shfl_xor_sync(kFull, f[i], o);
+        }
+    }
+    if (lane == 0)
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            sm.dsum[par][i][warp] = d[i];
+            sm.fsum[par][i][warp] = f[i];
+        }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        d[i] = df{0.f, 0.f};
+        f[i] = 0.f;
+#pragma unroll 8
+        for (int w = 0; w < kAlWarps; ++w) {
+            d[i] = df_add(d[i], sm.dsum[par][i][w]);
+            f[i] += sm.fsum[par][i][w];
+        }
+    }
+}
+
+// One narrowing choice over the float histogram, for the whole CTA: the
+// highest bin j with above + (the bins from j up) >= target, else bin 0.
+// above becomes the float mass above bin j. With first, target is first set
+// to top_p of above + every bin. Each thread sums its own bins and the warps
+// combine from the top, in a fixed order. The choice is a guess that the
+// double-float pass checks.
+__device__ int hist_pick(const float* hist, float& above, float& target, bool first, float tp, AloneSmem& sm) {
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    float loc[kAlBinsPerThread];
+    const float4* h4 = reinterpret_cast<const float4*>(hist) + t * (kAlBinsPerThread / 4);
+    float cs = 0.f;
+#pragma unroll
+    for (int i = 0; i < kAlBinsPerThread / 4; ++i) {
+        const float4 q = h4[i];
+        loc[4 * i] = q.x;
+        loc[4 * i + 1] = q.y;
+        loc[4 * i + 2] = q.z;
+        loc[4 * i + 3] = q.w;
+    }
+#pragma unroll
+    for (int i = 0; i < kAlBinsPerThread; ++i) cs += loc[i];
+    float x = cs;  // this lane's bins and every higher lane's
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_down_sync(kFull, x, o);
+        if (lane + o < 32) x += y;
+    }
+    float ex = __shfl_down_sync(kFull, x, 1);  // the higher lanes' alone
+    if (lane == 31) ex = 0.f;
+    if (lane == 0) sm.wtot[warp] = x;
+    if (t == 0) sm.bin = 0;
+    __syncthreads();
+    float up = above, all = above;  // above + the higher warps' bins; above + every bin
+    for (int w = kAlWarps - 1; w >= 0; --w) {
+        const float v = sm.wtot[w];
+        if (w > warp) up += v;
+        all += v;
+    }
+    if (first) target = tp * all;
+    const float base = up + ex;  // above + every bin above this thread's
+    float run = base;
+    int cand = -1;
+#pragma unroll
+    for (int i = kAlBinsPerThread - 1; i >= 0; --i) {
+        run += loc[i];
+        if (cand < 0 && !(target > run)) cand = t * kAlBinsPerThread + i;
+    }
+    if (cand >= 0) atomicMax(&sm.bin, cand);
+    __syncthreads();
+    const int j = sm.bin;
+    if (t == j / kAlBinsPerThread) {  // the bin's thread: the mass above the bin, summed as in the search
+        float a = base;
+#pragma unroll
+        for (int i = kAlBinsPerThread - 1; i >= 0; --i)
+            if (i > j % kAlBinsPerThread) a += loc[i];
+        sm.bin_above = a;
+    }
+    __syncthreads();
+    above = sm.bin_above;
+    return j;
+}
+
+// The nucleus of a whole row (top-p without top-k): the largest key K whose
+// values at or above it carry at least top_p of the row's double-float mass
+// (the nucleus kernel's weights and decision).
+//  1. Float narrowing: each pass spreads the float mass of the keys in
+//     [P, P + 2^R) over kAlBins bins of 2^(R-14) keys and keeps the bin where
+//     the float mass from the top reaches top_p of the row's, until R <= 4
+//     (one pass for bf16 keys, two for f32). The first pass also sums the
+//     row's double-float mass for the target.
+//  2. Double-float two-bit bisection over the kept range. Its first round
+//     also weighs the keys above the range and checks that the target falls
+//     inside it: mass(>= P) >= target > mass(>= P + 2^R). If the float guess
+//     was wrong, the bisection runs again over the whole key range.
+// Each round's range [prefix, hi) holds the keys still undecided; the mass of
+// the keys at or above hi is carried. Float sums of the sampler's weights go
+// along, for the row's sum over the nucleus.
+template <int DT>
+__device__ void row_nucleus_whole(const StatsParams& p, int64_t r, const char* row, float T, float tp, bool probs_row,
+                                  AloneSmem& sm, float* hist) {
+    using KT = KeyTraits<DT>;
+    constexpr int ESZ = KT::kEsz, EPV = 16 / ESZ, W = 8 * KT::kDigits;
+    const float2 rs = __ldcg(p.row_stats + r);
+    if (!(rs.y == rs.y)) return;  // an invalid row stays invalid
+    const float m = rs.x;
+    const int64_t V = p.V;
+    const df kd = k_of_temperature(T);
+    const float k2 = kLog2e / T, nmk = -__fmul_rn(m, k2);
+    auto weight = [&](float v) -> df {
+        return probs_row ? df{v, 0.f} : logit_weight<DT == SPECV_F32>(v, m, kd, sm.tab);
+    };
+    // 16-byte vectors from the row's first 16-byte boundary; the columns
+    // before it (head) and after the last full vector (from tail0) one by one
+    int64_t head = (int64_t)(((16u - (uint32_t)((uintptr_t)row & 15u)) & 15u) / ESZ);
+    if (head > V) head = V;
+    const int64_t nvec = (V - head) / EPV, tail0 = head + nvec * EPV;
+    const uint4* vrow = reinterpret_cast<const uint4*>(row + head * ESZ);
+    auto each = [&](auto&& f) {  // f(v) for every value of the row
+        for (int64_t vi = threadIdx.x; vi < nvec; vi += 2 * kAlThreads) {  // two loads in flight
+            const bool two = vi + kAlThreads < nvec;
+            const uint4 q0 = __ldcg(vrow + vi);
+            const uint4 q1 = two ? __ldcg(vrow + vi + kAlThreads) : make_uint4(0u, 0u, 0u, 0u);
+            vec_each<DT>(q0, f);
+            if (two) vec_each<DT>(q1, f);
+        }
+        if (threadIdx.x < head) f(ld_elem<DT>(row, threadIdx.x));
+        if (tail0 + threadIdx.x < V) f(ld_elem<DT>(row, tail0 + threadIdx.x));
+    };
+
+    // 1. float narrowing
+    df target{0.f, 0.f};
+    uint32_t P = 0;
+    int R = W, par = 0;
+    float above_h = 0.f, target_f = 0.f;
+#pragma unroll 1
+    while (R > 4) {
+        const int s = R - kAlBinBits;
+        const bool first = R == W;
+        const uint64_t span = 1ull << R;
+        for (int i = threadIdx.x; i < kAlBins; i += kAlThreads) hist[i] = 0.f;
+        __syncthreads();
+        df tot[1] = {{0.f, 0.f}};
+        float unused[1] = {0.f};
+        each([&](float v) {
+            const uint32_t key = key_of_value<DT>(v);
+            if (first) tot[0] = df_add(tot[0], weight(v));
+            const uint32_t off = key - P;  // wraps above span for key < P
+            if ((uint64_t)off >= span) return;
+            const float fw = kept_weight(v, probs_row, k2, nmk);
+            if (fw > 0.f) atomicAdd(hist + (off >> s), fw);
+        });
+        if (first) {
+            block_sum<1>(tot, unused, par, sm);
+            par ^= 1;
+            target = df_mul_f(tot[0], tp);
+        }
+        __syncthreads();  // the histogram is complete
+        const int j = hist_pick(hist, above_h, target_f, first, tp, sm);
+        P += (uint32_t)j << s;
+        R = s;
+    }
+
+    // 2. double-float bisection
+    df above{0.f, 0.f};
+    float above_f = 0.f, nucleus_f = 0.f;
+    uint32_t prefix = P;
+#pragma unroll 1
+    for (int attempt = 0; attempt < 2; ++attempt) {
+        const int b0 = attempt ? W - 2 : R - 2;
+        if (attempt) {  // the float guess was wrong: the whole key range
+            prefix = 0;
+            above = df{0.f, 0.f};
+            above_f = 0.f;
+        }
+        bool ok = true;
+#pragma unroll 1
+        for (int b = b0; b >= 0; b -= 2) {
+            const bool edge = attempt == 0 && b == b0;  // also weigh the keys at or above hi
+            const uint32_t c1 = prefix | (1u << b), c2 = prefix | (2u << b), c3 = prefix | (3u << b);
+            const uint64_t hi = (uint64_t)prefix + (4ull << b);
+            // d[i] / f[i], i < 4: the range's values at or above c_i (c_0 = prefix);
+            // d[4] / f[4]: the values at or above hi (edge round)
+            df d[5] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
+            float f[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+            each([&](float v) {
+                const uint32_t key = key_of_value<DT>(v);
+                if ((uint64_t)key >= hi) {
+                    if (edge) {
+                        d[4] = df_add(d[4], weight(v));
+                        f[4] += kept_weight(v, probs_row, k2, nmk);
+                    }
+                    return;
+                }
+                if (key < prefix) return;
+                const df w = weight(v);
+                const float fw = kept_weight(v, probs_row, k2, nmk);
+                d[0] = df_add(d[0], w);
+                f[0] += fw;
+                if (key >= c1) {
+                    d[1] = df_add(d[1], w);
+                    f[1] += fw;
+                }
+                if (key >= c2) {
+                    d[2] = df_add(d[2], w);
+                    f[2] += fw;
+                }
+                if (key >= c3) {
+                    d[3] = df_add(d[3], w);
+                    f[3] += fw;
+                }
+            });
+            block_sum<5>(d, f, par, sm);
+            par ^= 1;
+            if (edge) {
+                above = d[4];
+                above_f = f[4];
+                if (!df_gt(target, above) || df_gt(target, df_add(above, d[0]))) {  // the same in every thread
+                    ok = false;
+                    break;
+                }
+            }
+            const df t3 = df_add(above, d[3]), t2 = df_add(above, d[2]), t1 = df_add(above, d[1]);
+            if (!df_gt(target, t3)) {
+                prefix = c3;
+                nucleus_f = above_f + f[3];
+            } else if (!df_gt(target, t2)) {
+                prefix = c2;
+                above = t3;
+                nucleus_f = above_f + f[2];
+                above_f += f[3];
+            } else if (!df_gt(target, t1)) {
+                prefix = c1;
+                above = t2;
+                nucleus_f = above_f + f[1];
+                above_f += f[2];
+            } else {
+                above = t1;
+                nucleus_f = above_f + f[0];
+                above_f += f[1];
+            }
+        }
+        if (ok) break;
+    }
+    if (threadIdx.x == 0) {
+        p.row_stats[r] = make_float2(rs.x, nucleus_f);
+        p.tau[r] = KT::value(KT::bits_of_key(prefix));
+    }
+}
+
+// Rows with top-p and no top-k, after the top-k pass (which gave them their
+// maximum): the nucleus of the whole row. One CTA per row; the other rows
+// return at once.
+__global__ void __launch_bounds__(kAlThreads, 1) alone_kernel(StatsParams p) {
+    __shared__ AloneSmem sm;
+    extern __shared__ float4 al_hist[];
+    pdl_launch_dependents();
+    pdl_wait_primary();  // the top-k pass's row statistics
+    const int64_t r = blockIdx.x;
+    const bool is_t = r < p.rows_t;
+    const int64_t lr = is_t ? r : r - p.rows_t;
+    const int32_t b = row_seq(p, !is_t, lr);
+    if (b < 0) return;
+    const int64_t kk = p.top_ks ? (int64_t)__ldg(p.top_ks + b) : (int64_t)p.top_k;
+    const float tp = p.top_ps ? __ldg(p.top_ps + b) : p.top_p;
+    if ((kk >= 1 && kk < p.V) || !(tp > 0.f && tp < 1.f)) return;  // top-k on, or no top-p
+    float T = p.temps ? __ldg(p.temps + b) : p.temperature;
+    if (!(T > 0.f) || !isfinite(T)) T = 1.f;  // the finalize reports the sequence's bad temperature
+    const int dt = is_t ? p.tdt : p.ddt;
+    const bool probs_row = !is_t && p.probs != 0;
+    const char* row = (const char*)(is_t ? p.tgt : p.dft) + lr * p.V * (dt == SPECV_F32 ? 4 : 2);
+    if (threadIdx.x < 64) {
+        sm.tab.hi[threadIdx.x] = p.tab.hi[threadIdx.x];
+        sm.tab.lo[threadIdx.x] = p.tab.lo[threadIdx.x];
+    }
+    __syncthreads();
+    float* hist = reinterpret_cast<float*>(al_hist);
+    if (dt == SPECV_F32) row_nucleus_whole<SPECV_F32>(p, r, row, T, tp, probs_row, sm, hist);
+    else row_nucleus_whole<SPECV_BF16>(p, r, row, T, tp, probs_row, sm, hist);
+}
+
 // ---------------------------------------------------------------- top-p
 // The nucleus of each top-p row inside its top-k set: the largest key K
 // whose kept values at or above it carry at least top_p of the kept mass,
@@ -769,6 +1098,30 @@ cudaError_t launch_nucleus(const StatsParams& p, cudaStream_t s) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, nucleus_kernel, p);
+}
+
+cudaError_t launch_alone(const StatsParams& p, cudaStream_t s) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(alone_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAlSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const int64_t rows = p.rows_t + p.rows_d;
+    if (rows < 1) return cudaSuccess;
+    if (!p.top_ks && p.top_k >= 1 && p.top_k < p.V) return cudaSuccess;  // top-k on for every sequence
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rows);
+    cfg.blockDim = dim3(kAlThreads);
+    cfg.dynamicSmemBytes = kAlSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, alone_kernel, p);
 }
 
 cudaError_t launch_topk(const StatsParams& p, cudaStream_t s) {

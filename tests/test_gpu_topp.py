@@ -1,8 +1,9 @@
-"""GPU parity of top-p (nucleus) after top-k against the float64 oracle:
-per-sequence p with off values, both dtypes and odd vocabularies, the
-row path (large k, ties), probability drafts, the truncated distributions
-within 1e-5 with the same kept columns, the unsupported status, and the
-benchmarked workload at k = 50, p = 0.9."""
+"""GPU parity of top-p (nucleus) against the float64 oracle, after top-k
+and alone: per-sequence p with off values, both dtypes and odd
+vocabularies, the row path (large k, ties), probability drafts, top-p
+without top-k (the whole row's nucleus, short and flat rows), the truncated
+distributions within 1e-5 with the same kept columns, and the benchmarked
+workload at k = 50, p = 0.9."""
 import numpy as np
 import pytest
 
@@ -67,19 +68,80 @@ def test_topp_probs_draft(sv):
     run_rounds(w, range(10), seed=4, label="probs draft top-p")
 
 
-def test_topp_unsupported_status(sv):
-    rng = np.random.default_rng(3)
+def test_topp_without_top_k(sv):
+    """Top-p with top-k off (k <= 0 or k >= V): the nucleus of the whole
+    row. Per-sequence p with off values, and top-k rows, mixed in."""
     B = 8
-    w = wl.sampling_workload("topp status", config=395, batch=B, vocab=3001, gammas=np.full(B, 3), profile="zipf",
+    w = wl.sampling_workload("topp alone", config=395, batch=B, vocab=3001, gammas=np.full(B, 3), profile="zipf",
                              dtype="bf16", sigma=0.5, temps=1.0, pool=2,
                              top_k=np.array([0, 5, 3001, 5, 0, 5, -1, 10], np.int32),
                              top_p=np.array([0.9, 0.9, 0.5, 1.0, 0.0, np.nan, 0.2, 0.5], np.float32))
-    run_rounds(w, range(2), seed=3, label="top-p status")
+    run_rounds(w, range(4), seed=3, label="top-p alone")
     DeviceBatch = _harness()
     db = DeviceBatch(w, seed=3)
     db.run()
-    st = db.results()["status"]
-    assert st.tolist() == [7, 0, 7, 0, 0, 0, 7, 0]
+    assert db.results()["status"].tolist() == [0] * B
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V", [33, 1031, 32000])
+def test_topp_alone_sizes(sv, dtype, V):
+    rng = np.random.default_rng(900 + V)
+    B = 12
+    ps = rng.uniform(0.05, 0.99, size=B).astype(np.float32)
+    ps[:3] = [0.999, 0.5, 1e-6]
+    w = wl.sampling_workload(f"topp alone V{V}", config=397, batch=B, vocab=V, gammas=rng.integers(0, 6, size=B),
+                             profile="zipf", dtype=dtype, sigma=rng.uniform(0.2, 1.5, B),
+                             temps=rng.uniform(0.5, 1.5, B), ragged=True, pool=2, dataset=V, top_p=ps)
+    run_rounds(w, range(4), seed=9, label=f"top-p alone V={V} {dtype}")
+
+
+def test_topp_alone_flat_rows(sv):
+    """High temperature on Gaussian logits: the nucleus at p = 0.95 holds
+    tens of thousands of columns, with many equal bf16 values at its edge."""
+    w = wl.sampling_workload("topp alone flat", config=398, batch=6, vocab=40_009, gammas=np.full(6, 2),
+                             profile="gaussian", dtype="bf16", sigma=0.4, temps=1.5, pool=2, top_p=0.95,
+                             gauss_std=1.0)
+    run_rounds(w, range(3), seed=2, label="top-p alone, flat rows")
+
+
+def test_topp_alone_probs_draft(sv):
+    rng = np.random.default_rng(34)
+    B, g, V = 6, 3, 5003
+    base = wl.sampling_workload("probs alone", config=399, batch=B, vocab=V, gammas=np.full(B, g), profile="zipf",
+                                dtype="f32", sigma=0.7, temps=1.0, pool=2)
+    dvals = wl.stored_f32(base.draft)
+    probs = np.exp(dvals - dvals.max(axis=1, keepdims=True)).astype(np.float32)
+    probs *= rng.uniform(0.5, 3.0, size=(probs.shape[0], 1)).astype(np.float32)
+    w = wl.Workload(name="probs top-p alone", batch=B, vocab=V, gamma_max=g, gammas=base.gammas,
+                    target=wl.bf16_bits(wl.stored_f32(base.target)), draft=probs, draft_tokens=base.token_pool[0],
+                    token_pool=base.token_pool, draft_is_probs=True, temperature=1.0,
+                    top_ps=np.array([0.9, 0.5, 0.0, 0.3, 0.95, 0.99], np.float32))
+    run_rounds(w, range(6), seed=4, label="probs draft top-p alone")
+
+
+def test_topp_alone_target_at_a_group_edge(sv):
+    """Rows of two groups, n columns at logit 0 and the rest at -1 (T = 1),
+    with p the float nearest to the top group's share: the target sits
+    within a float rounding of the top group's mass, where a float sum can
+    take the other side from the double-float one (which decides)."""
+    B, g, V = 16, 2, 2003
+    base = wl.sampling_workload("group edge", config=400, batch=B, vocab=V, gammas=np.full(B, g), profile="zipf",
+                                dtype="f32", sigma=0.5, temps=1.0, pool=2)
+    ns = 3 + 7 * np.arange(B)
+    tgt = np.full((B, g + 1, V), -1.0, np.float32)
+    dft = np.full((B, g, V), -1.0, np.float32)
+    ps = np.empty(B, np.float32)
+    for b, n in enumerate(ns):
+        cols = np.random.default_rng(b).permutation(V)[:n]
+        tgt[b][:, cols] = 0.0
+        dft[b][:, cols] = 0.0
+        ps[b] = np.float32(n / (n + (V - n) * np.exp(-1.0)))
+    w = wl.Workload(name="top-p at a group edge", batch=B, vocab=V, gamma_max=g, gammas=base.gammas,
+                    target=wl.bf16_bits(tgt.reshape(B * (g + 1), V)), draft=dft.reshape(B * g, V),
+                    draft_tokens=base.token_pool[0], token_pool=base.token_pool, draft_is_probs=False,
+                    temperature=1.0, top_ps=ps)
+    run_rounds(w, range(4), seed=5, label="top-p alone at a group edge")
 
 
 def test_topp_debug_probs_within_1e5(sv):
@@ -91,7 +153,7 @@ def test_topp_debug_probs_within_1e5(sv):
     gam = np.array([3, 0, 5, 1, 2])
     w = wl.sampling_workload("dbg top-p", config=396, batch=B, vocab=5003, gammas=gam, profile="zipf", dtype="bf16",
                              sigma=rng.uniform(0.2, 2.0, B), temps=rng.uniform(0.5, 1.5, B), ragged=True, pool=1,
-                             top_k=np.array([50, 1, 300, 20, 2], np.int32),
+                             top_k=np.array([50, 1, 0, 20, 5003], np.int32),
                              top_p=np.array([0.9, 0.5, 0.3, 0.0, 0.99], np.float32))
     db = DeviceBatch(w, seed=3)
     db.run(rnd=1)

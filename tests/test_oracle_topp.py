@@ -1,10 +1,10 @@
-"""Pins of the oracle's top-p (nucleus) truncation after top-k (no GPU).
+"""Pins of the oracle's top-p (nucleus) truncation, after top-k or alone (no GPU).
 
 The threshold tau is fixed by two inequalities on the top-k-kept
 distribution: the columns at or above tau carry at least top_p of the mass,
 the columns strictly above tau carry less. The tests check those (with
-scipy's softmax for the masses), the limits, ties, the per-sequence status
-when top-k is off, and the acceptance-rate closed form on numpy-truncated
+scipy's softmax for the masses), the limits, ties, top-p with top-k off
+(the whole row's nucleus), and the acceptance-rate closed form on numpy-truncated
 pairs.
 """
 import numpy as np
@@ -71,7 +71,11 @@ def _wl(tgt, dft, gammas, toks, **kw):
                        draft=np.ascontiguousarray(dft, np.float32), draft_tokens=np.asarray(toks, np.int32), **kw)
 
 
-def test_status_without_top_k(orc):
+def test_top_p_without_top_k_is_the_whole_row_nucleus(orc):
+    """With top-k off (k <= 0 or k >= V) an active top-p takes the nucleus of
+    the whole row: the position rows are the softmax over the columns at or
+    above topp_threshold(row, T, -inf, p), every status OK; p outside (0, 1)
+    (or NaN) leaves the row whole."""
     rng = np.random.default_rng(4)
     V, g, B = 30, 3, 6
     tgt = rng.standard_normal((B * (g + 1), V)).astype(np.float32)
@@ -79,9 +83,21 @@ def test_status_without_top_k(orc):
     toks = rng.integers(0, V, size=B * g)
     ks = np.array([0, 5, V, 5, 0, 5], np.int32)
     ps = np.array([0.9, 0.9, 0.5, 1.0, 0.0, np.nan], np.float32)
-    res = orc.verify_sample(_wl(tgt, dft, np.full(B, g), toks, top_ks=ks, top_ps=ps), seed=1)
-    assert res["status"].tolist() == [orc.SEQ_UNSUPPORTED, 0, orc.SEQ_UNSUPPORTED, 0, 0, 0]
-    assert np.all(res["tokens"].reshape(B, g + 1)[[0, 2]] == -1)
+    w = _wl(tgt, dft, np.full(B, g), toks, top_ks=ks, top_ps=ps)
+    res = orc.verify_sample(w, seed=1)
+    assert res["status"].tolist() == [0] * B
+    for b in (0, 2, 4):
+        for i in range(g + 1):
+            st, p, q, wt, Z = orc.position_rows(w, b, i)
+            vals = tgt[b * (g + 1) + i].astype(np.float64)
+            tau = orc.topp_threshold(tgt[b * (g + 1) + i], 1.0, -np.inf, float(ps[b]))
+            ref = scipy.special.softmax(np.where(vals >= tau, vals, -np.inf))
+            assert st == 0 and np.max(np.abs(p - ref)) < 1e-14
+            if b == 4:
+                assert tau == -np.inf  # p = 0: off
+            else:
+                kept = ref[vals >= tau]
+                assert kept.sum() > 0 and np.count_nonzero(vals >= tau) < V
     # the greedy verify ignores top-p
     assert orc.verify_greedy(_wl(tgt, dft, np.full(B, g), toks, top_ks=ks, top_ps=ps, greedy=True))[
         "status"].tolist() == [0] * B
