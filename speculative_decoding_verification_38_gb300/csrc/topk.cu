@@ -635,6 +635,7 @@ struct AloneSmem {
     float wtot[kAlWarps];     // histogram choice: each warp's bins
     int bin;                  // histogram choice: the bin
     float bin_above;          // histogram choice: the float mass above the bin
+    uint32_t tail_key;        // 1 + the largest key left out of the histogram (0: none)
 };
 
 // f(v) for each value of one 16-byte vector, in column order.
@@ -687,10 +688,12 @@ __device__ void block_sum(df (&d)[N], float (&f)[N], int par, AloneSmem& sm) {
 // One narrowing choice over the float histogram, for the whole CTA: the
 // highest bin j with above + (the bins from j up) >= target, else bin 0.
 // above becomes the float mass above bin j. With first, target is first set
-// to top_p of above + every bin. Each thread sums its own bins and the warps
-// combine from the top, in a fixed order. The choice is a guess that the
-// double-float pass checks.
-__device__ int hist_pick(const float* hist, float& above, float& target, bool first, float tp, AloneSmem& sm) {
+// to top_p of above + every bin + below (mass left out of the histogram,
+// under its bins). Each thread sums its own bins and the warps combine from
+// the top, in a fixed order. The choice is a guess that the double-float
+// pass checks.
+__device__ int hist_pick(const float* hist, float& above, float& target, bool first, float tp, float below,
+                         AloneSmem& sm) {
     const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
     float loc[kAlBinsPerThread];
     const float4* h4 = reinterpret_cast<const float4*>(hist) + t * (kAlBinsPerThread / 4);
@@ -722,7 +725,7 @@ __device__ int hist_pick(const float* hist, float& above, float& target, bool fi
         if (w > warp) up += v;
         all += v;
     }
-    if (first) target = tp * all;
+    if (first) target = tp * (all + below);
     const float base = up + ex;  // above + every bin above this thread's
     float run = base;
     int cand = -1;
@@ -753,7 +756,10 @@ __device__ int hist_pick(const float* hist, float& above, float& target, bool fi
 //     [P, P + 2^R) over kAlBins bins of 2^(R-14) keys and keeps the bin where
 //     the float mass from the top reaches top_p of the row's, until R <= 4
 //     (one pass for bf16 keys, two for f32). The first pass also sums the
-//     row's double-float mass for the target.
+//     row's double-float mass for the target, and bins only the values that
+//     weigh at least 2^-16 of the row's largest (few in a peaked row), the
+//     rest being summed apart: if the bin found may hold such a value, that
+//     pass runs again over every value.
 //  2. Double-float two-bit bisection over the kept range. Its first round
 //     also weighs the keys above the range and checks that the target falls
 //     inside it: mass(>= P) >= target > mass(>= P + 2^R). If the float guess
@@ -798,30 +804,49 @@ __device__ void row_nucleus_whole(const StatsParams& p, int64_t r, const char* r
     uint32_t P = 0;
     int R = W, par = 0;
     float above_h = 0.f, target_f = 0.f;
+    const float light = probs_row ? m * 0x1p-16f : 0x1p-16f;  // the first pass bins weights from here up
+    bool skip = true;
 #pragma unroll 1
     while (R > 4) {
         const int s = R - kAlBinBits;
-        const bool first = R == W;
+        const bool first = R == W && skip;
         const uint64_t span = 1ull << R;
         for (int i = threadIdx.x; i < kAlBins; i += kAlThreads) hist[i] = 0.f;
+        if (threadIdx.x == 0) sm.tail_key = 0u;
         __syncthreads();
         df tot[1] = {{0.f, 0.f}};
-        float unused[1] = {0.f};
+        float tail[1] = {0.f};  // the float mass left out of the histogram
+        uint32_t tk = 0u;       // 1 + the largest key left out
         each([&](float v) {
             const uint32_t key = key_of_value<DT>(v);
             if (first) tot[0] = df_add(tot[0], weight(v));
             const uint32_t off = key - P;  // wraps above span for key < P
             if ((uint64_t)off >= span) return;
             const float fw = kept_weight(v, probs_row, k2, nmk);
-            if (fw > 0.f) atomicAdd(hist + (off >> s), fw);
+            if (!(fw > 0.f)) return;
+            if (first && fw < light) {
+                tail[0] += fw;
+                tk = max(tk, key + 1u);
+                return;
+            }
+            atomicAdd(hist + (off >> s), fw);
         });
+        if (tk) atomicMax(&sm.tail_key, tk);
         if (first) {
-            block_sum<1>(tot, unused, par, sm);
+            block_sum<1>(tot, tail, par, sm);
             par ^= 1;
             target = df_mul_f(tot[0], tp);
         }
         __syncthreads();  // the histogram is complete
-        const int j = hist_pick(hist, above_h, target_f, first, tp, sm);
+        const uint32_t tkb = sm.tail_key;
+        float ah = above_h;
+        const int j = hist_pick(hist, ah, target_f, first, tp, first ? tail[0] : 0.f, sm);
+        if (first && tkb && j <= (int)((tkb - 1u - P) >> s)) {  // the bin may hold values left out
+            skip = false;
+            continue;
+        }
+        skip = false;
+        above_h = ah;
         P += (uint32_t)j << s;
         R = s;
     }
