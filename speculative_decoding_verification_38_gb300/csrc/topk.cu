@@ -630,8 +630,10 @@ constexpr size_t kAlSmemBytes = kAlBins * sizeof(float);   // dynamic: the histo
 // Shared memory of alone_kernel (besides the histogram).
 struct AloneSmem {
     Exp2Table tab;
-    df dsum[2][5][kAlWarps];  // block sums, double-buffered
+    df dsum[2][5][kAlWarps];  // block sums: each warp's, double-buffered
     float fsum[2][5][kAlWarps];
+    df dfin[2][5];            // block sums: the CTA's
+    float ffin[2][5];
     float wtot[kAlWarps];     // histogram choice: each warp's bins
     int bin;                  // histogram choice: the bin
     float bin_above;          // histogram choice: the float mass above the bin
@@ -653,10 +655,13 @@ __device__ __forceinline__ void vec_each(const uint4& q, F&& f) {
     }
 }
 
-// N double-float and N float sums over the CTA in a fixed order; par
-// alternates between calls, so one barrier per call suffices.
+// N double-float and N float sums over the CTA, the same in every thread:
+// each warp reduces its lanes, warp 0 reduces the warps' sums and every
+// thread reads the result. par alternates between calls, so that a call's
+// writes never meet the previous call's reads.
 template <int N>
 __device__ void block_sum(df (&d)[N], float (&f)[N], int par, AloneSmem& sm) {
+    static_assert(kAlWarps == 32, "warp 0 reduces one warp sum per lane");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
     for (int i = 0; i < N; ++i) {
@@ -673,15 +678,27 @@ __device__ void block_sum(df (&d)[N], float (&f)[N], int par, AloneSmem& sm) {
             sm.fsum[par][i][warp] = f[i];
         }
     __syncthreads();
+    if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            df x = sm.dsum[par][i][lane];
+            float y = sm.fsum[par][i][lane];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                x = df_add(x, shfl_xor_df(x, o));
+                y += __shfl_xor_sync(kFull, y, o);
+            }
+            if (lane == 0) {
+                sm.dfin[par][i] = x;
+                sm.ffin[par][i] = y;
+            }
+        }
+    }
+    __syncthreads();
 #pragma unroll
     for (int i = 0; i < N; ++i) {
-        d[i] = df{0.f, 0.f};
-        f[i] = 0.f;
-#pragma unroll 8
-        for (int w = 0; w < kAlWarps; ++w) {
-            d[i] = df_add(d[i], sm.dsum[par][i][w]);
-            f[i] += sm.fsum[par][i][w];
-        }
+        d[i] = sm.dfin[par][i];
+        f[i] = sm.ffin[par][i];
     }
 }
 
