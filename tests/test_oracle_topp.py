@@ -98,6 +98,12 @@ def test_top_p_without_top_k_is_the_whole_row_nucleus(orc):
             else:
                 kept = ref[vals >= tau]
                 assert kept.sum() > 0 and np.count_nonzero(vals >= tau) < V
+                # the nucleus of the whole row, from its definition: tau is one of
+                # the row's values, the columns at or above it carry at least p of
+                # the softmax mass, the columns strictly above it less
+                full = scipy.special.softmax(vals)
+                assert tau in vals
+                assert full[vals >= tau].sum() >= ps[b] - 1e-12 and full[vals > tau].sum() < ps[b]
     # the greedy verify ignores top-p
     assert orc.verify_greedy(_wl(tgt, dft, np.full(B, g), toks, top_ks=ks, top_ps=ps, greedy=True))[
         "status"].tolist() == [0] * B
@@ -157,3 +163,23 @@ def test_acceptance_rate_of_nucleus_pair(orc):
     assert abs(emitted.mean() - E) / E < 0.01, (emitted.mean(), E)
     first = res["tokens"].reshape(B, gamma + 1)[:, 0]
     assert np.all(np.bincount(first, minlength=V)[pt == 0] == 0)
+
+
+def test_whole_row_threshold_brute_force(orc):
+    """topp_threshold over a whole row (tau_k = -inf) against brute force on
+    small rows with ties: walk the groups of equal values from the largest
+    down and stop at the first whose cumulative softmax mass reaches p."""
+    rng = np.random.default_rng(21)
+    for _ in range(300):
+        V = int(rng.integers(1, 9))
+        row = rng.choice(np.array([-3.0, -1.5, -1.0, 0.0, 0.5, 2.0], np.float32), size=V)
+        T = float(rng.choice([0.5, 1.0, 1.7]))
+        p = float(np.float32(rng.uniform(0.01, 0.99)))
+        mass = scipy.special.softmax(row.astype(np.float64) / T)
+        want = None
+        for v in np.unique(row)[::-1]:
+            if mass[row >= v].sum() >= p:
+                want = v
+                break
+        got = orc.topp_threshold(row, T, -np.inf, p)
+        assert got == want, (row, T, p, got, want)
