@@ -73,13 +73,23 @@ KERNELS = {
               "profile": "ngram_kernel_edit_contexts_dram.txt"},
     "tree": {"name": "tree_kernel (tree verification)", "sources": ("tree.cu", "common.cuh", "internal.h", "precise.cuh"),
              "profile": "tree_kernel_bench_trees_dram.txt"},
-    "topp": {"name": "topk_kernel (top-k threshold and top-p nucleus pass)",
+    "topp": {"name": "topk_kernel (top-k threshold pass, storing each top-p row's kept values for nucleus_kernel)",
              "sources": ("topk.cu", "common.cuh", "internal.h", "precise.cuh"), "profile": "topk_kernel_c3_k{k}_p_dram.txt"},
 }
 
 
 def topp_on(args):
     return 0 < args.top_p < 1
+
+
+def kernel_label(mode, args):
+    """The roofline's kernel: the mode's dominant kernel, except that with top-p
+    and no top-k the kernel timed is still the top-k pass (the row maximum and
+    sum), while the whole-row nucleus kernel after it takes most of the step."""
+    if mode == "topp" and args.top_k <= 0:
+        return ("topk_kernel (row maximum and sum pass); the whole-row nucleus kernel after it, alone_kernel, "
+                "takes most of the step and is issue-bound: profiles/alone_kernel_c3_p09.md")
+    return KERNELS[mode]["name"]
 
 
 def mode_of(args):
@@ -369,7 +379,7 @@ def run_ours(args):
                          + (1 if args.adaptive else 0)) * K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": KERNELS[mode]["name"], "kernel_ms": kern_ms,
+                     "kernel": kernel_label(mode, args), "kernel_ms": kern_ms,
                      "kernel_ms_samples": len(stats_ms),
                      "algorithmic_bytes_per_launch": algo_bytes + small_io,
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
