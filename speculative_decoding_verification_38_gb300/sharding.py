@@ -57,6 +57,8 @@ def shard(w: Workload, rank: int, world: int) -> tuple[Workload, int]:
         token_pool=[t[d0:d1] for t in w.token_pool],
         temperatures=None if w.temperatures is None else w.temperatures[b0:b1],
         kv_in=None if w.kv_in is None else w.kv_in[b0:b1],
+        top_ks=None if w.top_ks is None else w.top_ks[b0:b1],
+        top_ps=None if w.top_ps is None else w.top_ps[b0:b1],
         target_row_off=tro,
         draft_row_off=dro,
     )

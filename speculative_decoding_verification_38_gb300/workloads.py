@@ -87,7 +87,7 @@ class Workload:
     info: dict = field(default_factory=dict)
     top_k: int = 0                    # top-k truncation of every row (0: off)
     top_ks: np.ndarray | None = None  # per-sequence k (int32 [B]) instead of top_k
-    top_p: float = 0.0                # top-p after top-k (active for 0 < p < 1)
+    top_p: float = 0.0                # top-p, after top-k when that is on (active for 0 < p < 1)
     top_ps: np.ndarray | None = None  # per-sequence p (float32 [B]) instead of top_p
 
     @property
