@@ -1,7 +1,7 @@
 """GPU parity of top-p (nucleus) against the float64 oracle, after top-k
 and alone: per-sequence p with off values, both dtypes and odd
 vocabularies, the row path (large k, ties), probability drafts, top-p
-without top-k (the whole row's nucleus, short and flat rows), the truncated
+without top-k (the whole row's nucleus: short, flat and full-size rows), the truncated
 distributions within 1e-5 with the same kept columns, and the benchmarked
 workload at k = 50, p = 0.9."""
 import numpy as np
@@ -177,3 +177,10 @@ def test_topp_debug_probs_within_1e5(sv):
 def test_topp_config3_full_size(sv):
     w = wl.config3(top_k=50, top_p=0.9)
     run_rounds(w, range(8), seed=0, label="C3 top-k 50 top-p 0.9")
+
+
+def test_topp_alone_config3_full_size(sv):
+    """Top-p 0.9 without top-k on the benchmarked workload (B=64, gamma=8,
+    V=128256 bf16): every row's whole-row nucleus, in the bench's launch."""
+    w = wl.config3(top_k=0, top_p=0.9)
+    run_rounds(w, range(3), seed=0, label="C3 top-p 0.9 alone")
