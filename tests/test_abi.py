@@ -103,6 +103,25 @@ def test_workspace_size_is_host_arithmetic(sv):
     assert L.spec_verify_workspace_size(None, 0) == 0
 
 
+def test_workspace_grows_by_4kb_per_row_when_top_p_may_be_asked(sv):
+    L = sv.lib()
+    for top_p, top_ps in ((0.9, None), (0.0, 1 << 20)):
+        plain, topp = _args(sv, batch=64, gamma=8, vocab=128256), _args(sv, batch=64, gamma=8, vocab=128256)
+        topp.top_p = top_p
+        if top_ps:
+            topp.top_ps = top_ps
+        rows = plain.rows_target + plain.rows_draft
+        n0, n1 = (L.spec_verify_workspace_size(ctypes.byref(x), 0) for x in (plain, topp))
+        assert n1 - n0 >= rows * 4096 and n1 - n0 < rows * 4096 + rows * 4 + 512
+        # greedy ignores top-p
+        assert L.spec_verify_workspace_size(ctypes.byref(topp), 1) == L.spec_verify_workspace_size(
+            ctypes.byref(plain), 1)
+    off = _args(sv, batch=64, gamma=8, vocab=128256)
+    off.top_p = 1.0  # top-p off: no extra room
+    assert L.spec_verify_workspace_size(ctypes.byref(off), 0) == L.spec_verify_workspace_size(
+        ctypes.byref(_args(sv, batch=64, gamma=8, vocab=128256)), 0)
+
+
 def test_host_validation_rejects_before_cuda(sv):
     L = sv.lib()
 
@@ -126,6 +145,9 @@ def test_host_validation_rejects_before_cuda(sv):
     assert call(_args(sv, tdt=7), greedy=True) == sv.SPEC_ERR_INVALID_ARG
     a = _args(sv)
     a.top_ks = (1 << 20) + 2  # per-sequence k must be int32-aligned
+    assert call(a) == sv.SPEC_ERR_ALIGNMENT
+    a = _args(sv)
+    a.top_ps = (1 << 20) + 2  # per-sequence p must be float32-aligned
     assert call(a) == sv.SPEC_ERR_ALIGNMENT
     # the struct grew with top_k / top_ks: the size of the previous layout is rejected
     a = _args(sv)
