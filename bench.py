@@ -82,6 +82,18 @@ def topp_on(args):
     return 0 < args.top_p < 1
 
 
+def launches_per_step(greedy, mode, top_k, adaptive):
+    """Kernels one timed step launches: the row pass (the streaming pass, or
+    the top-k pass with truncation) and the finalize; sampling adds the
+    sampler's tile pass and the draw; top-p adds the nucleus kernel, and the
+    whole-row nucleus kernel when top-k is off; --adaptive adds the gamma
+    policy."""
+    n = 2 if greedy else 4
+    if mode == "topp":
+        n += 1 + (1 if top_k <= 0 else 0)
+    return n + (1 if adaptive else 0)
+
+
 def kernel_label(mode, args):
     """The roofline's kernel: the mode's dominant kernel, except that with top-p
     and no top-k the kernel timed is still the top-k pass (the row maximum and
@@ -372,11 +384,7 @@ def run_ours(args):
         "vocab_rows_per_s": rounds_per_s * w.vocab_rows(),
         "sequence_rounds_per_s": rounds_per_s * B,
         "step_hbm_gbs": rounds_per_s / world * algo_bytes / 1e9,
-        # row pass and finalize; sampling adds the sampler tile pass and the draw
-        # (+ the nucleus kernel with top-p, + the whole-row kernel for top-p
-        # without top-k, + the gamma policy with --adaptive)
-        "gpu_launches": ((2 if greedy else 4) + (1 if mode == "topp" else 0) + (1 if mode == "topp" and args.top_k <= 0 else 0)
-                         + (1 if args.adaptive else 0)) * K,
+        "gpu_launches": launches_per_step(greedy, mode, args.top_k, args.adaptive) * K,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": kernel_label(mode, args), "kernel_ms": kern_ms,

@@ -1,0 +1,59 @@
+"""The bench's JSON contract on the host (no GPU): the reference arm's line
+on the small workload, and the labels and launch counts the GPU arm reports
+for each mode."""
+import json
+import os
+import subprocess
+import sys
+import types
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def _ns(**kw):
+    d = dict(top_k=0, top_p=0.0, config=3, adaptive=False)
+    d.update(kw)
+    return types.SimpleNamespace(**d)
+
+
+def test_reference_arm_line(orc):
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "1",
+                          "--steps", "2", "--warmup", "1"], capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [ln for ln in out.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+              "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert k in d, k
+    assert d["impl"] == "reference" and d["value"] > 0 and d["higher_is_better"] is True
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"]["value"] == d["value"] and d["e2e"]["h2d_bytes_per_step"] == 0
+    assert d["metric"] == bench.CONFIGS[1][1] and d["config"]["workload"] == bench.CONFIGS[1][0]
+
+
+def test_modes_and_labels():
+    assert bench.mode_of(_ns()) == "stats"
+    assert bench.mode_of(_ns(top_k=50)) == "topk"
+    assert bench.mode_of(_ns(top_k=50, top_p=0.9)) == "topp"
+    assert bench.mode_of(_ns(top_p=0.9)) == "topp"
+    assert bench.mode_of(_ns(top_p=1.0)) == "stats"  # p = 1 is off
+    alone = _ns(top_p=0.9)
+    assert "alone_kernel" in bench.kernel_label("topp", alone)
+    assert "alone_kernel" not in bench.kernel_label("topp", _ns(top_k=50, top_p=0.9))
+    assert "top-p 0.9" in bench.metric_of(alone) and "top-k" not in bench.metric_of(alone)
+    assert "top-k 50" in bench.metric_of(_ns(top_k=50, top_p=0.9))
+    assert bench.metric_of(_ns()) == bench.METRIC
+
+
+def test_launches_per_step():
+    L = bench.launches_per_step
+    assert L(False, "stats", 0, False) == 4   # streaming pass, finalize, tile pass, draw
+    assert L(True, "stats", 0, False) == 2    # greedy: streaming pass, finalize
+    assert L(False, "topk", 50, False) == 4   # the top-k pass replaces the streaming pass
+    assert L(False, "topp", 50, False) == 5   # + the nucleus kernel
+    assert L(False, "topp", 0, False) == 6    # + the whole-row nucleus kernel
+    assert L(False, "stats", 0, True) == 5    # + the gamma policy
