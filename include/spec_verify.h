@@ -186,9 +186,11 @@ typedef struct {
      * rows alike ("Speculative decoding" (mhtirogla.ai), Implementation
      * notes: the same temperature, top-k and top-p processing). The masses
      * are double-float. Without top-k, one CTA per row takes the nucleus of
-     * the whole row by two-bit bisection on the value's bits, reading the row
-     * once per round (8 rounds for bf16 rows, 16 for f32). Zero-initialise
-     * both for no top-p. */
+     * the whole row: a float histogram pass guesses the boundary (two passes
+     * for f32 rows), and one double-float pass checks the guess and decides
+     * it, so the row is read about three times. A guess that fails the check
+     * costs a full double-float bisection (8 more passes for bf16, 16 for
+     * f32); the result is the same. Zero-initialise both for no top-p. */
     float top_p;
     const float* top_ps; /* device [B] or NULL */
 } spec_verify_args_t;
