@@ -186,11 +186,13 @@ typedef struct {
      * rows alike ("Speculative decoding" (mhtirogla.ai), Implementation
      * notes: the same temperature, top-k and top-p processing). The masses
      * are double-float. Without top-k, one CTA per row takes the nucleus of
-     * the whole row: a float histogram pass guesses the boundary (two passes
-     * for f32 rows), and one double-float pass checks the guess and decides
-     * it, so the row is read about three times. A guess that fails the check
-     * costs a full double-float bisection (8 more passes for bf16, 16 for
-     * f32); the result is the same. Zero-initialise both for no top-p. */
+     * the whole row. A float histogram pass guesses the boundary; it bins only
+     * values above 2^-16 of the row's largest and runs again over every value
+     * when the guessed bin may hold one of the rest. f32 rows take a second
+     * histogram pass. Double-float passes then check the guess and decide:
+     * two reads of a bf16 row, four of an f32 row. A guess that fails the
+     * check costs a full double-float bisection (8 more passes for bf16, 16
+     * for f32), with the same result. Zero-initialise both for no top-p. */
     float top_p;
     const float* top_ps; /* device [B] or NULL */
 } spec_verify_args_t;
