@@ -64,3 +64,52 @@ def test_draft_tokens_follow_q():
     xk = wl.gumbel_argmax(np.random.default_rng(9), logits, np.full(20000, T, np.float32),
                           k_per_row=np.full(20000, 2, np.int32))
     assert set(np.unique(xk)) <= set(np.argsort(logits[0])[::-1][:2].tolist())
+
+
+def test_tree_workload_structure():
+    w = wl.tree_workload("recipe tree", config=12, batch=5, vocab=500, branching=[3, 2], dtype="bf16")
+    n = int(w.node_off[1])
+    assert n == 1 + 3 + 6 and np.array_equal(w.node_off, np.arange(6) * n)
+    for b in range(5):
+        par = w.parent[b * n:(b + 1) * n]
+        assert par[0] == -1 and np.all((par[1:] >= 0) & (par[1:] < np.arange(1, n)))
+        assert np.bincount(par[1:], minlength=n)[0] == 3  # the root's three candidates
+        tok = w.tokens[b * n:(b + 1) * n]
+        assert tok[0] == -1 and np.all((tok[1:] >= 0) & (tok[1:] < 500))
+    r = wl.ragged_tree_workload("recipe ragged", config=13, batch=6, vocab=300, max_nodes=12)
+    sizes = np.diff(w.node_off)
+    sizes_r = np.diff(r.node_off)
+    assert sizes.min() == n and sizes_r[0] == 1 and sizes_r[-1] == 12 and sizes_r.max() <= 12
+
+
+def test_tree_candidates_drawn_from_q_at_the_parent():
+    """Trees of one root with 4 candidates over a 6-token vocabulary: the sum
+    over draws of q(x), under each tree's own root q = softmax(draft / T),
+    matches its expectation sum_t 4 sum_j q_j^2 (z-score), and the same
+    statistic rejects draws from the target's p, so the test has power."""
+    M = 4000
+    w = wl.tree_workload("recipe root draws", config=14, batch=M, vocab=6, branching=[4], dtype="f32",
+                         temps=0.8)
+    roots = np.arange(M) * 5
+    q = scipy.special.softmax(wl.stored_f32(w.draft)[roots].astype(np.float64) / 0.8, axis=1)
+    p = scipy.special.softmax(wl.stored_f32(w.target)[roots].astype(np.float64) / 0.8, axis=1)
+    toks = w.tokens.reshape(M, 5)[:, 1:]
+    stat = np.take_along_axis(q, toks, axis=1).sum()
+    s2, s3 = (q ** 2).sum(axis=1), (q ** 3).sum(axis=1)
+    mean, var = 4 * s2.sum(), 4 * (s3 - s2 ** 2).sum()
+    assert abs(stat - mean) / np.sqrt(var) < 4
+    mean_p = 4 * (p * q).sum()  # the statistic's mean if the candidates came from p
+    assert abs(mean_p - mean) / np.sqrt(var) > 6
+
+
+def test_ngram_contexts_copy_the_document():
+    ctx, off = wl.ngram_contexts(batch=3, doc_len=400, gen_len=100, vocab=5000)
+    assert off[0] == 0 and np.all(np.diff(off) >= 500) and ctx.dtype == np.int32
+    for b in range(3):
+        c = ctx[off[b]:off[b + 1]]
+        doc, gen = c[:400], c[400:]
+        assert np.all((c >= 0) & (c < 5000))
+        # with 5 % edits, most generated 4-grams occur in the document
+        grams = {tuple(doc[i:i + 4]) for i in range(len(doc) - 3)}
+        hit = np.mean([tuple(gen[i:i + 4]) in grams for i in range(len(gen) - 3)])
+        assert hit > 0.6
