@@ -57,3 +57,19 @@ def test_launches_per_step():
     assert L(False, "topp", 50, False) == 5   # + the nucleus kernel
     assert L(False, "topp", 0, False) == 6    # + the whole-row nucleus kernel
     assert L(False, "stats", 0, True) == 5    # + the gamma policy
+
+
+def test_clock_summary_from_nvidia_smi_rows():
+    S = bench.ClockSampler.summarize
+    row = ["0", "2070", "2070", "900.1", "0x0000000000000000", "Not Active", "Not Active", "Not Active", "Not Active"]
+    capped = row[:8] + ["Active"]
+    slow = row[:5] + ["Active"] + row[6:]
+    na = ["0", "[N/A]", "[N/A]", "[N/A]", "[N/A]", "[N/A]", "[N/A]", "[N/A]", "[N/A]"]
+    out = S([row, row, capped])
+    assert out["sm_mhz"] == 2070.0 and out["sm_max_mhz"] == 2070.0 and out["reasons"] == ["sw_power_cap"]
+    assert out["samples"] == 3
+    low = [row[:1] + ["1200"] + row[2:]] * 3 + [row] * 2
+    assert S(low)["sm_mhz"] == 1200.0  # the median under load, not the maximum
+    assert S([row, slow])["reasons"] == ["hw_slowdown"]
+    assert S([row, na])["sm_mhz"] == 2070.0  # unreadable fields are skipped
+    assert S([])["reasons"][0].startswith("unavailable")
