@@ -73,3 +73,28 @@ def test_clock_summary_from_nvidia_smi_rows():
     assert S([row, slow])["reasons"] == ["hw_slowdown"]
     assert S([row, na])["sm_mhz"] == 2070.0  # unreadable fields are skipped
     assert S([])["reasons"][0].startswith("unavailable")
+
+
+def test_traffic_only_while_the_source_hash_matches(tmp_path, monkeypatch):
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "stats_kernel_c3_dram.txt").write_text(
+        "# a capture\nsource_hash: abc123\ndram_bytes_per_launch: 282213376\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda mode="stats": "abc123")
+    assert bench.ncu_traffic_per_launch("stats", config=3) == 282213376
+    assert bench.ncu_traffic_per_launch("stats", config=4) is None  # no capture for that config
+    monkeypatch.setattr(bench, "kernel_source_hash", lambda mode="stats": "changed")
+    assert bench.ncu_traffic_per_launch("stats", config=3) is None  # the kernel changed since
+
+
+def test_committed_summaries_name_their_hash_and_bytes():
+    """Every committed DRAM summary carries a hash line and a byte count
+    (whether it still matches the sources is the bench's question)."""
+    for mode, k in bench.KERNELS.items():
+        name = k["profile"].format(k=50, c=3)
+        path = os.path.join(ROOT, "profiles", name)
+        if not os.path.exists(path):
+            continue
+        kv = dict(line.split(":", 1) for line in open(path) if ":" in line and not line.startswith("#"))
+        assert len(kv["source_hash"].strip()) == 16 and int(kv["dram_bytes_per_launch"]) > 0, name
