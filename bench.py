@@ -757,7 +757,8 @@ def _oracle_subset(w, nseq):
                        target=w.target[:rt], draft=None if w.draft is None else w.draft[:rd],
                        draft_tokens=w.draft_tokens[:rd], temperatures=cut(w.temperatures),
                        temperature=w.temperature, kv_in=cut(w.kv_in), block_size=w.block_size,
-                       target_row_off=tro, draft_row_off=dro, greedy=w.greedy, top_k=w.top_k, top_p=w.top_p)
+                       target_row_off=tro, draft_row_off=dro, greedy=w.greedy, draft_is_probs=w.draft_is_probs,
+                       top_k=w.top_k, top_ks=cut(w.top_ks), top_p=w.top_p, top_ps=cut(w.top_ps))
 
 
 def run_cpu_baseline(w, args):
@@ -817,7 +818,8 @@ def run_reference(args):
            "warmup": W, "ms_per_step": el / K * 1e3, "higher_is_better": True, "scaling": "weak",
            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded Zipf logits; no dataset)",
            "config": {"workload": workload_of(args), "batch": w.batch, "gamma": w.gamma_max, "vocab": w.vocab,
-                      "top_k": args.top_k, "logits_dtype": w.dtype_name, "parallelism": "host cores"},
+                      "top_k": args.top_k, "top_p": args.top_p, "logits_dtype": w.dtype_name,
+                      "parallelism": "host cores"},
            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                             "sample": f"each step verifies {per_step} of the {w.batch} sequences of one round "
                                       f"(counted as {per_step}/{w.batch} round), float64 C oracle"},

@@ -98,3 +98,29 @@ def test_committed_summaries_name_their_hash_and_bytes():
             continue
         kv = dict(line.split(":", 1) for line in open(path) if ":" in line and not line.startswith("#"))
         assert len(kv["source_hash"].strip()) == 16 and int(kv["dram_bytes_per_launch"]) > 0, name
+
+
+def test_reference_subset_is_the_batch_prefix(orc):
+    """The reference arm times the oracle on the first n sequences: their
+    outputs must be the whole batch's first n, per-sequence truncation and
+    probability drafts included."""
+    import numpy as np
+
+    from speculative_decoding_verification_38_gb300 import workloads as wl
+
+    B = 7
+    w = wl.sampling_workload("subset", config=402, batch=B, vocab=700, gammas=np.array([3, 0, 4, 2, 4, 1, 3]),
+                             profile="zipf", dtype="bf16", sigma=0.6, temps=np.linspace(0.7, 1.3, B).astype(np.float32),
+                             ragged=True, pool=1, top_k=np.array([0, 20, 5, 0, 700, 40, 0], np.int32),
+                             top_p=np.array([0.9, 0.0, 0.5, 0.3, 0.8, 0.95, 0.0], np.float32))
+    dv = wl.stored_f32(w.draft)
+    probs = np.exp(dv - dv.max(axis=1, keepdims=True)).astype(np.float32)
+    wp = wl.Workload(**{**w.__dict__, "name": "subset probs", "draft": probs, "draft_is_probs": True})
+    n = 4
+    rows = int(w.target_row_off[n])
+    for ww in (w, wp):
+        for rnd in range(4):
+            full = orc.verify_sample(ww, seed=3, rnd=rnd)
+            part = orc.verify_sample(bench._oracle_subset(ww, n), seed=3, rnd=rnd)
+            assert np.array_equal(part["accepted"], full["accepted"][:n])
+            assert np.array_equal(part["tokens"], full["tokens"][:rows])
