@@ -10,8 +10,10 @@ marshals numpy arrays through ctypes. Every function documents the page passage
 it follows; see the header of ``oracle.c`` for the sources and readings.
 
 Parity status of each function (what pins it; see tests/test_oracle_pins.py):
-  philox4x32_10 / uniform_pair   -- pinned: Triton's independent Philox (CPU
-                                    interpreter) and the published all-zero KAT
+  philox4x32_10 / uniform_pair   -- pinned: the generator's published
+                                    known-answer vectors (zero, all-ones,
+                                    pi digits) and Triton's independent
+                                    Philox (CPU interpreter)
   softmax_row / normalize_row    -- pinned: scipy.special.softmax, closed forms
   residual                       -- pinned: the page's worked example, the
                                     identity Z = 1 - sum min(p, q)

@@ -95,6 +95,21 @@ def test_philox_matches_triton_reference():
             assert got == words[4 * j:4 * j + 4], (seed, c)
 
 
+def test_philox_known_answer_vectors(orc):
+    """The oracle's Philox4x32-10 reproduces the published known-answer
+    vectors of the SC'11 generator (zero, all-ones and pi-digit inputs;
+    tests/golden/philox4x32_10_kat.txt)."""
+    rows = []
+    with open(os.path.join(GOLDEN, "philox4x32_10_kat.txt")) as f:
+        for line in f:
+            if line.strip() and not line.startswith("#"):
+                rows.append([int(x, 16) for x in line.split()[1:]])
+    assert len(rows) == 3
+    for r in rows:
+        ctr, key, want = r[0:4], r[4:6], r[6:10]
+        assert [int(x) for x in orc.philox4x32_10(ctr, key)] == want
+
+
 def test_uniform_pair_layout_and_uniformity(orc):
     """u = (w >> 8) * 2^-24 from words 0/1 of the block keyed (seed) with counter
     (pos, seq, round lo, round hi); 2^20 draws pass a 256-bin chi-square."""
