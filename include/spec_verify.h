@@ -249,7 +249,10 @@ SPEC_API spec_status_t spec_verify_greedy(const spec_verify_args_t* args, spec_s
  *     returns SPEC_ERR_WORKSPACE before any CUDA call.
  *   - Set-up: the first call on a device (that device current) looks up the
  *     array's device address with cudaGetSymbolAddress; make that first call
- *     before any stream capture.
+ *     before any stream capture. The address is kept for the life of the
+ *     process: it does not survive cudaDeviceReset (or any other teardown of
+ *     the device's primary context), after which this entry point must not be
+ *     called on that device again in the same process.
  *   - Every call clears the scratch's arrival counters and error word with a
  *     stream-ordered memset before its kernels; no spec_workspace_init needed.
  *   - There is one scratch per device: calls that overlap on the GPU (other

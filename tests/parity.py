@@ -159,3 +159,75 @@ def compare_tree(w, gpu: dict, orc: dict) -> Tally:
             T.unexcused.append((b, int(orc["accepted"][b]), int(gpu["accepted"][b]), orc["tokens"][seg][:8].tolist(),
                                 gpu["tokens"][seg][:8].tolist()))
     return T
+
+
+# ------------------------------------------------ element-level checks (GPU)
+def bulk_copy_path(w, db) -> bool:
+    """Whether a sampling call on this batch streams its rows with bulk
+    copies: every row starts on a 16-byte boundary (the library's documented
+    rule; otherwise the plain-load streaming kernel runs)."""
+    esz_t = 2 if w.target.dtype == np.uint16 else 4
+    esz_d = 2 if (w.draft is not None and w.draft.dtype == np.uint16) else 4
+    ok = (w.vocab * esz_t) % 16 == 0 and db.target.data_ptr() % 16 == 0
+    if db.draft is not None:
+        ok = ok and (w.vocab * esz_d) % 16 == 0 and db.draft.data_ptr() % 16 == 0
+    return ok
+
+
+def check_debug_probs(sv, w, db, positions, *, same_support=False, tol=1e-5):
+    """p_i, q_i, the normalised sampling weights (residual or bonus), p(x),
+    q(x) and Z that the GPU path uses, each within tol absolute of the
+    oracle's float64 values, for every (sequence, position) listed."""
+    import torch
+
+    V = w.vocab
+    op, oq, ow = (torch.zeros(V, device="cuda") for _ in range(3))
+    sc = torch.zeros(4, device="cuda")
+    worst = 0.0
+    for b, pos in positions:
+        sv.check(sv.spec_debug_probs(db.args, b, pos, op, oq, ow, sc), "debug_probs")
+        st, p, q, wts, Z = oracle.position_rows(w, b, pos, draft_tokens=w.draft_tokens)
+        assert st == 0
+        gp, gq, gw, gs = (t.cpu().numpy().astype(np.float64) for t in (op, oq, ow, sc))
+        if same_support:
+            assert np.array_equal(gp > 0, p > 0) and np.array_equal(gq > 0, q > 0)
+        errs = [np.max(np.abs(gp - p)), np.max(np.abs(gq - q)), np.max(np.abs(gw - wts / wts.sum()))]
+        g = int(np.asarray(w.gammas)[b])
+        if pos < g:
+            _, px, qx = oracle.accept_terms(w, b, pos, draft_tokens=w.draft_tokens)
+            errs += [abs(gs[0] - px), abs(gs[1] - qx), abs(gs[2] - Z)]
+        worst = max(worst, max(errs))
+        assert max(errs) < tol, (b, pos, errs)
+    return worst
+
+
+def check_row_stats(sv, w, db, *, top_ks=None, rel=1e-5):
+    """(m, s) of every row against float64: the raw maximum exactly, s =
+    sum 2^((l - m) log2(e) / T) (over the columns a top-k keeps) within rel."""
+    import torch
+
+    n = w.rows_target + w.rows_draft
+    m = torch.zeros(n, device="cuda")
+    s = torch.zeros(n, device="cuda")
+    sv.check(sv.spec_debug_row_stats(db.args, 0, m, s, None), "row_stats")
+    m, s = m.cpu().numpy(), s.cpu().numpy()
+    tro, dro = offsets(w)
+    L2E = 1.4426950408889634
+    temps = np.broadcast_to(np.asarray(w.temperatures if w.temperatures is not None else w.temperature,
+                                       dtype=np.float64), (w.batch,))
+    worst = 0.0
+    for b in range(w.batch):
+        T = float(temps[b])
+        rows = [(w.target, r, r) for r in range(tro[b], tro[b + 1])] + \
+               [(w.draft, r, w.rows_target + r) for r in range(dro[b], dro[b + 1])]
+        for arr, r, flat in rows:
+            vals = wl.stored_f32(arr[r]).astype(np.float64)
+            keep = vals
+            if top_ks is not None and 0 < int(top_ks[b]) < vals.size:
+                tau = np.sort(vals)[::-1][int(top_ks[b]) - 1]
+                keep = vals[vals >= tau]
+            assert m[flat] == vals.max()  # the raw maximum, exactly
+            ss = np.exp2((keep - vals.max()) / T * L2E).sum()
+            worst = max(worst, abs(s[flat] - ss) / ss)
+            assert abs(s[flat] - ss) <= rel * ss, (b, r, s[flat], ss)
+    return worst

@@ -91,69 +91,41 @@ def test_topk_probs_draft(sv):
     run_rounds(w, range(12), seed=4, label="probs draft top-k")
 
 
-def test_topk_debug_probs_within_1e5(sv):
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V", [5003, 4096, 128256])
+def test_topk_debug_probs_within_1e5(sv, V, dtype):
     """The truncated p_i, q_i, sampling weights, p(x), q(x) and Z the GPU path
-    uses, within 1e-5 of the oracle's."""
-    import torch
+    uses, within 1e-5 of the oracle's, with the same kept columns."""
+    from tests.parity import check_debug_probs
 
     DeviceBatch = _harness()
     rng = np.random.default_rng(22)
     B = 5
     gam = np.array([3, 0, 5, 1, 2])
     ks = np.array([10, 1, 300, 0, 2], np.int32)
-    w = wl.sampling_workload("dbg top-k", config=195, batch=B, vocab=5003, gammas=gam, profile="zipf",
-                             dtype="bf16", sigma=rng.uniform(0.2, 2.0, B), temps=rng.uniform(0.5, 1.5, B),
+    w = wl.sampling_workload("dbg top-k", config=195, batch=B, vocab=V, gammas=gam, profile="zipf",
+                             dtype=dtype, sigma=rng.uniform(0.2, 2.0, B), temps=rng.uniform(0.5, 1.5, B),
                              ragged=True, pool=1, top_k=ks)
     db = DeviceBatch(w, seed=3)
     db.run(rnd=1)
-    V = w.vocab
-    op, oq, ow = (torch.zeros(V, device="cuda") for _ in range(3))
-    sc = torch.zeros(4, device="cuda")
-    for b in range(B):
-        for pos in range(gam[b] + 1):
-            sv.check(sv.spec_debug_probs(db.args, b, pos, op, oq, ow, sc), "debug_probs")
-            st, p, q, wts, Z = oracle.position_rows(w, b, pos, draft_tokens=w.draft_tokens)
-            assert st == 0
-            gp, gq, gw, gs = (t.cpu().numpy().astype(np.float64) for t in (op, oq, ow, sc))
-            assert np.max(np.abs(gp - p)) < 1e-5
-            assert np.array_equal(gp > 0, p > 0)  # the same kept columns
-            assert np.max(np.abs(gq - q)) < 1e-5
-            assert np.max(np.abs(gw - wts / wts.sum())) < 1e-5
-            if pos < gam[b]:
-                _, px, qx = oracle.accept_terms(w, b, pos, draft_tokens=w.draft_tokens)
-                assert abs(gs[0] - px) < 1e-5 and abs(gs[1] - qx) < 1e-5
-                assert abs(gs[2] - Z) < 1e-5
+    pos = [(b, i) for b in range(B) for i in range(gam[b] + 1)]
+    print(f"top-k V={V} {dtype} worst abs error", check_debug_probs(sv, w, db, pos, same_support=True))
 
 
-def test_topk_row_stats(sv):
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("V", [77_777, 4096])
+def test_topk_row_stats(sv, V, dtype):
     """(m, s) of every row: the raw maximum exactly, s over the kept columns
     within 1e-5 relative of numpy's float64 sum."""
-    import torch
+    from tests.parity import check_row_stats
 
     DeviceBatch = _harness()
     ks = np.array([5, 64, 0, 1], np.int32)
-    w = wl.sampling_workload("rs top-k", config=196, batch=4, vocab=77_777, gammas=[2, 3, 1, 4], profile="zipf",
-                             dtype="bf16", sigma=0.8, temps=[0.6, 1.0, 1.4, 0.9], ragged=True, pool=1, top_k=ks)
+    w = wl.sampling_workload("rs top-k", config=196, batch=4, vocab=V, gammas=[2, 3, 1, 4], profile="zipf",
+                             dtype=dtype, sigma=0.8, temps=[0.6, 1.0, 1.4, 0.9], ragged=True, pool=1, top_k=ks)
     db = DeviceBatch(w)
     db.run()
-    n = w.rows_target + w.rows_draft
-    m = torch.zeros(n, device="cuda")
-    s = torch.zeros(n, device="cuda")
-    sv.check(sv.spec_debug_row_stats(db.args, 0, m, s, None), "row_stats")
-    m, s = m.cpu().numpy(), s.cpu().numpy()
-    tro, dro = np.asarray(w.target_row_off), np.asarray(w.draft_row_off)
-    L2E = 1.4426950408889634
-    for b in range(w.batch):
-        T = float(w.temperatures[b])
-        rows = [(w.target, r, r) for r in range(tro[b], tro[b + 1])] + \
-               [(w.draft, r, w.rows_target + r) for r in range(dro[b], dro[b + 1])]
-        for arr, r, flat in rows:
-            vals = wl.stored_f32(arr[r]).astype(np.float64)
-            k = int(ks[b])
-            tau = np.sort(vals)[::-1][k - 1] if 0 < k < vals.size else -np.inf
-            assert m[flat] == vals.max()
-            ss = np.exp2((vals[vals >= tau] - vals.max()) / T * L2E).sum()
-            assert abs(s[flat] - ss) <= 1e-5 * ss
+    print(f"top-k V={V} {dtype} worst relative error of s", check_row_stats(sv, w, db, top_ks=ks))
 
 
 def test_topk_one_matches_greedy(sv):
