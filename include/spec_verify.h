@@ -418,10 +418,21 @@ SPEC_API spec_status_t spec_debug_light_exp2(const float* x, float* y, int64_t n
 
 /* Profiling hook for the calling thread: when both are non-NULL, the next
  * spec_verify_sample / spec_verify_greedy call made by this thread records
- * start_event (a cudaEvent_t) on its stream just before the streaming pass and
- * stop_event just after it, then clears the hook. Lets a caller time the
- * dominant kernel with its own CUDA events. NULL, NULL clears it. */
+ * start_event (a cudaEvent_t) on its stream just before its dominant kernel
+ * (the fused verify kernel where a sampling call takes it, else the
+ * streaming pass) and stop_event just after it, then clears the hook. Lets a
+ * caller time that kernel with its own CUDA events. NULL, NULL clears it. */
 SPEC_API spec_status_t spec_debug_time_next_stats(void* start_event, void* stop_event);
+
+/* Test hook, process-wide: which kernels spec_verify_sample runs. path 0: the
+ * default choice (the separate kernels: streaming pass, finalize, tile pass,
+ * draw); 1: the separate kernels; 2: the fused verify kernel (one cooperative
+ * launch that streams the sequences in waves and runs each sequence's
+ * decision, tile pass and draw while later rows stream) wherever it applies:
+ * sampling without top-k / top-p, rows on 16-byte boundaries, V <= 262144.
+ * Both follow the same rules; the hook lets tests check each. Other values:
+ * SPEC_ERR_INVALID_ARG. */
+SPEC_API spec_status_t spec_debug_set_path(int32_t path);
 
 #ifdef __cplusplus
 }

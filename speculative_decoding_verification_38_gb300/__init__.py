@@ -164,6 +164,8 @@ def lib():
             L.spec_debug_light_exp2.argtypes = [vp, vp, i64, vp]
             L.spec_debug_time_next_stats.restype = ctypes.c_int
             L.spec_debug_time_next_stats.argtypes = [vp, vp]
+            L.spec_debug_set_path.restype = ctypes.c_int
+            L.spec_debug_set_path.argtypes = [ctypes.c_int32]
             if L.spec_abi_version() != SPEC_ABI_VERSION:
                 raise ImportError("libspecverify.so ABI version mismatch")
             _lib = L
@@ -439,6 +441,16 @@ def spec_debug_time_next_stats(start_event=None, stop_event=None) -> int:
     a = None if start_event is None else start_event.cuda_event
     b = None if stop_event is None else stop_event.cuda_event
     return lib().spec_debug_time_next_stats(a, b)
+
+
+PATH_DEFAULT, PATH_SEPARATE, PATH_FUSED = 0, 1, 2
+
+
+def spec_debug_set_path(path: int) -> int:
+    """Process-wide test switch for sampling calls: PATH_DEFAULT, PATH_SEPARATE
+    (the streaming, finalize, tile and draw kernels) or PATH_FUSED (the one
+    cooperative kernel, wherever it applies)."""
+    return lib().spec_debug_set_path(int(path))
 
 
 def spec_debug_light_exp2(x, y, stream=None) -> int:

@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libspecverify.so")
-SOURCES = ["api.cu", "stats.cu", "sampler.cu", "misc.cu", "topk.cu", "ngram.cu", "tree.cu"]
+SOURCES = ["api.cu", "stats.cu", "sampler.cu", "verify.cu", "misc.cu", "topk.cu", "ngram.cu", "tree.cu"]
 HEADERS = ["common.cuh", "internal.h", "precise.cuh", "stream.cuh", "tile.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -1,6 +1,8 @@
 // api.cu -- the extern "C" entry points of libspecverify.so: argument
 // validation, the workspace layout, and the launches. Nothing here computes
 // part of the verify step on the host; every step runs in the kernels.
+#include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
@@ -16,6 +18,7 @@ struct DeviceInfo {
     bool ready = false;
     int resident_sample = 0;
     int resident_greedy = 0;
+    int resident_verify = 0;  // CTAs of the fused verify kernel resident at once
     int sms = 0;
 };
 std::mutex g_mu;
@@ -30,6 +33,7 @@ bool device_info(int& dev, DeviceInfo& out) {
         d.resident_sample = stats_resident_ctas(dev, 0);
         d.resident_greedy = stats_resident_ctas(dev, 1);
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+        d.resident_verify = verify_resident_ctas(dev);
         if (d.resident_sample <= 0 || d.resident_greedy <= 0) return false;
         d.ready = true;
     }
@@ -220,11 +224,20 @@ bool build_params(const spec_verify_args_t* a, int greedy, int grid_cap, int tma
     return true;
 }
 
-spec_status_t prepare(const spec_verify_args_t* a, int greedy, StatsParams& p, Layout& L, int& dev) {
+// Which kernels a sampling call takes (spec_debug_set_path): 0 the default
+// choice, 1 the separate kernels, 2 the fused kernel wherever it applies.
+std::atomic<int> g_path{0};
+// The default: the separate kernels. The fused kernel is correct on every
+// case it takes but does not yet beat them on the benchmarked workload.
+constexpr bool kFusedByDefault = false;
+
+spec_status_t prepare(const spec_verify_args_t* a, int greedy, StatsParams& p, Layout& L, int& dev,
+                      DeviceInfo* info = nullptr) {
     spec_status_t st = check_call(a, greedy);
     if (st) return st;
     DeviceInfo di;
     if (!device_info(dev, di)) return SPEC_ERR_CUDA;
+    if (info) *info = di;
     const int tma = (SPECV_STREAM_TMA && tma_ok(a, greedy)) ? 1 : 0;
     int cap = tma ? di.sms : (greedy ? di.resident_greedy : di.resident_sample);
     if (cap > kGridCap) cap = kGridCap;
@@ -292,9 +305,65 @@ SPEC_API spec_status_t spec_verify_sample(const spec_verify_args_t* a, spec_stre
     StatsParams p;
     Layout L;
     int dev = 0;
-    spec_status_t st = prepare(a, 0, p, L, dev);
+    DeviceInfo di;
+    spec_status_t st = prepare(a, 0, p, L, dev, &di);
     if (st) return st;
     cudaStream_t s = (cudaStream_t)stream;
+    // The fused kernel: rows on 16-byte boundaries, no truncation, V within
+    // its tile limit, few enough rows per CTA, and the whole grid resident at
+    // once. Its grid is one CTA per SM (fewer for small problems); the
+    // sequences stream in W waves of about eight sequences each.
+    const int32_t ntile = (int32_t)((p.V + kTile - 1) / kTile);
+    const int64_t G = std::min<int64_t>(std::min(di.sms, di.resident_verify),
+                                        std::max<int64_t>(1, (p.N + kMinChunk - 1) / kMinChunk));
+    const int64_t chunk1 = std::max<int64_t>(kMinChunk, ((p.N + G - 1) / G + kChunkAlign - 1) / kChunkAlign * kChunkAlign);
+    const int path = g_path.load();
+    const bool want_fused = path == 2 || (path == 0 && kFusedByDefault);
+    if (want_fused && p.tma && !p.direct && ntile <= kVerifyMaxTiles && G >= 1 &&
+        2 * (chunk1 / p.V + 2) <= kVerifyMaxLocalRows) {
+        const int32_t W = std::max(1, std::min(kVerifyMaxWaves, (p.B + 7) / 8));
+        // partial slots as for the shortest slice any wave split can give
+        StatsParams q;
+        Layout Lf;
+        if (!build_params(a, 0, (int)(W * G), 1, q, Lf)) return SPEC_ERR_WORKSPACE;
+        q.grid = (int32_t)G;
+        VerifyParams vp;
+        vp.s = q;
+        SampleParams& sp = vp.t;
+        sp.tgt = q.tgt;
+        sp.dft = q.dft;
+        sp.tdt = q.tdt;
+        sp.ddt = q.ddt;
+        sp.V = q.V;
+        sp.B = q.B;
+        sp.ntile = ntile;
+        sp.tasks_in = q.tasks;
+        sp.tasks = q.tasks;
+        char* ws = (char*)a->workspace;
+        sp.recs = (TileRec*)(ws + Lf.off_recs);
+        sp.open = (uint16_t*)(ws + Lf.off_open);
+        sp.out_tokens = q.out_tokens;
+        sp.seq_status = q.seq_status;
+        sp.err = q.err;
+        sp.tab = exp2_table();
+        vp.spart = (float2*)(ws + Lf.off_spart);
+        vp.tiles_done = (uint32_t*)(ws + kTilesDoneOffset);
+        vp.ready = (uint32_t*)(ws + kReadyOffset);
+        vp.ready_tail = (uint32_t*)(ws + kReadyTailOffset);
+        vp.exit_count = (uint32_t*)(ws + kExitCountOffset);
+        vp.claim = (uint32_t*)(ws + kClaimOffset);
+        // a wait on another CTA gives up after 2 s plus the time to read the
+        // rows at 100 GB/s
+        const double bytes = (double)q.N * (q.tdt == SPEC_F32 ? 4.0 : 2.0);
+        vp.wait_ns = (uint64_t)(2e9 + bytes / 100.0);
+        vp.waves = W;
+        cudaEvent_t e0 = t_ev_start, e1 = t_ev_stop;
+        t_ev_start = t_ev_stop = nullptr;
+        if (e0 && e1 && cudaEventRecord(e0, s) != cudaSuccess) return SPEC_ERR_CUDA;
+        if (launch_verify(vp, s) != cudaSuccess) return SPEC_ERR_CUDA;
+        if (e0 && e1 && cudaEventRecord(e1, s) != cudaSuccess) return SPEC_ERR_CUDA;
+        return SPEC_OK;
+    }
     if (p.direct) {
         // top-k: thresholds and truncated row statistics in one pass, then finalize
         if (topk_with_hook(p, s) != cudaSuccess) return SPEC_ERR_CUDA;
@@ -459,6 +528,12 @@ SPEC_API spec_status_t spec_debug_probs(const spec_verify_args_t* a, int32_t seq
 SPEC_API spec_status_t spec_debug_light_exp2(const float* x, float* y, int64_t n, spec_stream_t stream) {
     if (!x || !y || n < 1 || !aligned(x, 4) || !aligned(y, 4)) return SPEC_ERR_INVALID_ARG;
     if (launch_debug_light_exp2(x, y, n, (cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
+SPEC_API spec_status_t spec_debug_set_path(int32_t path) {
+    if (path < 0 || path > 2) return SPEC_ERR_INVALID_ARG;
+    g_path.store(path);
     return SPEC_OK;
 }
 

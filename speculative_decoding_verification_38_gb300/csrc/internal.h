@@ -32,9 +32,22 @@ constexpr int kOpenCap = 32;           // open columns a sampler tile lists for 
 constexpr int64_t kChunkAlign = 64;   // elements; keeps 16-byte alignment for both dtypes
 constexpr int64_t kMinChunk = 1024;   // smallest slice one CTA streams
 constexpr int kGridCap = 4096;        // most CTAs of one streaming pass
-constexpr int kMaxBatch = 65536;      // arrival counters in the workspace header
-constexpr size_t kHeaderBytes = (size_t)kMaxBatch * 4 + 256;  // arrival counters + error words
-constexpr size_t kErrWordOffset = (size_t)kMaxBatch * 4;        // device error flags (bit 0: a wait timed out)
+constexpr int kMaxBatch = 65536;      // per-sequence words in the workspace header
+// Workspace header, zeroed once by spec_workspace_init; every word returns
+// to zero by the end of each call that uses it:
+//   [0, 4B)     per-sequence arrival counters (both streaming passes)
+//   [4B, 8B)    per-sequence tile items done (fused verify kernel)
+//   [8B, 12B)   fused verify kernel: sequences in the order they were
+//               finalized, as b + 1 (0: not yet)
+//   then 256 bytes of words: the device error flags, the fused kernel's
+//   ready-list length, its exit counter and its count of tile items handed out.
+constexpr size_t kTilesDoneOffset = (size_t)kMaxBatch * 4;
+constexpr size_t kReadyOffset = (size_t)kMaxBatch * 8;
+constexpr size_t kErrWordOffset = (size_t)kMaxBatch * 12;       // device error flags (bit 0: a wait timed out)
+constexpr size_t kReadyTailOffset = kErrWordOffset + 4;
+constexpr size_t kExitCountOffset = kErrWordOffset + 8;
+constexpr size_t kClaimOffset = kErrWordOffset + 12;              // fused kernel: tile items handed out
+constexpr size_t kHeaderBytes = kErrWordOffset + 256;
 
 constexpr int kSeqTimeout = 6;                                   // per-sequence status after a timed-out wait
 constexpr int kSeqUnsupported = 7;                               // per-sequence status: a tree node with too many candidates
@@ -92,7 +105,8 @@ struct StatsParams {
     int32_t* seq_status;
     // workspace views
     uint32_t* counters;  // [B] self-resetting arrival counters
-    uint32_t* err;       // device error word (bit 0: a bounded wait gave up)
+    uint32_t* err;       // device error word (bit 0: a bounded wait gave up; bit 1: the fused kernel saw more
+                         // finished sequences than the batch holds, i.e. offsets that break the work split)
     float2* partials;    // [rows_total * S * pw]
     float2* row_stats;   // [rows_total] merged per-row statistics
     float2* pq;          // [rows_d] (p(x), q(x))
@@ -147,8 +161,32 @@ struct SampleParams {
 struct Layout {
     int64_t rows_total, N, chunk;
     int32_t S, grid;
-    size_t off_partials, off_rowstats, off_pq, off_tasks, off_recs, off_open, off_tau, off_keep, off_keepn, total;
+    size_t off_partials, off_rowstats, off_pq, off_tasks, off_recs, off_open, off_tau, off_keep, off_keepn, off_spart,
+        total;
 };
+
+// The fused sampling verify (one cooperative launch): the streaming pass,
+// each sequence's accept scan as soon as its rows are folded, and the tile
+// pass and draw of each finished sequence while other rows still stream.
+struct VerifyParams {
+    StatsParams s;          // streaming pass and decision (s.tma layout: one partial per warp)
+    SampleParams t;         // tile pass and draw
+    float2* spart;          // [rows_total * S] one merged partial per (row, CTA slice)
+    uint32_t* tiles_done;   // header: [B] tile items finished
+    uint32_t* ready;        // header: [B] finalized sequences in order, b + 1
+    uint32_t* ready_tail;   // header word: entries in `ready`
+    uint32_t* exit_count;   // header word: CTAs that finished
+    uint32_t* claim;        // header word: tile items handed out
+    uint64_t wait_ns;       // a wait on another CTA gives up after this long
+    int32_t waves;          // sequence groups streamed one after another (1..kVerifyMaxWaves)
+};
+constexpr int kVerifyMaxLocalRows = 256;  // rows one CTA's slices of the fused kernel may touch
+constexpr int kVerifyMaxWaves = 16;
+constexpr int kVerifyMaxTiles = 256;      // fused kernel: V <= 256 * kTile
+// Launch the fused kernel (cooperative); cudaErrorNotSupported-like errors
+// leave the caller to use the separate kernels.
+cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
+int verify_resident_ctas(int device);  // CTAs of the fused kernel one device holds at once (0: unknown)
 
 // Work split and workspace layout for a given problem. grid_cap bounds the
 // number of streaming CTAs (the launch uses the device's resident capacity).

@@ -121,6 +121,21 @@ __device__ __forceinline__ df k_of_temperature(float T) {
     return fast_two_sum(q, __fdiv_rn(r, T));
 }
 
+// The same k as a pair whose low part is positive (at least the smallest
+// normal float), for the weights of the residual draw: then (l - m) * hi +
+// (l - m) * lo is -inf rather than NaN for a logit of -inf, with no separate
+// test. The pair still equals k to within about 2^-47 of k (one rounding of
+// the low part). k.hi > 0.
+__device__ __forceinline__ df k_pos_lo(df k) {
+    float hi = k.hi, lo = k.lo;
+    if (!(lo > 0.f)) {
+        const float h2 = __int_as_float(__float_as_int(hi) - 1);  // the float below hi
+        lo = __fadd_rn(lo, __fsub_rn(hi, h2));                  // hi - h2 is exact
+        hi = h2;
+    }
+    return df{hi, fmaxf(lo, 1.17549435e-38f)};
+}
+
 // Table 2^(i/64), i = 0..63, as float pairs.
 using Exp2Table = Exp2Pairs;
 static __device__ __noinline__ void exp2_table_init(Exp2Table& t) {

@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(kSampThreads, 4) sampler_kernel(SampleParams p
     const RowPair<TDT, DDT> rp = tile_rows<TDT, DDT>(p, t, tile);
     TileAcc acc;
     if (WIDE && warp >= kGroups) acc = TileAcc{};
-    else tile_sums<TDT, DDT, WIDE>(rp, resid, r_hi, r_lo, sm, p.open + item * kOpenCap, sw, warp, warp, acc);
+    else tile_sums_packed<TDT, DDT>(rp, resid, r_hi, r_lo, TileScratch{sm.q[warp], &sm.nu[sw], sm.uw[sw], &sm.tab},
+                                    p.open + item * kOpenCap, WIDE ? warp : 0, WIDE ? warp + 1 : kGroups, acc);
     df tot = warp_sum4_df(acc.st, acc.sd, resid ? acc.a : acc.st, acc.b);
     if (WIDE) {  // the groups' sums in warp order
         if (warp < kGroups && (lane & 7) == 0) {
@@ -217,7 +218,7 @@ __global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
             const float4 ab = __ldcg(reinterpret_cast<const float4*>(recs + ti));
             x = df_add(resid_of_sums(df{ab.x, ab.y}, df{ab.z, ab.w}, It, Id), warp_sum_df(c));
         } else {
-            x = warp_sum_df(lane_tile_sum(rp, 0, mode, It, Id, cl, *reinterpret_cast<SampSmem*>(&sm), warp));
+            x = warp_sum_df(lane_tile_sum(rp, 0, mode, It, Id, cl, TileScratch{sm.q[warp], nullptr, nullptr, &sm.tab}));
         }
         if (lane == 0) {
             sm.w_hi[ti] = x.hi;

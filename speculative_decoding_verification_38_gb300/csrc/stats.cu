@@ -438,7 +438,7 @@ __device__ void finalize_sample(const StatsParams& p, int32_t b, Smem& sm) {
             t.drow = a < g ? d0 + a : -1;
             t.out_slot = t0 + a;
             t.u = sm.us[a];
-            const df kk = k_of_temperature(temp_of(p, b));
+            const df kk = k_pos_lo(k_of_temperature(temp_of(p, b)));
             t.k_hi = kk.hi;
             t.k_lo = kk.lo;
             t.mt = sm.rs[a].x;
@@ -967,7 +967,7 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(StatsParams p) {
         t.out_slot = t0 + a;
         t.u = p.uniforms ? __ldg(p.uniforms + 2 * (t0 + a) + 1)
                          : draw_uniforms(p.seed, p.round, p.seq_offset + (uint32_t)b, (uint32_t)a).y;
-        const df kk = k_of_temperature(temp_of(p, b));
+        const df kk = k_pos_lo(k_of_temperature(temp_of(p, b)));
         t.k_hi = kk.hi;
         t.k_lo = kk.lo;
         t.mt = fs.rs[a].x;
@@ -1017,6 +1017,8 @@ Layout make_layout(int64_t B, int64_t V, int64_t rows_t, int64_t rows_d, int gre
     off = al(off + (keep ? (size_t)L.rows_total * kKeepCap * sizeof(uint32_t) : 0));
     L.off_keepn = off;
     off = al(off + (keep ? (size_t)L.rows_total * sizeof(int32_t) : 0));
+    L.off_spart = off;
+    off = al(off + (greedy ? 0 : (size_t)L.rows_total * L.S * sizeof(float2)));
     L.total = off;
     return L;
 }
