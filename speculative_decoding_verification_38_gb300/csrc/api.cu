@@ -312,7 +312,7 @@ SPEC_API spec_status_t spec_verify_sample(const spec_verify_args_t* a, spec_stre
     // The fused kernel: rows on 16-byte boundaries, no truncation, V within
     // its tile limit, few enough rows per CTA, and the whole grid resident at
     // once. Its grid is one CTA per SM (fewer for small problems); the
-    // sequences stream in W waves of about eight sequences each.
+    // sequences stream in W waves of about sixteen sequences each.
     const int32_t ntile = (int32_t)((p.V + kTile - 1) / kTile);
     const int64_t G = std::min<int64_t>(std::min(di.sms, di.resident_verify),
                                         std::max<int64_t>(1, (p.N + kMinChunk - 1) / kMinChunk));
@@ -321,7 +321,7 @@ SPEC_API spec_status_t spec_verify_sample(const spec_verify_args_t* a, spec_stre
     const bool want_fused = path == 2 || (path == 0 && kFusedByDefault);
     if (want_fused && p.tma && !p.direct && ntile <= kVerifyMaxTiles && G >= 1 &&
         2 * (chunk1 / p.V + 2) <= kVerifyMaxLocalRows) {
-        const int32_t W = std::max(1, std::min(kVerifyMaxWaves, (p.B + 7) / 8));
+        const int32_t W = std::max(1, std::min(kVerifyMaxWaves, (p.B + 15) / 16));
         // partial slots as for the shortest slice any wave split can give
         StatsParams q;
         Layout Lf;

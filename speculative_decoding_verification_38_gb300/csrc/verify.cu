@@ -49,6 +49,7 @@ constexpr int kVTailWarps = 8;
 constexpr int kVThreads = (kVStreamWarps + kVTailWarps) * 32;
 constexpr int kVRing = kTmaStages * (int)kTmaStageBytes;  // bytes of one streaming warp's ring
 constexpr int kVMaxSegs = 2 * kVerifyMaxWaves;           // a CTA's slice of a wave: a target part and a draft part
+constexpr int kVClosers = 2;                              // tail warps that close the CTA's rows
 
 // One contiguous flat range of the CTA's work (flat element e: row e / V of
 // the target rows, then of the draft rows, as in the streaming pass).
@@ -124,7 +125,7 @@ __device__ uint32_t warp_wait_nonzero(const uint32_t* w, uint64_t limit_ns) {
             unsigned ns = 64;
             for (uint32_t it = 0; it < kPollCap; ++it) {
                 __nanosleep(ns);
-                if (ns < 1024) ns <<= 1;
+                if (ns < 2048) ns <<= 1;
                 v = ld_acquire(w);
                 if (v || global_ns() - t0 > limit_ns) break;
             }
@@ -885,17 +886,19 @@ __device__ __noinline__ void draw_warp(const VerifyParams& vp, VScratch& x, cons
     if (lane == 0 && col >= 0) p.out_tokens[t.out_slot] = (int32_t)((int64_t)sel * kTile + col);
 }
 
-// The closer: tail warp 0 of each CTA closes the CTA's rows in order, each
-// as soon as all streaming warps have left it (shared-memory counters), so
-// the merges, the slice counts and the decisions they complete run beside
-// the stream. Every wait is bounded.
-__device__ void closer_warp(const VerifyParams& vp, VSmem& sm) {
+// The closers: tail warps 0 .. nclosers - 1 of each CTA close the CTA's
+// rows (closer c takes every nclosers-th row, in order), each as soon as all
+// streaming warps have left it (shared-memory counters), so the merges, the
+// slice counts and the decisions they complete run beside the stream. Every
+// wait is bounded.
+__device__ void closer_warp(const VerifyParams& vp, VSmem& sm, int which, int nclosers) {
     const StatsParams& p = vp.s;
     const int lane = threadIdx.x & 31;
     for (int s = 0; s < sm.nseg; ++s) {
         const VSeg& g = sm.seg[s];
         const int64_t r1 = (g.f1 - 1) / p.V;
         for (int64_t r = g.r0; r <= r1; ++r) {
+            if ((g.lbase + (r - g.r0)) % nclosers != which) continue;  // the other closer's row
             uint32_t* cnt = &sm.rowcnt[g.lbase + (r - g.r0)];
             int ok = 1;
             if (lane == 0) {
@@ -993,7 +996,7 @@ __global__ void __launch_bounds__(kVThreads, 1) verify_kernel(VerifyParams vp) {
         // no units left: the warp's ring becomes its scratch for tile items and draws
         if (clean) tail_loop<TDT, DDT>(vp, *reinterpret_cast<VScratch*>(ring + (size_t)warp * kVRing), sm.tab);
     } else {
-        if (warp == kVStreamWarps) closer_warp(vp, sm);
+        if (warp - kVStreamWarps < kVClosers) closer_warp(vp, sm, warp - kVStreamWarps, kVClosers);
         tail_loop<TDT, DDT>(vp, sm.ts[warp - kVStreamWarps], sm.tab);
     }
     __syncthreads();
