@@ -78,6 +78,10 @@ KERNELS = {
              "profile": "tree_kernel_bench_trees_dram.txt"},
     "topp": {"name": "topk_kernel (top-k threshold pass, storing each top-p row's kept values for nucleus_kernel)",
              "sources": ("topk.cu", "common.cuh", "internal.h", "precise.cuh"), "profile": "topk_kernel_c3_k{k}_p_dram.txt"},
+    "whole": {"name": "whole_nucleus_kernel (top-p without top-k: each bf16 row's pattern counts, nucleus and sum "
+                      "in one read of the row)",
+              "sources": ("topk.cu", "common.cuh", "internal.h", "precise.cuh"),
+              "profile": "whole_nucleus_kernel_c3_p09_dram.txt"},
 }
 
 
@@ -86,31 +90,27 @@ def topp_on(args):
 
 
 def launches_per_step(greedy, mode, top_k, adaptive):
-    """Kernels one timed step launches: the row pass (the streaming pass, or
-    the top-k pass with truncation) and the finalize; sampling adds the
-    sampler's tile pass and the draw; top-p adds the nucleus kernel, and the
-    whole-row nucleus kernel when top-k is off; --adaptive adds the gamma
-    policy."""
+    """Kernels one timed step launches: the row pass (the streaming pass, the
+    top-k pass with truncation, or the whole-row nucleus kernel for top-p
+    without top-k) and the finalize; sampling adds the sampler's tile pass and
+    the draw; top-p after top-k adds the nucleus kernel (the whole-row and
+    alone kernels are not launched when top-k is on for every sequence);
+    --adaptive adds the gamma policy."""
     n = 2 if greedy else 4
     if mode == "topp":
-        n += 1 + (1 if top_k <= 0 else 0)
+        n += 1
     return n + (1 if adaptive else 0)
 
 
 def kernel_label(mode, args):
-    """The roofline's kernel: the mode's dominant kernel, except that with top-p
-    and no top-k the kernel timed is still the top-k pass (the row maximum and
-    sum), while the whole-row nucleus kernel after it takes most of the step."""
-    if mode == "topp" and args.top_k <= 0:
-        return ("topk_kernel (row maximum and sum pass); the whole-row nucleus kernel after it, alone_kernel, "
-                "takes most of the step and is issue-bound: profiles/alone_kernel_c3_p09.md")
+    """The roofline's kernel: the mode's dominant kernel."""
     return KERNELS[mode]["name"]
 
 
 def mode_of(args):
-    if args.top_k > 0 or topp_on(args):
-        return "topp" if topp_on(args) else "topk"
-    return "stats"
+    if topp_on(args):
+        return "topp" if args.top_k > 0 else "whole"
+    return "topk" if args.top_k > 0 else "stats"
 
 
 # The other workloads of the scope table (C1, C2, C4, C5): descriptions and metrics.

@@ -71,14 +71,30 @@ cudaError_t stats_with_hook(const StatsParams& p, cudaStream_t s) {
     }
     return cudaSuccess;
 }
-// The top-k pass (hook as above) and the finalize kernel reading its rows.
-cudaError_t topk_with_hook(const StatsParams& p, cudaStream_t s) {
+// Whether whole_nucleus_kernel takes every row of the step: one top-p for
+// all sequences, top-k off, bf16 logits on both sides and no row offsets (so
+// no rows outside the sequences).
+bool whole_only(const StatsParams& p) {
+    return p.keep && !p.top_ks && !(p.top_k >= 1 && p.top_k < p.V) && !p.top_ps && p.top_p > 0.f &&
+           p.top_p < 1.f && p.tdt == SPEC_BF16 && (p.rows_d == 0 || (p.ddt == SPEC_BF16 && !p.probs)) && !p.tro;
+}
+// The top-k pass, the whole-row nucleus kernels and the finalize kernel
+// reading their rows. The hook brackets the top-k pass, or the whole-row
+// kernel when that one takes every row (the top-k pass then does not run).
+cudaError_t topk_with_hook(const StatsParams& p, int sms, cudaStream_t s) {
     cudaEvent_t e0 = t_ev_start, e1 = t_ev_stop;
     t_ev_start = t_ev_stop = nullptr;
+    cudaError_t e;
+    if (whole_only(p)) {
+        if (e0 && e1 && cudaEventRecord(e0, s) != cudaSuccess) return cudaErrorUnknown;
+        if ((e = launch_whole(p, sms, false, s)) != cudaSuccess) return e;
+        if (e0 && e1 && cudaEventRecord(e1, s) != cudaSuccess) return cudaErrorUnknown;
+        return launch_finalize(p, s);
+    }
     if (e0 && e1 && cudaEventRecord(e0, s) != cudaSuccess) return cudaErrorUnknown;
-    cudaError_t e = launch_topk(p, s);
-    if (e != cudaSuccess) return e;
+    if ((e = launch_topk(p, s)) != cudaSuccess) return e;
     if (e0 && e1 && cudaEventRecord(e1, s) != cudaSuccess) return cudaErrorUnknown;
+    if (p.keep && (e = launch_whole(p, sms, true, s)) != cudaSuccess) return e;
     if (p.keep && (e = launch_alone(p, s)) != cudaSuccess) return e;
     if (p.keep && (e = launch_nucleus(p, s)) != cudaSuccess) return e;
     return launch_finalize(p, s);
@@ -366,7 +382,7 @@ SPEC_API spec_status_t spec_verify_sample(const spec_verify_args_t* a, spec_stre
     }
     if (p.direct) {
         // top-k: thresholds and truncated row statistics in one pass, then finalize
-        if (topk_with_hook(p, s) != cudaSuccess) return SPEC_ERR_CUDA;
+        if (topk_with_hook(p, di.sms, s) != cudaSuccess) return SPEC_ERR_CUDA;
     } else if (stats_with_hook(p, s) != cudaSuccess) {
         return SPEC_ERR_CUDA;
     }

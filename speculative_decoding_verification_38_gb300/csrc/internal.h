@@ -207,9 +207,15 @@ cudaError_t launch_topk(const StatsParams& p, cudaStream_t s);
 // rewriting p.tau and the row sums; chained between launch_topk and
 // launch_finalize by programmatic launch.
 cudaError_t launch_nucleus(const StatsParams& p, cudaStream_t s);
-// Rows with top-p and no top-k: the nucleus of the whole row, one CTA per
-// row; chained after launch_topk (programmatic launch).
+// Rows with top-p and no top-k, f32 or probability rows (bf16 logits rows go
+// to launch_whole): the nucleus of the whole row, one CTA per row; chained
+// after launch_topk (programmatic launch).
 cudaError_t launch_alone(const StatsParams& p, cudaStream_t s);
+// Top-p without top-k on bf16 logits rows: each such row's maximum, nucleus
+// and sum over the nucleus, whole (the top-k pass and alone_kernel leave these
+// rows). One CTA per SM up to sms. after_topk: chained after launch_topk
+// (programmatic launch); else launched as the step's first kernel.
+cudaError_t launch_whole(const StatsParams& p, int sms, bool after_topk, cudaStream_t s);
 cudaError_t launch_sampler(const SampleParams& p, cudaStream_t s, bool pdl);
 void exp2_pairs(Exp2Pairs& t);  // host: fills the table
 cudaError_t launch_kv_rollback(const int32_t* kv_in, int32_t* kv_out, const int32_t* accepted,

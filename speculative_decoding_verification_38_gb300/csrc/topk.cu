@@ -34,6 +34,8 @@
 // one CTA per row.
 #include <math.h>
 
+#include <algorithm>
+
 #include "precise.cuh"
 
 namespace specv {
@@ -594,11 +596,27 @@ __device__ int32_t row_seq(const StatsParams& p, bool draft, int64_t lr) {
     return lo;
 }
 
+// Whether row r is a bf16 logits row of a sequence that samples from its
+// top-p nucleus with top-k off: whole_nucleus_kernel takes such a row whole
+// (its maximum, nucleus and sum over the nucleus), and the top-k pass and
+// alone_kernel leave it. Only with p.keep (some top-p on).
+__device__ bool whole_bf16_row(const StatsParams& p, int64_t r) {
+    if (!p.keep) return false;
+    const bool is_t = r < p.rows_t;
+    if ((is_t ? p.tdt : p.ddt) != SPECV_BF16 || (!is_t && p.probs != 0)) return false;
+    const int32_t b = row_seq(p, !is_t, is_t ? r : r - p.rows_t);
+    if (b < 0) return false;
+    const int64_t kk = p.top_ks ? (int64_t)__ldg(p.top_ks + b) : (int64_t)p.top_k;
+    const float tp = p.top_ps ? __ldg(p.top_ps + b) : p.top_p;
+    return !(kk >= 1 && kk < p.V) && tp > 0.f && tp < 1.f;
+}
+
 __global__ void __launch_bounds__(kTkThreads, 4) topk_kernel(StatsParams p) {
     extern __shared__ __align__(16) unsigned char tk_raw[];
     TkSmem& sm = *reinterpret_cast<TkSmem*>(tk_raw);
     pdl_launch_dependents();
     const int64_t r = blockIdx.x;
+    if (whole_bf16_row(p, r)) return;
     const bool is_t = r < p.rows_t;
     const int64_t lr = is_t ? r : r - p.rows_t;
     const int32_t b = row_seq(p, !is_t, lr);
@@ -786,10 +804,9 @@ __device__ int hist_pick(const float* hist, float& above, float& target, bool fi
 // along, for the row's sum over the nucleus.
 template <int DT>
 __device__ void row_nucleus_whole(const StatsParams& p, int64_t r, const char* row, float T, float tp, bool probs_row,
-                                  AloneSmem& sm, float* hist) {
+                                  AloneSmem& sm, float* hist, const float2 rs) {
     using KT = KeyTraits<DT>;
     constexpr int ESZ = KT::kEsz, EPV = 16 / ESZ, W = 8 * KT::kDigits;
-    const float2 rs = __ldcg(p.row_stats + r);
     if (!(rs.y == rs.y)) return;  // an invalid row stays invalid
     const float m = rs.x;
     const int64_t V = p.V;
@@ -975,6 +992,7 @@ __global__ void __launch_bounds__(kAlThreads, 1) alone_kernel(StatsParams p) {
     if (!(T > 0.f) || !isfinite(T)) T = 1.f;  // the finalize reports the sequence's bad temperature
     const int dt = is_t ? p.tdt : p.ddt;
     const bool probs_row = !is_t && p.probs != 0;
+    if (dt == SPECV_BF16 && !probs_row) return;  // whole_nucleus_kernel's row
     const char* row = (const char*)(is_t ? p.tgt : p.dft) + lr * p.V * (dt == SPECV_F32 ? 4 : 2);
     if (threadIdx.x < 64) {
         sm.tab.hi[threadIdx.x] = p.tab.hi[threadIdx.x];
@@ -982,8 +1000,9 @@ __global__ void __launch_bounds__(kAlThreads, 1) alone_kernel(StatsParams p) {
     }
     __syncthreads();
     float* hist = reinterpret_cast<float*>(al_hist);
-    if (dt == SPECV_F32) row_nucleus_whole<SPECV_F32>(p, r, row, T, tp, probs_row, sm, hist);
-    else row_nucleus_whole<SPECV_BF16>(p, r, row, T, tp, probs_row, sm, hist);
+    const float2 rs = __ldcg(p.row_stats + r);
+    if (dt == SPECV_F32) row_nucleus_whole<SPECV_F32>(p, r, row, T, tp, probs_row, sm, hist, rs);
+    else row_nucleus_whole<SPECV_BF16>(p, r, row, T, tp, probs_row, sm, hist, rs);
 }
 
 // ---------------------------------------------------------------- top-p
@@ -1124,6 +1143,765 @@ __global__ void __launch_bounds__(kNuThreads) nucleus_kernel(StatsParams p) {
         row_nucleus<SPECV_BF16>(p, r, row, T, tp, probs_row, tab);
 }
 
+// ------------------------------------------ top-p without top-k, bf16 logits
+// The nucleus of a whole bf16 logits row (top-p with top-k off), one CTA per
+// SM taking rows in turn. The rows reach shared memory through a ring of
+// bulk copies issued by one thread, a few chunks ahead of the CTA, across the
+// CTA's rows (the next row's first chunks arrive while the CTA decides the
+// current one).
+//  1. One pass over the row, chunk by chunk. Each chunk first raises the
+//     running maximum (its packed bf16 maxima, over the CTA). A bf16 logit's
+//     weight depends only on its 16-bit pattern, so the heavy columns
+//     (weight above 2^-13 of the running maximum's) are counted per pattern
+//     in shared memory (16-bit counters, two to a word), while the light
+//     ones are summed as they come: the SFU's 2^x, eight at a time and then
+//     in double-float, rescaled exactly whenever the maximum rises, with a
+//     bound on the sum's error (the SFU's relative error, the exponent's
+//     rounding, the summation's).
+//  2. Over the counts: each pattern's double-float weight times its count,
+//     summed from the highest pattern down (the patterns present spread over
+//     the threads, then a block scan); the total is those masses plus the
+//     light sum; the nucleus edge is the highest pattern whose mass at or
+//     above it reaches top_p of the total, found by one warp walking the
+//     patterns of the thread where the running mass crosses the target.
+//  3. The edge stands if it holds for every total within the light sum's
+//     bound and its pattern was heavy against the final maximum (so every
+//     column at or above it was counted). If not, or if the edge lies among
+//     the light columns, the row is counted again with every column by
+//     pattern and every pattern weighed in double-float (a pass with no light
+//     sum). A pattern held by 65536 columns or more wraps its counter; the
+//     counts then fall short of the columns counted and the row goes through
+//     the narrowing search of row_nucleus_whole instead.
+constexpr int kWnThreads = 1024, kWnWarps = kWnThreads / 32;
+constexpr int kWnKeys = 65536;
+constexpr int kWnWordsPerThread = kWnKeys / 2 / kWnThreads;     // 32 words: 64 consecutive patterns
+constexpr size_t kWnHistBytes = kWnKeys * sizeof(uint16_t);     // the counters (128 KB)
+constexpr int kWnStages = 2;                                    // ring stages
+constexpr uint32_t kWnChunk = 32u << 10;                        // bytes per stage: two 16-byte vectors per thread
+constexpr int kWnList = 4096;                                   // patterns present listed for the decision
+constexpr size_t kWnSmemBytes = kWnHistBytes + kWnStages * kWnChunk + kWnList * 6;  // counters, ring, list
+constexpr int kWnLoads = 4;                                     // 16-byte loads in flight per thread (recount)
+constexpr float kWnHeavy = -13.0f;  // exponents above this are counted by pattern, those below summed
+// Bound on the relative error of the SFU's 2^x used for the light sum (its
+// measured maximum on GB300 is 1.44e-7).
+constexpr float kWnEx2Err = 2.4e-7f;
+constexpr float kWnU = 5.9604645e-8f;  // 2^-24
+static_assert(kWnThreads == kAlThreads, "the narrowing search runs with the same CTA");
+static_assert(kWnHistBytes >= kAlSmemBytes, "the narrowing search reuses the counters' memory");
+static_assert(kWnWordsPerThread == 32, "one word per lane in the crossing walk");
+static_assert(kWnChunk == 32u * kWnThreads, "two vectors per thread per chunk");
+
+struct WholeSmem {
+    AloneSmem al;                    // the narrowing search's (its exp2 table serves every step)
+    df ws[kWnWarps], wf[kWnWarps];   // warp totals: masses, kept weights
+    df as[kWnWarps], af[kWnWarps];   // the same summed over the higher warps
+    df tot_s, tot_f;                 // the row's
+    df above_s, above_f;             // above the crossing thread's patterns
+    df lsum;                         // the light weights' sum
+    uint64_t full[kWnStages];        // ring: a stage's copy has landed
+    uint32_t wnz[kWnWarps];          // patterns present per warp
+    uint32_t cmax[3];                // a chunk step's maximum as an ordered key, by step modulo 3
+    uint32_t cnan, failed;
+    uint32_t negz, count, mink, maxk, nheavy;
+    int32_t tstar, verdict;
+};
+
+__device__ __forceinline__ df shfl_down_df(df v, int o) {
+    return df{__shfl_down_sync(kFull, v.hi, o), __shfl_down_sync(kFull, v.lo, o)};
+}
+
+// The value of a bf16 pattern key (the inverse of KeyTraits<SPECV_BF16>::key).
+__device__ __forceinline__ float bf16_of_key(uint32_t k) {
+    return __uint_as_float((k ^ ((k & 0x8000u) ? 0x8000u : 0xFFFFu)) << 16);
+}
+
+// Count one bf16 pattern (or both of a 32-bit word) under its order-preserving
+// key; -0 keeps a key of its own, joined to +0's when the counts are read.
+__device__ __forceinline__ void count_one(uint32_t* hist, uint32_t h) {
+    const uint32_t k = h ^ ((h & 0x8000u) ? 0xFFFFu : 0x8000u);
+    atomicAdd(hist + (k >> 1), 1u << ((k & 1u) << 4));
+}
+__device__ __forceinline__ void count_pair(uint32_t* hist, uint32_t w) {
+    const uint32_t sg = (w >> 15) & 0x00010001u;            // each half's sign bit
+    const uint32_t k = w ^ ((sg * 0x7FFFu) | 0x80008000u);  // both keys
+    const uint32_t k0 = k & 0xFFFFu, k1 = k >> 16;
+    atomicAdd(hist + (k0 >> 1), 1u << ((k0 & 1u) << 4));
+    atomicAdd(hist + (k1 >> 1), 1u << ((k1 & 1u) << 4));
+}
+
+// Both halves' maxima of two bf16 pairs, NaN propagating.
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// Row r's address.
+__device__ __forceinline__ const char* row_addr(const StatsParams& p, int64_t r) {
+    const bool is_t = r < p.rows_t;
+    const int dt = is_t ? p.tdt : p.ddt;
+    return (const char*)(is_t ? p.tgt : p.dft) + (is_t ? r : r - p.rows_t) * p.V * (dt == SPECV_F32 ? 4 : 2);
+}
+
+// A bf16 row as 16-byte vectors from its first 16-byte boundary, with the
+// columns before it (head) and after the last full vector (from tail0).
+struct RowSplit {
+    const uint4* vec;
+    int64_t head, nvec, tail0;
+};
+__device__ __forceinline__ RowSplit split_row(const char* row, int64_t V) {
+    RowSplit s;
+    s.head = (int64_t)(((16u - (uint32_t)((uintptr_t)row & 15u)) & 15u) / 2u);
+    if (s.head > V) s.head = V;
+    s.nvec = (V - s.head) / 8;
+    s.tail0 = s.head + s.nvec * 8;
+    s.vec = reinterpret_cast<const uint4*>(row + s.head * 2);
+    return s;
+}
+
+// f(q) for this thread's vectors, kWnLoads loads in flight; g(bits) for its
+// head and tail columns.
+template <typename F, typename G>
+__device__ __forceinline__ void each_vec(const char* row, int64_t V, F&& f, G&& g) {
+    const RowSplit rs = split_row(row, V);
+    const int t = threadIdx.x;
+    for (int64_t v0 = t; v0 < rs.nvec; v0 += kWnLoads * kWnThreads) {
+        uint4 q[kWnLoads];
+#pragma unroll
+        for (int i = 0; i < kWnLoads; ++i)
+            if (v0 + i * kWnThreads < rs.nvec) q[i] = ld_stream_v4(rs.vec + v0 + i * kWnThreads);
+#pragma unroll
+        for (int i = 0; i < kWnLoads; ++i)
+            if (v0 + i * kWnThreads < rs.nvec) f(q[i]);
+    }
+    const uint16_t* row16 = reinterpret_cast<const uint16_t*>(row);
+    if (t < rs.head) g((uint32_t)__ldg(row16 + t));
+    if (rs.tail0 + t < V) g((uint32_t)__ldg(row16 + rs.tail0 + t));
+}
+
+// Weight of a bf16 pattern relative to the maximum, double-float down to
+// 2^-120 (a single float below).
+__device__ __forceinline__ df pattern_weight(float v, float m, df kd, const Exp2Table& tab) {
+    const float dh = __fsub_rn(v, m);
+    if (!(dh > -INFINITY)) return df{0.f, 0.f};
+    const float x = __fmaf_rn(dh, kd.hi, __fmul_rn(dh, kd.lo));
+    if (x > -120.f) return heavy_weight(dh, 0.f, kd, tab);
+    return df{ex2(x), 0.f};
+}
+
+// The edge from the counts in hist (and, for the counts of heavy columns
+// only, the light sum L with error bound E), written to row r unless it is
+// not certain. expect: the columns counted. The patterns present are listed
+// in ascending order (when they fit the list) and split evenly over the
+// threads, so that their double-float weights are spread over the CTA (a row
+// with more patterns than the list holds splits the range of patterns
+// present instead, at most 64 to a thread). Returns 0 when written, 1 when
+// the edge needs every column counted, 2 when a counter wrapped. Every
+// thread returns the same.
+static __device__ __noinline__ int decide_edge(const StatsParams& p, int64_t r, uint32_t* hist, WholeSmem& sm,
+                                               float m, df kd, float k2, float tp, uint32_t expect, bool all, df L,
+                                               float E) {
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const uint16_t* h16 = reinterpret_cast<const uint16_t*>(hist);
+    uint16_t* lkey = reinterpret_cast<uint16_t*>(reinterpret_cast<char*>(hist) + kWnHistBytes + kWnStages * kWnChunk);
+    uint32_t* lcnt = reinterpret_cast<uint32_t*>(lkey + kWnList);
+    const float nmk = -__fmul_rn(m, k2);
+    const uint32_t negz = h16[0x7FFF];  // -0's count, joined to +0's
+    // this warp's counters: vectors warp*256 + i*32 + lane (i = 0..7), so that
+    // a warp reads contiguous words; vector v holds the patterns 8v .. 8v+7
+    const uint4* hw = reinterpret_cast<const uint4*>(hist) + warp * 256 + lane;
+
+    // A. the columns counted, the range of patterns present, and the number
+    // of patterns present in this warp's 2048 (list positions: the lower
+    // warps' come first, the list ascending)
+    {
+        uint32_t cnt = 0u, kmin = 0xFFFFFFFFu, kmax = 0u, nz = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint4 q = hw[i * 32];
+            if ((q.x | q.y | q.z | q.w) == 0u) continue;
+            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+            const uint32_t kb = 8u * (uint32_t)(warp * 256 + i * 32 + lane);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t key = kb + 2u * j, c0 = wv[j] & 0xFFFFu, c1 = wv[j] >> 16;
+                cnt += c0 + c1;
+                nz += (c0 ? 1u : 0u) + (c1 ? 1u : 0u);
+                if (c0) {
+                    kmin = min(kmin, key);
+                    kmax = key + 1u;
+                }
+                if (c1) {
+                    kmin = min(kmin, key + 1u);
+                    kmax = key + 2u;
+                }
+            }
+        }
+        if (warp == 0x7FFF / 2048 && lane == 31 && negz) --nz;                  // key 0x7FFF is no pattern of its own
+        if (warp == 0x8000 / 2048 && lane == 0 && negz && h16[0x8000] == 0u) ++nz;  // +0 present through -0 alone
+        cnt = __reduce_add_sync(kFull, cnt);
+        kmin = __reduce_min_sync(kFull, kmin);
+        kmax = __reduce_max_sync(kFull, kmax);
+        nz = __reduce_add_sync(kFull, nz);
+        if (lane == 0) {
+            atomicAdd(&sm.count, cnt);
+            atomicMin(&sm.mink, kmin);
+            atomicMax(&sm.maxk, kmax);
+            sm.wnz[warp] = nz;
+        }
+        __syncthreads();
+    }
+    if (sm.count != expect) return 2;
+    uint32_t klo = sm.mink, khi = sm.maxk - 1u;
+    if (klo == 0x7FFFu) klo = 0x8000u;  // -0 as +0
+    if (khi == 0x7FFFu) khi = 0x8000u;
+    uint32_t NZ = 0u, base = 0u;
+#pragma unroll 8
+    for (int w = 0; w < kWnWarps; ++w) {
+        const uint32_t v = sm.wnz[w];
+        NZ += v;
+        if (w < warp) base += v;
+    }
+    const bool listed = NZ <= (uint32_t)kWnList;
+    if (listed) {  // this warp's patterns, ascending, at its list position
+        uint32_t o = base;
+#pragma unroll 1
+        for (int i = 0; i < 8; ++i) {
+            const uint4 q = hw[i * 32];
+            const bool zero = (q.x | q.y | q.z | q.w) == 0u;
+            if (__all_sync(kFull, zero) && !(negz && warp == 0x8000 / 2048 && i == 0)) continue;
+            const uint32_t kb = 8u * (uint32_t)(warp * 256 + i * 32 + lane);
+            uint32_t c[8];
+            const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < 8; ++e) c[e] = (e & 1) ? wv[e >> 1] >> 16 : wv[e >> 1] & 0xFFFFu;
+            if (negz && (warp == 0x7FFF / 2048 || warp == 0x8000 / 2048)) {
+                if (kb + 7u == 0x7FFFu) c[7] = 0u;  // -0 ...
+                if (kb == 0x8000u) c[0] += negz;    // ... counts as +0
+            }
+            uint32_t n = 0u;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) n += c[e] ? 1u : 0u;
+            uint32_t x = n;  // inclusive prefix over the lanes
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, x, d);
+                if (lane >= d) x += y;
+            }
+            uint32_t pos = o + x - n;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (c[e]) {
+                    lkey[pos] = (uint16_t)(kb + e);
+                    lcnt[pos] = c[e];
+                    ++pos;
+                }
+            o += __shfl_sync(kFull, x, 31);
+        }
+        __syncthreads();
+    }
+    // thread tt's items, highest first: list entries, or the patterns of its range
+    const uint32_t per = listed ? (NZ + kWnThreads - 1) / kWnThreads : (khi - klo + kWnThreads) / kWnThreads;
+    auto items = [&](int tt) -> uint32_t {
+        const uint32_t b0 = listed ? min((uint32_t)tt * per, NZ) : min(klo + (uint32_t)tt * per, khi + 1u);
+        const uint32_t b1 = listed ? min(b0 + per, NZ) : min(b0 + per, khi + 1u);
+        return b1 - b0;
+    };
+    auto item = [&](int tt, uint32_t j, uint32_t& key) -> uint32_t {  // count of item j, its key in key
+        if (listed) {
+            const uint32_t e = min(min((uint32_t)tt * per, NZ) + per, NZ) - 1u - j;
+            key = lkey[e];
+            return lcnt[e];
+        }
+        const uint32_t b1 = min(min(klo + (uint32_t)tt * per, khi + 1u) + per, khi + 1u);
+        key = b1 - 1u - j;
+        uint32_t c = h16[key];
+        if (key == 0x7FFFu) c = 0u;
+        if (key == 0x8000u) c += negz;
+        return c;
+    };
+
+    // B. each thread's masses over its items, from the highest down
+    df S{0.f, 0.f}, F{0.f, 0.f};
+    {
+        const uint32_t n = items(t);
+#pragma unroll 1
+        for (uint32_t j = 0; j < n; ++j) {
+            uint32_t key;
+            const uint32_t c = item(t, j, key);
+            if (c == 0u) continue;
+            const float v = bf16_of_key(key), cf = (float)c;
+            S = df_add(S, df_mul_f(pattern_weight(v, m, kd, sm.al.tab), cf));
+            F = df_add(F, two_prod(kept_weight(v, false, k2, nmk), cf));
+        }
+    }
+
+    // C. masses above each thread's items: suffix sums over the lanes, then the warps
+    df xs = S, xf = F;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const df ys = shfl_down_df(xs, o), yf = shfl_down_df(xf, o);
+        if (lane + o < 32) {
+            xs = df_add(xs, ys);
+            xf = df_add(xf, yf);
+        }
+    }
+    df es = shfl_down_df(xs, 1), ef = shfl_down_df(xf, 1);  // the higher lanes' alone
+    if (lane == 31) es = ef = df{0.f, 0.f};
+    if (lane == 0) {
+        sm.ws[warp] = xs;
+        sm.wf[warp] = xf;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        df ys = sm.ws[lane], yf = sm.wf[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const df zs = shfl_down_df(ys, o), zf = shfl_down_df(yf, o);
+            if (lane + o < 32) {
+                ys = df_add(ys, zs);
+                yf = df_add(yf, zf);
+            }
+        }
+        df us = shfl_down_df(ys, 1), uf = shfl_down_df(yf, 1);
+        if (lane == 31) us = uf = df{0.f, 0.f};
+        sm.as[lane] = us;
+        sm.af[lane] = uf;
+        if (lane == 0) {
+            sm.tot_s = ys;
+            sm.tot_f = yf;
+        }
+    }
+    __syncthreads();
+    const df wa = sm.as[warp];
+    const df tot = df_add(sm.tot_s, L);
+    const df target = df_mul_f(tot, tp);
+
+    // D. the crossing thread: the highest one whose items reach the target
+    const bool cand = df_pos(S) && !df_gt(target, df_add(wa, xs));
+    const uint32_t tc = __reduce_max_sync(kFull, cand ? (uint32_t)t + 1u : 0u);
+    if (lane == 0 && tc) atomicMax(&sm.tstar, (int32_t)tc);
+    __syncthreads();
+    const int32_t ts = sm.tstar - 1;
+    if (ts < 0) {
+        if (!all) return 1;  // the edge lies among the light columns
+        // nothing reaches the target (rounding): the whole row
+        if (t == 0) {
+            const df f = sm.tot_f;
+            p.row_stats[r] = make_float2(m, __fadd_rn(f.hi, f.lo));
+            p.tau[r] = bf16_of_key(klo);
+        }
+        return 0;
+    }
+    if (t == ts) {
+        sm.above_s = df_add(wa, es);
+        sm.above_f = df_add(sm.af[warp], ef);
+    }
+    __syncthreads();
+    if (warp == (ts >> 5)) {
+        // E. the crossing thread's items, two per lane, lane 0 the highest
+        const uint32_t n = items(ts), j1 = 2u * (uint32_t)lane, j0 = j1 + 1u;
+        uint32_t key1 = 0u, key0 = 0u;
+        const uint32_t n1 = j1 < n ? item(ts, j1, key1) : 0u, n0 = j0 < n ? item(ts, j0, key0) : 0u;
+        df p1{0.f, 0.f}, p0{0.f, 0.f}, g1{0.f, 0.f}, g0{0.f, 0.f};
+        if (n1) {
+            const float v = bf16_of_key(key1);
+            p1 = df_mul_f(pattern_weight(v, m, kd, sm.al.tab), (float)n1);
+            g1 = two_prod(kept_weight(v, false, k2, nmk), (float)n1);
+        }
+        if (n0) {
+            const float v = bf16_of_key(key0);
+            p0 = df_mul_f(pattern_weight(v, m, kd, sm.al.tab), (float)n0);
+            g0 = two_prod(kept_weight(v, false, k2, nmk), (float)n0);
+        }
+        df x = df_add(p1, p0);  // inclusive prefix over the lanes (items downward)
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const df y = shfl_up_df(x, o);
+            if (lane >= o) x = df_add(y, x);
+        }
+        df ex = shfl_up_df(x, 1);
+        if (lane == 0) ex = df{0.f, 0.f};
+        const df base = df_add(sm.above_s, ex);
+        const df run1 = df_add(base, p1), run0 = df_add(run1, p0);
+        // 1 + the highest pattern whose mass at or above it reaches the
+        // target, with the mass above that pattern and at it
+        uint32_t kc = 0u;
+        df prev{0.f, 0.f}, at{0.f, 0.f};
+        if (df_pos(p1) && !df_gt(target, run1)) {
+            kc = key1 + 1u;
+            prev = base;
+            at = run1;
+        } else if (df_pos(p0) && !df_gt(target, run0)) {
+            kc = key0 + 1u;
+            prev = run1;
+            at = run0;
+        }
+        const uint32_t kbest = __reduce_max_sync(kFull, kc);
+        int verdict = 0;
+        uint32_t K;
+        if (kbest == 0u) {
+            // none within the thread (rounding): its lowest pattern with weight
+            const uint32_t lo = df_pos(p0) ? key0 : (df_pos(p1) ? key1 : 0xFFFFFFFFu);
+            K = __reduce_min_sync(kFull, lo);
+            verdict = all ? 0 : 1;
+        } else {
+            K = kbest - 1u;
+            if (!all) {
+                // the edge holds for every total within E of the estimate:
+                // the mass at or above K reaches the highest target, the
+                // mass above K stays under the lowest
+                const int src = __ffs(__ballot_sync(kFull, kc == kbest)) - 1;
+                const df pv = shfl_df(prev, src), av = shfl_df(at, src);
+                const df thi = df_mul_f(df_add(tot, df{E, 0.f}), tp);
+                const df tlo = df_mul_f(df_add(tot, df{-E, 0.f}), tp);
+                // and K heavy against the final maximum: then it was heavy
+                // against every running maximum, so every column at or
+                // above it was counted
+                const float dk = __fsub_rn(bf16_of_key(K), m);
+                const bool heavy = __fmaf_rn(dk, kd.hi, __fmul_rn(dk, kd.lo)) > kWnHeavy;
+                verdict = (heavy && !df_gt(thi, av) && df_gt(tlo, pv)) ? 0 : 1;
+            }
+        }
+        if (verdict == 0) {
+            df gs = (n1 && key1 >= K) ? g1 : df{0.f, 0.f};
+            if (n0 && key0 >= K) gs = df_add(gs, g0);
+            gs = warp_sum_df(gs);
+            if (lane == 0) {
+                const df f = df_add(sm.above_f, gs);
+                p.row_stats[r] = make_float2(m, __fadd_rn(f.hi, f.lo));
+                p.tau[r] = bf16_of_key(K);
+            }
+        }
+        if (lane == 0) sm.verdict = verdict;
+    }
+    __syncthreads();
+    return sm.verdict;
+}
+
+// Reset the counters and the scalars the counting steps accumulate into.
+__device__ __forceinline__ void clear_counts(uint32_t* hist, WholeSmem& sm) {
+    __syncthreads();  // earlier readers of the counters are done
+    uint4* h4 = reinterpret_cast<uint4*>(hist);
+#pragma unroll
+    for (int i = 0; i < kWnWordsPerThread / 4; ++i) h4[threadIdx.x + i * kWnThreads] = make_uint4(0u, 0u, 0u, 0u);
+    if (threadIdx.x == 0) {
+        sm.count = 0u;
+        sm.mink = 0xFFFFFFFFu;
+        sm.maxk = 0u;
+        sm.tstar = 0;
+        sm.nheavy = 0u;
+        sm.cnan = 0u;
+        sm.lsum = df{0.f, 0.f};
+    }
+    __syncthreads();
+}
+
+// Float bits as an unsigned key of the same order (NaN excluded).
+__device__ __forceinline__ uint32_t ord_key(float f) {
+    const uint32_t b = __float_as_uint(f);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float ord_value(uint32_t k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+constexpr uint32_t kOrdNegInf = 0x007FFFFFu;  // ord_key(-inf)
+constexpr uint32_t kOrdPosInf = 0xFF800000u;  // ord_key(+inf)
+
+// The ring's producer (thread 0): the CTA's rows in turn, each row's
+// 16-byte-aligned body in chunks of kWnChunk bytes.
+struct RingFeed {
+    int64_t row;      // the row being issued (>= rows: none left)
+    const char* src;  // the rest of its body
+    uint32_t left;    // bytes of it not yet issued
+    uint32_t g;       // chunks issued so far
+};
+__device__ __forceinline__ int64_t next_whole_row(const StatsParams& p, int64_t r, int64_t rows) {
+    while (r < rows && !whole_bf16_row(p, r)) r += gridDim.x;
+    return r;
+}
+__device__ void feed_set(RingFeed& f, const StatsParams& p, int64_t r, int64_t rows) {
+    for (;;) {
+        f.row = next_whole_row(p, r, rows);
+        f.left = 0u;
+        if (f.row >= rows) return;
+        const RowSplit rs = split_row(row_addr(p, f.row), p.V);
+        f.src = reinterpret_cast<const char*>(rs.vec);
+        f.left = (uint32_t)(rs.nvec * 16);
+        if (f.left) return;
+        r = f.row + gridDim.x;  // no full vector in this row: nothing to copy
+    }
+}
+__device__ void feed_issue(RingFeed& f, const StatsParams& p, int64_t rows, WholeSmem& sm, char* ring) {
+    if (f.row >= rows) return;
+    const uint32_t st = f.g % kWnStages, n = min(f.left, kWnChunk);
+    mbar_arrive_expect_tx(&sm.full[st], n);
+    bulk_g2s(ring + (size_t)st * kWnChunk, f.src, n, &sm.full[st]);
+    ++f.g;
+    f.src += n;
+    f.left -= n;
+    if (f.left == 0u) feed_set(f, p, f.row + gridDim.x, rows);
+}
+
+// A row whose edge the counts of its heavy columns could not settle (out of
+// line: rare). Unless a counter already wrapped, every column is counted by
+// pattern and every pattern weighed in double-float; a wrapped counter sends
+// the row to the narrowing search.
+static __device__ __noinline__ void whole_slow(const StatsParams& p, int64_t r, const char* row, float T, float tp,
+                                               uint32_t* hist, WholeSmem& sm, float m, df kd, float k2,
+                                               bool wrapped) {
+    const int64_t V = p.V;
+    int v = 2;
+    if (!wrapped) {
+        clear_counts(hist, sm);
+        each_vec(
+            row, V,
+            [&](const uint4& q) {
+                count_pair(hist, q.x);
+                count_pair(hist, q.y);
+                count_pair(hist, q.z);
+                count_pair(hist, q.w);
+            },
+            [&](uint32_t h) { count_one(hist, h); });
+        __syncthreads();
+        v = decide_edge(p, r, hist, sm, m, kd, k2, tp, (uint32_t)V, true, df{0.f, 0.f}, 0.f);
+    }
+    if (v == 2) {
+        __syncthreads();  // the counters' readers are done: the search reuses their memory
+        row_nucleus_whole<SPECV_BF16>(p, r, row, T, tp, false, sm.al, reinterpret_cast<float*>(hist),
+                                      make_float2(m, 0.f));
+    }
+}
+
+// 1. One pass over a row through the ring: the running maximum (chunk by
+// chunk, over the CTA), heavy columns counted by pattern, light ones summed
+// (out of line, so that the calls after it leave its registers alone).
+// Returns false if a ring wait gave up.
+static __device__ __noinline__ bool stream_row(const StatsParams& p, uint32_t* hist, char* ring, WholeSmem& sm,
+                                               uint32_t& g_io, uint32_t& cs_io, RingFeed& feed, int64_t rows,
+                                               uint32_t body, uint32_t nch, uint32_t eh, bool has_e, df kd,
+                                               float& m_out, df& l_out, uint32_t& nh_out, bool& nan_out) {
+    const int t = threadIdx.x, lane = t & 31;
+    uint32_t g = g_io, cs = cs_io;
+    df lacc{0.f, 0.f};
+    uint32_t nh = 0u;
+    float mrun = -INFINITY;
+    bool nan_row = false;
+    // the light weights of a vector's eight columns against the running
+    // maximum, summed in three levels; heavy columns counted instead
+    auto vec = [&](const uint4& q, float mr) -> float {
+        const uint32_t wv[4] = {q.x, q.y, q.z, q.w};
+        float x[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float dh = __fsub_rn((e & 1) ? bf16_hi(wv[e >> 1]) : bf16_lo(wv[e >> 1]), mr);
+            x[e] = __fmaf_rn(dh, kd.hi, __fmul_rn(dh, kd.lo));
+        }
+        const float xm = fmaxf(max3(x[0], x[1], x[2]), fmaxf(max3(x[3], x[4], x[5]), fmaxf(x[6], x[7])));
+        if (xm > kWnHeavy) {  // some column of the vector is heavy (rare)
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (x[e] > kWnHeavy) {
+                    count_one(hist, (e & 1) ? wv[e >> 1] >> 16 : wv[e >> 1] & 0xFFFFu);
+                    ++nh;
+                }
+        }
+        float w[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) w[e] = x[e] > kWnHeavy ? 0.f : ex2(x[e]);
+        return ((w[0] + w[1]) + (w[2] + w[3])) + ((w[4] + w[5]) + (w[6] + w[7]));
+    };
+    const uint4 ninf = make_uint4(0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u, 0xFF80FF80u);
+    const uint32_t steps = nch > 0u ? nch : 1u;
+#pragma unroll 1
+    for (uint32_t c = 0; c < steps; ++c) {
+        const bool has = c < nch;
+        const uint32_t st = g % kWnStages;
+        if (t == 0) sm.cmax[(cs + 1u) % 3u] = kOrdNegInf;  // its readers (step cs - 2) are past the last barrier
+        bool ok = true;
+        if (has) ok = mbar_wait_bounded(&sm.full[st], (g / kWnStages) & 1u, kWaitLimit);
+        const uint32_t nbytes = has ? min(kWnChunk, body - c * kWnChunk) : 0u;
+        const uint4* sv = reinterpret_cast<const uint4*>(ring + (size_t)st * kWnChunk);
+        const bool in0 = ok && (uint32_t)t * 16u < nbytes, in1 = ok && ((uint32_t)t + kWnThreads) * 16u < nbytes;
+        const uint4 q0 = in0 ? sv[t] : ninf, q1 = in1 ? sv[t + kWnThreads] : ninf;
+        uint32_t a = bmax2(bmax2(bmax2(q0.x, q0.y), bmax2(q0.z, q0.w)), bmax2(bmax2(q1.x, q1.y), bmax2(q1.z, q1.w)));
+        if (c == 0u && has_e) a = bmax2(a, eh | (eh << 16));
+        // the chunk's maximum over the CTA as an ordered key (a NaN, canonical
+        // from the packed maxima, ranks above +inf)
+        const uint32_t km = __reduce_max_sync(kFull, max(ord_key(bf16_lo(a)), ord_key(bf16_hi(a))));
+        if (lane == 0) atomicMax(&sm.cmax[cs % 3u], km);
+        // every thread has its vectors of this chunk: the stage is free again
+        if (__syncthreads_or(!ok)) {
+            g_io = g;
+            cs_io = cs;
+            return false;
+        }
+        if (t == 0 && has) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the reads above before the refill
+            feed_issue(feed, p, rows, sm, ring);
+        }
+        const uint32_t kc = sm.cmax[cs % 3u];
+        nan_row = nan_row || kc > kOrdPosInf;
+        const float mnew = nan_row ? mrun : fmaxf(mrun, ord_value(kc));
+        if (!nan_row && mnew < INFINITY && mnew > -INFINITY) {
+            if (mnew > mrun && mrun > -INFINITY) {
+                // rescale the light sum to the new maximum: 2^((mrun - mnew) k) in double-float
+                const df d = two_sum(mrun, -mnew);
+                const float x = __fmaf_rn(d.hi, kd.hi, __fmul_rn(d.hi, kd.lo));
+                lacc = x > -120.f ? df_mul(lacc, heavy_weight_t<true>(d.hi, d.lo, kd, sm.al.tab)) : df{0.f, 0.f};
+            }
+            mrun = mnew;
+            if (in0) acc_add(lacc, vec(q0, mrun));
+            if (in1) acc_add(lacc, vec(q1, mrun));
+            if (c == 0u && has_e) {
+                const float dh = __fsub_rn(__uint_as_float(eh << 16), mrun);
+                const float x = __fmaf_rn(dh, kd.hi, __fmul_rn(dh, kd.lo));
+                if (x > kWnHeavy) {
+                    count_one(hist, eh);
+                    ++nh;
+                } else {
+                    acc_add(lacc, ex2(x));
+                }
+            }
+        } else {
+            mrun = mnew;
+        }
+        if (has) ++g;
+        ++cs;
+    }
+    g_io = g;
+    cs_io = cs;
+    m_out = mrun;
+    l_out = lacc;
+    nh_out = nh;
+    nan_out = nan_row;
+    return true;
+}
+
+// One row (every thread). g: chunks taken from the ring so far; cs: chunk
+// steps so far (a row with no full vector takes one step with no chunk).
+// Returns false if a ring wait gave up (the CTA then stops).
+__device__ bool whole_row_bf16(const StatsParams& p, int64_t r, uint32_t* hist, char* ring, WholeSmem& sm,
+                               uint32_t& g, uint32_t& cs, RingFeed& feed, int64_t rows) {
+    const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+    const bool is_t = r < p.rows_t;
+    const int32_t b = row_seq(p, !is_t, is_t ? r : r - p.rows_t);
+    float T = p.temps ? __ldg(p.temps + b) : p.temperature;
+    if (!(T > 0.f) || !isfinite(T)) T = 1.f;  // the finalize reports the sequence's bad temperature
+    const float tp = p.top_ps ? __ldg(p.top_ps + b) : p.top_p;
+    const char* row = row_addr(p, r);
+    const int64_t V = p.V;
+    const RowSplit rs = split_row(row, V);
+    const uint32_t body = (uint32_t)(rs.nvec * 16), nch = (body + kWnChunk - 1u) / kWnChunk;
+    // the positive-low-part k: -inf logits give exponent -inf, not NaN
+    const df kd = k_pos_lo(k_of_temperature(T));
+    const float k2 = kLog2e / T;
+    // the columns outside the body: threads 0..7 the head, 8..15 the tail
+    uint32_t eh = 0xFF80u;  // -inf
+    bool has_e = false;
+    {
+        const uint16_t* row16 = reinterpret_cast<const uint16_t*>(row);
+        if (t < rs.head) {
+            eh = __ldg(row16 + t);
+            has_e = true;
+        } else if (t >= 8 && t < 16 && rs.tail0 + (t - 8) < V) {
+            eh = __ldg(row16 + rs.tail0 + (t - 8));
+            has_e = true;
+        }
+    }
+    clear_counts(hist, sm);
+
+    // 1. one pass: the running maximum, heavy columns counted, light ones summed
+    float mrun;
+    df lacc;
+    uint32_t nh;
+    bool nan_row;
+    if (!stream_row(p, hist, ring, sm, g, cs, feed, rows, body, nch, eh, has_e, kd, mrun, lacc, nh, nan_row))
+        return false;
+    const float m = mrun;
+    if (nan_row || !(m > -INFINITY && m < INFINITY)) {  // NaN anywhere, or an infinite maximum: invalid
+        if (t == 0) {
+            p.row_stats[r] = make_float2(m, NAN);
+            p.tau[r] = -INFINITY;
+        }
+        return true;
+    }
+    lacc = df_norm(lacc);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) lacc = df_add(lacc, shfl_xor_df(lacc, o));
+    nh = __reduce_add_sync(kFull, nh);
+    if (lane == 0) {
+        sm.ws[warp] = lacc;
+        atomicAdd(&sm.nheavy, nh);
+    }
+    __syncthreads();  // the counts and the warps' sums are complete
+    if (warp == 0) {
+        df y = sm.ws[lane];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) y = df_add(y, shfl_xor_df(y, o));
+        if (lane == 0) sm.lsum = y;
+    }
+    __syncthreads();
+    const df L = sm.lsum;
+    // |light sum - exact| <= E: each weight's SFU error; the exponent's two
+    // roundings (the difference v - m and the product by k, each within
+    // 2^-24 |x|, times ln 2 in the weight), where the sum over the light
+    // columns of w |x| = w log2(1/w) is at most L log2(n / L) for n columns
+    // (concavity), and at least 13 L; the summation's three roundings within
+    // each group of eight (the double-float sums and rescalings after them
+    // add no more than 2^-40 of the sum). Half again for margin.
+    const float lg = L.hi > 0.f ? fmaxf(-kWnHeavy, __log2f((float)V) - __log2f(L.hi) + 0.5f) : 0.f;
+    const float E = 1.5f * __fmul_rn(kWnEx2Err + 3.f * kWnU + 0x1p-40f + 2.f * 0.6931472f * kWnU * lg, L.hi);
+
+    // 2-3. the edge from the counts, else every column counted
+    const int v = decide_edge(p, r, hist, sm, m, kd, k2, tp, sm.nheavy, false, L, E);
+    if (v != 0) whole_slow(p, r, row, T, tp, hist, sm, m, kd, k2, v == 2);
+    return true;
+}
+
+// Every row whole_bf16_row selects, one CTA per SM taking rows in turn.
+// Launched after the top-k pass (or as the step's first kernel when it takes
+// every row); before it exits it waits for the kernel before it, so that the
+// kernels after it see both.
+__global__ void __launch_bounds__(kWnThreads, 1) whole_nucleus_kernel(StatsParams p) {
+    __shared__ WholeSmem sm;
+    extern __shared__ __align__(128) unsigned char wn_raw[];
+    uint32_t* hist = reinterpret_cast<uint32_t*>(wn_raw);
+    char* ring = reinterpret_cast<char*>(wn_raw + kWnHistBytes);
+    const int64_t rows = p.rows_t + p.rows_d;
+    if (threadIdx.x < 64) {
+        sm.al.tab.hi[threadIdx.x] = p.tab.hi[threadIdx.x];
+        sm.al.tab.lo[threadIdx.x] = p.tab.lo[threadIdx.x];
+    }
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kWnStages; ++i) mbar_init(&sm.full[i], 1);
+        sm.cmax[0] = sm.cmax[1] = sm.cmax[2] = kOrdNegInf;
+        sm.failed = 0u;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    RingFeed feed{rows, nullptr, 0u, 0u};  // thread 0's
+    if (threadIdx.x == 0) {
+        feed_set(feed, p, blockIdx.x, rows);
+        for (int i = 0; i < kWnStages; ++i) feed_issue(feed, p, rows, sm, ring);
+    }
+    uint32_t g = 0u, cs = 0u;
+    bool alive = true;
+    for (int64_t r = next_whole_row(p, blockIdx.x, rows); r < rows; r = next_whole_row(p, r + gridDim.x, rows)) {
+        if (!whole_row_bf16(p, r, hist, ring, sm, g, cs, feed, rows)) {
+            alive = false;
+            break;
+        }
+    }
+    // never leave while a copy into the ring may be in flight
+    if (threadIdx.x == 0) {
+        for (uint32_t q = g; q < feed.g; ++q)
+            mbar_wait_bounded(&sm.full[q % kWnStages], (q / kWnStages) & 1u, kWaitLimit);
+        if (!alive) atomicOr(p.err, 1u);
+    }
+    pdl_wait_primary();
+}
+
 }  // namespace
 
 cudaError_t launch_nucleus(const StatsParams& p, cudaStream_t s) {
@@ -1164,6 +1942,30 @@ cudaError_t launch_alone(const StatsParams& p, cudaStream_t s) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, alone_kernel, p);
+}
+
+cudaError_t launch_whole(const StatsParams& p, int sms, bool after_topk, cudaStream_t s) {
+    static bool attr_done = false;
+    if (!attr_done) {
+        const cudaError_t e = cudaFuncSetAttribute(whole_nucleus_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)kWnSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    const int64_t rows = p.rows_t + p.rows_d;
+    if (rows < 1 || !p.keep) return cudaSuccess;
+    if (!p.top_ks && p.top_k >= 1 && p.top_k < p.V) return cudaSuccess;  // top-k on for every sequence
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)std::min<int64_t>(rows, std::max(sms, 1)));
+    cfg.blockDim = dim3(kWnThreads);
+    cfg.dynamicSmemBytes = kWnSmemBytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = after_topk ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, whole_nucleus_kernel, p);
 }
 
 cudaError_t launch_topk(const StatsParams& p, cudaStream_t s) {

@@ -39,11 +39,11 @@ def test_modes_and_labels():
     assert bench.mode_of(_ns()) == "stats"
     assert bench.mode_of(_ns(top_k=50)) == "topk"
     assert bench.mode_of(_ns(top_k=50, top_p=0.9)) == "topp"
-    assert bench.mode_of(_ns(top_p=0.9)) == "topp"
+    assert bench.mode_of(_ns(top_p=0.9)) == "whole"  # top-p without top-k
     assert bench.mode_of(_ns(top_p=1.0)) == "stats"  # p = 1 is off
     alone = _ns(top_p=0.9)
-    assert "alone_kernel" in bench.kernel_label("topp", alone)
-    assert "alone_kernel" not in bench.kernel_label("topp", _ns(top_k=50, top_p=0.9))
+    assert "whole_nucleus_kernel" in bench.kernel_label("whole", alone)
+    assert "whole_nucleus_kernel" not in bench.kernel_label("topp", _ns(top_k=50, top_p=0.9))
     assert "top-p 0.9" in bench.metric_of(alone) and "top-k" not in bench.metric_of(alone)
     assert "top-k 50" in bench.metric_of(_ns(top_k=50, top_p=0.9))
     assert bench.metric_of(_ns()) == bench.METRIC
@@ -55,7 +55,7 @@ def test_launches_per_step():
     assert L(True, "stats", 0, False) == 2    # greedy: streaming pass, finalize
     assert L(False, "topk", 50, False) == 4   # the top-k pass replaces the streaming pass
     assert L(False, "topp", 50, False) == 5   # + the nucleus kernel
-    assert L(False, "topp", 0, False) == 6    # + the whole-row nucleus kernel
+    assert L(False, "whole", 0, False) == 4   # the whole-row nucleus kernel replaces the top-k pass
     assert L(False, "stats", 0, True) == 5    # + the gamma policy
 
 

@@ -176,3 +176,39 @@ def test_topp_alone_config3_full_size(sv):
     V=128256 bf16): every row's whole-row nucleus, in the bench's launch."""
     w = wl.config3(top_k=0, top_p=0.9)
     run_rounds(w, range(3), seed=0, label="C3 top-p 0.9 alone")
+
+
+def test_topp_alone_bf16_pattern_counts(sv):
+    """Whole-row nucleus of bf16 logits rows from pattern counts: a row where
+    one value fills 70,000 of 131,072 columns (its 16-bit counter wraps, so
+    the row takes the narrowing search), rows of +0 and -0 (joined to one
+    pattern; 40,000 of each, and 70,000 of -0), a row with NaN (invalid), a
+    row with -inf columns, and plain rows, all at top-p 0.9 with top-k off."""
+    rng = np.random.default_rng(41)
+    B, g, V = 8, 1, 131072
+    base = wl.sampling_workload("counts", config=401, batch=B, vocab=V, gammas=np.full(B, g), profile="zipf",
+                                dtype="bf16", sigma=0.6, temps=1.0, pool=2)
+    tgt = wl.stored_f32(base.target).reshape(B, g + 1, V).copy()
+    dft = wl.stored_f32(base.draft).reshape(B, g, V).copy()
+
+    def fill(b, cols, val):
+        tgt[b][:, cols] = val
+        dft[b][:, cols] = val
+
+    fill(0, rng.permutation(V)[:70_000], np.float32(-1.5))
+    perm = rng.permutation(V)
+    fill(1, perm[:40_000], np.float32(0.0))
+    fill(1, perm[40_000:80_000], np.float32(-0.0))
+    fill(2, rng.permutation(V)[:70_000], np.float32(-0.0))
+    tgt[3][0, 777] = np.nan  # position 0's target row: always read
+    fill(4, rng.permutation(V)[:5_000], np.float32(-np.inf))
+    w = wl.Workload(name="bf16 pattern counts", batch=B, vocab=V, gamma_max=g, gammas=base.gammas,
+                    target=wl.bf16_bits(tgt.reshape(B * (g + 1), V)), draft=wl.bf16_bits(dft.reshape(B * g, V)),
+                    draft_tokens=base.token_pool[0], token_pool=base.token_pool, draft_is_probs=False,
+                    temperature=1.0, top_p=0.9)
+    run_rounds(w, range(3), seed=7, label="top-p alone, bf16 pattern counts")
+    DeviceBatch = _harness()
+    db = DeviceBatch(w, seed=7)
+    db.run()
+    st = db.results()["status"].tolist()
+    assert st[3] != 0 and [s for i, s in enumerate(st) if i != 3] == [0] * (B - 1)
