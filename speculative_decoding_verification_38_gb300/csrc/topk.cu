@@ -1493,6 +1493,61 @@ static __device__ __noinline__ int decide_edge(const StatsParams& p, int64_t r, 
         }
         return 0;
     }
+    if (listed && per <= 4u) {
+        // E. few items a thread: the crossing thread walks its own, highest first
+        if (t == ts) {
+            const uint32_t n = items(ts);
+            const df above = df_add(wa, es);
+            df run = above, prev{0.f, 0.f}, at{0.f, 0.f};
+            uint32_t K = 0xFFFFFFFFu, lo = 0xFFFFFFFFu;
+#pragma unroll 1
+            for (uint32_t j = 0; j < n; ++j) {
+                uint32_t key;
+                const uint32_t c = item(ts, j, key);
+                if (c == 0u) continue;
+                const df pw = df_mul_f(pattern_weight(bf16_of_key(key), m, kd, sm.al.tab), (float)c);
+                if (!df_pos(pw)) continue;
+                const df before = run;
+                run = df_add(run, pw);
+                lo = key;
+                if (K == 0xFFFFFFFFu && !df_gt(target, run)) {
+                    K = key;
+                    prev = before;
+                    at = run;
+                }
+            }
+            int verdict = 0;
+            if (K == 0xFFFFFFFFu) {  // none within the thread (rounding): its lowest pattern with weight
+                K = lo;
+                verdict = all ? 0 : 1;
+            } else if (!all) {
+                // the edge holds for every total within E of the estimate:
+                // the mass at or above K reaches the highest target, the mass
+                // above K stays under the lowest; and K is heavy against the
+                // reference the columns were classified by, so every column
+                // at or above it was counted
+                const df thi = df_mul_f(df_add(tot, df{E, 0.f}), tp);
+                const df tlo = df_mul_f(df_add(tot, df{-E, 0.f}), tp);
+                const float dk = __fsub_rn(bf16_of_key(K), m);
+                const bool heavy = __fmaf_rn(dk, kd.hi, __fmul_rn(dk, kd.lo)) > kWnHeavy;
+                verdict = (heavy && !df_gt(thi, at) && df_gt(tlo, prev)) ? 0 : 1;
+            }
+            if (verdict == 0) {
+                df f = df_add(sm.af[warp], ef);
+#pragma unroll 1
+                for (uint32_t j = 0; j < n; ++j) {
+                    uint32_t key;
+                    const uint32_t c = item(ts, j, key);
+                    if (c != 0u && key >= K) f = df_add(f, two_prod(kept_weight(bf16_of_key(key), false, k2, nmk), (float)c));
+                }
+                p.row_stats[r] = make_float2(m, __fadd_rn(f.hi, f.lo));
+                p.tau[r] = bf16_of_key(K);
+            }
+            sm.verdict = verdict;
+        }
+        __syncthreads();
+        return sm.verdict;
+    }
     if (t == ts) {
         sm.above_s = df_add(wa, es);
         sm.above_f = df_add(sm.af[warp], ef);
