@@ -210,7 +210,7 @@ __device__ __forceinline__ float vec_max(const uint4& q) {
 // Append this lane's values of one vector that are >= thr (when `need`) to
 // the warp's buffer: lanes in order, each lane's values in column order.
 template <int DT>
-__device__ __forceinline__ void warp_append(typename KeyTraits<DT>::Bits* wb, int& cnt, const uint4& q, bool need,
+__device__ __noinline__ void warp_append(typename KeyTraits<DT>::Bits* wb, int& cnt, const uint4& q, bool need,
                                             float thr) {
     using KT = KeyTraits<DT>;
     constexpr int EPV = 16 / KT::kEsz;
@@ -259,7 +259,7 @@ __device__ __forceinline__ void raise_thr(WarpThr& t, uint32_t k) {
 // threshold to the kk-th largest entry and drop again. Returns false when
 // the survivors (ties) still leave fewer than `room` free entries.
 template <int DT>
-__device__ bool warp_make_room(typename KeyTraits<DT>::Bits* wb, int& cnt, uint32_t kk, WarpThr& thr,
+__device__ __noinline__ bool warp_make_room(typename KeyTraits<DT>::Bits* wb, int& cnt, uint32_t kk, WarpThr& thr,
                                uint32_t* shared_key, int room) {
     constexpr int C = kBufBytes / KeyTraits<DT>::kEsz;
     cnt = warp_compact<DT>(wb, cnt, thr.key);
