@@ -236,6 +236,41 @@ def ncu_traffic_per_launch(mode: str = "stats", top_k: int = 0, config: int = 3)
         return None
 
 
+def draft_agreement(w):
+    """The workload's acceptance rates alpha = sum_x min(p(x), q(x)) of each draft
+    position against its target row, both at the sequence's temperature (float64,
+    host side): the mean over positions, and a histogram of the per-sequence means
+    in tenths of [0, 1]. A property of the synthetic inputs, reported beside the
+    timing; nothing here runs on the GPU path."""
+    import numpy as np
+    from speculative_decoding_verification_38_gb300 import workloads as wl
+
+    if w.greedy or w.draft_is_probs or w.rows_draft == 0:
+        return None
+    tro, dro = (np.asarray(w.target_row_off), np.asarray(w.draft_row_off)) if w.target_row_off is not None \
+        else wl.offsets_for(w.gammas)
+    temps = np.broadcast_to(np.asarray(w.temperatures if w.temperatures is not None else w.temperature,
+                                       dtype=np.float64), (w.batch,))
+    per_seq, alphas = [], []
+    for b in range(w.batch):
+        g = int(dro[b + 1] - dro[b])
+        if g == 0:
+            continue
+        t = wl.stored_f32(w.target[int(tro[b]):int(tro[b]) + g]).astype(np.float64) / temps[b]
+        d = wl.stored_f32(w.draft[int(dro[b]):int(dro[b]) + g]).astype(np.float64) / temps[b]
+        pt = np.exp(t - t.max(axis=1, keepdims=True))
+        pt /= pt.sum(axis=1, keepdims=True)
+        qd = np.exp(d - d.max(axis=1, keepdims=True))
+        qd /= qd.sum(axis=1, keepdims=True)
+        a = np.minimum(pt, qd).sum(axis=1)
+        alphas.extend(a.tolist())
+        per_seq.append(float(a.mean()))
+    hist = np.histogram(per_seq, bins=10, range=(0.0, 1.0))[0].tolist()
+    return {"mean": float(np.mean(alphas)), "per_sequence_hist_tenths": hist,
+            "what": "sum_x min(p, q) per draft position at the sequence's temperature; histogram of the "
+                    "per-sequence means over [0, 1] in tenths"}
+
+
 def max_over_ranks(value: float, dist, device) -> float:
     """The largest of every rank's value (each rank gets the result)."""
     import torch
@@ -424,6 +459,11 @@ def run_ours(args):
         out["config"]["adaptive"] = "running acceptance (lambda 0.1) updated in finalize; gamma policy (c = 0.05) each step"
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
         out["cpu_baseline"] = run_cpu_baseline(w, args)
+    if rank == 0 and args.config in (2, 3) and args.top_k <= 0 and not topp_on(args):
+        # the scope table asks for the C3 acceptance histogram and the C2 draft sigma
+        out["config"]["acceptance"] = draft_agreement(w)
+        if args.config == 2:
+            out["config"]["draft_sigma"] = wl.C2_SIGMA
     if rank == 0:
         print(json.dumps(out), flush=True)
     if dist:
