@@ -236,6 +236,40 @@ def ncu_traffic_per_launch(mode: str = "stats", top_k: int = 0, config: int = 3)
         return None
 
 
+def nvtx(name):
+    """An NVTX range around one phase of a bench run (seen by a profiler's
+    timeline; nothing otherwise)."""
+    import contextlib
+
+    import torch
+
+    try:
+        return torch.cuda.nvtx.range(name)
+    except Exception:  # no NVTX in this build: the phase runs unmarked
+        return contextlib.nullcontext()
+
+
+def realised_acceptance(copies, w):
+    """What the last call of each resident copy produced: tokens emitted per
+    sequence and pass (accepted drafts + 1; greedy the same), and the fraction
+    of accept tests passed (a rejection ends a sequence's tests)."""
+    import numpy as np
+
+    acc, tests, emitted, seqs = 0, 0, 0, 0
+    g = np.asarray(w.gammas)
+    for db in copies:
+        r = db.results()
+        ok = r["status"] == 0
+        a = r["accepted"][ok].astype(np.int64)
+        gg = g[ok].astype(np.int64)
+        acc += int(a.sum())
+        tests += int(np.where(a < gg, a + 1, gg).sum())
+        emitted += int((a + 1).sum())
+        seqs += int(ok.sum())
+    return {"tokens_per_pass": emitted / max(seqs, 1), "accept_rate": acc / max(tests, 1),
+            "sequences": seqs, "what": "the last call of each of the two resident copies"}
+
+
 def draft_agreement(w):
     """The workload's acceptance rates alpha = sum_x min(p(x), q(x)) of each draft
     position against its target row, both at the sequence's temperature (float64,
@@ -335,9 +369,10 @@ def run_ours(args):
     if small:
         K = min(K, 5000)  # each step is timed alone, between L2 flushes
     flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") if small else None
-    for i in range(W):
-        step(i, i)
-    torch.cuda.synchronize()
+    with nvtx("warm-up"):
+        for i in range(W):
+            step(i, i)
+        torch.cuda.synchronize()
     if dist:
         dist.barrier()
     clk = ClockSampler(local_rank)
@@ -355,19 +390,20 @@ def run_ours(args):
         if small else []
     torch.cuda.synchronize()
     wall0 = time.time()
-    t_start.record()
-    for i in range(K):
-        if small:  # inputs smaller than L2: evict them, then time this step alone
-            flush.fill_(i & 255)
-            step_ev[i][0].record()
-        if i % HOOK_EVERY == 0:
-            e0, e1 = ev[i // HOOK_EVERY]
-            sv.spec_debug_time_next_stats(e0, e1)  # brackets this step's streaming kernel
-        step(i, W + i)
-        if small:
-            step_ev[i][1].record()
-    t_end.record()
-    torch.cuda.synchronize()
+    with nvtx("timed steps"):
+        t_start.record()
+        for i in range(K):
+            if small:  # inputs smaller than L2: evict them, then time this step alone
+                flush.fill_(i & 255)
+                step_ev[i][0].record()
+            if i % HOOK_EVERY == 0:
+                e0, e1 = ev[i // HOOK_EVERY]
+                sv.spec_debug_time_next_stats(e0, e1)  # brackets this step's streaming kernel
+            step(i, W + i)
+            if small:
+                step_ev[i][1].record()
+        t_end.record()
+        torch.cuda.synchronize()
     wall1 = time.time()
     if dist:
         dist.barrier()
@@ -403,13 +439,15 @@ def run_ours(args):
         a.record()
         b.record()
     torch.cuda.synchronize()
-    for i in range(KERNEL_SAMPLES):
-        if small:
-            flush.fill_(i & 255)
-        sv.spec_debug_time_next_stats(kev[i][0], kev[i][1])
-        step(i, W + K + i)
-    torch.cuda.synchronize()
+    with nvtx("dominant kernel samples"):
+        for i in range(KERNEL_SAMPLES):
+            if small:
+                flush.fill_(i & 255)
+            sv.spec_debug_time_next_stats(kev[i][0], kev[i][1])
+            step(i, W + K + i)
+        torch.cuda.synchronize()
     stats_ms = [a.elapsed_time(b) for a, b in kev]
+    realised = realised_acceptance(copies, w)
     if dist:
         elapsed_ms = max_over_ranks(elapsed_ms, dist, "cuda")
     ms_per_step = elapsed_ms / K
@@ -421,7 +459,8 @@ def run_ours(args):
     graph = time_graph(copies[0], W, flush, K) if small else None
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(copies[0], w, args, sv) if args.e2e_steps > 0 else None
+    with nvtx("end to end"):
+        e2e = run_e2e(copies[0], w, args, sv) if args.e2e_steps > 0 else None
 
     out = {
         "metric": metric_of(args), "value": rounds_per_s, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
@@ -451,6 +490,7 @@ def run_ours(args):
         "clocks": clocks,
         "e2e": e2e,
         "wall_s_timed": wall1 - wall0,
+        "realised": realised,
     }
     if graph is not None:
         out["cuda_graph"] = graph
@@ -458,7 +498,8 @@ def run_ours(args):
         out["adaptive_gamma"] = time_policy(sv, w.gamma_max)
         out["config"]["adaptive"] = "running acceptance (lambda 0.1) updated in finalize; gamma policy (c = 0.05) each step"
     if rank == 0 and world == 1 and args.cpu_seconds > 0:
-        out["cpu_baseline"] = run_cpu_baseline(w, args)
+        with nvtx("cpu baseline"):
+            out["cpu_baseline"] = run_cpu_baseline(w, args)
     if rank == 0 and args.config in (2, 3) and args.top_k <= 0 and not topp_on(args):
         # the scope table asks for the C3 acceptance histogram and the C2 draft sigma
         out["config"]["acceptance"] = draft_agreement(w)

@@ -434,6 +434,20 @@ SPEC_API spec_status_t spec_debug_time_next_stats(void* start_event, void* stop_
  * SPEC_ERR_INVALID_ARG. */
 SPEC_API spec_status_t spec_debug_set_path(int32_t path);
 
+/* Test hook for failure detection without a fault: one warp waits on the
+ * device word *flag with the bounded wait the fused verify kernel uses for
+ * its hand-offs between CTAs (poll with a growing sleep; give up after
+ * limit_ns of the GPU's global timer or 2^26 polls), then writes out[0] =
+ * the value it saw (0 if it gave up) and out[1] = 1 if it gave up, else 0.
+ * flag and out: device pointers, 4-byte aligned (out holds two words).
+ * limit_ns at most 10^10 (ten seconds). Asynchronous on `stream`; nothing
+ * else is touched, and the context stays usable whichever way the wait ends.
+ * Errors: SPEC_ERR_INVALID_ARG (null, misaligned or too long a limit),
+ * SPEC_ERR_CUDA (the launch failed). No counterpart on the pages: it tests
+ * the library's own bounded waits. */
+SPEC_API spec_status_t spec_debug_wait_probe(const uint32_t* flag, uint64_t limit_ns, uint32_t* out,
+                                             spec_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

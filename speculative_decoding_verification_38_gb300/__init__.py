@@ -166,6 +166,8 @@ def lib():
             L.spec_debug_time_next_stats.argtypes = [vp, vp]
             L.spec_debug_set_path.restype = ctypes.c_int
             L.spec_debug_set_path.argtypes = [ctypes.c_int32]
+            L.spec_debug_wait_probe.restype = ctypes.c_int
+            L.spec_debug_wait_probe.argtypes = [ctypes.c_void_p, ctypes.c_uint64, ctypes.c_void_p, ctypes.c_void_p]
             if L.spec_abi_version() != SPEC_ABI_VERSION:
                 raise ImportError("libspecverify.so ABI version mismatch")
             _lib = L
@@ -451,6 +453,13 @@ def spec_debug_set_path(path: int) -> int:
     (the streaming, finalize, tile and draw kernels) or PATH_FUSED (the one
     cooperative kernel, wherever it applies)."""
     return lib().spec_debug_set_path(int(path))
+
+
+def spec_debug_wait_probe(flag, limit_ns: int, out, stream=None) -> int:
+    """One warp's bounded wait on the device word flag[0] (the fused kernel's
+    hand-off wait): out[0] = the value seen (0 if it gave up), out[1] = 1 if
+    it gave up. flag and out: uint32 (or int32) CUDA tensors."""
+    return lib().spec_debug_wait_probe(flag.data_ptr(), int(limit_ns), out.data_ptr(), _stream(stream))
 
 
 def spec_debug_light_exp2(x, y, stream=None) -> int:

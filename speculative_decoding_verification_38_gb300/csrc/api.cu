@@ -547,6 +547,14 @@ SPEC_API spec_status_t spec_debug_light_exp2(const float* x, float* y, int64_t n
     return SPEC_OK;
 }
 
+SPEC_API spec_status_t spec_debug_wait_probe(const uint32_t* flag, uint64_t limit_ns, uint32_t* out,
+                                             spec_stream_t stream) {
+    if (!flag || !out || !aligned(flag, 4) || !aligned(out, 4)) return SPEC_ERR_INVALID_ARG;
+    if (limit_ns > 10000000000ull) return SPEC_ERR_INVALID_ARG;  // at most ten seconds
+    if (launch_wait_probe(flag, limit_ns, out, (cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
+    return SPEC_OK;
+}
+
 SPEC_API spec_status_t spec_debug_set_path(int32_t path) {
     if (path < 0 || path > 2) return SPEC_ERR_INVALID_ARG;
     g_path.store(path);

@@ -187,6 +187,9 @@ constexpr int kVerifyMaxTiles = 256;      // fused kernel: V <= 256 * kTile
 // leave the caller to use the separate kernels.
 cudaError_t launch_verify(const VerifyParams& p, cudaStream_t s);
 int verify_resident_ctas(int device);  // CTAs of the fused kernel one device holds at once (0: unknown)
+// Test hook: one warp's bounded wait on *flag (the verify kernel's wait),
+// recording the value seen (out[0]) and whether the wait gave up (out[1]).
+cudaError_t launch_wait_probe(const uint32_t* flag, uint64_t limit_ns, uint32_t* out, cudaStream_t s);
 
 // Work split and workspace layout for a given problem. grid_cap bounds the
 // number of streaming CTAs (the launch uses the device's resident capacity).

@@ -1034,7 +1034,23 @@ cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
     return cudaLaunchKernelEx(&cfg, verify_kernel<TDT, DDT>, p);
 }
 
+// Test hook: one warp waits on *flag through the same bounded wait the
+// verify kernel's hand-offs use and records what it saw (out[0]: the flag's
+// value, 0 if the wait gave up; out[1]: 1 if it gave up).
+__global__ void wait_probe_kernel(const uint32_t* flag, uint64_t limit_ns, uint32_t* out) {
+    const uint32_t v = warp_wait_nonzero(flag, limit_ns);
+    if (threadIdx.x == 0) {
+        out[0] = v;
+        out[1] = v ? 0u : 1u;
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_wait_probe(const uint32_t* flag, uint64_t limit_ns, uint32_t* out, cudaStream_t s) {
+    wait_probe_kernel<<<1, 32, 0, s>>>(flag, limit_ns, out);
+    return cudaGetLastError();
+}
 
 int verify_resident_ctas(int device) {
     int sms = 0, per = 0;
