@@ -212,3 +212,11 @@ def test_topp_alone_bf16_pattern_counts(sv):
     db.run()
     st = db.results()["status"].tolist()
     assert st[3] != 0 and [s for i, s in enumerate(st) if i != 3] == [0] * (B - 1)
+
+
+def test_topp_alone_config3_high_p(sv):
+    """Top-p 0.99 without top-k on the benchmarked workload: most rows' edges
+    lie among columns too light to be counted on the first pass, so they are
+    counted again with every column (the exact path), at full size."""
+    w = wl.config3(top_k=0, top_p=0.99)
+    run_rounds(w, range(2), seed=1, label="C3 top-p 0.99 alone")
