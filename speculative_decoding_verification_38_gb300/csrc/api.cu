@@ -578,10 +578,9 @@ SPEC_API spec_status_t spec_verify_sample_static(const spec_verify_args_t* a, sp
     spec_verify_args_t b = *a;
     b.workspace = ws;
     b.workspace_bytes = kStaticScratchBytes;
-    StatsParams p;
-    Layout L;
-    int dev = 0;
-    st = prepare(&b, 0, p, L, dev);
+    // the call's own checks before the header is touched (spec_verify_sample
+    // prepares the launch itself)
+    st = check_call(&b, 0);
     if (st) return st;
     // arrival counters and error word start at zero on every call
     if (cudaMemsetAsync(ws, 0, kHeaderBytes, (cudaStream_t)stream) != cudaSuccess) return SPEC_ERR_CUDA;
