@@ -1146,9 +1146,9 @@ __global__ void __launch_bounds__(kNuThreads) nucleus_kernel(StatsParams p) {
 // ------------------------------------------ top-p without top-k, bf16 logits
 // The nucleus of a whole bf16 logits row (top-p with top-k off), one CTA per
 // SM taking rows in turn. The rows reach shared memory through a ring of
-// bulk copies issued by one thread, a few chunks ahead of the CTA, across the
-// CTA's rows (the next row's first chunks arrive while the CTA decides the
-// current one).
+// two 32 KB bulk-copy stages filled by one thread a stage ahead of the CTA,
+// across the CTA's rows (the next row's first chunk arrives while the CTA
+// decides the current one).
 //  1. One pass over the row, chunk by chunk. Each chunk first raises the
 //     running maximum (its packed bf16 maxima, over the CTA). A bf16 logit's
 //     weight depends only on its 16-bit pattern, so the heavy columns
@@ -1162,8 +1162,9 @@ __global__ void __launch_bounds__(kNuThreads) nucleus_kernel(StatsParams p) {
 //     summed from the highest pattern down (the patterns present spread over
 //     the threads, then a block scan); the total is those masses plus the
 //     light sum; the nucleus edge is the highest pattern whose mass at or
-//     above it reaches top_p of the total, found by one warp walking the
-//     patterns of the thread where the running mass crosses the target.
+//     above it reaches top_p of the total, found by the thread where the
+//     running mass crosses the target walking its patterns (with its warp
+//     when it holds many).
 //  3. The edge stands if it holds for every total within the light sum's
 //     bound and its pattern was heavy against the final maximum (so every
 //     column at or above it was counted). If not, or if the edge lies among
@@ -1188,7 +1189,7 @@ constexpr float kWnEx2Err = 2.4e-7f;
 constexpr float kWnU = 5.9604645e-8f;  // 2^-24
 static_assert(kWnThreads == kAlThreads, "the narrowing search runs with the same CTA");
 static_assert(kWnHistBytes >= kAlSmemBytes, "the narrowing search reuses the counters' memory");
-static_assert(kWnWordsPerThread == 32, "one word per lane in the crossing walk");
+static_assert(kWnWordsPerThread == 32, "each warp's counters are 8 x 32 vectors of 8 patterns");
 static_assert(kWnChunk == 32u * kWnThreads, "two vectors per thread per chunk");
 
 struct WholeSmem {
