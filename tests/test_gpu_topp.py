@@ -220,3 +220,18 @@ def test_topp_alone_config3_high_p(sv):
     counted again with every column (the exact path), at full size."""
     w = wl.config3(top_k=0, top_p=0.99)
     run_rounds(w, range(2), seed=1, label="C3 top-p 0.99 alone")
+
+
+@pytest.mark.parametrize("V", [1, 5, 7, 600_011])
+def test_topp_alone_bf16_edge_sizes(sv, V):
+    """The whole-row nucleus kernel at its edges: rows shorter than one
+    16-byte vector (head and tail columns only), and rows of 600,011 columns
+    (19 ring stages, unaligned starts)."""
+    rng = np.random.default_rng(950 + V)
+    B = 6 if V < 1000 else 2
+    ps = rng.uniform(0.3, 0.99, size=B).astype(np.float32)
+    w = wl.sampling_workload(f"topp alone edge V{V}", config=403, batch=B, vocab=V,
+                             gammas=rng.integers(0, 4, size=B), profile="zipf", dtype="bf16",
+                             sigma=rng.uniform(0.2, 1.5, B), temps=rng.uniform(0.6, 1.4, B), ragged=True,
+                             pool=2, dataset=V, top_p=ps)
+    run_rounds(w, range(3), seed=11, label=f"top-p alone bf16 V={V}")
