@@ -106,7 +106,7 @@ struct DrawSmem {
     Exp2Table tab;
     int32_t q[kWarps][kQCap];  // lane_tile_sum's queues (tiles summed again)
     float w_hi[kMaxTiles], w_lo[kMaxTiles];  // tile sums
-    float red_hi[kWarps], red_lo[kWarps];
+    float red_hi[kWarps], red_lo[kWarps], red2_hi[kWarps], red2_lo[kWarps];
     int32_t dirty[kMaxTiles];
     int32_t ndirty, sel, col, last;
     float start_hi, start_lo;
@@ -124,6 +124,26 @@ __device__ __forceinline__ df block_sum_df(df x, DrawSmem& sm) {
     df t{0.f, 0.f};
     for (int i = 0; i < kWarps; ++i) t = df_add(t, df{sm.red_hi[i], sm.red_lo[i]});
     return t;
+}
+
+// Two block sums at once (one pair of barriers).
+__device__ __forceinline__ void block_sum_df2(df& x, df& y, DrawSmem& sm) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    x = warp_sum_df(x);
+    y = warp_sum_df(y);
+    __syncthreads();  // red[] is free
+    if (lane == 0) {
+        sm.red_hi[warp] = x.hi;
+        sm.red_lo[warp] = x.lo;
+        sm.red2_hi[warp] = y.hi;
+        sm.red2_lo[warp] = y.lo;
+    }
+    __syncthreads();
+    x = y = df{0.f, 0.f};
+    for (int i = 0; i < kWarps; ++i) {
+        x = df_add(x, df{sm.red_hi[i], sm.red_lo[i]});
+        y = df_add(y, df{sm.red2_hi[i], sm.red2_lo[i]});
+    }
 }
 
 // Exclusive block-wide prefix of one value per thread (thread order).
@@ -163,16 +183,32 @@ __global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
     const int nt = p.ntile;
     const int K = (nt + kSampThreads - 1) / kSampThreads;
     const int t0 = threadIdx.x * K, t1 = min(nt, t0 + K);
-    // the exact normalisers
+    // the exact normalisers; a thread with one tile (V up to 256 tiles) keeps
+    // its whole record for the tile sums below
     df st{0.f, 0.f}, sd{0.f, 0.f};
+    const bool one = K == 1;
+    float4 r_ab = make_float4(0.f, 0.f, 0.f, 0.f), r_ss = r_ab, r_uu = r_ab;
+    int32_t r_nu = 0;
+    if (one) {
+        if (t0 < t1) {
+            const float4* r = reinterpret_cast<const float4*>(recs + t0);
+            r_ab = __ldcg(r);
+            r_ss = __ldcg(r + 1);
+            r_uu = __ldcg(r + 2);
+            r_nu = __ldcg(reinterpret_cast<const int32_t*>(r + 3));
+            st = df{r_ss.x, r_ss.y};
+            sd = df{r_ss.z, r_ss.w};
+        }
+    } else {
 #pragma unroll 1
-    for (int ti = t0; ti < t1; ++ti) {
-        const float4 ss = __ldcg(reinterpret_cast<const float4*>(recs + ti) + 1);
-        st = df_add(st, df{ss.x, ss.y});
-        sd = df_add(sd, df{ss.z, ss.w});
+        for (int ti = t0; ti < t1; ++ti) {
+            const float4 ss = __ldcg(reinterpret_cast<const float4*>(recs + ti) + 1);
+            st = df_add(st, df{ss.x, ss.y});
+            sd = df_add(sd, df{ss.z, ss.w});
+        }
     }
-    const df St = block_sum_df(st, sm);
-    const df Sd = block_sum_df(sd, sm);
+    block_sum_df2(st, sd, sm);
+    const df St = st, Sd = sd;
     int mode = t.mode;
     const bool resid = mode == kTaskResidual;
     const df It = resid ? df_recip(St) : df{1.f, 0.f}, Id = resid ? df_recip(Sd) : df{1.f, 0.f};
@@ -184,18 +220,18 @@ __global__ void __launch_bounds__(kSampThreads) draw_kernel(SampleParams p) {
         const float4* r = reinterpret_cast<const float4*>(recs + ti);
         df v;
         if (!resid) {
-            const float4 ss = __ldcg(r + 1);
+            const float4 ss = one ? r_ss : __ldcg(r + 1);
             v = df{ss.x, ss.y};
         } else {
-            const int32_t nu = __ldcg(reinterpret_cast<const int32_t*>(r + 3));
+            const int32_t nu = one ? r_nu : __ldcg(reinterpret_cast<const int32_t*>(r + 3));
             if (nu > 1) {  // more than one open column: summed again below
                 sm.dirty[atomicAdd(&sm.ndirty, 1)] = ti;
                 continue;
             }
-            const float4 ab = __ldcg(r);
+            const float4 ab = one ? r_ab : __ldcg(r);
             v = resid_of_sums(df{ab.x, ab.y}, df{ab.z, ab.w}, It, Id);
             if (nu == 1) {
-                const float4 uu = __ldcg(r + 2);
+                const float4 uu = one ? r_uu : __ldcg(r + 2);
                 v = df_add(v, resid_of_sums(df{uu.x, uu.y}, df{uu.z, uu.w}, It, Id));
             }
         }
