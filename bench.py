@@ -460,7 +460,7 @@ def run_ours(args):
 
     # end to end through the public API with host buffers
     with nvtx("end to end"):
-        e2e = run_e2e(copies[0], w, args, sv) if args.e2e_steps > 0 else None
+        e2e = run_e2e(copies, w, args, sv) if args.e2e_steps > 0 else None
 
     out = {
         "metric": metric_of(args), "value": rounds_per_s, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": W,
@@ -740,7 +740,9 @@ def run_tree(args):
     per_launch = read / K
     peak, peak_kind = measured_hbm_peak()
     achieved = per_launch / (ms / K / 1e3) / 1e9
-    # end to end: every step copies the trees in from pinned host memory and reads the outputs back
+    # end to end: every step copies the trees in from pinned host memory and reads the outputs back;
+    # steps alternate between two of the resident row sets, so a step's row copies (over several copy
+    # streams) run while the previous step's walk reads the other set
     host_t, host_d = tgts[0].cpu().pin_memory(), dfts[0].cpu().pin_memory()
     host_meta = [x.cpu().pin_memory() for x in (dt.node_off, dt.parent, dt.tokens)]
     out_h = [torch.empty_like(x, device="cpu").pin_memory() for x in
@@ -748,15 +750,36 @@ def run_tree(args):
     h2d = host_t.numel() * 2 + host_d.numel() * 2 + sum(x.numel() * x.element_size() for x in host_meta)
     d2h = sum(x.numel() * 4 for x in out_h)
     n_e2e = max(3, min(args.e2e_steps, 30))
+    cur = torch.cuda.current_stream()
+    copy_streams = [torch.cuda.Stream() for _ in range(E2E_COPY_STREAMS)]
+    sets = []
+    for c in range(2):
+        pieces = []
+        for d, h in ((tgts[c], host_t), (dfts[c], host_d)):
+            dv, hv = d.view(-1), h.view(-1)
+            for o in range(0, dv.numel(), 16 << 20):  # 32 MB of bf16 per chunk
+                pieces.append((dv[o:o + (16 << 20)], hv[o:o + (16 << 20)]))
+        free = torch.cuda.Event()
+        free.record(cur)
+        sets.append((arg_sets[c], pieces, free))
 
     def one(i):
-        tgts[0].copy_(host_t, non_blocking=True)
-        dfts[0].copy_(host_d, non_blocking=True)
+        a, pieces, free = sets[i % 2]
+        for j, (d, h) in enumerate(pieces):
+            cs = copy_streams[j % len(copy_streams)]
+            if j < len(copy_streams):
+                cs.wait_event(free)
+            with torch.cuda.stream(cs):
+                d.copy_(h, non_blocking=True)
+        for cs in copy_streams:
+            e = torch.cuda.Event()
+            e.record(cs)
+            cur.wait_event(e)
         for d, h in zip((dt.node_off, dt.parent, dt.tokens), host_meta):
             d.copy_(h, non_blocking=True)
-        a = arg_sets[0]
         a.round = i
         sv.check(sv.spec_tree_verify(a, False), "tree verify")
+        free.record(cur)
         for h, d in zip(out_h, (dt.out_tokens, dt.out_path, dt.out_accepted, dt.status)):
             h.copy_(d, non_blocking=True)
 
@@ -787,7 +810,10 @@ def run_tree(args):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
         "clocks": ClockSampler.summarize(rows),
         "e2e": {"value": n_e2e / (e2e_ms / 1e3), "unit": "rounds/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h), "steps": n_e2e, "ms_per_step": e2e_ms / n_e2e,
+                "h2d_gbs": h2d / (e2e_ms / n_e2e / 1e3) / 1e9,
+                "copies": f"{len(sets[0][1])} chunks of at most 32 MB over {len(copy_streams)} copy streams per step; "
+                          "two device row sets, so a step's copies overlap the previous step's walk"},
     }
     if args.cpu_seconds > 0:
         import oracle
@@ -803,54 +829,60 @@ def run_tree(args):
     print(json.dumps(out), flush=True)
 
 
-def run_e2e(db, w, args, sv):
+def run_e2e(copies, w, args, sv):
     """Same metric through the C ABI with inputs in pinned host memory: every
     step copies that step's inputs host -> device, verifies, and reads the
-    outputs back device -> host, all inside the timed region."""
+    outputs back device -> host, all inside the timed region. Steps alternate
+    between the two device-resident input sets, so step i + 1's copies run
+    while step i verifies (a serving loop's double buffering)."""
     import torch
 
-    ins = [(d, d.cpu().pin_memory()) for d in (db.target, db.draft, db.kv_in) if d is not None]
-    host_tok = [t.cpu().pin_memory() for t in db.token_pool]
-    outs = [(d, torch.empty_like(d, device="cpu").pin_memory())
-            for d in (db.out_tokens, db.out_accepted, db.kv_out, db.status) if d is not None]
-    h2d = sum(h.numel() * h.element_size() for _, h in ins) + host_tok[0].numel() * 4
-    d2h = sum(h.numel() * h.element_size() for _, h in outs)
+    host_in = [d.cpu().pin_memory() for d in (copies[0].target, copies[0].draft, copies[0].kv_in) if d is not None]
+    host_tok = [t.cpu().pin_memory() for t in copies[0].token_pool]
+    h2d = sum(h.numel() * h.element_size() for h in host_in) + host_tok[0].numel() * 4
     n = max(3, args.e2e_steps)
     # The input rows go over in chunks of about 32 MB spread over several
-    # copy streams, so that more than one copy engine moves them; each
-    # step's copies start after the previous step's verify (which reads the
-    # same device buffers) and the verify waits for all of them.
+    # copy streams, so that more than one copy engine moves them. The copies
+    # into a set start once the verify that last read it is done; the verify
+    # waits for all of its own step's copies.
     cur = torch.cuda.current_stream()
     copy_streams = [torch.cuda.Stream() for _ in range(E2E_COPY_STREAMS)]
-    pieces = []
-    for d, h in ins:
-        dv, hv = d.view(-1), h.view(-1)
-        step = max(1, (32 << 20) // dv.element_size())
-        for o in range(0, dv.numel(), step):
-            pieces.append((dv[o:o + step], hv[o:o + step]))
+    sets = []
+    for db in copies:
+        dev_in = [d for d in (db.target, db.draft, db.kv_in) if d is not None]
+        pieces = []
+        for d, h in zip(dev_in, host_in):
+            dv, hv = d.view(-1), h.view(-1)
+            step = max(1, (32 << 20) // dv.element_size())
+            for o in range(0, dv.numel(), step):
+                pieces.append((dv[o:o + step], hv[o:o + step]))
+        outs = [(d, torch.empty_like(d, device="cpu").pin_memory())
+                for d in (db.out_tokens, db.out_accepted, db.kv_out, db.status) if d is not None]
+        free = torch.cuda.Event()
+        free.record(cur)
+        sets.append({"db": db, "pieces": pieces, "outs": outs, "free": free})
+    d2h = sum(h.numel() * h.element_size() for _, h in sets[0]["outs"])
 
     def one(i):
-        ready = torch.cuda.Event()
-        ready.record(cur)
-        done = []
-        for j, (d, h) in enumerate(pieces):
+        st = sets[i % len(sets)]
+        db = st["db"]
+        for j, (d, h) in enumerate(st["pieces"]):
             cs = copy_streams[j % len(copy_streams)]
             if j < len(copy_streams):
-                cs.wait_event(ready)
+                cs.wait_event(st["free"])
             with torch.cuda.stream(cs):
                 d.copy_(h, non_blocking=True)
         for cs in copy_streams:
             e = torch.cuda.Event()
             e.record(cs)
-            done.append(e)
+            cur.wait_event(e)
         tok = db.token_pool[i % len(db.token_pool)]
         tok.copy_(host_tok[i % len(host_tok)], non_blocking=True)
-        for e in done:
-            cur.wait_event(e)
-        st = db.call(rnd=i, pool_index=i)
-        if st != 0:
-            raise sv.SpecError(st, "verify")
-        for d, h in outs:
+        rc = db.call(rnd=i, pool_index=i)
+        if rc != 0:
+            raise sv.SpecError(rc, "verify")
+        st["free"].record(cur)
+        for d, h in st["outs"]:
             h.copy_(d, non_blocking=True)
 
     for i in range(3):
@@ -865,7 +897,8 @@ def run_e2e(db, w, args, sv):
     ms = a.elapsed_time(b)
     return {"value": n / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
             "steps": n, "ms_per_step": ms / n, "h2d_gbs": h2d / (ms / n / 1e3) / 1e9,
-            "copies": f"{len(pieces)} chunks of at most 32 MB over {len(copy_streams)} copy streams per step"}
+            "copies": f"{len(sets[0]['pieces'])} chunks of at most 32 MB over {len(copy_streams)} copy streams per "
+                      f"step; two device input sets, so a step's copies overlap the previous step's verify"}
 
 
 # ---------------------------------------------------------------- CPU / oracle
